@@ -1,0 +1,168 @@
+"""fp64 CPU oracle for window + landmark sparse attention (test infrastructure).
+
+This package is the correctness authority the CUDA library is checked
+against.  It is TEST INFRASTRUCTURE: only the tests, ``__graft_entry__.smoke``
+and the benchmark's CPU-baseline leg may import it.  It shares no code with
+the CUDA path and never imports it.
+
+The arithmetic lives in ``msa_oracle.c`` (plain C, fp64, OpenMP over rows and
+heads); this module compiles it with gcc on first use and marshals numpy
+arrays into it.  The definition it follows, and the reading of the pages it
+takes, is stated at the top of ``msa_oracle.c``.
+
+Inputs are numpy arrays: ``float32``, or ``uint16`` holding bf16 bit patterns
+(``dtype="bf16"``).  Outputs are float64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "msa_oracle.c")
+_LIB = os.path.join(_HERE, "libmsa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16 = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into ``libmsa_oracle.so`` (gcc, fp64, OpenMP)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        vp = ctypes.c_void_p
+        lib.oracle_landmark_pool.argtypes = [vp, i32, i64, i32, i32, i32, vp]
+        lib.oracle_landmark_pool.restype = i32
+        lib.oracle_attn_rows.argtypes = [vp, vp, i64, vp, vp, i64, i64, i32,
+                                         i32, i32, i32, i64, vp, vp, i32, i64,
+                                         dbl, vp, vp]
+        lib.oracle_attn_rows.restype = i32
+        lib.oracle_lse_merge.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp]
+        lib.oracle_lse_merge.restype = i32
+        lib.oracle_set_threads.argtypes = [i32]
+        lib.oracle_get_threads.restype = i32
+        _lib = lib
+        return lib
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"oracle inputs must be float32 or uint16 (bf16 bits), got {a.dtype}")
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def set_threads(n: int) -> None:
+    _load().oracle_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(_load().oracle_get_threads())
+
+
+def landmark_pool(x: np.ndarray, n_landmarks: int) -> np.ndarray:
+    """Block means of x [n, H, d] over G = n_landmarks blocks -> [G, H, d] fp64."""
+    x = np.ascontiguousarray(x)
+    n, H, d = x.shape
+    out = np.empty((n_landmarks, H, d), dtype=np.float64)
+    rc = _load().oracle_landmark_pool(_ptr(x), _dtype_code(x), n, H, d,
+                                      n_landmarks, _ptr(out))
+    if rc != 0:
+        raise ValueError("landmark_pool: n must be a positive multiple of G")
+    return out
+
+
+def attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int,
+         n_landmarks: int, scale: float, rows=None, q_start: int = 0,
+         kv_start: int = 0, n_total: int | None = None):
+    """Window + landmark attention in fp64.
+
+    q: [n_q, Hq, d] query rows at global positions q_start + index; k, v:
+    [n_kv, Hkv, d] at global positions kv_start + index.  ``rows`` selects a
+    subset of q's rows (indices into q).  Landmarks (G = n_landmarks > 0)
+    are the block means of k and v over n_total = len(k) tokens, which
+    requires kv_start == 0.  Returns (O [n_rows, Hq, d], lse [Hq, n_rows]).
+    """
+    q = np.ascontiguousarray(q)
+    k = np.ascontiguousarray(k)
+    v = np.ascontiguousarray(v)
+    dt = _dtype_code(q)
+    if _dtype_code(k) != dt or _dtype_code(v) != dt:
+        raise TypeError("q, k, v must share one dtype")
+    n_q, Hq, d = q.shape
+    n_kv, Hkv, _ = k.shape
+    if rows is None:
+        rows = np.arange(n_q, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    qg = np.ascontiguousarray(q[rows]) if len(rows) != n_q or not np.array_equal(rows, np.arange(n_q)) else q
+    pos = np.ascontiguousarray(rows + int(q_start), dtype=np.int64)
+    G = int(n_landmarks)
+    if G > 0:
+        if kv_start != 0:
+            raise ValueError("landmarks need the whole sequence (kv_start == 0)")
+        k_lm = landmark_pool(k, G)
+        v_lm = landmark_pool(v, G)
+        B = n_kv // G
+        lm_k, lm_v = _ptr(k_lm), _ptr(v_lm)
+    else:
+        B = 1
+        lm_k = lm_v = None
+    out = np.empty((len(rows), Hq, d), dtype=np.float64)
+    lse = np.empty((Hq, len(rows)), dtype=np.float64)
+    rc = _load().oracle_attn_rows(_ptr(qg), _ptr(pos), len(rows), _ptr(k),
+                                  _ptr(v), n_kv, int(kv_start), dt, Hq, Hkv, d,
+                                  int(window), lm_k, lm_v, G, B, float(scale),
+                                  _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("attn: inconsistent arguments")
+    return out, lse
+
+
+def lse_merge(o_parts: np.ndarray, lse_parts: np.ndarray):
+    """Merge P partials: o_parts [P, n, Hq, d], lse_parts [P, Hq, n] (fp64)."""
+    o_parts = np.ascontiguousarray(o_parts, dtype=np.float64)
+    lse_parts = np.ascontiguousarray(lse_parts, dtype=np.float64)
+    P, n, Hq, d = o_parts.shape
+    out = np.empty((n, Hq, d), dtype=np.float64)
+    lse = np.empty((Hq, n), dtype=np.float64)
+    rc = _load().oracle_lse_merge(_ptr(o_parts), _ptr(lse_parts), P, n, Hq, d,
+                                  _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("lse_merge: bad shapes")
+    return out, lse
+
+
+def attended_count(pos: int, window: int, n_landmarks: int, block: int,
+                   kv_start: int = 0, n_kv: int | None = None) -> int:
+    """Size of row pos's attended set, counted from the set definitions."""
+    lo = max(pos - window + 1, kv_start)
+    hi = pos if n_kv is None else min(pos, kv_start + n_kv - 1)
+    n_win = max(0, hi - lo + 1)
+    n_lm = sum(1 for l in range(n_landmarks) if (l + 1) * block <= pos - window + 1)
+    return n_win + n_lm

@@ -1,0 +1,254 @@
+/*
+ * Plain fp64 CPU oracle for window + landmark sparse attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the correctness authority that the
+ * CUDA library is checked against.  It shares no code, header, table or
+ * helper with the CUDA path, and nothing in the product path may load it:
+ * only the tests, the smoke check and the benchmark's CPU-baseline leg do.
+ *
+ * What it computes (the method of "Scaling GPU Cluster for Million Token
+ * Context", section "Why Sparse Attention Changes the Game" and "What is
+ * Flash-MSA Sparse Attention in GPU Clusters?": a local window of w tokens
+ * plus a set of landmark tokens that summarise distant context, one fused
+ * pass; and the online-softmax partial/merge step of "Training at 1M+ Token
+ * Context: Ring Attention, YaRN, NTK-Aware Scaling", Ring Attention
+ * paragraph).  The pages leave the exact definition open; the reading taken
+ * is:
+ *   - row i (global position) attends keys j with i-w < j <= i (causal
+ *     window of w keys including itself);
+ *   - landmark l is the mean of K (and of V) over the contiguous block of
+ *     B = n/G tokens [lB, (l+1)B), and row i attends landmark l only when
+ *     that block lies wholly before its window: (l+1)B <= i-w+1;
+ *   - one softmax over the union of both sets, scores scale*<q,k>, no extra
+ *     bias for landmarks; query head h reads KV head h / (Hq/Hkv);
+ *   - outputs: O[i,h,:] and lse[h,i] = natural log of the softmax
+ *     denominator (max-shifted), i.e. m + ln(sum exp(s-m)).
+ *   - a "partial" restricts the window keys to one contiguous KV chunk and
+ *     uses no landmarks; a row with no key gets lse = -inf and O = 0;
+ *   - the merge of partials is lse = ln sum_p exp(lse_p) and
+ *     O = sum_p exp(lse_p - lse) O_p over the parts with finite lse_p.
+ *
+ * Every score, exponential and sum is computed in double precision, two
+ * passes per row (maximum first, then the sums).  Inputs are read in the
+ * precision they are stored in (fp32, or bf16 bit patterns), which every
+ * double represents exactly.
+ *
+ * Pins (see the tests): dense brute force on tiny inputs, reduction to exact
+ * causal attention when w >= n and G = 0, merge-of-chunks equals single pass,
+ * convexity of every output row, and closed forms (K = 0 gives uniform
+ * weights and lse = ln |attended set|; V = c gives O = c; K = position gives
+ * exact block means).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+
+/* Element idx of a buffer stored as fp32 or as bf16 bit patterns. */
+static double oracle_load(const void *base, int64_t idx, int dtype) {
+    if (dtype == ORACLE_F32) return (double)((const float *)base)[idx];
+    uint16_t h = ((const uint16_t *)base)[idx];
+    uint32_t w = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int oracle_get_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Landmark pooling: out[l][h][c] = (1/B) * sum_{j=lB}^{(l+1)B-1} x[j][h][c],
+ * B = n / G.  x is [n][H][d] (fp32 or bf16), out is [G][H][d] fp64.
+ * Returns 0, or -1 when G does not divide n.
+ */
+int oracle_landmark_pool(const void *x, int dtype, int64_t n, int H, int d,
+                         int G, double *out) {
+    if (G <= 0 || n <= 0 || n % G != 0) return -1;
+    int64_t B = n / G;
+    int64_t row = (int64_t)H * d;
+#pragma omp parallel for schedule(static)
+    for (int64_t l = 0; l < G; ++l) {
+        for (int64_t e = 0; e < row; ++e) {
+            double s = 0.0;
+            for (int64_t j = l * B; j < (l + 1) * B; ++j)
+                s += oracle_load(x, j * row + e, dtype);
+            out[l * row + e] = s / (double)B;
+        }
+    }
+    return 0;
+}
+
+/* Number of landmarks whose whole block lies before row pos's window. */
+static int64_t oracle_visible_landmarks(int64_t pos, int64_t window,
+                                        int64_t B, int G) {
+    int64_t count = 0;
+    for (int64_t l = 0; l < G; ++l) {
+        if ((l + 1) * B <= pos - window + 1) count = l + 1;
+        else break;
+    }
+    return count;
+}
+
+/*
+ * Attention rows.
+ *   q      [n_rows][Hq][d]   the query rows to evaluate (gathered)
+ *   pos    [n_rows]          global position of each of those rows
+ *   k, v   [n_kv][Hkv][d]    keys/values of global positions kv_start..
+ *   k_lm, v_lm [G][Hkv][d]   fp64 landmarks (NULL when G == 0); landmark
+ *                            block size B
+ *   out    [n_rows][Hq][d]   fp64
+ *   lse    [Hq][n_rows]      fp64, natural log; -inf for an empty set
+ * Returns 0, or -1 on inconsistent arguments.
+ */
+int oracle_attn_rows(const void *q, const int64_t *pos, int64_t n_rows,
+                     const void *k, const void *v, int64_t n_kv,
+                     int64_t kv_start, int dtype, int Hq, int Hkv, int d,
+                     int64_t window, const double *k_lm, const double *v_lm,
+                     int G, int64_t B, double scale, double *out,
+                     double *lse) {
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || window < 1)
+        return -1;
+    if (G < 0 || (G > 0 && (k_lm == NULL || v_lm == NULL || B < 1)))
+        return -1;
+    const int group = Hq / Hkv;
+#pragma omp parallel
+    {
+        double *s_win = NULL, *s_lm = NULL;
+        int64_t cap_win = 0;
+        s_lm = (double *)malloc(sizeof(double) * (size_t)(G > 0 ? G : 1));
+#pragma omp for collapse(2) schedule(dynamic, 4)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            for (int h = 0; h < Hq; ++h) {
+                const int64_t i = pos[r];
+                const int c = h / group;
+                /* Window keys: i-w < j <= i, intersected with the chunk. */
+                int64_t j_lo = i - window + 1;
+                if (j_lo < kv_start) j_lo = kv_start;
+                int64_t j_hi = i;
+                if (j_hi > kv_start + n_kv - 1) j_hi = kv_start + n_kv - 1;
+                int64_t n_win = j_hi >= j_lo ? j_hi - j_lo + 1 : 0;
+                int64_t n_lm = G > 0 ? oracle_visible_landmarks(i, window, B, G) : 0;
+                if (n_win > cap_win) {
+                    free(s_win);
+                    cap_win = n_win;
+                    s_win = (double *)malloc(sizeof(double) * (size_t)cap_win);
+                }
+                double *o = out + (r * Hq + h) * (int64_t)d;
+                if (n_win + n_lm == 0) {
+                    for (int e = 0; e < d; ++e) o[e] = 0.0;
+                    lse[(int64_t)h * n_rows + r] = -INFINITY;
+                    continue;
+                }
+                const int64_t qoff = (r * Hq + h) * (int64_t)d;
+                /* Pass 1: scores and their maximum. */
+                double m = -INFINITY;
+                for (int64_t t = 0; t < n_win; ++t) {
+                    int64_t koff = ((j_lo + t - kv_start) * Hkv + c) * (int64_t)d;
+                    double dot = 0.0;
+                    for (int e = 0; e < d; ++e)
+                        dot += oracle_load(q, qoff + e, dtype) *
+                               oracle_load(k, koff + e, dtype);
+                    s_win[t] = scale * dot;
+                    if (s_win[t] > m) m = s_win[t];
+                }
+                for (int64_t l = 0; l < n_lm; ++l) {
+                    const double *kl = k_lm + (l * Hkv + c) * (int64_t)d;
+                    double dot = 0.0;
+                    for (int e = 0; e < d; ++e)
+                        dot += oracle_load(q, qoff + e, dtype) * kl[e];
+                    s_lm[l] = scale * dot;
+                    if (s_lm[l] > m) m = s_lm[l];
+                }
+                /* Pass 2: denominator and weighted sum of values. */
+                double denom = 0.0;
+                for (int e = 0; e < d; ++e) o[e] = 0.0;
+                for (int64_t t = 0; t < n_win; ++t) {
+                    double p = exp(s_win[t] - m);
+                    denom += p;
+                    int64_t voff = ((j_lo + t - kv_start) * Hkv + c) * (int64_t)d;
+                    for (int e = 0; e < d; ++e)
+                        o[e] += p * oracle_load(v, voff + e, dtype);
+                }
+                for (int64_t l = 0; l < n_lm; ++l) {
+                    double p = exp(s_lm[l] - m);
+                    denom += p;
+                    const double *vl = v_lm + (l * Hkv + c) * (int64_t)d;
+                    for (int e = 0; e < d; ++e) o[e] += p * vl[e];
+                }
+                for (int e = 0; e < d; ++e) o[e] /= denom;
+                lse[(int64_t)h * n_rows + r] = m + log(denom);
+            }
+        }
+        free(s_win);
+        free(s_lm);
+    }
+    return 0;
+}
+
+/*
+ * Merge of P partial results over disjoint key sets.
+ *   o_parts   [P][n_rows][Hq][d] fp64, lse_parts [P][Hq][n_rows] fp64
+ *   out       [n_rows][Hq][d],          lse       [Hq][n_rows]
+ * A part with lse_p = -inf holds no key for that row and is skipped; when
+ * every part is -inf the row's lse is -inf and its O is 0.
+ */
+int oracle_lse_merge(const double *o_parts, const double *lse_parts, int P,
+                     int64_t n_rows, int Hq, int d, double *out,
+                     double *lse) {
+    if (P < 1 || n_rows < 0 || Hq < 1 || d < 1) return -1;
+    const int64_t part_o = n_rows * Hq * (int64_t)d;
+    const int64_t part_l = (int64_t)Hq * n_rows;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        for (int h = 0; h < Hq; ++h) {
+            const int64_t li = (int64_t)h * n_rows + r;
+            const int64_t oi = (r * Hq + h) * (int64_t)d;
+            double mx = -INFINITY;
+            for (int p = 0; p < P; ++p) {
+                double l = lse_parts[p * part_l + li];
+                if (l > mx) mx = l;
+            }
+            double *o = out + oi;
+            for (int e = 0; e < d; ++e) o[e] = 0.0;
+            if (mx == -INFINITY) {
+                lse[li] = -INFINITY;
+                continue;
+            }
+            double sum = 0.0;
+            for (int p = 0; p < P; ++p) {
+                double l = lse_parts[p * part_l + li];
+                if (l == -INFINITY) continue;
+                sum += exp(l - mx);
+            }
+            const double total = mx + log(sum);
+            for (int p = 0; p < P; ++p) {
+                double l = lse_parts[p * part_l + li];
+                if (l == -INFINITY) continue;
+                const double wgt = exp(l - total);
+                const double *op = o_parts + p * part_o + oi;
+                for (int e = 0; e < d; ++e) o[e] += wgt * op[e];
+            }
+            lse[li] = total;
+        }
+    }
+    return 0;
+}

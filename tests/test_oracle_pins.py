@@ -1,0 +1,368 @@
+"""Pins for the fp64 CPU oracle (no GPU).
+
+The oracle is only trusted because these checks tie it to something other
+than itself: a dense brute force written from the set definitions, exact
+causal attention from a library routine, the merge invariant of Ring
+Attention ("Training at 1M+ Token Context", Ring Attention paragraph: each
+round aggregates softmax statistics), convexity, closed forms, and the
+page's own dot-product counts ("Scaling GPU Cluster for Million Token
+Context", section "The Cost of Attention: O(n^2) vs Sparse").
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from long_context_sparse_landmark_gb300.workloads import WORKLOADS
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- brute force
+def dense_bruteforce(q, k, v, window, G, scale):
+    """Materialise the full [n, n+G] masked score matrix per head (numpy).
+
+    Independent of the oracle: the mask is built element by element from the
+    two set definitions (window i-w < j <= i; landmark l visible when its
+    whole block [lB, (l+1)B) ends at or before i-w+1), landmarks come from
+    numpy's block mean, the softmax is taken over the masked row.
+    """
+    q = q.astype(np.float64)
+    k = k.astype(np.float64)
+    v = v.astype(np.float64)
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv
+    if G > 0:
+        B = n // G
+        klm = k.reshape(G, B, Hkv, d).mean(axis=1)
+        vlm = v.reshape(G, B, Hkv, d).mean(axis=1)
+    else:
+        B = 1
+        klm = np.zeros((0, Hkv, d))
+        vlm = np.zeros((0, Hkv, d))
+    mask = np.zeros((n, n + G), dtype=bool)
+    for i in range(n):
+        for j in range(n):
+            mask[i, j] = (i - window < j) and (j <= i)
+        for l in range(G):
+            block_last = (l + 1) * B - 1
+            mask[i, n + l] = block_last <= i - window
+    out = np.zeros((n, Hq, d))
+    lse = np.zeros((Hq, n))
+    for h in range(Hq):
+        c = h // g
+        keys = np.concatenate([k[:, c], klm[:, c]], axis=0)
+        vals = np.concatenate([v[:, c], vlm[:, c]], axis=0)
+        s = scale * q[:, h] @ keys.T
+        s = np.where(mask, s, -np.inf)
+        mx = s.max(axis=1, keepdims=True)
+        e = np.where(mask, np.exp(s - mx), 0.0)
+        den = e.sum(axis=1, keepdims=True)
+        out[:, h] = (e / den) @ vals
+        lse[h] = (mx + np.log(den))[:, 0]
+    return out, lse
+
+
+def to_bits(x32):
+    """fp32 array -> bf16 bit patterns (round to nearest even) and the fp32
+    values those bits hold."""
+    t = torch.from_numpy(np.ascontiguousarray(x32)).to(torch.bfloat16)
+    bits = t.view(torch.int16).numpy().view(np.uint16).copy()
+    return bits, t.to(torch.float32).numpy()
+
+
+def rand_qkv(rng, n, Hq, Hkv, d):
+    q = rng.standard_normal((n, Hq, d)).astype(np.float32)
+    k = rng.standard_normal((n, Hkv, d)).astype(np.float32)
+    v = rng.standard_normal((n, Hkv, d)).astype(np.float32)
+    return q, k, v
+
+
+def landmark_count(i, window, G, B):
+    """L(i) = clamp(floor((i - w + 1) / B), 0, G), the closed form."""
+    if G == 0:
+        return 0
+    return int(min(G, max(0, (i - window + 1) // B)))
+
+
+# ------------------------------------------------------------------- P1
+CASES = []
+for (n, G) in [(1, 0), (1, 1), (7, 0), (7, 7), (16, 0), (16, 1), (16, 2),
+               (16, 4), (16, 8), (16, 16), (48, 6), (64, 8)]:
+    B = n // G if G else 1
+    for w in sorted({1, 2, max(1, B - 1), B, B + 1, n, n + 5}):
+        CASES.append((n, G, w))
+
+
+@pytest.mark.parametrize("n,G,w", CASES)
+def test_p1_bruteforce(oracle_mod, n, G, w):
+    rng = np.random.default_rng(1000 * n + 10 * G + w)
+    for (Hq, Hkv), d in itertools.product([(1, 1), (2, 1), (4, 2), (4, 1)], [4, 8]):
+        q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+        scale = 1.0 / math.sqrt(d)
+        ref_o, ref_l = dense_bruteforce(q, k, v, w, G, scale)
+        o, l = oracle_mod.attn(q, k, v, w, G, scale)
+        np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l, ref_l, rtol=0, atol=1e-12)
+
+
+def test_p1_bruteforce_bf16_storage(oracle_mod):
+    """bf16 bit patterns are read as the values they encode."""
+    rng = np.random.default_rng(7)
+    n, G, w, Hq, Hkv, d = 32, 4, 5, 4, 2, 8
+    q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+    (qb, qf), (kb, kf), (vb, vf) = to_bits(q), to_bits(k), to_bits(v)
+    ref_o, ref_l = dense_bruteforce(qf, kf, vf, w, G, 0.3)
+    o, l = oracle_mod.attn(qb, kb, vb, w, G, 0.3)
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, ref_l, rtol=0, atol=1e-12)
+
+
+def test_p1_sampled_rows_match_all_rows(oracle_mod):
+    rng = np.random.default_rng(3)
+    q, k, v = rand_qkv(rng, 64, 4, 2, 8)
+    o, l = oracle_mod.attn(q, k, v, 9, 8, 0.35)
+    rows = np.array([0, 5, 17, 63])
+    os_, ls_ = oracle_mod.attn(q, k, v, 9, 8, 0.35, rows=rows)
+    np.testing.assert_array_equal(os_, o[rows])
+    np.testing.assert_array_equal(ls_, l[:, rows])
+
+
+# ------------------------------------------------------------------- P2
+@pytest.mark.parametrize("n,Hq,Hkv,d", [(1, 1, 1, 4), (33, 4, 2, 8),
+                                        (128, 8, 1, 16), (200, 4, 4, 32)])
+def test_p2_causal_special_case(oracle_mod, n, Hq, Hkv, d):
+    """w >= n and G = 0 is exact causal attention (torch SDPA, fp64, CPU)."""
+    rng = np.random.default_rng(n)
+    q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+    scale = 1.0 / math.sqrt(d)
+    for w in (n, n + 17):
+        o, _ = oracle_mod.attn(q, k, v, w, 0, scale)
+        g = Hq // Hkv
+        tq = torch.from_numpy(q).double().permute(1, 0, 2)[None]
+        tk = torch.from_numpy(k).double().repeat_interleave(g, dim=1).permute(1, 0, 2)[None]
+        tv = torch.from_numpy(v).double().repeat_interleave(g, dim=1).permute(1, 0, 2)[None]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            tq, tk, tv, is_causal=True, scale=scale)[0].permute(1, 0, 2).numpy()
+        np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------- P3
+def _chunked(oracle_mod, q, k, v, w, scale, bounds):
+    parts_o, parts_l = [], []
+    for lo, hi in zip(bounds[:-1], bounds[1:]):
+        o, l = oracle_mod.attn(q, k[lo:hi], v[lo:hi], w, 0, scale, kv_start=lo)
+        parts_o.append(o)
+        parts_l.append(l)
+    return np.stack(parts_o), np.stack(parts_l)
+
+
+@pytest.mark.parametrize("w", [1, 5, 40, 1000])
+def test_p3_merge_of_chunks_equals_single_pass(oracle_mod, w):
+    rng = np.random.default_rng(w)
+    n, Hq, Hkv, d = 96, 4, 2, 8
+    q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+    scale = 0.4
+    ref_o, ref_l = oracle_mod.attn(q, k, v, w, 0, scale)
+    for bounds in ([0, 1, 8, 96], [0, 7, 14, 21, 28, 35, 42, 49, 56, 63, 70, 77, 84, 91, 96],
+                   [0, 12, 24, 36, 48, 60, 72, 84, 96], [0, 50, 51, 96], [0, 96]):
+        po, pl = _chunked(oracle_mod, q, k, v, w, scale, bounds)
+        o, l = oracle_mod.lse_merge(po, pl)
+        np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l, ref_l, rtol=0, atol=1e-12)
+
+
+def test_p3_merge_pr1_size(oracle_mod):
+    """Causal attention on the 2048-token fp32 shape: 8 chunks merged."""
+    wl = WORKLOADS["pr1_2k"]
+    rng = np.random.default_rng(0)
+    q, k, v = rand_qkv(rng, wl.n, wl.Hq, wl.Hkv, wl.d)
+    rows = np.arange(0, wl.n, 7)
+    ref_o, ref_l = oracle_mod.attn(q, k, v, wl.n, 0, wl.scale, rows=rows)
+    bounds = list(range(0, wl.n + 1, wl.n // 8))
+    parts_o, parts_l = [], []
+    for lo, hi in zip(bounds[:-1], bounds[1:]):
+        o, l = oracle_mod.attn(q, k[lo:hi], v[lo:hi], wl.n, 0, wl.scale,
+                               rows=rows, kv_start=lo)
+        parts_o.append(o)
+        parts_l.append(l)
+    o, l = oracle_mod.lse_merge(np.stack(parts_o), np.stack(parts_l))
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, ref_l, rtol=0, atol=1e-12)
+
+
+def test_p3_empty_parts(oracle_mod):
+    """A chunk entirely after a row gives lse = -inf and is skipped."""
+    rng = np.random.default_rng(5)
+    q, k, v = rand_qkv(rng, 16, 2, 1, 4)
+    o, l = oracle_mod.attn(q, k[8:], v[8:], 16, 0, 0.5, kv_start=8)
+    assert np.all(np.isneginf(l[:, :8]))
+    assert np.all(o[:8] == 0.0)
+    assert np.all(np.isfinite(l[:, 8:]))
+    mo, ml = oracle_mod.lse_merge(np.stack([o, o]), np.stack([l, l]))
+    assert np.all(np.isneginf(ml[:, :8]))
+    np.testing.assert_allclose(mo[8:], o[8:], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ml[:, 8:], l[:, 8:] + math.log(2.0), rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------- P4
+@pytest.mark.parametrize("n,G,w", [(16, 4, 3), (24, 6, 1), (32, 8, 9), (12, 12, 2)])
+def test_p4_weights_are_a_convex_combination(oracle_mod, n, G, w):
+    """With V = identity (d = n), O[i, k] is the weight the row puts on
+    token k (window part plus its block's landmark share / B): all weights
+    are >= 0 and they sum to 1."""
+    rng = np.random.default_rng(n + G)
+    d = n
+    q = rng.standard_normal((n, 2, d)).astype(np.float32)
+    k = rng.standard_normal((n, 1, d)).astype(np.float32)
+    v = np.eye(n, dtype=np.float32)[:, None, :]
+    o, _ = oracle_mod.attn(q, k, v, w, G, 0.3)
+    assert np.all(o >= -1e-15)
+    np.testing.assert_allclose(o.sum(axis=2), 1.0, rtol=0, atol=1e-12)
+    # Weight sits only on attended tokens: the window, or a visible block.
+    B = n // G
+    for i in range(n):
+        L = landmark_count(i, w, G, B)
+        for kk in range(n):
+            attended = (i - w < kk <= i) or (kk // B < L)
+            if not attended:
+                assert np.all(o[i, :, kk] == 0.0)
+
+
+def test_p4_rows_within_value_hull(oracle_mod):
+    rng = np.random.default_rng(11)
+    n, G, w, d = 40, 5, 6, 8
+    q, k, v = rand_qkv(rng, n, 2, 1, d)
+    o, _ = oracle_mod.attn(q, k, v, w, G, 0.5)
+    B = n // G
+    vlm = v.astype(np.float64).reshape(G, B, 1, d).mean(axis=1)
+    for i in range(n):
+        rows = [v[j, 0].astype(np.float64) for j in range(max(0, i - w + 1), i + 1)]
+        rows += [vlm[l, 0] for l in range(landmark_count(i, w, G, B))]
+        rows = np.stack(rows)
+        lo, hi = rows.min(axis=0), rows.max(axis=0)
+        for h in range(2):
+            assert np.all(o[i, h] >= lo - 1e-12) and np.all(o[i, h] <= hi + 1e-12)
+
+
+# ------------------------------------------------------------------- P5
+@pytest.mark.parametrize("n,G,w", [(64, 8, 1), (64, 8, 9), (64, 16, 20), (60, 5, 13)])
+def test_p5a_zero_keys_give_uniform_weights(oracle_mod, n, G, w):
+    rng = np.random.default_rng(n * w)
+    d = 4
+    q = rng.standard_normal((n, 2, d)).astype(np.float32)
+    k = np.zeros((n, 1, d), dtype=np.float32)
+    v = rng.standard_normal((n, 1, d)).astype(np.float32)
+    o, l = oracle_mod.attn(q, k, v, w, G, 0.7)
+    B = n // G
+    vlm = v.astype(np.float64).reshape(G, B, 1, d).mean(axis=1)
+    for i in range(n):
+        L = landmark_count(i, w, G, B)
+        cnt = min(w, i + 1) + L
+        assert l[0, i] == pytest.approx(math.log(cnt), abs=1e-13)
+        rows = [v[j, 0].astype(np.float64) for j in range(max(0, i - w + 1), i + 1)]
+        rows += [vlm[x, 0] for x in range(L)]
+        np.testing.assert_allclose(o[i, 0], np.mean(rows, axis=0), rtol=0, atol=1e-12)
+
+
+def test_p5b_constant_values(oracle_mod):
+    rng = np.random.default_rng(2)
+    q, k, _ = rand_qkv(rng, 48, 4, 2, 8)
+    v = np.full((48, 2, 8), 0.625, dtype=np.float32)
+    o, _ = oracle_mod.attn(q, k, v, 7, 6, 0.35)
+    np.testing.assert_allclose(o, 0.625, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("n,G", [(64, 8), (2048, 16), (96, 96)])
+def test_p5c_position_keys_give_block_centres(oracle_mod, n, G):
+    k = np.repeat(np.arange(n, dtype=np.float32)[:, None, None], 3, axis=1)
+    k = np.repeat(k, 4, axis=2)
+    lm = oracle_mod.landmark_pool(k, G)
+    B = n // G
+    for l in range(G):
+        assert np.all(lm[l] == l * B + (B - 1) / 2.0)
+
+
+def test_p5d_hard_max_limit(oracle_mod):
+    """Q[i] = lambda * K[i] with lambda large: row i's output tends to V[i]
+    whenever its own key beats every other attended key."""
+    rng = np.random.default_rng(4)
+    n, G, w, d = 32, 4, 6, 16
+    k = rng.standard_normal((n, 1, d)).astype(np.float32)
+    v = rng.standard_normal((n, 1, d)).astype(np.float32)
+    lam = 200.0
+    q = (lam * k).astype(np.float32)
+    o, _ = oracle_mod.attn(q, k, v, w, G, 1.0 / math.sqrt(d))
+    B = n // G
+    klm = k.astype(np.float64).reshape(G, B, 1, d).mean(axis=1)
+    checked = 0
+    for i in range(n):
+        own = float(k[i, 0] @ k[i, 0])
+        others = [float(k[i, 0] @ k[j, 0]) for j in range(max(0, i - w + 1), i)]
+        others += [float(k[i, 0] @ klm[x, 0]) for x in range(landmark_count(i, w, G, B))]
+        if others and own - max(others) < 1.0:
+            continue
+        np.testing.assert_allclose(o[i, 0], v[i, 0], rtol=0, atol=1e-6)
+        checked += 1
+    assert checked > n // 2
+
+
+# ------------------------------------------------------------------- P6
+def attended_total_closed_form(n, w, G):
+    """sum_i min(w, i+1) + L(i) per head, vectorised closed form."""
+    i = np.arange(n, dtype=np.int64)
+    win = np.minimum(w, i + 1)
+    if G == 0:
+        return int(win.sum())
+    B = n // G
+    lm = np.clip((i - w + 1) // B, 0, G)
+    return int(win.sum() + lm.sum())
+
+
+def test_p6_count_closed_form_matches_set_definition():
+    for n, w, G in [(64, 1, 8), (64, 9, 8), (60, 13, 5), (96, 96, 96), (128, 200, 4)]:
+        B = n // G
+        brute = 0
+        for i in range(n):
+            brute += sum(1 for j in range(n) if i - w < j <= i)
+            brute += sum(1 for l in range(G) if (l + 1) * B <= i - w + 1)
+        assert attended_total_closed_form(n, w, G) == brute
+
+
+def test_p6_oracle_count_via_zero_keys(oracle_mod):
+    """With K = 0, exp(lse) is the size of the attended set."""
+    n, w, G = 256, 37, 16
+    q = np.ones((n, 1, 1), dtype=np.float32)
+    k = np.zeros((n, 1, 1), dtype=np.float32)
+    _, l = oracle_mod.attn(q, k, k, w, G, 1.0)
+    counts = np.rint(np.exp(l[0])).astype(np.int64)
+    assert int(counts.sum()) == attended_total_closed_form(n, w, G)
+
+
+def test_p6_workload_totals_match_golden():
+    with open(os.path.join(GOLDEN, "attended_counts.json")) as f:
+        golden = json.load(f)
+    for name, wl in WORKLOADS.items():
+        assert attended_total_closed_form(wl.n, wl.window, wl.G) == golden["per_head"][name], name
+
+
+def test_p6_page_dot_product_arithmetic():
+    """"The Cost of Attention" section counts 64 heads x 1M x 4K = 0.256e12
+    window dot products and 64 x 1M x 512 = 0.033e12 landmark ones per layer
+    (its 1M = 1e6, 4K = 4e3).  Our exact window count for the million-token
+    layer agrees to first order; the landmark count is lower because only
+    blocks wholly before the window are visible."""
+    wl = WORKLOADS["1m_70b_layer"]
+    i = np.arange(wl.n, dtype=np.int64)
+    window_total = wl.Hq * int(np.minimum(wl.window, i + 1).sum())
+    assert abs(window_total / 0.256e12 - 1.0) < 0.10
+    lm_total = wl.Hq * int(np.clip((i - wl.window + 1) // wl.block, 0, wl.G).sum())
+    assert 0.3 < lm_total / 0.033e12 < 1.0
+    # "Training at 1M+ Token Context", memory paragraph: the KV cache of one
+    # layer at 1M tokens, 8 KV heads x 128 x bf16, is about 2 GB per tensor.
+    assert abs(wl.n * wl.Hkv * wl.d * 2 / 2**30 - 2.0) < 1e-9
