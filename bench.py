@@ -1,0 +1,452 @@
+#!/usr/bin/env python
+"""Benchmark: window + landmark sparse attention forward on GB300.
+
+One step = one pass of the hot path over one layer of synthetic input:
+landmark pooling (K1) then the fused window + landmark attention (K2) on the
+128K-token 70B-style layer (n=131072, 64 query / 8 KV heads, d=128, w=4096,
+512 landmarks, bf16).  The headline value is useful TFLOP/s of that step
+(4 * d * Hq * sum_i |attended set of row i|; masked work not counted).
+The same run also measures the million-token layer and the Ring Attention
+emulation (8 KV-chunk partials + LSE merge, K3) and reports them under
+"also".
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl msa|reference]
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path has no exchange step on one GPU); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "128k_70b_layer"
+METRIC = "sparse-attn fwd TFLOP/s & tokens/s at 128K and 1M tokens; % of bf16 TC peak"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p["bf16_tflops_sustained"], "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def attended_total(wl) -> int:
+    """sum_i |window(i)| + |visible landmarks(i)| for one head (closed form)."""
+    import numpy as np
+    i = np.arange(wl.n, dtype=np.int64)
+    win = np.minimum(wl.window, i + 1).sum()
+    lm = np.clip((i - wl.window + 1) // wl.block, 0, wl.G).sum() if wl.G else 0
+    return int(win + lm)
+
+
+def useful_flops(wl) -> float:
+    return 4.0 * wl.d * wl.Hq * attended_total(wl)
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+def run_window_landmark(wl, steps, warmup, dev, B, torch):
+    """Device-resident inputs; each step = pool (K1) + fused attention (K2)."""
+    from long_context_sparse_landmark_gb300.workloads import generate
+    q, k, v = generate(wl, device=dev)
+    k_lm = torch.empty((wl.G, wl.Hkv, wl.d), dtype=k.dtype, device=dev)
+    v_lm = torch.empty_like(k_lm)
+    out = torch.empty((wl.n, wl.Hq, wl.d), dtype=q.dtype, device=dev)
+    lse = torch.empty((wl.Hq, wl.n), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        B.landmark_pool(k, v, k_lm, v_lm, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        B.attn_fwd(q, k, v, k_lm, v_lm, out, lse, wl.window, wl.G, wl.scale, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(steps):
+        step(evs[s])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    assert B.device_status() == 0, "a bounded device wait ran out"
+    total_ms = t0.elapsed_time(t1)
+    pool_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    res = {"total_ms": total_ms, "ms_per_step": total_ms / steps,
+           "pool_ms": statistics.mean(pool_ms), "attn_ms": statistics.mean(attn_ms),
+           "launches_per_step": 2}
+    del q, k, v, k_lm, v_lm, out, lse
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_e2e(wl, steps, dev, torch):
+    """Through the public API with pinned HOST buffers: every step copies
+    Q/K/V host->device, runs msa_attention, copies O and lse back."""
+    import long_context_sparse_landmark_gb300 as pkg
+    from long_context_sparse_landmark_gb300.workloads import generate
+    q, k, v = generate(wl, device=dev)
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    del q, k, v
+    torch.cuda.empty_cache()
+    ho = torch.empty((wl.n, wl.Hq, wl.d), dtype=hq.dtype).pin_memory()
+    hl = torch.empty((wl.Hq, wl.n), dtype=torch.float32).pin_memory()
+
+    def step():
+        dq = hq.to(dev, non_blocking=True)
+        dk = hk.to(dev, non_blocking=True)
+        dv = hv.to(dev, non_blocking=True)
+        o, l = pkg.msa_attention(dq, dk, dv, wl.window, wl.G, wl.scale)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(l, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    step()
+    t = time.perf_counter()
+    for _ in range(steps):
+        step()
+    el = time.perf_counter() - t
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    return el / steps, h2d, d2h
+
+
+def run_ring(wl, steps, warmup, dev, B, torch):
+    """Ring emulation: per step 8 chunk partials (K2 partial mode) + merge (K3)."""
+    from long_context_sparse_landmark_gb300.workloads import generate
+    q, k, v = generate(wl, device=dev)
+    n, Hq, d = q.shape
+    P = wl.ring_chunks
+    c = n // P
+    o_parts = [torch.empty((n, Hq, d), dtype=torch.float32, device=dev) for _ in range(P)]
+    l_parts = [torch.empty((Hq, n), dtype=torch.float32, device=dev) for _ in range(P)]
+    out = torch.empty((n, Hq, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Hq, n), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        for p in range(P):
+            B.attn_fwd_partial(q, k[p * c:(p + 1) * c], v[p * c:(p + 1) * c], o_parts[p],
+                               l_parts[p], 0, p * c, wl.window, wl.scale, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        B.lse_merge(o_parts, l_parts, out, lse, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for s in range(steps):
+        step(evs[s])
+    torch.cuda.synchronize()
+    assert B.device_status() == 0
+    part_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    merge_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    # Required merge bytes: every lse_p, every O_p row with finite lse_p, output.
+    finite = sum(int(torch.isfinite(l).sum()) for l in l_parts)
+    merge_bytes = P * n * Hq * 4 + finite * d * 4 + n * Hq * (d * 2 + 4)
+    del q, k, v, o_parts, l_parts, out, lse
+    torch.cuda.empty_cache()
+    return {"partials_ms": part_ms, "merge_ms": merge_ms, "merge_bytes": merge_bytes,
+            "launches_per_step": P + 1}
+
+
+def cpu_baseline(wl, rows_target, torch):
+    """The fp64 oracle on the host cores, on a bounded row sample of the
+    same workload; extrapolated to the full layer by rows."""
+    import numpy as np
+    import oracle
+    from long_context_sparse_landmark_gb300.workloads import generate, to_numpy_bits
+    oracle.set_threads(os.cpu_count() or 1)
+    q, k, v = generate(wl, device="cuda")
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(wl.n, size=rows_target, replace=False)).astype(np.int64)
+    qs = to_numpy_bits(q.index_select(0, torch.as_tensor(rows, device=q.device)))
+    kn, vn = to_numpy_bits(k), to_numpy_bits(v)
+    del q, k, v
+    torch.cuda.empty_cache()
+    t = time.perf_counter()
+    k_lm = oracle.landmark_pool(kn, wl.G)
+    v_lm = oracle.landmark_pool(vn, wl.G)
+    pool_s = time.perf_counter() - t
+    t = time.perf_counter()
+    oracle.attn(qs, kn, vn, wl.window, wl.G, wl.scale, q_positions=rows, landmarks=(k_lm, v_lm))
+    rows_s = time.perf_counter() - t
+    i = rows
+    per_row = np.minimum(wl.window, i + 1) + np.clip((i - wl.window + 1) // wl.block, 0, wl.G)
+    sample_flops = 4.0 * wl.d * wl.Hq * float(per_row.sum())
+    full_s = pool_s + rows_s * useful_flops(wl) / sample_flops
+    return {"value": useful_flops(wl) / full_s / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.get_threads(), "kind": "oracle",
+            "sample": (f"{rows_target} random rows x {wl.Hq} heads of {wl.name} "
+                       f"({rows_s:.1f} s) + landmark pooling of the full K/V ({pool_s:.1f} s); "
+                       f"extrapolated to all {wl.n} rows by attended keys"),
+            "wall_s": pool_s + rows_s}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["msa", "reference"], default="msa")
+    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--no-also", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    import torch
+    from long_context_sparse_landmark_gb300.workloads import WORKLOADS
+    wl = WORKLOADS[HEADLINE]
+    peaks = load_peaks()
+
+    if args.impl == "reference":
+        run_reference(args, wl, rank, world, torch)
+        return
+
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    from long_context_sparse_landmark_gb300 import _binding as B
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    with ClockSampler(local_rank) as clk:
+        res = run_window_landmark(wl, args.steps, args.warmup, dev, B, torch)
+    barrier()
+    total_ms = res["total_ms"]
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    flops = useful_flops(wl)
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    tokens_per_s = world * wl.n / (ms_per_step * 1e-3)
+    attn_tflops = flops / (res["attn_ms"] * 1e-3) / 1e12
+    pool_bytes = 2 * wl.n * wl.Hkv * wl.d * 2 + 2 * wl.G * wl.Hkv * wl.d * 2
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (i.i.d. N(0,1) Q/K/V from seed 0, bf16)",
+        "config": {"workload": HEADLINE, "n": wl.n, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                   "window": wl.window, "landmarks": wl.G, "batch": 1,
+                   "step": "landmark pool + fused window/landmark attention",
+                   "l2": "inputs larger than L2 (Q 2.1 GB, K/V 0.27 GB each)",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(tokens_per_s, 1),
+        "pct_bf16_peak": round(100.0 * value / world / peaks["bf16_tflops"], 2),
+        "kernels_ms": {"landmark_pool": round(res["pool_ms"], 4),
+                       "attn_fwd": round(res["attn_ms"], 4)},
+        "roofline": {"bound": "tensor", "kernel": "attn_tc_kernel",
+                     "achieved": round(attn_tflops, 2),
+                     "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": round(attn_tflops / peaks["bf16_tflops_sustained"], 4),
+                     "peak_kind": f"bf16 sustained ({peaks['source']})",
+                     "frac_of_burst": round(attn_tflops / peaks["bf16_tflops"], 4),
+                     "traffic": None},
+        "pool_roofline": {"bound": "hbm",
+                          "achieved": round(pool_bytes / (res["pool_ms"] * 1e-3) / 1e9, 1),
+                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": round(pool_bytes / (res["pool_ms"] * 1e-3) / 1e9
+                                        / peaks["hbm_gbs"], 4)},
+        "gpu_launches": res["launches_per_step"] * args.steps,
+        "clocks": clk.summary(),
+    }
+
+    if not args.no_e2e and rank == 0:
+        e2e_s, h2d, d2h = run_e2e(wl, 3, dev, torch)
+        line["e2e"] = {"value": round(flops / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(e2e_s * 1e3, 3)}
+
+    if not args.no_also and rank == 0:
+        also = {}
+        wl1m = WORKLOADS["1m_70b_layer"]
+        r1 = run_window_landmark(wl1m, 3, 1, dev, B, torch)
+        f1 = useful_flops(wl1m)
+        also["1m_70b_layer"] = {
+            "ms_per_step": round(r1["ms_per_step"], 3),
+            "tflops": round(f1 / (r1["ms_per_step"] * 1e-3) / 1e12, 2),
+            "tokens_per_s": round(wl1m.n / (r1["ms_per_step"] * 1e-3), 1),
+            "attn_tflops": round(f1 / (r1["attn_ms"] * 1e-3) / 1e12, 2),
+            "pct_bf16_peak": round(100.0 * f1 / (r1["ms_per_step"] * 1e-3) / 1e12
+                                   / peaks["bf16_tflops"], 2),
+            "pool_gbs": round((2 * wl1m.n * wl1m.Hkv * wl1m.d * 2 + 2 * wl1m.G * wl1m.Hkv
+                               * wl1m.d * 2) / (r1["pool_ms"] * 1e-3) / 1e9, 1),
+            "steps": 3}
+        wlr = WORKLOADS["ring_128k"]
+        rr = run_ring(wlr, 3, 1, dev, B, torch)
+        fr = useful_flops(wlr)
+        also["ring_128k"] = {
+            "partials_ms": round(rr["partials_ms"], 3), "merge_ms": round(rr["merge_ms"], 3),
+            "partials_tflops": round(fr / (rr["partials_ms"] * 1e-3) / 1e12, 2),
+            "merge_gbs": round(rr["merge_bytes"] / (rr["merge_ms"] * 1e-3) / 1e9, 1),
+            "merge_frac_hbm": round(rr["merge_bytes"] / (rr["merge_ms"] * 1e-3) / 1e9
+                                    / peaks["hbm_gbs"], 4),
+            "steps": 3}
+        line["also"] = also
+
+    if not args.no_cpu and rank == 0:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows, torch)
+
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args, wl, rank, world, torch):
+    """Reference arm: the fp64 oracle on the host cores (there is no code
+    of the pages to install); each step evaluates a bounded row sample of
+    the 128K layer, extrapolated to the full layer."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from long_context_sparse_landmark_gb300.workloads import generate, to_numpy_bits
+    oracle.build()
+    oracle.set_threads(os.cpu_count() or 1)
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    q, k, v = generate(wl, device=gen_dev)
+    kn, vn = to_numpy_bits(k), to_numpy_bits(v)
+    k_lm = oracle.landmark_pool(kn, wl.G)
+    v_lm = oracle.landmark_pool(vn, wl.G)
+    rows_per_step = 64
+    rng = np.random.default_rng(0)
+    flops_full = useful_flops(wl)
+
+    def one(rows):
+        qs = to_numpy_bits(q.index_select(0, torch.as_tensor(rows, device=q.device)))
+        t = time.perf_counter()
+        oracle.attn(qs, kn, vn, wl.window, wl.G, wl.scale, q_positions=rows,
+                    landmarks=(k_lm, v_lm))
+        el = time.perf_counter() - t
+        per_row = np.minimum(wl.window, rows + 1) + np.clip((rows - wl.window + 1) // wl.block,
+                                                            0, wl.G)
+        return el, 4.0 * wl.d * wl.Hq * float(per_row.sum())
+
+    for _ in range(args.warmup):
+        one(np.sort(rng.choice(wl.n, rows_per_step, replace=False)).astype(np.int64))
+    tot_s, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        el, f = one(np.sort(rng.choice(wl.n, rows_per_step, replace=False)).astype(np.int64))
+        tot_s += el
+        tot_f += f
+    value = tot_f / tot_s / 1e12
+    ms_per_step = flops_full / (value * 1e12) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs)",
+            "config": {"workload": HEADLINE, "n": wl.n, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                       "window": wl.window, "landmarks": wl.G, "batch": 1},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.get_threads(),
+                             "kind": "oracle",
+                             "sample": f"{rows_per_step} random rows x {wl.Hq} heads per step, "
+                                       "landmarks pooled once; extrapolated to the full layer"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,182 @@
+/*
+ * msa.h -- C ABI of libmsa: window + landmark sparse attention forward on
+ * one GB300 (sm_103a), plus the log-sum-exp merge of Ring Attention partials.
+ *
+ * The method.  "Scaling GPU Cluster for Million Token Context", sections
+ * "Why Sparse Attention Changes the Game" and "What is Flash-MSA Sparse
+ * Attention in GPU Clusters?", describe Flash-MSA: every token attends to a
+ * local window (4096 tokens there) and to a set of about 512 landmark tokens
+ * that summarise distant context, fused in one pass that never materialises
+ * the n x n score matrix.  The pages do not define landmarks or the mask;
+ * this library fixes them as follows (batch 1, token-major layouts):
+ *
+ *   Q [n, Hq, d], K and V [n, Hkv, d]; query head h reads KV head
+ *   h / (Hq/Hkv) (grouped-query attention, contiguous groups).
+ *   Landmark l (0 <= l < G) is the mean of K (resp. V) over the contiguous
+ *   block of B = n/G tokens [lB, (l+1)B).
+ *   Row i attends keys j with i-w < j <= i, and every landmark l whose whole
+ *   block lies before that window: (l+1)B <= i-w+1.
+ *   One softmax over the union, scores scale * <q, k>:
+ *   O[i,h,:] = sum_x softmax_x * V_x,  lse[h,i] = ln sum_x exp(scale<q,k_x>).
+ *
+ * Ring Attention ("Training at 1M+ Token Context: Ring Attention, YaRN,
+ * NTK-Aware Scaling", Ring Attention paragraph) computes, per round, partial
+ * attention of local queries against one contiguous KV block and aggregates
+ * the softmax statistics; msa_attn_fwd_partial + msa_lse_merge are those two
+ * steps, run on one GPU.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous
+ *     and 16-byte aligned, unless stated otherwise.  The library never
+ *     allocates device memory and never synchronises the stream; all work
+ *     is enqueued on `stream` (NULL = legacy default stream) and results are
+ *     valid in stream order.
+ *   - Arguments are validated before anything is enqueued.  On failure the
+ *     call enqueues nothing, returns a status code and records a message
+ *     that msa_last_error_string() returns (per calling thread).
+ *   - A launch failure returns MSA_ERR_CUDA.  Kernels that wait on
+ *     asynchronous copies bound every wait; a wait that runs out makes the
+ *     kernel finish early and record MSA_ERR_TIMEOUT in a per-device status
+ *     word that msa_device_status() reads.
+ *   - lse is always fp32, natural log.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *msa_stream_t; /* same object as cudaStream_t */
+
+typedef enum {
+    MSA_OK = 0,
+    MSA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or shape */
+    MSA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d not 64/128) */
+    MSA_ERR_CUDA = 3,        /* CUDA runtime or driver error */
+    MSA_ERR_TIMEOUT = 4      /* a bounded device wait ran out */
+} msa_status;
+
+typedef enum { MSA_F32 = 0, MSA_BF16 = 1 } msa_dtype;
+
+/* Version as major*10000 + minor*100 + patch. */
+int msa_version(void);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char *msa_last_error_string(void);
+
+/*
+ * Landmark pooling ("Scaling GPU Cluster for Million Token Context",
+ * "What is Flash-MSA ...": landmarks summarise distant context; defined here
+ * as block means).
+ *   k, v       [n, Hkv, d] in dtype `dt`
+ *   k_lm, v_lm [G, Hkv, d] in dtype `dt`, written:
+ *              k_lm[l,c,:] = (1/B) sum_{j=lB}^{(l+1)B-1} k[j,c,:], B = n/G,
+ *              summed in fp32, rounded to `dt` (nearest even).
+ * Errors: INVALID_ARG if a pointer is null or not 16-byte aligned, n < 1,
+ * Hkv < 1, G < 1, G > n or n % G != 0; UNSUPPORTED if d is not 64 or 128.
+ */
+msa_status msa_landmark_pool(const void *k, const void *v, void *k_lm,
+                             void *v_lm, int64_t n, int Hkv, int d,
+                             int n_landmarks, msa_dtype dt,
+                             msa_stream_t stream);
+
+/*
+ * Fused window + landmark attention forward (the Flash-MSA pass above).
+ *   q          [n, Hq, d]  in `in_dt`
+ *   k, v       [n, Hkv, d] in `in_dt`
+ *   k_lm, v_lm [G, Hkv, d] in `in_dt`: the landmarks msa_landmark_pool
+ *              wrote for these k, v (may be NULL iff G == 0)
+ *   out        [n, Hq, d]  in `out_dt`, written
+ *   lse        [Hq, n] fp32, written (natural log of the softmax denominator)
+ *   window     w >= 1 (keys i-w < j <= i); w >= n with G = 0 is causal
+ *              attention
+ *   scale      score scale (1/sqrt(d) for standard attention)
+ * bf16 inputs with d = 128 run on the tensor cores (TMA + tcgen05, fp32
+ * accumulation in tensor memory); other inputs run a CUDA-core kernel with
+ * fp32 arithmetic.
+ * Errors: INVALID_ARG for null/misaligned pointers, n < 1, w < 1, Hq or Hkv
+ * < 1, Hq % Hkv != 0, G < 0, G > n, G > 0 with n % G != 0, G > 0 with null
+ * landmarks; UNSUPPORTED if d is not 64 or 128.
+ */
+msa_status msa_attn_fwd(const void *q, const void *k, const void *v,
+                        const void *k_lm, const void *v_lm, void *out,
+                        float *lse, int64_t n, int Hq, int Hkv, int d,
+                        int64_t window, int n_landmarks, float scale,
+                        msa_dtype in_dt, msa_dtype out_dt,
+                        msa_stream_t stream);
+
+/*
+ * One Ring Attention round's partial: queries at global positions
+ * q_start .. q_start+n_q-1 against the contiguous KV chunk at global
+ * positions kv_start .. kv_start+n_kv-1, with the causal window mask
+ * i-w < j <= i taken in global positions, no landmarks.
+ *   q        [n_q, Hq, d]   in `in_dt`
+ *   k_chunk, v_chunk [n_kv, Hkv, d] in `in_dt`
+ *   out_part [n_q, Hq, d] fp32, written for every row with at least one key
+ *   lse_part [Hq, n_q] fp32, written; -inf for a row with no key in the
+ *            chunk (its out_part row is then left untouched)
+ * Errors: as msa_attn_fwd, plus INVALID_ARG for n_q < 1, n_kv < 1,
+ * q_start < 0 or kv_start < 0.
+ */
+msa_status msa_attn_fwd_partial(const void *q, const void *k_chunk,
+                                 const void *v_chunk, float *out_part,
+                                 float *lse_part, int64_t n_q, int64_t q_start,
+                                 int64_t n_kv, int64_t kv_start, int Hq,
+                                 int Hkv, int d, int64_t window, float scale,
+                                 msa_dtype in_dt, msa_stream_t stream);
+
+/* Largest number of partials msa_lse_merge accepts in one call. */
+#define MSA_MAX_MERGE_PARTS 64
+
+/*
+ * Exact merge of partial results over disjoint key sets (the aggregation
+ * step of a Ring Attention round):
+ *   lse = ln sum_p exp(lse_p),   out = sum_p exp(lse_p - lse) * o_p,
+ * skipping parts whose lse_p is -inf; a row where every part is -inf gets
+ * lse = -inf and out = 0.
+ *   o_parts   HOST array of n_parts DEVICE pointers, each [n, Hq, d] fp32
+ *   lse_parts HOST array of n_parts DEVICE pointers, each [Hq, n] fp32
+ *   out       [n, Hq, d] in `out_dt`, written; with out_dt = MSA_F32 it may
+ *             alias o_parts[0] (in-place running accumulation)
+ *   lse       [Hq, n] fp32, written; may alias lse_parts[0]
+ * Errors: INVALID_ARG for null arrays/pointers, misalignment, n_parts < 1
+ * or > MSA_MAX_MERGE_PARTS, n < 1, Hq < 1, d < 4 or d % 4 != 0, or an
+ * alias that is not allowed.
+ */
+msa_status msa_lse_merge(const float *const *o_parts,
+                         const float *const *lse_parts, int n_parts,
+                         void *out, float *lse, int64_t n, int Hq, int d,
+                         msa_dtype out_dt, msa_stream_t stream);
+
+/*
+ * Which attention kernel msa_attn_fwd / msa_attn_fwd_partial run for these
+ * arguments: 1 = tensor-core kernel (TMA + tcgen05), 0 = CUDA-core kernel.
+ */
+int msa_attn_uses_tensor_cores(int Hq, int Hkv, int d, msa_dtype in_dt);
+
+/*
+ * Reads (and, if `clear` is nonzero, resets) the status word that the
+ * kernels of this library set on the current device when a bounded wait
+ * runs out.  Synchronises the device.  Returns MSA_OK, MSA_ERR_TIMEOUT, or
+ * MSA_ERR_CUDA if the read itself failed.
+ */
+msa_status msa_device_status(int clear);
+
+/*
+ * Test hook: sets the limit, in nanoseconds, of every bounded wait in the
+ * tensor-core kernel for launches made after the call (0 restores the
+ * default of 4 s).  A very small limit makes waits run out on purpose, to
+ * check that the kernel then finishes early with MSA_ERR_TIMEOUT instead of
+ * hanging.  Copies already in flight are still waited for with the default
+ * limit before a kernel exits.
+ */
+void msa_debug_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

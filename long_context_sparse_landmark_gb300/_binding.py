@@ -1,0 +1,149 @@
+"""ctypes binding of libmsa's C ABI (include/msa.h), argument marshalling only.
+
+Each function here takes torch tensors, checks device/dtype/contiguity,
+and passes raw device pointers plus the current CUDA stream to the C entry
+point of the same name.  All arithmetic runs in libmsa's CUDA kernels; if
+the library is missing the import fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmsa.so")
+
+MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_CUDA, MSA_ERR_TIMEOUT = range(5)
+MSA_F32, MSA_BF16 = 0, 1
+MAX_MERGE_PARTS = 64
+
+# Every symbol include/msa.h declares.
+EXPORTS = ("msa_version", "msa_last_error_string", "msa_landmark_pool", "msa_attn_fwd",
+           "msa_attn_fwd_partial", "msa_lse_merge", "msa_attn_uses_tensor_cores",
+           "msa_device_status", "msa_debug_set_wait_limit_ns")
+
+
+class MsaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"msa status {status}: {msg}")
+        self.status = status
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"libmsa.so not found at {path}; build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    lib.msa_version.restype = i32
+    lib.msa_last_error_string.restype = ctypes.c_char_p
+    lib.msa_landmark_pool.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i32, vp]
+    lib.msa_landmark_pool.restype = i32
+    lib.msa_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32, f32,
+                                 i32, i32, vp]
+    lib.msa_attn_fwd.restype = i32
+    lib.msa_attn_fwd_partial.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, i32,
+                                         i64, f32, i32, vp]
+    lib.msa_attn_fwd_partial.restype = i32
+    lib.msa_lse_merge.argtypes = [vp, vp, i32, vp, vp, i64, i32, i32, i32, vp]
+    lib.msa_lse_merge.restype = i32
+    lib.msa_attn_uses_tensor_cores.argtypes = [i32, i32, i32, i32]
+    lib.msa_attn_uses_tensor_cores.restype = i32
+    lib.msa_device_status.argtypes = [i32]
+    lib.msa_device_status.restype = i32
+    lib.msa_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.msa_debug_set_wait_limit_ns.restype = None
+    return lib
+
+
+_lib = load_library()
+
+
+def _check(status: int) -> None:
+    if status != MSA_OK:
+        raise MsaError(status, _lib.msa_last_error_string().decode())
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return MSA_F32
+    if t.dtype == torch.bfloat16:
+        return MSA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def version() -> int:
+    return int(_lib.msa_version())
+
+
+def uses_tensor_cores(Hq: int, Hkv: int, d: int, dtype: torch.dtype) -> bool:
+    return bool(_lib.msa_attn_uses_tensor_cores(Hq, Hkv, d, MSA_BF16 if dtype == torch.bfloat16
+                                                else MSA_F32))
+
+
+def device_status(clear: bool = True) -> int:
+    return int(_lib.msa_device_status(1 if clear else 0))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    _lib.msa_debug_set_wait_limit_ns(int(ns))
+
+
+def landmark_pool(k: torch.Tensor, v: torch.Tensor, k_lm: torch.Tensor, v_lm: torch.Tensor,
+                  stream=None) -> None:
+    """msa_landmark_pool: block means of k, v [n, Hkv, d] into k_lm, v_lm [G, Hkv, d]."""
+    n, Hkv, d = k.shape
+    G = k_lm.shape[0]
+    _check(_lib.msa_landmark_pool(_ptr(k), _ptr(v), _ptr(k_lm), _ptr(v_lm), n, Hkv, d, G, _dt(k),
+                                  _stream(stream)))
+
+
+def attn_fwd(q, k, v, k_lm, v_lm, out, lse, window: int, n_landmarks: int, scale: float,
+             stream=None) -> None:
+    """msa_attn_fwd: window + landmark attention; out [n, Hq, d], lse [Hq, n] fp32."""
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    _check(_lib.msa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(k_lm), _ptr(v_lm), _ptr(out),
+                             _ptr(lse), n, Hq, Hkv, d, int(window), int(n_landmarks),
+                             float(scale), _dt(q), _dt(out), _stream(stream)))
+
+
+def attn_fwd_partial(q, k_chunk, v_chunk, out_part, lse_part, q_start: int, kv_start: int,
+                     window: int, scale: float, stream=None) -> None:
+    """msa_attn_fwd_partial: one Ring Attention round's partial (fp32 out_part)."""
+    n_q, Hq, d = q.shape
+    n_kv, Hkv, _ = k_chunk.shape
+    _check(_lib.msa_attn_fwd_partial(_ptr(q), _ptr(k_chunk), _ptr(v_chunk), _ptr(out_part),
+                                     _ptr(lse_part), n_q, int(q_start), n_kv, int(kv_start), Hq,
+                                     Hkv, d, int(window), float(scale), _dt(q), _stream(stream)))
+
+
+def lse_merge(o_parts, lse_parts, out, lse, stream=None) -> None:
+    """msa_lse_merge: exact LSE-weighted merge of partials (lists of tensors)."""
+    P = len(o_parts)
+    if P != len(lse_parts):
+        raise ValueError("o_parts and lse_parts differ in length")
+    n, Hq, d = out.shape
+    arr_o = (ctypes.c_void_p * max(P, 1))(*[t.data_ptr() for t in o_parts])
+    arr_l = (ctypes.c_void_p * max(P, 1))(*[t.data_ptr() for t in lse_parts])
+    for t in list(o_parts) + list(lse_parts):
+        _ptr(t)
+    _check(_lib.msa_lse_merge(arr_o, arr_l, P, _ptr(out), _ptr(lse), n, Hq, d, _dt(out),
+                              _stream(stream)))

@@ -1,0 +1,70 @@
+"""User-facing calls: allocate outputs with torch, run libmsa's kernels.
+
+``msa_attention`` is the whole window + landmark forward (pool, then fused
+attention); ``ring_attention`` is the one-GPU emulation of a Ring Attention
+layer (per-chunk partials, then the LSE merge).  Both only marshal
+arguments: every arithmetic step runs in libmsa's CUDA kernels.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _binding as B
+
+
+def landmarks(k: torch.Tensor, v: torch.Tensor, n_landmarks: int, stream=None):
+    """Block-mean landmarks K_lm, V_lm [G, Hkv, d] of k, v [n, Hkv, d]."""
+    n, Hkv, d = k.shape
+    k_lm = torch.empty((n_landmarks, Hkv, d), dtype=k.dtype, device=k.device)
+    v_lm = torch.empty_like(k_lm)
+    B.landmark_pool(k, v, k_lm, v_lm, stream=stream)
+    return k_lm, v_lm
+
+
+def msa_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int,
+                  n_landmarks: int, scale: float | None = None,
+                  out_dtype: torch.dtype | None = None, stream=None):
+    """Window + landmark attention forward.
+
+    q [n, Hq, d], k/v [n, Hkv, d] (bf16 or fp32, same dtype, on one GPU).
+    Returns (out [n, Hq, d] in ``out_dtype`` (default: q's dtype),
+    lse [Hq, n] fp32).
+    """
+    n, Hq, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = torch.empty((n, Hq, d), dtype=out_dtype or q.dtype, device=q.device)
+    lse = torch.empty((Hq, n), dtype=torch.float32, device=q.device)
+    if n_landmarks > 0:
+        k_lm, v_lm = landmarks(k, v, n_landmarks, stream=stream)
+    else:
+        k_lm = v_lm = None
+    B.attn_fwd(q, k, v, k_lm, v_lm, out, lse, window, n_landmarks, scale, stream=stream)
+    return out, lse
+
+
+def ring_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_chunks: int,
+                   window: int | None = None, scale: float | None = None,
+                   out_dtype: torch.dtype | None = None, stream=None):
+    """Causal (windowed) attention computed as a Ring Attention layer would:
+    the KV sequence is cut into ``n_chunks`` contiguous chunks, each chunk's
+    partial (O_p fp32, lse_p) is computed against all queries, and the
+    partials are merged by their log-sum-exps.  Returns (out, lse)."""
+    n, Hq, d = q.shape
+    if n % n_chunks != 0:
+        raise ValueError("n must be a multiple of n_chunks")
+    window = n if window is None else window
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    c = n // n_chunks
+    o_parts = [torch.empty((n, Hq, d), dtype=torch.float32, device=q.device)
+               for _ in range(n_chunks)]
+    lse_parts = [torch.empty((Hq, n), dtype=torch.float32, device=q.device)
+                 for _ in range(n_chunks)]
+    for p in range(n_chunks):
+        B.attn_fwd_partial(q, k[p * c:(p + 1) * c], v[p * c:(p + 1) * c], o_parts[p],
+                           lse_parts[p], 0, p * c, window, scale, stream=stream)
+    out = torch.empty((n, Hq, d), dtype=out_dtype or q.dtype, device=q.device)
+    lse = torch.empty((Hq, n), dtype=torch.float32, device=q.device)
+    B.lse_merge(o_parts, lse_parts, out, lse, stream=stream)
+    return out, lse

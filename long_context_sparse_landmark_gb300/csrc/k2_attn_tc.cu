@@ -1,0 +1,544 @@
+// K2 (tensor-core variant): fused window + landmark attention forward for
+// bf16 Q/K/V with d = 128 on sm_103a -- TMA-staged tiles, tcgen05 MMAs with
+// fp32 accumulators in tensor memory (TMEM), online softmax in registers.
+//
+// Method: "Scaling GPU Cluster for Million Token Context", sections "Why
+// Sparse Attention Changes the Game" / "What is Flash-MSA Sparse Attention in
+// GPU Clusters?" (local window + landmark attention fused in one pass, tiled
+// so that the score matrix never reaches HBM; only tiles that hold attended
+// pairs are visited, cf. "skip irrelevant pairs").  Row i attends keys
+// i-w < j <= i and the landmarks whose whole block lies before that window;
+// one softmax over the union.  The running-max/running-sum statistics are
+// those a Ring Attention round aggregates ("Training at 1M+ Token Context",
+// Ring Attention paragraph); with `partial` set the kernel computes one such
+// round's partial against a KV chunk.
+//
+// Work unit = 128 query rows x 2 query heads of one KV group (GQA: both heads
+// read the same K/V tiles, so every K/V tile fetched from L2 feeds two
+// 128x128x128 MMA pairs).  One CTA per unit, 12 warps:
+//   warp 0      TMA producer: Q tiles once, then K and V tiles through a
+//               2-stage ring (landmark tiles first, then window tiles);
+//   warp 1      allocates 512 TMEM columns; one lane issues every MMA:
+//               S_s = Q_s K^T (SS: both from shared memory) and
+//               O_s += P_s V (TS: P from TMEM, V from shared memory);
+//   warps 4-7   softmax of head slot 0 (TMEM lanes 0..127, one row each);
+//   warps 8-11  softmax of head slot 1.
+// TMEM columns: slot s uses [256s, 256s+128) for S (P overwrites its first
+// 64 columns as packed bf16) and [256s+128, 256s+256) for O.
+// MMA issue order per tile t: PV_0(t), S_0(t+1), PV_1(t), S_1(t+1), so the
+// tensor pipe works on one slot while the other slot's softmax runs.
+// S_s(t+1) is issued after PV_s(t), which reads P_s(t) from the same TMEM
+// columns; tcgen05 MMAs from one thread execute in issue order.
+//
+// Softmax: scores are kept in log2 units (scale*log2(e) folded into one FMA);
+// the exponent base m is only raised when the row maximum exceeds it by more
+// than kTau (then O and l are rescaled in TMEM/registers), so p <= 2^kTau;
+// O/l and lse = (m + log2 l) ln 2 are exact for any base.
+//
+// Every mbarrier wait is bounded (globaltimer); a wait that runs out sets a
+// CTA-wide abort flag and the device status word, all roles leave their
+// loops, in-flight TMA copies and MMAs are waited for, TMEM is freed, and the
+// kernel returns.
+#include <cuda.h>
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "msa_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBM = 128;                 // query rows per slot = TMEM lanes
+constexpr int kBN = 128;                 // keys per tile
+constexpr int kSlots = 2;                // query heads per CTA
+constexpr int kThreads = 384;
+constexpr int kChunkBytes = 128 * 128;   // 128 rows x 64 bf16 (one 128-B swizzle span)
+constexpr int kTileBytes = 2 * kChunkBytes;  // 128 rows x 128 bf16
+constexpr int kStages = 2;
+constexpr float kTau = 8.0f;
+constexpr uint64_t kDrainLimitNs = 4000000000ull;
+
+// Shared memory layout (offsets from a 1024-byte aligned base).
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kSlots * kTileBytes;
+constexpr int kOffV = kOffK + kStages * kTileBytes;
+constexpr int kOffBar = kOffV + kStages * kTileBytes;
+constexpr int kNumBars = 16;
+constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
+constexpr int kOffAbort = kOffTmemSlot + 8;
+constexpr int kSmemUsed = kOffAbort + 8;
+constexpr int kSmemBytes = kSmemUsed + 1024;  // alignment slack
+
+// Barrier indices.
+constexpr int BAR_Q = 0;
+__host__ __device__ constexpr int BAR_KF(int s) { return 1 + s; }
+__host__ __device__ constexpr int BAR_KE(int s) { return 3 + s; }
+__host__ __device__ constexpr int BAR_VF(int s) { return 5 + s; }
+__host__ __device__ constexpr int BAR_VE(int s) { return 7 + s; }
+__host__ __device__ constexpr int BAR_SF(int s) { return 9 + s; }
+__host__ __device__ constexpr int BAR_PF(int s) { return 11 + s; }
+__host__ __device__ constexpr int BAR_OD(int s) { return 13 + s; }
+constexpr int BAR_CLEAN = 15;
+
+struct TcParams {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_klm;
+  CUtensorMap tm_vlm;
+  void* out;
+  float* lse;
+  int64_t n_q, q_start, n_kv, kv_start, window, block;
+  int Hq, Hkv, G, group, pairs, n_qtiles;
+  int out_bf16, partial;
+  float scale_log2;
+  int* status;
+  uint64_t wait_ns;
+};
+
+struct WaitCtl {
+  volatile int* abort;
+  int* status;
+  uint64_t limit;
+};
+
+// Bounded wait on phase `parity` of an mbarrier.  Returns false when the
+// CTA is aborting (flag set by another role, or this wait ran out).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl& c) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*c.abort) return false;
+    if (ptx::globaltimer() - t0 > c.limit) {
+      *c.abort = 1;
+      record_status(c.status, MSA_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Wait used while draining: ignores the abort flag, fixed limit.
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, int* status) {
+  if (ptx::mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer() - t0 > kDrainLimitNs) {
+      record_status(status, MSA_ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = ptx::smem_u32(smem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
+  auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8 * i; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work unit: (KV head, query tile, head pair); late query tiles first.
+  int u = blockIdx.x;
+  const int pair = u % p.pairs;
+  u /= p.pairs;
+  const int qt = p.n_qtiles - 1 - (u % p.n_qtiles);
+  const int kvh = u / p.n_qtiles;
+  const int h0 = kvh * p.group + 2 * pair;
+  const int n_slots = (2 * pair + 1 < p.group) ? 2 : 1;
+  const int64_t qr0 = static_cast<int64_t>(qt) * kBM;
+  const int64_t g0 = p.q_start + qr0;
+  const int64_t g_last = p.q_start + min64(qr0 + kBM, p.n_q) - 1;
+  const int64_t kv_end = p.kv_start + p.n_kv;
+  const int64_t j_lo = max64(g0 - p.window + 1, p.kv_start);
+  const int64_t j_hi = min64(g_last, kv_end - 1);
+  int kt_lo = 0, n_win_tiles = 0;
+  if (j_hi >= j_lo) {
+    kt_lo = static_cast<int>((j_lo - p.kv_start) / kBN);
+    n_win_tiles = static_cast<int>((j_hi - p.kv_start) / kBN) - kt_lo + 1;
+  }
+  const int64_t n_lm = visible_landmarks(g_last, p.window, p.block, p.G);
+  const int n_lm_tiles = static_cast<int>((n_lm + kBN - 1) / kBN);
+  const int T = n_lm_tiles + n_win_tiles;
+
+  if (T == 0) {  // no key for any row of this unit (partial chunks only)
+    if (warp >= 4) {
+      const int slot = (warp - 4) >> 2;
+      const int64_t i_loc = qr0 + (warp & 3) * 32 + lane;
+      if (slot < n_slots && i_loc < p.n_q)
+        p.lse[static_cast<int64_t>(h0 + slot) * p.n_q + i_loc] = -INFINITY;
+    }
+    return;
+  }
+
+  WaitCtl ctl{abort_flag, p.status, p.wait_ns};
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(BAR_Q), 1);
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(bar(BAR_KF(s)), 1);
+      ptx::mbar_init(bar(BAR_KE(s)), 1);
+      ptx::mbar_init(bar(BAR_VF(s)), 1);
+      ptx::mbar_init(bar(BAR_VE(s)), 1);
+    }
+    for (int s = 0; s < kSlots; ++s) {
+      ptx::mbar_init(bar(BAR_SF(s)), 1);
+      ptx::mbar_init(bar(BAR_PF(s)), 4);  // one arrive per softmax warp
+      ptx::mbar_init(bar(BAR_OD(s)), 1);
+    }
+    ptx::mbar_init(bar(BAR_CLEAN), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_async_shared();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&p.tm_q);
+      ptx::tma_prefetch_desc(&p.tm_k);
+      ptx::tma_prefetch_desc(&p.tm_v);
+      int k_issued = 0, v_issued = 0;
+      ptx::mbar_arrive_expect_tx(bar(BAR_Q), n_slots * kTileBytes);
+      for (int s = 0; s < n_slots; ++s)
+        for (int c = 0; c < 2; ++c)
+          ptx::tma_load_3d(sb + kOffQ + s * kTileBytes + c * kChunkBytes, &p.tm_q, bar(BAR_Q),
+                           c * 64, h0 + s, static_cast<int>(qr0));
+      for (int t = 0; t < T; ++t) {
+        const int st = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        const bool lm = t < n_lm_tiles;
+        const CUtensorMap* mk = lm ? &p.tm_klm : &p.tm_k;
+        const CUtensorMap* mv = lm ? &p.tm_vlm : &p.tm_v;
+        const int row = lm ? t * kBN : (kt_lo + t - n_lm_tiles) * kBN;
+        if (!wait_bar(bar(BAR_KE(st)), ph ^ 1, ctl)) break;
+        ptx::mbar_arrive_expect_tx(bar(BAR_KF(st)), kTileBytes);
+        for (int c = 0; c < 2; ++c)
+          ptx::tma_load_3d(sb + kOffK + st * kTileBytes + c * kChunkBytes, mk, bar(BAR_KF(st)),
+                           c * 64, kvh, row);
+        k_issued = t + 1;
+        if (!wait_bar(bar(BAR_VE(st)), ph ^ 1, ctl)) break;
+        ptx::mbar_arrive_expect_tx(bar(BAR_VF(st)), kTileBytes);
+        for (int c = 0; c < 2; ++c)
+          ptx::tma_load_3d(sb + kOffV + st * kTileBytes + c * kChunkBytes, mv, bar(BAR_VF(st)),
+                           c * 64, kvh, row);
+        v_issued = t + 1;
+      }
+      // Drain: every copy this thread issued must have landed before exit.
+      drain_bar(bar(BAR_Q), 0, p.status);
+      for (int s = 0; s < kStages; ++s) {
+        int last = k_issued - 1;
+        if (last >= 0 && (last & 1) != s) --last;
+        if (last >= 0) drain_bar(bar(BAR_KF(s)), (last >> 1) & 1, p.status);
+        last = v_issued - 1;
+        if (last >= 0 && (last & 1) != s) --last;
+        if (last >= 0) drain_bar(bar(BAR_VF(s)), (last >> 1) & 1, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBM, kBN, false);
+      constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kBM, kD, true);
+      auto issue_s = [&](int slot, int t) {
+        const uint32_t qa = sb + kOffQ + slot * kTileBytes;
+        const uint32_t kb = sb + kOffK + (t & 1) * kTileBytes;
+        const uint32_t d = tmem + slot * 256;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+          ptx::mma_ss(d, ptx::smem_desc_sw128(qa + off, 16, 1024),
+                      ptx::smem_desc_sw128(kb + off, 16, 1024), kIdescS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int slot, int t) {
+        const uint32_t vb = sb + kOffV + (t & 1) * kTileBytes;
+        const uint32_t d = tmem + slot * 256 + 128;
+        const uint32_t pa = tmem + slot * 256;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          ptx::mma_ts(d, pa + kk * 8, ptx::smem_desc_sw128(vb + kk * 2048, kChunkBytes, 1024),
+                      kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = wait_bar(bar(BAR_Q), 0, ctl);
+      if (ok) ok = wait_bar(bar(BAR_KF(0)), 0, ctl);
+      if (ok) {
+        ptx::tc_fence_after();
+        for (int s = 0; s < n_slots; ++s) {
+          issue_s(s, 0);
+          ptx::mma_commit(bar(BAR_SF(s)));
+        }
+        ptx::mma_commit(bar(BAR_KE(0)));
+      }
+      for (int t = 0; ok && t < T; ++t) {
+        const int st = t & 1;
+        const bool nxt = t + 1 < T;
+        if (!(ok = wait_bar(bar(BAR_VF(st)), (t >> 1) & 1, ctl))) break;
+        for (int s = 0; s < n_slots; ++s) {
+          if (!(ok = wait_bar(bar(BAR_PF(s)), t & 1, ctl))) break;
+          ptx::tc_fence_after();
+          issue_pv(s, t);
+          if (nxt) {
+            if (s == 0) {
+              if (!(ok = wait_bar(bar(BAR_KF(st ^ 1)), ((t + 1) >> 1) & 1, ctl))) break;
+              ptx::tc_fence_after();
+            }
+            issue_s(s, t + 1);
+            ptx::mma_commit(bar(BAR_SF(s)));
+          } else {
+            ptx::mma_commit(bar(BAR_OD(s)));
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar(BAR_VE(st)));
+        if (nxt) ptx::mma_commit(bar(BAR_KE(st ^ 1)));
+      }
+      // Drain: all MMAs issued so far complete before TMEM is released.
+      ptx::mma_commit(bar(BAR_CLEAN));
+      drain_bar(bar(BAR_CLEAN), 0, p.status);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int slot = (warp - 4) >> 2;
+    const int wq = warp & 3;
+    if (slot < n_slots) {
+      const int64_t i_loc = qr0 + wq * 32 + lane;
+      const bool row_ok = i_loc < p.n_q;
+      const int64_t i = p.q_start + i_loc;
+      const int h = h0 + slot;
+      const uint32_t tS = tmem + slot * 256 + (static_cast<uint32_t>(wq * 32) << 16);
+      const uint32_t tO = tS + 128;
+      const int64_t my_lo = max64(i - p.window + 1, p.kv_start);
+      const int64_t my_hi = min64(i, kv_end - 1);
+      const int64_t my_lm = visible_landmarks(i, p.window, p.block, p.G);
+      const float sl2 = p.scale_log2;
+      float m_used = -INFINITY;
+      float l = 0.f;
+      bool ok = true;
+      for (int t = 0; t < T; ++t) {
+        ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF(slot)), t & 1, ctl));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        float s[128];
+        ptx::tmem_ld32(tS + 0, *reinterpret_cast<float(*)[32]>(&s[0]));
+        ptx::tmem_ld32(tS + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
+        ptx::tmem_ld32(tS + 64, *reinterpret_cast<float(*)[32]>(&s[64]));
+        ptx::tmem_ld32(tS + 96, *reinterpret_cast<float(*)[32]>(&s[96]));
+        ptx::tmem_wait_ld();
+        // Valid columns [lo, hi) of this tile for this row.
+        int64_t lo, hi;
+        if (t < n_lm_tiles) {
+          lo = 0;
+          hi = my_lm - static_cast<int64_t>(t) * kBN;
+        } else {
+          const int64_t kb = p.kv_start + static_cast<int64_t>(kt_lo + t - n_lm_tiles) * kBN;
+          lo = my_lo - kb;
+          hi = my_hi - kb + 1;
+        }
+        if (!row_ok) hi = lo;
+        if (lo > 0 || hi < kBN) {
+          const int lo_c = static_cast<int>(max64(0, min64(kBN, lo)));
+          const int hi_c = static_cast<int>(max64(0, min64(kBN, hi)));
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = (c >= lo_c && c < hi_c) ? s[c] : -INFINITY;
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        const float m_new = fmaxf(m_used, mx * sl2);
+        const bool need = m_new > m_used + kTau;
+        if (need) {
+          const float alpha = ptx::ex2(m_used - m_new);  // 0 when m_used = -inf
+          l *= alpha;
+        }
+        if (t > 0 && __any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ptx::ex2(m_used - m_new) : 1.f;
+#pragma unroll 1
+          for (int cc = 0; cc < 8; ++cc) {
+            float o[16];
+            ptx::tmem_ld16(tO + cc * 16, o);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] *= alpha;
+            ptx::tmem_st16(tO + cc * 16, *reinterpret_cast<uint32_t(*)[16]>(o));
+          }
+        }
+        if (need) m_used = m_new;
+        const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ptx::ex2(fmaf(s[cc * 32 + 2 * e], sl2, -mb));
+            const float p1 = ptx::ex2(fmaf(s[cc * 32 + 2 * e + 1], sl2, -mb));
+            l += p0 + p1;
+            pk[e] = ptx::pack_bf16x2(p0, p1);
+          }
+          ptx::tmem_st16(tS + cc * 16, pk);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(BAR_PF(slot)));
+      }
+      if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_OD(slot)), 0, ctl));
+      if (ok) {
+        ptx::tc_fence_after();
+        const bool has = row_ok && l > 0.f;
+        const float inv = has ? 1.f / l : 0.f;
+        const int64_t obase = (i_loc * p.Hq + h) * static_cast<int64_t>(kD);
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          ptx::tmem_ld32(tO + cc * 32, o);
+          ptx::tmem_wait_ld();
+          if (has) {
+            if (p.out_bf16) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + obase + cc * 32);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint4 w;
+                w.x = ptx::pack_bf16x2(o[8 * v + 0] * inv, o[8 * v + 1] * inv);
+                w.y = ptx::pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv);
+                w.z = ptx::pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv);
+                w.w = ptx::pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv);
+                dst[v] = w;
+              }
+            } else {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + cc * 32);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                dst[v] = make_float4(o[4 * v] * inv, o[4 * v + 1] * inv, o[4 * v + 2] * inv,
+                                     o[4 * v + 3] * inv);
+            }
+          }
+        }
+        if (row_ok) {
+          p.lse[static_cast<int64_t>(h) * p.n_q + i_loc] =
+              l > 0.f ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// [rows, H, 128] bf16 tensor, boxes of 64 (d) x 1 (head) x 128 (rows),
+// 128-byte swizzle: each box lands as 128 rows of 128 bytes, the canonical
+// K-major SW128 layout for Q/K and the MN-major SW128 layout for V.
+bool encode_map(EncodeTiledFn fn, CUtensorMap* m, const void* ptr, int64_t rows, int H) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
+                           static_cast<cuuint64_t>(H) * kD * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool attn_tc_supported(int Hq, int Hkv, int d, int in_bf16) {
+  (void)Hq;
+  (void)Hkv;
+  return in_bf16 && d == kD;
+}
+
+cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s, const char** why) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) {
+    *why = "cuTensorMapEncodeTiled is not available from the driver";
+    return cudaErrorNotSupported;
+  }
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  const bool ok = encode_map(fn, &p.tm_q, a.q, a.n_q, a.Hq) &&
+                  encode_map(fn, &p.tm_k, a.k, a.n_kv, a.Hkv) &&
+                  encode_map(fn, &p.tm_v, a.v, a.n_kv, a.Hkv) &&
+                  (a.G > 0 ? encode_map(fn, &p.tm_klm, a.k_lm, a.G, a.Hkv) &&
+                                 encode_map(fn, &p.tm_vlm, a.v_lm, a.G, a.Hkv)
+                           : true);
+  if (!ok) {
+    *why = "cuTensorMapEncodeTiled rejected a tensor (alignment or size)";
+    return cudaErrorInvalidValue;
+  }
+  if (a.G == 0) {
+    p.tm_klm = p.tm_k;
+    p.tm_vlm = p.tm_v;
+  }
+  p.out = a.out;
+  p.lse = a.lse;
+  p.n_q = a.n_q;
+  p.q_start = a.q_start;
+  p.n_kv = a.n_kv;
+  p.kv_start = a.kv_start;
+  p.window = a.window;
+  p.block = a.block;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.G = a.G;
+  p.group = a.Hq / a.Hkv;
+  p.pairs = (p.group + 1) / 2;
+  p.n_qtiles = static_cast<int>((a.n_q + kBM - 1) / kBM);
+  p.out_bf16 = a.out_bf16;
+  p.partial = a.partial;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.status = a.status;
+  p.wait_ns = a.wait_limit_ns;
+
+  cudaError_t attr_err = cudaFuncSetAttribute(
+      attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (attr_err != cudaSuccess) return attr_err;
+  const int64_t units = static_cast<int64_t>(a.Hkv) * p.pairs * p.n_qtiles;
+  attn_tc_kernel<<<static_cast<unsigned>(units), kThreads, kSmemBytes, s>>>(p);
+  return cudaPeekAtLastError();
+}
+
+}  // namespace msa

@@ -1,0 +1,265 @@
+// C ABI of libmsa: argument validation, kernel selection and launch.
+// Every entry point validates all arguments before enqueueing anything and
+// never allocates or synchronises (msa_device_status excepted, which reads
+// the status word and says so).
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+
+#include "msa_common.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+msa_status fail(msa_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+msa_status ok() {
+  g_last_error.clear();
+  return MSA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dtype(msa_dtype d) { return d == MSA_F32 || d == MSA_BF16; }
+
+// Per-device status word written by kernels when a bounded wait runs out.
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mu;
+int* g_status_ptr[kMaxDevices] = {};
+
+std::atomic<uint64_t> g_wait_limit_ns{0};
+constexpr uint64_t kDefaultWaitNs = 4000000000ull;
+
+msa_status device_status_ptr(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(MSA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_status);
+    if (e != cudaSuccess)
+      return fail(MSA_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return MSA_OK;
+}
+
+msa_status launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
+  return ok();
+}
+
+msa_status check_attn_common(const void* q, const void* k, const void* v, const void* out,
+                             const float* lse, int Hq, int Hkv, int d, int64_t window,
+                             float scale, msa_dtype in_dt) {
+  if (!q || !k || !v || !out || !lse) return fail(MSA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return fail(MSA_ERR_INVALID_ARG, "tensor pointer not 16-byte aligned");
+  if (Hq < 1 || Hkv < 1) return fail(MSA_ERR_INVALID_ARG, "Hq=%d Hkv=%d must be >= 1", Hq, Hkv);
+  if (Hq % Hkv != 0) return fail(MSA_ERR_INVALID_ARG, "Hq=%d not a multiple of Hkv=%d", Hq, Hkv);
+  if (window < 1) return fail(MSA_ERR_INVALID_ARG, "window=%lld must be >= 1", (long long)window);
+  if (!(scale > 0.f) || !isfinite(scale))
+    return fail(MSA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (!valid_dtype(in_dt)) return fail(MSA_ERR_INVALID_ARG, "bad input dtype %d", (int)in_dt);
+  if (d != 64 && d != 128) return fail(MSA_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+  return MSA_OK;
+}
+
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 256;  // TMA coordinates are 32-bit
+
+msa_status run_attn(const msa::AttnArgs& a0, cudaStream_t stream) {
+  msa::AttnArgs a = a0;
+  msa_status st = device_status_ptr(&a.status);
+  if (st != MSA_OK) return st;
+  const uint64_t lim = g_wait_limit_ns.load();
+  a.wait_limit_ns = lim ? lim : kDefaultWaitNs;
+  if (msa::attn_tc_supported(a.Hq, a.Hkv, a.d, a.in_bf16)) {
+    const char* why = nullptr;
+    cudaError_t e = msa::launch_attn_tc(a, stream, &why);
+    if (e != cudaSuccess && why) return fail(MSA_ERR_CUDA, "tensor-core attention: %s", why);
+    return launched(e, "tensor-core attention");
+  }
+  return launched(msa::launch_attn_simt(a, stream), "attention");
+}
+
+}  // namespace
+
+extern "C" {
+
+int msa_version(void) { return 100; }
+
+const char* msa_last_error_string(void) { return g_last_error.c_str(); }
+
+msa_status msa_landmark_pool(const void* k, const void* v, void* k_lm, void* v_lm, int64_t n,
+                             int Hkv, int d, int n_landmarks, msa_dtype dt, msa_stream_t stream) {
+  if (!k || !v || !k_lm || !v_lm) return fail(MSA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_lm) || !aligned16(v_lm))
+    return fail(MSA_ERR_INVALID_ARG, "tensor pointer not 16-byte aligned");
+  if (n < 1 || Hkv < 1) return fail(MSA_ERR_INVALID_ARG, "n=%lld Hkv=%d", (long long)n, Hkv);
+  if (n_landmarks < 1 || n_landmarks > n || n % n_landmarks != 0)
+    return fail(MSA_ERR_INVALID_ARG, "G=%d must satisfy 1 <= G <= n and n %% G == 0 (n=%lld)",
+                n_landmarks, (long long)n);
+  if (!valid_dtype(dt)) return fail(MSA_ERR_INVALID_ARG, "bad dtype %d", (int)dt);
+  if (d != 64 && d != 128) return fail(MSA_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+  msa::PoolArgs a{k, v, k_lm, v_lm, n, Hkv * d, n_landmarks, dt == MSA_BF16 ? 1 : 0};
+  return launched(msa::launch_landmark_pool(a, reinterpret_cast<cudaStream_t>(stream)),
+                  "landmark pool");
+}
+
+msa_status msa_attn_fwd(const void* q, const void* k, const void* v, const void* k_lm,
+                        const void* v_lm, void* out, float* lse, int64_t n, int Hq, int Hkv, int d,
+                        int64_t window, int n_landmarks, float scale, msa_dtype in_dt,
+                        msa_dtype out_dt, msa_stream_t stream) {
+  msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, window, scale, in_dt);
+  if (st != MSA_OK) return st;
+  if (n < 1 || n > kMaxRows) return fail(MSA_ERR_INVALID_ARG, "n=%lld out of range", (long long)n);
+  if (!valid_dtype(out_dt)) return fail(MSA_ERR_INVALID_ARG, "bad output dtype %d", (int)out_dt);
+  if (n_landmarks < 0 || n_landmarks > n || (n_landmarks > 0 && n % n_landmarks != 0))
+    return fail(MSA_ERR_INVALID_ARG, "G=%d must satisfy 0 <= G <= n and n %% G == 0 (n=%lld)",
+                n_landmarks, (long long)n);
+  if (n_landmarks > 0) {
+    if (!k_lm || !v_lm) return fail(MSA_ERR_INVALID_ARG, "null landmark pointer with G > 0");
+    if (!aligned16(k_lm) || !aligned16(v_lm))
+      return fail(MSA_ERR_INVALID_ARG, "landmark pointer not 16-byte aligned");
+  }
+  msa::AttnArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.k_lm = n_landmarks > 0 ? k_lm : nullptr;
+  a.v_lm = n_landmarks > 0 ? v_lm : nullptr;
+  a.out = out;
+  a.lse = lse;
+  a.n_q = n;
+  a.q_start = 0;
+  a.n_kv = n;
+  a.kv_start = 0;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.window = window;
+  a.G = n_landmarks;
+  a.block = n_landmarks > 0 ? n / n_landmarks : 1;
+  a.scale = scale;
+  a.in_bf16 = in_dt == MSA_BF16;
+  a.out_bf16 = out_dt == MSA_BF16;
+  a.partial = 0;
+  return run_attn(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_attn_fwd_partial(const void* q, const void* k_chunk, const void* v_chunk,
+                                 float* out_part, float* lse_part, int64_t n_q, int64_t q_start,
+                                 int64_t n_kv, int64_t kv_start, int Hq, int Hkv, int d,
+                                 int64_t window, float scale, msa_dtype in_dt,
+                                 msa_stream_t stream) {
+  msa_status st =
+      check_attn_common(q, k_chunk, v_chunk, out_part, lse_part, Hq, Hkv, d, window, scale, in_dt);
+  if (st != MSA_OK) return st;
+  if (n_q < 1 || n_q > kMaxRows || n_kv < 1 || n_kv > kMaxRows)
+    return fail(MSA_ERR_INVALID_ARG, "n_q=%lld n_kv=%lld out of range", (long long)n_q,
+                (long long)n_kv);
+  if (q_start < 0 || kv_start < 0)
+    return fail(MSA_ERR_INVALID_ARG, "q_start=%lld kv_start=%lld must be >= 0",
+                (long long)q_start, (long long)kv_start);
+  msa::AttnArgs a{};
+  a.q = q;
+  a.k = k_chunk;
+  a.v = v_chunk;
+  a.out = out_part;
+  a.lse = lse_part;
+  a.n_q = n_q;
+  a.q_start = q_start;
+  a.n_kv = n_kv;
+  a.kv_start = kv_start;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.window = window;
+  a.G = 0;
+  a.block = 1;
+  a.scale = scale;
+  a.in_bf16 = in_dt == MSA_BF16;
+  a.out_bf16 = 0;
+  a.partial = 1;
+  return run_attn(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_lse_merge(const float* const* o_parts, const float* const* lse_parts, int n_parts,
+                         void* out, float* lse, int64_t n, int Hq, int d, msa_dtype out_dt,
+                         msa_stream_t stream) {
+  if (!o_parts || !lse_parts || !out || !lse)
+    return fail(MSA_ERR_INVALID_ARG, "null array or output pointer");
+  if (n_parts < 1 || n_parts > MSA_MAX_MERGE_PARTS)
+    return fail(MSA_ERR_INVALID_ARG, "n_parts=%d (1..%d)", n_parts, MSA_MAX_MERGE_PARTS);
+  if (n < 1 || Hq < 1) return fail(MSA_ERR_INVALID_ARG, "n=%lld Hq=%d", (long long)n, Hq);
+  if (d < 4 || d % 4 != 0) return fail(MSA_ERR_INVALID_ARG, "d=%d must be a multiple of 4", d);
+  if (!valid_dtype(out_dt)) return fail(MSA_ERR_INVALID_ARG, "bad output dtype %d", (int)out_dt);
+  if (!aligned16(out) || !aligned16(lse))
+    return fail(MSA_ERR_INVALID_ARG, "output pointer not 16-byte aligned");
+  msa::MergeArgs a{};
+  for (int p = 0; p < n_parts; ++p) {
+    if (!o_parts[p] || !lse_parts[p]) return fail(MSA_ERR_INVALID_ARG, "null partial %d", p);
+    if (!aligned16(o_parts[p]) || !aligned16(lse_parts[p]))
+      return fail(MSA_ERR_INVALID_ARG, "partial %d not 16-byte aligned", p);
+    if (static_cast<const void*>(o_parts[p]) == out && (p > 0 || out_dt != MSA_F32))
+      return fail(MSA_ERR_INVALID_ARG, "out may alias only o_parts[0], and only with fp32 output");
+    if (lse_parts[p] == lse && p > 0)
+      return fail(MSA_ERR_INVALID_ARG, "lse may alias only lse_parts[0]");
+    a.o_parts[p] = o_parts[p];
+    a.lse_parts[p] = lse_parts[p];
+  }
+  a.n_parts = n_parts;
+  a.out = out;
+  a.lse = lse;
+  a.n = n;
+  a.Hq = Hq;
+  a.d = d;
+  a.out_bf16 = out_dt == MSA_BF16;
+  return launched(msa::launch_lse_merge(a, reinterpret_cast<cudaStream_t>(stream)), "lse merge");
+}
+
+int msa_attn_uses_tensor_cores(int Hq, int Hkv, int d, msa_dtype in_dt) {
+  return msa::attn_tc_supported(Hq, Hkv, d, in_dt == MSA_BF16) ? 1 : 0;
+}
+
+msa_status msa_device_status(int clear) {
+  int* ptr = nullptr;
+  msa_status st = device_status_ptr(&ptr);
+  if (st != MSA_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+  int v = 0;
+  e = cudaMemcpy(&v, ptr, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (clear) {
+    const int zero = 0;
+    e = cudaMemcpy(ptr, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
+  }
+  if (v == MSA_ERR_TIMEOUT) return fail(MSA_ERR_TIMEOUT, "a bounded device wait ran out");
+  if (v != 0) return fail(static_cast<msa_status>(v), "device status %d", v);
+  return ok();
+}
+
+void msa_debug_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns); }
+
+}  // extern "C"

@@ -1,0 +1,90 @@
+// Shared device/host helpers of libmsa (CUDA path only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "msa.h"
+
+namespace msa {
+
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+// Number of visible landmarks for global row `pos`: the count of blocks l
+// with (l+1)*B <= pos - w + 1, i.e. clamp(floor((pos-w+1)/B), 0, G).
+__host__ __device__ __forceinline__ int64_t visible_landmarks(int64_t pos, int64_t window,
+                                                              int64_t block, int G) {
+  if (G <= 0) return 0;
+  int64_t x = pos - window + 1;
+  if (x < block) return 0;
+  int64_t c = x / block;
+  return c < G ? c : G;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Launch helpers implemented per translation unit; all return cudaError_t of
+// the launch (cudaPeekAtLastError) and never synchronise.
+struct PoolArgs {
+  const void* k;
+  const void* v;
+  void* k_lm;
+  void* v_lm;
+  int64_t n;
+  int C;  // Hkv * d elements per token
+  int G;
+  int bf16;
+};
+cudaError_t launch_landmark_pool(const PoolArgs& a, cudaStream_t s);
+
+struct MergeArgs {
+  const float* o_parts[MSA_MAX_MERGE_PARTS];
+  const float* lse_parts[MSA_MAX_MERGE_PARTS];
+  int n_parts;
+  void* out;
+  float* lse;
+  int64_t n;
+  int Hq;
+  int d;
+  int out_bf16;
+};
+cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t s);
+
+struct AttnArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* k_lm;
+  const void* v_lm;
+  void* out;
+  float* lse;
+  int64_t n_q;
+  int64_t q_start;
+  int64_t n_kv;
+  int64_t kv_start;
+  int Hq;
+  int Hkv;
+  int d;
+  int64_t window;
+  int G;
+  int64_t block;  // landmark block size B (1 when G == 0)
+  float scale;
+  int in_bf16;
+  int out_bf16;
+  int partial;  // rows with no key: lse = -inf, out row untouched
+  int* status;  // device status word
+  uint64_t wait_limit_ns;
+};
+cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s, const char** why);
+bool attn_tc_supported(int Hq, int Hkv, int d, int in_bf16);
+
+}  // namespace msa

@@ -100,14 +100,18 @@ def landmark_pool(x: np.ndarray, n_landmarks: int) -> np.ndarray:
 
 def attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int,
          n_landmarks: int, scale: float, rows=None, q_start: int = 0,
-         kv_start: int = 0, n_total: int | None = None):
+         kv_start: int = 0, q_positions=None, landmarks=None):
     """Window + landmark attention in fp64.
 
     q: [n_q, Hq, d] query rows at global positions q_start + index; k, v:
     [n_kv, Hkv, d] at global positions kv_start + index.  ``rows`` selects a
-    subset of q's rows (indices into q).  Landmarks (G = n_landmarks > 0)
-    are the block means of k and v over n_total = len(k) tokens, which
-    requires kv_start == 0.  Returns (O [n_rows, Hq, d], lse [Hq, n_rows]).
+    subset of q's rows (indices into q).  Alternatively ``q_positions`` gives
+    the global position of every row of q (q then holds exactly those rows,
+    e.g. a gathered sample).  Landmarks (G = n_landmarks > 0) are the block
+    means of k and v over the whole sequence, which requires kv_start == 0;
+    ``landmarks=(k_lm, v_lm)`` passes ones already computed by
+    ``landmark_pool`` for these k, v.
+    Returns (O [n_rows, Hq, d], lse [Hq, n_rows]).
     """
     q = np.ascontiguousarray(q)
     k = np.ascontiguousarray(k)
@@ -117,25 +121,40 @@ def attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int,
         raise TypeError("q, k, v must share one dtype")
     n_q, Hq, d = q.shape
     n_kv, Hkv, _ = k.shape
-    if rows is None:
-        rows = np.arange(n_q, dtype=np.int64)
-    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
-    qg = np.ascontiguousarray(q[rows]) if len(rows) != n_q or not np.array_equal(rows, np.arange(n_q)) else q
-    pos = np.ascontiguousarray(rows + int(q_start), dtype=np.int64)
+    if q_positions is not None:
+        if rows is not None:
+            raise ValueError("give rows or q_positions, not both")
+        pos = np.ascontiguousarray(np.asarray(q_positions, dtype=np.int64))
+        if len(pos) != n_q:
+            raise ValueError("q_positions must have one entry per row of q")
+        qg = q
+    else:
+        if rows is None:
+            rows = np.arange(n_q, dtype=np.int64)
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        qg = np.ascontiguousarray(q[rows])
+        pos = np.ascontiguousarray(rows + int(q_start), dtype=np.int64)
+    n_rows = len(pos)
     G = int(n_landmarks)
     if G > 0:
         if kv_start != 0:
             raise ValueError("landmarks need the whole sequence (kv_start == 0)")
-        k_lm = landmark_pool(k, G)
-        v_lm = landmark_pool(v, G)
+        if landmarks is None:
+            k_lm = landmark_pool(k, G)
+            v_lm = landmark_pool(v, G)
+        else:
+            k_lm = np.ascontiguousarray(landmarks[0], dtype=np.float64)
+            v_lm = np.ascontiguousarray(landmarks[1], dtype=np.float64)
+            if k_lm.shape != (G, Hkv, d) or v_lm.shape != (G, Hkv, d):
+                raise ValueError("landmarks must be [G, Hkv, d]")
         B = n_kv // G
         lm_k, lm_v = _ptr(k_lm), _ptr(v_lm)
     else:
         B = 1
         lm_k = lm_v = None
-    out = np.empty((len(rows), Hq, d), dtype=np.float64)
-    lse = np.empty((Hq, len(rows)), dtype=np.float64)
-    rc = _load().oracle_attn_rows(_ptr(qg), _ptr(pos), len(rows), _ptr(k),
+    out = np.empty((n_rows, Hq, d), dtype=np.float64)
+    lse = np.empty((Hq, n_rows), dtype=np.float64)
+    rc = _load().oracle_attn_rows(_ptr(qg), _ptr(pos), n_rows, _ptr(k),
                                   _ptr(v), n_kv, int(kv_start), dt, Hq, Hkv, d,
                                   int(window), lm_k, lm_v, G, B, float(scale),
                                   _ptr(out), _ptr(lse))

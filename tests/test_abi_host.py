@@ -1,0 +1,127 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every function include/msa.h declares, and
+reject bad arguments with the documented status codes before it touches
+the GPU (validation precedes any CUDA call).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from long_context_sparse_landmark_gb300 import build
+    path = build.build()
+    from long_context_sparse_landmark_gb300 import _binding
+    return _binding.load_library(path)
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(msa_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"msa_attn_fwd", "msa_landmark_pool", "msa_lse_merge"} <= names
+    for name in names:
+        assert hasattr(lib, name), name
+    from long_context_sparse_landmark_gb300 import _binding
+    assert set(_binding.EXPORTS) == names
+
+
+def test_version(lib):
+    assert lib.msa_version() == 100
+
+
+P = ctypes.c_void_p
+GOOD = P(1 << 20)        # never dereferenced: validation fails first
+BAD_ALIGN = P((1 << 20) + 8)
+
+
+def _err(lib):
+    return lib.msa_last_error_string().decode()
+
+
+def test_pool_validation(lib):
+    f = lib.msa_landmark_pool
+    assert f(None, GOOD, GOOD, GOOD, 128, 1, 64, 4, 0, None) == 1
+    assert f(GOOD, GOOD, BAD_ALIGN, GOOD, 128, 1, 64, 4, 0, None) == 1
+    assert f(GOOD, GOOD, GOOD, GOOD, 0, 1, 64, 4, 0, None) == 1
+    assert f(GOOD, GOOD, GOOD, GOOD, 128, 1, 64, 3, 0, None) == 1   # n % G != 0
+    assert "G=3" in _err(lib)
+    assert f(GOOD, GOOD, GOOD, GOOD, 128, 1, 64, 0, 0, None) == 1   # G < 1
+    assert f(GOOD, GOOD, GOOD, GOOD, 128, 1, 64, 256, 0, None) == 1  # G > n
+    assert f(GOOD, GOOD, GOOD, GOOD, 128, 1, 64, 4, 7, None) == 1   # dtype
+    assert f(GOOD, GOOD, GOOD, GOOD, 128, 1, 96, 4, 0, None) == 2   # d unsupported
+
+
+def _attn(lib, **kw):
+    a = dict(q=GOOD, k=GOOD, v=GOOD, klm=GOOD, vlm=GOOD, out=GOOD, lse=GOOD, n=256, Hq=4,
+             Hkv=2, d=128, w=16, G=4, scale=0.125, idt=1, odt=0)
+    a.update(kw)
+    return lib.msa_attn_fwd(a["q"], a["k"], a["v"], a["klm"], a["vlm"], a["out"], a["lse"],
+                            a["n"], a["Hq"], a["Hkv"], a["d"], a["w"], a["G"],
+                            ctypes.c_float(a["scale"]), a["idt"], a["odt"], None)
+
+
+def test_attn_validation(lib):
+    assert _attn(lib, q=None) == 1
+    assert _attn(lib, lse=BAD_ALIGN) == 1
+    assert _attn(lib, n=0) == 1
+    assert _attn(lib, w=0) == 1
+    assert _attn(lib, Hq=3, Hkv=2) == 1
+    assert _attn(lib, Hkv=0) == 1
+    assert _attn(lib, G=3) == 1       # 256 % 3
+    assert _attn(lib, G=-1) == 1
+    assert _attn(lib, G=512) == 1     # G > n
+    assert _attn(lib, klm=None) == 1  # G > 0 needs landmarks
+    assert _attn(lib, scale=0.0) == 1
+    assert _attn(lib, scale=float("nan")) == 1
+    assert _attn(lib, idt=5) == 1
+    assert _attn(lib, odt=5) == 1
+    assert _attn(lib, d=96) == 2
+    assert "d=96" in _err(lib)
+
+
+def test_partial_validation(lib):
+    f = lib.msa_attn_fwd_partial
+
+    def call(**kw):
+        a = dict(q=GOOD, k=GOOD, v=GOOD, o=GOOD, l=GOOD, nq=128, qs=0, nkv=64, kvs=0, Hq=2, Hkv=1,
+                 d=128, w=128, idt=1)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["o"], a["l"], a["nq"], a["qs"], a["nkv"], a["kvs"],
+                 a["Hq"], a["Hkv"], a["d"], a["w"], ctypes.c_float(0.1), a["idt"], None)
+
+    assert call(o=None) == 1
+    assert call(nq=0) == 1
+    assert call(nkv=0) == 1
+    assert call(qs=-1) == 1
+    assert call(kvs=-5) == 1
+    assert call(d=32) == 2
+
+
+def test_merge_validation(lib):
+    f = lib.msa_lse_merge
+    arr = (ctypes.c_void_p * 2)(1 << 20, 2 << 20)
+    larr = (ctypes.c_void_p * 2)(3 << 20, 4 << 20)
+    assert f(None, larr, 2, GOOD, GOOD, 16, 2, 8, 0, None) == 1
+    assert f(arr, larr, 0, GOOD, GOOD, 16, 2, 8, 0, None) == 1
+    assert f(arr, larr, 65, GOOD, GOOD, 16, 2, 8, 0, None) == 1
+    assert f(arr, larr, 2, GOOD, GOOD, 16, 2, 6, 0, None) == 1      # d % 4
+    assert f(arr, larr, 2, P(2 << 20), GOOD, 16, 2, 8, 0, None) == 1  # out aliases part 1
+    assert f(arr, larr, 2, P(1 << 20), GOOD, 16, 2, 8, 1, None) == 1  # bf16 out aliasing
+    assert f(arr, larr, 2, GOOD, P(4 << 20), 16, 2, 8, 0, None) == 1  # lse aliases part 1
+    bad = (ctypes.c_void_p * 2)(1 << 20, (2 << 20) + 4)
+    assert f(bad, larr, 2, P(5 << 20), P(6 << 20), 16, 2, 8, 0, None) == 1

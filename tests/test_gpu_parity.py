@@ -1,0 +1,255 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs -- landmark pooling, the fused window + landmark
+attention (tensor-core kernel for bf16 / d=128, CUDA-core kernel otherwise),
+Ring Attention partials and their LSE merge.  Small cases span several tiles
+and ragged tails; the five workloads run in the launch configuration the
+benchmark times, on all rows where the oracle finishes in seconds and on a
+fixed row sample otherwise."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_sparse_landmark_gb300.workloads import (WORKLOADS, Workload, generate,
+                                                          sample_rows, to_numpy_bits)
+from tests.gpu_helpers import (bf16_round, bf16_ulp, binding, compare, gather_rows,
+                               oracle_attention, run_gpu_attention, tol)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _oracle_threads():
+    import os
+    oracle.set_threads(os.cpu_count() or 1)
+
+
+# ------------------------------------------------------------------ pooling
+POOL_CASES = [(2048, 1, 64, 16, "f32"), (2048, 2, 128, 16, "bf16"), (32768, 1, 128, 512, "bf16"),
+              (1000, 2, 64, 8, "f32"), (129, 1, 128, 129, "bf16"), (128, 3, 64, 1, "bf16"),
+              (131072, 8, 128, 512, "bf16")]
+
+
+@pytest.mark.parametrize("n,Hkv,d,G,dt", POOL_CASES)
+def test_landmark_pool_parity(n, Hkv, d, G, dt):
+    B = binding()
+    wl = Workload("pool", n, Hkv, Hkv, d, 1, G, dt, seed=n + G)
+    _, k, v = generate(wl, device=DEV)
+    k_lm = torch.empty((G, Hkv, d), dtype=k.dtype, device=DEV)
+    v_lm = torch.empty_like(k_lm)
+    B.landmark_pool(k, v, k_lm, v_lm)
+    torch.cuda.synchronize()
+    for got, src in ((k_lm, k), (v_lm, v)):
+        ref = oracle.landmark_pool(to_numpy_bits(src), G)
+        g = got.float().cpu().numpy().astype(np.float64)
+        if dt == "f32":
+            compare(g, ref, 2e-6, 2e-7, f"pool f32 n={n}")
+        else:
+            # fp32 mean rounded to bf16: within one bf16 spacing of the exact mean
+            assert np.all(np.abs(g - ref) <= bf16_ulp(bf16_round(ref))), f"pool bf16 n={n}"
+
+
+# ------------------------------------------------------------------ attention, small grid
+def _small_cases():
+    heads = [(1, 1), (2, 1), (8, 1), (4, 2), (6, 6), (8, 2)]
+    cases = []
+    idx = 0
+    for dt, d in (("bf16", 128), ("f32", 64), ("f32", 128), ("bf16", 64)):
+        for n, G in ((1, 0), (1, 1), (127, 0), (127, 127), (128, 1), (128, 16), (129, 0),
+                     (129, 3), (640, 5), (1000, 8), (1000, 1000)):
+            B = n // G if G else n
+            for w in sorted({1, max(1, B - 1), B, n, 300}):
+                Hq, Hkv = heads[idx % len(heads)]
+                idx += 1
+                cases.append((dt, d, n, G, w, Hq, Hkv))
+    return cases
+
+
+@pytest.mark.parametrize("dt,d,n,G,w,Hq,Hkv", _small_cases())
+def test_attention_small_grid(dt, d, n, G, w, Hq, Hkv):
+    B = binding()
+    wl = Workload("small", n, Hq, Hkv, d, w, G, dt, seed=7 * n + G + w)
+    q, k, v = generate(wl, device=DEV)
+    out, lse = run_gpu_attention(q, k, v, wl)
+    torch.cuda.synchronize()
+    ro, rl = oracle_attention(q, k, v, wl)
+    mx, mean = tol(dt)
+    compare(out.cpu().numpy(), ro, mx, mean, f"O {wl}")
+    compare(lse.cpu().numpy(), rl, mx, mean, f"lse {wl}")
+    assert B.uses_tensor_cores(Hq, Hkv, d, q.dtype) == (dt == "bf16" and d == 128)
+
+
+# ------------------------------------------------------------------ the five workloads
+def test_pr1_2k_all_rows():
+    wl = WORKLOADS["pr1_2k"]
+    q, k, v = generate(wl, device=DEV)
+    out, lse = run_gpu_attention(q, k, v, wl)
+    torch.cuda.synchronize()
+    ro, rl = oracle_attention(q, k, v, wl)
+    compare(out.cpu().numpy(), ro, 1e-5, 1e-5, "pr1 O")
+    compare(lse.cpu().numpy(), rl, 1e-5, 1e-5, "pr1 lse")
+
+
+def test_32k_outliers_all_rows():
+    wl = WORKLOADS["32k_outliers"]
+    q, k, v = generate(wl, device=DEV)
+    out, lse = run_gpu_attention(q, k, v, wl)
+    torch.cuda.synchronize()
+    ro, rl = oracle_attention(q, k, v, wl)
+    compare(out.cpu().numpy(), ro, 1e-2, 1e-3, "32k O")
+    compare(lse.cpu().numpy(), rl, 1e-2, 1e-3, "32k lse")
+
+
+@pytest.mark.parametrize("name", ["128k_70b_layer", "1m_70b_layer"])
+def test_large_workload_sampled_rows(name):
+    wl = WORKLOADS[name]
+    q, k, v = generate(wl, device=DEV)
+    out, lse = run_gpu_attention(q, k, v, wl)
+    torch.cuda.synchronize()
+    rows = sample_rows(wl).numpy()
+    go, gl = gather_rows(out, lse, rows)
+    del out
+    ro, rl = oracle_attention(q, k, v, wl, rows=rows)
+    compare(go, ro, 1e-2, 1e-3, f"{name} O (sampled)")
+    compare(gl, rl, 1e-2, 1e-3, f"{name} lse (sampled)")
+
+
+def test_ring_128k_partials_and_merge():
+    """8 KV chunks -> per-chunk partials -> LSE merge; equals the oracle's
+    single-pass causal attention on sampled rows, and the GPU single pass
+    on every row."""
+    B = binding()
+    wl = WORKLOADS["ring_128k"]
+    q, k, v = generate(wl, device=DEV)
+    n, Hq, d = q.shape
+    c = n // wl.ring_chunks
+    o_parts = [torch.empty((n, Hq, d), dtype=torch.float32, device=DEV)
+               for _ in range(wl.ring_chunks)]
+    l_parts = [torch.empty((Hq, n), dtype=torch.float32, device=DEV)
+               for _ in range(wl.ring_chunks)]
+    for p in range(wl.ring_chunks):
+        B.attn_fwd_partial(q, k[p * c:(p + 1) * c], v[p * c:(p + 1) * c], o_parts[p], l_parts[p],
+                           0, p * c, wl.window, wl.scale)
+    merged = torch.empty((n, Hq, d), dtype=torch.float32, device=DEV)
+    mlse = torch.empty((Hq, n), dtype=torch.float32, device=DEV)
+    B.lse_merge(o_parts, l_parts, merged, mlse)
+    # rows before a chunk have no key in it
+    for p in range(1, wl.ring_chunks):
+        assert bool(torch.isneginf(l_parts[p][:, : p * c]).all())
+        assert bool(torch.isfinite(l_parts[p][:, p * c:]).all())
+    del o_parts, l_parts
+    single, slse = run_gpu_attention(q, k, v, wl)
+    torch.cuda.synchronize()
+    compare(merged.cpu().numpy(), single.cpu().numpy(), 1e-2, 1e-3, "ring merged vs single")
+    compare(mlse.cpu().numpy(), slse.cpu().numpy(), 1e-2, 1e-3, "ring lse merged vs single")
+    rows = sample_rows(wl).numpy()
+    go, gl = gather_rows(merged, mlse, rows)
+    ro, rl = oracle_attention(q, k, v, wl, rows=rows)
+    compare(go, ro, 1e-2, 1e-3, "ring merged O vs oracle")
+    compare(gl, rl, 1e-2, 1e-3, "ring merged lse vs oracle")
+
+
+# ------------------------------------------------------------------ partial + merge, small
+@pytest.mark.parametrize("dt,d", [("bf16", 128), ("f32", 64), ("bf16", 64)])
+@pytest.mark.parametrize("n,chunks,w", [(512, 4, 512), (384, 3, 100), (1000, 8, 1000)])
+def test_partial_merge_small(dt, d, n, chunks, w):
+    B = binding()
+    wl = Workload("ring_small", n, 4, 2, d, w, 0, dt, seed=n + chunks)
+    q, k, v = generate(wl, device=DEV)
+    bounds = np.linspace(0, n, chunks + 1).astype(int)
+    o_parts, l_parts = [], []
+    for lo, hi in zip(bounds[:-1], bounds[1:]):
+        o = torch.full((n, 4, d), 7.0, dtype=torch.float32, device=DEV)
+        l = torch.empty((4, n), dtype=torch.float32, device=DEV)
+        B.attn_fwd_partial(q, k[lo:hi], v[lo:hi], o, l, 0, int(lo), w, wl.scale)
+        o_parts.append(o)
+        l_parts.append(l)
+    torch.cuda.synchronize()
+    qn, kn, vn = to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v)
+    mx, mean = tol(dt)
+    for (lo, hi), o, l in zip(zip(bounds[:-1], bounds[1:]), o_parts, l_parts):
+        ro, rl = oracle.attn(qn, kn[lo:hi], vn[lo:hi], w, 0, wl.scale, kv_start=int(lo))
+        compare(l.cpu().numpy(), rl, mx, mean, f"partial lse [{lo},{hi})")
+        has = np.isfinite(rl[0])
+        go = o.cpu().numpy()
+        compare(go[has], ro[has], mx, mean, f"partial O [{lo},{hi})")
+        assert np.all(go[~has] == 7.0), "rows without keys must be left untouched"
+    out = torch.empty((n, 4, d), dtype=torch.float32, device=DEV)
+    lse = torch.empty((4, n), dtype=torch.float32, device=DEV)
+    B.lse_merge(o_parts, l_parts, out, lse)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attn(qn, kn, vn, w, 0, wl.scale)
+    compare(out.cpu().numpy(), ro, mx, mean, "merged O")
+    compare(lse.cpu().numpy(), rl, mx, mean, "merged lse")
+
+
+# ------------------------------------------------------------------ merge alone
+@pytest.mark.parametrize("P,n,Hq,d,out_dt", [(8, 1000, 4, 128, "f32"), (3, 257, 2, 64, "f32"),
+                                             (64, 33, 2, 8, "f32"), (5, 500, 32, 128, "bf16"),
+                                             (1, 17, 1, 4, "f32")])
+def test_lse_merge_parity(P, n, Hq, d, out_dt):
+    """Seeded random partials (some rows -inf in some parts, one row -inf in
+    every part) merged on the GPU and by the oracle."""
+    B = binding()
+    g = torch.Generator(device="cpu").manual_seed(P * 1000 + n)
+    o = torch.randn((P, n, Hq, d), generator=g, dtype=torch.float32)
+    l = torch.randn((P, Hq, n), generator=g, dtype=torch.float32) * 3.0
+    drop = torch.rand((P, Hq, n), generator=g) < 0.3
+    l[drop] = -float("inf")
+    l[:, :, 0] = -float("inf")
+    o_d = [o[p].contiguous().to(DEV) for p in range(P)]
+    l_d = [l[p].contiguous().to(DEV) for p in range(P)]
+    tdt = torch.float32 if out_dt == "f32" else torch.bfloat16
+    out = torch.empty((n, Hq, d), dtype=tdt, device=DEV)
+    lse = torch.empty((Hq, n), dtype=torch.float32, device=DEV)
+    B.lse_merge(o_d, l_d, out, lse)
+    torch.cuda.synchronize()
+    ro, rl = oracle.lse_merge(o.double().numpy(), l.double().numpy())
+    compare(lse.cpu().numpy(), rl, 2e-6, 2e-7, "merge lse")
+    got = out.float().cpu().numpy()
+    if out_dt == "f32":
+        compare(got, ro, 1e-5, 1e-6, "merge O")
+    else:
+        assert np.all(np.abs(got - ro) <= bf16_ulp(bf16_round(ro)) + 1e-6)
+    assert np.all(got[0] == 0.0)
+
+
+def test_lse_merge_in_place():
+    B = binding()
+    g = torch.Generator(device="cpu").manual_seed(3)
+    P, n, Hq, d = 4, 300, 8, 128
+    o = torch.randn((P, n, Hq, d), generator=g)
+    l = torch.randn((P, Hq, n), generator=g)
+    o_d = [o[p].contiguous().to(DEV) for p in range(P)]
+    l_d = [l[p].contiguous().to(DEV) for p in range(P)]
+    B.lse_merge(o_d, l_d, o_d[0], l_d[0])
+    torch.cuda.synchronize()
+    ro, rl = oracle.lse_merge(o.double().numpy(), l.double().numpy())
+    compare(o_d[0].cpu().numpy(), ro, 1e-5, 1e-6, "in-place merge O")
+    compare(l_d[0].cpu().numpy(), rl, 2e-6, 2e-7, "in-place merge lse")
+
+
+# ------------------------------------------------------------------ output dtype, determinism
+def test_bf16_output_within_one_ulp():
+    wl = Workload("bf16out", 2000, 8, 2, 128, 700, 8, "bf16", seed=11)
+    q, k, v = generate(wl, device=DEV)
+    out, lse = run_gpu_attention(q, k, v, wl, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    ro, rl = oracle_attention(q, k, v, wl)
+    ref = bf16_round(ro)
+    got = out.float().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= bf16_ulp(ref)), "bf16 O more than one ulp from oracle"
+    assert float(np.abs(got - ro).mean()) <= 1e-3
+    compare(lse.cpu().numpy(), rl, 1e-2, 1e-3, "lse")
+
+
+def test_tensor_core_kernel_is_deterministic():
+    wl = Workload("det", 4096, 16, 2, 128, 1000, 16, "bf16", seed=5)
+    q, k, v = generate(wl, device=DEV)
+    o1, l1 = run_gpu_attention(q, k, v, wl)
+    o2, l2 = run_gpu_attention(q, k, v, wl)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert binding().device_status() == 0
