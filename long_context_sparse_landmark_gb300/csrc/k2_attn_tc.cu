@@ -33,7 +33,10 @@
 // Softmax: scores are kept in log2 units (scale*log2(e) folded into one FMA);
 // the exponent base m is only raised when the row maximum exceeds it by more
 // than kTau (then O and l are rescaled in TMEM/registers), so p <= 2^kTau;
-// O/l and lse = (m + log2 l) ln 2 are exact for any base.
+// O/l and lse = (m + log2 l) ln 2 are exact for any base.  P enters the PV
+// MMA rounded to bf16 and l sums those same rounded values, so each output
+// row is an exactly normalised combination of V rows (a key that dominates
+// a row then reproduces its V row without the bf16 rounding of its weight).
 //
 // Every mbarrier wait is bounded (globaltimer); a wait that runs out sets a
 // CTA-wide abort flag and the device status word, all roles leave their
@@ -208,6 +211,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Register budget: the producer/MMA warpgroup needs few registers, the
+  // two softmax warpgroups hold a 128-score row each.  Launch allocation is
+  // 384 x 168; 128 x 72 + 256 x 216 uses exactly that.  Each role raises or
+  // lowers its own budget inside its branch.
+  if (warp < 4) {
+    ptx::reg_dealloc<72>();
+  }
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -316,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
+    ptx::reg_alloc<216>();
     const int slot = (warp - 4) >> 2;
     const int wq = warp & 3;
     if (slot < n_slots) {
@@ -359,9 +370,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c >= lo_c && c < hi_c) ? s[c] : -INFINITY;
         }
-        float mx = -INFINITY;
+        // Row maximum: four independent chains of three-input maxima.
+        float a0 = fmaxf(s[0], s[1]), a1 = fmaxf(s[2], s[3]);
+        float a2 = fmaxf(s[4], s[5]), a3 = fmaxf(s[6], s[7]);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        for (int c = 8; c < 128; c += 8) {
+          a0 = ptx::max3(a0, s[c], s[c + 1]);
+          a1 = ptx::max3(a1, s[c + 2], s[c + 3]);
+          a2 = ptx::max3(a2, s[c + 4], s[c + 5]);
+          a3 = ptx::max3(a3, s[c + 6], s[c + 7]);
+        }
+        const float mx = ptx::max3(a0, a1, fmaxf(a2, a3));
         const float m_new = fmaxf(m_used, mx * sl2);
         const bool need = m_new > m_used + kTau;
         if (need) {
@@ -382,17 +401,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         }
         if (need) m_used = m_new;
         const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+        // p = 2^(s*scale*log2e - m) two at a time (packed FMA), rounded to
+        // bf16 pairs for the PV MMA; the denominator sums those same
+        // rounded weights (so O is normalised by exactly the weights it was
+        // built from), in two packed accumulators.
+        const uint64_t c2 = ptx::f2(sl2, sl2);
+        const uint64_t nb2 = ptx::f2(-mb, -mb);
+        uint64_t acc0 = ptx::f2(0.f, 0.f), acc1 = ptx::f2(0.f, 0.f);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ptx::ex2(fmaf(s[cc * 32 + 2 * e], sl2, -mb));
-            const float p1 = ptx::ex2(fmaf(s[cc * 32 + 2 * e + 1], sl2, -mb));
-            l += p0 + p1;
-            pk[e] = ptx::pack_bf16x2(p0, p1);
+            const uint64_t x =
+                ptx::fma2(ptx::f2(s[cc * 32 + 2 * e], s[cc * 32 + 2 * e + 1]), c2, nb2);
+            float x0, x1;
+            ptx::f2_split(x, x0, x1);
+            pk[e] = ptx::pack_bf16x2(ptx::ex2(x0), ptx::ex2(x1));
+            const uint64_t r =
+                ptx::f2(__uint_as_float(pk[e] << 16), __uint_as_float(pk[e] & 0xffff0000u));
+            if (e & 1)
+              acc1 = ptx::add2(acc1, r);
+            else
+              acc0 = ptx::add2(acc0, r);
           }
           ptx::tmem_st16(tS + cc * 16, pk);
+        }
+        {
+          float l0, l1, l2, l3;
+          ptx::f2_split(acc0, l0, l1);
+          ptx::f2_split(acc1, l2, l3);
+          l += (l0 + l1) + (l2 + l3);
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
