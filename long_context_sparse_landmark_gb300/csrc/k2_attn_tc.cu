@@ -266,25 +266,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     if (lane == 0) {
       constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBM, kBN, false);
       constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kBM, kD, true);
+      // Descriptor low halves of every operand base, computed once; per K
+      // step the low half advances by a compile-time constant (Q/K: 32 B
+      // within a 128-B swizzle row, 16 KB to the second 64-column chunk;
+      // V: 16 key rows = 2 KB), see the layouts at the TMA maps.
+      const uint32_t q_lo0 = ptx::desc_lo(sb + kOffQ, 16);
+      const uint32_t k_lo0 = ptx::desc_lo(sb + kOffK, 16);
+      const uint32_t v_lo0 = ptx::desc_lo(sb + kOffV, kChunkBytes);
+      constexpr uint32_t kTileLo = kTileBytes >> 4;
       auto issue_s = [&](int slot, int t) {
-        const uint32_t qa = sb + kOffQ + slot * kTileBytes;
-        const uint32_t kb = sb + kOffK + (t & 1) * kTileBytes;
+        const uint32_t qa = q_lo0 + slot * kTileLo;
+        const uint32_t kb = k_lo0 + (t & 1) * kTileLo;
         const uint32_t d = tmem + slot * 256;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          ptx::mma_ss(d, ptx::smem_desc_sw128(qa + off, 16, 1024),
-                      ptx::smem_desc_sw128(kb + off, 16, 1024), kIdescS, kk > 0);
+          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+          ptx::mma_ss_lohi(d, qa + off, ptx::kDescHiSw128, kb + off, ptx::kDescHiSw128, kIdescS,
+                           kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int slot, int t) {
-        const uint32_t vb = sb + kOffV + (t & 1) * kTileBytes;
+        const uint32_t vb = v_lo0 + (t & 1) * kTileLo;
         const uint32_t d = tmem + slot * 256 + 128;
         const uint32_t pa = tmem + slot * 256;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          ptx::mma_ts(d, pa + kk * 8, ptx::smem_desc_sw128(vb + kk * 2048, kChunkBytes, 1024),
-                      kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_ts_lohi(d, pa + kk * 8, vb + ((kk * 2048) >> 4), ptx::kDescHiSw128, kIdescO,
+                           (t > 0 || kk > 0) ? 1u : 0u);
         }
       };
       bool ok = wait_bar(bar(BAR_Q), 0, ctl);

@@ -173,6 +173,43 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+
+// The same two MMAs with each shared-memory descriptor given as its two
+// 32-bit halves: the high half (stride offset, version, swizzle) is fixed
+// per operand, the low half (start address >> 4, leading offset) changes
+// by a constant per K step, so issuing costs one add per operand.
+__device__ __forceinline__ void mma_ss_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                            uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_lohi(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                            uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Descriptor halves for the 128-byte-swizzled layouts used here: high half
+// = stride offset 1024 B (8 rows of 128 B) >> 4, version bit, swizzle 2.
+constexpr uint32_t kDescHiSw128 = (1024u >> 4) | (1u << 14) | (2u << 29);
+// Low half: start address >> 4 and the leading byte offset >> 4.
+__device__ __forceinline__ uint32_t desc_lo(uint32_t addr, uint32_t lbo) {
+  return ((addr & 0x3FFFFu) >> 4) | ((lbo >> 4) << 16);
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued
 // before has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -257,6 +294,31 @@ __device__ __forceinline__ void reg_dealloc() {
 template <int N>
 __device__ __forceinline__ void reg_alloc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// 2^x for two values without the MUFU unit: Cody-Waite range reduction
+// x = j + f with j = round(x) (|f| <= 1/2) by adding and subtracting
+// 1.5 * 2^23, a degree-3 polynomial for 2^f fitted for minimum relative
+// error on [-1/2, 1/2] with constant term 1 (max relative error 1.0e-4 in
+// fp32 Horner form), and j added into the exponent field.  x is clamped at
+// -127 first, where the result is exactly +0 (j = -127, f = 0), so masked
+// scores (-inf) give 0.  Valid for x <= 127.
+__device__ __forceinline__ void exp2_poly_pair(uint64_t x2, float& y0, float& y1) {
+  float x0, x1;
+  f2_split(x2, x0, x1);
+  const uint64_t xc = f2(fmaxf(x0, -127.f), fmaxf(x1, -127.f));
+  const uint64_t t = add2(xc, f2(12582912.f, 12582912.f));
+  const uint64_t j = add2(t, f2(-12582912.f, -12582912.f));
+  const uint64_t fr = fma2(j, f2(-1.f, -1.f), xc);
+  uint64_t p = fma2(f2(0.05500892922282219f, 0.05500892922282219f), fr,
+                    f2(0.2422109693288803f, 0.2422109693288803f));
+  p = fma2(p, fr, f2(0.6932829022407532f, 0.6932829022407532f));
+  p = fma2(p, fr, f2(1.f, 1.f));
+  float t0, t1, p0, p1;
+  f2_split(t, t0, t1);
+  f2_split(p, p0, p1);
+  y0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
+  y1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
 }
 
 }  // namespace ptx
