@@ -45,6 +45,29 @@ def load_peaks():
                 "source": "fallback"}
 
 
+# DRAM traffic of one attention launch on the 128K layer, from the ncu
+# capture summarised in profiles/attn_tc_kernel_128k_70b_layer.md.  It only
+# applies to the kernel source it was measured on (SHA-256 of
+# k2_attn_tc.cu); after any change the traffic is reported as null.
+ATTN_TRAFFIC = {"128k_70b_layer": {
+    "bytes": 2.689312e9 + 2.140172e9,
+    "kernel_sha256": "e531575fe3bc196001a906d0dc8d15c65a3d0cbb62daae40c8755013f3acf81a"}}
+
+
+def kernel_sha256() -> str:
+    import hashlib
+    path = os.path.join(ROOT, "long_context_sparse_landmark_gb300", "csrc", "k2_attn_tc.cu")
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def attn_traffic(name: str):
+    rec = ATTN_TRAFFIC.get(name)
+    if not rec or rec["bytes"] is None or rec["kernel_sha256"] != kernel_sha256():
+        return None
+    return rec["bytes"]
+
+
 def attended_total(wl) -> int:
     """sum_i |window(i)| + |visible landmarks(i)| for one head (closed form)."""
     import numpy as np
@@ -75,7 +98,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -272,7 +295,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["msa", "reference"], default="msa")
-    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--workload", default=HEADLINE,
                     help="window+landmark workload timed as the step (profiling uses smaller ones)")
     ap.add_argument("--no-also", action="store_true")
@@ -322,6 +345,9 @@ def main():
     tokens_per_s = world * wl.n / (ms_per_step * 1e-3)
     attn_tflops = flops / (res["attn_ms"] * 1e-3) / 1e12
     pool_bytes = 2 * wl.n * wl.Hkv * wl.d * 2 + 2 * wl.G * wl.Hkv * wl.d * 2
+    # Q, K, V and the landmarks read once, O (bf16) and lse written once.
+    attn_bytes = (wl.n * wl.Hq * wl.d * 2 + 2 * wl.n * wl.Hkv * wl.d * 2
+                  + 2 * wl.G * wl.Hkv * wl.d * 2 + wl.n * wl.Hq * (wl.d * 2 + 4))
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -343,7 +369,8 @@ def main():
                      "frac": round(attn_tflops / peaks["bf16_tflops_sustained"], 4),
                      "peak_kind": f"bf16 sustained ({peaks['source']})",
                      "frac_of_burst": round(attn_tflops / peaks["bf16_tflops"], 4),
-                     "traffic": None},
+                     "traffic": attn_traffic(wl.name),
+                     "algorithmic_bytes": attn_bytes},
         "pool_roofline": {"bound": "hbm",
                           "achieved": round(pool_bytes / (res["pool_ms"] * 1e-3) / 1e9, 1),
                           "peak": peaks["hbm_gbs"], "unit": "GB/s",

@@ -296,30 +296,5 @@ __device__ __forceinline__ void reg_alloc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// 2^x for two values without the MUFU unit: Cody-Waite range reduction
-// x = j + f with j = round(x) (|f| <= 1/2) by adding and subtracting
-// 1.5 * 2^23, a degree-3 polynomial for 2^f fitted for minimum relative
-// error on [-1/2, 1/2] with constant term 1 (max relative error 1.0e-4 in
-// fp32 Horner form), and j added into the exponent field.  x is clamped at
-// -127 first, where the result is exactly +0 (j = -127, f = 0), so masked
-// scores (-inf) give 0.  Valid for x <= 127.
-__device__ __forceinline__ void exp2_poly_pair(uint64_t x2, float& y0, float& y1) {
-  float x0, x1;
-  f2_split(x2, x0, x1);
-  const uint64_t xc = f2(fmaxf(x0, -127.f), fmaxf(x1, -127.f));
-  const uint64_t t = add2(xc, f2(12582912.f, 12582912.f));
-  const uint64_t j = add2(t, f2(-12582912.f, -12582912.f));
-  const uint64_t fr = fma2(j, f2(-1.f, -1.f), xc);
-  uint64_t p = fma2(f2(0.05500892922282219f, 0.05500892922282219f), fr,
-                    f2(0.2422109693288803f, 0.2422109693288803f));
-  p = fma2(p, fr, f2(0.6932829022407532f, 0.6932829022407532f));
-  p = fma2(p, fr, f2(1.f, 1.f));
-  float t0, t1, p0, p1;
-  f2_split(t, t0, t1);
-  f2_split(p, p0, p1);
-  y0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
-  y1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
-}
-
 }  // namespace ptx
 }  // namespace msa
