@@ -70,7 +70,7 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kSlots * kTileBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
 constexpr int kOffBar = kOffV + kStages * kTileBytes;
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 17;
 constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemUsed = kOffAbort + 8;
@@ -86,6 +86,7 @@ __host__ __device__ constexpr int BAR_SF(int s) { return 9 + s; }
 __host__ __device__ constexpr int BAR_PF(int s) { return 11 + s; }
 __host__ __device__ constexpr int BAR_OD(int s) { return 13 + s; }
 constexpr int BAR_CLEAN = 15;
+constexpr int BAR_QE = 16;  // Q buffer free (the unit's last S MMA completed)
 
 struct TcParams {
   CUtensorMap tm_q;
@@ -96,7 +97,7 @@ struct TcParams {
   void* out;
   float* lse;
   int64_t n_q, q_start, n_kv, kv_start, window, block;
-  int Hq, Hkv, G, group, pairs, n_qtiles;
+  int Hq, Hkv, G, group, pairs, n_qtiles, units;
   int out_bf16, partial;
   float scale_log2;
   int* status;
@@ -137,6 +138,44 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, int* st
   }
 }
 
+// One work unit: 128 query rows x (up to) 2 heads of one KV group, and the
+// key tiles those rows visit (landmark tiles first, then window tiles).
+struct Unit {
+  int h0, kvh, n_slots, kt_lo, n_lm_tiles, T;
+  int64_t qr0;
+};
+
+// Unit u in the schedule order: head pair fastest, then query tiles from the
+// last one down (the causal partials' heaviest units first), then KV heads.
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
+  Unit w;
+  const int pair = u % p.pairs;
+  u /= p.pairs;
+  const int qt = p.n_qtiles - 1 - (u % p.n_qtiles);
+  w.kvh = u / p.n_qtiles;
+  w.h0 = w.kvh * p.group + 2 * pair;
+  w.n_slots = (2 * pair + 1 < p.group) ? 2 : 1;
+  w.qr0 = static_cast<int64_t>(qt) * kBM;
+  const int64_t g0 = p.q_start + w.qr0;
+  const int64_t g_last = p.q_start + min64(w.qr0 + kBM, p.n_q) - 1;
+  const int64_t kv_end = p.kv_start + p.n_kv;
+  const int64_t j_lo = max64(g0 - p.window + 1, p.kv_start);
+  const int64_t j_hi = min64(g_last, kv_end - 1);
+  w.kt_lo = 0;
+  int n_win = 0;
+  if (j_hi >= j_lo) {
+    w.kt_lo = static_cast<int>((j_lo - p.kv_start) / kBN);
+    n_win = static_cast<int>((j_hi - p.kv_start) / kBN) - w.kt_lo + 1;
+  }
+  const int64_t n_lm = visible_landmarks(g_last, p.window, p.block, p.G);
+  w.n_lm_tiles = static_cast<int>((n_lm + kBN - 1) / kBN);
+  w.T = w.n_lm_tiles + n_win;
+  return w;
+}
+
+// Persistent: one CTA per SM walks units blockIdx.x, +gridDim.x, ...  The
+// K/V ring, the Q buffer and TMEM carry over from unit to unit, so the next
+// unit's Q load and first S MMAs overlap the current unit's epilogue.
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -148,44 +187,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- work unit: (KV head, query tile, head pair); late query tiles first.
-  int u = blockIdx.x;
-  const int pair = u % p.pairs;
-  u /= p.pairs;
-  const int qt = p.n_qtiles - 1 - (u % p.n_qtiles);
-  const int kvh = u / p.n_qtiles;
-  const int h0 = kvh * p.group + 2 * pair;
-  const int n_slots = (2 * pair + 1 < p.group) ? 2 : 1;
-  const int64_t qr0 = static_cast<int64_t>(qt) * kBM;
-  const int64_t g0 = p.q_start + qr0;
-  const int64_t g_last = p.q_start + min64(qr0 + kBM, p.n_q) - 1;
-  const int64_t kv_end = p.kv_start + p.n_kv;
-  const int64_t j_lo = max64(g0 - p.window + 1, p.kv_start);
-  const int64_t j_hi = min64(g_last, kv_end - 1);
-  int kt_lo = 0, n_win_tiles = 0;
-  if (j_hi >= j_lo) {
-    kt_lo = static_cast<int>((j_lo - p.kv_start) / kBN);
-    n_win_tiles = static_cast<int>((j_hi - p.kv_start) / kBN) - kt_lo + 1;
-  }
-  const int64_t n_lm = visible_landmarks(g_last, p.window, p.block, p.G);
-  const int n_lm_tiles = static_cast<int>((n_lm + kBN - 1) / kBN);
-  const int T = n_lm_tiles + n_win_tiles;
-
-  if (T == 0) {  // no key for any row of this unit (partial chunks only)
-    if (warp >= 4) {
-      const int slot = (warp - 4) >> 2;
-      const int64_t i_loc = qr0 + (warp & 3) * 32 + lane;
-      if (slot < n_slots && i_loc < p.n_q)
-        p.lse[static_cast<int64_t>(h0 + slot) * p.n_q + i_loc] = -INFINITY;
-    }
-    return;
-  }
-
   WaitCtl ctl{abort_flag, p.status, p.wait_ns};
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(BAR_Q), 1);
+    ptx::mbar_init(bar(BAR_QE), 1);
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(bar(BAR_KF(s)), 1);
       ptx::mbar_init(bar(BAR_KE(s)), 1);
@@ -213,10 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
   // Register budget: the producer/MMA warpgroup needs few registers, the
   // two softmax warpgroups hold a 128-score row each.  Launch allocation is
-  // 384 x 168; 128 x 72 + 256 x 216 uses exactly that.  Each role raises or
-  // lowers its own budget inside its branch.
+  // 384 x 168; 128 x 96 + 256 x 200 fits in it with no spills.  Each role
+  // raises or lowers its own budget inside its branch.
   if (warp < 4) {
-    ptx::reg_dealloc<72>();
+    ptx::reg_dealloc<96>();
   }
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -224,39 +230,56 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       ptx::tma_prefetch_desc(&p.tm_q);
       ptx::tma_prefetch_desc(&p.tm_k);
       ptx::tma_prefetch_desc(&p.tm_v);
-      int k_issued = 0, v_issued = 0;
-      ptx::mbar_arrive_expect_tx(bar(BAR_Q), n_slots * kTileBytes);
-      for (int s = 0; s < n_slots; ++s)
-        for (int c = 0; c < 2; ++c)
-          ptx::tma_load_3d(sb + kOffQ + s * kTileBytes + c * kChunkBytes, &p.tm_q, bar(BAR_Q),
-                           c * 64, h0 + s, static_cast<int>(qr0));
-      for (int t = 0; t < T; ++t) {
-        const int st = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        const bool lm = t < n_lm_tiles;
-        const CUtensorMap* mk = lm ? &p.tm_klm : &p.tm_k;
-        const CUtensorMap* mv = lm ? &p.tm_vlm : &p.tm_v;
-        const int row = lm ? t * kBN : (kt_lo + t - n_lm_tiles) * kBN;
-        if (!wait_bar(bar(BAR_KE(st)), ph ^ 1, ctl)) break;
-        ptx::mbar_arrive_expect_tx(bar(BAR_KF(st)), kTileBytes);
-        for (int c = 0; c < 2; ++c)
-          ptx::tma_load_3d(sb + kOffK + st * kTileBytes + c * kChunkBytes, mk, bar(BAR_KF(st)),
-                           c * 64, kvh, row);
-        k_issued = t + 1;
-        if (!wait_bar(bar(BAR_VE(st)), ph ^ 1, ctl)) break;
-        ptx::mbar_arrive_expect_tx(bar(BAR_VF(st)), kTileBytes);
-        for (int c = 0; c < 2; ++c)
-          ptx::tma_load_3d(sb + kOffV + st * kTileBytes + c * kChunkBytes, mv, bar(BAR_VF(st)),
-                           c * 64, kvh, row);
-        v_issued = t + 1;
+      uint32_t gk = 0, gv = 0;  // K / V tiles issued so far (ring position)
+      uint32_t qn = 0;          // units whose Q was issued
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        if (w.T == 0) continue;
+        // The Q buffer is free once the previous unit's last S MMA is done.
+        if (qn > 0 && !(ok = wait_bar(bar(BAR_QE), (qn - 1) & 1, ctl))) break;
+        ptx::mbar_arrive_expect_tx(bar(BAR_Q), w.n_slots * kTileBytes);
+        for (int s = 0; s < w.n_slots; ++s)
+          for (int c = 0; c < 2; ++c)
+            ptx::tma_load_3d(sb + kOffQ + s * kTileBytes + c * kChunkBytes, &p.tm_q, bar(BAR_Q),
+                             c * 64, w.h0 + s, static_cast<int>(w.qr0));
+        ++qn;
+        // Warm L2 with this CTA's next Q tiles: they are read once, from
+        // HBM, exactly when the tensor pipe waits for them.
+        if (u + static_cast<int>(gridDim.x) < p.units) {
+          const Unit nw = decode_unit(p, u + gridDim.x);
+          for (int s = 0; s < nw.n_slots; ++s)
+            for (int c = 0; c < 2; ++c)
+              ptx::tma_prefetch_3d(&p.tm_q, c * 64, nw.h0 + s, static_cast<int>(nw.qr0));
+        }
+        for (int t = 0; t < w.T; ++t) {
+          const bool lm = t < w.n_lm_tiles;
+          const CUtensorMap* mk = lm ? &p.tm_klm : &p.tm_k;
+          const CUtensorMap* mv = lm ? &p.tm_vlm : &p.tm_v;
+          const int row = lm ? t * kBN : (w.kt_lo + t - w.n_lm_tiles) * kBN;
+          int st = gk & 1;
+          if (!(ok = wait_bar(bar(BAR_KE(st)), ((gk >> 1) & 1) ^ 1, ctl))) break;
+          ptx::mbar_arrive_expect_tx(bar(BAR_KF(st)), kTileBytes);
+          for (int c = 0; c < 2; ++c)
+            ptx::tma_load_3d(sb + kOffK + st * kTileBytes + c * kChunkBytes, mk, bar(BAR_KF(st)),
+                             c * 64, w.kvh, row);
+          ++gk;
+          st = gv & 1;
+          if (!(ok = wait_bar(bar(BAR_VE(st)), ((gv >> 1) & 1) ^ 1, ctl))) break;
+          ptx::mbar_arrive_expect_tx(bar(BAR_VF(st)), kTileBytes);
+          for (int c = 0; c < 2; ++c)
+            ptx::tma_load_3d(sb + kOffV + st * kTileBytes + c * kChunkBytes, mv, bar(BAR_VF(st)),
+                             c * 64, w.kvh, row);
+          ++gv;
+        }
       }
       // Drain: every copy this thread issued must have landed before exit.
-      drain_bar(bar(BAR_Q), 0, p.status);
+      if (qn > 0) drain_bar(bar(BAR_Q), (qn - 1) & 1, p.status);
       for (int s = 0; s < kStages; ++s) {
-        int last = k_issued - 1;
+        int last = static_cast<int>(gk) - 1;
         if (last >= 0 && (last & 1) != s) --last;
         if (last >= 0) drain_bar(bar(BAR_KF(s)), (last >> 1) & 1, p.status);
-        last = v_issued - 1;
+        last = static_cast<int>(gv) - 1;
         if (last >= 0 && (last & 1) != s) --last;
         if (last >= 0) drain_bar(bar(BAR_VF(s)), (last >> 1) & 1, p.status);
       }
@@ -274,9 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const uint32_t k_lo0 = ptx::desc_lo(sb + kOffK, 16);
       const uint32_t v_lo0 = ptx::desc_lo(sb + kOffV, kChunkBytes);
       constexpr uint32_t kTileLo = kTileBytes >> 4;
-      auto issue_s = [&](int slot, int t) {
+      auto issue_s = [&](int slot, uint32_t stage) {
         const uint32_t qa = q_lo0 + slot * kTileLo;
-        const uint32_t kb = k_lo0 + (t & 1) * kTileLo;
+        const uint32_t kb = k_lo0 + stage * kTileLo;
         const uint32_t d = tmem + slot * 256;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -285,74 +308,99 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                            kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int slot, int t) {
-        const uint32_t vb = v_lo0 + (t & 1) * kTileLo;
+      auto issue_pv = [&](int slot, uint32_t stage, bool first) {
+        const uint32_t vb = v_lo0 + stage * kTileLo;
         const uint32_t d = tmem + slot * 256 + 128;
         const uint32_t pa = tmem + slot * 256;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           ptx::mma_ts_lohi(d, pa + kk * 8, vb + ((kk * 2048) >> 4), ptx::kDescHiSw128, kIdescO,
-                           (t > 0 || kk > 0) ? 1u : 0u);
+                           (!first || kk > 0) ? 1u : 0u);
         }
       };
-      bool ok = wait_bar(bar(BAR_Q), 0, ctl);
-      if (ok) ok = wait_bar(bar(BAR_KF(0)), 0, ctl);
-      if (ok) {
+      uint32_t g = 0;                 // global tile index (K/V ring position)
+      uint32_t qn = 0;                // units processed
+      uint32_t sc[kSlots] = {0, 0};   // tiles processed per slot (SF/PF phases)
+      uint32_t oc[kSlots] = {0, 0};   // units processed per slot (OD phases)
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        if (w.T == 0) continue;
+        if (!(ok = wait_bar(bar(BAR_Q), qn & 1, ctl))) break;
+        if (!(ok = wait_bar(bar(BAR_KF(g & 1)), (g >> 1) & 1, ctl))) break;
         ptx::tc_fence_after();
-        for (int s = 0; s < n_slots; ++s) {
-          issue_s(s, 0);
+        for (int s = 0; s < w.n_slots; ++s) {
+          issue_s(s, g & 1);
           ptx::mma_commit(bar(BAR_SF(s)));
         }
-        ptx::mma_commit(bar(BAR_KE(0)));
-      }
-      for (int t = 0; ok && t < T; ++t) {
-        const int st = t & 1;
-        const bool nxt = t + 1 < T;
-        if (!(ok = wait_bar(bar(BAR_VF(st)), (t >> 1) & 1, ctl))) break;
-        for (int s = 0; s < n_slots; ++s) {
-          if (!(ok = wait_bar(bar(BAR_PF(s)), t & 1, ctl))) break;
-          ptx::tc_fence_after();
-          issue_pv(s, t);
-          if (nxt) {
-            if (s == 0) {
-              if (!(ok = wait_bar(bar(BAR_KF(st ^ 1)), ((t + 1) >> 1) & 1, ctl))) break;
-              ptx::tc_fence_after();
+        if (w.T == 1) ptx::mma_commit(bar(BAR_QE));  // the unit's last S MMA
+        ptx::mma_commit(bar(BAR_KE(g & 1)));
+        for (int t = 0; ok && t < w.T; ++t, ++g) {
+          const uint32_t st = g & 1;
+          const bool nxt = t + 1 < w.T;
+          if (!(ok = wait_bar(bar(BAR_VF(st)), (g >> 1) & 1, ctl))) break;
+          for (int s = 0; s < w.n_slots; ++s) {
+            if (!(ok = wait_bar(bar(BAR_PF(s)), (sc[s] + t) & 1, ctl))) break;
+            ptx::tc_fence_after();
+            // PV_s(t) reads P_s(t) from the S columns; S_s(t+1) overwrites
+            // them and is issued after it by this same thread.
+            issue_pv(s, st, t == 0);
+            if (nxt) {
+              if (s == 0) {
+                if (!(ok = wait_bar(bar(BAR_KF(st ^ 1)), ((g + 1) >> 1) & 1, ctl))) break;
+                ptx::tc_fence_after();
+              }
+              issue_s(s, st ^ 1);
+              ptx::mma_commit(bar(BAR_SF(s)));
+            } else {
+              ptx::mma_commit(bar(BAR_OD(s)));
             }
-            issue_s(s, t + 1);
-            ptx::mma_commit(bar(BAR_SF(s)));
-          } else {
-            ptx::mma_commit(bar(BAR_OD(s)));
           }
+          if (!ok) break;
+          if (t + 2 == w.T) ptx::mma_commit(bar(BAR_QE));  // S(T-1) was the last S
+          ptx::mma_commit(bar(BAR_VE(st)));
+          if (nxt) ptx::mma_commit(bar(BAR_KE(st ^ 1)));
         }
-        if (!ok) break;
-        ptx::mma_commit(bar(BAR_VE(st)));
-        if (nxt) ptx::mma_commit(bar(BAR_KE(st ^ 1)));
+        for (int s = 0; s < w.n_slots; ++s) {
+          sc[s] += w.T;
+          oc[s] += 1;
+        }
+        ++qn;
       }
+      (void)oc;
       // Drain: all MMAs issued so far complete before TMEM is released.
       ptx::mma_commit(bar(BAR_CLEAN));
       drain_bar(bar(BAR_CLEAN), 0, p.status);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    ptx::reg_alloc<216>();
+    ptx::reg_alloc<200>();
     const int slot = (warp - 4) >> 2;
     const int wq = warp & 3;
-    if (slot < n_slots) {
-      const int64_t i_loc = qr0 + wq * 32 + lane;
+    const uint32_t tS = tmem + slot * 256 + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t tO = tS + 128;
+    const int64_t kv_end = p.kv_start + p.n_kv;
+    const float sl2 = p.scale_log2;
+    uint32_t sc = 0, oc = 0;  // tiles / units this slot has processed
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+      const Unit w = decode_unit(p, u);
+      if (slot >= w.n_slots) continue;
+      const int64_t i_loc = w.qr0 + wq * 32 + lane;
       const bool row_ok = i_loc < p.n_q;
       const int64_t i = p.q_start + i_loc;
-      const int h = h0 + slot;
-      const uint32_t tS = tmem + slot * 256 + (static_cast<uint32_t>(wq * 32) << 16);
-      const uint32_t tO = tS + 128;
+      const int h = w.h0 + slot;
+      if (w.T == 0) {  // no key for any row of this unit (partial chunks only)
+        if (row_ok) p.lse[static_cast<int64_t>(h) * p.n_q + i_loc] = -INFINITY;
+        continue;
+      }
       const int64_t my_lo = max64(i - p.window + 1, p.kv_start);
       const int64_t my_hi = min64(i, kv_end - 1);
       const int64_t my_lm = visible_landmarks(i, p.window, p.block, p.G);
-      const float sl2 = p.scale_log2;
       float m_used = -INFINITY;
       float l = 0.f;
-      bool ok = true;
-      for (int t = 0; t < T; ++t) {
-        ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF(slot)), t & 1, ctl));
+      for (int t = 0; t < w.T; ++t) {
+        ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF(slot)), (sc + t) & 1, ctl));
         if (!ok) break;
         ptx::tc_fence_after();
         float s[128];
@@ -363,11 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         ptx::tmem_wait_ld();
         // Valid columns [lo, hi) of this tile for this row.
         int64_t lo, hi;
-        if (t < n_lm_tiles) {
+        if (t < w.n_lm_tiles) {
           lo = 0;
           hi = my_lm - static_cast<int64_t>(t) * kBN;
         } else {
-          const int64_t kb = p.kv_start + static_cast<int64_t>(kt_lo + t - n_lm_tiles) * kBN;
+          const int64_t kb = p.kv_start + static_cast<int64_t>(w.kt_lo + t - w.n_lm_tiles) * kBN;
           lo = my_lo - kb;
           hi = my_hi - kb + 1;
         }
@@ -446,43 +494,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar(BAR_PF(slot)));
       }
-      if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_OD(slot)), 0, ctl));
-      if (ok) {
-        ptx::tc_fence_after();
-        const bool has = row_ok && l > 0.f;
-        const float inv = has ? 1.f / l : 0.f;
-        const int64_t obase = (i_loc * p.Hq + h) * static_cast<int64_t>(kD);
+      if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_OD(slot)), oc & 1, ctl));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      // Epilogue.  The TMEM reads of O complete (wait::ld) before this slot
+      // arrives for the next unit's first P, which the MMA thread waits for
+      // before the next unit's first PV overwrites O.
+      const bool has = row_ok && l > 0.f;
+      const float inv = has ? 1.f / l : 0.f;
+      const int64_t obase = (i_loc * p.Hq + h) * static_cast<int64_t>(kD);
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          float o[32];
-          ptx::tmem_ld32(tO + cc * 32, o);
-          ptx::tmem_wait_ld();
-          if (has) {
-            if (p.out_bf16) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + obase + cc * 32);
+      for (int cc = 0; cc < 4; ++cc) {
+        float o[32];
+        ptx::tmem_ld32(tO + cc * 32, o);
+        ptx::tmem_wait_ld();
+        if (has) {
+          if (p.out_bf16) {
+            uint4* dst =
+                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + obase + cc * 32);
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                uint4 w;
-                w.x = ptx::pack_bf16x2(o[8 * v + 0] * inv, o[8 * v + 1] * inv);
-                w.y = ptx::pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv);
-                w.z = ptx::pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv);
-                w.w = ptx::pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv);
-                dst[v] = w;
-              }
-            } else {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + cc * 32);
-#pragma unroll
-              for (int v = 0; v < 8; ++v)
-                dst[v] = make_float4(o[4 * v] * inv, o[4 * v + 1] * inv, o[4 * v + 2] * inv,
-                                     o[4 * v + 3] * inv);
+            for (int v = 0; v < 4; ++v) {
+              uint4 q4;
+              q4.x = ptx::pack_bf16x2(o[8 * v + 0] * inv, o[8 * v + 1] * inv);
+              q4.y = ptx::pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv);
+              q4.z = ptx::pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv);
+              q4.w = ptx::pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv);
+              dst[v] = q4;
             }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + cc * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(o[4 * v] * inv, o[4 * v + 1] * inv, o[4 * v + 2] * inv,
+                                   o[4 * v + 3] * inv);
           }
         }
-        if (row_ok) {
-          p.lse[static_cast<int64_t>(h) * p.n_q + i_loc] =
-              l > 0.f ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
-        }
       }
+      if (row_ok) {
+        p.lse[static_cast<int64_t>(h) * p.n_q + i_loc] =
+            l > 0.f ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+      }
+      sc += w.T;
+      oc += 1;
     }
   }
 
@@ -584,7 +637,13 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s, const char** why) 
       attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t units = static_cast<int64_t>(a.Hkv) * p.pairs * p.n_qtiles;
-  attn_tc_kernel<<<static_cast<unsigned>(units), kThreads, kSmemBytes, s>>>(p);
+  p.units = static_cast<int>(units);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = units < sms ? units : sms;
+  attn_tc_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(p);
   return cudaPeekAtLastError();
 }
 
