@@ -70,23 +70,25 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kSlots * kTileBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
 constexpr int kOffBar = kOffV + kStages * kTileBytes;
-constexpr int kNumBars = 17;
+constexpr int kNumBars = 14;
 constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemUsed = kOffAbort + 8;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // alignment slack
 
-// Barrier indices.
-constexpr int BAR_Q = 0;
-__host__ __device__ constexpr int BAR_KF(int s) { return 1 + s; }
-__host__ __device__ constexpr int BAR_KE(int s) { return 3 + s; }
-__host__ __device__ constexpr int BAR_VF(int s) { return 5 + s; }
-__host__ __device__ constexpr int BAR_VE(int s) { return 7 + s; }
-__host__ __device__ constexpr int BAR_SF(int s) { return 9 + s; }
-__host__ __device__ constexpr int BAR_PF(int s) { return 11 + s; }
-__host__ __device__ constexpr int BAR_OD(int s) { return 13 + s; }
-constexpr int BAR_CLEAN = 15;
-constexpr int BAR_QE = 16;  // Q buffer free (the unit's last S MMA completed)
+// Barrier indices.  The K/V ring is organised in pairs: pair g carries V of
+// global tile g together with K of tile g+1 (which may be the first tile of
+// the next unit), so one barrier tracks both copies and one commit releases
+// both buffers.  K of the very first tile of a CTA has its own barrier.
+constexpr int BAR_Q = 0;                                 // Q tiles landed
+constexpr int BAR_K0 = 1;                                // first K tile landed
+__host__ __device__ constexpr int BAR_KVF(int b) { return 2 + b; }  // pair landed
+__host__ __device__ constexpr int BAR_KVE(int b) { return 4 + b; }  // pair consumed
+__host__ __device__ constexpr int BAR_SF(int s) { return 6 + s; }   // S_s computed
+__host__ __device__ constexpr int BAR_PF(int s) { return 8 + s; }   // P_s written
+__host__ __device__ constexpr int BAR_OD(int s) { return 10 + s; }  // O_s final
+constexpr int BAR_CLEAN = 12;
+constexpr int BAR_QE = 13;  // Q buffer free (the unit's last S MMA completed)
 
 struct TcParams {
   CUtensorMap tm_q;
@@ -192,11 +194,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(BAR_Q), 1);
     ptx::mbar_init(bar(BAR_QE), 1);
-    for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(bar(BAR_KF(s)), 1);
-      ptx::mbar_init(bar(BAR_KE(s)), 1);
-      ptx::mbar_init(bar(BAR_VF(s)), 1);
-      ptx::mbar_init(bar(BAR_VE(s)), 1);
+    ptx::mbar_init(bar(BAR_K0), 1);
+    for (int b = 0; b < kStages; ++b) {
+      ptx::mbar_init(bar(BAR_KVF(b)), 1);
+      ptx::mbar_init(bar(BAR_KVE(b)), 1);
     }
     for (int s = 0; s < kSlots; ++s) {
       ptx::mbar_init(bar(BAR_SF(s)), 1);
@@ -230,12 +231,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       ptx::tma_prefetch_desc(&p.tm_q);
       ptx::tma_prefetch_desc(&p.tm_k);
       ptx::tma_prefetch_desc(&p.tm_v);
-      uint32_t gk = 0, gv = 0;  // K / V tiles issued so far (ring position)
-      uint32_t qn = 0;          // units whose Q was issued
+      uint32_t g = 0;       // pairs issued (global tile index)
+      uint32_t qn = 0;      // units whose Q was issued
+      bool k0 = false;      // first K tile issued
       bool ok = true;
+      auto load_tile = [&](const Unit& w, int t, bool is_k, uint32_t dst, uint32_t mbar) {
+        const bool lm = t < w.n_lm_tiles;
+        const CUtensorMap* m = is_k ? (lm ? &p.tm_klm : &p.tm_k) : (lm ? &p.tm_vlm : &p.tm_v);
+        const int row = lm ? t * kBN : (w.kt_lo + t - w.n_lm_tiles) * kBN;
+        for (int c = 0; c < 2; ++c)
+          ptx::tma_load_3d(dst + c * kChunkBytes, m, mbar, c * 64, w.kvh, row);
+      };
       for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
         const Unit w = decode_unit(p, u);
         if (w.T == 0) continue;
+        // The next unit of this CTA that has tiles: its first K rides with
+        // this unit's last V.
+        int un = u + gridDim.x;
+        Unit nw{};
+        while (un < p.units) {
+          nw = decode_unit(p, un);
+          if (nw.T > 0) break;
+          un += gridDim.x;
+        }
+        const bool has_next = un < p.units;
         // The Q buffer is free once the previous unit's last S MMA is done.
         if (qn > 0 && !(ok = wait_bar(bar(BAR_QE), (qn - 1) & 1, ctl))) break;
         ptx::mbar_arrive_expect_tx(bar(BAR_Q), w.n_slots * kTileBytes);
@@ -246,42 +265,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         ++qn;
         // Warm L2 with this CTA's next Q tiles: they are read once, from
         // HBM, exactly when the tensor pipe waits for them.
-        if (u + static_cast<int>(gridDim.x) < p.units) {
-          const Unit nw = decode_unit(p, u + gridDim.x);
+        if (has_next)
           for (int s = 0; s < nw.n_slots; ++s)
             for (int c = 0; c < 2; ++c)
               ptx::tma_prefetch_3d(&p.tm_q, c * 64, nw.h0 + s, static_cast<int>(nw.qr0));
+        if (!k0) {
+          ptx::mbar_arrive_expect_tx(bar(BAR_K0), kTileBytes);
+          load_tile(w, 0, true, sb + kOffK + (g & 1) * kTileBytes, bar(BAR_K0));
+          k0 = true;
         }
-        for (int t = 0; t < w.T; ++t) {
-          const bool lm = t < w.n_lm_tiles;
-          const CUtensorMap* mk = lm ? &p.tm_klm : &p.tm_k;
-          const CUtensorMap* mv = lm ? &p.tm_vlm : &p.tm_v;
-          const int row = lm ? t * kBN : (w.kt_lo + t - w.n_lm_tiles) * kBN;
-          int st = gk & 1;
-          if (!(ok = wait_bar(bar(BAR_KE(st)), ((gk >> 1) & 1) ^ 1, ctl))) break;
-          ptx::mbar_arrive_expect_tx(bar(BAR_KF(st)), kTileBytes);
-          for (int c = 0; c < 2; ++c)
-            ptx::tma_load_3d(sb + kOffK + st * kTileBytes + c * kChunkBytes, mk, bar(BAR_KF(st)),
-                             c * 64, w.kvh, row);
-          ++gk;
-          st = gv & 1;
-          if (!(ok = wait_bar(bar(BAR_VE(st)), ((gv >> 1) & 1) ^ 1, ctl))) break;
-          ptx::mbar_arrive_expect_tx(bar(BAR_VF(st)), kTileBytes);
-          for (int c = 0; c < 2; ++c)
-            ptx::tma_load_3d(sb + kOffV + st * kTileBytes + c * kChunkBytes, mv, bar(BAR_VF(st)),
-                             c * 64, w.kvh, row);
-          ++gv;
+        for (int t = 0; t < w.T; ++t, ++g) {
+          const int b = g & 1;
+          // Pair g refills the buffers of pair g-2.  Pair 1's K buffer held
+          // the CTA's first K tile instead, whose release is the first
+          // completion of barrier 1; barrier 0's first wait passes at once.
+          const uint32_t parity = b == 0 ? ((g >> 1) & 1) ^ 1 : (g >> 1) & 1;
+          if (!(ok = wait_bar(bar(BAR_KVE(b)), parity, ctl))) break;
+          const bool with_k = (t + 1 < w.T) || has_next;
+          ptx::mbar_arrive_expect_tx(bar(BAR_KVF(b)), with_k ? 2 * kTileBytes : kTileBytes);
+          load_tile(w, t, false, sb + kOffV + b * kTileBytes, bar(BAR_KVF(b)));
+          if (t + 1 < w.T)
+            load_tile(w, t + 1, true, sb + kOffK + ((g + 1) & 1) * kTileBytes, bar(BAR_KVF(b)));
+          else if (has_next)
+            load_tile(nw, 0, true, sb + kOffK + ((g + 1) & 1) * kTileBytes, bar(BAR_KVF(b)));
         }
       }
       // Drain: every copy this thread issued must have landed before exit.
       if (qn > 0) drain_bar(bar(BAR_Q), (qn - 1) & 1, p.status);
-      for (int s = 0; s < kStages; ++s) {
-        int last = static_cast<int>(gk) - 1;
-        if (last >= 0 && (last & 1) != s) --last;
-        if (last >= 0) drain_bar(bar(BAR_KF(s)), (last >> 1) & 1, p.status);
-        last = static_cast<int>(gv) - 1;
-        if (last >= 0 && (last & 1) != s) --last;
-        if (last >= 0) drain_bar(bar(BAR_VF(s)), (last >> 1) & 1, p.status);
+      if (k0) drain_bar(bar(BAR_K0), 0, p.status);
+      for (int b = 0; b < kStages; ++b) {
+        int last = static_cast<int>(g) - 1;
+        if (last >= 0 && (last & 1) != b) --last;
+        if (last >= 0) drain_bar(bar(BAR_KVF(b)), (last >> 1) & 1, p.status);
       }
     }
   } else if (warp == 1) {
@@ -321,36 +336,45 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       uint32_t g = 0;                 // global tile index (K/V ring position)
       uint32_t qn = 0;                // units processed
       uint32_t sc[kSlots] = {0, 0};   // tiles processed per slot (SF/PF phases)
-      uint32_t oc[kSlots] = {0, 0};   // units processed per slot (OD phases)
+      bool first = true;              // first unit: K tile 0 has its own barrier
+      int pending = -1;               // pair whose K feeds the next unit's S(0)
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
         const Unit w = decode_unit(p, u);
         if (w.T == 0) continue;
         if (!(ok = wait_bar(bar(BAR_Q), qn & 1, ctl))) break;
-        if (!(ok = wait_bar(bar(BAR_KF(g & 1)), (g >> 1) & 1, ctl))) break;
+        const bool first_unit = first;
+        if (first) {
+          if (!(ok = wait_bar(bar(BAR_K0), 0, ctl))) break;
+          first = false;
+        }
+        // (Otherwise K of this tile came with the previous unit's last pair,
+        // which that unit's last iteration waited for.)
         ptx::tc_fence_after();
         for (int s = 0; s < w.n_slots; ++s) {
           issue_s(s, g & 1);
           ptx::mma_commit(bar(BAR_SF(s)));
         }
+        // The first K tile's buffer is refilled by pair 1: release it.
+        if (first_unit) ptx::mma_commit(bar(BAR_KVE(1)));
         if (w.T == 1) ptx::mma_commit(bar(BAR_QE));  // the unit's last S MMA
-        ptx::mma_commit(bar(BAR_KE(g & 1)));
+        if (pending >= 0) {
+          ptx::mma_commit(bar(BAR_KVE(pending & 1)));
+          pending = -1;
+        }
         for (int t = 0; ok && t < w.T; ++t, ++g) {
-          const uint32_t st = g & 1;
+          const uint32_t b = g & 1;
           const bool nxt = t + 1 < w.T;
-          if (!(ok = wait_bar(bar(BAR_VF(st)), (g >> 1) & 1, ctl))) break;
+          // Pair g: V of this tile and K of the next one.
+          if (!(ok = wait_bar(bar(BAR_KVF(b)), (g >> 1) & 1, ctl))) break;
           for (int s = 0; s < w.n_slots; ++s) {
             if (!(ok = wait_bar(bar(BAR_PF(s)), (sc[s] + t) & 1, ctl))) break;
             ptx::tc_fence_after();
             // PV_s(t) reads P_s(t) from the S columns; S_s(t+1) overwrites
             // them and is issued after it by this same thread.
-            issue_pv(s, st, t == 0);
+            issue_pv(s, b, t == 0);
             if (nxt) {
-              if (s == 0) {
-                if (!(ok = wait_bar(bar(BAR_KF(st ^ 1)), ((g + 1) >> 1) & 1, ctl))) break;
-                ptx::tc_fence_after();
-              }
-              issue_s(s, st ^ 1);
+              issue_s(s, b ^ 1);
               ptx::mma_commit(bar(BAR_SF(s)));
             } else {
               ptx::mma_commit(bar(BAR_OD(s)));
@@ -358,16 +382,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           }
           if (!ok) break;
           if (t + 2 == w.T) ptx::mma_commit(bar(BAR_QE));  // S(T-1) was the last S
-          ptx::mma_commit(bar(BAR_VE(st)));
-          if (nxt) ptx::mma_commit(bar(BAR_KE(st ^ 1)));
+          if (nxt)
+            ptx::mma_commit(bar(BAR_KVE(b)));
+          else
+            pending = static_cast<int>(g);  // released after the next unit's S(0)
         }
-        for (int s = 0; s < w.n_slots; ++s) {
-          sc[s] += w.T;
-          oc[s] += 1;
-        }
+        for (int s = 0; s < w.n_slots; ++s) sc[s] += w.T;
         ++qn;
       }
-      (void)oc;
+      if (pending >= 0) ptx::mma_commit(bar(BAR_KVE(pending & 1)));
       // Drain: all MMAs issued so far complete before TMEM is released.
       ptx::mma_commit(bar(BAR_CLEAN));
       drain_bar(bar(BAR_CLEAN), 0, p.status);
