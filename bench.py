@@ -81,6 +81,23 @@ def useful_flops(wl) -> float:
     return 4.0 * wl.d * wl.Hq * attended_total(wl)
 
 
+def reduce_max(value: float, dist, device) -> float:
+    """Maximum of a per-rank timing over all ranks (the slowest replica sets
+    the job's time); identity without a process group."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank: float, ms_per_step: float) -> float:
+    """Whole-job units per second: every rank processes units_per_rank per
+    step (weak scaling) and the step takes the slowest rank's time."""
+    return world * units_per_rank / (ms_per_step * 1e-3)
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     """Samples SM clock and throttle reasons with nvidia-smi while running."""
@@ -334,15 +351,11 @@ def main():
     with ClockSampler(local_rank) as clk:
         res = run_window_landmark(wl, args.steps, args.warmup, dev, B, torch)
     barrier()
-    total_ms = res["total_ms"]
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(res["total_ms"], dist, dev)
     ms_per_step = total_ms / args.steps
     flops = useful_flops(wl)
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
-    tokens_per_s = world * wl.n / (ms_per_step * 1e-3)
+    value = job_throughput(world, flops, ms_per_step) / 1e12
+    tokens_per_s = job_throughput(world, wl.n, ms_per_step)
     attn_tflops = flops / (res["attn_ms"] * 1e-3) / 1e12
     pool_bytes = 2 * wl.n * wl.Hkv * wl.d * 2 + 2 * wl.G * wl.Hkv * wl.d * 2
     # Q, K, V and the landmarks read once, O (bf16) and lse written once.
