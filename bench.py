@@ -50,8 +50,8 @@ def load_peaks():
 # applies to the kernel source it was measured on (SHA-256 of
 # k2_attn_tc.cu); after any change the traffic is reported as null.
 ATTN_TRAFFIC = {"128k_70b_layer": {
-    "bytes": 2.689312e9 + 2.140172e9,
-    "kernel_sha256": "e531575fe3bc196001a906d0dc8d15c65a3d0cbb62daae40c8755013f3acf81a"}}
+    "bytes": 2.709777e9 + 2.142333e9,
+    "kernel_sha256": "3d1e704361e4ebf3044434f1912ba81267f81924b647b02ac2406d9c9b27e516"}}
 
 
 def kernel_sha256() -> str:
