@@ -254,14 +254,30 @@ def run_ring(wl, steps, warmup, dev, B, torch):
         if ev is not None:
             ev[2].record(stream)
 
+    def fused_step():
+        # One ring layer with the aggregation inside every round.
+        B.attn_fwd_partial(q, k[:c], v[:c], o_parts[0], l_parts[0], 0, 0, wl.window, wl.scale,
+                           stream=stream)
+        for p in range(1, P):
+            B.attn_fwd_partial_merge(q, k[p * c:(p + 1) * c], v[p * c:(p + 1) * c], o_parts[0],
+                                     l_parts[0], 0, p * c, wl.window, wl.scale, stream=stream)
+
     for _ in range(warmup):
         step()
+        fused_step()
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     for s in range(steps):
         step(evs[s])
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for s in range(steps):
+        fused_step()
+    f1.record(stream)
     torch.cuda.synchronize()
     assert B.device_status() == 0
+    fused_ms = f0.elapsed_time(f1) / steps
     part_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     merge_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     # Required merge bytes: every lse_p, every O_p row with finite lse_p, output.
@@ -270,7 +286,7 @@ def run_ring(wl, steps, warmup, dev, B, torch):
     del q, k, v, o_parts, l_parts, out, lse
     torch.cuda.empty_cache()
     return {"partials_ms": part_ms, "merge_ms": merge_ms, "merge_bytes": merge_bytes,
-            "launches_per_step": P + 1}
+            "fused_ms": fused_ms, "launches_per_step": P + 1}
 
 
 def cpu_baseline(wl, rows_target, torch):
@@ -423,6 +439,8 @@ def main():
             "merge_gbs": round(rr["merge_bytes"] / (rr["merge_ms"] * 1e-3) / 1e9, 1),
             "merge_frac_hbm": round(rr["merge_bytes"] / (rr["merge_ms"] * 1e-3) / 1e9
                                     / peaks["hbm_gbs"], 4),
+            "fused_rounds_ms": round(rr["fused_ms"], 3),
+            "fused_rounds_tflops": round(fr / (rr["fused_ms"] * 1e-3) / 1e12, 2),
             "steps": 3}
         line["also"] = also
 

@@ -128,6 +128,33 @@ msa_status msa_attn_fwd_partial(const void *q, const void *k_chunk,
                                  int Hkv, int d, int64_t window, float scale,
                                  msa_dtype in_dt, msa_stream_t stream);
 
+/*
+ * One Ring Attention round with its aggregation fused in ("Training at 1M+
+ * Token Context", Ring Attention paragraph: each round computes partial
+ * attention against one KV block and immediately aggregates the softmax
+ * statistics).  Computes the partial of msa_attn_fwd_partial for queries
+ * q_start.. against the chunk kv_start.., and merges it into the running
+ * result in place:
+ *   lse_run <- ln(exp(lse_run) + exp(lse_p)),
+ *   out_run <- exp(lse_run_old - lse_run) out_run + exp(lse_p - lse_run) O_p,
+ * so the partial never reaches HBM.  Rows with no key in the chunk are left
+ * untouched.  A row whose lse_run is -inf takes O_p as is (out_run is not
+ * read there), so a fresh run starts from lse_run = -inf and any out_run.
+ * After every chunk has been merged (any order), out_run/lse_run equal the
+ * single-pass msa_attn_fwd result up to rounding.
+ *   q        [n_q, Hq, d] in `in_dt`;  k_chunk, v_chunk [n_kv, Hkv, d]
+ *   out_run  [n_q, Hq, d] fp32, read and written
+ *   lse_run  [Hq, n_q] fp32, read and written
+ * Errors: as msa_attn_fwd_partial.
+ */
+msa_status msa_attn_fwd_partial_merge(const void *q, const void *k_chunk,
+                                       const void *v_chunk, float *out_run,
+                                       float *lse_run, int64_t n_q,
+                                       int64_t q_start, int64_t n_kv,
+                                       int64_t kv_start, int Hq, int Hkv, int d,
+                                       int64_t window, float scale,
+                                       msa_dtype in_dt, msa_stream_t stream);
+
 /* Largest number of partials msa_lse_merge accepts in one call. */
 #define MSA_MAX_MERGE_PARTS 64
 

@@ -21,8 +21,8 @@ MAX_MERGE_PARTS = 64
 
 # Every symbol include/msa.h declares.
 EXPORTS = ("msa_version", "msa_last_error_string", "msa_landmark_pool", "msa_attn_fwd",
-           "msa_attn_fwd_partial", "msa_lse_merge", "msa_attn_uses_tensor_cores",
-           "msa_device_status", "msa_debug_set_wait_limit_ns")
+           "msa_attn_fwd_partial", "msa_attn_fwd_partial_merge", "msa_lse_merge",
+           "msa_attn_uses_tensor_cores", "msa_device_status", "msa_debug_set_wait_limit_ns")
 
 
 class MsaError(RuntimeError):
@@ -47,6 +47,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_attn_fwd_partial.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, i32,
                                          i64, f32, i32, vp]
     lib.msa_attn_fwd_partial.restype = i32
+    lib.msa_attn_fwd_partial_merge.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32,
+                                               i32, i64, f32, i32, vp]
+    lib.msa_attn_fwd_partial_merge.restype = i32
     lib.msa_lse_merge.argtypes = [vp, vp, i32, vp, vp, i64, i32, i32, i32, vp]
     lib.msa_lse_merge.restype = i32
     lib.msa_attn_uses_tensor_cores.argtypes = [i32, i32, i32, i32]
@@ -133,6 +136,17 @@ def attn_fwd_partial(q, k_chunk, v_chunk, out_part, lse_part, q_start: int, kv_s
     _check(_lib.msa_attn_fwd_partial(_ptr(q), _ptr(k_chunk), _ptr(v_chunk), _ptr(out_part),
                                      _ptr(lse_part), n_q, int(q_start), n_kv, int(kv_start), Hq,
                                      Hkv, d, int(window), float(scale), _dt(q), _stream(stream)))
+
+
+def attn_fwd_partial_merge(q, k_chunk, v_chunk, out_run, lse_run, q_start: int, kv_start: int,
+                           window: int, scale: float, stream=None) -> None:
+    """msa_attn_fwd_partial_merge: one ring round merged into (out_run, lse_run) in place."""
+    n_q, Hq, d = q.shape
+    n_kv, Hkv, _ = k_chunk.shape
+    _check(_lib.msa_attn_fwd_partial_merge(_ptr(q), _ptr(k_chunk), _ptr(v_chunk), _ptr(out_run),
+                                           _ptr(lse_run), n_q, int(q_start), n_kv, int(kv_start),
+                                           Hq, Hkv, d, int(window), float(scale), _dt(q),
+                                           _stream(stream)))
 
 
 def lse_merge(o_parts, lse_parts, out, lse, stream=None) -> None:

@@ -46,17 +46,30 @@ def msa_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int
 
 def ring_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_chunks: int,
                    window: int | None = None, scale: float | None = None,
-                   out_dtype: torch.dtype | None = None, stream=None):
+                   out_dtype: torch.dtype | None = None, fused: bool = True, stream=None):
     """Causal (windowed) attention computed as a Ring Attention layer would:
-    the KV sequence is cut into ``n_chunks`` contiguous chunks, each chunk's
-    partial (O_p fp32, lse_p) is computed against all queries, and the
-    partials are merged by their log-sum-exps.  Returns (out, lse)."""
+    the KV sequence is cut into ``n_chunks`` contiguous chunks and each
+    chunk's partial is aggregated by log-sum-exp.  ``fused`` merges every
+    chunk into a running fp32 result inside the attention kernel (the
+    partials never reach HBM); otherwise all partials are written and merged
+    by ``msa_lse_merge`` at the end.  Returns (out, lse); with ``fused`` the
+    output is fp32 (the running accumulator)."""
     n, Hq, d = q.shape
     if n % n_chunks != 0:
         raise ValueError("n must be a multiple of n_chunks")
     window = n if window is None else window
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     c = n // n_chunks
+    if fused:
+        # The first round writes the running result (rows with no key get
+        # lse = -inf, which later rounds treat as empty); the others merge.
+        out = torch.empty((n, Hq, d), dtype=torch.float32, device=q.device)
+        lse = torch.empty((Hq, n), dtype=torch.float32, device=q.device)
+        B.attn_fwd_partial(q, k[:c], v[:c], out, lse, 0, 0, window, scale, stream=stream)
+        for p in range(1, n_chunks):
+            B.attn_fwd_partial_merge(q, k[p * c:(p + 1) * c], v[p * c:(p + 1) * c], out, lse, 0,
+                                     p * c, window, scale, stream=stream)
+        return out, lse
     o_parts = [torch.empty((n, Hq, d), dtype=torch.float32, device=q.device)
                for _ in range(n_chunks)]
     lse_parts = [torch.empty((Hq, n), dtype=torch.float32, device=q.device)

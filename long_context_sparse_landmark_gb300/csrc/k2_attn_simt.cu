@@ -158,21 +158,42 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnArgs a) {
   if (!row_ok) return;
   const int64_t lse_idx = static_cast<int64_t>(h) * a.n_q + i_loc;
   if (l == 0.f) {  // no key for this row (only possible for a partial)
+    if (a.merge) return;  // a running merge leaves the row untouched
     if (qd == 0) a.lse[lse_idx] = -INFINITY;
     if (a.partial) return;
   }
-  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const float lse_p = l > 0.f ? m + logf(l) : -INFINITY;
+  float w_new = l > 0.f ? 1.f / l : 0.f;
+  float w_run = 0.f;
+  float lse_out = lse_p;
+  if (a.merge) {  // lse_run <- ln(e^lse_run + e^lse_p), O <- O w_run + O_p w
+    const float L = a.lse[lse_idx];
+    if (L != -INFINITY) {
+      const float mx = fmaxf(L, lse_p);
+      lse_out = mx + logf(expf(L - mx) + expf(lse_p - mx));
+      w_run = expf(L - lse_out);
+      w_new *= expf(lse_p - lse_out);
+    }
+  }
   const int64_t obase = (i_loc * a.Hq + h) * static_cast<int64_t>(D);
   if (a.out_bf16) {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + obase;
 #pragma unroll
-    for (int e = 0; e < DQ; ++e) out[4 * e + qd] = __float2bfloat16_rn(o[e] * inv);
+    for (int e = 0; e < DQ; ++e) out[4 * e + qd] = __float2bfloat16_rn(o[e] * w_new);
   } else {
     float* out = static_cast<float*>(a.out) + obase;
+    if (w_run != 0.f) {
 #pragma unroll
-    for (int e = 0; e < DQ; ++e) out[4 * e + qd] = o[e] * inv;
+      for (int e = 0; e < DQ; ++e) out[4 * e + qd] = fmaf(out[4 * e + qd], w_run, o[e] * w_new);
+    } else {
+#pragma unroll
+      for (int e = 0; e < DQ; ++e) out[4 * e + qd] = o[e] * w_new;
+    }
   }
-  if (qd == 0 && l > 0.f) a.lse[lse_idx] = m + logf(l);
+  // All four threads of the row have read the running lse above; the row's
+  // first thread writes it only after the other three are past that read.
+  __syncwarp();
+  if (qd == 0 && l > 0.f) a.lse[lse_idx] = lse_out;
 }
 
 template <bool kBf16In, int D>

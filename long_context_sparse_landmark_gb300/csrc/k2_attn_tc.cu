@@ -100,7 +100,7 @@ struct TcParams {
   float* lse;
   int64_t n_q, q_start, n_kv, kv_start, window, block;
   int Hq, Hkv, G, group, pairs, n_qtiles, units;
-  int out_bf16, partial;
+  int out_bf16, partial, merge;
   float scale_log2;
   int* status;
   uint64_t wait_ns;
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const int64_t i = p.q_start + i_loc;
       const int h = w.h0 + slot;
       if (w.T == 0) {  // no key for any row of this unit (partial chunks only)
-        if (row_ok) p.lse[static_cast<int64_t>(h) * p.n_q + i_loc] = -INFINITY;
+        if (row_ok && !p.merge) p.lse[static_cast<int64_t>(h) * p.n_q + i_loc] = -INFINITY;
         continue;
       }
       const int64_t my_lo = max64(i - p.window + 1, p.kv_start);
@@ -524,7 +524,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       // arrives for the next unit's first P, which the MMA thread waits for
       // before the next unit's first PV overwrites O.
       const bool has = row_ok && l > 0.f;
-      const float inv = has ? 1.f / l : 0.f;
+      const int64_t lse_idx = static_cast<int64_t>(h) * p.n_q + i_loc;
+      // O = acc * w_new (+ running O * w_run when merging into a running
+      // result: lse_run <- ln(e^lse_run + e^lse_p)).
+      const float lse_p = has ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+      float w_new = has ? 1.f / l : 0.f;
+      float w_run = 0.f;
+      float lse_out = lse_p;
+      if (p.merge && has) {
+        const float L = p.lse[lse_idx];
+        if (L != -INFINITY) {
+          const float mx = fmaxf(L, lse_p);
+          lse_out = mx + logf(expf(L - mx) + expf(lse_p - mx));
+          w_run = expf(L - lse_out);
+          w_new *= expf(lse_p - lse_out);
+        }
+      }
       const int64_t obase = (i_loc * p.Hq + h) * static_cast<int64_t>(kD);
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
@@ -538,25 +553,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               uint4 q4;
-              q4.x = ptx::pack_bf16x2(o[8 * v + 0] * inv, o[8 * v + 1] * inv);
-              q4.y = ptx::pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv);
-              q4.z = ptx::pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv);
-              q4.w = ptx::pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv);
+              q4.x = ptx::pack_bf16x2(o[8 * v + 0] * w_new, o[8 * v + 1] * w_new);
+              q4.y = ptx::pack_bf16x2(o[8 * v + 2] * w_new, o[8 * v + 3] * w_new);
+              q4.z = ptx::pack_bf16x2(o[8 * v + 4] * w_new, o[8 * v + 5] * w_new);
+              q4.w = ptx::pack_bf16x2(o[8 * v + 6] * w_new, o[8 * v + 7] * w_new);
               dst[v] = q4;
             }
           } else {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + cc * 32);
+            if (w_run != 0.f) {
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[v] = make_float4(o[4 * v] * inv, o[4 * v + 1] * inv, o[4 * v + 2] * inv,
-                                   o[4 * v + 3] * inv);
+              for (int v = 0; v < 8; ++v) {
+                const float4 r = dst[v];
+                dst[v] = make_float4(fmaf(r.x, w_run, o[4 * v] * w_new),
+                                     fmaf(r.y, w_run, o[4 * v + 1] * w_new),
+                                     fmaf(r.z, w_run, o[4 * v + 2] * w_new),
+                                     fmaf(r.w, w_run, o[4 * v + 3] * w_new));
+              }
+            } else {
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                dst[v] = make_float4(o[4 * v] * w_new, o[4 * v + 1] * w_new, o[4 * v + 2] * w_new,
+                                     o[4 * v + 3] * w_new);
+            }
           }
         }
       }
-      if (row_ok) {
-        p.lse[static_cast<int64_t>(h) * p.n_q + i_loc] =
-            l > 0.f ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
-      }
+      // Rows without a key: -inf (a partial), or untouched (a running merge).
+      if (row_ok && (has || !p.merge)) p.lse[lse_idx] = lse_out;
       sc += w.T;
       oc += 1;
     }
@@ -652,6 +676,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s, const char** why) 
   p.n_qtiles = static_cast<int>((a.n_q + kBM - 1) / kBM);
   p.out_bf16 = a.out_bf16;
   p.partial = a.partial;
+  p.merge = a.merge;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = a.status;
   p.wait_ns = a.wait_limit_ns;

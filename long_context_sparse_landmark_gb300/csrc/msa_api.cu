@@ -203,6 +203,44 @@ msa_status msa_attn_fwd_partial(const void* q, const void* k_chunk, const void* 
   return run_attn(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+msa_status msa_attn_fwd_partial_merge(const void* q, const void* k_chunk, const void* v_chunk,
+                                       float* out_run, float* lse_run, int64_t n_q,
+                                       int64_t q_start, int64_t n_kv, int64_t kv_start, int Hq,
+                                       int Hkv, int d, int64_t window, float scale,
+                                       msa_dtype in_dt, msa_stream_t stream) {
+  msa_status st =
+      check_attn_common(q, k_chunk, v_chunk, out_run, lse_run, Hq, Hkv, d, window, scale, in_dt);
+  if (st != MSA_OK) return st;
+  if (n_q < 1 || n_q > kMaxRows || n_kv < 1 || n_kv > kMaxRows)
+    return fail(MSA_ERR_INVALID_ARG, "n_q=%lld n_kv=%lld out of range", (long long)n_q,
+                (long long)n_kv);
+  if (q_start < 0 || kv_start < 0)
+    return fail(MSA_ERR_INVALID_ARG, "q_start=%lld kv_start=%lld must be >= 0",
+                (long long)q_start, (long long)kv_start);
+  msa::AttnArgs a{};
+  a.q = q;
+  a.k = k_chunk;
+  a.v = v_chunk;
+  a.out = out_run;
+  a.lse = lse_run;
+  a.n_q = n_q;
+  a.q_start = q_start;
+  a.n_kv = n_kv;
+  a.kv_start = kv_start;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.window = window;
+  a.G = 0;
+  a.block = 1;
+  a.scale = scale;
+  a.in_bf16 = in_dt == MSA_BF16;
+  a.out_bf16 = 0;
+  a.partial = 1;
+  a.merge = 1;
+  return run_attn(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 msa_status msa_lse_merge(const float* const* o_parts, const float* const* lse_parts, int n_parts,
                          void* out, float* lse, int64_t n, int Hq, int d, msa_dtype out_dt,
                          msa_stream_t stream) {

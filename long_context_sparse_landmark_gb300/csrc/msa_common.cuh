@@ -80,6 +80,7 @@ struct AttnArgs {
   int in_bf16;
   int out_bf16;
   int partial;  // rows with no key: lse = -inf, out row untouched
+  int merge;    // out/lse hold a running result: merge this partial into it
   int* status;  // device status word
   uint64_t wait_limit_ns;
 };

@@ -112,6 +112,24 @@ def test_partial_validation(lib):
     assert call(d=32) == 2
 
 
+def test_partial_merge_validation(lib):
+    f = lib.msa_attn_fwd_partial_merge
+
+    def call(**kw):
+        a = dict(q=GOOD, k=GOOD, v=GOOD, o=GOOD, l=GOOD, nq=128, qs=0, nkv=64, kvs=0, Hq=2, Hkv=1,
+                 d=128, w=128, idt=1)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["o"], a["l"], a["nq"], a["qs"], a["nkv"], a["kvs"],
+                 a["Hq"], a["Hkv"], a["d"], a["w"], ctypes.c_float(0.1), a["idt"], None)
+
+    assert call(l=None) == 1
+    assert call(o=BAD_ALIGN) == 1
+    assert call(nkv=0) == 1
+    assert call(kvs=-1) == 1
+    assert call(Hq=3, Hkv=2) == 1
+    assert call(d=32) == 2
+
+
 def test_merge_validation(lib):
     f = lib.msa_lse_merge
     arr = (ctypes.c_void_p * 2)(1 << 20, 2 << 20)

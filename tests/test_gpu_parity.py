@@ -185,6 +185,53 @@ def test_partial_merge_small(dt, d, n, chunks, w):
     compare(lse.cpu().numpy(), rl, mx, mean, "merged lse")
 
 
+# ------------------------------------------------------------------ fused ring rounds
+@pytest.mark.parametrize("dt,d", [("bf16", 128), ("f32", 64), ("bf16", 64), ("f32", 128)])
+@pytest.mark.parametrize("n,chunks,w,order", [(512, 4, 512, "fwd"), (384, 3, 100, "rev"),
+                                              (1000, 8, 1000, "mixed"), (257, 2, 64, "fwd")])
+def test_partial_merge_running_result(dt, d, n, chunks, w, order):
+    """Chunks merged into a running (O, lse) in any order equal the oracle's
+    single pass; rows never reached keep their initial (garbage) O."""
+    B = binding()
+    wl = Workload("ring_run", n, 4, 2, d, w, 0, dt, seed=3 * n + chunks)
+    q, k, v = generate(wl, device=DEV)
+    bounds = np.linspace(0, n, chunks + 1).astype(int)
+    pieces = list(zip(bounds[:-1], bounds[1:]))
+    if order == "rev":
+        pieces = pieces[::-1]
+    elif order == "mixed":
+        pieces = pieces[1::2] + pieces[0::2]
+    out = torch.full((n, 4, d), float("nan"), dtype=torch.float32, device=DEV)
+    lse = torch.full((4, n), -float("inf"), dtype=torch.float32, device=DEV)
+    for lo, hi in pieces:
+        B.attn_fwd_partial_merge(q, k[lo:hi], v[lo:hi], out, lse, 0, int(lo), w, wl.scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attn(to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v), w, 0, wl.scale)
+    mx, mean = tol(dt)
+    compare(out.cpu().numpy(), ro, mx, mean, "running O")
+    compare(lse.cpu().numpy(), rl, mx, mean, "running lse")
+
+
+def test_ring_128k_fused_rounds():
+    """The ring workload through eight fused rounds equals the oracle on
+    sampled rows and the separate partial + merge path on every row."""
+    import long_context_sparse_landmark_gb300.api as api
+    wl = WORKLOADS["ring_128k"]
+    q, k, v = generate(wl, device=DEV)
+    out, lse = api.ring_attention(q, k, v, wl.ring_chunks, fused=True)
+    ref_o, ref_l = api.ring_attention(q, k, v, wl.ring_chunks, fused=False,
+                                      out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    compare(out.cpu().numpy(), ref_o.cpu().numpy(), 1e-2, 1e-3, "fused vs separate O")
+    compare(lse.cpu().numpy(), ref_l.cpu().numpy(), 1e-2, 1e-3, "fused vs separate lse")
+    del ref_o
+    rows = sample_rows(wl, count=512).numpy()
+    go, gl = gather_rows(out, lse, rows)
+    ro, rl = oracle_attention(q, k, v, wl, rows=rows)
+    compare(go, ro, 1e-2, 1e-3, "fused ring O vs oracle")
+    compare(gl, rl, 1e-2, 1e-3, "fused ring lse vs oracle")
+
+
 # ------------------------------------------------------------------ merge alone
 @pytest.mark.parametrize("P,n,Hq,d,out_dt", [(8, 1000, 4, 128, "f32"), (3, 257, 2, 64, "f32"),
                                              (64, 33, 2, 8, "f32"), (5, 500, 32, 128, "bf16"),
