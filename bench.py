@@ -331,6 +331,10 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--workload", default=HEADLINE,
                     help="window+landmark workload timed as the step (profiling uses smaller ones)")
+    ap.add_argument("--only", choices=["ring"], default=None,
+                    help="run only the ring emulation (partials, merge, fused rounds)")
+    ap.add_argument("--ring-n", type=int, default=None,
+                    help="tokens of the ring emulation (default 131072; smaller for profiling)")
     ap.add_argument("--no-also", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -357,6 +361,22 @@ def main():
         dist.init_process_group("nccl")
 
     from long_context_sparse_landmark_gb300 import _binding as B
+
+    if args.only == "ring":
+        wlr = WORKLOADS["ring_128k"]
+        if args.ring_n:
+            wlr = wlr.with_n(args.ring_n, name=f"ring_{args.ring_n}")
+        rr = run_ring(wlr, args.steps, args.warmup, dev, B, torch)
+        fr = useful_flops(wlr)
+        if rank == 0:
+            print(json.dumps({
+                "workload": wlr.name, "n": wlr.n, "Hq": wlr.Hq, "Hkv": wlr.Hkv, "d": wlr.d,
+                "chunks": wlr.ring_chunks, "partials_ms": round(rr["partials_ms"], 4),
+                "partials_tflops": round(fr / (rr["partials_ms"] * 1e-3) / 1e12, 2),
+                "merge_ms": round(rr["merge_ms"], 4), "merge_bytes": rr["merge_bytes"],
+                "merge_gbs": round(rr["merge_bytes"] / (rr["merge_ms"] * 1e-3) / 1e9, 1),
+                "fused_rounds_ms": round(rr["fused_ms"], 4)}), flush=True)
+        return
 
     def barrier():
         if dist is not None:

@@ -44,26 +44,29 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def _configure(lib):
+    """Declare the C signatures on a loaded oracle library."""
+    i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    vp = ctypes.c_void_p
+    lib.oracle_landmark_pool.argtypes = [vp, i32, i64, i32, i32, i32, vp]
+    lib.oracle_landmark_pool.restype = i32
+    lib.oracle_attn_rows.argtypes = [vp, vp, i64, vp, vp, i64, i64, i32,
+                                     i32, i32, i32, i64, vp, vp, i32, i64,
+                                     dbl, vp, vp]
+    lib.oracle_attn_rows.restype = i32
+    lib.oracle_lse_merge.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp]
+    lib.oracle_lse_merge.restype = i32
+    lib.oracle_set_threads.argtypes = [i32]
+    lib.oracle_get_threads.restype = i32
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        lib = ctypes.CDLL(build())
-        i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
-        vp = ctypes.c_void_p
-        lib.oracle_landmark_pool.argtypes = [vp, i32, i64, i32, i32, i32, vp]
-        lib.oracle_landmark_pool.restype = i32
-        lib.oracle_attn_rows.argtypes = [vp, vp, i64, vp, vp, i64, i64, i32,
-                                         i32, i32, i32, i64, vp, vp, i32, i64,
-                                         dbl, vp, vp]
-        lib.oracle_attn_rows.restype = i32
-        lib.oracle_lse_merge.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp]
-        lib.oracle_lse_merge.restype = i32
-        lib.oracle_set_threads.argtypes = [i32]
-        lib.oracle_get_threads.restype = i32
-        _lib = lib
-        return lib
+        if _lib is None:
+            _lib = _configure(ctypes.CDLL(build()))
+        return _lib
 
 
 def _dtype_code(a: np.ndarray) -> int:
