@@ -54,6 +54,9 @@ def _configure(lib):
                                      i32, i32, i32, i64, vp, vp, i32, i64,
                                      dbl, vp, vp]
     lib.oracle_attn_rows.restype = i32
+    lib.oracle_attn_band_rows.argtypes = [vp, vp, i64, vp, vp, i64, i32, i32,
+                                          i32, i32, i64, i64, dbl, vp, vp]
+    lib.oracle_attn_band_rows.restype = i32
     lib.oracle_lse_merge.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp]
     lib.oracle_lse_merge.restype = i32
     lib.oracle_set_threads.argtypes = [i32]
@@ -163,6 +166,36 @@ def attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int,
                                   _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError("attn: inconsistent arguments")
+    return out, lse
+
+
+def attn_band(q: np.ndarray, k: np.ndarray, v: np.ndarray, band_block: int,
+              band_half: int, scale: float, rows=None, q_positions=None):
+    """Block-band attention in fp64: row i attends every key of the blocks
+    (size band_block) within band_half blocks of its own, not causal.
+    Returns (O [n_rows, Hq, d], lse [Hq, n_rows])."""
+    q = np.ascontiguousarray(q)
+    k = np.ascontiguousarray(k)
+    v = np.ascontiguousarray(v)
+    dt = _dtype_code(q)
+    if _dtype_code(k) != dt or _dtype_code(v) != dt:
+        raise TypeError("q, k, v must share one dtype")
+    n_q, Hq, d = q.shape
+    n_kv, Hkv, _ = k.shape
+    if q_positions is not None:
+        pos = np.ascontiguousarray(np.asarray(q_positions, dtype=np.int64))
+        qg = q
+    else:
+        rows = np.arange(n_q, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+        qg = np.ascontiguousarray(q[rows])
+        pos = np.ascontiguousarray(rows)
+    out = np.empty((len(pos), Hq, d), dtype=np.float64)
+    lse = np.empty((Hq, len(pos)), dtype=np.float64)
+    rc = _load().oracle_attn_band_rows(_ptr(qg), _ptr(pos), len(pos), _ptr(k), _ptr(v), n_kv,
+                                       dt, Hq, Hkv, d, int(band_block), int(band_half),
+                                       float(scale), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("attn_band: inconsistent arguments")
     return out, lse
 
 

@@ -252,3 +252,77 @@ int oracle_lse_merge(const double *o_parts, const double *lse_parts, int P,
     }
     return 0;
 }
+
+/*
+ * Block-band attention (the 2-D block-sparse mask of "Million Token Context
+ * Window Optimization: What Actually Works", section "The indexing game:
+ * smarter context management": each 128-token block attends to 16 other
+ * blocks, left and right).  Reading taken: with
+ * block size bb and half-width hw, row i attends every key j of the blocks
+ * within hw of its own, |floor(j/bb) - floor(i/bb)| <= hw, 0 <= j < n_kv (not
+ * causal); one softmax, scores scale*<q,k>.
+ *   q [n_rows][Hq][d] at positions pos[]; k, v [n_kv][Hkv][d]
+ *   out [n_rows][Hq][d], lse [Hq][n_rows] (fp64)
+ */
+int oracle_attn_band_rows(const void *q, const int64_t *pos, int64_t n_rows,
+                          const void *k, const void *v, int64_t n_kv,
+                          int dtype, int Hq, int Hkv, int d, int64_t bb,
+                          int64_t hw, double scale, double *out,
+                          double *lse) {
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || bb < 1 || hw < 0)
+        return -1;
+    const int group = Hq / Hkv;
+#pragma omp parallel
+    {
+        double *sc = NULL;
+        int64_t cap = 0;
+#pragma omp for collapse(2) schedule(dynamic, 4)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            for (int h = 0; h < Hq; ++h) {
+                const int64_t i = pos[r];
+                const int c = h / group;
+                const int64_t bi = i / bb;
+                int64_t j_lo = (bi - hw) * bb;
+                if (j_lo < 0) j_lo = 0;
+                int64_t j_hi = (bi + hw + 1) * bb - 1;
+                if (j_hi > n_kv - 1) j_hi = n_kv - 1;
+                const int64_t nk = j_hi >= j_lo ? j_hi - j_lo + 1 : 0;
+                double *o = out + (r * Hq + h) * (int64_t)d;
+                if (nk == 0) {
+                    for (int e = 0; e < d; ++e) o[e] = 0.0;
+                    lse[(int64_t)h * n_rows + r] = -INFINITY;
+                    continue;
+                }
+                if (nk > cap) {
+                    free(sc);
+                    cap = nk;
+                    sc = (double *)malloc(sizeof(double) * (size_t)cap);
+                }
+                const int64_t qoff = (r * Hq + h) * (int64_t)d;
+                double m = -INFINITY;
+                for (int64_t t = 0; t < nk; ++t) {
+                    const int64_t koff = ((j_lo + t) * Hkv + c) * (int64_t)d;
+                    double dot = 0.0;
+                    for (int e = 0; e < d; ++e)
+                        dot += oracle_load(q, qoff + e, dtype) *
+                               oracle_load(k, koff + e, dtype);
+                    sc[t] = scale * dot;
+                    if (sc[t] > m) m = sc[t];
+                }
+                double denom = 0.0;
+                for (int e = 0; e < d; ++e) o[e] = 0.0;
+                for (int64_t t = 0; t < nk; ++t) {
+                    const double p = exp(sc[t] - m);
+                    denom += p;
+                    const int64_t voff = ((j_lo + t) * Hkv + c) * (int64_t)d;
+                    for (int e = 0; e < d; ++e)
+                        o[e] += p * oracle_load(v, voff + e, dtype);
+                }
+                for (int e = 0; e < d; ++e) o[e] /= denom;
+                lse[(int64_t)h * n_rows + r] = m + log(denom);
+            }
+        }
+        free(sc);
+    }
+    return 0;
+}

@@ -366,3 +366,69 @@ def test_p6_page_dot_product_arithmetic():
     # "Training at 1M+ Token Context", memory paragraph: the KV cache of one
     # layer at 1M tokens, 8 KV heads x 128 x bf16, is about 2 GB per tensor.
     assert abs(wl.n * wl.Hkv * wl.d * 2 / 2**30 - 2.0) < 1e-9
+
+
+# ------------------------------------------------------------------- band mask
+def band_bruteforce(q, k, v, bb, hw, scale):
+    """Dense [n, n] band mask built element by element from its definition
+    (key block within hw blocks of the row's block), masked softmax."""
+    q = q.astype(np.float64)
+    k = k.astype(np.float64)
+    v = v.astype(np.float64)
+    n, Hq, d = q.shape
+    g = Hq // k.shape[1]
+    mask = np.zeros((n, n), dtype=bool)
+    for i in range(n):
+        for j in range(n):
+            mask[i, j] = abs(j // bb - i // bb) <= hw
+    out = np.zeros((n, Hq, d))
+    lse = np.zeros((Hq, n))
+    for h in range(Hq):
+        s = np.where(mask, scale * q[:, h] @ k[:, h // g].T, -np.inf)
+        mx = s.max(axis=1, keepdims=True)
+        e = np.where(mask, np.exp(s - mx), 0.0)
+        den = e.sum(axis=1, keepdims=True)
+        out[:, h] = (e / den) @ v[:, h // g]
+        lse[h] = (mx + np.log(den))[:, 0]
+    return out, lse
+
+
+@pytest.mark.parametrize("n,bb,hw", [(1, 1, 0), (40, 4, 0), (40, 4, 2), (37, 8, 1), (64, 16, 3),
+                                     (50, 7, 10)])
+def test_band_bruteforce(oracle_mod, n, bb, hw):
+    rng = np.random.default_rng(n * bb + hw)
+    for (Hq, Hkv), d in itertools.product([(1, 1), (4, 2), (4, 1)], [4, 8]):
+        q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+        ro, rl = band_bruteforce(q, k, v, bb, hw, 0.4)
+        o, l = oracle_mod.attn_band(q, k, v, bb, hw, 0.4)
+        np.testing.assert_allclose(o, ro, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l, rl, rtol=0, atol=1e-12)
+
+
+def test_band_wide_enough_is_full_attention(oracle_mod):
+    """A half-width covering the sequence is full (non-causal) attention:
+    torch SDPA in fp64."""
+    rng = np.random.default_rng(9)
+    n, Hq, Hkv, d = 96, 4, 2, 16
+    q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+    o, _ = oracle_mod.attn_band(q, k, v, 16, 6, 0.25)
+    tq = torch.from_numpy(q).double().permute(1, 0, 2)[None]
+    tk = torch.from_numpy(k).double().repeat_interleave(2, dim=1).permute(1, 0, 2)[None]
+    tv = torch.from_numpy(v).double().repeat_interleave(2, dim=1).permute(1, 0, 2)[None]
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=0.25)
+    np.testing.assert_allclose(o, ref[0].permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def test_band_count_via_zero_keys(oracle_mod):
+    """K = 0: lse = ln of the band's key count; the page's '1/16th' memory
+    figure for 16 neighbour blocks out of 256 (a 32K sequence) is the
+    first-order ratio (2*8+1)/256."""
+    n, bb, hw = 1000, 128, 2
+    q = np.ones((n, 1, 1), dtype=np.float32)
+    k = np.zeros((n, 1, 1), dtype=np.float32)
+    _, l = oracle_mod.attn_band(q, k, k, bb, hw, 1.0)
+    i = np.arange(n)
+    lo = np.maximum(0, (i // bb - hw) * bb)
+    hi = np.minimum(n, (i // bb + hw + 1) * bb)
+    np.testing.assert_allclose(np.exp(l[0]), hi - lo, rtol=1e-12)
+    assert abs((2 * 8 + 1) / 256 - 1 / 16) < 0.005
