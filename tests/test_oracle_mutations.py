@@ -86,8 +86,9 @@ def test_unmodified_oracle_passes_the_battery(swap_lib):
 @pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
 def test_planted_mistake_is_caught(swap_lib, tmp_path, name, old, new):
     text = open(SRC).read()
-    assert text.count(old) == 1, f"pattern for '{name}' not found exactly once"
-    lib = _compile(text.replace(old, new), tmp_path, abs(hash(name)) % 10**8)
+    assert text.count(old) >= 1, f"pattern for '{name}' not found"
+    # The first occurrence is in the window + landmark path.
+    lib = _compile(text.replace(old, new, 1), tmp_path, abs(hash(name)) % 10**8)
     oracle._lib = lib
     failed = battery(oracle)
     assert failed, f"no pin caught: {name}"
