@@ -289,6 +289,39 @@ def run_ring(wl, steps, warmup, dev, B, torch):
             "fused_ms": fused_ms, "launches_per_step": P + 1}
 
 
+def band_flops(wl) -> float:
+    """Useful FLOPs of the block-band mask: 4*d*Hq*sum_i |band keys of i|."""
+    import numpy as np
+    i = np.arange(wl.n, dtype=np.int64)
+    b = i // wl.band_block
+    lo = np.maximum(0, (b - wl.band_half) * wl.band_block)
+    hi = np.minimum(wl.n, (b + wl.band_half + 1) * wl.band_block)
+    return 4.0 * wl.d * wl.Hq * float((hi - lo).sum())
+
+
+def run_band(wl, steps, warmup, dev, B, torch):
+    """Block-band attention, device-resident inputs; returns ms per launch."""
+    from long_context_sparse_landmark_gb300.workloads import generate
+    q, k, v = generate(wl, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((wl.Hq, wl.n), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        B.attn_fwd_band(q, k, v, out, lse, wl.band_block, wl.band_half, wl.scale, stream=stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        B.attn_fwd_band(q, k, v, out, lse, wl.band_block, wl.band_half, wl.scale, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert B.device_status() == 0
+    del q, k, v, out, lse
+    torch.cuda.empty_cache()
+    return e0.elapsed_time(e1) / steps
+
+
 def cpu_baseline(wl, rows_target, torch):
     """The fp64 oracle on the host cores, on a bounded row sample of the
     same workload; extrapolated to the full layer by rows."""
@@ -450,6 +483,14 @@ def main():
             "pool_gbs": round((2 * wl1m.n * wl1m.Hkv * wl1m.d * 2 + 2 * wl1m.G * wl1m.Hkv
                                * wl1m.d * 2) / (r1["pool_ms"] * 1e-3) / 1e9, 1),
             "steps": 3}
+        wlb = WORKLOADS["band_128k"]
+        bms = run_band(wlb, 3, 1, dev, B, torch)
+        fb = band_flops(wlb)
+        also["band_128k"] = {"ms_per_step": round(bms, 3),
+                             "tflops": round(fb / (bms * 1e-3) / 1e12, 2),
+                             "pct_bf16_peak": round(100.0 * fb / (bms * 1e-3) / 1e12
+                                                    / peaks["bf16_tflops"], 2),
+                             "steps": 3}
         wlr = WORKLOADS["ring_128k"]
         rr = run_ring(wlr, 3, 1, dev, B, torch)
         fr = useful_flops(wlr)

@@ -109,6 +109,25 @@ msa_status msa_attn_fwd(const void *q, const void *k, const void *v,
                         msa_stream_t stream);
 
 /*
+ * Block-band attention: the 2-D block-sparse mask of "Million Token Context
+ * Window Optimization: What Actually Works", section "The indexing game:
+ * smarter context management" (each 128-token block attends to 16 other
+ * blocks, left and right).  Row i attends every key j of the blocks within
+ * band_half blocks of its own, |floor(j/band_block) - floor(i/band_block)|
+ * <= band_half, 0 <= j < n (not causal); one softmax, scores scale*<q,k>.
+ * (128-token blocks and 16 neighbours: band_block = 128, band_half = 8.)
+ *   q [n, Hq, d], k, v [n, Hkv, d] in `in_dt`; out [n, Hq, d] in `out_dt`;
+ *   lse [Hq, n] fp32.
+ * Errors: as msa_attn_fwd, plus INVALID_ARG for band_block < 1 or
+ * band_half < 0.
+ */
+msa_status msa_attn_fwd_band(const void *q, const void *k, const void *v,
+                             void *out, float *lse, int64_t n, int Hq,
+                             int Hkv, int d, int64_t band_block,
+                             int64_t band_half, float scale, msa_dtype in_dt,
+                             msa_dtype out_dt, msa_stream_t stream);
+
+/*
  * One Ring Attention round's partial: queries at global positions
  * q_start .. q_start+n_q-1 against the contiguous KV chunk at global
  * positions kv_start .. kv_start+n_kv-1, with the causal window mask

@@ -21,7 +21,8 @@ MAX_MERGE_PARTS = 64
 
 # Every symbol include/msa.h declares.
 EXPORTS = ("msa_version", "msa_last_error_string", "msa_landmark_pool", "msa_attn_fwd",
-           "msa_attn_fwd_partial", "msa_attn_fwd_partial_merge", "msa_lse_merge",
+           "msa_attn_fwd_band", "msa_attn_fwd_partial", "msa_attn_fwd_partial_merge",
+           "msa_lse_merge",
            "msa_attn_uses_tensor_cores", "msa_device_status", "msa_debug_set_wait_limit_ns")
 
 
@@ -44,6 +45,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32, f32,
                                  i32, i32, vp]
     lib.msa_attn_fwd.restype = i32
+    lib.msa_attn_fwd_band.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i64, f32,
+                                      i32, i32, vp]
+    lib.msa_attn_fwd_band.restype = i32
     lib.msa_attn_fwd_partial.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, i32,
                                          i64, f32, i32, vp]
     lib.msa_attn_fwd_partial.restype = i32
@@ -126,6 +130,16 @@ def attn_fwd(q, k, v, k_lm, v_lm, out, lse, window: int, n_landmarks: int, scale
     _check(_lib.msa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(k_lm), _ptr(v_lm), _ptr(out),
                              _ptr(lse), n, Hq, Hkv, d, int(window), int(n_landmarks),
                              float(scale), _dt(q), _dt(out), _stream(stream)))
+
+
+def attn_fwd_band(q, k, v, out, lse, band_block: int, band_half: int, scale: float,
+                  stream=None) -> None:
+    """msa_attn_fwd_band: block-band attention (not causal)."""
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    _check(_lib.msa_attn_fwd_band(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), n, Hq, Hkv, d,
+                                  int(band_block), int(band_half), float(scale), _dt(q), _dt(out),
+                                  _stream(stream)))
 
 
 def attn_fwd_partial(q, k_chunk, v_chunk, out_part, lse_part, q_start: int, kv_start: int,

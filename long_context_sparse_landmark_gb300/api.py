@@ -44,6 +44,19 @@ def msa_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int
     return out, lse
 
 
+def band_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, band_block: int = 128,
+                   band_half: int = 8, scale: float | None = None,
+                   out_dtype: torch.dtype | None = None, stream=None):
+    """Block-band attention (each band_block-token block attends the blocks
+    within band_half of it, both sides).  Returns (out, lse)."""
+    n, Hq, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = torch.empty((n, Hq, d), dtype=out_dtype or q.dtype, device=q.device)
+    lse = torch.empty((Hq, n), dtype=torch.float32, device=q.device)
+    B.attn_fwd_band(q, k, v, out, lse, band_block, band_half, scale, stream=stream)
+    return out, lse
+
+
 def ring_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_chunks: int,
                    window: int | None = None, scale: float | None = None,
                    out_dtype: torch.dtype | None = None, fused: bool = True, stream=None):

@@ -64,16 +64,28 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnArgs a) {
   // Key ranges of the whole tile (global positions).
   const int64_t g0 = a.q_start + qr0;
   const int64_t g_last = a.q_start + min64(qr0 + kBQ, a.n_q) - 1;
-  int64_t j_lo = max64(g0 - a.window + 1, a.kv_start);
-  int64_t j_hi = min64(g_last, kv_end - 1);
+  int64_t j_lo, j_hi;
+  if (a.band) {  // union of the rows' bands (whole sequence: kv_start = 0)
+    int64_t unused;
+    band_keys(g0, a.band_block, a.band_half, a.n_kv, &j_lo, &unused);
+    band_keys(g_last, a.band_block, a.band_half, a.n_kv, &unused, &j_hi);
+  } else {
+    j_lo = max64(g0 - a.window + 1, a.kv_start);
+    j_hi = min64(g_last, kv_end - 1);
+  }
   const int64_t n_win = j_hi >= j_lo ? j_hi - j_lo + 1 : 0;
   const int64_t n_lm = visible_landmarks(g_last, a.window, a.block, a.G);
   const int64_t lm_tiles = (n_lm + kBK - 1) / kBK;
   const int64_t win_tiles = (n_win + kBK - 1) / kBK;
 
   // This row's own sets.
-  const int64_t my_lo = max64(i - a.window + 1, a.kv_start);
-  const int64_t my_hi = min64(i, kv_end - 1);
+  int64_t my_lo, my_hi;
+  if (a.band) {
+    band_keys(i, a.band_block, a.band_half, a.n_kv, &my_lo, &my_hi);
+  } else {
+    my_lo = max64(i - a.window + 1, a.kv_start);
+    my_hi = min64(i, kv_end - 1);
+  }
   const int64_t my_lm = visible_landmarks(i, a.window, a.block, a.G);
 
   constexpr int DQ = D / 4;

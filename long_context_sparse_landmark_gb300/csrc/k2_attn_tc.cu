@@ -100,7 +100,8 @@ struct TcParams {
   float* lse;
   int64_t n_q, q_start, n_kv, kv_start, window, block;
   int Hq, Hkv, G, group, pairs, n_qtiles, units;
-  int out_bf16, partial, merge;
+  int out_bf16, partial, merge, band;
+  int64_t band_block, band_half;
   float scale_log2;
   int* status;
   uint64_t wait_ns;
@@ -161,8 +162,15 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   const int64_t g0 = p.q_start + w.qr0;
   const int64_t g_last = p.q_start + min64(w.qr0 + kBM, p.n_q) - 1;
   const int64_t kv_end = p.kv_start + p.n_kv;
-  const int64_t j_lo = max64(g0 - p.window + 1, p.kv_start);
-  const int64_t j_hi = min64(g_last, kv_end - 1);
+  int64_t j_lo, j_hi;
+  if (p.band) {  // union of the rows' bands (whole sequence: kv_start = 0)
+    int64_t unused;
+    band_keys(g0, p.band_block, p.band_half, p.n_kv, &j_lo, &unused);
+    band_keys(g_last, p.band_block, p.band_half, p.n_kv, &unused, &j_hi);
+  } else {
+    j_lo = max64(g0 - p.window + 1, p.kv_start);
+    j_hi = min64(g_last, kv_end - 1);
+  }
   w.kt_lo = 0;
   int n_win = 0;
   if (j_hi >= j_lo) {
@@ -417,8 +425,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (row_ok && !p.merge) p.lse[static_cast<int64_t>(h) * p.n_q + i_loc] = -INFINITY;
         continue;
       }
-      const int64_t my_lo = max64(i - p.window + 1, p.kv_start);
-      const int64_t my_hi = min64(i, kv_end - 1);
+      int64_t my_lo, my_hi;
+      if (p.band) {
+        band_keys(i, p.band_block, p.band_half, p.n_kv, &my_lo, &my_hi);
+      } else {
+        my_lo = max64(i - p.window + 1, p.kv_start);
+        my_hi = min64(i, kv_end - 1);
+      }
       const int64_t my_lm = visible_landmarks(i, p.window, p.block, p.G);
       float m_used = -INFINITY;
       float l = 0.f;
@@ -677,6 +690,9 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s, const char** why) 
   p.out_bf16 = a.out_bf16;
   p.partial = a.partial;
   p.merge = a.merge;
+  p.band = a.band;
+  p.band_block = a.band_block;
+  p.band_half = a.band_half;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = a.status;
   p.wait_ns = a.wait_limit_ns;

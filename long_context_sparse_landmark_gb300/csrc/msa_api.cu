@@ -166,6 +166,42 @@ msa_status msa_attn_fwd(const void* q, const void* k, const void* v, const void*
   return run_attn(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+msa_status msa_attn_fwd_band(const void* q, const void* k, const void* v, void* out, float* lse,
+                             int64_t n, int Hq, int Hkv, int d, int64_t band_block,
+                             int64_t band_half, float scale, msa_dtype in_dt, msa_dtype out_dt,
+                             msa_stream_t stream) {
+  msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, 1, scale, in_dt);
+  if (st != MSA_OK) return st;
+  if (n < 1 || n > kMaxRows) return fail(MSA_ERR_INVALID_ARG, "n=%lld out of range", (long long)n);
+  if (!valid_dtype(out_dt)) return fail(MSA_ERR_INVALID_ARG, "bad output dtype %d", (int)out_dt);
+  if (band_block < 1 || band_half < 0)
+    return fail(MSA_ERR_INVALID_ARG, "band_block=%lld must be >= 1 and band_half=%lld >= 0",
+                (long long)band_block, (long long)band_half);
+  msa::AttnArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  a.n_q = n;
+  a.q_start = 0;
+  a.n_kv = n;
+  a.kv_start = 0;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.window = 1;
+  a.G = 0;
+  a.block = 1;
+  a.scale = scale;
+  a.in_bf16 = in_dt == MSA_BF16;
+  a.out_bf16 = out_dt == MSA_BF16;
+  a.band = 1;
+  a.band_block = band_block;
+  a.band_half = band_half;
+  return run_attn(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 msa_status msa_attn_fwd_partial(const void* q, const void* k_chunk, const void* v_chunk,
                                  float* out_part, float* lse_part, int64_t n_q, int64_t q_start,
                                  int64_t n_kv, int64_t kv_start, int Hq, int Hkv, int d,

@@ -31,6 +31,15 @@ __device__ __forceinline__ void record_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Keys of row `pos` under the block-band mask: every key of the blocks
+// (size bb) within hw blocks of the row's own, clipped to [0, n_kv).
+__host__ __device__ __forceinline__ void band_keys(int64_t pos, int64_t bb, int64_t hw,
+                                                   int64_t n_kv, int64_t* lo, int64_t* hi) {
+  const int64_t b = pos / bb;
+  *lo = max64(0, (b - hw) * bb);
+  *hi = min64(n_kv - 1, (b + hw + 1) * bb - 1);
+}
+
 // Launch helpers implemented per translation unit; all return cudaError_t of
 // the launch (cudaPeekAtLastError) and never synchronise.
 struct PoolArgs {
@@ -81,6 +90,8 @@ struct AttnArgs {
   int out_bf16;
   int partial;  // rows with no key: lse = -inf, out row untouched
   int merge;    // out/lse hold a running result: merge this partial into it
+  int band;     // block-band mask instead of window + landmarks
+  int64_t band_block, band_half;
   int* status;  // device status word
   uint64_t wait_limit_ns;
 };

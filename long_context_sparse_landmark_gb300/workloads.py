@@ -33,6 +33,8 @@ class Workload:
     outliers: bool = False   # 1% of K rows get one N(0, variance 2) bias each
     ring_chunks: int = 0     # > 0: KV split into this many contiguous chunks
     seed: int = 0
+    band_block: int = 0      # > 0: block-band mask (blocks of this size) instead
+    band_half: int = 0       #      of window + landmarks; half-width in blocks
 
     @property
     def scale(self) -> float:
@@ -70,6 +72,10 @@ WORKLOADS = {
     # the KV sequence split into 8 contiguous chunks of 16384 tokens.
     "ring_128k": Workload("ring_128k", 131072, 32, 8, 128, 131072, 0, "bf16",
                           ring_chunks=8),
+    # Block-band mask of the 70B-style layer at 128K tokens: 128-token
+    # blocks, each attending the 8 blocks on either side (16 neighbours).
+    "band_128k": Workload("band_128k", 131072, 64, 8, 128, 1, 0, "bf16",
+                          band_block=128, band_half=8),
 }
 
 

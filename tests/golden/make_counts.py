@@ -25,12 +25,15 @@ def main():
     for name, wl in WORKLOADS.items():
         q = np.ones((wl.n, 1, 1), dtype=np.float32)
         k = np.zeros((wl.n, 1, 1), dtype=np.float32)
-        _, lse = oracle.attn(q, k, k, wl.window, wl.G, 1.0)
+        if wl.band_block > 0:
+            _, lse = oracle.attn_band(q, k, k, wl.band_block, wl.band_half, 1.0)
+        else:
+            _, lse = oracle.attn(q, k, k, wl.window, wl.G, 1.0)
         counts = np.rint(np.exp(lse[0])).astype(np.int64)
         per_head[name] = int(counts.sum())
         print(name, per_head[name], flush=True)
     out = {
-        "what": "sum over rows of |attended set| per head (window + visible landmarks)",
+        "what": "sum over rows of |attended set| per head (window + visible landmarks, or the block band)",
         "written_by": "tests/golden/make_counts.py (CPU oracle, K = 0 so lse = ln count)",
         "per_head": per_head,
     }

@@ -112,6 +112,24 @@ def test_partial_validation(lib):
     assert call(d=32) == 2
 
 
+def test_band_validation(lib):
+    f = lib.msa_attn_fwd_band
+
+    def call(**kw):
+        a = dict(q=GOOD, k=GOOD, v=GOOD, o=GOOD, l=GOOD, n=256, Hq=4, Hkv=2, d=128, bb=128, hw=2,
+                 idt=1, odt=0)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["o"], a["l"], a["n"], a["Hq"], a["Hkv"], a["d"],
+                 a["bb"], a["hw"], ctypes.c_float(0.1), a["idt"], a["odt"], None)
+
+    assert call(q=None) == 1
+    assert call(bb=0) == 1
+    assert call(hw=-1) == 1
+    assert call(n=0) == 1
+    assert call(odt=3) == 1
+    assert call(d=96) == 2
+
+
 def test_partial_merge_validation(lib):
     f = lib.msa_attn_fwd_partial_merge
 

@@ -185,6 +185,42 @@ def test_partial_merge_small(dt, d, n, chunks, w):
     compare(lse.cpu().numpy(), rl, mx, mean, "merged lse")
 
 
+# ------------------------------------------------------------------ block band
+@pytest.mark.parametrize("dt,d", [("bf16", 128), ("f32", 64), ("bf16", 64)])
+@pytest.mark.parametrize("n,bb,hw", [(1, 1, 0), (127, 128, 1), (128, 128, 0), (300, 128, 1),
+                                     (1000, 128, 8), (1000, 64, 3), (513, 100, 2), (700, 128, 40)])
+def test_band_small(dt, d, n, bb, hw):
+    B = binding()
+    wl = Workload("band_small", n, 8, 2, d, 1, 0, dt, seed=n + 17 * bb + hw)
+    q, k, v = generate(wl, device=DEV)
+    out = torch.empty((n, 8, d), dtype=torch.float32, device=DEV)
+    lse = torch.empty((8, n), dtype=torch.float32, device=DEV)
+    B.attn_fwd_band(q, k, v, out, lse, bb, hw, wl.scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attn_band(to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v), bb, hw,
+                              wl.scale)
+    mx, mean = tol(dt)
+    compare(out.cpu().numpy(), ro, mx, mean, f"band O n={n} bb={bb} hw={hw}")
+    compare(lse.cpu().numpy(), rl, mx, mean, f"band lse n={n} bb={bb} hw={hw}")
+
+
+def test_band_128k_sampled_rows():
+    import long_context_sparse_landmark_gb300.api as api
+    wl = WORKLOADS["band_128k"]
+    q, k, v = generate(wl, device=DEV)
+    out, lse = api.band_attention(q, k, v, wl.band_block, wl.band_half, wl.scale,
+                                  out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    rows = sample_rows(wl).numpy()
+    go, gl = gather_rows(out, lse, rows)
+    idx = torch.as_tensor(rows, device=DEV)
+    ro, rl = oracle.attn_band(to_numpy_bits(q.index_select(0, idx)), to_numpy_bits(k),
+                              to_numpy_bits(v), wl.band_block, wl.band_half, wl.scale,
+                              q_positions=rows)
+    compare(go, ro, 1e-2, 1e-3, "band 128K O (sampled)")
+    compare(gl, rl, 1e-2, 1e-3, "band 128K lse (sampled)")
+
+
 # ------------------------------------------------------------------ fused ring rounds
 @pytest.mark.parametrize("dt,d", [("bf16", 128), ("f32", 64), ("bf16", 64), ("f32", 128)])
 @pytest.mark.parametrize("n,chunks,w,order", [(512, 4, 512, "fwd"), (384, 3, 100, "rev"),

@@ -344,11 +344,22 @@ def test_p6_oracle_count_via_zero_keys(oracle_mod):
     assert int(counts.sum()) == attended_total_closed_form(n, w, G)
 
 
+def band_total_closed_form(n, bb, hw):
+    i = np.arange(n, dtype=np.int64)
+    lo = np.maximum(0, (i // bb - hw) * bb)
+    hi = np.minimum(n, (i // bb + hw + 1) * bb)
+    return int((hi - lo).sum())
+
+
 def test_p6_workload_totals_match_golden():
     with open(os.path.join(GOLDEN, "attended_counts.json")) as f:
         golden = json.load(f)
     for name, wl in WORKLOADS.items():
-        assert attended_total_closed_form(wl.n, wl.window, wl.G) == golden["per_head"][name], name
+        if wl.band_block > 0:
+            total = band_total_closed_form(wl.n, wl.band_block, wl.band_half)
+        else:
+            total = attended_total_closed_form(wl.n, wl.window, wl.G)
+        assert total == golden["per_head"][name], name
 
 
 def test_p6_page_dot_product_arithmetic():
