@@ -57,6 +57,13 @@ def _configure(lib):
     lib.oracle_attn_band_rows.argtypes = [vp, vp, i64, vp, vp, i64, i32, i32,
                                           i32, i32, i64, i64, dbl, vp, vp]
     lib.oracle_attn_band_rows.restype = i32
+    lib.oracle_block_scores.argtypes = [vp, i32, i64, i32, i32, i32, vp, i32, i64,
+                                        i64, i64, vp]
+    lib.oracle_block_scores.restype = i32
+    lib.oracle_attn_select_rows.argtypes = [vp, vp, i64, vp, vp, i64, i32, i32, i32,
+                                            i32, i64, i64, i64, vp, vp, i32, dbl, vp,
+                                            vp]
+    lib.oracle_attn_select_rows.restype = i32
     lib.oracle_lse_merge.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp]
     lib.oracle_lse_merge.restype = i32
     lib.oracle_set_threads.argtypes = [i32]
@@ -196,6 +203,75 @@ def attn_band(q: np.ndarray, k: np.ndarray, v: np.ndarray, band_block: int,
                                        float(scale), _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError("attn_band: inconsistent arguments")
+    return out, lse
+
+
+def block_scores(q: np.ndarray, k: np.ndarray, n_landmarks: int, window: int,
+                 q_block: int = 128) -> np.ndarray:
+    """Scores [n_qb, Hkv, G] (fp64) of every key block for every query
+    block and KV group; -inf where the block is not wholly before the
+    window of the query block's first row."""
+    q = np.ascontiguousarray(q)
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    G = int(n_landmarks)
+    k_lm = landmark_pool(k, G)
+    n_qb = (n + q_block - 1) // q_block
+    scores = np.empty((n_qb, Hkv, G), dtype=np.float64)
+    rc = _load().oracle_block_scores(_ptr(q), _dtype_code(q), n, Hq, Hkv, d, _ptr(k_lm), G,
+                                     n // G, int(window), int(q_block), _ptr(scores))
+    if rc != 0:
+        raise ValueError("block_scores: inconsistent arguments")
+    return scores
+
+
+def select_top_k(scores: np.ndarray, top_k: int):
+    """The top-k blocks of every (query block, KV group): highest scores
+    first, ties to the lower block index, -inf never chosen.  Returns
+    (sel [n_qb, Hkv, top_k] int32 in ascending block order, cnt [n_qb, Hkv])."""
+    n_qb, Hkv, G = scores.shape
+    sel = np.zeros((n_qb, Hkv, max(top_k, 1)), dtype=np.int32)
+    cnt = np.zeros((n_qb, Hkv), dtype=np.int32)
+    for t in range(n_qb):
+        for c in range(Hkv):
+            cand = [l for l in range(G) if np.isfinite(scores[t, c, l])]
+            cand.sort(key=lambda l: (-scores[t, c, l], l))
+            chosen = sorted(cand[:top_k])
+            cnt[t, c] = len(chosen)
+            sel[t, c, :len(chosen)] = chosen
+    return sel[:, :, :top_k] if top_k > 0 else sel[:, :, :0], cnt
+
+
+def attn_select(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int, n_landmarks: int,
+                sel: np.ndarray, cnt: np.ndarray, scale: float, q_block: int = 128,
+                rows=None, q_positions=None):
+    """Attention over each row's causal window plus every token of its query
+    block's selected key blocks (sel/cnt as select_top_k returns).  Returns
+    (O [n_rows, Hq, d], lse [Hq, n_rows]) in fp64."""
+    q = np.ascontiguousarray(q)
+    k = np.ascontiguousarray(k)
+    v = np.ascontiguousarray(v)
+    dt = _dtype_code(q)
+    n_q, Hq, d = q.shape
+    n, Hkv, _ = k.shape
+    if q_positions is not None:
+        pos = np.ascontiguousarray(np.asarray(q_positions, dtype=np.int64))
+        qg = q
+    else:
+        rows = np.arange(n_q, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+        qg = np.ascontiguousarray(q[rows])
+        pos = np.ascontiguousarray(rows)
+    top_k = sel.shape[2]
+    sel = np.ascontiguousarray(sel, dtype=np.int32)
+    cnt = np.ascontiguousarray(cnt, dtype=np.int32)
+    out = np.empty((len(pos), Hq, d), dtype=np.float64)
+    lse = np.empty((Hq, len(pos)), dtype=np.float64)
+    rc = _load().oracle_attn_select_rows(_ptr(qg), _ptr(pos), len(pos), _ptr(k), _ptr(v), n, dt,
+                                         Hq, Hkv, d, int(window), n // int(n_landmarks),
+                                         int(q_block), _ptr(sel), _ptr(cnt), int(top_k),
+                                         float(scale), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("attn_select: inconsistent arguments")
     return out, lse
 
 

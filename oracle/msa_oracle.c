@@ -326,3 +326,131 @@ int oracle_attn_band_rows(const void *q, const int64_t *pos, int64_t n_rows,
     }
     return 0;
 }
+
+/*
+ * Landmark-scored block selection, standing in for the hierarchical context
+ * index of "Million Token Context Window Optimization: What Actually Works",
+ * section "The indexing game: smarter context management" (chunks of the
+ * input are scored against the query and only the top-k chunks plus a
+ * history window are attended; the pages score chunks with a BERT embedding,
+ * which needs trained weights, so the chunk's landmark -- its mean key --
+ * scores it here).  Reading taken: query blocks of q_block rows; for query
+ * block t and KV group c the score of key block l (bs tokens) is
+ *   sum over rows i of block t and heads h of group c of <q[i,h], Kbar[l,c]>,
+ * defined only for blocks wholly before the window of the block's first row,
+ * (l+1)*bs <= t*q_block - w + 1; other blocks score -inf.
+ *   q [n][Hq][d]; k_lm [G][Hkv][d] fp64; scores [n_qb][Hkv][G] fp64,
+ *   n_qb = ceil(n / q_block).
+ */
+int oracle_block_scores(const void *q, int dtype, int64_t n, int Hq, int Hkv,
+                        int d, const double *k_lm, int G, int64_t bs,
+                        int64_t window, int64_t q_block, double *scores) {
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || G < 1 || bs < 1 ||
+        q_block < 1 || window < 1)
+        return -1;
+    const int group = Hq / Hkv;
+    const int64_t n_qb = (n + q_block - 1) / q_block;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t t = 0; t < n_qb; ++t) {
+        for (int c = 0; c < Hkv; ++c) {
+            double *qsum = (double *)calloc((size_t)d, sizeof(double));
+            const int64_t r_end = (t + 1) * q_block < n ? (t + 1) * q_block : n;
+            for (int64_t i = t * q_block; i < r_end; ++i)
+                for (int hh = 0; hh < group; ++hh) {
+                    const int64_t off = (i * Hq + c * group + hh) * (int64_t)d;
+                    for (int e = 0; e < d; ++e) qsum[e] += oracle_load(q, off + e, dtype);
+                }
+            double *row = scores + (t * Hkv + c) * (int64_t)G;
+            for (int l = 0; l < G; ++l) {
+                if ((l + 1) * bs <= t * q_block - window + 1) {
+                    const double *kl = k_lm + ((int64_t)l * Hkv + c) * d;
+                    double sc = 0.0;
+                    for (int e = 0; e < d; ++e) sc += qsum[e] * kl[e];
+                    row[l] = sc;
+                } else {
+                    row[l] = -INFINITY;
+                }
+            }
+            free(qsum);
+        }
+    }
+    return 0;
+}
+
+/*
+ * Attention over the causal window plus the tokens of the selected blocks:
+ * row i (query block t = i / q_block, KV group c) attends keys
+ * i-w < j <= i and every token of the blocks sel[t][c][0..cnt[t][c]).
+ * One softmax, scores scale*<q,k>.
+ *   q [n_rows][Hq][d] at positions pos[]; k, v [n][Hkv][d];
+ *   sel [n_qb][Hkv][topk] int32, cnt [n_qb][Hkv] int32;
+ *   out [n_rows][Hq][d], lse [Hq][n_rows] fp64.
+ */
+int oracle_attn_select_rows(const void *q, const int64_t *pos, int64_t n_rows,
+                            const void *k, const void *v, int64_t n, int dtype,
+                            int Hq, int Hkv, int d, int64_t window,
+                            int64_t bs, int64_t q_block, const int32_t *sel,
+                            const int32_t *cnt, int topk, double scale,
+                            double *out, double *lse) {
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || window < 1 ||
+        bs < 1 || q_block < 1 || topk < 0)
+        return -1;
+    const int group = Hq / Hkv;
+#pragma omp parallel
+    {
+        int64_t *keys = NULL;
+        double *sc = NULL;
+        int64_t cap = 0;
+#pragma omp for collapse(2) schedule(dynamic, 4)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            for (int h = 0; h < Hq; ++h) {
+                const int64_t i = pos[r];
+                const int c = h / group;
+                const int64_t t = i / q_block;
+                const int32_t ns = cnt[t * Hkv + c];
+                const int32_t *bl = sel + (t * Hkv + c) * (int64_t)topk;
+                int64_t j_lo = i - window + 1;
+                if (j_lo < 0) j_lo = 0;
+                const int64_t need = (i - j_lo + 1) + (int64_t)ns * bs;
+                if (need > cap) {
+                    free(keys);
+                    free(sc);
+                    cap = need;
+                    keys = (int64_t *)malloc(sizeof(int64_t) * (size_t)cap);
+                    sc = (double *)malloc(sizeof(double) * (size_t)cap);
+                }
+                int64_t nk = 0;
+                for (int32_t b = 0; b < ns; ++b)
+                    for (int64_t j = (int64_t)bl[b] * bs; j < ((int64_t)bl[b] + 1) * bs; ++j)
+                        keys[nk++] = j;
+                for (int64_t j = j_lo; j <= i; ++j) keys[nk++] = j;
+                const int64_t qoff = (r * Hq + h) * (int64_t)d;
+                double m = -INFINITY;
+                for (int64_t x = 0; x < nk; ++x) {
+                    const int64_t koff = (keys[x] * Hkv + c) * (int64_t)d;
+                    double dot = 0.0;
+                    for (int e = 0; e < d; ++e)
+                        dot += oracle_load(q, qoff + e, dtype) *
+                               oracle_load(k, koff + e, dtype);
+                    sc[x] = scale * dot;
+                    if (sc[x] > m) m = sc[x];
+                }
+                double *o = out + (r * Hq + h) * (int64_t)d;
+                double denom = 0.0;
+                for (int e = 0; e < d; ++e) o[e] = 0.0;
+                for (int64_t x = 0; x < nk; ++x) {
+                    const double p = exp(sc[x] - m);
+                    denom += p;
+                    const int64_t voff = (keys[x] * Hkv + c) * (int64_t)d;
+                    for (int e = 0; e < d; ++e)
+                        o[e] += p * oracle_load(v, voff + e, dtype);
+                }
+                for (int e = 0; e < d; ++e) o[e] /= denom;
+                lse[(int64_t)h * n_rows + r] = m + log(denom);
+            }
+        }
+        free(keys);
+        free(sc);
+    }
+    return 0;
+}

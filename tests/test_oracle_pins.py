@@ -443,3 +443,109 @@ def test_band_count_via_zero_keys(oracle_mod):
     hi = np.minimum(n, (i // bb + hw + 1) * bb)
     np.testing.assert_allclose(np.exp(l[0]), hi - lo, rtol=1e-12)
     assert abs((2 * 8 + 1) / 256 - 1 / 16) < 0.005
+
+
+# ------------------------------------------------------------------- top-k blocks
+def topk_bruteforce(q, k, v, window, G, top_k, scale, qb):
+    """numpy: block means, query-block sums, candidate rule, top-k with
+    ties to the lower index, dense mask (window or selected block) built
+    element by element, masked softmax."""
+    q = q.astype(np.float64)
+    k = k.astype(np.float64)
+    v = v.astype(np.float64)
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv
+    bs = n // G
+    klm = k.reshape(G, bs, Hkv, d).mean(axis=1)
+    n_qb = (n + qb - 1) // qb
+    chosen = {}
+    scores = np.full((n_qb, Hkv, G), -np.inf)
+    for t in range(n_qb):
+        rows = slice(t * qb, min(n, (t + 1) * qb))
+        for c in range(Hkv):
+            qs = q[rows, c * g:(c + 1) * g].sum(axis=(0, 1))
+            for l in range(G):
+                if (l + 1) * bs <= t * qb - window + 1:
+                    scores[t, c, l] = qs @ klm[l, c]
+            cand = [l for l in range(G) if np.isfinite(scores[t, c, l])]
+            order = np.lexsort((np.array(cand), -scores[t, c, cand])) if cand else []
+            chosen[(t, c)] = sorted(cand[o] for o in list(order)[:top_k])
+    out = np.zeros((n, Hq, d))
+    lse = np.zeros((Hq, n))
+    for h in range(Hq):
+        c = h // g
+        mask = np.zeros((n, n), dtype=bool)
+        for i in range(n):
+            for j in range(n):
+                mask[i, j] = (i - window < j <= i) or (j // bs in chosen[(i // qb, c)])
+        s = np.where(mask, scale * q[:, h] @ k[:, c].T, -np.inf)
+        mx = s.max(axis=1, keepdims=True)
+        e = np.where(mask, np.exp(s - mx), 0.0)
+        den = e.sum(axis=1, keepdims=True)
+        out[:, h] = (e / den) @ v[:, c]
+        lse[h] = (mx + np.log(den))[:, 0]
+    return scores, chosen, out, lse
+
+
+@pytest.mark.parametrize("n,G,w,top_k,qb", [(64, 16, 3, 2, 8), (64, 8, 9, 3, 16), (96, 12, 20, 1, 8),
+                                            (48, 48, 2, 5, 4), (40, 10, 1, 100, 8)])
+def test_topk_bruteforce(oracle_mod, n, G, w, top_k, qb):
+    rng = np.random.default_rng(n + G + w + top_k)
+    for (Hq, Hkv), d in itertools.product([(2, 1), (4, 2)], [4, 8]):
+        q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+        rs, rch, ro, rl = topk_bruteforce(q, k, v, w, G, top_k, 0.4, qb)
+        sc = oracle_mod.block_scores(q, k, G, w, q_block=qb)
+        np.testing.assert_allclose(sc, rs, rtol=1e-12, atol=1e-12)
+        sel, cnt = oracle_mod.select_top_k(sc, top_k)
+        for (t, c), blocks in rch.items():
+            assert list(sel[t, c, :cnt[t, c]]) == blocks
+        o, l = oracle_mod.attn_select(q, k, v, w, G, sel, cnt, 0.4, q_block=qb)
+        np.testing.assert_allclose(o, ro, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l, rl, rtol=0, atol=1e-12)
+
+
+def test_topk_zero_is_window_attention(oracle_mod):
+    rng = np.random.default_rng(21)
+    q, k, v = rand_qkv(rng, 64, 4, 2, 8)
+    sc = oracle_mod.block_scores(q, k, 8, 5, q_block=16)
+    sel, cnt = oracle_mod.select_top_k(sc, 0)
+    o, l = oracle_mod.attn_select(q, k, v, 5, 8, sel, cnt, 0.3, q_block=16)
+    ro, rl = oracle_mod.attn(q, k, v, 5, 0, 0.3)
+    np.testing.assert_allclose(o, ro, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, rl, rtol=0, atol=1e-12)
+
+
+def test_topk_counts_and_ties(oracle_mod):
+    """K = 0: every candidate scores 0 (all tied), the lowest indices win,
+    and exp(lse) = window size + selected blocks x block size."""
+    n, G, w, top_k, qb = 128, 16, 10, 3, 16
+    bs = n // G
+    q = np.ones((n, 2, 4), dtype=np.float32)
+    k = np.zeros((n, 1, 4), dtype=np.float32)
+    sc = oracle_mod.block_scores(q, k, G, w, q_block=qb)
+    sel, cnt = oracle_mod.select_top_k(sc, top_k)
+    for t in range(n // qb):
+        n_cand = sum(1 for l in range(G) if (l + 1) * bs <= t * qb - w + 1)
+        assert cnt[t, 0] == min(top_k, n_cand)
+        assert list(sel[t, 0, :cnt[t, 0]]) == list(range(cnt[t, 0]))
+    _, l = oracle_mod.attn_select(q, k, k, w, G, sel, cnt, 1.0, q_block=qb)
+    i = np.arange(n)
+    expect = np.minimum(w, i + 1) + cnt[i // qb, 0] * bs
+    np.testing.assert_allclose(np.exp(l[0]), expect, rtol=1e-12)
+
+
+def test_topk_planted_block_is_chosen(oracle_mod):
+    """Keys of block 2 aligned with every query: block 2 scores highest for
+    every query block that may see it."""
+    rng = np.random.default_rng(5)
+    n, G, w, qb, d = 256, 16, 16, 32, 16
+    bs = n // G
+    q = (rng.standard_normal((n, 2, d)) * 0.1 + 1.0).astype(np.float32)
+    k = (rng.standard_normal((n, 1, d)) * 0.1).astype(np.float32)
+    k[2 * bs:3 * bs] += 3.0
+    sc = oracle_mod.block_scores(q, k, G, w, q_block=qb)
+    sel, cnt = oracle_mod.select_top_k(sc, 1)
+    for t in range(n // qb):
+        if 3 * bs <= t * qb - w + 1:
+            assert cnt[t, 0] == 1 and sel[t, 0, 0] == 2
