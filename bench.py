@@ -322,6 +322,57 @@ def run_band(wl, steps, warmup, dev, B, torch):
     return e0.elapsed_time(e1) / steps
 
 
+def topk_flops(wl) -> float:
+    """Useful FLOPs of window + top-k blocks: every row attends its window
+    and min(top_k, candidates of its 128-row query block) whole blocks."""
+    import numpy as np
+    i = np.arange(wl.n, dtype=np.int64)
+    r0 = (i // 128) * 128
+    cand = np.clip((r0 - wl.window + 1) // wl.block, 0, wl.G)
+    per_row = np.minimum(wl.window, i + 1) + np.minimum(wl.top_k, cand) * wl.block
+    return 4.0 * wl.d * wl.Hq * float(per_row.sum())
+
+
+def run_topk(wl, steps, warmup, dev, B, torch):
+    """Pool K + block select + attention in one call (msa_attn_fwd_topk),
+    device-resident inputs and a preallocated workspace; also times the
+    selection kernel alone.  Returns ms per call of each."""
+    from long_context_sparse_landmark_gb300.workloads import generate
+    q, k, v = generate(wl, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((wl.Hq, wl.n), dtype=torch.float32, device=dev)
+    ws = torch.empty((B.topk_workspace_size(wl.n, wl.Hkv, wl.d, wl.G, wl.top_k, q.dtype),),
+                     dtype=torch.uint8, device=dev)
+    k_lm = torch.empty((wl.G, wl.Hkv, wl.d), dtype=k.dtype, device=dev)
+    n_qb = (wl.n + 127) // 128
+    sel = torch.empty((n_qb, wl.Hkv, wl.top_k), dtype=torch.int32, device=dev)
+    cnt = torch.empty((n_qb, wl.Hkv), dtype=torch.int32, device=dev)
+    B.landmark_pool(k, v, k_lm, torch.empty_like(k_lm))
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, n_iter):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_iter):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n_iter
+
+    fused_ms = timed(lambda: B.attn_fwd_topk(q, k, v, out, lse, wl.window, wl.G, wl.top_k,
+                                             wl.scale, ws, stream=stream), steps)
+    select_ms = timed(lambda: B.block_select(q, k_lm, sel, cnt, wl.window, wl.top_k,
+                                             stream=stream), steps)
+    assert B.device_status() == 0
+    del q, k, v, out, lse, ws, k_lm, sel, cnt
+    torch.cuda.empty_cache()
+    return {"fused_ms": fused_ms, "select_ms": select_ms}
+
+
 def cpu_baseline(wl, rows_target, torch):
     """The fp64 oracle on the host cores, on a bounded row sample of the
     same workload; extrapolated to the full layer by rows."""
@@ -491,6 +542,19 @@ def main():
                              "pct_bf16_peak": round(100.0 * fb / (bms * 1e-3) / 1e12
                                                     / peaks["bf16_tflops"], 2),
                              "steps": 3}
+        wlt = WORKLOADS["topk_128k"]
+        rt = run_topk(wlt, 3, 1, dev, B, torch)
+        ft = topk_flops(wlt)
+        # selection reads Q once (the block-mean keys are 1/256 of K)
+        sel_bytes = wlt.n * wlt.Hq * wlt.d * 2
+        also["topk_128k"] = {"ms_per_step": round(rt["fused_ms"], 3),
+                             "tflops": round(ft / (rt["fused_ms"] * 1e-3) / 1e12, 2),
+                             "pct_bf16_peak": round(100.0 * ft / (rt["fused_ms"] * 1e-3)
+                                                    / 1e12 / peaks["bf16_tflops"], 2),
+                             "select_ms": round(rt["select_ms"], 4),
+                             "select_gbs": round(sel_bytes / (rt["select_ms"] * 1e-3) / 1e9,
+                                                 1),
+                             "launches_per_step": 3, "steps": 3}
         wlr = WORKLOADS["ring_128k"]
         rr = run_ring(wlr, 3, 1, dev, B, torch)
         fr = useful_flops(wlr)

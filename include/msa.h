@@ -43,6 +43,7 @@
 #ifndef MSA_H_
 #define MSA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -126,6 +127,75 @@ msa_status msa_attn_fwd_band(const void *q, const void *k, const void *v,
                              int Hkv, int d, int64_t band_block,
                              int64_t band_half, float scale, msa_dtype in_dt,
                              msa_dtype out_dt, msa_stream_t stream);
+
+/* Largest number of key blocks (G) the top-k selection accepts. */
+#define MSA_MAX_SELECT_BLOCKS 1024
+
+/*
+ * Landmark-scored top-k block selection, standing in for the hierarchical
+ * context index of "Million Token Context Window Optimization: What Actually
+ * Works", section "The indexing game: smarter context management" (score
+ * the input's chunks against the query; attend only the top-k chunks plus a
+ * history window).  A chunk is one of G contiguous key blocks of B = n/G
+ * tokens and its landmark (mean key, from msa_landmark_pool) scores it.
+ * For every query block t of 128 rows and KV group c:
+ *   score(l) = sum over rows i of block t, heads h of group c of
+ *              <q[i,h], k_lm[l,c]>,
+ * defined for the blocks wholly before the window of the block's first row,
+ * (l+1)B <= 128t - w + 1.  The min(top_k, #candidates) best blocks are
+ * chosen (ties to the lower index; scores summed in fp32).
+ *   q    [n, Hq, d] in `in_dt`;  k_lm [G, Hkv, d] in `in_dt`
+ *   sel  [ceil(n/128), Hkv, top_k] int32, written: chosen blocks ascending
+ *   cnt  [ceil(n/128), Hkv] int32, written: how many were chosen
+ * Errors: INVALID_ARG for null/misaligned pointers, Hq % Hkv != 0, w < 1,
+ * G < 1, G > n, n % G != 0, top_k < 1 or top_k > G; UNSUPPORTED if d is not
+ * 64 or 128 or G > MSA_MAX_SELECT_BLOCKS.
+ */
+msa_status msa_block_select(const void *q, const void *k_lm, int32_t *sel,
+                            int32_t *cnt, int64_t n, int Hq, int Hkv, int d,
+                            int64_t window, int n_landmarks, int top_k,
+                            msa_dtype in_dt, msa_stream_t stream);
+
+/*
+ * Attention over each row's causal window (i-w < j <= i) plus every token
+ * of the key blocks msa_block_select chose for its query block; one
+ * softmax, scores scale*<q,k>.
+ *   q [n, Hq, d], k, v [n, Hkv, d] in `in_dt`; sel, cnt as written by
+ *   msa_block_select for the same n, Hkv, G, top_k; out [n, Hq, d] in
+ *   `out_dt`; lse [Hq, n] fp32.
+ * Errors: as msa_attn_fwd and msa_block_select.  The kernels check the
+ * selection they read: a count above min(top_k, candidates) or a block that
+ * is not a candidate of its query block is clamped (to that bound / to block
+ * 0) and MSA_ERR_INVALID_ARG recorded in the device status word
+ * (msa_device_status), so a bad selection never reads outside K and V.
+ */
+msa_status msa_attn_fwd_select(const void *q, const void *k, const void *v,
+                               const int32_t *sel, const int32_t *cnt,
+                               void *out, float *lse, int64_t n, int Hq,
+                               int Hkv, int d, int64_t window, int n_landmarks,
+                               int top_k, float scale, msa_dtype in_dt,
+                               msa_dtype out_dt, msa_stream_t stream);
+
+/* Bytes of workspace msa_attn_fwd_topk needs (0 for invalid sizes). */
+size_t msa_attn_fwd_topk_workspace_size(int64_t n, int Hkv, int d,
+                                        int n_landmarks, int top_k,
+                                        msa_dtype in_dt);
+
+/*
+ * The whole top-k path in one call: pool the block-mean keys, select each
+ * query block's top-k key blocks (msa_block_select), attend window +
+ * selected blocks (msa_attn_fwd_select).  The intermediate keys and
+ * selection live in the caller's `workspace` (device memory, 256-byte
+ * aligned, at least msa_attn_fwd_topk_workspace_size bytes).
+ * Errors: as the three steps, plus INVALID_ARG for a null, misaligned or
+ * too small workspace.
+ */
+msa_status msa_attn_fwd_topk(const void *q, const void *k, const void *v,
+                             void *out, float *lse, int64_t n, int Hq, int Hkv,
+                             int d, int64_t window, int n_landmarks, int top_k,
+                             float scale, msa_dtype in_dt, msa_dtype out_dt,
+                             void *workspace, size_t workspace_bytes,
+                             msa_stream_t stream);
 
 /*
  * One Ring Attention round's partial: queries at global positions

@@ -21,8 +21,9 @@ MAX_MERGE_PARTS = 64
 
 # Every symbol include/msa.h declares.
 EXPORTS = ("msa_version", "msa_last_error_string", "msa_landmark_pool", "msa_attn_fwd",
-           "msa_attn_fwd_band", "msa_attn_fwd_partial", "msa_attn_fwd_partial_merge",
-           "msa_lse_merge",
+           "msa_attn_fwd_band", "msa_block_select", "msa_attn_fwd_select",
+           "msa_attn_fwd_topk_workspace_size", "msa_attn_fwd_topk", "msa_attn_fwd_partial",
+           "msa_attn_fwd_partial_merge", "msa_lse_merge",
            "msa_attn_uses_tensor_cores", "msa_device_status", "msa_debug_set_wait_limit_ns")
 
 
@@ -48,6 +49,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_attn_fwd_band.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i64, f32,
                                       i32, i32, vp]
     lib.msa_attn_fwd_band.restype = i32
+    lib.msa_block_select.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i64, i32, i32, i32, vp]
+    lib.msa_block_select.restype = i32
+    lib.msa_attn_fwd_select.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32,
+                                        i32, f32, i32, i32, vp]
+    lib.msa_attn_fwd_select.restype = i32
+    lib.msa_attn_fwd_topk_workspace_size.argtypes = [i64, i32, i32, i32, i32, i32]
+    lib.msa_attn_fwd_topk_workspace_size.restype = ctypes.c_size_t
+    lib.msa_attn_fwd_topk.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32, i32, f32,
+                                      i32, i32, vp, ctypes.c_size_t, vp]
+    lib.msa_attn_fwd_topk.restype = i32
     lib.msa_attn_fwd_partial.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, i32,
                                          i64, f32, i32, vp]
     lib.msa_attn_fwd_partial.restype = i32
@@ -140,6 +151,42 @@ def attn_fwd_band(q, k, v, out, lse, band_block: int, band_half: int, scale: flo
     _check(_lib.msa_attn_fwd_band(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), n, Hq, Hkv, d,
                                   int(band_block), int(band_half), float(scale), _dt(q), _dt(out),
                                   _stream(stream)))
+
+
+def block_select(q, k_lm, sel, cnt, window: int, top_k: int, stream=None) -> None:
+    """msa_block_select: top-k key blocks per 128-row query block and KV group."""
+    n, Hq, d = q.shape
+    G, Hkv, _ = k_lm.shape
+    _check(_lib.msa_block_select(_ptr(q), _ptr(k_lm), _ptr(sel), _ptr(cnt), n, Hq, Hkv, d,
+                                 int(window), G, int(top_k), _dt(q), _stream(stream)))
+
+
+def attn_fwd_select(q, k, v, sel, cnt, out, lse, window: int, n_landmarks: int, top_k: int,
+                    scale: float, stream=None) -> None:
+    """msa_attn_fwd_select: window + the selected key blocks."""
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    _check(_lib.msa_attn_fwd_select(_ptr(q), _ptr(k), _ptr(v), _ptr(sel), _ptr(cnt), _ptr(out),
+                                    _ptr(lse), n, Hq, Hkv, d, int(window), int(n_landmarks),
+                                    int(top_k), float(scale), _dt(q), _dt(out), _stream(stream)))
+
+
+def topk_workspace_size(n: int, Hkv: int, d: int, n_landmarks: int, top_k: int,
+                        dtype: torch.dtype) -> int:
+    return int(_lib.msa_attn_fwd_topk_workspace_size(n, Hkv, d, n_landmarks, top_k,
+                                                     MSA_BF16 if dtype == torch.bfloat16
+                                                     else MSA_F32))
+
+
+def attn_fwd_topk(q, k, v, out, lse, window: int, n_landmarks: int, top_k: int, scale: float,
+                  workspace: torch.Tensor, stream=None) -> None:
+    """msa_attn_fwd_topk: pool, select and attend in one call (workspace given)."""
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    _check(_lib.msa_attn_fwd_topk(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), n, Hq, Hkv, d,
+                                  int(window), int(n_landmarks), int(top_k), float(scale), _dt(q),
+                                  _dt(out), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def attn_fwd_partial(q, k_chunk, v_chunk, out_part, lse_part, q_start: int, kv_start: int,

@@ -57,6 +57,21 @@ def band_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, band_block
     return out, lse
 
 
+def topk_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int,
+                   n_landmarks: int, top_k: int, scale: float | None = None,
+                   out_dtype: torch.dtype | None = None, stream=None):
+    """Window + top-k selected key blocks (msa_attn_fwd_topk; the workspace
+    is a torch allocation).  Returns (out, lse)."""
+    n, Hq, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = torch.empty((n, Hq, d), dtype=out_dtype or q.dtype, device=q.device)
+    lse = torch.empty((Hq, n), dtype=torch.float32, device=q.device)
+    nbytes = B.topk_workspace_size(n, k.shape[1], d, n_landmarks, top_k, q.dtype)
+    ws = torch.empty((nbytes,), dtype=torch.uint8, device=q.device)
+    B.attn_fwd_topk(q, k, v, out, lse, window, n_landmarks, top_k, scale, ws, stream=stream)
+    return out, lse
+
+
 def ring_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_chunks: int,
                    window: int | None = None, scale: float | None = None,
                    out_dtype: torch.dtype | None = None, fused: bool = True, stream=None):

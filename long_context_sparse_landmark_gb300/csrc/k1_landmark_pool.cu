@@ -113,7 +113,7 @@ cudaError_t launch_landmark_pool(const PoolArgs& a, cudaStream_t s) {
   const int vn = a.bf16 ? 8 : 4;
   const int strips = (a.C / vn + 31) / 32;
   const int64_t B = a.n / a.G;
-  dim3 grid(static_cast<unsigned>(static_cast<int64_t>(a.G) * strips), 2);
+  dim3 grid(static_cast<unsigned>(static_cast<int64_t>(a.G) * strips), a.v ? 2 : 1);
   dim3 block(kPoolWarps * 32);
   if (a.bf16) {
     landmark_pool_kernel<true><<<grid, block, 0, s>>>(

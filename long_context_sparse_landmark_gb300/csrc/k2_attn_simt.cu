@@ -74,7 +74,15 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnArgs a) {
     j_hi = min64(g_last, kv_end - 1);
   }
   const int64_t n_win = j_hi >= j_lo ? j_hi - j_lo + 1 : 0;
-  const int64_t n_lm = visible_landmarks(g_last, a.window, a.block, a.G);
+  // Landmark keys, or (select mode) the tokens of the query block's
+  // selected key blocks; a 64-row tile lies inside one 128-row query block.
+  const int64_t qb = qr0 / kSelQBlock;
+  const int64_t n_cand = a.sel ? visible_landmarks(qb * kSelQBlock, a.window, a.block, a.G) : 0;
+  const int32_t* sel_list =
+      a.sel ? a.sel + (qb * a.Hkv + c) * static_cast<int64_t>(a.top_k) : nullptr;
+  const int64_t n_lm =
+      a.sel ? sel_count_checked(a.sel_cnt[qb * a.Hkv + c], a.top_k, n_cand, a.status) * a.block
+            : visible_landmarks(g_last, a.window, a.block, a.G);
   const int64_t lm_tiles = (n_lm + kBK - 1) / kBK;
   const int64_t win_tiles = (n_win + kBK - 1) / kBK;
 
@@ -86,7 +94,7 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnArgs a) {
     my_lo = max64(i - a.window + 1, a.kv_start);
     my_hi = min64(i, kv_end - 1);
   }
-  const int64_t my_lm = visible_landmarks(i, a.window, a.block, a.G);
+  const int64_t my_lm = a.sel ? n_lm : visible_landmarks(i, a.window, a.block, a.G);
 
   constexpr int DQ = D / 4;
   float o[DQ];
@@ -104,7 +112,14 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnArgs a) {
       const int64_t key = base + kk;
       float kv = 0.f, vv = 0.f;
       if (key < limit) {
-        if (is_lm) {
+        if (is_lm && sel_list) {
+          const int64_t tok =
+              sel_block_checked(sel_list[key / a.block], n_cand, a.status) * a.block +
+              key % a.block;
+          const int64_t off = (tok * a.Hkv + c) * static_cast<int64_t>(D) + e;
+          kv = ld_in<kBf16In>(a.k, off);
+          vv = ld_in<kBf16In>(a.v, off);
+        } else if (is_lm) {
           const int64_t off = (key * a.Hkv + c) * static_cast<int64_t>(D) + e;
           kv = ld_in<kBf16In>(a.k_lm, off);
           vv = ld_in<kBf16In>(a.v_lm, off);

@@ -102,6 +102,9 @@ struct TcParams {
   int Hq, Hkv, G, group, pairs, n_qtiles, units;
   int out_bf16, partial, merge, band;
   int64_t band_block, band_half;
+  const int32_t* sel;
+  const int32_t* sel_cnt;
+  int top_k, select;
   float scale_log2;
   int* status;
   uint64_t wait_ns;
@@ -177,8 +180,15 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
     w.kt_lo = static_cast<int>((j_lo - p.kv_start) / kBN);
     n_win = static_cast<int>((j_hi - p.kv_start) / kBN) - w.kt_lo + 1;
   }
-  const int64_t n_lm = visible_landmarks(g_last, p.window, p.block, p.G);
-  w.n_lm_tiles = static_cast<int>((n_lm + kBN - 1) / kBN);
+  if (p.select) {  // the unit's selected key blocks, each block/128 full tiles
+    const int64_t cnt =
+        sel_count_checked(p.sel_cnt[static_cast<int64_t>(qt) * p.Hkv + w.kvh], p.top_k,
+                          visible_landmarks(g0, p.window, p.block, p.G), p.status);
+    w.n_lm_tiles = static_cast<int>(cnt * (p.block / kBN));
+  } else {
+    const int64_t n_lm = visible_landmarks(g_last, p.window, p.block, p.G);
+    w.n_lm_tiles = static_cast<int>((n_lm + kBN - 1) / kBN);
+  }
   w.T = w.n_lm_tiles + n_win;
   return w;
 }
@@ -245,8 +255,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       bool ok = true;
       auto load_tile = [&](const Unit& w, int t, bool is_k, uint32_t dst, uint32_t mbar) {
         const bool lm = t < w.n_lm_tiles;
-        const CUtensorMap* m = is_k ? (lm ? &p.tm_klm : &p.tm_k) : (lm ? &p.tm_vlm : &p.tm_v);
-        const int row = lm ? t * kBN : (w.kt_lo + t - w.n_lm_tiles) * kBN;
+        int row;
+        const CUtensorMap* m;
+        if (lm && p.select) {  // tile of a selected block, from K/V themselves
+          const int tpb = static_cast<int>(p.block / kBN);
+          const int64_t blk = sel_block_checked(
+              p.sel[(w.qr0 / kBM * p.Hkv + w.kvh) * p.top_k + t / tpb],
+              visible_landmarks(w.qr0, p.window, p.block, p.G), p.status);
+          row = static_cast<int>(blk * p.block) + (t % tpb) * kBN;
+          m = is_k ? &p.tm_k : &p.tm_v;
+        } else {
+          m = is_k ? (lm ? &p.tm_klm : &p.tm_k) : (lm ? &p.tm_vlm : &p.tm_v);
+          row = lm ? t * kBN : (w.kt_lo + t - w.n_lm_tiles) * kBN;
+        }
         for (int c = 0; c < 2; ++c)
           ptx::tma_load_3d(dst + c * kChunkBytes, m, mbar, c * 64, w.kvh, row);
       };
@@ -432,7 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         my_lo = max64(i - p.window + 1, p.kv_start);
         my_hi = min64(i, kv_end - 1);
       }
-      const int64_t my_lm = visible_landmarks(i, p.window, p.block, p.G);
+      // Selected blocks lie wholly before every row's window: no mask.
+      const int64_t my_lm =
+          p.select ? INT64_MAX / 2 : visible_landmarks(i, p.window, p.block, p.G);
       float m_used = -INFINITY;
       float l = 0.f;
       for (int t = 0; t < w.T; ++t) {
@@ -662,14 +685,14 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s, const char** why) 
   const bool ok = encode_map(fn, &p.tm_q, a.q, a.n_q, a.Hq) &&
                   encode_map(fn, &p.tm_k, a.k, a.n_kv, a.Hkv) &&
                   encode_map(fn, &p.tm_v, a.v, a.n_kv, a.Hkv) &&
-                  (a.G > 0 ? encode_map(fn, &p.tm_klm, a.k_lm, a.G, a.Hkv) &&
-                                 encode_map(fn, &p.tm_vlm, a.v_lm, a.G, a.Hkv)
-                           : true);
+                  (a.G > 0 && !a.sel ? encode_map(fn, &p.tm_klm, a.k_lm, a.G, a.Hkv) &&
+                                           encode_map(fn, &p.tm_vlm, a.v_lm, a.G, a.Hkv)
+                                     : true);
   if (!ok) {
     *why = "cuTensorMapEncodeTiled rejected a tensor (alignment or size)";
     return cudaErrorInvalidValue;
   }
-  if (a.G == 0) {
+  if (a.G == 0 || a.sel) {  // no landmark tensors read
     p.tm_klm = p.tm_k;
     p.tm_vlm = p.tm_v;
   }
@@ -693,6 +716,10 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s, const char** why) 
   p.band = a.band;
   p.band_block = a.band_block;
   p.band_half = a.band_half;
+  p.sel = a.sel;
+  p.sel_cnt = a.sel_cnt;
+  p.top_k = a.top_k;
+  p.select = a.sel != nullptr;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = a.status;
   p.wait_ns = a.wait_limit_ns;

@@ -1,0 +1,129 @@
+// K4: landmark-scored top-k block selection -- the stand-in for the
+// hierarchical context index of "Million Token Context Window Optimization:
+// What Actually Works", section "The indexing game: smarter context
+// management" (score the chunks of the input against the query, attend only
+// the top-k chunks plus a history window; a chunk's landmark, its mean key,
+// scores it here instead of a BERT embedding).
+//
+// One CTA per (query block of 128 rows, KV group): it sums the block's
+// queries over rows and the group's heads (fp32), scores every key block
+// wholly before the window of the block's first row against its landmark
+// key, ranks the scores (ties to the lower block index) and writes the
+// top-k block indices in ascending order, and their count.
+#include <math.h>
+
+#include "msa_common.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kSelThreads = 256;
+
+template <bool kBf16>
+__device__ __forceinline__ float ld_el(const void* base, int64_t idx) {
+  if constexpr (kBf16) {
+    return bf16_bits_to_float(static_cast<const uint16_t*>(base)[idx]);
+  } else {
+    return static_cast<const float*>(base)[idx];
+  }
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectArgs a) {
+  extern __shared__ float ssm[];
+  float* qsum = ssm;               // [d]
+  float* part = qsum + a.d;        // [2][d] partial sums
+  float* score = part + 2 * a.d;   // [G]
+  int* flag = reinterpret_cast<int*>(score + a.G);  // [G]
+  const int t = blockIdx.x;        // query block
+  const int c = blockIdx.y;        // KV group
+  const int d = a.d;
+  const int g = a.Hq / a.Hkv;
+  const int64_t r0 = static_cast<int64_t>(t) * kSelQBlock;
+  const int64_t r1 = min64(r0 + kSelQBlock, a.n);
+
+  // Query-block sum over rows and the group's heads.
+  for (int col = threadIdx.x; col < 2 * d; col += blockDim.x) {
+    const int e = col % d;
+    const int half = col / d;
+    float s = 0.f;
+    for (int64_t i = r0 + half; i < r1; i += 2)
+      for (int hh = 0; hh < g; ++hh)
+        s += ld_el<kBf16>(a.q, (i * a.Hq + c * g + hh) * static_cast<int64_t>(d) + e);
+    part[half * d + e] = s;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < d; e += blockDim.x) qsum[e] = part[e] + part[d + e];
+  __syncthreads();
+
+  // Candidates: blocks l with (l+1)*bs <= r0 - w + 1.
+  const int64_t n_cand = visible_landmarks(r0, a.window, a.block, a.G);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int64_t l = warp; l < n_cand; l += kSelThreads / 32) {
+    float s = 0.f;
+    for (int e = lane; e < d; e += 32)
+      s += qsum[e] * ld_el<kBf16>(a.k_lm, (l * a.Hkv + c) * static_cast<int64_t>(d) + e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    // NaN ranks as -inf so that (score, index) stays a total order and
+    // exactly min(top_k, n_cand) blocks are chosen.
+    if (lane == 0) score[l] = isnan(s) ? -INFINITY : s;
+  }
+  __syncthreads();
+
+  // Rank: block l is chosen iff fewer than top_k blocks beat it (higher
+  // score, or equal score and lower index).
+  for (int64_t l = threadIdx.x; l < n_cand; l += blockDim.x) {
+    const float sl = score[l];
+    int beaten = 0;
+    for (int64_t m = 0; m < n_cand && beaten < a.top_k; ++m) {
+      const float sm = score[m];
+      beaten += (sm > sl || (sm == sl && m < l)) ? 1 : 0;
+    }
+    flag[l] = beaten < a.top_k ? 1 : 0;
+  }
+  __syncthreads();
+
+  // Compact the chosen indices in ascending order (one warp, ballots).
+  if (warp == 0) {
+    int32_t* out = a.sel + (static_cast<int64_t>(t) * a.Hkv + c) * a.top_k;
+    int base = 0;
+    for (int64_t l0 = 0; l0 < n_cand; l0 += 32) {
+      const int64_t l = l0 + lane;
+      const bool f = l < n_cand && flag[l];
+      const unsigned m = __ballot_sync(0xffffffffu, f);
+      const int slot = base + __popc(m & ((1u << lane) - 1u));
+      if (f && slot < a.top_k) out[slot] = static_cast<int32_t>(l);
+      base += __popc(m);
+    }
+    if (lane == 0) a.cnt[static_cast<int64_t>(t) * a.Hkv + c] = min(base, a.top_k);
+  }
+}
+
+}  // namespace
+
+size_t block_select_smem(int d, int G) {
+  return sizeof(float) * (3 * static_cast<size_t>(d) + G) + sizeof(int) * static_cast<size_t>(G);
+}
+
+cudaError_t launch_block_select(const SelectArgs& a, cudaStream_t s) {
+  const size_t smem = block_select_smem(a.d, a.G);
+  const int64_t n_qb = (a.n + kSelQBlock - 1) / kSelQBlock;
+  dim3 grid(static_cast<unsigned>(n_qb), a.Hkv);
+  if (a.bf16) {
+    cudaError_t e = cudaFuncSetAttribute(block_select_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    block_select_kernel<true><<<grid, kSelThreads, smem, s>>>(a);
+  } else {
+    cudaError_t e = cudaFuncSetAttribute(block_select_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    block_select_kernel<false><<<grid, kSelThreads, smem, s>>>(a);
+  }
+  return cudaPeekAtLastError();
+}
+
+}  // namespace msa

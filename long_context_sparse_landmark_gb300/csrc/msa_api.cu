@@ -92,13 +92,51 @@ msa_status run_attn(const msa::AttnArgs& a0, cudaStream_t stream) {
   if (st != MSA_OK) return st;
   const uint64_t lim = g_wait_limit_ns.load();
   a.wait_limit_ns = lim ? lim : kDefaultWaitNs;
-  if (msa::attn_tc_supported(a.Hq, a.Hkv, a.d, a.in_bf16)) {
+  // Selected blocks map to whole 128-key tiles on the tensor-core path.
+  const bool tiles_ok = !a.sel || a.block % 128 == 0;
+  if (tiles_ok && msa::attn_tc_supported(a.Hq, a.Hkv, a.d, a.in_bf16)) {
     const char* why = nullptr;
     cudaError_t e = msa::launch_attn_tc(a, stream, &why);
     if (e != cudaSuccess && why) return fail(MSA_ERR_CUDA, "tensor-core attention: %s", why);
     return launched(e, "tensor-core attention");
   }
   return launched(msa::launch_attn_simt(a, stream), "attention");
+}
+
+// Pool the block-mean keys, select each query block's top-k key blocks,
+// attend window + selected blocks: three launches on `stream`.
+msa_status topk_forward(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int64_t n, int Hq, int Hkv, int d, int64_t window, int G, int top_k,
+                        float scale, msa_dtype in_dt, msa_dtype out_dt, void* k_lm, int32_t* sel,
+                        int32_t* cnt, cudaStream_t stream) {
+  msa::PoolArgs pa{k, nullptr, k_lm, nullptr, n, Hkv * d, G, in_dt == MSA_BF16 ? 1 : 0};
+  msa_status st = launched(msa::launch_landmark_pool(pa, stream), "landmark pool");
+  if (st != MSA_OK) return st;
+  msa::SelectArgs sa{q, k_lm, sel, cnt, n, Hq, Hkv, d, window, G, n / G, top_k,
+                     in_dt == MSA_BF16 ? 1 : 0};
+  st = launched(msa::launch_block_select(sa, stream), "block select");
+  if (st != MSA_OK) return st;
+  msa::AttnArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  a.n_q = n;
+  a.n_kv = n;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.window = window;
+  a.G = G;
+  a.block = n / G;
+  a.scale = scale;
+  a.in_bf16 = in_dt == MSA_BF16;
+  a.out_bf16 = out_dt == MSA_BF16;
+  a.sel = sel;
+  a.sel_cnt = cnt;
+  a.top_k = top_k;
+  return run_attn(a, stream);
 }
 
 }  // namespace
@@ -200,6 +238,119 @@ msa_status msa_attn_fwd_band(const void* q, const void* k, const void* v, void* 
   a.band_block = band_block;
   a.band_half = band_half;
   return run_attn(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Shared checks of the top-k entry points.
+static msa_status check_topk(int64_t n, int G, int top_k) {
+  if (n < 1 || n > kMaxRows) return fail(MSA_ERR_INVALID_ARG, "n=%lld out of range", (long long)n);
+  if (G < 1 || G > n || n % G != 0)
+    return fail(MSA_ERR_INVALID_ARG, "G=%d must satisfy 1 <= G <= n and n %% G == 0", G);
+  if (G > MSA_MAX_SELECT_BLOCKS)
+    return fail(MSA_ERR_UNSUPPORTED, "G=%d key blocks (at most %d)", G, MSA_MAX_SELECT_BLOCKS);
+  if (top_k < 1 || top_k > G) return fail(MSA_ERR_INVALID_ARG, "top_k=%d must be in [1, G]", top_k);
+  return MSA_OK;
+}
+
+msa_status msa_block_select(const void* q, const void* k_lm, int32_t* sel, int32_t* cnt, int64_t n,
+                            int Hq, int Hkv, int d, int64_t window, int n_landmarks, int top_k,
+                            msa_dtype in_dt, msa_stream_t stream) {
+  if (!q || !k_lm || !sel || !cnt) return fail(MSA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k_lm) || !aligned16(sel) || !aligned16(cnt))
+    return fail(MSA_ERR_INVALID_ARG, "tensor pointer not 16-byte aligned");
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+    return fail(MSA_ERR_INVALID_ARG, "Hq=%d Hkv=%d", Hq, Hkv);
+  if (window < 1) return fail(MSA_ERR_INVALID_ARG, "window must be >= 1");
+  if (!valid_dtype(in_dt)) return fail(MSA_ERR_INVALID_ARG, "bad input dtype %d", (int)in_dt);
+  if (d != 64 && d != 128) return fail(MSA_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+  msa_status st = check_topk(n, n_landmarks, top_k);
+  if (st != MSA_OK) return st;
+  msa::SelectArgs a{q, k_lm, sel, cnt, n, Hq, Hkv, d, window, n_landmarks, n / n_landmarks, top_k,
+                    in_dt == MSA_BF16 ? 1 : 0};
+  return launched(msa::launch_block_select(a, reinterpret_cast<cudaStream_t>(stream)),
+                  "block select");
+}
+
+msa_status msa_attn_fwd_select(const void* q, const void* k, const void* v, const int32_t* sel,
+                               const int32_t* cnt, void* out, float* lse, int64_t n, int Hq,
+                               int Hkv, int d, int64_t window, int n_landmarks, int top_k,
+                               float scale, msa_dtype in_dt, msa_dtype out_dt,
+                               msa_stream_t stream) {
+  msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, window, scale, in_dt);
+  if (st != MSA_OK) return st;
+  if (!sel || !cnt) return fail(MSA_ERR_INVALID_ARG, "null selection pointer");
+  if (!aligned16(sel) || !aligned16(cnt))
+    return fail(MSA_ERR_INVALID_ARG, "selection pointer not 16-byte aligned");
+  if (!valid_dtype(out_dt)) return fail(MSA_ERR_INVALID_ARG, "bad output dtype %d", (int)out_dt);
+  st = check_topk(n, n_landmarks, top_k);
+  if (st != MSA_OK) return st;
+  msa::AttnArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  a.n_q = n;
+  a.n_kv = n;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.window = window;
+  a.G = n_landmarks;
+  a.block = n / n_landmarks;
+  a.scale = scale;
+  a.in_bf16 = in_dt == MSA_BF16;
+  a.out_bf16 = out_dt == MSA_BF16;
+  a.sel = sel;
+  a.sel_cnt = cnt;
+  a.top_k = top_k;
+  return run_attn(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Workspace layout of msa_attn_fwd_topk: block-mean keys, then the
+// selection indices, then the counts, each 256-byte aligned.
+struct TopkLayout {
+  size_t k_lm, sel, cnt, total;
+};
+
+static TopkLayout topk_layout(int64_t n, int Hkv, int d, int G, int top_k, msa_dtype in_dt) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t es = in_dt == MSA_BF16 ? 2 : 4;
+  const size_t n_qb = static_cast<size_t>((n + msa::kSelQBlock - 1) / msa::kSelQBlock);
+  TopkLayout L;
+  L.k_lm = 0;
+  L.sel = up(static_cast<size_t>(G) * Hkv * d * es);
+  L.cnt = L.sel + up(n_qb * Hkv * top_k * sizeof(int32_t));
+  L.total = L.cnt + up(n_qb * Hkv * sizeof(int32_t));
+  return L;
+}
+
+size_t msa_attn_fwd_topk_workspace_size(int64_t n, int Hkv, int d, int n_landmarks, int top_k,
+                                        msa_dtype in_dt) {
+  if (Hkv < 1 || d < 1 || !valid_dtype(in_dt) || check_topk(n, n_landmarks, top_k) != MSA_OK)
+    return 0;
+  return topk_layout(n, Hkv, d, n_landmarks, top_k, in_dt).total;
+}
+
+msa_status msa_attn_fwd_topk(const void* q, const void* k, const void* v, void* out, float* lse,
+                             int64_t n, int Hq, int Hkv, int d, int64_t window, int n_landmarks,
+                             int top_k, float scale, msa_dtype in_dt, msa_dtype out_dt,
+                             void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, window, scale, in_dt);
+  if (st != MSA_OK) return st;
+  if (!valid_dtype(out_dt)) return fail(MSA_ERR_INVALID_ARG, "bad output dtype %d", (int)out_dt);
+  st = check_topk(n, n_landmarks, top_k);
+  if (st != MSA_OK) return st;
+  const TopkLayout L = topk_layout(n, Hkv, d, n_landmarks, top_k, in_dt);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(MSA_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
+  if (workspace_bytes < L.total)
+    return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                L.total);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return topk_forward(q, k, v, out, lse, n, Hq, Hkv, d, window, n_landmarks, top_k, scale, in_dt,
+                      out_dt, ws + L.k_lm, reinterpret_cast<int32_t*>(ws + L.sel),
+                      reinterpret_cast<int32_t*>(ws + L.cnt),
+                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 msa_status msa_attn_fwd_partial(const void* q, const void* k_chunk, const void* v_chunk,

@@ -31,6 +31,28 @@ __device__ __forceinline__ void record_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Selection entries are device data the caller may have written: a count
+// outside [0, min(top_k, candidates)] or a block index that is not a
+// candidate of its query block is clamped into range (count) or replaced by
+// block 0 (index) and MSA_ERR_INVALID_ARG recorded, so that no selection
+// can make a kernel read outside K and V.
+__device__ __forceinline__ int64_t sel_count_checked(int32_t cnt, int top_k, int64_t n_cand,
+                                                     int* status) {
+  const int64_t hi = min64(top_k, n_cand);
+  if (cnt < 0 || cnt > hi) {
+    record_status(status, MSA_ERR_INVALID_ARG);
+    return cnt < 0 ? 0 : hi;
+  }
+  return cnt;
+}
+__device__ __forceinline__ int64_t sel_block_checked(int32_t blk, int64_t n_cand, int* status) {
+  if (blk < 0 || blk >= n_cand) {
+    record_status(status, MSA_ERR_INVALID_ARG);
+    return 0;
+  }
+  return blk;
+}
+
 // Keys of row `pos` under the block-band mask: every key of the blocks
 // (size bb) within hw blocks of the row's own, clipped to [0, n_kv).
 __host__ __device__ __forceinline__ void band_keys(int64_t pos, int64_t bb, int64_t hw,
@@ -92,10 +114,35 @@ struct AttnArgs {
   int merge;    // out/lse hold a running result: merge this partial into it
   int band;     // block-band mask instead of window + landmarks
   int64_t band_block, band_half;
+  // Top-k selected key blocks instead of landmarks: sel[t][c][0..cnt[t][c])
+  // are the blocks (of `block` tokens) attended by query block t (128 rows)
+  // of KV group c, in full, besides the window.
+  const int32_t* sel;
+  const int32_t* sel_cnt;
+  int top_k;
   int* status;  // device status word
   uint64_t wait_limit_ns;
 };
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t s);
+
+// Query rows per selection block (one tensor-core work unit).
+constexpr int kSelQBlock = 128;
+
+struct SelectArgs {
+  const void* q;
+  const void* k_lm;
+  int32_t* sel;   // [n_qb, Hkv, top_k]
+  int32_t* cnt;   // [n_qb, Hkv]
+  int64_t n;
+  int Hq, Hkv, d;
+  int64_t window;
+  int G;
+  int64_t block;  // tokens per key block (n / G)
+  int top_k;
+  int bf16;
+};
+cudaError_t launch_block_select(const SelectArgs& a, cudaStream_t s);
+size_t block_select_smem(int d, int G);
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s, const char** why);
 bool attn_tc_supported(int Hq, int Hkv, int d, int in_bf16);
 

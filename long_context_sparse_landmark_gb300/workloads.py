@@ -1,6 +1,6 @@
 """Seeded synthetic workloads (shapes and input generators only).
 
-This module holds no attention arithmetic: it names the five workloads the
+This module holds no attention arithmetic: it names the workloads the
 library is measured and checked on, draws their Q/K/V from a seeded
 generator, and picks the sampled rows that large parity checks evaluate.
 Both the CUDA path's tests/benchmark and the CPU oracle's tests read their
@@ -35,6 +35,8 @@ class Workload:
     seed: int = 0
     band_block: int = 0      # > 0: block-band mask (blocks of this size) instead
     band_half: int = 0       #      of window + landmarks; half-width in blocks
+    top_k: int = 0           # > 0: window + the top_k landmark-scored key blocks
+                             #      of each 128-row query block (G blocks)
 
     @property
     def scale(self) -> float:
@@ -76,6 +78,13 @@ WORKLOADS = {
     # blocks, each attending the 8 blocks on either side (16 neighbours).
     "band_128k": Workload("band_128k", 131072, 64, 8, 128, 1, 0, "bf16",
                           band_block=128, band_half=8),
+    # Top-k block selection on the 70B-style layer at 128K tokens: 256-token
+    # chunks (512 blocks), the 50 best-scoring ones per query block plus a
+    # 1024-token window ("Million Token Context Window Optimization: What
+    # Actually Works", section "The indexing game: smarter context
+    # management").
+    "topk_128k": Workload("topk_128k", 131072, 64, 8, 128, 1024, 512, "bf16",
+                          top_k=50),
 }
 
 

@@ -27,13 +27,19 @@ def main():
         k = np.zeros((wl.n, 1, 1), dtype=np.float32)
         if wl.band_block > 0:
             _, lse = oracle.attn_band(q, k, k, wl.band_block, wl.band_half, 1.0)
+        elif wl.top_k > 0:
+            # every score 0: the count does not depend on which blocks win
+            scores = oracle.block_scores(q, k, wl.G, wl.window)
+            sel, cnt = oracle.select_top_k(scores, wl.top_k)
+            _, lse = oracle.attn_select(q, k, k, wl.window, wl.G, sel, cnt, 1.0)
         else:
             _, lse = oracle.attn(q, k, k, wl.window, wl.G, 1.0)
         counts = np.rint(np.exp(lse[0])).astype(np.int64)
         per_head[name] = int(counts.sum())
         print(name, per_head[name], flush=True)
     out = {
-        "what": "sum over rows of |attended set| per head (window + visible landmarks, or the block band)",
+        "what": ("sum over rows of |attended set| per head (window + visible landmarks, "
+                 "the block band, or window + selected blocks)"),
         "written_by": "tests/golden/make_counts.py (CPU oracle, K = 0 so lse = ln count)",
         "per_head": per_head,
     }

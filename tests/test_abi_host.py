@@ -161,3 +161,71 @@ def test_merge_validation(lib):
     assert f(arr, larr, 2, GOOD, P(4 << 20), 16, 2, 8, 0, None) == 1  # lse aliases part 1
     bad = (ctypes.c_void_p * 2)(1 << 20, (2 << 20) + 4)
     assert f(bad, larr, 2, P(5 << 20), P(6 << 20), 16, 2, 8, 0, None) == 1
+
+
+def test_block_select_validation(lib):
+    f = lib.msa_block_select
+
+    def call(**kw):
+        a = dict(q=GOOD, klm=GOOD, sel=GOOD, cnt=GOOD, n=1024, Hq=4, Hkv=2, d=128, w=64, G=8,
+                 k=3, idt=1)
+        a.update(kw)
+        return f(a["q"], a["klm"], a["sel"], a["cnt"], a["n"], a["Hq"], a["Hkv"], a["d"], a["w"],
+                 a["G"], a["k"], a["idt"], None)
+
+    assert call(sel=None) == 1
+    assert call(cnt=BAD_ALIGN) == 1
+    assert call(Hq=3) == 1
+    assert call(w=0) == 1
+    assert call(G=0) == 1
+    assert call(G=7) == 1          # n % G
+    assert call(G=2048, n=2048) == 2  # above the largest block count
+    assert call(k=0) == 1
+    assert call(k=9) == 1          # top_k > G
+    assert call(n=0) == 1
+    assert call(d=96) == 2
+
+
+def test_attn_select_validation(lib):
+    f = lib.msa_attn_fwd_select
+
+    def call(**kw):
+        a = dict(q=GOOD, k=GOOD, v=GOOD, sel=GOOD, cnt=GOOD, o=GOOD, l=GOOD, n=1024, Hq=4, Hkv=2,
+                 d=128, w=64, G=8, tk=3, idt=1, odt=0)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["sel"], a["cnt"], a["o"], a["l"], a["n"], a["Hq"],
+                 a["Hkv"], a["d"], a["w"], a["G"], a["tk"], ctypes.c_float(0.1), a["idt"],
+                 a["odt"], None)
+
+    assert call(cnt=None) == 1
+    assert call(sel=BAD_ALIGN) == 1
+    assert call(v=None) == 1
+    assert call(odt=5) == 1
+    assert call(G=3) == 1
+    assert call(tk=0) == 1
+    assert call(d=32) == 2
+
+
+def test_topk_workspace_size_and_validation(lib):
+    size = lib.msa_attn_fwd_topk_workspace_size
+    # k_lm 8*2*128 bf16 = 4096; sel 8 query blocks*2*3*4 = 192 -> 256; cnt 64 -> 256
+    assert size(1024, 2, 128, 8, 3, 1) == 4096 + 256 + 256
+    assert size(1000, 2, 128, 8, 3, 1) == 4096 + 256 + 256
+    assert size(1024, 2, 128, 8, 0, 1) == 0   # invalid sizes
+    assert size(1024, 2, 128, 7, 3, 1) == 0
+    f = lib.msa_attn_fwd_topk
+    need = size(1024, 2, 128, 8, 3, 1)
+
+    def call(**kw):
+        a = dict(q=GOOD, k=GOOD, v=GOOD, o=GOOD, l=GOOD, n=1024, Hq=4, Hkv=2, d=128, w=64, G=8,
+                 tk=3, idt=1, odt=0, ws=GOOD, wsb=need)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["o"], a["l"], a["n"], a["Hq"], a["Hkv"], a["d"],
+                 a["w"], a["G"], a["tk"], ctypes.c_float(0.1), a["idt"], a["odt"], a["ws"],
+                 a["wsb"], None)
+
+    assert call(ws=None) == 1
+    assert call(ws=P((1 << 20) + 16)) == 1    # not 256-byte aligned
+    assert call(wsb=need - 1) == 1
+    assert call(tk=9) == 1
+    assert call(d=96) == 2

@@ -351,12 +351,24 @@ def band_total_closed_form(n, bb, hw):
     return int((hi - lo).sum())
 
 
+def topk_total_closed_form(n, w, G, top_k, q_block=128):
+    """Each row: its window plus min(top_k, candidates of its query block's
+    first row) whole blocks."""
+    i = np.arange(n, dtype=np.int64)
+    B = n // G
+    r0 = (i // q_block) * q_block
+    cand = np.clip((r0 - w + 1) // B, 0, G)
+    return int((np.minimum(w, i + 1) + np.minimum(top_k, cand) * B).sum())
+
+
 def test_p6_workload_totals_match_golden():
     with open(os.path.join(GOLDEN, "attended_counts.json")) as f:
         golden = json.load(f)
     for name, wl in WORKLOADS.items():
         if wl.band_block > 0:
             total = band_total_closed_form(wl.n, wl.band_block, wl.band_half)
+        elif wl.top_k > 0:
+            total = topk_total_closed_form(wl.n, wl.window, wl.G, wl.top_k)
         else:
             total = attended_total_closed_form(wl.n, wl.window, wl.G)
         assert total == golden["per_head"][name], name
