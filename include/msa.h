@@ -197,6 +197,38 @@ msa_status msa_attn_fwd_topk(const void *q, const void *k, const void *v,
                              void *workspace, size_t workspace_bytes,
                              msa_stream_t stream);
 
+/* Bytes of the fixed device scratch msa_attn_fwd_topk_noalloc uses (16 MiB;
+ * the 1M-token layer with 512 blocks, 8 KV heads, d = 128 bf16 and top-50
+ * needs 14,417,920). */
+#define MSA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * msa_attn_fwd_topk without a workspace argument, for callers that cannot
+ * allocate device memory (a plain C host program holding no allocator, or a
+ * runtime that must not call cudaMalloc between launches).  The pages
+ * describe no such entry point; it is an interface convenience only, with
+ * the same kernels and results as msa_attn_fwd_topk.
+ * The intermediates live in one fixed, file-scope device array of
+ * MSA_NOALLOC_SCRATCH_BYTES per device; nothing is allocated or freed.
+ *   - The first call on a device looks up that array's address (with the
+ *     device current) and caches it; make that first call, on each device,
+ *     before any stream capture begins.
+ *   - The scratch is shared by every call on a device: calls whose work can
+ *     overlap (unordered streams, several host threads) race on it and give
+ *     wrong results.  Order them on one stream.
+ *   - Nothing in the scratch needs to start at zero.
+ * Errors: as msa_attn_fwd_topk; MSA_ERR_UNSUPPORTED (with the sizes in
+ * msa_last_error_string) when the sizes need more than
+ * MSA_NOALLOC_SCRATCH_BYTES, i.e. msa_attn_fwd_topk_workspace_size above it;
+ * MSA_ERR_CUDA if the address lookup fails.
+ */
+msa_status msa_attn_fwd_topk_noalloc(const void *q, const void *k, const void *v,
+                                     void *out, float *lse, int64_t n, int Hq,
+                                     int Hkv, int d, int64_t window,
+                                     int n_landmarks, int top_k, float scale,
+                                     msa_dtype in_dt, msa_dtype out_dt,
+                                     msa_stream_t stream);
+
 /*
  * One Ring Attention round's partial: queries at global positions
  * q_start .. q_start+n_q-1 against the contiguous KV chunk at global

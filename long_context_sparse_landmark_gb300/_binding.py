@@ -22,7 +22,8 @@ MAX_MERGE_PARTS = 64
 # Every symbol include/msa.h declares.
 EXPORTS = ("msa_version", "msa_last_error_string", "msa_landmark_pool", "msa_attn_fwd",
            "msa_attn_fwd_band", "msa_block_select", "msa_attn_fwd_select",
-           "msa_attn_fwd_topk_workspace_size", "msa_attn_fwd_topk", "msa_attn_fwd_partial",
+           "msa_attn_fwd_topk_workspace_size", "msa_attn_fwd_topk", "msa_attn_fwd_topk_noalloc",
+           "msa_attn_fwd_partial",
            "msa_attn_fwd_partial_merge", "msa_lse_merge",
            "msa_attn_uses_tensor_cores", "msa_device_status", "msa_debug_set_wait_limit_ns")
 
@@ -59,6 +60,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_attn_fwd_topk.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32, i32, f32,
                                       i32, i32, vp, ctypes.c_size_t, vp]
     lib.msa_attn_fwd_topk.restype = i32
+    lib.msa_attn_fwd_topk_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32,
+                                              i32, f32, i32, i32, vp]
+    lib.msa_attn_fwd_topk_noalloc.restype = i32
     lib.msa_attn_fwd_partial.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, i32,
                                          i64, f32, i32, vp]
     lib.msa_attn_fwd_partial.restype = i32
@@ -187,6 +191,17 @@ def attn_fwd_topk(q, k, v, out, lse, window: int, n_landmarks: int, top_k: int, 
                                   int(window), int(n_landmarks), int(top_k), float(scale), _dt(q),
                                   _dt(out), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def attn_fwd_topk_noalloc(q, k, v, out, lse, window: int, n_landmarks: int, top_k: int,
+                          scale: float, stream=None) -> None:
+    """msa_attn_fwd_topk_noalloc: the one-call top-k path on the library's
+    fixed per-device scratch (no workspace argument)."""
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    _check(_lib.msa_attn_fwd_topk_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), n, Hq,
+                                          Hkv, d, int(window), int(n_landmarks), int(top_k),
+                                          float(scale), _dt(q), _dt(out), _stream(stream)))
 
 
 def attn_fwd_partial(q, k_chunk, v_chunk, out_part, lse_part, q_start: int, kv_start: int,

@@ -141,6 +141,39 @@ msa_status topk_forward(const void* q, const void* k, const void* v, void* out, 
 
 }  // namespace
 
+// Fixed per-device scratch of msa_attn_fwd_topk_noalloc: the block-mean
+// keys, the selection and its counts of one call, laid out as the caller
+// workspace of msa_attn_fwd_topk.  Nothing in it needs to start at zero:
+// every launch writes each byte it later reads (all block-mean keys, every
+// count, and the chosen indices below each count) before reading it.
+static __device__ __align__(256) uint8_t g_topk_scratch[MSA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_scratch_mu;
+uint8_t* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device, looked up once per
+// device (with that device current) and cached.
+msa_status topk_scratch_ptr(uint8_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(MSA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_topk_scratch);
+    if (e != cudaSuccess)
+      return fail(MSA_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    g_scratch_ptr[dev] = static_cast<uint8_t*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return MSA_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int msa_version(void) { return 100; }
@@ -347,6 +380,36 @@ msa_status msa_attn_fwd_topk(const void* q, const void* k, const void* v, void* 
     return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
                 L.total);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return topk_forward(q, k, v, out, lse, n, Hq, Hkv, d, window, n_landmarks, top_k, scale, in_dt,
+                      out_dt, ws + L.k_lm, reinterpret_cast<int32_t*>(ws + L.sel),
+                      reinterpret_cast<int32_t*>(ws + L.cnt),
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+// The top-k path for callers that cannot allocate device memory: a plain C
+// host program that links only this library and holds no allocator of its
+// own, or a runtime that must not call cudaMalloc between launches because
+// it can synchronise the whole device and stall its other streams.  Same
+// kernels and launches as msa_attn_fwd_topk; the intermediates go to the
+// fixed scratch above instead of a caller workspace.
+msa_status msa_attn_fwd_topk_noalloc(const void* q, const void* k, const void* v, void* out,
+                                     float* lse, int64_t n, int Hq, int Hkv, int d,
+                                     int64_t window, int n_landmarks, int top_k, float scale,
+                                     msa_dtype in_dt, msa_dtype out_dt, msa_stream_t stream) {
+  msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, window, scale, in_dt);
+  if (st != MSA_OK) return st;
+  if (!valid_dtype(out_dt)) return fail(MSA_ERR_INVALID_ARG, "bad output dtype %d", (int)out_dt);
+  st = check_topk(n, n_landmarks, top_k);
+  if (st != MSA_OK) return st;
+  const TopkLayout L = topk_layout(n, Hkv, d, n_landmarks, top_k, in_dt);
+  if (L.total > static_cast<size_t>(MSA_NOALLOC_SCRATCH_BYTES))
+    return fail(MSA_ERR_UNSUPPORTED,
+                "these sizes need %zu bytes of scratch; the fixed scratch holds %zu "
+                "(use msa_attn_fwd_topk with a workspace)",
+                L.total, static_cast<size_t>(MSA_NOALLOC_SCRATCH_BYTES));
+  uint8_t* ws = nullptr;
+  st = topk_scratch_ptr(&ws);
+  if (st != MSA_OK) return st;
   return topk_forward(q, k, v, out, lse, n, Hq, Hkv, d, window, n_landmarks, top_k, scale, in_dt,
                       out_dt, ws + L.k_lm, reinterpret_cast<int32_t*>(ws + L.sel),
                       reinterpret_cast<int32_t*>(ws + L.cnt),
