@@ -37,6 +37,15 @@ class Workload:
     band_half: int = 0       #      of window + landmarks; half-width in blocks
     top_k: int = 0           # > 0: window + the top_k landmark-scored key blocks
                              #      of each 128-row query block (G blocks)
+    global_every: int = 0    # > 0: rows c*global_every - 1 are global query rows
+                             #      (attend every key j <= i); G gives the
+                             #      compression tokens of the other rows
+
+    def global_rows(self):
+        """Positions of the global query rows (ascending), as a list."""
+        if self.global_every <= 0:
+            return []
+        return list(range(self.global_every - 1, self.n, self.global_every))
 
     @property
     def scale(self) -> float:
@@ -85,6 +94,13 @@ WORKLOADS = {
     # management").
     "topk_128k": Workload("topk_128k", 131072, 64, 8, 128, 1024, 512, "bf16",
                           top_k=50),
+    # Compression tokens + global rows on the 70B-style layer at 128K tokens:
+    # 4096-token window, one compression token per 32-token sub-block (256
+    # per 8192-token chunk, G = 4096), and the last row of every 8192-token
+    # chunk a global row attending all earlier keys ("Training at 1M+ Token
+    # Context", Block-Sparse Flash Attention paragraph).
+    "compress_128k": Workload("compress_128k", 131072, 64, 8, 128, 4096, 4096, "bf16",
+                              global_every=8192),
 }
 
 

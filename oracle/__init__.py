@@ -275,6 +275,39 @@ def attn_select(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int, n_land
     return out, lse
 
 
+def attn_compressed(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int, block: int,
+                    global_rows, scale: float, rows=None):
+    """Compression tokens plus global query rows, after the Block-Sparse
+    Flash Attention paragraph of "Training at 1M+ Token Context: Ring
+    Attention, YaRN, NTK-Aware Scaling GPU Cost" (local rows see a sliding
+    window, compression tokens summarise distant context, global tokens
+    attend to everything; 256 compression tokens per 8192-token chunk).
+
+    A compression token is the mean of K (and of V) over one ``block``-token
+    sub-block (block = 32 gives 256 per 8192 tokens).  A row not in
+    ``global_rows`` attends its window and the compression tokens of the
+    sub-blocks wholly before it -- window + landmark attention with
+    G = n / block.  A row in ``global_rows`` attends every key j <= i and
+    nothing else.  Returns (O [n_rows, Hq, d], lse [Hq, n_rows]) for
+    ``rows`` (indices of q, default all).
+    """
+    n = q.shape[0]
+    if block < 1 or n % block != 0:
+        raise ValueError("block must divide n")
+    rows = np.arange(n, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    is_global = np.isin(rows, np.asarray(global_rows, dtype=np.int64))
+    Hq, d = q.shape[1], q.shape[2]
+    out = np.empty((len(rows), Hq, d), dtype=np.float64)
+    lse = np.empty((Hq, len(rows)), dtype=np.float64)
+    local = np.nonzero(~is_global)[0]
+    glob = np.nonzero(is_global)[0]
+    if local.size:
+        out[local], lse[:, local] = attn(q, k, v, window, n // block, scale, rows=rows[local])
+    if glob.size:
+        out[glob], lse[:, glob] = attn(q, k, v, n, 0, scale, rows=rows[glob])
+    return out, lse
+
+
 def lse_merge(o_parts: np.ndarray, lse_parts: np.ndarray):
     """Merge P partials: o_parts [P, n, Hq, d], lse_parts [P, Hq, n] (fp64)."""
     o_parts = np.ascontiguousarray(o_parts, dtype=np.float64)

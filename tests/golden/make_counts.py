@@ -27,6 +27,8 @@ def main():
         k = np.zeros((wl.n, 1, 1), dtype=np.float32)
         if wl.band_block > 0:
             _, lse = oracle.attn_band(q, k, k, wl.band_block, wl.band_half, 1.0)
+        elif wl.global_every > 0:
+            _, lse = oracle.attn_compressed(q, k, k, wl.window, wl.block, wl.global_rows(), 1.0)
         elif wl.top_k > 0:
             # every score 0: the count does not depend on which blocks win
             scores = oracle.block_scores(q, k, wl.G, wl.window)
@@ -39,7 +41,8 @@ def main():
         print(name, per_head[name], flush=True)
     out = {
         "what": ("sum over rows of |attended set| per head (window + visible landmarks, "
-                 "the block band, or window + selected blocks)"),
+                 "the block band, window + selected blocks, or window + compression tokens "
+                 "and global rows)"),
         "written_by": "tests/golden/make_counts.py (CPU oracle, K = 0 so lse = ln count)",
         "per_head": per_head,
     }

@@ -361,6 +361,15 @@ def topk_total_closed_form(n, w, G, top_k, q_block=128):
     return int((np.minimum(w, i + 1) + np.minimum(top_k, cand) * B).sum())
 
 
+def compressed_total_closed_form(n, w, G, every):
+    """Rows c*every - 1 count i + 1 keys, the others min(w, i+1) + L(i)."""
+    i = np.arange(n, dtype=np.int64)
+    per = np.minimum(w, i + 1) + np.clip((i - w + 1) // (n // G), 0, G)
+    glob = np.arange(every - 1, n, every)
+    per[glob] = glob + 1
+    return int(per.sum())
+
+
 def test_p6_workload_totals_match_golden():
     with open(os.path.join(GOLDEN, "attended_counts.json")) as f:
         golden = json.load(f)
@@ -369,6 +378,8 @@ def test_p6_workload_totals_match_golden():
             total = band_total_closed_form(wl.n, wl.band_block, wl.band_half)
         elif wl.top_k > 0:
             total = topk_total_closed_form(wl.n, wl.window, wl.G, wl.top_k)
+        elif wl.global_every > 0:
+            total = compressed_total_closed_form(wl.n, wl.window, wl.G, wl.global_every)
         else:
             total = attended_total_closed_form(wl.n, wl.window, wl.G)
         assert total == golden["per_head"][name], name
@@ -561,3 +572,84 @@ def test_topk_planted_block_is_chosen(oracle_mod):
     for t in range(n // qb):
         if 3 * bs <= t * qb - w + 1:
             assert cnt[t, 0] == 1 and sel[t, 0, 0] == 2
+
+
+# ------------------------------------------------------------------- compression tokens + global rows
+def compressed_bruteforce(q, k, v, window, block, global_rows, scale):
+    """Dense [n, n + n/block] mask built element by element: a global row
+    sees every key j <= i; any other row its window and the sub-block means
+    whose whole sub-block ends at or before i - w + 1; masked softmax."""
+    q = q.astype(np.float64)
+    k = k.astype(np.float64)
+    v = v.astype(np.float64)
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv
+    C = n // block
+    kc = np.stack([k[c * block:(c + 1) * block].mean(axis=0) for c in range(C)])
+    vc = np.stack([v[c * block:(c + 1) * block].mean(axis=0) for c in range(C)])
+    gset = set(int(r) for r in global_rows)
+    mask = np.zeros((n, n + C), dtype=bool)
+    for i in range(n):
+        for j in range(n):
+            mask[i, j] = j <= i if i in gset else (i - window < j <= i)
+        if i not in gset:
+            for c in range(C):
+                mask[i, n + c] = (c + 1) * block - 1 <= i - window
+    out = np.zeros((n, Hq, d))
+    lse = np.zeros((Hq, n))
+    for h in range(Hq):
+        keys = np.concatenate([k[:, h // g], kc[:, h // g]])
+        vals = np.concatenate([v[:, h // g], vc[:, h // g]])
+        s_ = np.where(mask, scale * q[:, h] @ keys.T, -np.inf)
+        mx = s_.max(axis=1, keepdims=True)
+        e = np.where(mask, np.exp(s_ - mx), 0.0)
+        den = e.sum(axis=1, keepdims=True)
+        out[:, h] = (e / den) @ vals
+        lse[h] = (mx + np.log(den))[:, 0]
+    return out, lse
+
+
+@pytest.mark.parametrize("n,block,w,glob", [(64, 4, 9, [5, 40, 63]), (64, 8, 1, [0]),
+                                            (48, 2, 16, []), (40, 40, 3, [39]),
+                                            (96, 4, 20, list(range(0, 96, 7)))])
+def test_compressed_bruteforce(oracle_mod, n, block, w, glob):
+    rng = np.random.default_rng(n + block + w)
+    for (Hq, Hkv), d in itertools.product([(1, 1), (4, 2), (4, 1)], [4, 8]):
+        q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+        ro, rl = compressed_bruteforce(q, k, v, w, block, glob, 0.3)
+        o, l = oracle_mod.attn_compressed(q, k, v, w, block, glob, 0.3)
+        np.testing.assert_allclose(o, ro, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l, rl, rtol=0, atol=1e-12)
+
+
+def test_compressed_global_rows_are_causal_attention(oracle_mod):
+    """Global rows equal torch SDPA with the causal mask (fp64) at those
+    rows, whatever the window and compression."""
+    rng = np.random.default_rng(21)
+    n, Hq, Hkv, d = 128, 4, 2, 16
+    q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+    glob = [3, 31, 64, 127]
+    o, l = oracle_mod.attn_compressed(q, k, v, 8, 16, glob, 0.25, rows=glob)
+    tq = torch.from_numpy(q).double().permute(1, 0, 2)[None]
+    tk = torch.from_numpy(k).double().repeat_interleave(2, dim=1).permute(1, 0, 2)[None]
+    tv = torch.from_numpy(v).double().repeat_interleave(2, dim=1).permute(1, 0, 2)[None]
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=0.25,
+                                                           is_causal=True)
+    np.testing.assert_allclose(o, ref[0].permute(1, 0, 2).numpy()[glob], rtol=0, atol=1e-12)
+
+
+def test_compressed_counts_and_page_ratio(oracle_mod):
+    """K = 0: exp(lse) counts i + 1 keys on global rows and min(w, i+1) +
+    L(i) with 32-token sub-blocks elsewhere; 32-token sub-blocks give the
+    page's 256 compression tokens per 8192-token chunk."""
+    assert 8192 // 32 == 256
+    n, w, block = 1024, 100, 32
+    glob = [0, 511, 1023]
+    q = np.ones((n, 1, 1), dtype=np.float32)
+    k = np.zeros((n, 1, 1), dtype=np.float32)
+    _, l = oracle_mod.attn_compressed(q, k, k, w, block, glob, 1.0)
+    i = np.arange(n)
+    want = np.minimum(w, i + 1) + np.clip((i - w + 1) // block, 0, n // block)
+    want[glob] = np.asarray(glob) + 1
+    np.testing.assert_allclose(np.exp(l[0]), want, rtol=1e-12)
