@@ -373,6 +373,59 @@ def run_topk(wl, steps, warmup, dev, B, torch):
     return {"fused_ms": fused_ms, "select_ms": select_ms}
 
 
+def compressed_flops(wl) -> float:
+    """Useful FLOPs of window + compression tokens with global rows: rows
+    c*every - 1 attend i + 1 keys, the others min(w, i+1) + L(i)."""
+    import numpy as np
+    i = np.arange(wl.n, dtype=np.int64)
+    per_row = np.minimum(wl.window, i + 1) + np.clip((i - wl.window + 1) // wl.block, 0, wl.G)
+    glob = np.asarray(wl.global_rows(), dtype=np.int64)
+    per_row[glob] = glob + 1
+    return 4.0 * wl.d * wl.Hq * float(per_row.sum())
+
+
+def run_compressed(wl, steps, warmup, dev, B, torch):
+    """Compression tokens (pool with n/32 blocks) + window/compression
+    attention + global rows, device-resident inputs and preallocated
+    buffers; returns ms per step and of the global-rows call alone."""
+    from long_context_sparse_landmark_gb300.workloads import generate
+    q, k, v = generate(wl, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((wl.Hq, wl.n), dtype=torch.float32, device=dev)
+    k_lm = torch.empty((wl.G, wl.Hkv, wl.d), dtype=k.dtype, device=dev)
+    v_lm = torch.empty_like(k_lm)
+    rows = torch.as_tensor(wl.global_rows(), dtype=torch.int64, device=dev)
+    ws = torch.empty((B.global_rows_workspace_size(wl.n, rows.numel(), wl.Hq, wl.Hkv, wl.d),),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        B.landmark_pool(k, v, k_lm, v_lm, stream=stream)
+        B.attn_fwd(q, k, v, k_lm, v_lm, out, lse, wl.window, wl.G, wl.scale, stream=stream)
+        B.attn_fwd_global_rows(q, k, v, rows, out, lse, wl.scale, ws, stream=stream)
+
+    def glob():
+        B.attn_fwd_global_rows(q, k, v, rows, out, lse, wl.scale, ws, stream=stream)
+
+    res = {}
+    for name, fn in (("step_ms", step), ("global_ms", glob)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) / steps
+    assert B.device_status() == 0
+    del q, k, v, out, lse, k_lm, v_lm, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 def cpu_baseline(wl, rows_target, torch):
     """The fp64 oracle on the host cores, on a bounded row sample of the
     same workload; extrapolated to the full layer by rows."""
@@ -555,6 +608,18 @@ def main():
                              "select_gbs": round(sel_bytes / (rt["select_ms"] * 1e-3) / 1e9,
                                                  1),
                              "launches_per_step": 3, "steps": 3}
+        wlc = WORKLOADS["compress_128k"]
+        rc = run_compressed(wlc, 3, 1, dev, B, torch)
+        fc = compressed_flops(wlc)
+        fg = 4.0 * wlc.d * wlc.Hq * float(sum(r + 1 for r in wlc.global_rows()))
+        also["compress_128k"] = {"ms_per_step": round(rc["step_ms"], 3),
+                                 "tflops": round(fc / (rc["step_ms"] * 1e-3) / 1e12, 2),
+                                 "pct_bf16_peak": round(100.0 * fc / (rc["step_ms"] * 1e-3)
+                                                        / 1e12 / peaks["bf16_tflops"], 2),
+                                 "global_rows_ms": round(rc["global_ms"], 4),
+                                 "global_rows_tflops": round(fg / (rc["global_ms"] * 1e-3)
+                                                             / 1e12, 2),
+                                 "launches_per_step": 4, "steps": 3}
         wlr = WORKLOADS["ring_128k"]
         rr = run_ring(wlr, 3, 1, dev, B, torch)
         fr = useful_flops(wlr)

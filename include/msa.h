@@ -230,6 +230,40 @@ msa_status msa_attn_fwd_topk_noalloc(const void *q, const void *k, const void *v
                                      msa_stream_t stream);
 
 /*
+ * Global query rows of the block-sparse pattern in "Training at 1M+ Token
+ * Context: Ring Attention, YaRN, NTK-Aware Scaling GPU Cost" (Block-Sparse
+ * Flash Attention paragraph: global tokens attend to all, local tokens to a
+ * sliding window, compression tokens summarise distant context).  The local
+ * rows are msa_attn_fwd with n_landmarks = n / 32 (one compression token,
+ * the mean of K and of V, per 32-token sub-block: 256 per 8192 tokens);
+ * this call then overwrites, for every position r in rows[0..n_global),
+ * out[r, :, :] and lse[:, r] with attention over every key j <= r (causal,
+ * no compression tokens), one softmax.
+ *   q [n, Hq, d], k, v [n, Hkv, d] in `in_dt`; rows: device int64 array of
+ *   positions (any order; a repeated position is computed twice, same
+ *   result); out [n, Hq, d] in `out_dt`, lse [Hq, n] fp32: only the listed
+ *   rows are written.
+ *   workspace: device memory, 256-byte aligned, at least
+ *   msa_attn_fwd_global_rows_workspace_size bytes (per-split partials).
+ * Errors: as msa_attn_fwd, plus INVALID_ARG for a null or misaligned rows
+ * array or workspace, n_global < 1 or > n, a too small workspace;
+ * UNSUPPORTED when n_global * Hq / Hkv exceeds 262140.  A position outside
+ * [0, n) in rows is skipped by the kernels and MSA_ERR_INVALID_ARG recorded
+ * in the device status word (msa_device_status).
+ */
+msa_status msa_attn_fwd_global_rows(const void *q, const void *k, const void *v,
+                                    const int64_t *rows, int64_t n_global,
+                                    void *out, float *lse, int64_t n, int Hq,
+                                    int Hkv, int d, float scale,
+                                    msa_dtype in_dt, msa_dtype out_dt,
+                                    void *workspace, size_t workspace_bytes,
+                                    msa_stream_t stream);
+
+/* Bytes of workspace msa_attn_fwd_global_rows needs (0 for invalid sizes). */
+size_t msa_attn_fwd_global_rows_workspace_size(int64_t n, int64_t n_global,
+                                               int Hq, int Hkv, int d);
+
+/*
  * One Ring Attention round's partial: queries at global positions
  * q_start .. q_start+n_q-1 against the contiguous KV chunk at global
  * positions kv_start .. kv_start+n_kv-1, with the causal window mask

@@ -8,12 +8,13 @@ a missing library raises ImportError: there is no CPU fallback.
 from .workloads import WORKLOADS, Workload, generate, sample_rows  # noqa: F401
 
 __all__ = ["WORKLOADS", "Workload", "generate", "sample_rows", "msa_attention",
-           "ring_attention", "band_attention", "topk_attention", "landmarks", "binding"]
+           "ring_attention", "band_attention", "topk_attention", "compressed_attention", "landmarks",
+           "binding"]
 
 
 def __getattr__(name):
     if name in ("msa_attention", "ring_attention", "band_attention", "topk_attention",
-                "landmarks"):
+                "compressed_attention", "landmarks"):
         from . import api
         return getattr(api, name)
     if name == "binding":

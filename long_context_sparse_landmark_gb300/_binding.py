@@ -23,6 +23,7 @@ MAX_MERGE_PARTS = 64
 EXPORTS = ("msa_version", "msa_last_error_string", "msa_landmark_pool", "msa_attn_fwd",
            "msa_attn_fwd_band", "msa_block_select", "msa_attn_fwd_select",
            "msa_attn_fwd_topk_workspace_size", "msa_attn_fwd_topk", "msa_attn_fwd_topk_noalloc",
+           "msa_attn_fwd_global_rows", "msa_attn_fwd_global_rows_workspace_size",
            "msa_attn_fwd_partial",
            "msa_attn_fwd_partial_merge", "msa_lse_merge",
            "msa_attn_uses_tensor_cores", "msa_device_status", "msa_debug_set_wait_limit_ns")
@@ -63,6 +64,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_attn_fwd_topk_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32,
                                               i32, f32, i32, i32, vp]
     lib.msa_attn_fwd_topk_noalloc.restype = i32
+    lib.msa_attn_fwd_global_rows.argtypes = [vp, vp, vp, vp, i64, vp, vp, i64, i32, i32, i32, f32,
+                                             i32, i32, vp, ctypes.c_size_t, vp]
+    lib.msa_attn_fwd_global_rows.restype = i32
+    lib.msa_attn_fwd_global_rows_workspace_size.argtypes = [i64, i64, i32, i32, i32]
+    lib.msa_attn_fwd_global_rows_workspace_size.restype = ctypes.c_size_t
     lib.msa_attn_fwd_partial.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, i32,
                                          i64, f32, i32, vp]
     lib.msa_attn_fwd_partial.restype = i32
@@ -202,6 +208,25 @@ def attn_fwd_topk_noalloc(q, k, v, out, lse, window: int, n_landmarks: int, top_
     _check(_lib.msa_attn_fwd_topk_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), n, Hq,
                                           Hkv, d, int(window), int(n_landmarks), int(top_k),
                                           float(scale), _dt(q), _dt(out), _stream(stream)))
+
+
+def global_rows_workspace_size(n: int, n_global: int, Hq: int, Hkv: int, d: int) -> int:
+    return int(_lib.msa_attn_fwd_global_rows_workspace_size(n, n_global, Hq, Hkv, d))
+
+
+def attn_fwd_global_rows(q, k, v, rows, out, lse, scale: float, workspace: torch.Tensor,
+                         stream=None) -> None:
+    """msa_attn_fwd_global_rows: rows (int64 positions on the device) attend
+    every key j <= their position; their rows of out / lse are overwritten."""
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if rows.dtype != torch.int64:
+        raise TypeError("rows must be int64")
+    _check(_lib.msa_attn_fwd_global_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(rows), rows.numel(),
+                                         _ptr(out), _ptr(lse), n, Hq, Hkv, d, float(scale),
+                                         _dt(q), _dt(out), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream(stream)))
 
 
 def attn_fwd_partial(q, k_chunk, v_chunk, out_part, lse_part, q_start: int, kv_start: int,

@@ -72,6 +72,31 @@ def topk_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: in
     return out, lse
 
 
+def compressed_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int,
+                         block: int, global_rows: torch.Tensor, scale: float | None = None,
+                         out_dtype: torch.dtype | None = None, stream=None):
+    """Compression tokens + global query rows: every row attends its window
+    and the means of the `block`-token sub-blocks wholly before it
+    (msa_landmark_pool + msa_attn_fwd with n / block landmarks); the rows in
+    `global_rows` (int64 positions on the device) then attend every key
+    j <= their position (msa_attn_fwd_global_rows).  Returns (out, lse)."""
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    G = n // block
+    k_lm = torch.empty((G, Hkv, d), dtype=k.dtype, device=k.device)
+    v_lm = torch.empty_like(k_lm)
+    B.landmark_pool(k, v, k_lm, v_lm, stream=stream)
+    out = torch.empty((n, Hq, d), dtype=out_dtype or q.dtype, device=q.device)
+    lse = torch.empty((Hq, n), dtype=torch.float32, device=q.device)
+    B.attn_fwd(q, k, v, k_lm, v_lm, out, lse, window, G, scale, stream=stream)
+    if global_rows.numel() > 0:
+        ws = torch.empty((B.global_rows_workspace_size(n, global_rows.numel(), Hq, Hkv, d),),
+                         dtype=torch.uint8, device=q.device)
+        B.attn_fwd_global_rows(q, k, v, global_rows, out, lse, scale, ws, stream=stream)
+    return out, lse
+
+
 def ring_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_chunks: int,
                    window: int | None = None, scale: float | None = None,
                    out_dtype: torch.dtype | None = None, fused: bool = True, stream=None):

@@ -46,10 +46,10 @@
 #include <math.h>
 #include <string.h>
 
-#include <mutex>
-
 #include "msa_common.cuh"
 #include "tc_ptx.cuh"
+#include "tc_sync.cuh"
+#include "tma_map.h"
 
 namespace msa {
 namespace {
@@ -63,7 +63,6 @@ constexpr int kChunkBytes = 128 * 128;   // 128 rows x 64 bf16 (one 128-B swizzl
 constexpr int kTileBytes = 2 * kChunkBytes;  // 128 rows x 128 bf16
 constexpr int kStages = 2;
 constexpr float kTau = 8.0f;
-constexpr uint64_t kDrainLimitNs = 4000000000ull;
 
 // Shared memory layout (offsets from a 1024-byte aligned base).
 constexpr int kOffQ = 0;
@@ -109,40 +108,6 @@ struct TcParams {
   int* status;
   uint64_t wait_ns;
 };
-
-struct WaitCtl {
-  volatile int* abort;
-  int* status;
-  uint64_t limit;
-};
-
-// Bounded wait on phase `parity` of an mbarrier.  Returns false when the
-// CTA is aborting (flag set by another role, or this wait ran out).
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl& c) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer();
-  while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*c.abort) return false;
-    if (ptx::globaltimer() - t0 > c.limit) {
-      *c.abort = 1;
-      record_status(c.status, MSA_ERR_TIMEOUT);
-      return false;
-    }
-  }
-}
-
-// Wait used while draining: ignores the abort flag, fixed limit.
-__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, int* status) {
-  if (ptx::mbar_try_wait(bar, parity)) return;
-  const uint64_t t0 = ptx::globaltimer();
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if (ptx::globaltimer() - t0 > kDrainLimitNs) {
-      record_status(status, MSA_ERR_TIMEOUT);
-      return;
-    }
-  }
-}
 
 // One work unit: 128 query rows x (up to) 2 heads of one KV group, and the
 // key tiles those rows visit (landmark tiles first, then window tiles).
@@ -628,42 +593,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
-}
-
-// ---------------------------------------------------------------- host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-// [rows, H, 128] bf16 tensor, boxes of 64 (d) x 1 (head) x 128 (rows),
-// 128-byte swizzle: each box lands as 128 rows of 128 bytes, the canonical
-// K-major SW128 layout for Q/K and the MN-major SW128 layout for V.
-bool encode_map(EncodeTiledFn fn, CUtensorMap* m, const void* ptr, int64_t rows, int H) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H),
-                        static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
-                           static_cast<cuuint64_t>(H) * kD * 2};
-  cuuint32_t box[3] = {64, 1, 128};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
 }
 
 }  // namespace

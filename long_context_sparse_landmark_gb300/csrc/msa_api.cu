@@ -416,6 +416,101 @@ msa_status msa_attn_fwd_topk_noalloc(const void* q, const void* k, const void* v
                       reinterpret_cast<cudaStream_t>(stream));
 }
 
+// Key splits and workspace layout of msa_attn_fwd_global_rows: enough
+// (split, M tile, KV head) CTAs to fill the GPU several times over, splits
+// of whole 128-key tiles; partial O, then partial lse, 256-byte aligned.
+struct GrPlan {
+  int64_t Mc, span;
+  int n_splits;
+  size_t lse_off, total;
+};
+
+static GrPlan gr_plan(int64_t n, int64_t n_global, int Hq, int Hkv, int d) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  GrPlan P{};
+  P.Mc = n_global * (Hq / Hkv);
+  const int64_t mtiles = (P.Mc + 127) / 128;
+  const int64_t tiles = (n + 127) / 128;
+  const int64_t per_split = mtiles * Hkv;
+  int64_t S = (1024 + per_split - 1) / per_split;
+  S = S < 1 ? 1 : (S > tiles ? tiles : S);
+  const int64_t span_tiles = (tiles + S - 1) / S;
+  P.span = span_tiles * 128;
+  P.n_splits = static_cast<int>((tiles + span_tiles - 1) / span_tiles);
+  const size_t slabs = static_cast<size_t>(P.n_splits) * Hkv * static_cast<size_t>(P.Mc);
+  P.lse_off = up(slabs * d * sizeof(float));
+  P.total = P.lse_off + up(slabs * sizeof(float));
+  return P;
+}
+
+// Largest n_global * (Hq / Hkv) the launch grids accept.
+constexpr int64_t kMaxGlobalM = int64_t(4) * 65535;
+
+static msa_status check_global_rows(int64_t n, int64_t n_global, int Hq, int Hkv) {
+  if (n < 1 || n > kMaxRows) return fail(MSA_ERR_INVALID_ARG, "n=%lld out of range", (long long)n);
+  if (n_global < 1 || n_global > n)
+    return fail(MSA_ERR_INVALID_ARG, "n_global=%lld must be in [1, n]", (long long)n_global);
+  if (n_global * (Hq / Hkv) > kMaxGlobalM)
+    return fail(MSA_ERR_UNSUPPORTED, "n_global * Hq / Hkv = %lld above %lld",
+                (long long)(n_global * (Hq / Hkv)), (long long)kMaxGlobalM);
+  return MSA_OK;
+}
+
+size_t msa_attn_fwd_global_rows_workspace_size(int64_t n, int64_t n_global, int Hq, int Hkv,
+                                               int d) {
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (d != 64 && d != 128) ||
+      check_global_rows(n, n_global, Hq, Hkv) != MSA_OK)
+    return 0;
+  return gr_plan(n, n_global, Hq, Hkv, d).total;
+}
+
+msa_status msa_attn_fwd_global_rows(const void* q, const void* k, const void* v,
+                                    const int64_t* rows, int64_t n_global, void* out, float* lse,
+                                    int64_t n, int Hq, int Hkv, int d, float scale,
+                                    msa_dtype in_dt, msa_dtype out_dt, void* workspace,
+                                    size_t workspace_bytes, msa_stream_t stream) {
+  msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, 1, scale, in_dt);
+  if (st != MSA_OK) return st;
+  if (!rows || (reinterpret_cast<uintptr_t>(rows) & 7u) != 0)
+    return fail(MSA_ERR_INVALID_ARG, "rows must be non-null and 8-byte aligned");
+  if (!valid_dtype(out_dt)) return fail(MSA_ERR_INVALID_ARG, "bad output dtype %d", (int)out_dt);
+  st = check_global_rows(n, n_global, Hq, Hkv);
+  if (st != MSA_OK) return st;
+  const GrPlan P = gr_plan(n, n_global, Hq, Hkv, d);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(MSA_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
+  if (workspace_bytes < P.total)
+    return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                P.total);
+  msa::GlobalRowsArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.rows = rows;
+  a.n_global = n_global;
+  a.out = out;
+  a.lse = lse;
+  a.o_part = static_cast<float*>(workspace);
+  a.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + P.lse_off);
+  a.n = n;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.span = P.span;
+  a.n_splits = P.n_splits;
+  a.scale = scale;
+  a.in_bf16 = in_dt == MSA_BF16;
+  a.out_bf16 = out_dt == MSA_BF16;
+  st = device_status_ptr(&a.status);
+  if (st != MSA_OK) return st;
+  const uint64_t lim = g_wait_limit_ns.load();
+  a.wait_limit_ns = lim ? lim : kDefaultWaitNs;
+  const char* why = nullptr;
+  cudaError_t e = msa::launch_global_rows(a, reinterpret_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess && why) return fail(MSA_ERR_CUDA, "global rows: %s", why);
+  return launched(e, "global rows");
+}
+
 msa_status msa_attn_fwd_partial(const void* q, const void* k_chunk, const void* v_chunk,
                                  float* out_part, float* lse_part, int64_t n_q, int64_t q_start,
                                  int64_t n_kv, int64_t kv_start, int Hq, int Hkv, int d,

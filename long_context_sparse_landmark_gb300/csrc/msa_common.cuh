@@ -143,6 +143,31 @@ struct SelectArgs {
 };
 cudaError_t launch_block_select(const SelectArgs& a, cudaStream_t s);
 size_t block_select_smem(int d, int G);
+
+// Global query rows: each listed row attends every key j <= its position.
+// Partials per (key split, KV head, M row m = r*g + hh) go to o_part
+// [n_splits, Hkv, n_global*g, d] and lse_part [n_splits, Hkv, n_global*g]
+// (fp32); the merge writes rows of out / lse.
+struct GlobalRowsArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int64_t* rows;
+  int64_t n_global;
+  void* out;
+  float* lse;
+  float* o_part;
+  float* lse_part;
+  int64_t n;
+  int Hq, Hkv, d;
+  int64_t span;  // keys per split (multiple of 128)
+  int n_splits;
+  float scale;
+  int in_bf16, out_bf16;
+  int* status;
+  uint64_t wait_limit_ns;
+};
+cudaError_t launch_global_rows(const GlobalRowsArgs& a, cudaStream_t s, const char** why);
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s, const char** why);
 bool attn_tc_supported(int Hq, int Hkv, int d, int in_bf16);
 

@@ -276,7 +276,7 @@ def attn_select(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int, n_land
 
 
 def attn_compressed(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int, block: int,
-                    global_rows, scale: float, rows=None):
+                    global_rows, scale: float, rows=None, q_positions=None):
     """Compression tokens plus global query rows, after the Block-Sparse
     Flash Attention paragraph of "Training at 1M+ Token Context: Ring
     Attention, YaRN, NTK-Aware Scaling GPU Cost" (local rows see a sliding
@@ -289,22 +289,29 @@ def attn_compressed(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int, bl
     sub-blocks wholly before it -- window + landmark attention with
     G = n / block.  A row in ``global_rows`` attends every key j <= i and
     nothing else.  Returns (O [n_rows, Hq, d], lse [Hq, n_rows]) for
-    ``rows`` (indices of q, default all).
+    ``rows`` (indices of q, default all), or, with ``q_positions``, for the
+    rows q holds, at those positions.
     """
-    n = q.shape[0]
+    n = k.shape[0]
     if block < 1 or n % block != 0:
         raise ValueError("block must divide n")
-    rows = np.arange(n, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
-    is_global = np.isin(rows, np.asarray(global_rows, dtype=np.int64))
+    if q_positions is not None:
+        pos = np.asarray(q_positions, dtype=np.int64)
+        qg = np.ascontiguousarray(q)
+    else:
+        pos = np.arange(n, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+        qg = np.ascontiguousarray(q[pos])
+    is_global = np.isin(pos, np.asarray(global_rows, dtype=np.int64))
     Hq, d = q.shape[1], q.shape[2]
-    out = np.empty((len(rows), Hq, d), dtype=np.float64)
-    lse = np.empty((Hq, len(rows)), dtype=np.float64)
+    out = np.empty((len(pos), Hq, d), dtype=np.float64)
+    lse = np.empty((Hq, len(pos)), dtype=np.float64)
     local = np.nonzero(~is_global)[0]
     glob = np.nonzero(is_global)[0]
     if local.size:
-        out[local], lse[:, local] = attn(q, k, v, window, n // block, scale, rows=rows[local])
+        out[local], lse[:, local] = attn(qg[local], k, v, window, n // block, scale,
+                                         q_positions=pos[local])
     if glob.size:
-        out[glob], lse[:, glob] = attn(q, k, v, n, 0, scale, rows=rows[glob])
+        out[glob], lse[:, glob] = attn(qg[glob], k, v, n, 0, scale, q_positions=pos[glob])
     return out, lse
 
 

@@ -229,3 +229,31 @@ def test_topk_workspace_size_and_validation(lib):
     assert call(wsb=need - 1) == 1
     assert call(tk=9) == 1
     assert call(d=96) == 2
+
+
+def test_global_rows_validation(lib):
+    size = lib.msa_attn_fwd_global_rows_workspace_size
+    need = size(1024, 4, 8, 2, 128)
+    assert need > 0
+    assert size(1024, 0, 8, 2, 128) == 0
+    assert size(1024, 4, 8, 3, 128) == 0
+    f = lib.msa_attn_fwd_global_rows
+
+    def call(**kw):
+        a = dict(q=GOOD, k=GOOD, v=GOOD, rows=GOOD, ng=4, o=GOOD, l=GOOD, n=1024, Hq=8, Hkv=2,
+                 d=128, idt=1, odt=0, ws=GOOD, wsb=need)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["rows"], a["ng"], a["o"], a["l"], a["n"], a["Hq"],
+                 a["Hkv"], a["d"], ctypes.c_float(0.1), a["idt"], a["odt"], a["ws"], a["wsb"],
+                 None)
+
+    assert call(rows=None) == 1
+    assert call(rows=P((1 << 20) + 4)) == 1   # not 8-byte aligned
+    assert call(ng=0) == 1
+    assert call(ng=1025) == 1
+    assert call(ws=None) == 1
+    assert call(ws=P((1 << 20) + 64)) == 1     # not 256-byte aligned
+    assert call(wsb=need - 1) == 1
+    assert call(odt=7) == 1
+    assert call(d=96) == 2
+    assert call(n=1 << 20, ng=40000, Hq=64, Hkv=8, wsb=1 << 62) == 2  # M above the grid limit

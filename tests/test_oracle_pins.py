@@ -653,3 +653,15 @@ def test_compressed_counts_and_page_ratio(oracle_mod):
     want = np.minimum(w, i + 1) + np.clip((i - w + 1) // block, 0, n // block)
     want[glob] = np.asarray(glob) + 1
     np.testing.assert_allclose(np.exp(l[0]), want, rtol=1e-12)
+
+
+def test_compressed_gathered_rows_match_indexed_rows(oracle_mod):
+    rng = np.random.default_rng(5)
+    n = 128
+    q, k, v = rand_qkv(rng, n, 4, 2, 8)
+    rows = np.array([0, 9, 63, 64, 100, 127])
+    glob = [9, 100]
+    a = oracle_mod.attn_compressed(q, k, v, 20, 8, glob, 0.3, rows=rows)
+    b = oracle_mod.attn_compressed(q[rows], k, v, 20, 8, glob, 0.3, q_positions=rows)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
