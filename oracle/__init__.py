@@ -54,6 +54,9 @@ def _configure(lib):
                                      i32, i32, i32, i64, vp, vp, i32, i64,
                                      dbl, vp, vp]
     lib.oracle_attn_rows.restype = i32
+    lib.oracle_attn_bwd.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, i32, i64, i32, dbl,
+                                    vp, vp, vp]
+    lib.oracle_attn_bwd.restype = i32
     lib.oracle_attn_band_rows.argtypes = [vp, vp, i64, vp, vp, i64, i32, i32,
                                           i32, i32, i64, i64, dbl, vp, vp]
     lib.oracle_attn_band_rows.restype = i32
@@ -313,6 +316,28 @@ def attn_compressed(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int, bl
     if glob.size:
         out[glob], lse[:, glob] = attn(qg[glob], k, v, n, 0, scale, q_positions=pos[glob])
     return out, lse
+
+
+def attn_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray, window: int,
+             n_landmarks: int, scale: float):
+    """Gradients (dQ [n,Hq,d], dK, dV [n,Hkv,d], fp64) of sum <dout, O> for
+    window + landmark attention over the whole sequence, landmark gradients
+    scattered back to the tokens they average (1/B each)."""
+    q, k, v, dout = (np.ascontiguousarray(x) for x in (q, k, v, dout))
+    dt = _dtype_code(q)
+    if any(_dtype_code(x) != dt for x in (k, v, dout)):
+        raise TypeError("q, k, v, dout must share one dtype")
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    dq = np.empty((n, Hq, d), dtype=np.float64)
+    dk = np.empty((n, Hkv, d), dtype=np.float64)
+    dv = np.empty((n, Hkv, d), dtype=np.float64)
+    rc = _load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), dt, n, Hq, Hkv, d,
+                                 int(window), int(n_landmarks), float(scale), _ptr(dq),
+                                 _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError("attn_bwd: inconsistent arguments")
+    return dq, dk, dv
 
 
 def lse_merge(o_parts: np.ndarray, lse_parts: np.ndarray):

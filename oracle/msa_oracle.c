@@ -454,3 +454,182 @@ int oracle_attn_select_rows(const void *q, const int64_t *pos, int64_t n_rows,
     }
     return 0;
 }
+
+/*
+ * Backward pass: the gradients of L = sum_{i,h} <dO[i,h], O[i,h]> with
+ * respect to Q, K and V, for training with the sparse pattern (the
+ * Block-Sparse Flash Attention paragraph of "Training at 1M+ Token
+ * Context" trains with it).  With A(i) the attended set of row i (window
+ * keys and visible landmarks), P the softmax over A(i) and a running over
+ * A(i):
+ *   D_i   = <dO_i, O_i> = sum_a P_ia <dO_i, v_a>
+ *   dS_ia = P_ia (<dO_i, v_a> - D_i)
+ *   dQ_i  = scale sum_a dS_ia k_a,  dk_a += scale dS_ia q_i,
+ *   dv_a += P_ia dO_i;
+ * a landmark is the mean of its B tokens, so its gradient reaches each of
+ * them divided by B: dK[j] += dK_lm[l] / B for j in block l (same for V).
+ *   q, dout [n][Hq][d]; k, v [n][Hkv][d] (fp32 or bf16 bits, one dtype)
+ *   dq [n][Hq][d], dk, dv [n][Hkv][d]  fp64, written
+ * Three passes, each free of write conflicts: rows (lse_i, D_i, dQ_i),
+ * window keys (the rows i in [j, j+w-1] of each key j), landmarks (the
+ * rows that see each landmark), then the scatter of landmark gradients.
+ */
+int oracle_attn_bwd(const void *q, const void *k, const void *v,
+                    const void *dout, int dtype, int64_t n, int Hq, int Hkv,
+                    int d, int64_t window, int G, double scale, double *dq,
+                    double *dk, double *dv) {
+    if (n < 1 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 ||
+        window < 1 || G < 0 || (G > 0 && n % G != 0))
+        return -1;
+    const int group = Hq / Hkv;
+    const int64_t B = G > 0 ? n / G : 1;
+    const int64_t row_kv = (int64_t)Hkv * d;
+    double *k_lm = NULL, *v_lm = NULL, *dk_lm = NULL, *dv_lm = NULL;
+    if (G > 0) {
+        k_lm = (double *)malloc(sizeof(double) * (size_t)(G * row_kv));
+        v_lm = (double *)malloc(sizeof(double) * (size_t)(G * row_kv));
+        dk_lm = (double *)calloc((size_t)(G * row_kv), sizeof(double));
+        dv_lm = (double *)calloc((size_t)(G * row_kv), sizeof(double));
+        oracle_landmark_pool(k, dtype, n, Hkv, d, G, k_lm);
+        oracle_landmark_pool(v, dtype, n, Hkv, d, G, v_lm);
+    }
+    double *lse = (double *)malloc(sizeof(double) * (size_t)(n * Hq));
+    double *Dv = (double *)malloc(sizeof(double) * (size_t)(n * Hq));
+
+    /* Pass 1: per (row, head) the softmax, O, D and dQ. */
+#pragma omp parallel
+    {
+        double *sc = (double *)malloc(sizeof(double) * (size_t)(window + G));
+        double *o = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for collapse(2) schedule(dynamic, 4)
+        for (int64_t i = 0; i < n; ++i) {
+            for (int h = 0; h < Hq; ++h) {
+                const int c = h / group;
+                const int64_t j_lo = i - window + 1 > 0 ? i - window + 1 : 0;
+                const int64_t n_win = i - j_lo + 1;
+                const int64_t n_lm = G > 0 ? oracle_visible_landmarks(i, window, B, G) : 0;
+                const int64_t qoff = (i * Hq + h) * (int64_t)d;
+                double m = -INFINITY;
+                for (int64_t a = 0; a < n_win + n_lm; ++a) {
+                    double dot = 0.0;
+                    for (int e = 0; e < d; ++e) {
+                        const double ke = a < n_win
+                            ? oracle_load(k, ((j_lo + a) * Hkv + c) * (int64_t)d + e, dtype)
+                            : k_lm[((a - n_win) * Hkv + c) * (int64_t)d + e];
+                        dot += oracle_load(q, qoff + e, dtype) * ke;
+                    }
+                    sc[a] = scale * dot;
+                    if (sc[a] > m) m = sc[a];
+                }
+                double denom = 0.0;
+                for (int e = 0; e < d; ++e) o[e] = 0.0;
+                for (int64_t a = 0; a < n_win + n_lm; ++a) {
+                    const double p = exp(sc[a] - m);
+                    denom += p;
+                    for (int e = 0; e < d; ++e)
+                        o[e] += p * (a < n_win
+                            ? oracle_load(v, ((j_lo + a) * Hkv + c) * (int64_t)d + e, dtype)
+                            : v_lm[((a - n_win) * Hkv + c) * (int64_t)d + e]);
+                }
+                const double L = m + log(denom);
+                double Di = 0.0;
+                for (int e = 0; e < d; ++e)
+                    Di += oracle_load(dout, qoff + e, dtype) * (o[e] / denom);
+                lse[(int64_t)h * n + i] = L;
+                Dv[(int64_t)h * n + i] = Di;
+                double *g = dq + qoff;
+                for (int e = 0; e < d; ++e) g[e] = 0.0;
+                for (int64_t a = 0; a < n_win + n_lm; ++a) {
+                    const double p = exp(sc[a] - L);
+                    double dp = 0.0;
+                    for (int e = 0; e < d; ++e)
+                        dp += oracle_load(dout, qoff + e, dtype) * (a < n_win
+                            ? oracle_load(v, ((j_lo + a) * Hkv + c) * (int64_t)d + e, dtype)
+                            : v_lm[((a - n_win) * Hkv + c) * (int64_t)d + e]);
+                    const double ds = p * (dp - Di);
+                    for (int e = 0; e < d; ++e)
+                        g[e] += scale * ds * (a < n_win
+                            ? oracle_load(k, ((j_lo + a) * Hkv + c) * (int64_t)d + e, dtype)
+                            : k_lm[((a - n_win) * Hkv + c) * (int64_t)d + e]);
+                }
+            }
+        }
+        free(sc);
+        free(o);
+    }
+
+    /* Pass 2: window keys.  Key j is seen by rows i in [j, j+w-1]. */
+#pragma omp parallel for collapse(2) schedule(dynamic, 16)
+    for (int64_t j = 0; j < n; ++j) {
+        for (int c = 0; c < Hkv; ++c) {
+            double *gk = dk + (j * Hkv + c) * (int64_t)d;
+            double *gv = dv + (j * Hkv + c) * (int64_t)d;
+            for (int e = 0; e < d; ++e) gk[e] = gv[e] = 0.0;
+            const int64_t koff = (j * Hkv + c) * (int64_t)d;
+            const int64_t i_hi = j + window - 1 < n - 1 ? j + window - 1 : n - 1;
+            for (int64_t i = j; i <= i_hi; ++i) {
+                for (int h = c * group; h < (c + 1) * group; ++h) {
+                    const int64_t qoff = (i * Hq + h) * (int64_t)d;
+                    double s = 0.0, dp = 0.0;
+                    for (int e = 0; e < d; ++e) {
+                        s += oracle_load(q, qoff + e, dtype) * oracle_load(k, koff + e, dtype);
+                        dp += oracle_load(dout, qoff + e, dtype) *
+                              oracle_load(v, koff + e, dtype);
+                    }
+                    const double p = exp(scale * s - lse[(int64_t)h * n + i]);
+                    const double ds = p * (dp - Dv[(int64_t)h * n + i]);
+                    for (int e = 0; e < d; ++e) {
+                        gk[e] += scale * ds * oracle_load(q, qoff + e, dtype);
+                        gv[e] += p * oracle_load(dout, qoff + e, dtype);
+                    }
+                }
+            }
+        }
+    }
+
+    /* Pass 3: landmarks.  Landmark l is seen by rows with (l+1)B <= i-w+1. */
+    if (G > 0) {
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+        for (int64_t l = 0; l < G; ++l) {
+            for (int c = 0; c < Hkv; ++c) {
+                const double *kl = k_lm + (l * Hkv + c) * (int64_t)d;
+                const double *vl = v_lm + (l * Hkv + c) * (int64_t)d;
+                double *gk = dk_lm + (l * Hkv + c) * (int64_t)d;
+                double *gv = dv_lm + (l * Hkv + c) * (int64_t)d;
+                for (int64_t i = (l + 1) * B + window - 1; i < n; ++i) {
+                    for (int h = c * group; h < (c + 1) * group; ++h) {
+                        const int64_t qoff = (i * Hq + h) * (int64_t)d;
+                        double s = 0.0, dp = 0.0;
+                        for (int e = 0; e < d; ++e) {
+                            s += oracle_load(q, qoff + e, dtype) * kl[e];
+                            dp += oracle_load(dout, qoff + e, dtype) * vl[e];
+                        }
+                        const double p = exp(scale * s - lse[(int64_t)h * n + i]);
+                        const double ds = p * (dp - Dv[(int64_t)h * n + i]);
+                        for (int e = 0; e < d; ++e) {
+                            gk[e] += scale * ds * oracle_load(q, qoff + e, dtype);
+                            gv[e] += p * oracle_load(dout, qoff + e, dtype);
+                        }
+                    }
+                }
+            }
+        }
+        /* Scatter: each token of block l receives 1/B of its landmark's
+           gradient. */
+#pragma omp parallel for schedule(static)
+        for (int64_t j = 0; j < n; ++j) {
+            const int64_t l = j / B;
+            for (int64_t e = 0; e < row_kv; ++e) {
+                dk[j * row_kv + e] += dk_lm[l * row_kv + e] / (double)B;
+                dv[j * row_kv + e] += dv_lm[l * row_kv + e] / (double)B;
+            }
+        }
+    }
+    free(lse);
+    free(Dv);
+    free(k_lm);
+    free(v_lm);
+    free(dk_lm);
+    free(dv_lm);
+    return 0;
+}

@@ -36,6 +36,21 @@ MUTATIONS = [
      "const double wgt = exp(l - mx);"),
     ("chunk offset ignored", "int64_t koff = ((j_lo + t - kv_start) * Hkv + c) * (int64_t)d;",
      "int64_t koff = ((j_lo + t) * Hkv + c) * (int64_t)d;"),
+    ("backward: D not subtracted", "const double ds = p * (dp - Di);",
+     "const double ds = p * dp;"),
+    ("backward: dK unscaled", "gk[e] += scale * ds * oracle_load(q, qoff + e, dtype);",
+     "gk[e] += ds * oracle_load(q, qoff + e, dtype);"),
+    ("backward: dV weighted by dS", "gv[e] += p * oracle_load(dout, qoff + e, dtype);",
+     "gv[e] += ds * oracle_load(dout, qoff + e, dtype);"),
+    ("backward: last row of a key's window dropped",
+     "const int64_t i_hi = j + window - 1 < n - 1 ? j + window - 1 : n - 1;",
+     "const int64_t i_hi = j + window - 2 < n - 1 ? j + window - 2 : n - 1;"),
+    ("backward: first row seeing a landmark skipped",
+     "for (int64_t i = (l + 1) * B + window - 1; i < n; ++i)",
+     "for (int64_t i = (l + 1) * B + window; i < n; ++i)"),
+    ("backward: landmark gradient not divided by B",
+     "dk[j * row_kv + e] += dk_lm[l * row_kv + e] / (double)B;",
+     "dk[j * row_kv + e] += dk_lm[l * row_kv + e];"),
 ]
 
 
@@ -52,6 +67,9 @@ def battery(mod):
         "uniform weights": lambda: P.test_p5a_zero_keys_give_uniform_weights(mod, 64, 8, 9),
         "block centres": lambda: P.test_p5c_position_keys_give_block_centres(mod, 64, 8),
         "count via K=0": lambda: P.test_p6_oracle_count_via_zero_keys(mod),
+        "bwd autograd 16/4/3": lambda: P.test_bwd_matches_dense_autograd(mod, 16, 4, 3),
+        "bwd autograd 40/5/13": lambda: P.test_bwd_matches_dense_autograd(mod, 40, 5, 13),
+        "bwd identities": lambda: P.test_bwd_sum_identities(mod),
     }
     failed = []
     for name, fn in checks.items():
@@ -87,7 +105,7 @@ def test_unmodified_oracle_passes_the_battery(swap_lib):
 def test_planted_mistake_is_caught(swap_lib, tmp_path, name, old, new):
     text = open(SRC).read()
     assert text.count(old) >= 1, f"pattern for '{name}' not found"
-    # The first occurrence is in the window + landmark path.
+    # The first occurrence is in the path the mistake names.
     lib = _compile(text.replace(old, new, 1), tmp_path, abs(hash(name)) % 10**8)
     oracle._lib = lib
     failed = battery(oracle)

@@ -665,3 +665,113 @@ def test_compressed_gathered_rows_match_indexed_rows(oracle_mod):
     b = oracle_mod.attn_compressed(q[rows], k, v, 20, 8, glob, 0.3, q_positions=rows)
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1], b[1])
+
+
+# ------------------------------------------------------------------- backward
+def dense_torch_grads(q, k, v, dout, window, G, scale):
+    """Autograd (fp64) through a dense masked softmax whose mask is built
+    element by element from the set definitions and whose landmarks are
+    torch block means: an implementation independent of the oracle's
+    hand-derived backward."""
+    tq = torch.tensor(q, dtype=torch.float64, requires_grad=True)
+    tk = torch.tensor(k, dtype=torch.float64, requires_grad=True)
+    tv = torch.tensor(v, dtype=torch.float64, requires_grad=True)
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv
+    B = n // G if G else 1
+    mask = np.zeros((n, n + G), dtype=bool)
+    for i in range(n):
+        for j in range(n):
+            mask[i, j] = i - window < j <= i
+        for l in range(G):
+            mask[i, n + l] = (l + 1) * B - 1 <= i - window
+    mask_t = torch.from_numpy(mask)
+    if G:
+        klm = tk.reshape(G, B, Hkv, d).mean(dim=1)
+        vlm = tv.reshape(G, B, Hkv, d).mean(dim=1)
+        keys, vals = torch.cat([tk, klm]), torch.cat([tv, vlm])
+    else:
+        keys, vals = tk, tv
+    outs = []
+    for h in range(Hq):
+        s = scale * tq[:, h] @ keys[:, h // g].T
+        s = s.masked_fill(~mask_t, float("-inf"))
+        outs.append(torch.softmax(s, dim=1) @ vals[:, h // g])
+    o = torch.stack(outs, dim=1)
+    (o * torch.from_numpy(dout.astype(np.float64))).sum().backward()
+    return tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+@pytest.mark.parametrize("n,G,w", [(16, 4, 3), (16, 0, 5), (24, 6, 1), (32, 8, 9), (12, 12, 2),
+                                   (20, 1, 20), (40, 5, 13)])
+def test_bwd_matches_dense_autograd(oracle_mod, n, G, w):
+    rng = np.random.default_rng(n * 7 + G + w)
+    for (Hq, Hkv), d in itertools.product([(1, 1), (4, 2), (4, 1)], [4, 8]):
+        q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+        do = rng.standard_normal((n, Hq, d)).astype(np.float32)
+        gq, gk, gv = dense_torch_grads(q, k, v, do, w, G, 0.35)
+        dq, dk, dv = oracle_mod.attn_bwd(q, k, v, do, w, G, 0.35)
+        np.testing.assert_allclose(dq, gq, rtol=0, atol=1e-11)
+        np.testing.assert_allclose(dk, gk, rtol=0, atol=1e-11)
+        np.testing.assert_allclose(dv, gv, rtol=0, atol=1e-11)
+
+
+def test_bwd_causal_special_case_is_sdpa_backward(oracle_mod):
+    """w >= n, G = 0: the gradients of torch SDPA (causal, fp64)."""
+    rng = np.random.default_rng(33)
+    n, Hq, Hkv, d = 48, 4, 2, 16
+    q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+    do = rng.standard_normal((n, Hq, d)).astype(np.float32)
+    tq = torch.tensor(q, dtype=torch.float64, requires_grad=True)
+    tk = torch.tensor(k, dtype=torch.float64, requires_grad=True)
+    tv = torch.tensor(v, dtype=torch.float64, requires_grad=True)
+    o = torch.nn.functional.scaled_dot_product_attention(
+        tq.permute(1, 0, 2)[None], tk.repeat_interleave(2, dim=1).permute(1, 0, 2)[None],
+        tv.repeat_interleave(2, dim=1).permute(1, 0, 2)[None], scale=0.25, is_causal=True)
+    (o[0].permute(1, 0, 2) * torch.from_numpy(do.astype(np.float64))).sum().backward()
+    dq, dk, dv = oracle_mod.attn_bwd(q, k, v, do, n + 3, 0, 0.25)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=0, atol=1e-11)
+
+
+def test_bwd_central_differences(oracle_mod):
+    """A few entries of each gradient against central differences of
+    L = sum <dO, O> computed by the forward oracle (fp32 inputs, steps of
+    2^-8 that fp32 represents exactly)."""
+    rng = np.random.default_rng(4)
+    n, Hq, Hkv, d, G, w, sc = 16, 2, 1, 4, 4, 3, 0.5
+    q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+    do = rng.standard_normal((n, Hq, d)).astype(np.float32)
+    dq, dk, dv = oracle_mod.attn_bwd(q, k, v, do, w, G, sc)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle_mod.attn(q_, k_, v_, w, G, sc)
+        return float((o * do.astype(np.float64)).sum())
+
+    h = 2.0 ** -8
+    for which, grad in ((0, dq), (1, dk), (2, dv)):
+        for idx in [(0, 0, 0), (5, 0, 2), (15, Hkv - 1, 3), (9, 0, 1)]:
+            args = [q.copy(), k.copy(), v.copy()]
+            if idx[1] >= args[which].shape[1]:
+                continue
+            args[which][idx] += h
+            up = loss(*args)
+            args[which][idx] -= 2 * h
+            dn = loss(*args)
+            assert abs((up - dn) / (2 * h) - grad[idx]) < 2e-4, (which, idx)
+
+
+def test_bwd_sum_identities(oracle_mod):
+    """Rows of P sum to 1 and rows of dS to 0, so summed over all tokens
+    (landmark gradients included) dV of a KV head equals the sum of its
+    query heads' dO, and dK sums to zero."""
+    rng = np.random.default_rng(8)
+    n, Hq, Hkv, d, G, w = 64, 4, 2, 8, 8, 10
+    q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+    do = rng.standard_normal((n, Hq, d)).astype(np.float32)
+    _, dk, dv = oracle_mod.attn_bwd(q, k, v, do, w, G, 0.3)
+    want = do.astype(np.float64).reshape(n, Hkv, Hq // Hkv, d).sum(axis=(0, 2))
+    np.testing.assert_allclose(dv.sum(axis=0), want, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(dk.sum(axis=0), 0.0, rtol=0, atol=1e-10)
