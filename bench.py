@@ -426,6 +426,48 @@ def run_compressed(wl, steps, warmup, dev, B, torch):
     return res
 
 
+def run_bwd(wl, steps, warmup, dev, B, torch):
+    """Backward of the window + landmark layer (msa_attn_bwd) on device-
+    resident q, k, v, out, lse, dout and preallocated gradients; returns ms
+    per call."""
+    from long_context_sparse_landmark_gb300.workloads import generate
+    q, k, v = generate(wl, device=dev)
+    k_lm = torch.empty((wl.G, wl.Hkv, wl.d), dtype=k.dtype, device=dev)
+    v_lm = torch.empty_like(k_lm)
+    out = torch.empty_like(q)
+    lse = torch.empty((wl.Hq, wl.n), dtype=torch.float32, device=dev)
+    B.landmark_pool(k, v, k_lm, v_lm)
+    B.attn_fwd(q, k, v, k_lm, v_lm, out, lse, wl.window, wl.G, wl.scale)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    dout = torch.randn(q.shape, generator=gen, device=dev).to(torch.bfloat16)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    ws = torch.empty((B.attn_bwd_workspace_size(wl.n, wl.Hq, wl.Hkv, wl.d, wl.G),),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        B.attn_bwd(q, k, v, k_lm, v_lm, out, lse, dout, dq, dk, dv, wl.window, wl.G, wl.scale,
+                   ws, stream=stream)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert B.device_status() == 0
+    del q, k, v, out, lse, dout, dq, dk, dv, ws, k_lm, v_lm
+    torch.cuda.empty_cache()
+    return e0.elapsed_time(e1) / steps
+
+
 def cpu_baseline(wl, rows_target, torch):
     """The fp64 oracle on the host cores, on a bounded row sample of the
     same workload; extrapolated to the full layer by rows."""
@@ -620,6 +662,15 @@ def main():
                                  "global_rows_tflops": round(fg / (rc["global_ms"] * 1e-3)
                                                              / 1e12, 2),
                                  "launches_per_step": 4, "steps": 3}
+        bms = run_bwd(wl, 3, 1, dev, B, torch)
+        # Standard backward count: five GEMMs per attended pair (S, dP, dV,
+        # dK, dQ), 2.5 x the forward's useful FLOPs.
+        fbw = 2.5 * flops
+        also["bwd_" + wl.name] = {"ms_per_step": round(bms, 3),
+                                  "tflops": round(fbw / (bms * 1e-3) / 1e12, 2),
+                                  "pct_bf16_peak": round(100.0 * fbw / (bms * 1e-3) / 1e12
+                                                         / peaks["bf16_tflops"], 2),
+                                  "launches_per_step": 5, "steps": 3}
         wlr = WORKLOADS["ring_128k"]
         rr = run_ring(wlr, 3, 1, dev, B, torch)
         fr = useful_flops(wlr)

@@ -264,6 +264,38 @@ size_t msa_attn_fwd_global_rows_workspace_size(int64_t n, int64_t n_global,
                                                int Hq, int Hkv, int d);
 
 /*
+ * Backward pass of msa_attn_fwd: the gradients of sum <dout, out> with
+ * respect to q, k and v, for training with the sparse pattern (the
+ * Block-Sparse Flash Attention paragraph of "Training at 1M+ Token Context:
+ * Ring Attention, YaRN, NTK-Aware Scaling GPU Cost" trains with it).  With
+ * P recomputed from the forward's lse, D_i = <dout_i, out_i> and
+ * dS = P (dout V^T - D): dq = scale dS K, dk = scale dS^T Q, dv = P^T dout,
+ * summed over the query heads of each KV group; a landmark's gradient
+ * reaches each of the B = n/G tokens it averages divided by B.
+ *   q, k, v, k_lm, v_lm as given to msa_attn_fwd (bf16, d = 128);
+ *   out [n, Hq, d] (`out_dt`) and lse [Hq, n] fp32 as msa_attn_fwd wrote
+ *   them; dout [n, Hq, d] bf16;
+ *   dq [n, Hq, d], dk, dv [n, Hkv, d] in `grad_dt`, written;
+ *   workspace: device memory, 256-byte aligned, at least
+ *   msa_attn_bwd_workspace_size bytes.
+ * Errors: as msa_attn_fwd, plus INVALID_ARG for null/misaligned gradient
+ * pointers or workspace, a too small workspace; UNSUPPORTED unless the
+ * inputs are bf16 with d = 128.
+ */
+msa_status msa_attn_bwd(const void *q, const void *k, const void *v,
+                        const void *k_lm, const void *v_lm, const void *out,
+                        const float *lse, const void *dout, void *dq, void *dk,
+                        void *dv, int64_t n, int Hq, int Hkv, int d,
+                        int64_t window, int n_landmarks, float scale,
+                        msa_dtype in_dt, msa_dtype out_dt, msa_dtype grad_dt,
+                        void *workspace, size_t workspace_bytes,
+                        msa_stream_t stream);
+
+/* Bytes of workspace msa_attn_bwd needs (0 for invalid sizes). */
+size_t msa_attn_bwd_workspace_size(int64_t n, int Hq, int Hkv, int d,
+                                   int n_landmarks);
+
+/*
  * One Ring Attention round's partial: queries at global positions
  * q_start .. q_start+n_q-1 against the contiguous KV chunk at global
  * positions kv_start .. kv_start+n_kv-1, with the causal window mask

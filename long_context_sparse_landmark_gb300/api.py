@@ -134,3 +134,66 @@ def ring_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_chunks: 
     lse = torch.empty((Hq, n), dtype=torch.float32, device=q.device)
     B.lse_merge(o_parts, lse_parts, out, lse, stream=stream)
     return out, lse
+
+
+def msa_attention_backward(q, k, v, out, lse, dout, window: int, n_landmarks: int,
+                           scale: float | None = None, grad_dtype: torch.dtype | None = None,
+                           landmarks_kv=None, stream=None):
+    """Gradients (dq, dk, dv) of sum <dout, out> for the window + landmark
+    forward whose (out, lse) are given; bf16 inputs, d = 128.  The landmark
+    keys/values are pooled again unless ``landmarks_kv`` passes the
+    forward's."""
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if n_landmarks > 0:
+        k_lm, v_lm = landmarks_kv if landmarks_kv is not None else landmarks(
+            k, v, n_landmarks, stream=stream)
+    else:
+        k_lm = v_lm = None
+    gdt = grad_dtype or q.dtype
+    dq = torch.empty((n, Hq, d), dtype=gdt, device=q.device)
+    dk = torch.empty((n, Hkv, d), dtype=gdt, device=q.device)
+    dv = torch.empty_like(dk)
+    ws = torch.empty((B.attn_bwd_workspace_size(n, Hq, Hkv, d, n_landmarks),), dtype=torch.uint8,
+                     device=q.device)
+    B.attn_bwd(q, k, v, k_lm, v_lm, out, lse, dout.contiguous(), dq, dk, dv, window,
+               n_landmarks, scale, ws, stream=stream)
+    return dq, dk, dv
+
+
+class _MSAAttention(torch.autograd.Function):
+    """Window + landmark attention as a differentiable op (libmsa forward
+    and backward kernels)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, window, n_landmarks, scale):
+        n, Hq, d = q.shape
+        out = torch.empty_like(q)
+        lse = torch.empty((Hq, n), dtype=torch.float32, device=q.device)
+        if n_landmarks > 0:
+            k_lm, v_lm = landmarks(k, v, n_landmarks)
+        else:
+            k_lm = v_lm = None
+        B.attn_fwd(q, k, v, k_lm, v_lm, out, lse, window, n_landmarks, scale)
+        ctx.save_for_backward(q, k, v, out, lse)
+        ctx.lm = (k_lm, v_lm)
+        ctx.cfg = (window, n_landmarks, scale)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, lse = ctx.saved_tensors
+        window, n_landmarks, scale = ctx.cfg
+        dq, dk, dv = msa_attention_backward(
+            q, k, v, out, lse, dout.to(q.dtype), window, n_landmarks, scale,
+            landmarks_kv=ctx.lm if n_landmarks > 0 else None)
+        return dq, dk, dv, None, None, None
+
+
+def msa_attention_trainable(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int,
+                            n_landmarks: int, scale: float | None = None) -> torch.Tensor:
+    """Differentiable window + landmark attention (bf16, d = 128): returns
+    out [n, Hq, d]; ``out.backward(g)`` runs msa_attn_bwd."""
+    scale = 1.0 / math.sqrt(q.shape[2]) if scale is None else scale
+    return _MSAAttention.apply(q, k, v, window, n_landmarks, scale)

@@ -511,6 +511,113 @@ msa_status msa_attn_fwd_global_rows(const void* q, const void* k, const void* v,
   return launched(e, "global rows");
 }
 
+// Workspace layout of msa_attn_bwd: D [Hq, n], landmark gradient partials
+// [chunks][2][G][Hkv][d] and their sums [2][G][Hkv][d] (fp32, 256-byte
+// aligned).  Landmark work is split over query chunks so that
+// (landmark tile, KV head, chunk) CTAs fill the GPU.
+struct BwdPlan {
+  int lm_chunks, chunk_tiles;
+  size_t part_off, grad_off, total;
+};
+
+static BwdPlan bwd_plan(int64_t n, int Hq, int Hkv, int d, int G) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  BwdPlan P{};
+  const int64_t n_qt = (n + 127) / 128;
+  if (G > 0) {
+    const int64_t per = ((G + 127) / 128) * static_cast<int64_t>(Hkv);
+    int64_t ch = (512 + per - 1) / per;
+    ch = ch < 1 ? 1 : (ch > n_qt ? n_qt : ch);
+    P.chunk_tiles = static_cast<int>((n_qt + ch - 1) / ch);
+    P.lm_chunks = static_cast<int>((n_qt + P.chunk_tiles - 1) / P.chunk_tiles);
+  }
+  const size_t lm = 2 * static_cast<size_t>(G) * Hkv * d * sizeof(float);
+  P.part_off = up(static_cast<size_t>(Hq) * n * sizeof(float));
+  P.grad_off = P.part_off + up(static_cast<size_t>(P.lm_chunks) * lm);
+  P.total = P.grad_off + up(lm);
+  return P;
+}
+
+static msa_status check_bwd_sizes(int64_t n, int Hq, int Hkv, int d, int G) {
+  if (n < 1 || n > kMaxRows) return fail(MSA_ERR_INVALID_ARG, "n=%lld out of range", (long long)n);
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+    return fail(MSA_ERR_INVALID_ARG, "Hq=%d Hkv=%d", Hq, Hkv);
+  if (G < 0 || G > n || (G > 0 && n % G != 0))
+    return fail(MSA_ERR_INVALID_ARG, "G=%d must satisfy 0 <= G <= n and n %% G == 0 (n=%lld)", G,
+                (long long)n);
+  if (d != 128) return fail(MSA_ERR_UNSUPPORTED, "backward: head dim d=%d (supported: 128)", d);
+  return MSA_OK;
+}
+
+size_t msa_attn_bwd_workspace_size(int64_t n, int Hq, int Hkv, int d, int n_landmarks) {
+  if (check_bwd_sizes(n, Hq, Hkv, d, n_landmarks) != MSA_OK) return 0;
+  return bwd_plan(n, Hq, Hkv, d, n_landmarks).total;
+}
+
+msa_status msa_attn_bwd(const void* q, const void* k, const void* v, const void* k_lm,
+                        const void* v_lm, const void* out, const float* lse, const void* dout,
+                        void* dq, void* dk, void* dv, int64_t n, int Hq, int Hkv, int d,
+                        int64_t window, int n_landmarks, float scale, msa_dtype in_dt,
+                        msa_dtype out_dt, msa_dtype grad_dt, void* workspace,
+                        size_t workspace_bytes, msa_stream_t stream) {
+  msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, window, scale, in_dt);
+  if (st != MSA_OK) return st;
+  if (!dout || !dq || !dk || !dv) return fail(MSA_ERR_INVALID_ARG, "null gradient pointer");
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(MSA_ERR_INVALID_ARG, "gradient pointer not 16-byte aligned");
+  if (!valid_dtype(out_dt) || !valid_dtype(grad_dt))
+    return fail(MSA_ERR_INVALID_ARG, "bad output/gradient dtype %d/%d", (int)out_dt, (int)grad_dt);
+  st = check_bwd_sizes(n, Hq, Hkv, d, n_landmarks);
+  if (st != MSA_OK) return st;
+  if (in_dt != MSA_BF16)
+    return fail(MSA_ERR_UNSUPPORTED, "backward: inputs must be bf16 (tensor-core kernels)");
+  if (n_landmarks > 0) {
+    if (!k_lm || !v_lm) return fail(MSA_ERR_INVALID_ARG, "null landmark pointer with G > 0");
+    if (!aligned16(k_lm) || !aligned16(v_lm))
+      return fail(MSA_ERR_INVALID_ARG, "landmark pointer not 16-byte aligned");
+  }
+  const BwdPlan P = bwd_plan(n, Hq, Hkv, d, n_landmarks);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(MSA_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
+  if (workspace_bytes < P.total)
+    return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                P.total);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  msa::BwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.k_lm = n_landmarks > 0 ? k_lm : nullptr;
+  a.v_lm = n_landmarks > 0 ? v_lm : nullptr;
+  a.out = out;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.D = reinterpret_cast<float*>(ws);
+  a.lm_part = reinterpret_cast<float*>(ws + P.part_off);
+  a.lm_grad = reinterpret_cast<float*>(ws + P.grad_off);
+  a.n = n;
+  a.window = window;
+  a.G = n_landmarks;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.scale = scale;
+  a.out_bf16 = out_dt == MSA_BF16;
+  a.grad_bf16 = grad_dt == MSA_BF16;
+  a.lm_chunks = P.lm_chunks;
+  a.chunk_tiles = P.chunk_tiles;
+  st = device_status_ptr(&a.status);
+  if (st != MSA_OK) return st;
+  const uint64_t lim = g_wait_limit_ns.load();
+  a.wait_limit_ns = lim ? lim : kDefaultWaitNs;
+  const char* why = nullptr;
+  cudaError_t e = msa::launch_attn_bwd(a, reinterpret_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess && why) return fail(MSA_ERR_CUDA, "backward: %s", why);
+  return launched(e, "backward");
+}
+
 msa_status msa_attn_fwd_partial(const void* q, const void* k_chunk, const void* v_chunk,
                                  float* out_part, float* lse_part, int64_t n_q, int64_t q_start,
                                  int64_t n_kv, int64_t kv_start, int Hq, int Hkv, int d,

@@ -168,6 +168,35 @@ struct GlobalRowsArgs {
   uint64_t wait_limit_ns;
 };
 cudaError_t launch_global_rows(const GlobalRowsArgs& a, cudaStream_t s, const char** why);
+
+// Backward pass (bf16, d = 128).  Workspace pieces: D [Hq, n], landmark
+// gradient partials [lm_chunks][2][G][Hkv][d] and their sums [2][G][Hkv][d]
+// (fp32).
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* k_lm;
+  const void* v_lm;
+  const void* out;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* D;
+  float* lm_part;
+  float* lm_grad;
+  int64_t n, window;
+  int G, Hq, Hkv;
+  float scale;
+  int out_bf16, grad_bf16;
+  int lm_chunks, chunk_tiles;
+  int* status;
+  uint64_t wait_limit_ns;
+};
+bool attn_bwd_supported(int d, int in_bf16);
+cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why);
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s, const char** why);
 bool attn_tc_supported(int Hq, int Hkv, int d, int in_bf16);
 

@@ -57,6 +57,9 @@ def _configure(lib):
     lib.oracle_attn_bwd.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, i32, i64, i32, dbl,
                                     vp, vp, vp]
     lib.oracle_attn_bwd.restype = i32
+    lib.oracle_attn_bwd_dq_rows.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, i32, i64, i32,
+                                            dbl, vp, i64, vp]
+    lib.oracle_attn_bwd_dq_rows.restype = i32
     lib.oracle_attn_band_rows.argtypes = [vp, vp, i64, vp, vp, i64, i32, i32,
                                           i32, i32, i64, i64, dbl, vp, vp]
     lib.oracle_attn_band_rows.restype = i32
@@ -338,6 +341,22 @@ def attn_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray, wind
     if rc != 0:
         raise ValueError("attn_bwd: inconsistent arguments")
     return dq, dk, dv
+
+
+def attn_bwd_dq_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray, window: int,
+                     n_landmarks: int, scale: float, rows):
+    """dQ [n_rows, Hq, d] (fp64) of the listed rows only (q, dout whole)."""
+    q, k, v, dout = (np.ascontiguousarray(x) for x in (q, k, v, dout))
+    dt = _dtype_code(q)
+    n, Hq, d = q.shape
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    dq = np.empty((len(rows), Hq, d), dtype=np.float64)
+    rc = _load().oracle_attn_bwd_dq_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), dt, n, Hq,
+                                         k.shape[1], d, int(window), int(n_landmarks),
+                                         float(scale), _ptr(rows), len(rows), _ptr(dq))
+    if rc != 0:
+        raise ValueError("attn_bwd_dq_rows: inconsistent arguments")
+    return dq
 
 
 def lse_merge(o_parts: np.ndarray, lse_parts: np.ndarray):

@@ -456,6 +456,67 @@ int oracle_attn_select_rows(const void *q, const int64_t *pos, int64_t n_rows,
 }
 
 /*
+ * One (row i, head h) of the backward's first pass: the softmax over A(i),
+ * O_i, lse_i, D_i = <dO_i, O_i> and dQ_i = scale sum_a P_ia (<dO_i, v_a> -
+ * D_i) k_a.  sc and o are scratch of window + G and d doubles.
+ */
+static void oracle_bwd_row(const void *q, const void *k, const void *v,
+                           const void *dout, int dtype, int64_t n, int64_t i,
+                           int h, int Hq, int Hkv, int d, int64_t window, int G,
+                           int64_t B, const double *k_lm, const double *v_lm,
+                           double scale, double *sc, double *o, double *lse_out,
+                           double *D_out, double *g) {
+    (void)n;
+    const int c = h / (Hq / Hkv);
+    const int64_t j_lo = i - window + 1 > 0 ? i - window + 1 : 0;
+    const int64_t n_win = i - j_lo + 1;
+    const int64_t n_lm = G > 0 ? oracle_visible_landmarks(i, window, B, G) : 0;
+    const int64_t qoff = (i * Hq + h) * (int64_t)d;
+    double m = -INFINITY;
+    for (int64_t a = 0; a < n_win + n_lm; ++a) {
+        double dot = 0.0;
+        for (int e = 0; e < d; ++e) {
+            const double ke = a < n_win
+                ? oracle_load(k, ((j_lo + a) * Hkv + c) * (int64_t)d + e, dtype)
+                : k_lm[((a - n_win) * Hkv + c) * (int64_t)d + e];
+            dot += oracle_load(q, qoff + e, dtype) * ke;
+        }
+        sc[a] = scale * dot;
+        if (sc[a] > m) m = sc[a];
+    }
+    double denom = 0.0;
+    for (int e = 0; e < d; ++e) o[e] = 0.0;
+    for (int64_t a = 0; a < n_win + n_lm; ++a) {
+        const double p = exp(sc[a] - m);
+        denom += p;
+        for (int e = 0; e < d; ++e)
+            o[e] += p * (a < n_win
+                ? oracle_load(v, ((j_lo + a) * Hkv + c) * (int64_t)d + e, dtype)
+                : v_lm[((a - n_win) * Hkv + c) * (int64_t)d + e]);
+    }
+    const double L = m + log(denom);
+    double Di = 0.0;
+    for (int e = 0; e < d; ++e)
+        Di += oracle_load(dout, qoff + e, dtype) * (o[e] / denom);
+    *lse_out = L;
+    *D_out = Di;
+    for (int e = 0; e < d; ++e) g[e] = 0.0;
+    for (int64_t a = 0; a < n_win + n_lm; ++a) {
+        const double p = exp(sc[a] - L);
+        double dp = 0.0;
+        for (int e = 0; e < d; ++e)
+            dp += oracle_load(dout, qoff + e, dtype) * (a < n_win
+                ? oracle_load(v, ((j_lo + a) * Hkv + c) * (int64_t)d + e, dtype)
+                : v_lm[((a - n_win) * Hkv + c) * (int64_t)d + e]);
+        const double ds = p * (dp - Di);
+        for (int e = 0; e < d; ++e)
+            g[e] += scale * ds * (a < n_win
+                ? oracle_load(k, ((j_lo + a) * Hkv + c) * (int64_t)d + e, dtype)
+                : k_lm[((a - n_win) * Hkv + c) * (int64_t)d + e]);
+    }
+}
+
+/*
  * Backward pass: the gradients of L = sum_{i,h} <dO[i,h], O[i,h]> with
  * respect to Q, K and V, for training with the sparse pattern (the
  * Block-Sparse Flash Attention paragraph of "Training at 1M+ Token
@@ -502,58 +563,11 @@ int oracle_attn_bwd(const void *q, const void *k, const void *v,
         double *sc = (double *)malloc(sizeof(double) * (size_t)(window + G));
         double *o = (double *)malloc(sizeof(double) * (size_t)d);
 #pragma omp for collapse(2) schedule(dynamic, 4)
-        for (int64_t i = 0; i < n; ++i) {
-            for (int h = 0; h < Hq; ++h) {
-                const int c = h / group;
-                const int64_t j_lo = i - window + 1 > 0 ? i - window + 1 : 0;
-                const int64_t n_win = i - j_lo + 1;
-                const int64_t n_lm = G > 0 ? oracle_visible_landmarks(i, window, B, G) : 0;
-                const int64_t qoff = (i * Hq + h) * (int64_t)d;
-                double m = -INFINITY;
-                for (int64_t a = 0; a < n_win + n_lm; ++a) {
-                    double dot = 0.0;
-                    for (int e = 0; e < d; ++e) {
-                        const double ke = a < n_win
-                            ? oracle_load(k, ((j_lo + a) * Hkv + c) * (int64_t)d + e, dtype)
-                            : k_lm[((a - n_win) * Hkv + c) * (int64_t)d + e];
-                        dot += oracle_load(q, qoff + e, dtype) * ke;
-                    }
-                    sc[a] = scale * dot;
-                    if (sc[a] > m) m = sc[a];
-                }
-                double denom = 0.0;
-                for (int e = 0; e < d; ++e) o[e] = 0.0;
-                for (int64_t a = 0; a < n_win + n_lm; ++a) {
-                    const double p = exp(sc[a] - m);
-                    denom += p;
-                    for (int e = 0; e < d; ++e)
-                        o[e] += p * (a < n_win
-                            ? oracle_load(v, ((j_lo + a) * Hkv + c) * (int64_t)d + e, dtype)
-                            : v_lm[((a - n_win) * Hkv + c) * (int64_t)d + e]);
-                }
-                const double L = m + log(denom);
-                double Di = 0.0;
-                for (int e = 0; e < d; ++e)
-                    Di += oracle_load(dout, qoff + e, dtype) * (o[e] / denom);
-                lse[(int64_t)h * n + i] = L;
-                Dv[(int64_t)h * n + i] = Di;
-                double *g = dq + qoff;
-                for (int e = 0; e < d; ++e) g[e] = 0.0;
-                for (int64_t a = 0; a < n_win + n_lm; ++a) {
-                    const double p = exp(sc[a] - L);
-                    double dp = 0.0;
-                    for (int e = 0; e < d; ++e)
-                        dp += oracle_load(dout, qoff + e, dtype) * (a < n_win
-                            ? oracle_load(v, ((j_lo + a) * Hkv + c) * (int64_t)d + e, dtype)
-                            : v_lm[((a - n_win) * Hkv + c) * (int64_t)d + e]);
-                    const double ds = p * (dp - Di);
-                    for (int e = 0; e < d; ++e)
-                        g[e] += scale * ds * (a < n_win
-                            ? oracle_load(k, ((j_lo + a) * Hkv + c) * (int64_t)d + e, dtype)
-                            : k_lm[((a - n_win) * Hkv + c) * (int64_t)d + e]);
-                }
-            }
-        }
+        for (int64_t i = 0; i < n; ++i)
+            for (int h = 0; h < Hq; ++h)
+                oracle_bwd_row(q, k, v, dout, dtype, n, i, h, Hq, Hkv, d, window, G, B, k_lm,
+                               v_lm, scale, sc, o, &lse[(int64_t)h * n + i],
+                               &Dv[(int64_t)h * n + i], dq + (i * Hq + h) * (int64_t)d);
         free(sc);
         free(o);
     }
@@ -631,5 +645,44 @@ int oracle_attn_bwd(const void *q, const void *k, const void *v,
     free(v_lm);
     free(dk_lm);
     free(dv_lm);
+    return 0;
+}
+
+/*
+ * dQ of selected rows only (the first pass of oracle_attn_bwd on them):
+ *   rows [n_rows] positions, dq [n_rows][Hq][d] fp64, written.
+ */
+int oracle_attn_bwd_dq_rows(const void *q, const void *k, const void *v,
+                            const void *dout, int dtype, int64_t n, int Hq,
+                            int Hkv, int d, int64_t window, int G, double scale,
+                            const int64_t *rows, int64_t n_rows, double *dq) {
+    if (n < 1 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 ||
+        window < 1 || G < 0 || (G > 0 && n % G != 0))
+        return -1;
+    const int64_t B = G > 0 ? n / G : 1;
+    const int64_t row_kv = (int64_t)Hkv * d;
+    double *k_lm = NULL, *v_lm = NULL;
+    if (G > 0) {
+        k_lm = (double *)malloc(sizeof(double) * (size_t)(G * row_kv));
+        v_lm = (double *)malloc(sizeof(double) * (size_t)(G * row_kv));
+        oracle_landmark_pool(k, dtype, n, Hkv, d, G, k_lm);
+        oracle_landmark_pool(v, dtype, n, Hkv, d, G, v_lm);
+    }
+#pragma omp parallel
+    {
+        double *sc = (double *)malloc(sizeof(double) * (size_t)(window + G));
+        double *o = (double *)malloc(sizeof(double) * (size_t)d);
+        double L, Dd;
+#pragma omp for collapse(2) schedule(dynamic, 4)
+        for (int64_t r = 0; r < n_rows; ++r)
+            for (int h = 0; h < Hq; ++h)
+                oracle_bwd_row(q, k, v, dout, dtype, n, rows[r], h, Hq, Hkv, d, window, G, B,
+                               k_lm, v_lm, scale, sc, o, &L, &Dd,
+                               dq + (r * Hq + h) * (int64_t)d);
+        free(sc);
+        free(o);
+    }
+    free(k_lm);
+    free(v_lm);
     return 0;
 }

@@ -257,3 +257,33 @@ def test_global_rows_validation(lib):
     assert call(odt=7) == 1
     assert call(d=96) == 2
     assert call(n=1 << 20, ng=40000, Hq=64, Hkv=8, wsb=1 << 62) == 2  # M above the grid limit
+
+
+def test_backward_validation(lib):
+    size = lib.msa_attn_bwd_workspace_size
+    need = size(1024, 8, 2, 128, 8)
+    assert need > 0
+    assert size(1024, 8, 2, 64, 8) == 0     # d = 64 has no backward
+    assert size(1024, 8, 3, 128, 8) == 0
+    assert size(1000, 8, 2, 128, 7) == 0
+    f = lib.msa_attn_bwd
+
+    def call(**kw):
+        a = dict(q=GOOD, k=GOOD, v=GOOD, klm=GOOD, vlm=GOOD, o=GOOD, l=GOOD, do=GOOD, dq=GOOD,
+                 dk=GOOD, dv=GOOD, n=1024, Hq=8, Hkv=2, d=128, w=64, G=8, idt=1, odt=0, gdt=0,
+                 ws=GOOD, wsb=need)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["klm"], a["vlm"], a["o"], a["l"], a["do"], a["dq"],
+                 a["dk"], a["dv"], a["n"], a["Hq"], a["Hkv"], a["d"], a["w"], a["G"],
+                 ctypes.c_float(0.1), a["idt"], a["odt"], a["gdt"], a["ws"], a["wsb"], None)
+
+    assert call(do=None) == 1
+    assert call(dk=BAD_ALIGN) == 1
+    assert call(klm=None) == 1
+    assert call(G=7) == 1
+    assert call(gdt=4) == 1
+    assert call(ws=P((1 << 20) + 16)) == 1
+    assert call(wsb=need - 1) == 1
+    assert call(idt=0) == 2      # fp32 inputs: no backward kernels
+    assert call(d=64) == 2
+    assert call(w=0) == 1

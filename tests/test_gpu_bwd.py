@@ -1,0 +1,165 @@
+"""GPU parity of the backward pass (msa_attn_bwd, bf16 inputs, d = 128)
+through the C ABI, against the fp64 oracle's gradients on the same inputs.
+
+Bar.  Gradients have no scale of their own and their rows differ widely in
+size (a query with few keys, or a key that few rows see but weight
+heavily, has gradients ten times the tensor's RMS), so each d-vector (one
+token, one head) is held to its own size: max |g - r| <= 2^-5 (max |r| of
+that vector + RMS of the tensor), and over the tensor mean |g - r| <=
+2^-8 RMS.  The kernels round P and dS to bf16 (relative 2^-9) before the
+gradient MMAs, accumulate in fp32, and take D from the forward's O, whose
+weights were bf16 too; summed over terms of either sign this stays a small
+multiple of 2^-9 of the vector's size.  A bf16 gradient output adds one
+rounding (half a bf16 spacing per element)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_sparse_landmark_gb300.workloads import (Workload, generate, sample_rows,
+                                                          to_numpy_bits)
+from tests.gpu_helpers import bf16_ulp, binding
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+MAX_REL, MEAN_REL = 2.0 ** -5, 2.0 ** -8
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _oracle_threads():
+    import os
+    oracle.set_threads(os.cpu_count() or 1)
+
+
+def rel_compare(gpu, ref, what, max_rel=MAX_REL, mean_rel=MEAN_REL, extra=None):
+    g = np.asarray(gpu, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    assert g.shape == r.shape, what
+    assert np.isfinite(g).all(), f"{what}: non-finite"
+    rms = float(np.sqrt(np.mean(r * r))) or 1.0
+    err = np.abs(g - r)
+    if extra is not None:
+        err = np.maximum(err - extra, 0.0)
+    vec_scale = np.abs(r).max(axis=-1, keepdims=True) + rms
+    mx = float((err / vec_scale).max())
+    mean = float(err.mean()) / rms
+    assert mx <= max_rel and mean <= mean_rel, (
+        f"{what}: max-abs/(vector max + rms) {mx:.3e} (bar {max_rel:.1e}), mean-abs/rms "
+        f"{mean:.3e} (bar {mean_rel:.1e}), rms {rms:.3e}")
+    return mx, mean
+
+
+def make_dout(wl, seed):
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(seed)
+    return torch.randn((wl.n, wl.Hq, wl.d), generator=gen, device=DEV).to(torch.bfloat16)
+
+
+def gpu_backward(q, k, v, do, wl, grad_dtype=torch.float32):
+    import long_context_sparse_landmark_gb300.api as api
+    out, lse = api.msa_attention(q, k, v, wl.window, wl.G, wl.scale, out_dtype=torch.float32)
+    grads = api.msa_attention_backward(q, k, v, out, lse, do, wl.window, wl.G, wl.scale,
+                                       grad_dtype=grad_dtype)
+    torch.cuda.synchronize()
+    assert binding().device_status() == 0
+    return grads
+
+
+BWD_CASES = [
+    # n, Hq, Hkv, w, G
+    (256, 2, 1, 64, 4),
+    (1000, 4, 2, 100, 8),
+    (1024, 8, 2, 1, 8),
+    (2048, 8, 1, 300, 16),
+    (640, 4, 4, 640, 0),
+    (384, 6, 2, 50, 384),
+    (4096, 16, 2, 1024, 32),
+    (129, 2, 2, 7, 3),
+]
+
+
+@pytest.mark.parametrize("n,Hq,Hkv,w,G", BWD_CASES)
+def test_backward_parity(n, Hq, Hkv, w, G):
+    wl = Workload("bwd", n, Hq, Hkv, 128, w, G, "bf16", seed=n + 3 * G + w)
+    q, k, v = generate(wl, device=DEV)
+    do = make_dout(wl, seed=n + 1)
+    dq, dk, dv = gpu_backward(q, k, v, do, wl)
+    rq, rk, rv = oracle.attn_bwd(to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v),
+                                 to_numpy_bits(do), w, G, wl.scale)
+    rel_compare(dq.cpu().numpy(), rq, f"dQ {wl}")
+    rel_compare(dk.cpu().numpy(), rk, f"dK {wl}")
+    rel_compare(dv.cpu().numpy(), rv, f"dV {wl}")
+
+
+def test_backward_bf16_gradients():
+    wl = Workload("bwd16", 2048, 8, 2, 128, 256, 16, "bf16", seed=77)
+    q, k, v = generate(wl, device=DEV)
+    do = make_dout(wl, seed=78)
+    grads = gpu_backward(q, k, v, do, wl, grad_dtype=torch.bfloat16)
+    refs = oracle.attn_bwd(to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v),
+                           to_numpy_bits(do), wl.window, wl.G, wl.scale)
+    for name, g, r in zip("QKV", grads, refs):
+        rel_compare(g.float().cpu().numpy(), r, f"bf16 d{name}", extra=0.5 * bf16_ulp(r))
+
+
+def test_autograd_wrapper_matches_backward_call():
+    import long_context_sparse_landmark_gb300.api as api
+    wl = Workload("ag", 1024, 4, 2, 128, 200, 8, "bf16", seed=5)
+    q, k, v = generate(wl, device=DEV)
+    do = make_dout(wl, seed=6)
+    qa, ka, va = (t.clone().requires_grad_(True) for t in (q, k, v))
+    out = api.msa_attention_trainable(qa, ka, va, wl.window, wl.G)
+    out.backward(do)
+    torch.cuda.synchronize()
+    refs = oracle.attn_bwd(to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v),
+                           to_numpy_bits(do), wl.window, wl.G, wl.scale)
+    for name, t, r in zip("QKV", (qa, ka, va), refs):
+        rel_compare(t.grad.float().cpu().numpy(), r, f"autograd d{name}",
+                    extra=0.5 * bf16_ulp(r))
+
+
+def test_backward_16k_full():
+    """A 16K-token layer slice (8 query heads on one KV head, w = 2048, 64
+    landmarks of 256 tokens): every gradient element against the oracle."""
+    wl = Workload("bwd16k", 16384, 8, 1, 128, 2048, 64, "bf16", seed=161)
+    q, k, v = generate(wl, device=DEV)
+    do = make_dout(wl, seed=162)
+    dq, dk, dv = gpu_backward(q, k, v, do, wl)
+    rq, rk, rv = oracle.attn_bwd(to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v),
+                                 to_numpy_bits(do), wl.window, wl.G, wl.scale)
+    rel_compare(dq.cpu().numpy(), rq, "16K dQ")
+    rel_compare(dk.cpu().numpy(), rk, "16K dK")
+    rel_compare(dv.cpu().numpy(), rv, "16K dV")
+
+
+def test_backward_128k_layer_properties_and_sampled_dq():
+    """The 128K 70B-style layer: dQ on sampled rows against the oracle, and
+    at full size the identities sum_j dV[j, c] = sum over the group's heads
+    of sum_i dO and sum_j dK[j, c] = 0 (rows of P sum to 1, rows of dS to
+    0, landmark gradients included)."""
+    from long_context_sparse_landmark_gb300.workloads import WORKLOADS
+    wl = WORKLOADS["128k_70b_layer"]
+    q, k, v = generate(wl, device=DEV)
+    do = make_dout(wl, seed=1281)
+    dq, dk, dv = gpu_backward(q, k, v, do, wl)
+    g = wl.Hq // wl.Hkv
+    do4 = do.double().reshape(wl.n, wl.Hkv, g, wl.d)
+    want_v = do4.sum(dim=(0, 2))
+    # Each row's bf16-rounded weights sum to 1 within 2^-9 of their sum,
+    # so the dV total is off by at most 2^-9 sum |dO| (fp32 sums: 2^-8).
+    bound_v = 2.0 ** -8 * do4.abs().sum(dim=(0, 2))
+    err_v = (dv.double().sum(dim=0) - want_v).abs()
+    err_k = dk.double().sum(dim=0).abs()
+    scale_k = dk.double().abs().sum(dim=0)
+    print(f"sum dV: max err/bound {float((err_v / bound_v).max()):.3e}; "
+          f"sum dK: max |sum|/sum|.| {float((err_k / scale_k).max()):.3e}")
+    assert torch.all(err_v <= bound_v), "sum of dV"
+    assert torch.all(err_k <= 2.0 ** -6 * scale_k), "sum of dK"
+    rows = sample_rows(wl, count=256).numpy()
+    idx = torch.as_tensor(rows, device=DEV)
+    gq = dq.index_select(0, idx).cpu().numpy()
+    del dq, dk, dv
+    rq = oracle.attn_bwd_dq_rows(to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v),
+                                 to_numpy_bits(do), wl.window, wl.G, wl.scale, rows)
+    rel_compare(gq, rq, "128K dQ (sampled)")

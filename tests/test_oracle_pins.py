@@ -775,3 +775,14 @@ def test_bwd_sum_identities(oracle_mod):
     want = do.astype(np.float64).reshape(n, Hkv, Hq // Hkv, d).sum(axis=(0, 2))
     np.testing.assert_allclose(dv.sum(axis=0), want, rtol=0, atol=1e-10)
     np.testing.assert_allclose(dk.sum(axis=0), 0.0, rtol=0, atol=1e-10)
+
+
+def test_bwd_dq_rows_match_full_backward(oracle_mod):
+    rng = np.random.default_rng(12)
+    n, Hq, Hkv, d, G, w = 64, 4, 2, 8, 8, 10
+    q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+    do = rng.standard_normal((n, Hq, d)).astype(np.float32)
+    dq, _, _ = oracle_mod.attn_bwd(q, k, v, do, w, G, 0.3)
+    rows = [0, 9, 10, 33, 63]
+    np.testing.assert_array_equal(oracle_mod.attn_bwd_dq_rows(q, k, v, do, w, G, 0.3, rows),
+                                  dq[rows])
