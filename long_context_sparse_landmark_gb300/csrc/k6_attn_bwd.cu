@@ -12,7 +12,8 @@
 // tokens divided by B.
 //
 // Launches, in stream order:
-//   1. bwd_preprocess_kernel: D [Hq, n] (fp32);
+//   1. bwd_preprocess_kernel: per-row lse (log2 units) and D (fp32), padded
+//      to whole 128-row tiles so that the dK/dV kernel copies them per tile;
 //   2. bwd_dkdv_tc_kernel, landmark mode: per (landmark tile, KV head,
 //      query chunk) partial dK_lm / dV_lm over the rows that see the
 //      landmarks (up to all n rows per landmark, hence the chunks);
@@ -24,11 +25,14 @@
 //   5. bwd_dq_tc_kernel: per (128-row query tile, head) over the landmark
 //      and window key tiles, as the forward.
 // Each tensor-core kernel: warps 0-3 elementwise (one TMEM lane = one row
-// each), warp 4 TMA producer, warp 5 TMEM allocation and MMA issue.  Per
-// iteration the two score-like MMAs run, the elementwise warps turn them
-// into bf16 P / dS in the same TMEM columns, and the two gradient MMAs
-// accumulate in TMEM; tcgen05 MMAs from one thread execute in issue order,
-// so the next iteration's score MMAs may be issued right after.  Every wait
+// each), warp 4 TMA producer, warp 5 TMEM allocation and MMA issue.  Every
+// 128-column tile is handled as two 64-column halves with their own TMEM
+// columns: the score-like MMAs of a half land, the elementwise warps turn
+// them into bf16 P / dS in the same columns, the half's gradient MMAs
+// accumulate in TMEM and the next tile's scores of that half follow at
+// once -- so the tensor pipe works on one half while the warps process the
+// other (tcgen05 MMAs from one thread execute in issue order, which makes
+// overwriting a half's columns after its gradient MMAs safe).  Every wait
 // is bounded; a wait that runs out aborts the CTA cleanly.
 #include <cuda.h>
 #include <math.h>
@@ -44,6 +48,7 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kT = 128;                      // rows per tile (queries or keys)
+constexpr int kHalf = 64;                    // columns per pipelined half
 constexpr int kChunkBytes = 128 * 128;       // 128 rows x 64 bf16
 constexpr int kTileBytes = 2 * kChunkBytes;  // 128 rows x 128 bf16
 constexpr uint32_t kTileLo = kTileBytes >> 4;
@@ -61,28 +66,30 @@ enum {
   BAR_FIX = 0,      // fixed tiles landed
   BAR_FULL0 = 1,    // ring stage b landed (1, 2)
   BAR_EMPTY0 = 3,   // ring stage b consumed (3, 4)
-  BAR_SF = 5,       // score-like MMAs done
-  BAR_EF = 6,       // elementwise results written (4 warp arrivals)
-  BAR_ACC = 7,      // gradient accumulators final
-  BAR_CLEAN = 8,
-  kNumBars = 9
+  BAR_SF0 = 5,      // score-like MMAs of half h done (5, 6)
+  BAR_EF0 = 7,      // elementwise results of half h written, 4 warp arrivals (7, 8)
+  BAR_ACC = 9,      // gradient accumulators final
+  BAR_CLEAN = 10,
+  kNumBars = 11
 };
-constexpr int kOffStats = kOffBar + 8 * kNumBars;  // dK/dV: [4 warps][lse, D][128] fp32
-constexpr int kOffTmemSlot = kOffStats + 4 * 2 * kT * 4;
+// dK/dV: [2 stages][L2, D][128] fp32, bulk-copied: 128-byte aligned.
+constexpr int kOffStats = (kOffBar + 8 * kNumBars + 127) / 128 * 128;
+constexpr int kStatBytes = 2 * kT * 4;  // one stage's L2 and D rows
+constexpr int kOffTmemSlot = kOffStats + 2 * kStatBytes;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemUsed = kOffAbort + 8;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 
 struct BwdParams {
   CUtensorMap tm_q, tm_do, tm_k, tm_v, tm_klm, tm_vlm;
-  const float* lse;   // [Hq, n]
-  const float* D;     // [Hq, n]
+  const float* L2;    // [Hq, n_pad] lse * log2(e), +inf past n
+  const float* D;     // [Hq, n_pad] <dO, O>, 0 past n
   void* dq;           // [n, Hq, d]
   void* dk;           // [n, Hkv, d]
   void* dv;
   float* lm_part;     // [chunks][2][G][Hkv][d]
   const float* lm_grad;  // [2][G][Hkv][d]
-  int64_t n, window, block;
+  int64_t n, n_pad, window, block;
   int Hq, Hkv, G, group, grad_bf16;
   int lm_mode, lm_chunks, chunk_tiles;
   float scale, scale_log2;
@@ -119,8 +126,10 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t sb, int wa
       ptx::mbar_init(sb + kOffBar + 8 * (BAR_FULL0 + b), 1);
       ptx::mbar_init(sb + kOffBar + 8 * (BAR_EMPTY0 + b), 1);
     }
-    ptx::mbar_init(sb + kOffBar + 8 * BAR_SF, 1);
-    ptx::mbar_init(sb + kOffBar + 8 * BAR_EF, 4);
+    for (int h = 0; h < 2; ++h) {
+      ptx::mbar_init(sb + kOffBar + 8 * (BAR_SF0 + h), 1);
+      ptx::mbar_init(sb + kOffBar + 8 * (BAR_EF0 + h), 4);
+    }
     ptx::mbar_init(sb + kOffBar + 8 * BAR_ACC, 1);
     ptx::mbar_init(sb + kOffBar + 8 * BAR_CLEAN, 1);
     *reinterpret_cast<volatile int*>(smem + kOffAbort) = 0;
@@ -147,10 +156,11 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem, int warp) {
 }
 
 // Producer: the fixed pair once, then `iters` ring pairs; `coord(it, &map_a,
-// &map_b, &y_a, &y_b, &row)` names the tensors and coordinates of pair it.
-template <typename Coord>
+// &map_b, &y_a, &y_b, &row)` names the tensors and coordinates of pair it,
+// `stats(it, &l2, &d)` the statistics rows to copy with it (or none).
+template <typename Coord, typename Stats>
 __device__ __forceinline__ void produce(uint32_t sb, const CUtensorMap* fa, const CUtensorMap* fb,
-                                        int fy, int frow, int iters, Coord coord,
+                                        int fy, int frow, int iters, Coord coord, Stats stats,
                                         const WaitCtl& ctl, int* status) {
   auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8 * i; };
   ptx::mbar_arrive_expect_tx(bar(BAR_FIX), 2 * kTileBytes);
@@ -165,7 +175,14 @@ __device__ __forceinline__ void produce(uint32_t sb, const CUtensorMap* fa, cons
     const CUtensorMap *ma, *mb;
     int ya, yb, row;
     coord(it, &ma, &mb, &ya, &yb, &row);
-    ptx::mbar_arrive_expect_tx(bar(BAR_FULL0 + b), 2 * kTileBytes);
+    const float *sl = nullptr, *sd = nullptr;
+    stats(it, &sl, &sd);
+    ptx::mbar_arrive_expect_tx(bar(BAR_FULL0 + b), 2 * kTileBytes + (sl ? kStatBytes : 0));
+    if (sl) {  // this stage's per-query lse and D rows (512 bytes each)
+      const uint32_t dst = sb + kOffStats + b * kStatBytes;
+      ptx::bulk_load(dst, sl, kT * 4, bar(BAR_FULL0 + b));
+      ptx::bulk_load(dst + kT * 4, sd, kT * 4, bar(BAR_FULL0 + b));
+    }
     for (int ch = 0; ch < 2; ++ch) {
       ptx::tma_load_3d(sb + kOffRingA + b * kTileBytes + ch * kChunkBytes, ma,
                        bar(BAR_FULL0 + b), ch * 64, ya, row);
@@ -182,31 +199,78 @@ __device__ __forceinline__ void produce(uint32_t sb, const CUtensorMap* fa, cons
   }
 }
 
-// 8 SS MMAs (K = 128 in steps of 16): D[128 x 128] = A[128 x 128] B[128 x 128]^T,
-// both operands K-major tiles in shared memory.
-__device__ __forceinline__ void mma_scores(uint32_t d, uint32_t a_lo, uint32_t b_lo) {
-  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kT, kT, false);
+// Score-like MMAs of one half: D[128 x 64] = A[128 x 128] B_half[64 x 128]^T,
+// 8 SS MMAs (K = 128 in steps of 16); B_half = rows 64h..64h+63 of a K-major
+// tile (8 KB into each 64-column chunk).
+__device__ __forceinline__ void mma_scores_half(uint32_t d, uint32_t a_lo, uint32_t b_lo,
+                                                int half) {
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kT, kHalf, false);
+  const uint32_t b_half = b_lo + ((half * kHalf * 128) >> 4);
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk) {
     const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-    ptx::mma_ss_lohi(d, a_lo + off, ptx::kDescHiSw128, b_lo + off, ptx::kDescHiSw128, kIdesc,
+    ptx::mma_ss_lohi(d, a_lo + off, ptx::kDescHiSw128, b_half + off, ptx::kDescHiSw128, kIdesc,
                      kk > 0 ? 1u : 0u);
   }
 }
 
-// 8 TS MMAs: D[128 x 128] += A (bf16 in TMEM columns a..a+63) B, B an
-// MN-major tile in shared memory (128 rows of K, 128 of N).
-__device__ __forceinline__ void mma_grad(uint32_t d, uint32_t a_tmem, uint32_t b_lo, bool first) {
+// Gradient MMAs of one half: D[128 x 128] += A (bf16 in TMEM columns
+// a..a+31: 128 x 64) B_half, B_half = rows 64h..64h+63 of an MN-major tile
+// (K = 64 in steps of 16).
+__device__ __forceinline__ void mma_grad_half(uint32_t d, uint32_t a_tmem, uint32_t b_mn,
+                                              int half, bool first) {
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kT, kD, true);
 #pragma unroll
-  for (int kk = 0; kk < kT / 16; ++kk)
-    ptx::mma_ts_lohi(d, a_tmem + kk * 8, b_lo + ((kk * 2048) >> 4), ptx::kDescHiSw128, kIdesc,
-                     (!first || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < kHalf / 16; ++kk)
+    ptx::mma_ts_lohi(d, a_tmem + kk * 8, b_mn + ((half * kHalf * 128 + kk * 2048) >> 4),
+                     ptx::kDescHiSw128, kIdesc, (!first || kk > 0) ? 1u : 0u);
+}
+
+// TMEM columns of the two halves: scores of half h at [64h.. 64h+64) of
+// the first 128, the second score-like product at +128; bf16 results
+// overwrite the first 32 columns of each (already read).
+__device__ __forceinline__ uint32_t col_s(int half) { return half * kHalf; }
+__device__ __forceinline__ uint32_t col_p(int half) { return 128 + half * kHalf; }
+
+// The MMA issuer's pipeline over `iters` ring stages.  Per stage: scores of
+// half 0 and half 1; then, as the elementwise warps finish each half, that
+// half's gradient MMAs followed by the next stage's scores of the same half,
+// so the tensor pipe works on one half while the warps process the other.
+template <typename Scores, typename Grads>
+__device__ __forceinline__ bool mma_pipeline(uint32_t sb, int iters, Scores scores, Grads grads,
+                                             const WaitCtl& ctl) {
+  auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8 * i; };
+  bool ok = wait_bar(bar(BAR_FIX), 0, ctl) && wait_bar(bar(BAR_FULL0), 0, ctl);
+  if (!ok) return false;
+  ptx::tc_fence_after();
+  for (int h = 0; h < 2; ++h) {
+    scores(0, h);
+    ptx::mma_commit(bar(BAR_SF0 + h));
+  }
+  for (int it = 0; it < iters; ++it) {
+    const int b = it & 1;
+    const bool next = it + 1 < iters;
+    for (int h = 0; h < 2; ++h) {
+      if (!(ok = wait_bar(bar(BAR_EF0 + h), it & 1, ctl))) break;
+      ptx::tc_fence_after();
+      grads(it, h);
+      if (h == 1) ptx::mma_commit(bar(BAR_EMPTY0 + b));  // stage b fully consumed
+      if (next) {
+        if (h == 0 && !(ok = wait_bar(bar(BAR_FULL0 + (b ^ 1)), ((it + 1) >> 1) & 1, ctl)))
+          break;
+        scores(it + 1, h);
+        ptx::mma_commit(bar(BAR_SF0 + h));
+      }
+    }
+    if (!ok) break;
+  }
+  if (ok) ptx::mma_commit(bar(BAR_ACC));
+  return ok;
 }
 
 // --------------------------------------------------------------------- dQ
-// CTA = (query tile, query head).  TMEM: S 0..127 (dS over 0..63), dP
-// 128..255, dQ 256..383.
+// CTA = (query tile, query head).  TMEM: S of key halves 0/1 at 0..63 /
+// 64..127 (dS over their first 32 columns), dP at 128..255, dQ 256..383.
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -238,7 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
         *ya = *yb = c;
         *row = lm ? t * kT : (kt_lo + t - n_lm_tiles) * kT;
       };
-      produce(sb, &p.tm_q, &p.tm_do, h, static_cast<int>(qr0), T, coord, ctl, p.status);
+      auto no_stats = [](int, const float**, const float**) {};
+      produce(sb, &p.tm_q, &p.tm_do, h, static_cast<int>(qr0), T, coord, no_stats, ctl,
+              p.status);
     }
   } else if (warp == 5) {
     if (lane == 0) {
@@ -247,20 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
       const uint32_t k_lo = ptx::desc_lo(sb + kOffRingA, 16);
       const uint32_t v_lo = ptx::desc_lo(sb + kOffRingB, 16);
       const uint32_t k_mn = ptx::desc_lo(sb + kOffRingA, kChunkBytes);
-      bool ok = wait_bar(bar(BAR_FIX), 0, ctl);
-      for (int t = 0; ok && t < T; ++t) {
-        const int b = t & 1;
-        if (!(ok = wait_bar(bar(BAR_FULL0 + b), (t >> 1) & 1, ctl))) break;
-        ptx::tc_fence_after();
-        mma_scores(tmem, q_lo, k_lo + b * kTileLo);          // S  = Q K^T
-        mma_scores(tmem + 128, do_lo, v_lo + b * kTileLo);   // dP = dO V^T
-        ptx::mma_commit(bar(BAR_SF));
-        if (!(ok = wait_bar(bar(BAR_EF), t & 1, ctl))) break;
-        ptx::tc_fence_after();
-        mma_grad(tmem + 256, tmem, k_mn + b * kTileLo, t == 0);  // dQ += dS K
-        ptx::mma_commit(bar(BAR_EMPTY0 + b));
-      }
-      if (ok) ptx::mma_commit(bar(BAR_ACC));
+      auto scores = [&](int t, int half) {
+        const uint32_t st = (t & 1) * kTileLo;
+        mma_scores_half(tmem + col_s(half), q_lo, k_lo + st, half);   // S  = Q K^T
+        mma_scores_half(tmem + col_p(half), do_lo, v_lo + st, half);  // dP = dO V^T
+      };
+      auto grads = [&](int t, int half) {  // dQ += dS K
+        mma_grad_half(tmem + 256, tmem + col_s(half), k_mn + (t & 1) * kTileLo, half,
+                      t == 0 && half == 0);
+      };
+      mma_pipeline(sb, T, scores, grads, ctl);
       ptx::mma_commit(bar(BAR_CLEAN));
       drain_bar(bar(BAR_CLEAN), 0, p.status);
     }
@@ -268,16 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const int64_t i = qr0 + threadIdx.x;
     const bool row_ok = i < p.n;
-    const float L2 = row_ok ? p.lse[static_cast<int64_t>(h) * p.n + i] * kLog2e : INFINITY;
-    const float Di = row_ok ? p.D[static_cast<int64_t>(h) * p.n + i] : 0.f;
+    const float L2 = p.L2[static_cast<int64_t>(h) * p.n_pad + i];
+    const float Di = p.D[static_cast<int64_t>(h) * p.n_pad + i];
     const int64_t my_lm = visible_landmarks(i, p.window, p.block, p.G);
     const int64_t my_lo = max64(i - p.window + 1, 0);
     const float sl2 = p.scale_log2;
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF), t & 1, ctl));
-      if (!ok) break;
-      ptx::tc_fence_after();
+    for (int t = 0; ok && t < T; ++t) {
       int64_t lo, hi;  // valid columns [lo, hi) of this key tile for row i
       if (t < n_lm_tiles) {
         lo = 0;
@@ -288,33 +347,38 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
         hi = i - kb + 1;
       }
       if (!row_ok) hi = lo;
-      const int lo_c = static_cast<int>(max64(0, min64(kT, lo)));
-      const int hi_c = static_cast<int>(max64(0, min64(kT, hi)));
+      for (int half = 0; half < 2; ++half) {
+        ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF0 + half), t & 1, ctl));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const int lo_c = static_cast<int>(max64(0, min64(kHalf, lo - half * kHalf)));
+        const int hi_c = static_cast<int>(max64(0, min64(kHalf, hi - half * kHalf)));
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        float s[32], dp[32];
-        ptx::tmem_ld32(tl + cc * 32, s);
-        ptx::tmem_ld32(tl + 128 + cc * 32, dp);
-        ptx::tmem_wait_ld();
-        uint32_t pk[16];
+        for (int cc = 0; cc < 2; ++cc) {
+          float s[32], dp[32];
+          ptx::tmem_ld32(tl + col_s(half) + cc * 32, s);
+          ptx::tmem_ld32(tl + col_p(half) + cc * 32, dp);
+          ptx::tmem_wait_ld();
+          uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float ds[2];
+          for (int e = 0; e < 16; ++e) {
+            float ds[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = cc * 32 + 2 * e + u;
-            const bool valid = col >= lo_c && col < hi_c;
-            const float pr = valid ? ptx::ex2(fmaf(s[2 * e + u], sl2, -L2)) : 0.f;
-            ds[u] = pr * (dp[2 * e + u] - Di);
+            for (int u = 0; u < 2; ++u) {
+              const int col = cc * 32 + 2 * e + u;
+              const bool valid = col >= lo_c && col < hi_c;
+              const float pr = valid ? ptx::ex2(fmaf(s[2 * e + u], sl2, -L2)) : 0.f;
+              ds[u] = pr * (dp[2 * e + u] - Di);
+            }
+            pk[e] = ptx::pack_bf16x2(ds[0], ds[1]);
           }
-          pk[e] = ptx::pack_bf16x2(ds[0], ds[1]);
+          ptx::tmem_st16(tl + col_s(half) + cc * 16, pk);  // dS over columns already read
         }
-        ptx::tmem_st16(tl + cc * 16, pk);  // dS over columns already read
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(BAR_EF0 + half));
       }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(BAR_EF));
     }
     if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_ACC), 0, ctl));
     if (ok) {
@@ -333,9 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
 }
 
 // ------------------------------------------------------------------ dK, dV
-// CTA = (key tile or landmark tile, KV head[, query chunk]).  TMEM: S^T
-// 0..127 (P^T over 0..63), dP^T 128..255 (dS^T over 128..191), dV
-// 256..383, dK 384..511.
+// CTA = (key tile or landmark tile, KV head[, query chunk]).  TMEM: S^T of
+// query halves 0/1 at 0..63 / 64..127 (P^T over their first 32 columns),
+// dP^T at 128..255 (dS^T likewise), dV 256..383, dK 384..511.
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -383,8 +447,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         *ya = *yb = c * p.group + it % p.group;
         *row = static_cast<int>((qt_lo + it / p.group) * kT);
       };
+      auto stats = [&](int it, const float** sl, const float** sd) {
+        const int64_t off = static_cast<int64_t>(c * p.group + it % p.group) * p.n_pad +
+                            (qt_lo + it / p.group) * kT;
+        *sl = p.L2 + off;
+        *sd = p.D + off;
+      };
       produce(sb, p.lm_mode ? &p.tm_klm : &p.tm_k, p.lm_mode ? &p.tm_vlm : &p.tm_v, c,
-              static_cast<int>(kb), iters, coord, ctl, p.status);
+              static_cast<int>(kb), iters, coord, stats, ctl, p.status);
     }
   } else if (warp == 5) {
     if (lane == 0) {
@@ -394,47 +464,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t do_lo = ptx::desc_lo(sb + kOffRingB, 16);
       const uint32_t q_mn = ptx::desc_lo(sb + kOffRingA, kChunkBytes);
       const uint32_t do_mn = ptx::desc_lo(sb + kOffRingB, kChunkBytes);
-      bool ok = wait_bar(bar(BAR_FIX), 0, ctl);
-      for (int it = 0; ok && it < iters; ++it) {
-        const int b = it & 1;
-        if (!(ok = wait_bar(bar(BAR_FULL0 + b), (it >> 1) & 1, ctl))) break;
-        ptx::tc_fence_after();
-        mma_scores(tmem, k_lo, q_lo + b * kTileLo);          // S^T  = K Q^T
-        mma_scores(tmem + 128, v_lo, do_lo + b * kTileLo);   // dP^T = V dO^T
-        ptx::mma_commit(bar(BAR_SF));
-        if (!(ok = wait_bar(bar(BAR_EF), it & 1, ctl))) break;
-        ptx::tc_fence_after();
-        mma_grad(tmem + 256, tmem, do_mn + b * kTileLo, it == 0);       // dV += P^T dO
-        mma_grad(tmem + 384, tmem + 128, q_mn + b * kTileLo, it == 0);  // dK += dS^T Q
-        ptx::mma_commit(bar(BAR_EMPTY0 + b));
-      }
-      if (ok) ptx::mma_commit(bar(BAR_ACC));
+      auto scores = [&](int it, int half) {
+        const uint32_t st = (it & 1) * kTileLo;
+        mma_scores_half(tmem + col_s(half), k_lo, q_lo + st, half);   // S^T  = K Q^T
+        mma_scores_half(tmem + col_p(half), v_lo, do_lo + st, half);  // dP^T = V dO^T
+      };
+      auto grads = [&](int it, int half) {
+        const uint32_t st = (it & 1) * kTileLo;
+        const bool first = it == 0 && half == 0;
+        mma_grad_half(tmem + 256, tmem + col_s(half), do_mn + st, half, first);  // dV += P^T dO
+        mma_grad_half(tmem + 384, tmem + col_p(half), q_mn + st, half, first);   // dK += dS^T Q
+      };
+      mma_pipeline(sb, iters, scores, grads, ctl);
       ptx::mma_commit(bar(BAR_CLEAN));
       drain_bar(bar(BAR_CLEAN), 0, p.status);
     }
   } else if (warp < 4) {
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const int64_t j = kb + threadIdx.x;  // key (window mode) or landmark (landmark mode)
-    float* stats = reinterpret_cast<float*>(smem + kOffStats);
     const float sl2 = p.scale_log2;
     bool ok = true;
-    for (int it = 0; it < iters; ++it) {
+    for (int it = 0; ok && it < iters; ++it) {
       const int64_t qr0 = (qt_lo + it / p.group) * kT;
-      const int h = c * p.group + it % p.group;
-      // This iteration's per-query lse (log2 units) and D in a warp-private
-      // copy (no cross-warp barrier, so an aborting warp cannot stall the
-      // others).
-      float* sL = stats + warp * 2 * kT;
-      float* sD = sL + kT;
-      __syncwarp();  // every lane is done with the previous iteration's copy
-#pragma unroll
-      for (int u = 0; u < kT / 32; ++u) {
-        const int col = lane + 32 * u;
-        const int64_t i = qr0 + col;
-        sL[col] = i < p.n ? p.lse[static_cast<int64_t>(h) * p.n + i] * kLog2e : INFINITY;
-        sD[col] = i < p.n ? p.D[static_cast<int64_t>(h) * p.n + i] : 0.f;
-      }
-      __syncwarp();
+      // This iteration's per-query lse (log2 units) and D came with its
+      // Q / dO stage; the stage has landed once its scores exist, and it is
+      // not refilled before this iteration's results are in.
+      const float* sL = reinterpret_cast<const float*>(smem + kOffStats + (it & 1) * kStatBytes);
+      const float* sD = sL + kT;
       // Rows i of this query tile that see key/landmark j: [lo, hi) columns.
       int64_t lo, hi;
       if (p.lm_mode) {
@@ -444,38 +500,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         lo = j - qr0;
         hi = j + p.window - qr0;
       }
-      const int lo_c = static_cast<int>(max64(0, min64(kT, lo)));
-      const int hi_c = static_cast<int>(max64(0, min64(kT, hi)));
-      ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF), it & 1, ctl));
-      if (!ok) break;
-      ptx::tc_fence_after();
+      for (int half = 0; half < 2; ++half) {
+        ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF0 + half), it & 1, ctl));
+        if (ok && half == 0)  // completed already; makes the copied rows visible here
+          ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_FULL0 + (it & 1)), (it >> 1) & 1, ctl));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const int lo_c = static_cast<int>(max64(0, min64(kHalf, lo - half * kHalf)));
+        const int hi_c = static_cast<int>(max64(0, min64(kHalf, hi - half * kHalf)));
+        const float* hL = sL + half * kHalf;
+        const float* hD = sD + half * kHalf;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        float s[32], dp[32];
-        ptx::tmem_ld32(tl + cc * 32, s);
-        ptx::tmem_ld32(tl + 128 + cc * 32, dp);
-        ptx::tmem_wait_ld();
-        uint32_t pp[16], dd[16];
+        for (int cc = 0; cc < 2; ++cc) {
+          float s[32], dp[32];
+          ptx::tmem_ld32(tl + col_s(half) + cc * 32, s);
+          ptx::tmem_ld32(tl + col_p(half) + cc * 32, dp);
+          ptx::tmem_wait_ld();
+          uint32_t pp[16], dd[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float pr[2], ds[2];
+          for (int e = 0; e < 16; ++e) {
+            float pr[2], ds[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = cc * 32 + 2 * e + u;
-            const bool valid = col >= lo_c && col < hi_c;
-            pr[u] = valid ? ptx::ex2(fmaf(s[2 * e + u], sl2, -sL[col])) : 0.f;
-            ds[u] = pr[u] * (dp[2 * e + u] - sD[col]);
+            for (int u = 0; u < 2; ++u) {
+              const int col = cc * 32 + 2 * e + u;
+              const bool valid = col >= lo_c && col < hi_c;
+              pr[u] = valid ? ptx::ex2(fmaf(s[2 * e + u], sl2, -hL[col])) : 0.f;
+              ds[u] = pr[u] * (dp[2 * e + u] - hD[col]);
+            }
+            pp[e] = ptx::pack_bf16x2(pr[0], pr[1]);
+            dd[e] = ptx::pack_bf16x2(ds[0], ds[1]);
           }
-          pp[e] = ptx::pack_bf16x2(pr[0], pr[1]);
-          dd[e] = ptx::pack_bf16x2(ds[0], ds[1]);
+          ptx::tmem_st16(tl + col_s(half) + cc * 16, pp);  // P^T over columns already read
+          ptx::tmem_st16(tl + col_p(half) + cc * 16, dd);  // dS^T likewise
         }
-        ptx::tmem_st16(tl + cc * 16, pp);        // P^T over columns already read
-        ptx::tmem_st16(tl + 128 + cc * 16, dd);  // dS^T likewise
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(BAR_EF0 + half));
       }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(BAR_EF));
     }
     if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_ACC), 0, ctl));
     if (ok) {
@@ -527,27 +589,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ----------------------------------------------------------- small kernels
-// D[h, i] = <dO[i, h], O[i, h]>: one warp per (row, head), 4 elements a lane.
+// Row statistics: L2[h, i] = lse[h, i] * log2(e) and D[h, i] = <dO[i, h],
+// O[i, h]> for i < n, +inf and 0 for the padding up to n_pad; one warp per
+// (row, head), 4 elements a lane.
 template <bool kOutBf16>
 __global__ void __launch_bounds__(256)
-    bwd_preprocess_kernel(const void* out, const uint16_t* dout, float* D, int64_t n, int Hq) {
+    bwd_preprocess_kernel(const void* out, const uint16_t* dout, const float* lse, float* L2,
+                          float* D, int64_t n, int64_t n_pad, int Hq) {
   const int64_t pair = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (pair >= n * Hq) return;
-  const int64_t base = pair * kD + lane * 4;
+  if (pair >= n_pad * Hq) return;
+  const int64_t i = pair / Hq;
+  const int h = static_cast<int>(pair % Hq);
   float acc = 0.f;
+  if (i < n) {
+    const int64_t base = pair * kD + lane * 4;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float o = kOutBf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(out)[base + e])
-                             : static_cast<const float*>(out)[base + e];
-    acc = fmaf(o, bf16_bits_to_float(dout[base + e]), acc);
+    for (int e = 0; e < 4; ++e) {
+      const float o = kOutBf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(out)[base + e])
+                               : static_cast<const float*>(out)[base + e];
+      acc = fmaf(o, bf16_bits_to_float(dout[base + e]), acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) {
-    const int64_t i = pair / Hq;
-    const int h = static_cast<int>(pair % Hq);
-    D[static_cast<int64_t>(h) * n + i] = acc;
+    const int64_t at = static_cast<int64_t>(h) * n_pad + i;
+    D[at] = acc;
+    L2[at] = i < n ? lse[static_cast<int64_t>(h) * n + i] * kLog2e : INFINITY;
   }
 }
 
@@ -595,14 +664,15 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why) 
     p.tm_klm = p.tm_k;
     p.tm_vlm = p.tm_v;
   }
-  p.lse = a.lse;
-  p.D = a.D;
+  p.L2 = a.stats;
+  p.D = a.stats + static_cast<int64_t>(a.Hq) * a.n_pad;
   p.dq = a.dq;
   p.dk = a.dk;
   p.dv = a.dv;
   p.lm_part = a.lm_part;
   p.lm_grad = a.lm_grad;
   p.n = a.n;
+  p.n_pad = a.n_pad;
   p.window = a.window;
   p.block = a.G > 0 ? a.n / a.G : 1;
   p.Hq = a.Hq;
@@ -617,14 +687,16 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why) 
   p.status = a.status;
   p.wait_ns = a.wait_limit_ns;
 
-  const int64_t pairs = a.n * a.Hq;
+  const int64_t pairs = a.n_pad * a.Hq;
   const unsigned pre_blocks = static_cast<unsigned>((pairs + 7) / 8);
+  float* L2w = a.stats;
+  float* Dw = a.stats + static_cast<int64_t>(a.Hq) * a.n_pad;
   if (a.out_bf16)
     bwd_preprocess_kernel<true><<<pre_blocks, 256, 0, s>>>(
-        a.out, static_cast<const uint16_t*>(a.dout), a.D, a.n, a.Hq);
+        a.out, static_cast<const uint16_t*>(a.dout), a.lse, L2w, Dw, a.n, a.n_pad, a.Hq);
   else
     bwd_preprocess_kernel<false><<<pre_blocks, 256, 0, s>>>(
-        a.out, static_cast<const uint16_t*>(a.dout), a.D, a.n, a.Hq);
+        a.out, static_cast<const uint16_t*>(a.dout), a.lse, L2w, Dw, a.n, a.n_pad, a.Hq);
   cudaError_t e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
   for (auto* k : {bwd_dkdv_tc_kernel, bwd_dq_tc_kernel}) {

@@ -511,7 +511,8 @@ msa_status msa_attn_fwd_global_rows(const void* q, const void* k, const void* v,
   return launched(e, "global rows");
 }
 
-// Workspace layout of msa_attn_bwd: D [Hq, n], landmark gradient partials
+// Workspace layout of msa_attn_bwd: row statistics [2][Hq][n rounded up to
+// 128] (lse in log2 units, D), landmark gradient partials
 // [chunks][2][G][Hkv][d] and their sums [2][G][Hkv][d] (fp32, 256-byte
 // aligned).  Landmark work is split over query chunks so that
 // (landmark tile, KV head, chunk) CTAs fill the GPU.
@@ -532,7 +533,7 @@ static BwdPlan bwd_plan(int64_t n, int Hq, int Hkv, int d, int G) {
     P.lm_chunks = static_cast<int>((n_qt + P.chunk_tiles - 1) / P.chunk_tiles);
   }
   const size_t lm = 2 * static_cast<size_t>(G) * Hkv * d * sizeof(float);
-  P.part_off = up(static_cast<size_t>(Hq) * n * sizeof(float));
+  P.part_off = up(2 * static_cast<size_t>(Hq) * n_qt * 128 * sizeof(float));
   P.grad_off = P.part_off + up(static_cast<size_t>(P.lm_chunks) * lm);
   P.total = P.grad_off + up(lm);
   return P;
@@ -595,10 +596,11 @@ msa_status msa_attn_bwd(const void* q, const void* k, const void* v, const void*
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.D = reinterpret_cast<float*>(ws);
+  a.stats = reinterpret_cast<float*>(ws);
   a.lm_part = reinterpret_cast<float*>(ws + P.part_off);
   a.lm_grad = reinterpret_cast<float*>(ws + P.grad_off);
   a.n = n;
+  a.n_pad = (n + 127) / 128 * 128;
   a.window = window;
   a.G = n_landmarks;
   a.Hq = Hq;

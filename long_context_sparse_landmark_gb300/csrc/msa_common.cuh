@@ -169,9 +169,10 @@ struct GlobalRowsArgs {
 };
 cudaError_t launch_global_rows(const GlobalRowsArgs& a, cudaStream_t s, const char** why);
 
-// Backward pass (bf16, d = 128).  Workspace pieces: D [Hq, n], landmark
-// gradient partials [lm_chunks][2][G][Hkv][d] and their sums [2][G][Hkv][d]
-// (fp32).
+// Backward pass (bf16, d = 128).  Workspace pieces: per-row statistics
+// [2][Hq][n_pad] (lse in log2 units, then D; n_pad = n rounded up to 128,
+// padding +inf / 0), landmark gradient partials [lm_chunks][2][G][Hkv][d]
+// and their sums [2][G][Hkv][d] (fp32).
 struct BwdArgs {
   const void* q;
   const void* k;
@@ -184,10 +185,10 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
-  float* D;
+  float* stats;
   float* lm_part;
   float* lm_grad;
-  int64_t n, window;
+  int64_t n, n_pad, window;
   int G, Hq, Hkv;
   float scale;
   int out_bf16, grad_bf16;
