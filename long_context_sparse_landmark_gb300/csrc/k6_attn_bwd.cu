@@ -82,8 +82,8 @@ constexpr int kSmemBytes = kSmemUsed + 1024;
 
 struct BwdParams {
   CUtensorMap tm_q, tm_do, tm_k, tm_v, tm_klm, tm_vlm;
-  const float* L2;    // [Hq, n_pad] lse * log2(e), +inf past n
-  const float* D;     // [Hq, n_pad] <dO, O>, 0 past n
+  const float* L2;    // [Hq, n_pad] -lse * log2(e), -inf past n
+  const float* D;     // [Hq, n_pad] -<dO, O>, 0 past n
   void* dq;           // [n, Hq, d]
   void* dk;           // [n, Hkv, d]
   void* dv;
@@ -330,11 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const int64_t i = qr0 + threadIdx.x;
     const bool row_ok = i < p.n;
-    const float L2 = p.L2[static_cast<int64_t>(h) * p.n_pad + i];
-    const float Di = p.D[static_cast<int64_t>(h) * p.n_pad + i];
+    const float nL2 = p.L2[static_cast<int64_t>(h) * p.n_pad + i];
+    const float nD = p.D[static_cast<int64_t>(h) * p.n_pad + i];
+    const uint64_t c2 = ptx::f2(p.scale_log2, p.scale_log2);
+    const uint64_t nL22 = ptx::f2(nL2, nL2);
+    const uint64_t nD2 = ptx::f2(nD, nD);
     const int64_t my_lm = visible_landmarks(i, p.window, p.block, p.G);
     const int64_t my_lo = max64(i - p.window + 1, 0);
-    const float sl2 = p.scale_log2;
     bool ok = true;
     for (int t = 0; ok && t < T; ++t) {
       int64_t lo, hi;  // valid columns [lo, hi) of this key tile for row i
@@ -353,24 +355,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
         ptx::tc_fence_after();
         const int lo_c = static_cast<int>(max64(0, min64(kHalf, lo - half * kHalf)));
         const int hi_c = static_cast<int>(max64(0, min64(kHalf, hi - half * kHalf)));
+        const bool full = lo_c == 0 && hi_c == kHalf;
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
           float s[32], dp[32];
           ptx::tmem_ld32(tl + col_s(half) + cc * 32, s);
           ptx::tmem_ld32(tl + col_p(half) + cc * 32, dp);
           ptx::tmem_wait_ld();
+          if (!full) {  // masked columns: weight 0
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int col = cc * 32 + e;
+              s[e] = (col >= lo_c && col < hi_c) ? s[e] : -INFINITY;
+            }
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            float ds[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int col = cc * 32 + 2 * e + u;
-              const bool valid = col >= lo_c && col < hi_c;
-              const float pr = valid ? ptx::ex2(fmaf(s[2 * e + u], sl2, -L2)) : 0.f;
-              ds[u] = pr * (dp[2 * e + u] - Di);
-            }
-            pk[e] = ptx::pack_bf16x2(ds[0], ds[1]);
+            // p = 2^(s scale log2e - lse log2e), dS = p (dP - D)
+            float x0, x1;
+            ptx::f2_split(ptx::fma2(ptx::f2(s[2 * e], s[2 * e + 1]), c2, nL22), x0, x1);
+            const uint64_t pr = ptx::f2(ptx::ex2(x0), ptx::ex2(x1));
+            float d0, d1;
+            ptx::f2_split(ptx::mul2(pr, ptx::add2(ptx::f2(dp[2 * e], dp[2 * e + 1]), nD2)), d0,
+                          d1);
+            pk[e] = ptx::pack_bf16x2(d0, d1);
           }
           ptx::tmem_st16(tl + col_s(half) + cc * 16, pk);  // dS over columns already read
         }
@@ -482,11 +491,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 4) {
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const int64_t j = kb + threadIdx.x;  // key (window mode) or landmark (landmark mode)
-    const float sl2 = p.scale_log2;
+    const uint64_t c2 = ptx::f2(p.scale_log2, p.scale_log2);
     bool ok = true;
     for (int it = 0; ok && it < iters; ++it) {
       const int64_t qr0 = (qt_lo + it / p.group) * kT;
-      // This iteration's per-query lse (log2 units) and D came with its
+      // This iteration's per-query -lse (log2 units) and -D came with its
       // Q / dO stage; the stage has landed once its scores exist, and it is
       // not refilled before this iteration's results are in.
       const float* sL = reinterpret_cast<const float*>(smem + kOffStats + (it & 1) * kStatBytes);
@@ -508,27 +517,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const int lo_c = static_cast<int>(max64(0, min64(kHalf, lo - half * kHalf)));
         const int hi_c = static_cast<int>(max64(0, min64(kHalf, hi - half * kHalf)));
-        const float* hL = sL + half * kHalf;
-        const float* hD = sD + half * kHalf;
+        const float4* hL = reinterpret_cast<const float4*>(sL + half * kHalf);
+        const float4* hD = reinterpret_cast<const float4*>(sD + half * kHalf);
+        const bool full = lo_c == 0 && hi_c == kHalf;
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
           float s[32], dp[32];
           ptx::tmem_ld32(tl + col_s(half) + cc * 32, s);
           ptx::tmem_ld32(tl + col_p(half) + cc * 32, dp);
           ptx::tmem_wait_ld();
+          if (!full) {  // masked columns: weight 0
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int col = cc * 32 + e;
+              s[e] = (col >= lo_c && col < hi_c) ? s[e] : -INFINITY;
+            }
+          }
           uint32_t pp[16], dd[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float pr[2], ds[2];
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 l4 = hL[cc * 8 + q4];  // -lse log2e of 4 queries (broadcast)
+            const float4 d4 = hD[cc * 8 + q4];  // -D of the same queries
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const int col = cc * 32 + 2 * e + u;
-              const bool valid = col >= lo_c && col < hi_c;
-              pr[u] = valid ? ptx::ex2(fmaf(s[2 * e + u], sl2, -hL[col])) : 0.f;
-              ds[u] = pr[u] * (dp[2 * e + u] - hD[col]);
+              const int e = 2 * q4 + u;
+              const uint64_t nl = u ? ptx::f2(l4.z, l4.w) : ptx::f2(l4.x, l4.y);
+              const uint64_t nd = u ? ptx::f2(d4.z, d4.w) : ptx::f2(d4.x, d4.y);
+              float x0, x1;
+              ptx::f2_split(ptx::fma2(ptx::f2(s[2 * e], s[2 * e + 1]), c2, nl), x0, x1);
+              const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+              float d0, d1;
+              ptx::f2_split(
+                  ptx::mul2(ptx::f2(p0, p1), ptx::add2(ptx::f2(dp[2 * e], dp[2 * e + 1]), nd)),
+                  d0, d1);
+              pp[e] = ptx::pack_bf16x2(p0, p1);
+              dd[e] = ptx::pack_bf16x2(d0, d1);
             }
-            pp[e] = ptx::pack_bf16x2(pr[0], pr[1]);
-            dd[e] = ptx::pack_bf16x2(ds[0], ds[1]);
           }
           ptx::tmem_st16(tl + col_s(half) + cc * 16, pp);  // P^T over columns already read
           ptx::tmem_st16(tl + col_p(half) + cc * 16, dd);  // dS^T likewise
@@ -589,9 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ----------------------------------------------------------- small kernels
-// Row statistics: L2[h, i] = lse[h, i] * log2(e) and D[h, i] = <dO[i, h],
-// O[i, h]> for i < n, +inf and 0 for the padding up to n_pad; one warp per
-// (row, head), 4 elements a lane.
+// Row statistics, stored negated for the packed FMAs that use them:
+// nL2[h, i] = -lse[h, i] log2(e) and nD[h, i] = -<dO[i, h], O[i, h]> for
+// i < n, -inf and 0 for the padding up to n_pad; one warp per (row, head),
+// 4 elements a lane.
 template <bool kOutBf16>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const void* out, const uint16_t* dout, const float* lse, float* L2,
@@ -615,8 +640,8 @@ __global__ void __launch_bounds__(256)
   }
   if (lane == 0) {
     const int64_t at = static_cast<int64_t>(h) * n_pad + i;
-    D[at] = acc;
-    L2[at] = i < n ? lse[static_cast<int64_t>(h) * n + i] * kLog2e : INFINITY;
+    D[at] = -acc;
+    L2[at] = i < n ? -lse[static_cast<int64_t>(h) * n + i] * kLog2e : -INFINITY;
   }
 }
 
