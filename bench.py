@@ -199,8 +199,10 @@ def run_window_landmark(wl, steps, warmup, dev, B, torch):
 
 
 def run_e2e(wl, steps, dev, torch):
-    """Through the public API with pinned HOST buffers: every step copies
-    Q/K/V host->device, runs msa_attention, copies O and lse back."""
+    """Through the public host-buffer API (msa_attention_host) with pinned
+    HOST inputs and outputs: every step copies Q/K/V host->device, pools,
+    runs the attention on row chunks and copies O and lse back, the copies
+    overlapping the kernels; the call returns with the host results final."""
     import long_context_sparse_landmark_gb300 as pkg
     from long_context_sparse_landmark_gb300.workloads import generate
     q, k, v = generate(wl, device=dev)
@@ -211,13 +213,8 @@ def run_e2e(wl, steps, dev, torch):
     hl = torch.empty((wl.Hq, wl.n), dtype=torch.float32).pin_memory()
 
     def step():
-        dq = hq.to(dev, non_blocking=True)
-        dk = hk.to(dev, non_blocking=True)
-        dv = hv.to(dev, non_blocking=True)
-        o, l = pkg.msa_attention(dq, dk, dv, wl.window, wl.G, wl.scale)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(l, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        pkg.msa_attention_host(hq, hk, hv, wl.window, wl.G, wl.scale, out=ho, lse=hl,
+                               device=dev)
 
     step()
     t = time.perf_counter()

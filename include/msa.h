@@ -110,6 +110,27 @@ msa_status msa_attn_fwd(const void *q, const void *k, const void *v,
                         msa_stream_t stream);
 
 /*
+ * msa_attn_fwd restricted to the contiguous query rows [q_start, q_start +
+ * n_q): the same window + landmark attention, so that a caller can stream
+ * Q and O through the device in row chunks (keys, values and landmarks are
+ * the whole sequence's).
+ *   q_rows [n_q, Hq, d] = rows q_start.. of Q; k, v [n, Hkv, d]; k_lm, v_lm
+ *   [G, Hkv, d]; out_rows [n_q, Hq, d] in `out_dt`; lse: lse[h * lse_ld + r]
+ *   receives row q_start + r of head h (lse_ld >= n_q; pass the full [Hq, n]
+ *   array offset by q_start and lse_ld = n to fill it chunk by chunk; lse
+ *   needs 4-byte alignment only, the other pointers 16).
+ * Errors: as msa_attn_fwd, plus INVALID_ARG when the rows do not lie in
+ * [0, n) or lse_ld < n_q.
+ */
+msa_status msa_attn_fwd_rows(const void *q_rows, const void *k, const void *v,
+                             const void *k_lm, const void *v_lm, void *out_rows,
+                             float *lse, int64_t lse_ld, int64_t q_start,
+                             int64_t n_q, int64_t n, int Hq, int Hkv, int d,
+                             int64_t window, int n_landmarks, float scale,
+                             msa_dtype in_dt, msa_dtype out_dt,
+                             msa_stream_t stream);
+
+/*
  * Block-band attention: the 2-D block-sparse mask of "Million Token Context
  * Window Optimization: What Actually Works", section "The indexing game:
  * smarter context management" (each 128-token block attends to 16 other

@@ -21,7 +21,7 @@ MAX_MERGE_PARTS = 64
 
 # Every symbol include/msa.h declares.
 EXPORTS = ("msa_version", "msa_last_error_string", "msa_landmark_pool", "msa_attn_fwd",
-           "msa_attn_fwd_band", "msa_block_select", "msa_attn_fwd_select",
+           "msa_attn_fwd_rows", "msa_attn_fwd_band", "msa_block_select", "msa_attn_fwd_select",
            "msa_attn_fwd_topk_workspace_size", "msa_attn_fwd_topk", "msa_attn_fwd_topk_noalloc",
            "msa_attn_fwd_global_rows", "msa_attn_fwd_global_rows_workspace_size",
            "msa_attn_bwd", "msa_attn_bwd_workspace_size", "msa_attn_fwd_partial",
@@ -51,6 +51,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_attn_fwd_band.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i64, f32,
                                       i32, i32, vp]
     lib.msa_attn_fwd_band.restype = i32
+    lib.msa_attn_fwd_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, i32,
+                                      i64, i32, f32, i32, i32, vp]
+    lib.msa_attn_fwd_rows.restype = i32
     lib.msa_block_select.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i64, i32, i32, i32, vp]
     lib.msa_block_select.restype = i32
     lib.msa_attn_fwd_select.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32,
@@ -166,6 +169,22 @@ def attn_fwd_band(q, k, v, out, lse, band_block: int, band_half: int, scale: flo
     _check(_lib.msa_attn_fwd_band(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), n, Hq, Hkv, d,
                                   int(band_block), int(band_half), float(scale), _dt(q), _dt(out),
                                   _stream(stream)))
+
+
+def attn_fwd_rows(q_rows, k, v, k_lm, v_lm, out_rows, lse, q_start: int, window: int,
+                  n_landmarks: int, scale: float, stream=None) -> None:
+    """msa_attn_fwd_rows: query rows [q_start, q_start + len(q_rows)) of the
+    window + landmark attention; lse is the full [Hq, n] array (its columns
+    q_start.. are written)."""
+    n_q, Hq, d = q_rows.shape
+    n, Hkv, _ = k.shape
+    if lse.shape != (Hq, n) or not lse.is_contiguous():
+        raise ValueError("lse must be the contiguous [Hq, n] array")
+    lse_ptr = lse.data_ptr() + 4 * int(q_start)
+    _check(_lib.msa_attn_fwd_rows(_ptr(q_rows), _ptr(k), _ptr(v), _ptr(k_lm), _ptr(v_lm),
+                                  _ptr(out_rows), ctypes.c_void_p(lse_ptr), n, int(q_start), n_q,
+                                  n, Hq, Hkv, d, int(window), int(n_landmarks), float(scale),
+                                  _dt(q_rows), _dt(out_rows), _stream(stream)))
 
 
 def block_select(q, k_lm, sel, cnt, window: int, top_k: int, stream=None) -> None:

@@ -197,3 +197,75 @@ def msa_attention_trainable(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, w
     out [n, Hq, d]; ``out.backward(g)`` runs msa_attn_bwd."""
     scale = 1.0 / math.sqrt(q.shape[2]) if scale is None else scale
     return _MSAAttention.apply(q, k, v, window, n_landmarks, scale)
+
+
+def msa_attention_host(hq: torch.Tensor, hk: torch.Tensor, hv: torch.Tensor, window: int,
+                       n_landmarks: int, scale: float | None = None, out: torch.Tensor | None = None,
+                       lse: torch.Tensor | None = None, chunk_rows: int = 16384, device=None):
+    """Window + landmark attention on host (pinned) tensors.
+
+    K and V are copied to the device first (every query needs all of them)
+    and pooled; Q and O then stream through the device in chunks of
+    ``chunk_rows`` rows: on one copy stream Q chunk c+1 goes in, on the
+    compute stream msa_attn_fwd_rows runs on chunk c, on a second copy
+    stream O of chunk c-1 comes back, double-buffered, so the transfers
+    overlap the kernels.  Returns host (out [n, Hq, d] in q's dtype, lse
+    [Hq, n] fp32), complete when the call returns.
+    """
+    dev = torch.device(device) if device is not None else torch.device("cuda")
+    n, Hq, d = hq.shape
+    Hkv = hk.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    rows = max(128, (int(chunk_rows) + 127) // 128 * 128)
+    if out is None:
+        out = torch.empty((n, Hq, d), dtype=hq.dtype, pin_memory=True)
+    if lse is None:
+        lse = torch.empty((Hq, n), dtype=torch.float32, pin_memory=True)
+    comp = torch.cuda.current_stream(dev)
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    s_in.wait_stream(comp)
+    with torch.cuda.stream(s_in):
+        dk = hk.to(dev, non_blocking=True)
+        dv = hv.to(dev, non_blocking=True)
+        qbuf = [torch.empty((min(rows, n), Hq, d), dtype=hq.dtype, device=dev)
+                for _ in range(2)]
+    kv_ready = torch.cuda.Event()
+    kv_ready.record(s_in)
+    comp.wait_event(kv_ready)
+    if n_landmarks > 0:
+        k_lm, v_lm = landmarks(dk, dv, n_landmarks, stream=comp)
+    else:
+        k_lm = v_lm = None
+    obuf = [torch.empty((min(rows, n), Hq, d), dtype=hq.dtype, device=dev) for _ in range(2)]
+    dlse = torch.empty((Hq, n), dtype=torch.float32, device=dev)
+    q_free = [None, None]  # compute of the chunk that last used the buffer
+    o_free = [None, None]  # copy-out of the chunk that last used the buffer
+    done = None
+    for c, r0 in enumerate(range(0, n, rows)):
+        r1 = min(n, r0 + rows)
+        m = r1 - r0
+        b = c & 1
+        if q_free[b] is not None:
+            s_in.wait_event(q_free[b])
+        with torch.cuda.stream(s_in):
+            qbuf[b][:m].copy_(hq[r0:r1], non_blocking=True)
+        q_ready = torch.cuda.Event()
+        q_ready.record(s_in)
+        comp.wait_event(q_ready)
+        if o_free[b] is not None:
+            comp.wait_event(o_free[b])
+        B.attn_fwd_rows(qbuf[b][:m], dk, dv, k_lm, v_lm, obuf[b][:m], dlse, r0, window,
+                        n_landmarks, scale, stream=comp)
+        done = torch.cuda.Event()
+        done.record(comp)
+        q_free[b] = done
+        s_out.wait_event(done)
+        with torch.cuda.stream(s_out):
+            out[r0:r1].copy_(obuf[b][:m], non_blocking=True)
+        o_free[b] = torch.cuda.Event()
+        o_free[b].record(s_out)
+    with torch.cuda.stream(s_out):
+        lse.copy_(dlse, non_blocking=True)
+    s_out.synchronize()
+    return out, lse

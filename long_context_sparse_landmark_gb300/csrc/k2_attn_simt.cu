@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnArgs a) {
   }
 
   if (!row_ok) return;
-  const int64_t lse_idx = static_cast<int64_t>(h) * a.n_q + i_loc;
+  const int64_t lse_idx = static_cast<int64_t>(h) * a.lse_ld + i_loc;
   if (l == 0.f) {  // no key for this row (only possible for a partial)
     if (a.merge) return;  // a running merge leaves the row untouched
     if (qd == 0) a.lse[lse_idx] = -INFINITY;

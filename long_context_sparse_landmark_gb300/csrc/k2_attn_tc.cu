@@ -97,7 +97,7 @@ struct TcParams {
   CUtensorMap tm_vlm;
   void* out;
   float* lse;
-  int64_t n_q, q_start, n_kv, kv_start, window, block;
+  int64_t n_q, q_start, n_kv, kv_start, window, block, lse_ld;
   int Hq, Hkv, G, group, pairs, n_qtiles, units;
   int out_bf16, partial, merge, band;
   int64_t band_block, band_half;
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const int64_t i = p.q_start + i_loc;
       const int h = w.h0 + slot;
       if (w.T == 0) {  // no key for any row of this unit (partial chunks only)
-        if (row_ok && !p.merge) p.lse[static_cast<int64_t>(h) * p.n_q + i_loc] = -INFINITY;
+        if (row_ok && !p.merge) p.lse[static_cast<int64_t>(h) * p.lse_ld + i_loc] = -INFINITY;
         continue;
       }
       int64_t my_lo, my_hi;
@@ -525,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       // arrives for the next unit's first P, which the MMA thread waits for
       // before the next unit's first PV overwrites O.
       const bool has = row_ok && l > 0.f;
-      const int64_t lse_idx = static_cast<int64_t>(h) * p.n_q + i_loc;
+      const int64_t lse_idx = static_cast<int64_t>(h) * p.lse_ld + i_loc;
       // O = acc * w_new (+ running O * w_run when merging into a running
       // result: lse_run <- ln(e^lse_run + e^lse_p)).
       const float lse_p = has ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
@@ -628,6 +628,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s, const char** why) 
   p.out = a.out;
   p.lse = a.lse;
   p.n_q = a.n_q;
+  p.lse_ld = a.lse_ld;
   p.q_start = a.q_start;
   p.n_kv = a.n_kv;
   p.kv_start = a.kv_start;

@@ -68,12 +68,16 @@ msa_status launched(cudaError_t e, const char* what) {
   return ok();
 }
 
+// lse_align: alignment the lse pointer needs (16, or 4 where it may point
+// into the middle of an [Hq, n] array).
 msa_status check_attn_common(const void* q, const void* k, const void* v, const void* out,
                              const float* lse, int Hq, int Hkv, int d, int64_t window,
-                             float scale, msa_dtype in_dt) {
+                             float scale, msa_dtype in_dt, uintptr_t lse_align = 16) {
   if (!q || !k || !v || !out || !lse) return fail(MSA_ERR_INVALID_ARG, "null tensor pointer");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
-    return fail(MSA_ERR_INVALID_ARG, "tensor pointer not 16-byte aligned");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(lse) & (lse_align - 1)) != 0)
+    return fail(MSA_ERR_INVALID_ARG, "tensor pointer not 16-byte aligned (lse: %u)",
+                static_cast<unsigned>(lse_align));
   if (Hq < 1 || Hkv < 1) return fail(MSA_ERR_INVALID_ARG, "Hq=%d Hkv=%d must be >= 1", Hq, Hkv);
   if (Hq % Hkv != 0) return fail(MSA_ERR_INVALID_ARG, "Hq=%d not a multiple of Hkv=%d", Hq, Hkv);
   if (window < 1) return fail(MSA_ERR_INVALID_ARG, "window=%lld must be >= 1", (long long)window);
@@ -88,6 +92,7 @@ constexpr int64_t kMaxRows = (int64_t(1) << 31) - 256;  // TMA coordinates are 3
 
 msa_status run_attn(const msa::AttnArgs& a0, cudaStream_t stream) {
   msa::AttnArgs a = a0;
+  if (a.lse_ld == 0) a.lse_ld = a.n_q;
   msa_status st = device_status_ptr(&a.status);
   if (st != MSA_OK) return st;
   const uint64_t lim = g_wait_limit_ns.load();
@@ -234,6 +239,53 @@ msa_status msa_attn_fwd(const void* q, const void* k, const void* v, const void*
   a.in_bf16 = in_dt == MSA_BF16;
   a.out_bf16 = out_dt == MSA_BF16;
   a.partial = 0;
+  return run_attn(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_attn_fwd_rows(const void* q_rows, const void* k, const void* v, const void* k_lm,
+                             const void* v_lm, void* out_rows, float* lse, int64_t lse_ld,
+                             int64_t q_start, int64_t n_q, int64_t n, int Hq, int Hkv, int d,
+                             int64_t window, int n_landmarks, float scale, msa_dtype in_dt,
+                             msa_dtype out_dt, msa_stream_t stream) {
+  msa_status st = check_attn_common(q_rows, k, v, out_rows, lse, Hq, Hkv, d, window, scale,
+                                    in_dt, 4);
+  if (st != MSA_OK) return st;
+  if (n < 1 || n > kMaxRows) return fail(MSA_ERR_INVALID_ARG, "n=%lld out of range", (long long)n);
+  if (n_q < 1 || q_start < 0 || q_start + n_q > n)
+    return fail(MSA_ERR_INVALID_ARG, "rows [%lld, %lld) not inside [0, n=%lld)",
+                (long long)q_start, (long long)(q_start + n_q), (long long)n);
+  if (lse_ld < n_q) return fail(MSA_ERR_INVALID_ARG, "lse_ld=%lld below n_q", (long long)lse_ld);
+  if (!valid_dtype(out_dt)) return fail(MSA_ERR_INVALID_ARG, "bad output dtype %d", (int)out_dt);
+  if (n_landmarks < 0 || n_landmarks > n || (n_landmarks > 0 && n % n_landmarks != 0))
+    return fail(MSA_ERR_INVALID_ARG, "G=%d must satisfy 0 <= G <= n and n %% G == 0 (n=%lld)",
+                n_landmarks, (long long)n);
+  if (n_landmarks > 0) {
+    if (!k_lm || !v_lm) return fail(MSA_ERR_INVALID_ARG, "null landmark pointer with G > 0");
+    if (!aligned16(k_lm) || !aligned16(v_lm))
+      return fail(MSA_ERR_INVALID_ARG, "landmark pointer not 16-byte aligned");
+  }
+  msa::AttnArgs a{};
+  a.q = q_rows;
+  a.k = k;
+  a.v = v;
+  a.k_lm = n_landmarks > 0 ? k_lm : nullptr;
+  a.v_lm = n_landmarks > 0 ? v_lm : nullptr;
+  a.out = out_rows;
+  a.lse = lse;
+  a.lse_ld = lse_ld;
+  a.n_q = n_q;
+  a.q_start = q_start;
+  a.n_kv = n;
+  a.kv_start = 0;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.window = window;
+  a.G = n_landmarks;
+  a.block = n_landmarks > 0 ? n / n_landmarks : 1;
+  a.scale = scale;
+  a.in_bf16 = in_dt == MSA_BF16;
+  a.out_bf16 = out_dt == MSA_BF16;
   return run_attn(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

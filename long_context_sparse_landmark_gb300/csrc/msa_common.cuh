@@ -97,6 +97,7 @@ struct AttnArgs {
   const void* v_lm;
   void* out;
   float* lse;
+  int64_t lse_ld;  // row stride of lse [Hq][lse_ld] (0: n_q)
   int64_t n_q;
   int64_t q_start;
   int64_t n_kv;

@@ -287,3 +287,23 @@ def test_backward_validation(lib):
     assert call(idt=0) == 2      # fp32 inputs: no backward kernels
     assert call(d=64) == 2
     assert call(w=0) == 1
+
+
+def test_rows_validation(lib):
+    f = lib.msa_attn_fwd_rows
+
+    def call(**kw):
+        a = dict(q=GOOD, k=GOOD, v=GOOD, klm=GOOD, vlm=GOOD, o=GOOD, l=GOOD, ld=1024, qs=256,
+                 nq=128, n=1024, Hq=8, Hkv=2, d=128, w=64, G=8, idt=1, odt=0)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["klm"], a["vlm"], a["o"], a["l"], a["ld"], a["qs"],
+                 a["nq"], a["n"], a["Hq"], a["Hkv"], a["d"], a["w"], a["G"],
+                 ctypes.c_float(0.1), a["idt"], a["odt"], None)
+
+    assert call(qs=-1) == 1
+    assert call(qs=900, nq=128) == 1     # past n
+    assert call(nq=0) == 1
+    assert call(ld=100) == 1             # below n_q
+    assert call(klm=None) == 1
+    assert call(G=7) == 1
+    assert call(d=80) == 2
