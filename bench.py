@@ -50,15 +50,20 @@ def load_peaks():
 # applies to the kernel source it was measured on (SHA-256 of
 # k2_attn_tc.cu); after any change the traffic is reported as null.
 ATTN_TRAFFIC = {"128k_70b_layer": {
-    "bytes": 2.709747e9 + 2.142574e9,
-    "kernel_sha256": "658aa1cfeed9c439c69a6cc7c458f3e4b0691b379becf375e813f836ac4badbc"}}
+    "bytes": 2.704536e9 + 2.141867e9,
+    "kernel_sha256": "e711af4599a96daa93891cce7463421cb01b18bdb6b519b5f43847f9b3902df1"}}
 
 
 def kernel_sha256() -> str:
+    """SHA-256 over the attention kernel's source and the headers it
+    includes: recorded DRAM traffic is reported only for this exact code."""
     import hashlib
-    path = os.path.join(ROOT, "long_context_sparse_landmark_gb300", "csrc", "k2_attn_tc.cu")
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "long_context_sparse_landmark_gb300", "csrc")
+    for name in ("k2_attn_tc.cu", "tc_ptx.cuh", "tc_sync.cuh", "tma_map.h", "msa_common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def attn_traffic(name: str):
