@@ -6,7 +6,8 @@
 // scores it here instead of a BERT embedding).
 //
 // One CTA per (query block of 128 rows, KV group): it sums the block's
-// queries over rows and the group's heads (fp32), scores every key block
+// queries over rows and the group's heads (fp32, 16-byte vector loads, the
+// partial sums reduced in a fixed order), scores every key block
 // wholly before the window of the block's first row against its landmark
 // key, ranks the scores (ties to the lower block index) and writes the
 // top-k block indices in ascending order, and their count.
@@ -30,10 +31,11 @@ __device__ __forceinline__ float ld_el(const void* base, int64_t idx) {
 
 template <bool kBf16>
 __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectArgs a) {
+  constexpr int V = kBf16 ? 8 : 4;  // elements per 16-byte load
   extern __shared__ float ssm[];
-  float* qsum = ssm;               // [d]
-  float* part = qsum + a.d;        // [2][d] partial sums
-  float* score = part + 2 * a.d;   // [G]
+  float* qsum = ssm;                    // [d]
+  float* part = qsum + a.d;             // [kSelThreads * V] partial sums
+  float* score = part + kSelThreads * 8;  // [G]
   int* flag = reinterpret_cast<int*>(score + a.G);  // [G]
   const int t = blockIdx.x;        // query block
   const int c = blockIdx.y;        // KV group
@@ -42,19 +44,50 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectA
   const int64_t r0 = static_cast<int64_t>(t) * kSelQBlock;
   const int64_t r1 = min64(r0 + kSelQBlock, a.n);
 
-  // Query-block sum over rows and the group's heads.
-  for (int col = threadIdx.x; col < 2 * d; col += blockDim.x) {
-    const int e = col % d;
-    const int half = col / d;
-    float s = 0.f;
-    for (int64_t i = r0 + half; i < r1; i += 2)
-      for (int hh = 0; hh < g; ++hh)
-        s += ld_el<kBf16>(a.q, (i * a.Hq + c * g + hh) * static_cast<int64_t>(d) + e);
-    part[half * d + e] = s;
+  // Query-block sum over rows and the group's heads: thread (slot, vi)
+  // adds 16-byte vector vi of every slots-th (row, head) pair (a row's g
+  // heads are contiguous), then the slots are summed in a fixed order.
+  {
+    const int VP = d / V;                 // vectors per (row, head)
+    const int slots = kSelThreads / VP;
+    const int vi = threadIdx.x % VP;
+    const int ps = threadIdx.x / VP;
+    const int64_t npairs = (r1 - r0) * g;
+    float acc[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) acc[k] = 0.f;
+    const uint8_t* qb = static_cast<const uint8_t*>(a.q);
+    constexpr int ES = kBf16 ? 2 : 4;
+#pragma unroll 4
+    for (int64_t pr = ps; pr < npairs; pr += slots) {
+      const int64_t i = r0 + pr / g;
+      const int hh = static_cast<int>(pr % g);
+      const uint4 x = __ldg(reinterpret_cast<const uint4*>(
+          qb + ((i * a.Hq + c * g + hh) * static_cast<int64_t>(d) + vi * V) * ES));
+      if constexpr (kBf16) {
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[2 * k] += __uint_as_float(w[k] << 16);
+          acc[2 * k + 1] += __uint_as_float(w[k] & 0xffff0000u);
+        }
+      } else {
+        acc[0] += __uint_as_float(x.x);
+        acc[1] += __uint_as_float(x.y);
+        acc[2] += __uint_as_float(x.z);
+        acc[3] += __uint_as_float(x.w);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < V; ++k) part[ps * d + vi * V + k] = acc[k];
+    __syncthreads();
+    for (int e = threadIdx.x; e < d; e += blockDim.x) {
+      float s = 0.f;
+      for (int q = 0; q < slots; ++q) s += part[q * d + e];
+      qsum[e] = s;
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < d; e += blockDim.x) qsum[e] = part[e] + part[d + e];
-  __syncthreads();
 
   // Candidates: blocks l with (l+1)*bs <= r0 - w + 1.
   const int64_t n_cand = visible_landmarks(r0, a.window, a.block, a.G);
@@ -103,7 +136,8 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectA
 }  // namespace
 
 size_t block_select_smem(int d, int G) {
-  return sizeof(float) * (3 * static_cast<size_t>(d) + G) + sizeof(int) * static_cast<size_t>(G);
+  return sizeof(float) * (static_cast<size_t>(d) + kSelThreads * 8 + G) +
+         sizeof(int) * static_cast<size_t>(G);
 }
 
 cudaError_t launch_block_select(const SelectArgs& a, cudaStream_t s) {
