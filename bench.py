@@ -512,8 +512,11 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--workload", default=HEADLINE,
                     help="window+landmark workload timed as the step (profiling uses smaller ones)")
-    ap.add_argument("--only", choices=["ring"], default=None,
-                    help="run only the ring emulation (partials, merge, fused rounds)")
+    ap.add_argument("--only", choices=["ring", "bwd", "topk"], default=None,
+                    help="run only one leg: the ring emulation (partials, merge, fused "
+                         "rounds), the backward pass, or the top-k call (for profiling)")
+    ap.add_argument("--leg-n", type=int, default=None,
+                    help="tokens of the --only bwd / topk leg (default: the workload's)")
     ap.add_argument("--ring-n", type=int, default=None,
                     help="tokens of the ring emulation (default 131072; smaller for profiling)")
     ap.add_argument("--no-also", action="store_true")
@@ -542,6 +545,21 @@ def main():
         dist.init_process_group("nccl")
 
     from long_context_sparse_landmark_gb300 import _binding as B
+
+    if args.only in ("bwd", "topk"):
+        base = wl if args.only == "bwd" else WORKLOADS["topk_128k"]
+        wlx = base.with_n(args.leg_n, name=f"{base.name}_{args.leg_n}") if args.leg_n else base
+        if args.only == "bwd":
+            ms = run_bwd(wlx, args.steps, args.warmup, dev, B, torch)
+            res = {"workload": wlx.name, "bwd_ms": round(ms, 4),
+                   "tflops": round(2.5 * useful_flops(wlx) / (ms * 1e-3) / 1e12, 2)}
+        else:
+            r = run_topk(wlx, args.steps, args.warmup, dev, B, torch)
+            res = {"workload": wlx.name, "fused_ms": round(r["fused_ms"], 4),
+                   "select_ms": round(r["select_ms"], 4)}
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
 
     if args.only == "ring":
         wlr = WORKLOADS["ring_128k"]
