@@ -204,19 +204,25 @@ def msa_attention_host(hq: torch.Tensor, hk: torch.Tensor, hv: torch.Tensor, win
                        lse: torch.Tensor | None = None, chunk_rows: int = 16384, device=None):
     """Window + landmark attention on host (pinned) tensors.
 
-    K and V are copied to the device first (every query needs all of them)
-    and pooled; Q and O then stream through the device in chunks of
-    ``chunk_rows`` rows: on one copy stream Q chunk c+1 goes in, on the
-    compute stream msa_attn_fwd_rows runs on chunk c, on a second copy
-    stream O of chunk c-1 comes back, double-buffered, so the transfers
-    overlap the kernels.  Returns host (out [n, Hq, d] in q's dtype, lse
-    [Hq, n] fp32), complete when the call returns.
+    Rows [r0, r1) of the result need only K/V rows [0, r1) and the landmarks
+    of the blocks inside them, so everything streams through the device in
+    chunks of ``chunk_rows`` rows: on one copy stream chunk c of K, V and Q
+    goes in, on the compute stream the landmarks of chunk c are pooled and
+    msa_attn_fwd_rows runs on its queries, on a second copy stream O of chunk
+    c comes back -- Q and O double-buffered -- so the transfers overlap the
+    kernels.  (When the chunk is not a whole number of landmark blocks, K
+    and V are copied and pooled whole before the first chunk.)  Returns
+    host (out [n, Hq, d] in q's dtype, lse [Hq, n] fp32), complete when the
+    call returns.
     """
     dev = torch.device(device) if device is not None else torch.device("cuda")
     n, Hq, d = hq.shape
     Hkv = hk.shape[1]
+    G = int(n_landmarks)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     rows = max(128, (int(chunk_rows) + 127) // 128 * 128)
+    blk = n // G if G > 0 else 1
+    kv_stream = G == 0 or rows % blk == 0  # K/V (and pooling) per chunk
     if out is None:
         out = torch.empty((n, Hq, d), dtype=hq.dtype, pin_memory=True)
     if lse is None:
@@ -226,22 +232,27 @@ def msa_attention_host(hq: torch.Tensor, hk: torch.Tensor, hv: torch.Tensor, win
     s_out = torch.cuda.Stream(dev)
     s_in.wait_stream(comp)
     with torch.cuda.stream(s_in):
-        dk = hk.to(dev, non_blocking=True)
-        dv = hv.to(dev, non_blocking=True)
+        dk = torch.empty((n, Hkv, d), dtype=hk.dtype, device=dev)
+        dv = torch.empty_like(dk)
         qbuf = [torch.empty((min(rows, n), Hq, d), dtype=hq.dtype, device=dev)
                 for _ in range(2)]
-    kv_ready = torch.cuda.Event()
-    kv_ready.record(s_in)
-    comp.wait_event(kv_ready)
-    if n_landmarks > 0:
-        k_lm, v_lm = landmarks(dk, dv, n_landmarks, stream=comp)
-    else:
-        k_lm = v_lm = None
+        if not kv_stream:
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+    # Zeros: while streaming, a landmark tile can reach past the blocks pooled
+    # so far; those (masked) rows must hold finite values, as 0 * NaN in the
+    # PV product would not vanish.
+    k_lm = torch.zeros((max(G, 1), Hkv, d), dtype=hk.dtype, device=dev) if G else None
+    v_lm = torch.zeros_like(k_lm) if G else None
+    if G and not kv_stream:
+        kv_ready = torch.cuda.Event()
+        kv_ready.record(s_in)
+        comp.wait_event(kv_ready)
+        B.landmark_pool(dk, dv, k_lm, v_lm, stream=comp)
     obuf = [torch.empty((min(rows, n), Hq, d), dtype=hq.dtype, device=dev) for _ in range(2)]
     dlse = torch.empty((Hq, n), dtype=torch.float32, device=dev)
     q_free = [None, None]  # compute of the chunk that last used the buffer
     o_free = [None, None]  # copy-out of the chunk that last used the buffer
-    done = None
     for c, r0 in enumerate(range(0, n, rows)):
         r1 = min(n, r0 + rows)
         m = r1 - r0
@@ -249,14 +260,20 @@ def msa_attention_host(hq: torch.Tensor, hk: torch.Tensor, hv: torch.Tensor, win
         if q_free[b] is not None:
             s_in.wait_event(q_free[b])
         with torch.cuda.stream(s_in):
+            if kv_stream:
+                dk[r0:r1].copy_(hk[r0:r1], non_blocking=True)
+                dv[r0:r1].copy_(hv[r0:r1], non_blocking=True)
             qbuf[b][:m].copy_(hq[r0:r1], non_blocking=True)
-        q_ready = torch.cuda.Event()
-        q_ready.record(s_in)
-        comp.wait_event(q_ready)
+        in_ready = torch.cuda.Event()
+        in_ready.record(s_in)
+        comp.wait_event(in_ready)
+        if G and kv_stream:  # the landmarks of this chunk's blocks (r0, r1: whole blocks)
+            l0, l1 = r0 // blk, r1 // blk
+            B.landmark_pool(dk[r0:r1], dv[r0:r1], k_lm[l0:l1], v_lm[l0:l1], stream=comp)
         if o_free[b] is not None:
             comp.wait_event(o_free[b])
-        B.attn_fwd_rows(qbuf[b][:m], dk, dv, k_lm, v_lm, obuf[b][:m], dlse, r0, window,
-                        n_landmarks, scale, stream=comp)
+        B.attn_fwd_rows(qbuf[b][:m], dk, dv, k_lm, v_lm, obuf[b][:m], dlse, r0, window, G,
+                        scale, stream=comp)
         done = torch.cuda.Event()
         done.record(comp)
         q_free[b] = done

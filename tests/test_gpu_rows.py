@@ -2,7 +2,9 @@
 (msa_attention_host): row chunks reproduce the whole-sequence call bit for
 bit when they start on 128-row tiles (the same tiles run the same
 arithmetic), ragged chunks match the oracle at their global positions, and
-the host API returns exactly the device API's results."""
+the host API returns exactly the device API's results (K/V and landmarks
+streamed per chunk when chunks are whole landmark blocks, copied whole
+first otherwise; ragged last chunks; no landmarks)."""
 import numpy as np
 import pytest
 import torch
@@ -63,7 +65,8 @@ def test_ragged_row_range_matches_oracle(dt, d, q_start, n_q):
 
 
 @pytest.mark.parametrize("name,chunk", [("32k_outliers", 4096), ("128k_70b_layer", 16384),
-                                        ("pr1_2k", 300)])
+                                        ("pr1_2k", 300), ("32k_outliers", 4160),
+                                        ("ring_128k", 20000)])
 def test_host_api_equals_device_api(name, chunk):
     import long_context_sparse_landmark_gb300.api as api
     wl = WORKLOADS[name]
