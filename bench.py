@@ -491,16 +491,29 @@ def cpu_baseline(wl, rows_target, torch):
     t = time.perf_counter()
     oracle.attn(qs, kn, vn, wl.window, wl.G, wl.scale, q_positions=rows, landmarks=(k_lm, v_lm))
     rows_s = time.perf_counter() - t
-    i = rows
-    per_row = np.minimum(wl.window, i + 1) + np.clip((i - wl.window + 1) // wl.block, 0, wl.G)
-    sample_flops = 4.0 * wl.d * wl.Hq * float(per_row.sum())
-    full_s = pool_s + rows_s * useful_flops(wl) / sample_flops
+    cores = oracle.get_threads()
+
+    def flops_of(r):
+        per_row = np.minimum(wl.window, r + 1) + np.clip((r - wl.window + 1) // wl.block, 0, wl.G)
+        return 4.0 * wl.d * wl.Hq * float(per_row.sum())
+
+    full_s = pool_s + rows_s * useful_flops(wl) / flops_of(rows)
+    # The same oracle on one thread, on the first 1/16 of the sample.
+    r1 = rows[: max(1, rows_target // 16)]
+    oracle.set_threads(1)
+    t = time.perf_counter()
+    oracle.attn(qs[: len(r1)], kn, vn, wl.window, wl.G, wl.scale, q_positions=r1,
+                landmarks=(k_lm, v_lm))
+    one_s = time.perf_counter() - t
+    oracle.set_threads(cores)
     return {"value": useful_flops(wl) / full_s / 1e12, "unit": "TFLOP/s",
-            "cores": oracle.get_threads(), "kind": "oracle",
+            "cores": cores, "kind": "oracle",
             "sample": (f"{rows_target} random rows x {wl.Hq} heads of {wl.name} "
                        f"({rows_s:.1f} s) + landmark pooling of the full K/V ({pool_s:.1f} s); "
                        f"extrapolated to all {wl.n} rows by attended keys"),
-            "wall_s": pool_s + rows_s}
+            "value_1_thread": flops_of(r1) / one_s / 1e12,
+            "sample_1_thread": f"{len(r1)} of those rows on one thread ({one_s:.1f} s)",
+            "wall_s": pool_s + rows_s + one_s}
 
 
 def main():
