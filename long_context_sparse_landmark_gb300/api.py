@@ -201,12 +201,14 @@ def msa_attention_trainable(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, w
 
 def msa_attention_host(hq: torch.Tensor, hk: torch.Tensor, hv: torch.Tensor, window: int,
                        n_landmarks: int, scale: float | None = None, out: torch.Tensor | None = None,
-                       lse: torch.Tensor | None = None, chunk_rows: int = 16384, device=None):
+                       lse: torch.Tensor | None = None, chunk_rows: int | None = None,
+                       device=None):
     """Window + landmark attention on host (pinned) tensors.
 
     Rows [r0, r1) of the result need only K/V rows [0, r1) and the landmarks
     of the blocks inside them, so everything streams through the device in
-    chunks of ``chunk_rows`` rows: on one copy stream chunk c of K, V and Q
+    chunks of ``chunk_rows`` rows (default: n/32, at least 4096): on one copy
+    stream chunk c of K, V and Q
     goes in, on the compute stream the landmarks of chunk c are pooled and
     msa_attn_fwd_rows runs on its queries, on a second copy stream O of chunk
     c comes back -- Q and O double-buffered -- so the transfers overlap the
@@ -220,6 +222,8 @@ def msa_attention_host(hq: torch.Tensor, hk: torch.Tensor, hv: torch.Tensor, win
     Hkv = hk.shape[1]
     G = int(n_landmarks)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if chunk_rows is None:  # about 32 chunks, at least 4096 rows (4096 at 128K tokens)
+        chunk_rows = max(4096, -(-n // 32))
     rows = max(128, (int(chunk_rows) + 127) // 128 * 128)
     blk = n // G if G > 0 else 1
     kv_stream = G == 0 or rows % blk == 0  # K/V (and pooling) per chunk
