@@ -66,7 +66,7 @@ def test_ragged_row_range_matches_oracle(dt, d, q_start, n_q):
 
 @pytest.mark.parametrize("name,chunk", [("32k_outliers", 4096), ("128k_70b_layer", 16384),
                                         ("pr1_2k", 300), ("32k_outliers", 4160),
-                                        ("ring_128k", 20000)])
+                                        ("ring_128k", 20000), ("128k_70b_layer", None)])
 def test_host_api_equals_device_api(name, chunk):
     import long_context_sparse_landmark_gb300.api as api
     wl = WORKLOADS[name]
