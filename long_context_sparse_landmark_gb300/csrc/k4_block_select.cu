@@ -21,15 +21,6 @@ namespace {
 constexpr int kSelThreads = 256;
 
 template <bool kBf16>
-__device__ __forceinline__ float ld_el(const void* base, int64_t idx) {
-  if constexpr (kBf16) {
-    return bf16_bits_to_float(static_cast<const uint16_t*>(base)[idx]);
-  } else {
-    return static_cast<const float*>(base)[idx];
-  }
-}
-
-template <bool kBf16>
 __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectArgs a) {
   constexpr int V = kBf16 ? 8 : 4;  // elements per 16-byte load
   extern __shared__ float ssm[];
@@ -90,17 +81,38 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectA
   }
 
   // Candidates: blocks l with (l+1)*bs <= r0 - w + 1.
+  // One thread per candidate: its landmark key row in 16-byte loads (all in
+  // flight at once), dotted with the query sum read as a shared-memory
+  // broadcast, in a fixed order.
   const int64_t n_cand = visible_landmarks(r0, a.window, a.block, a.G);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int64_t l = warp; l < n_cand; l += kSelThreads / 32) {
+  for (int64_t l = threadIdx.x; l < n_cand; l += blockDim.x) {
+    constexpr int ES = kBf16 ? 2 : 4;
+    const uint4* row = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.k_lm) +
+                                                      (l * a.Hkv + c) * static_cast<int64_t>(d) *
+                                                          ES);
     float s = 0.f;
-    for (int e = lane; e < d; e += 32)
-      s += qsum[e] * ld_el<kBf16>(a.k_lm, (l * a.Hkv + c) * static_cast<int64_t>(d) + e);
+#pragma unroll 4
+    for (int v0 = 0; v0 < d / V; ++v0) {
+      const uint4 x = __ldg(row + v0);
+      const float* qv = qsum + v0 * V;
+      if constexpr (kBf16) {
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        for (int k = 0; k < 4; ++k) {
+          s = fmaf(qv[2 * k], __uint_as_float(w[k] << 16), s);
+          s = fmaf(qv[2 * k + 1], __uint_as_float(w[k] & 0xffff0000u), s);
+        }
+      } else {
+        s = fmaf(qv[0], __uint_as_float(x.x), s);
+        s = fmaf(qv[1], __uint_as_float(x.y), s);
+        s = fmaf(qv[2], __uint_as_float(x.z), s);
+        s = fmaf(qv[3], __uint_as_float(x.w), s);
+      }
+    }
     // NaN ranks as -inf so that (score, index) stays a total order and
     // exactly min(top_k, n_cand) blocks are chosen.
-    if (lane == 0) score[l] = isnan(s) ? -INFINITY : s;
+    score[l] = isnan(s) ? -INFINITY : s;
   }
   __syncthreads();
 
