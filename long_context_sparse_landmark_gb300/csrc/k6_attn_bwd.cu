@@ -615,30 +615,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ----------------------------------------------------------- small kernels
 // Row statistics, stored negated for the packed FMAs that use them:
 // nL2[h, i] = -lse[h, i] log2(e) and nD[h, i] = -<dO[i, h], O[i, h]> for
-// i < n, -inf and 0 for the padding up to n_pad; one warp per (row, head),
-// 4 elements a lane.
+// i < n, -inf and 0 for the padding up to n_pad.  Eight lanes per (row,
+// head), 16 elements a lane from 16-byte loads, four pairs a warp.
 template <bool kOutBf16>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const void* out, const uint16_t* dout, const float* lse, float* L2,
                           float* D, int64_t n, int64_t n_pad, int Hq) {
-  const int64_t pair = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (pair >= n_pad * Hq) return;
+  const int64_t pair = static_cast<int64_t>(blockIdx.x) * 32 + (threadIdx.x >> 3);
+  const int sub = threadIdx.x & 7;  // lane within the pair's 8
+  if (pair >= n_pad * Hq) return;  // whole 8-lane groups leave together
   const int64_t i = pair / Hq;
   const int h = static_cast<int>(pair % Hq);
   float acc = 0.f;
   if (i < n) {
-    const int64_t base = pair * kD + lane * 4;
+    const int64_t base = pair * kD + sub * 16;
+    const uint4* g4 = reinterpret_cast<const uint4*>(dout + base);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float o = kOutBf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(out)[base + e])
-                               : static_cast<const float*>(out)[base + e];
-      acc = fmaf(o, bf16_bits_to_float(dout[base + e]), acc);
+    for (int half = 0; half < 2; ++half) {
+      const uint4 gv = __ldg(g4 + half);
+      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+      float o[8];
+      if constexpr (kOutBf16) {
+        const uint4 ov = __ldg(reinterpret_cast<const uint4*>(
+                                   static_cast<const uint16_t*>(out) + base) + half);
+        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          o[2 * k] = __uint_as_float(ow[k] << 16);
+          o[2 * k + 1] = __uint_as_float(ow[k] & 0xffff0000u);
+        }
+      } else {
+        const float4* o4 = reinterpret_cast<const float4*>(static_cast<const float*>(out) + base);
+        const float4 a = __ldg(o4 + 2 * half), b = __ldg(o4 + 2 * half + 1);
+        o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+        o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc = fmaf(o[2 * k], __uint_as_float(gw[k] << 16), acc);
+        acc = fmaf(o[2 * k + 1], __uint_as_float(gw[k] & 0xffff0000u), acc);
+      }
     }
+    // The 8 lanes of this pair take the same branches: reduce among them.
+    const unsigned gmask = 0xffu << (threadIdx.x & 24);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    for (int off = 4; off > 0; off >>= 1) acc += __shfl_xor_sync(gmask, acc, off);
   }
-  if (lane == 0) {
+  if (sub == 0) {
     const int64_t at = static_cast<int64_t>(h) * n_pad + i;
     D[at] = -acc;
     L2[at] = i < n ? -lse[static_cast<int64_t>(h) * n + i] * kLog2e : -INFINITY;
@@ -713,7 +736,7 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why) 
   p.wait_ns = a.wait_limit_ns;
 
   const int64_t pairs = a.n_pad * a.Hq;
-  const unsigned pre_blocks = static_cast<unsigned>((pairs + 7) / 8);
+  const unsigned pre_blocks = static_cast<unsigned>((pairs + 31) / 32);
   float* L2w = a.stats;
   float* Dw = a.stats + static_cast<int64_t>(a.Hq) * a.n_pad;
   if (a.out_bf16)
