@@ -290,3 +290,44 @@ def msa_attention_host(hq: torch.Tensor, hk: torch.Tensor, hv: torch.Tensor, win
         lse.copy_(dlse, non_blocking=True)
     s_out.synchronize()
     return out, lse
+
+
+class SparseLandmarkAttention(torch.nn.Module):
+    """Window + landmark attention as a module, configured like the pages'
+    Flash-MSA layer ("Scaling GPU Cluster for Million Token Context": a
+    local window and a number of global landmark tokens, set by the
+    SPARSE_WINDOW and SPARSE_GLOBAL_TOKENS environment variables in its
+    launch script).  ``window`` and ``num_global`` default to those
+    variables, else 4096 and 512.  Unlike the pages' sketch, which returns
+    the local and global contributions separately, the result is one
+    attention over both sets (one softmax, one lse).
+
+    forward(q, k, v): q [n, Hq, d] or [batch, n, Hq, d], k and v with Hkv
+    heads; num_global must divide n.  Differentiable (msa_attn_bwd) for bf16
+    inputs with d = 128 when gradients are required.
+    """
+
+    def __init__(self, window: int | None = None, num_global: int | None = None,
+                 scale: float | None = None):
+        super().__init__()
+        import os
+        self.window = int(os.environ.get("SPARSE_WINDOW", "4096")) if window is None else int(window)
+        self.num_global = (int(os.environ.get("SPARSE_GLOBAL_TOKENS", "512"))
+                           if num_global is None else int(num_global))
+        self.scale = scale
+        if self.window < 1 or self.num_global < 0:
+            raise ValueError("window must be >= 1 and num_global >= 0")
+
+    def _one(self, q, k, v):
+        n = q.shape[0]
+        if self.num_global and n % self.num_global != 0:
+            raise ValueError(f"num_global={self.num_global} must divide the sequence length {n}")
+        scale = 1.0 / math.sqrt(q.shape[2]) if self.scale is None else self.scale
+        if torch.is_grad_enabled() and (q.requires_grad or k.requires_grad or v.requires_grad):
+            return msa_attention_trainable(q, k, v, self.window, self.num_global, scale)
+        return msa_attention(q, k, v, self.window, self.num_global, scale)[0]
+
+    def forward(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> torch.Tensor:
+        if q.dim() == 3:
+            return self._one(q, k, v)
+        return torch.stack([self._one(q[b], k[b], v[b]) for b in range(q.shape[0])])

@@ -75,3 +75,25 @@ def test_host_api_equals_device_api(name, chunk):
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
     ho, hl = api.msa_attention_host(hq, hk, hv, wl.window, wl.G, wl.scale, chunk_rows=chunk)
     assert torch.equal(ho, ref_o.cpu()) and torch.equal(hl, ref_l.cpu())
+
+
+def test_module_batches_and_gradients():
+    """SparseLandmarkAttention over a batch of 2 equals per-sequence calls;
+    with gradients it runs the backward kernels."""
+    import long_context_sparse_landmark_gb300.api as api
+    from long_context_sparse_landmark_gb300 import SparseLandmarkAttention
+    wl = Workload("mod", 2048, 8, 2, 128, 300, 16, "bf16", seed=91)
+    qs, ks, vs = zip(*(generate(wl, device=DEV, seed=s) for s in (91, 92)))
+    q, k, v = (torch.stack(t) for t in (qs, ks, vs))
+    m = SparseLandmarkAttention(window=wl.window, num_global=wl.G)
+    with torch.no_grad():
+        out = m(q, k, v)
+    for b in range(2):
+        ref, _ = api.msa_attention(q[b], k[b], v[b], wl.window, wl.G)
+        assert torch.equal(out[b], ref)
+    qa = q.clone().requires_grad_(True)
+    out = m(qa, k, v)
+    out.float().sum().backward()
+    torch.cuda.synchronize()
+    assert qa.grad is not None and torch.isfinite(qa.grad.float()).all()
+    assert binding().device_status() == 0
