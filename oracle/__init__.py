@@ -359,6 +359,29 @@ def attn_bwd_dq_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarr
     return dq
 
 
+def attn_bwd_compressed(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray,
+                        window: int, block: int, global_rows, scale: float):
+    """Gradients (dQ, dK, dV, fp64) of sum <dout, O> for the compression-token
+    pattern of ``attn_compressed``.  The output of a global row does not
+    depend on the window or the compression tokens, and the other rows' do
+    not depend on the global rows' queries, so the gradient is the sum of
+    the window + compression-token backward with the global rows' dout set
+    to zero, and the causal (w = n, no landmarks) backward with only the
+    global rows' dout."""
+    n = q.shape[0]
+    rows = np.asarray(global_rows, dtype=np.int64)
+    is_global = np.zeros(n, dtype=bool)
+    is_global[rows] = True
+    zero = np.zeros_like(dout[:1])
+    d_local = np.where(is_global[:, None, None], zero, dout)
+    d_glob = np.where(is_global[:, None, None], dout, zero)
+    a = attn_bwd(q, k, v, np.ascontiguousarray(d_local), window, n // block, scale)
+    if rows.size == 0:
+        return a
+    b = attn_bwd(q, k, v, np.ascontiguousarray(d_glob), n, 0, scale)
+    return tuple(x + y for x, y in zip(a, b))
+
+
 def lse_merge(o_parts: np.ndarray, lse_parts: np.ndarray):
     """Merge P partials: o_parts [P, n, Hq, d], lse_parts [P, Hq, n] (fp64)."""
     o_parts = np.ascontiguousarray(o_parts, dtype=np.float64)

@@ -786,3 +786,46 @@ def test_bwd_dq_rows_match_full_backward(oracle_mod):
     rows = [0, 9, 10, 33, 63]
     np.testing.assert_array_equal(oracle_mod.attn_bwd_dq_rows(q, k, v, do, w, G, 0.3, rows),
                                   dq[rows])
+
+
+def compressed_torch_grads(q, k, v, dout, window, block, global_rows, scale):
+    """Autograd (fp64) through the dense mask of the compression-token
+    pattern, built element by element as in ``compressed_bruteforce``."""
+    tq = torch.tensor(q, dtype=torch.float64, requires_grad=True)
+    tk = torch.tensor(k, dtype=torch.float64, requires_grad=True)
+    tv = torch.tensor(v, dtype=torch.float64, requires_grad=True)
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv
+    C = n // block
+    gset = set(int(r) for r in global_rows)
+    mask = np.zeros((n, n + C), dtype=bool)
+    for i in range(n):
+        for j in range(n):
+            mask[i, j] = j <= i if i in gset else (i - window < j <= i)
+        if i not in gset:
+            for c in range(C):
+                mask[i, n + c] = (c + 1) * block - 1 <= i - window
+    kc = tk.reshape(C, block, Hkv, d).mean(dim=1)
+    vc = tv.reshape(C, block, Hkv, d).mean(dim=1)
+    keys, vals = torch.cat([tk, kc]), torch.cat([tv, vc])
+    m = torch.from_numpy(mask)
+    outs = []
+    for h in range(Hq):
+        s_ = (scale * tq[:, h] @ keys[:, h // g].T).masked_fill(~m, float("-inf"))
+        outs.append(torch.softmax(s_, dim=1) @ vals[:, h // g])
+    (torch.stack(outs, dim=1) * torch.from_numpy(dout.astype(np.float64))).sum().backward()
+    return tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+@pytest.mark.parametrize("n,block,w,glob", [(64, 4, 9, [5, 40, 63]), (48, 8, 1, [0, 47]),
+                                            (40, 2, 16, []), (96, 4, 20, list(range(0, 96, 7)))])
+def test_compressed_bwd_matches_dense_autograd(oracle_mod, n, block, w, glob):
+    rng = np.random.default_rng(n + 3 * block + w)
+    for (Hq, Hkv), d in itertools.product([(1, 1), (4, 2)], [4, 8]):
+        q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+        do = rng.standard_normal((n, Hq, d)).astype(np.float32)
+        ref = compressed_torch_grads(q, k, v, do, w, block, glob, 0.3)
+        got = oracle_mod.attn_bwd_compressed(q, k, v, do, w, block, glob, 0.3)
+        for g_, r_ in zip(got, ref):
+            np.testing.assert_allclose(g_, r_, rtol=0, atol=1e-11)
