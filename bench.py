@@ -470,6 +470,53 @@ def run_bwd(wl, steps, warmup, dev, B, torch):
     return e0.elapsed_time(e1) / steps
 
 
+def run_bwd_compressed(wl, steps, warmup, dev, B, torch):
+    """Backward of the compression-token pattern (msa_attn_bwd_global_rows)
+    on device-resident tensors; returns ms per call."""
+    from long_context_sparse_landmark_gb300.workloads import generate
+    q, k, v = generate(wl, device=dev)
+    k_lm = torch.empty((wl.G, wl.Hkv, wl.d), dtype=k.dtype, device=dev)
+    v_lm = torch.empty_like(k_lm)
+    out = torch.empty_like(q)
+    lse = torch.empty((wl.Hq, wl.n), dtype=torch.float32, device=dev)
+    rows = torch.as_tensor(wl.global_rows(), dtype=torch.int64, device=dev)
+    fws = torch.empty((B.global_rows_workspace_size(wl.n, rows.numel(), wl.Hq, wl.Hkv, wl.d),),
+                      dtype=torch.uint8, device=dev)
+    B.landmark_pool(k, v, k_lm, v_lm)
+    B.attn_fwd(q, k, v, k_lm, v_lm, out, lse, wl.window, wl.G, wl.scale)
+    B.attn_fwd_global_rows(q, k, v, rows, out, lse, wl.scale, fws)
+    del fws
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(8)
+    dout = torch.randn(q.shape, generator=gen, device=dev).to(torch.bfloat16)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    ws = torch.empty((B.attn_bwd_global_rows_workspace_size(wl.n, rows.numel(), wl.Hq, wl.Hkv,
+                                                            wl.d, wl.G),),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        B.attn_bwd_global_rows(q, k, v, k_lm, v_lm, out, lse, dout, rows, dq, dk, dv, wl.window,
+                               wl.G, wl.scale, ws, stream=stream)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert B.device_status() == 0
+    del q, k, v, out, lse, dout, dq, dk, dv, ws, k_lm, v_lm
+    torch.cuda.empty_cache()
+    return e0.elapsed_time(e1) / steps
+
+
 def cpu_baseline(wl, rows_target, torch):
     """The fp64 oracle on the host cores, on a bounded row sample of the
     same workload; extrapolated to the full layer by rows."""
@@ -704,6 +751,13 @@ def main():
                                   "pct_bf16_peak": round(100.0 * fbw / (bms * 1e-3) / 1e12
                                                          / peaks["bf16_tflops"], 2),
                                   "launches_per_step": 5, "steps": 3}
+        cms = run_bwd_compressed(wlc, 3, 1, dev, B, torch)
+        fcb = 2.5 * fc
+        also["bwd_compress_128k"] = {"ms_per_step": round(cms, 3),
+                                     "tflops": round(fcb / (cms * 1e-3) / 1e12, 2),
+                                     "pct_bf16_peak": round(100.0 * fcb / (cms * 1e-3) / 1e12
+                                                            / peaks["bf16_tflops"], 2),
+                                     "launches_per_step": 9, "steps": 3}
         wlr = WORKLOADS["ring_128k"]
         rr = run_ring(wlr, 3, 1, dev, B, torch)
         fr = useful_flops(wlr)

@@ -317,6 +317,40 @@ size_t msa_attn_bwd_workspace_size(int64_t n, int Hq, int Hkv, int d,
                                    int n_landmarks);
 
 /*
+ * Backward pass of the compression-token pattern: msa_attn_fwd (window +
+ * n_landmarks compression tokens) followed by msa_attn_fwd_global_rows on
+ * rows[0..n_global) -- the pattern the Block-Sparse Flash Attention
+ * paragraph of "Training at 1M+ Token Context" trains with.  A global row's
+ * output does not depend on the window or the compression tokens and the
+ * other rows' do not depend on the global rows' queries, so the gradients
+ * are those of msa_attn_bwd with the global rows given no weight, plus
+ * those of the global rows' causal attention (every key j <= the row):
+ * their dQ rows, and their dK / dV added into every key they see.
+ *   Arguments as msa_attn_bwd, plus rows / n_global as given to
+ *   msa_attn_fwd_global_rows (out and lse as both forward calls left
+ *   them); a repeated position counts once.
+ *   workspace: at least msa_attn_bwd_global_rows_workspace_size bytes.
+ * Errors: as msa_attn_bwd and msa_attn_fwd_global_rows; a position outside
+ * [0, n) is skipped and MSA_ERR_INVALID_ARG recorded in the device status
+ * word.
+ */
+msa_status msa_attn_bwd_global_rows(const void *q, const void *k, const void *v,
+                                    const void *k_lm, const void *v_lm,
+                                    const void *out, const float *lse,
+                                    const void *dout, const int64_t *rows,
+                                    int64_t n_global, void *dq, void *dk,
+                                    void *dv, int64_t n, int Hq, int Hkv, int d,
+                                    int64_t window, int n_landmarks, float scale,
+                                    msa_dtype in_dt, msa_dtype out_dt,
+                                    msa_dtype grad_dt, void *workspace,
+                                    size_t workspace_bytes, msa_stream_t stream);
+
+/* Bytes of workspace msa_attn_bwd_global_rows needs (0 for invalid sizes). */
+size_t msa_attn_bwd_global_rows_workspace_size(int64_t n, int64_t n_global,
+                                               int Hq, int Hkv, int d,
+                                               int n_landmarks);
+
+/*
  * One Ring Attention round's partial: queries at global positions
  * q_start .. q_start+n_q-1 against the contiguous KV chunk at global
  * positions kv_start .. kv_start+n_kv-1, with the causal window mask

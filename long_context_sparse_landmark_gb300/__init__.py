@@ -10,13 +10,15 @@ from .workloads import WORKLOADS, Workload, generate, sample_rows  # noqa: F401
 __all__ = ["WORKLOADS", "Workload", "generate", "sample_rows", "msa_attention",
            "ring_attention", "band_attention", "topk_attention", "compressed_attention", "landmarks",
            "msa_attention_backward", "msa_attention_trainable", "msa_attention_host",
+           "compressed_attention_backward",
            "SparseLandmarkAttention", "binding"]
 
 
 def __getattr__(name):
     if name in ("msa_attention", "ring_attention", "band_attention", "topk_attention",
                 "compressed_attention", "landmarks", "msa_attention_backward",
-                "msa_attention_trainable", "msa_attention_host", "SparseLandmarkAttention"):
+                "msa_attention_trainable", "msa_attention_host", "SparseLandmarkAttention",
+                "compressed_attention_backward"):
         from . import api
         return getattr(api, name)
     if name == "binding":

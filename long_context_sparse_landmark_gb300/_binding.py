@@ -24,7 +24,8 @@ EXPORTS = ("msa_version", "msa_last_error_string", "msa_landmark_pool", "msa_att
            "msa_attn_fwd_rows", "msa_attn_fwd_band", "msa_block_select", "msa_attn_fwd_select",
            "msa_attn_fwd_topk_workspace_size", "msa_attn_fwd_topk", "msa_attn_fwd_topk_noalloc",
            "msa_attn_fwd_global_rows", "msa_attn_fwd_global_rows_workspace_size",
-           "msa_attn_bwd", "msa_attn_bwd_workspace_size", "msa_attn_fwd_partial",
+           "msa_attn_bwd", "msa_attn_bwd_workspace_size", "msa_attn_bwd_global_rows",
+           "msa_attn_bwd_global_rows_workspace_size", "msa_attn_fwd_partial",
            "msa_attn_fwd_partial_merge", "msa_lse_merge",
            "msa_attn_uses_tensor_cores", "msa_device_status", "msa_debug_set_wait_limit_ns")
 
@@ -77,6 +78,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_attn_bwd.restype = i32
     lib.msa_attn_bwd_workspace_size.argtypes = [i64, i32, i32, i32, i32]
     lib.msa_attn_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.msa_attn_bwd_global_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp,
+                                             i64, i32, i32, i32, i64, i32, f32, i32, i32, i32,
+                                             vp, ctypes.c_size_t, vp]
+    lib.msa_attn_bwd_global_rows.restype = i32
+    lib.msa_attn_bwd_global_rows_workspace_size.argtypes = [i64, i64, i32, i32, i32, i32]
+    lib.msa_attn_bwd_global_rows_workspace_size.restype = ctypes.c_size_t
     lib.msa_attn_fwd_partial.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, i32,
                                          i64, f32, i32, vp]
     lib.msa_attn_fwd_partial.restype = i32
@@ -268,6 +275,28 @@ def attn_bwd(q, k, v, k_lm, v_lm, out, lse, dout, dq, dk, dv, window: int, n_lan
                              int(window), int(n_landmarks), float(scale), _dt(q), _dt(out),
                              _dt(dq), _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def attn_bwd_global_rows_workspace_size(n: int, n_global: int, Hq: int, Hkv: int, d: int,
+                                        n_landmarks: int) -> int:
+    return int(_lib.msa_attn_bwd_global_rows_workspace_size(n, n_global, Hq, Hkv, d,
+                                                            n_landmarks))
+
+
+def attn_bwd_global_rows(q, k, v, k_lm, v_lm, out, lse, dout, rows, dq, dk, dv, window: int,
+                         n_landmarks: int, scale: float, workspace: torch.Tensor,
+                         stream=None) -> None:
+    """msa_attn_bwd_global_rows: gradients of the compression-token pattern
+    (window + landmarks, then the global rows)."""
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if rows.dtype != torch.int64:
+        raise TypeError("rows must be int64")
+    _check(_lib.msa_attn_bwd_global_rows(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(k_lm), _ptr(v_lm), _ptr(out), _ptr(lse), _ptr(dout),
+        _ptr(rows), rows.numel(), _ptr(dq), _ptr(dk), _ptr(dv), n, Hq, Hkv, d, int(window),
+        int(n_landmarks), float(scale), _dt(q), _dt(out), _dt(dq), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def attn_fwd_partial(q, k_chunk, v_chunk, out_part, lse_part, q_start: int, kv_start: int,

@@ -162,6 +162,28 @@ def msa_attention_backward(q, k, v, out, lse, dout, window: int, n_landmarks: in
     return dq, dk, dv
 
 
+def compressed_attention_backward(q, k, v, out, lse, dout, window: int, block: int,
+                                  global_rows: torch.Tensor, scale: float | None = None,
+                                  grad_dtype: torch.dtype | None = None, stream=None):
+    """Gradients (dq, dk, dv) of sum <dout, out> for ``compressed_attention``
+    (whose out, lse are given): bf16 inputs, d = 128."""
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    G = n // block
+    k_lm, v_lm = landmarks(k, v, G, stream=stream)
+    gdt = grad_dtype or q.dtype
+    dq = torch.empty((n, Hq, d), dtype=gdt, device=q.device)
+    dk = torch.empty((n, Hkv, d), dtype=gdt, device=q.device)
+    dv = torch.empty_like(dk)
+    ws = torch.empty((B.attn_bwd_global_rows_workspace_size(n, global_rows.numel(), Hq, Hkv, d,
+                                                           G),),
+                     dtype=torch.uint8, device=q.device)
+    B.attn_bwd_global_rows(q, k, v, k_lm, v_lm, out, lse, dout.contiguous(), global_rows, dq,
+                           dk, dv, window, G, scale, ws, stream=stream)
+    return dq, dk, dv
+
+
 class _MSAAttention(torch.autograd.Function):
     """Window + landmark attention as a differentiable op (libmsa forward
     and backward kernels)."""

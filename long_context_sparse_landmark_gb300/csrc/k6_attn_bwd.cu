@@ -72,9 +72,10 @@ enum {
   BAR_CLEAN = 10,
   kNumBars = 11
 };
-// dK/dV: [2 stages][L2, D][128] fp32, bulk-copied: 128-byte aligned.
+// dK/dV: [2 stages][L2, D, positions][128] 4-byte values, bulk-copied:
+// 128-byte aligned (positions only in the gathered global-row mode).
 constexpr int kOffStats = (kOffBar + 8 * kNumBars + 127) / 128 * 128;
-constexpr int kStatBytes = 2 * kT * 4;  // one stage's L2 and D rows
+constexpr int kStatBytes = 3 * kT * 4;  // one stage's L2, D and position rows
 constexpr int kOffTmemSlot = kOffStats + 2 * kStatBytes;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemUsed = kOffAbort + 8;
@@ -89,7 +90,16 @@ struct BwdParams {
   void* dv;
   float* lm_part;     // [chunks][2][G][Hkv][d]
   const float* lm_grad;  // [2][G][Hkv][d]
-  int64_t n, n_pad, window, block;
+  // Gathered global-row mode (kernels instantiated with kG = true): the
+  // query side is the global rows,
+  // M row m = r * group + hh of KV head c at position gpos[m] (-1: padding),
+  // tm_q / tm_do map the gathered Qg / dOg [Mp][Hkv][d], L2 / D are
+  // [Hkv][Mp]; each row attends every key j <= its position.
+  const int* gpos;    // [Mp]
+  float* dq_part;     // [n_splits][Hkv][Mp][d]: dQ of the global rows per key split
+  float* extra_k;     // [n][Hkv][d]: the global rows' dK / dV, added by the
+  float* extra_v;     //   window pass (null outside the global-row backward)
+  int64_t n, n_pad, window, block, span, Mp;
   int Hq, Hkv, G, group, grad_bf16;
   int lm_mode, lm_chunks, chunk_tiles;
   float scale, scale_log2;
@@ -157,7 +167,8 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem, int warp) {
 
 // Producer: the fixed pair once, then `iters` ring pairs; `coord(it, &map_a,
 // &map_b, &y_a, &y_b, &row)` names the tensors and coordinates of pair it,
-// `stats(it, &l2, &d)` the statistics rows to copy with it (or none).
+// `stats(it, &l2, &d, &pos)` the statistics rows to copy with it (or none;
+// positions only in the gathered mode).
 template <typename Coord, typename Stats>
 __device__ __forceinline__ void produce(uint32_t sb, const CUtensorMap* fa, const CUtensorMap* fb,
                                         int fy, int frow, int iters, Coord coord, Stats stats,
@@ -176,12 +187,15 @@ __device__ __forceinline__ void produce(uint32_t sb, const CUtensorMap* fa, cons
     int ya, yb, row;
     coord(it, &ma, &mb, &ya, &yb, &row);
     const float *sl = nullptr, *sd = nullptr;
-    stats(it, &sl, &sd);
-    ptx::mbar_arrive_expect_tx(bar(BAR_FULL0 + b), 2 * kTileBytes + (sl ? kStatBytes : 0));
+    const int* sp = nullptr;
+    stats(it, &sl, &sd, &sp);
+    ptx::mbar_arrive_expect_tx(bar(BAR_FULL0 + b),
+                               2 * kTileBytes + (sl ? 2 * kT * 4 : 0) + (sp ? kT * 4 : 0));
     if (sl) {  // this stage's per-query lse and D rows (512 bytes each)
       const uint32_t dst = sb + kOffStats + b * kStatBytes;
       ptx::bulk_load(dst, sl, kT * 4, bar(BAR_FULL0 + b));
       ptx::bulk_load(dst + kT * 4, sd, kT * 4, bar(BAR_FULL0 + b));
+      if (sp) ptx::bulk_load(dst + 2 * kT * 4, sp, kT * 4, bar(BAR_FULL0 + b));
     }
     for (int ch = 0; ch < 2; ++ch) {
       ptx::tma_load_3d(sb + kOffRingA + b * kTileBytes + ch * kChunkBytes, ma,
@@ -271,6 +285,7 @@ __device__ __forceinline__ bool mma_pipeline(uint32_t sb, int iters, Scores scor
 // --------------------------------------------------------------------- dQ
 // CTA = (query tile, query head).  TMEM: S of key halves 0/1 at 0..63 /
 // 64..127 (dS over their first 32 columns), dP at 128..255, dQ 256..383.
+template <bool kG>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -278,16 +293,29 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
   const uint32_t sb = ptx::smem_u32(smem);
   auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8 * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t qr0 = static_cast<int64_t>(blockIdx.x) * kT;
-  const int h = blockIdx.y;
-  const int c = h / p.group;
-  // Key tiles: landmark tiles first, then the window tiles of the rows.
-  const int64_t q_last = min64(qr0 + kT, p.n) - 1;
-  const int64_t n_lm = visible_landmarks(q_last, p.window, p.block, p.G);
-  const int n_lm_tiles = static_cast<int>((n_lm + kT - 1) / kT);
-  const int64_t j_lo = max64(qr0 - p.window + 1, 0);
-  const int kt_lo = static_cast<int>(j_lo / kT);
-  const int T = n_lm_tiles + static_cast<int>(q_last / kT) - kt_lo + 1;
+  // Window mode: CTA (query tile, head); key tiles = landmark tiles, then the
+  // window tiles of the rows.  Gathered mode: CTA (key split, M tile, KV
+  // head); key tiles = the split's.
+  const int split = kG ? blockIdx.x : 0;
+  const int64_t qr0 = static_cast<int64_t>(kG ? blockIdx.y : blockIdx.x) * kT;
+  const int h = kG ? 0 : blockIdx.y;
+  const int c = kG ? blockIdx.z : h / p.group;
+  const int fy = kG ? c : h;  // head coordinate of the fixed Q / dO tiles
+  int n_lm_tiles, kt_lo, T;
+  if constexpr (kG) {
+    const int64_t key_lo = static_cast<int64_t>(split) * p.span;
+    const int64_t key_hi = min64(key_lo + p.span, p.n);
+    n_lm_tiles = 0;
+    kt_lo = static_cast<int>(key_lo / kT);
+    T = static_cast<int>((key_hi - key_lo + kT - 1) / kT);
+  } else {
+    const int64_t q_last = min64(qr0 + kT, p.n) - 1;
+    const int64_t n_lm = visible_landmarks(q_last, p.window, p.block, p.G);
+    n_lm_tiles = static_cast<int>((n_lm + kT - 1) / kT);
+    const int64_t j_lo = max64(qr0 - p.window + 1, 0);
+    kt_lo = static_cast<int>(j_lo / kT);
+    T = n_lm_tiles + static_cast<int>(q_last / kT) - kt_lo + 1;
+  }
 
   const uint32_t tmem = bwd_setup(smem, sb, warp);
   WaitCtl ctl{reinterpret_cast<volatile int*>(smem + kOffAbort), p.status, p.wait_ns};
@@ -302,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
         *ya = *yb = c;
         *row = lm ? t * kT : (kt_lo + t - n_lm_tiles) * kT;
       };
-      auto no_stats = [](int, const float**, const float**) {};
-      produce(sb, &p.tm_q, &p.tm_do, h, static_cast<int>(qr0), T, coord, no_stats, ctl,
+      auto no_stats = [](int, const float**, const float**, const int**) {};
+      produce(sb, &p.tm_q, &p.tm_do, fy, static_cast<int>(qr0), T, coord, no_stats, ctl,
               p.status);
     }
   } else if (warp == 5) {
@@ -328,10 +356,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
     }
   } else if (warp < 4) {
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int64_t i = qr0 + threadIdx.x;
-    const bool row_ok = i < p.n;
-    const float nL2 = p.L2[static_cast<int64_t>(h) * p.n_pad + i];
-    const float nD = p.D[static_cast<int64_t>(h) * p.n_pad + i];
+    const int64_t i_row = qr0 + threadIdx.x;  // query row, or gathered M row
+    // Position of the row (its own index outside the gathered mode).
+    const int64_t i = kG ? p.gpos[i_row] : i_row;
+    const bool row_ok = kG ? i >= 0 : i < p.n;
+    const int64_t st = kG ? static_cast<int64_t>(c) * p.Mp + i_row
+                               : static_cast<int64_t>(h) * p.n_pad + i_row;
+    const float nL2 = p.L2[st];
+    const float nD = p.D[st];
     const uint64_t c2 = ptx::f2(p.scale_log2, p.scale_log2);
     const uint64_t nL22 = ptx::f2(nL2, nL2);
     const uint64_t nD2 = ptx::f2(nD, nD);
@@ -345,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
         hi = my_lm - static_cast<int64_t>(t) * kT;
       } else {
         const int64_t kb = static_cast<int64_t>(kt_lo + t - n_lm_tiles) * kT;
-        lo = my_lo - kb;
+        lo = kG ? 0 : my_lo - kb;  // a global row sees every key j <= i
         hi = i - kb + 1;
       }
       if (!row_ok) hi = lo;
@@ -392,13 +424,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
     if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_ACC), 0, ctl));
     if (ok) {
       ptx::tc_fence_after();
-      const int64_t off = (i * p.Hq + h) * static_cast<int64_t>(kD);
+      // Gathered mode: this split's share of the row's dQ, fp32.
+      void* dst = kG ? static_cast<void*>(p.dq_part) : p.dq;
+      const int64_t off =
+          kG ? ((static_cast<int64_t>(split) * p.Hkv + c) * p.Mp + i_row) * kD
+                  : (i_row * p.Hq + h) * static_cast<int64_t>(kD);
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         float o[32];
         ptx::tmem_ld32(tl + 256 + cc * 32, o);
         ptx::tmem_wait_ld();
-        if (row_ok) store_row(p.dq, off + cc * 32, o, p.scale, p.grad_bf16);
+        if (row_ok) store_row(dst, off + cc * 32, o, p.scale, kG ? 0 : p.grad_bf16);
       }
     }
   }
@@ -409,6 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
 // CTA = (key tile or landmark tile, KV head[, query chunk]).  TMEM: S^T of
 // query halves 0/1 at 0..63 / 64..127 (P^T over their first 32 columns),
 // dP^T at 128..255 (dS^T likewise), dV 256..383, dK 384..511.
+template <bool kG>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -423,7 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t n_qt = (p.n + kT - 1) / kT;
   // Query tiles [qt_lo, qt_hi] whose rows see some key of the tile.
   int64_t qt_lo, qt_hi;
-  if (p.lm_mode) {
+  if constexpr (kG) {  // every M tile of the gathered global rows
+    qt_lo = 0;
+    qt_hi = p.Mp / kT - 1;
+  } else if (p.lm_mode) {
     const int64_t first_row = (kb + 1) * p.block + p.window - 1;  // sees landmark kb
     const int64_t base = first_row / kT;
     qt_lo = base + static_cast<int64_t>(chunk) * p.chunk_tiles;
@@ -432,7 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     qt_lo = kb / kT;
     qt_hi = min64(p.n - 1, kb + kT - 1 + p.window - 1) / kT;
   }
-  const int iters = qt_hi >= qt_lo ? static_cast<int>((qt_hi - qt_lo + 1) * p.group) : 0;
+  const int hpi = kG ? 1 : p.group;  // heads per query tile (M rows hold them in gmode)
+  const int iters = qt_hi >= qt_lo ? static_cast<int>((qt_hi - qt_lo + 1) * hpi) : 0;
   if (iters == 0) {  // landmark chunk beyond the last row: a zero partial
     if (p.lm_mode && threadIdx.x < kT && kb + threadIdx.x < p.G) {
       for (int which = 0; which < 2; ++which) {
@@ -453,14 +494,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                        int* row) {
         *ma = &p.tm_q;
         *mb = &p.tm_do;
-        *ya = *yb = c * p.group + it % p.group;
-        *row = static_cast<int>((qt_lo + it / p.group) * kT);
+        *ya = *yb = kG ? c : c * p.group + it % p.group;
+        *row = static_cast<int>((qt_lo + it / hpi) * kT);
       };
-      auto stats = [&](int it, const float** sl, const float** sd) {
-        const int64_t off = static_cast<int64_t>(c * p.group + it % p.group) * p.n_pad +
-                            (qt_lo + it / p.group) * kT;
+      auto stats = [&](int it, const float** sl, const float** sd, const int** sp) {
+        const int64_t row = (qt_lo + it / hpi) * kT;
+        const int64_t off = kG ? static_cast<int64_t>(c) * p.Mp + row
+                                    : static_cast<int64_t>(c * p.group + it % p.group) * p.n_pad +
+                                          row;
         *sl = p.L2 + off;
         *sd = p.D + off;
+        if (kG) *sp = p.gpos + row;
       };
       produce(sb, p.lm_mode ? &p.tm_klm : &p.tm_k, p.lm_mode ? &p.tm_vlm : &p.tm_v, c,
               static_cast<int>(kb), iters, coord, stats, ctl, p.status);
@@ -494,15 +538,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t c2 = ptx::f2(p.scale_log2, p.scale_log2);
     bool ok = true;
     for (int it = 0; ok && it < iters; ++it) {
-      const int64_t qr0 = (qt_lo + it / p.group) * kT;
+      const int64_t qr0 = (qt_lo + it / hpi) * kT;
       // This iteration's per-query -lse (log2 units) and -D came with its
       // Q / dO stage; the stage has landed once its scores exist, and it is
       // not refilled before this iteration's results are in.
       const float* sL = reinterpret_cast<const float*>(smem + kOffStats + (it & 1) * kStatBytes);
       const float* sD = sL + kT;
+      const int* sP = reinterpret_cast<const int*>(sD + kT);  // positions (gathered mode)
       // Rows i of this query tile that see key/landmark j: [lo, hi) columns.
       int64_t lo, hi;
-      if (p.lm_mode) {
+      if constexpr (kG) {  // per column below (each M row has its own position)
+        lo = 0;
+        hi = kT;
+      } else if (p.lm_mode) {
         lo = j < p.G ? (j + 1) * p.block + p.window - 1 - qr0 : kT;
         hi = kT;
       } else {
@@ -532,6 +580,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int col = cc * 32 + e;
               s[e] = (col >= lo_c && col < hi_c) ? s[e] : -INFINITY;
             }
+          }
+          if constexpr (kG) {  // global row m sees key j iff j <= its position
+            const int* hp = sP + half * kHalf + cc * 32;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s[e] = j <= hp[e] ? s[e] : -INFINITY;
           }
           uint32_t pp[16], dd[16];
 #pragma unroll
@@ -566,7 +619,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_ACC), 0, ctl));
     if (ok) {
       ptx::tc_fence_after();
-      if (p.lm_mode) {
+      if constexpr (kG) {  // the global rows' share of dK (scaled) and dV, fp32
+        const bool row_ok = j < p.n;
+        const int64_t off = (j * p.Hkv + c) * static_cast<int64_t>(kD);
+        for (int which = 0; which < 2; ++which) {
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            float o[32];
+            ptx::tmem_ld32(tl + (which == 0 ? 384 : 256) + cc * 32, o);
+            ptx::tmem_wait_ld();
+            if (row_ok)
+              store_row(which == 0 ? p.extra_k : p.extra_v, off + cc * 32, o,
+                        which == 0 ? p.scale : 1.f, 0);
+          }
+        }
+      } else if (p.lm_mode) {
         const bool row_ok = j < p.G;
         for (int which = 0; which < 2; ++which) {  // 0: dK_lm, 1: dV_lm
           float* dst = p.lm_part + ((((static_cast<int64_t>(chunk) * 2 + which) * p.G + j) *
@@ -602,6 +669,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lm) {
 #pragma unroll
               for (int e = 0; e < 32; ++e) o[e] = fmaf(lm[cc * 32 + e], invB / w, o[e]);
+            }
+            const float* ex = which == 0 ? p.extra_k : p.extra_v;
+            if (ex && row_ok) {  // the global rows' share (already scaled)
+              const float* exr = ex + off + cc * 32;
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] += exr[e] / w;
             }
             if (row_ok) store_row(which == 0 ? p.dk : p.dv, off + cc * 32, o, w, p.grad_bf16);
           }
@@ -678,6 +751,115 @@ __global__ void __launch_bounds__(256)
   grad[e] = s;
 }
 
+// True when global row r repeats an earlier row's position (its output is
+// that row's; only the first occurrence carries a gradient).
+__device__ __forceinline__ bool repeated_row(const int64_t* rows, int64_t r, int64_t pos) {
+  for (int64_t q = 0; q < r; ++q)
+    if (rows[q] == pos) return true;
+  return false;
+}
+
+// The window pass gives the global rows no weight: L2 = -inf, D = 0.
+__global__ void __launch_bounds__(256)
+    suppress_rows_kernel(const int64_t* rows, int64_t n_global, float* L2, float* D, int64_t n,
+                         int64_t n_pad, int Hq) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= n_global * Hq) return;
+  const int64_t pos = rows[idx / Hq];
+  const int h = static_cast<int>(idx % Hq);
+  if (pos < 0 || pos >= n) return;
+  L2[static_cast<int64_t>(h) * n_pad + pos] = -INFINITY;
+  D[static_cast<int64_t>(h) * n_pad + pos] = 0.f;
+}
+
+// One warp per (M row m, KV head c): Qg / dOg rows gathered from Q / dO at
+// the row's position (lanes 0-15 and 16-31, 16 bytes each), and its
+// statistics -lse log2(e) and -<dO, O>; padding, repeated and invalid
+// rows (the latter reported) get position -1 and no weight.
+template <bool kOutBf16>
+__global__ void __launch_bounds__(256)
+    gather_rows_kernel(const uint16_t* q, const uint16_t* dout, const void* out,
+                       const float* lse, const int64_t* rows, int64_t Mc, int64_t Mp, int64_t n,
+                       int Hq, int Hkv, int group, uint16_t* Qg, uint16_t* dOg, float* gL2,
+                       float* gD, int* gpos, int* status) {
+  const int64_t pair = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (pair >= Mp * Hkv) return;
+  const int64_t m = pair / Hkv;
+  const int c = static_cast<int>(pair % Hkv);
+  int64_t pos = -1;
+  if (m < Mc) {
+    const int64_t r = m / group;
+    pos = rows[r];
+    if (pos < 0 || pos >= n) {
+      if (lane == 0) record_status(status, MSA_ERR_INVALID_ARG);
+      pos = -1;
+    } else if (repeated_row(rows, r, pos)) {
+      pos = -1;
+    }
+  }
+  const int h = c * group + static_cast<int>(m % group);
+  const int64_t dst = (m * Hkv + c) * kD;
+  const int half = lane >> 4;
+  uint4* gdst = reinterpret_cast<uint4*>((half ? dOg : Qg) + dst) + (lane & 15);
+  float acc = 0.f;
+  if (pos >= 0) {
+    const int64_t src = (pos * Hq + h) * kD;
+    *gdst = __ldg(reinterpret_cast<const uint4*>((half ? dout : q) + src) + (lane & 15));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int64_t at = src + lane * 4 + e;
+      const float o = kOutBf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(out)[at])
+                               : static_cast<const float*>(out)[at];
+      acc = fmaf(o, bf16_bits_to_float(dout[at]), acc);
+    }
+  } else {
+    *gdst = make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    gL2[static_cast<int64_t>(c) * Mp + m] =
+        pos >= 0 ? -lse[static_cast<int64_t>(h) * n + pos] * kLog2e : -INFINITY;
+    gD[static_cast<int64_t>(c) * Mp + m] = -acc;
+    if (c == 0) gpos[m] = static_cast<int>(pos);
+  }
+}
+
+// One warp per (global row, query head): its dQ = the sum of the key
+// splits' shares up to its position, written to row pos of dq.
+__global__ void __launch_bounds__(256)
+    dq_scatter_kernel(const float* dq_part, const int64_t* rows, int64_t n_global, int64_t Mp,
+                      int n_splits, int64_t span, int64_t n, int Hq, int Hkv, int group, void* dq,
+                      int grad_bf16) {
+  const int64_t pair = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (pair >= n_global * Hq) return;
+  const int64_t r = pair / Hq;
+  const int h = static_cast<int>(pair % Hq);
+  const int64_t pos = rows[r];
+  if (pos < 0 || pos >= n || repeated_row(rows, r, pos)) return;
+  const int c = h / group;
+  const int64_t m = r * group + h % group;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int sp = 0; sp < n_splits && static_cast<int64_t>(sp) * span <= pos; ++sp) {
+    const float4 x = *reinterpret_cast<const float4*>(
+        dq_part + ((static_cast<int64_t>(sp) * Hkv + c) * Mp + m) * kD + lane * 4);
+    acc[0] += x.x;
+    acc[1] += x.y;
+    acc[2] += x.z;
+    acc[3] += x.w;
+  }
+  const int64_t off = (pos * Hq + h) * kD + lane * 4;
+  if (grad_bf16) {
+    __nv_bfloat16* d = static_cast<__nv_bfloat16*>(dq) + off;
+    for (int e = 0; e < 4; ++e) d[e] = __float2bfloat16_rn(acc[e]);
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(dq) + off) =
+        make_float4(acc[0], acc[1], acc[2], acc[3]);
+  }
+}
+
 }  // namespace
 
 bool attn_bwd_supported(int d, int in_bf16) { return in_bf16 && d == kD; }
@@ -747,15 +929,53 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why) 
         a.out, static_cast<const uint16_t*>(a.dout), a.lse, L2w, Dw, a.n, a.n_pad, a.Hq);
   cudaError_t e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
-  for (auto* k : {bwd_dkdv_tc_kernel, bwd_dq_tc_kernel}) {
+  for (auto* k : {bwd_dkdv_tc_kernel<false>, bwd_dq_tc_kernel<false>, bwd_dkdv_tc_kernel<true>,
+                  bwd_dq_tc_kernel<true>}) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
   }
   const unsigned n_tiles = static_cast<unsigned>((a.n + kT - 1) / kT);
+  const int group = a.Hq / a.Hkv;
+  BwdParams pg;  // the gathered global-row launches
+  if (a.rows) {
+    suppress_rows_kernel<<<static_cast<unsigned>((a.n_global * a.Hq + 255) / 256), 256, 0, s>>>(
+        a.rows, a.n_global, L2w, Dw, a.n, a.n_pad, a.Hq);
+    const unsigned gblocks = static_cast<unsigned>((a.Mp * a.Hkv + 7) / 8);
+    if (a.out_bf16)
+      gather_rows_kernel<true><<<gblocks, 256, 0, s>>>(
+          static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.dout), a.out, a.lse,
+          a.rows, a.Mc, a.Mp, a.n, a.Hq, a.Hkv, group, static_cast<uint16_t*>(a.Qg),
+          static_cast<uint16_t*>(a.dOg), a.gL2, a.gD, a.gpos, a.status);
+    else
+      gather_rows_kernel<false><<<gblocks, 256, 0, s>>>(
+          static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.dout), a.out, a.lse,
+          a.rows, a.Mc, a.Mp, a.n, a.Hq, a.Hkv, group, static_cast<uint16_t*>(a.Qg),
+          static_cast<uint16_t*>(a.dOg), a.gL2, a.gD, a.gpos, a.status);
+    e = cudaPeekAtLastError();
+    if (e != cudaSuccess) return e;
+    pg = p;
+    if (!encode_map(fn, &pg.tm_q, a.Qg, a.Mp, a.Hkv) ||
+        !encode_map(fn, &pg.tm_do, a.dOg, a.Mp, a.Hkv)) {
+      *why = "cuTensorMapEncodeTiled rejected the gathered rows";
+      return cudaErrorInvalidValue;
+    }
+    pg.L2 = a.gL2;
+    pg.D = a.gD;
+    pg.gpos = a.gpos;
+    pg.Mp = a.Mp;
+    pg.span = a.span;
+    pg.dq_part = a.dq_part;
+    pg.extra_k = a.extra_k;
+    pg.extra_v = a.extra_v;
+    // The global rows' dK / dV first: the window pass adds them in.
+    bwd_dkdv_tc_kernel<true><<<dim3(n_tiles, a.Hkv, 1), kThreads, kSmemBytes, s>>>(pg);
+    e = cudaPeekAtLastError();
+    if (e != cudaSuccess) return e;
+  }
   if (a.G > 0) {
     p.lm_mode = 1;
     dim3 grid(static_cast<unsigned>((a.G + kT - 1) / kT), a.Hkv, a.lm_chunks);
-    bwd_dkdv_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+    bwd_dkdv_tc_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
     e = cudaPeekAtLastError();
     if (e != cudaSuccess) return e;
     const int64_t per_chunk = 2 * static_cast<int64_t>(a.G) * a.Hkv * kD;
@@ -765,10 +985,22 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why) 
     if (e != cudaSuccess) return e;
   }
   p.lm_mode = 0;
-  bwd_dkdv_tc_kernel<<<dim3(n_tiles, a.Hkv, 1), kThreads, kSmemBytes, s>>>(p);
+  p.extra_k = a.rows ? a.extra_k : nullptr;
+  p.extra_v = a.rows ? a.extra_v : nullptr;
+  bwd_dkdv_tc_kernel<false><<<dim3(n_tiles, a.Hkv, 1), kThreads, kSmemBytes, s>>>(p);
   e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
-  bwd_dq_tc_kernel<<<dim3(n_tiles, a.Hq), kThreads, kSmemBytes, s>>>(p);
+  bwd_dq_tc_kernel<false><<<dim3(n_tiles, a.Hq), kThreads, kSmemBytes, s>>>(p);
+  e = cudaPeekAtLastError();
+  if (e != cudaSuccess || !a.rows) return e;
+  // The global rows' dQ: per key split, then summed into their rows.
+  bwd_dq_tc_kernel<true><<<dim3(a.n_splits, static_cast<unsigned>(a.Mp / kT), a.Hkv),
+                           kThreads, kSmemBytes, s>>>(pg);
+  e = cudaPeekAtLastError();
+  if (e != cudaSuccess) return e;
+  dq_scatter_kernel<<<static_cast<unsigned>((a.n_global * a.Hq + 7) / 8), 256, 0, s>>>(
+      a.dq_part, a.rows, a.n_global, a.Mp, a.n_splits, a.span, a.n, a.Hq, a.Hkv, group, a.dq,
+      a.grad_bf16);
   return cudaPeekAtLastError();
 }
 

@@ -605,17 +605,62 @@ static msa_status check_bwd_sizes(int64_t n, int Hq, int Hkv, int d, int G) {
   return MSA_OK;
 }
 
+// Extra workspace of msa_attn_bwd_global_rows after the msa_attn_bwd part:
+// gathered Qg / dOg, their statistics and positions, the per-split dQ
+// shares and the global rows' dK / dV; key splits as for the forward's
+// global rows (about one wave of CTAs).
+struct BwdGrPlan {
+  int64_t Mc, Mp, span;
+  int n_splits;
+  size_t qg, dog, gl2, gd, gpos, dq_part, extra_k, extra_v, total;
+};
+
+static BwdGrPlan bwd_gr_plan(size_t base, int64_t n, int64_t n_global, int Hq, int Hkv, int d) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  BwdGrPlan P{};
+  P.Mc = n_global * (Hq / Hkv);
+  P.Mp = (P.Mc + 127) / 128 * 128;
+  const int64_t tiles = (n + 127) / 128;
+  const int64_t per_split = (P.Mp / 128) * Hkv;
+  int64_t S = (152 + per_split - 1) / per_split;
+  S = S < 1 ? 1 : (S > tiles ? tiles : S);
+  const int64_t span_tiles = (tiles + S - 1) / S;
+  P.span = span_tiles * 128;
+  P.n_splits = static_cast<int>((tiles + span_tiles - 1) / span_tiles);
+  const size_t rows_bytes = static_cast<size_t>(P.Mp) * Hkv * d * 2;
+  size_t at = up(base);
+  P.qg = at;
+  at += up(rows_bytes);
+  P.dog = at;
+  at += up(rows_bytes);
+  P.gl2 = at;
+  at += up(static_cast<size_t>(Hkv) * P.Mp * 4);
+  P.gd = at;
+  at += up(static_cast<size_t>(Hkv) * P.Mp * 4);
+  P.gpos = at;
+  at += up(static_cast<size_t>(P.Mp) * 4);
+  P.dq_part = at;
+  at += up(static_cast<size_t>(P.n_splits) * Hkv * P.Mp * d * 4);
+  P.extra_k = at;
+  at += up(static_cast<size_t>(n) * Hkv * d * 4);
+  P.extra_v = at;
+  at += up(static_cast<size_t>(n) * Hkv * d * 4);
+  P.total = at;
+  return P;
+}
+
 size_t msa_attn_bwd_workspace_size(int64_t n, int Hq, int Hkv, int d, int n_landmarks) {
   if (check_bwd_sizes(n, Hq, Hkv, d, n_landmarks) != MSA_OK) return 0;
   return bwd_plan(n, Hq, Hkv, d, n_landmarks).total;
 }
 
-msa_status msa_attn_bwd(const void* q, const void* k, const void* v, const void* k_lm,
-                        const void* v_lm, const void* out, const float* lse, const void* dout,
-                        void* dq, void* dk, void* dv, int64_t n, int Hq, int Hkv, int d,
-                        int64_t window, int n_landmarks, float scale, msa_dtype in_dt,
-                        msa_dtype out_dt, msa_dtype grad_dt, void* workspace,
-                        size_t workspace_bytes, msa_stream_t stream) {
+static msa_status attn_bwd_impl(const void* q, const void* k, const void* v, const void* k_lm,
+                                const void* v_lm, const void* out, const float* lse,
+                                const void* dout, const int64_t* rows, int64_t n_global, void* dq,
+                                void* dk, void* dv, int64_t n, int Hq, int Hkv, int d,
+                                int64_t window, int n_landmarks, float scale, msa_dtype in_dt,
+                                msa_dtype out_dt, msa_dtype grad_dt, void* workspace,
+                                size_t workspace_bytes, msa_stream_t stream) {
   msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, window, scale, in_dt);
   if (st != MSA_OK) return st;
   if (!dout || !dq || !dk || !dv) return fail(MSA_ERR_INVALID_ARG, "null gradient pointer");
@@ -632,12 +677,19 @@ msa_status msa_attn_bwd(const void* q, const void* k, const void* v, const void*
     if (!aligned16(k_lm) || !aligned16(v_lm))
       return fail(MSA_ERR_INVALID_ARG, "landmark pointer not 16-byte aligned");
   }
+  if (rows) {
+    if ((reinterpret_cast<uintptr_t>(rows) & 7u) != 0)
+      return fail(MSA_ERR_INVALID_ARG, "rows must be 8-byte aligned");
+    st = check_global_rows(n, n_global, Hq, Hkv);
+    if (st != MSA_OK) return st;
+  }
   const BwdPlan P = bwd_plan(n, Hq, Hkv, d, n_landmarks);
+  const BwdGrPlan R = rows ? bwd_gr_plan(P.total, n, n_global, Hq, Hkv, d) : BwdGrPlan{};
+  const size_t need = rows ? R.total : P.total;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(MSA_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
-  if (workspace_bytes < P.total)
-    return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
-                P.total);
+  if (workspace_bytes < need)
+    return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   msa::BwdArgs a{};
   a.q = q;
@@ -665,6 +717,22 @@ msa_status msa_attn_bwd(const void* q, const void* k, const void* v, const void*
   a.grad_bf16 = grad_dt == MSA_BF16;
   a.lm_chunks = P.lm_chunks;
   a.chunk_tiles = P.chunk_tiles;
+  if (rows) {
+    a.rows = rows;
+    a.n_global = n_global;
+    a.Mc = R.Mc;
+    a.Mp = R.Mp;
+    a.span = R.span;
+    a.n_splits = R.n_splits;
+    a.Qg = ws + R.qg;
+    a.dOg = ws + R.dog;
+    a.gL2 = reinterpret_cast<float*>(ws + R.gl2);
+    a.gD = reinterpret_cast<float*>(ws + R.gd);
+    a.gpos = reinterpret_cast<int*>(ws + R.gpos);
+    a.dq_part = reinterpret_cast<float*>(ws + R.dq_part);
+    a.extra_k = reinterpret_cast<float*>(ws + R.extra_k);
+    a.extra_v = reinterpret_cast<float*>(ws + R.extra_v);
+  }
   st = device_status_ptr(&a.status);
   if (st != MSA_OK) return st;
   const uint64_t lim = g_wait_limit_ns.load();
@@ -673,6 +741,39 @@ msa_status msa_attn_bwd(const void* q, const void* k, const void* v, const void*
   cudaError_t e = msa::launch_attn_bwd(a, reinterpret_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess && why) return fail(MSA_ERR_CUDA, "backward: %s", why);
   return launched(e, "backward");
+}
+
+msa_status msa_attn_bwd(const void* q, const void* k, const void* v, const void* k_lm,
+                        const void* v_lm, const void* out, const float* lse, const void* dout,
+                        void* dq, void* dk, void* dv, int64_t n, int Hq, int Hkv, int d,
+                        int64_t window, int n_landmarks, float scale, msa_dtype in_dt,
+                        msa_dtype out_dt, msa_dtype grad_dt, void* workspace,
+                        size_t workspace_bytes, msa_stream_t stream) {
+  return attn_bwd_impl(q, k, v, k_lm, v_lm, out, lse, dout, nullptr, 0, dq, dk, dv, n, Hq, Hkv,
+                       d, window, n_landmarks, scale, in_dt, out_dt, grad_dt, workspace,
+                       workspace_bytes, stream);
+}
+
+size_t msa_attn_bwd_global_rows_workspace_size(int64_t n, int64_t n_global, int Hq, int Hkv,
+                                               int d, int n_landmarks) {
+  if (check_bwd_sizes(n, Hq, Hkv, d, n_landmarks) != MSA_OK ||
+      check_global_rows(n, n_global, Hq, Hkv) != MSA_OK)
+    return 0;
+  return bwd_gr_plan(bwd_plan(n, Hq, Hkv, d, n_landmarks).total, n, n_global, Hq, Hkv, d).total;
+}
+
+msa_status msa_attn_bwd_global_rows(const void* q, const void* k, const void* v,
+                                    const void* k_lm, const void* v_lm, const void* out,
+                                    const float* lse, const void* dout, const int64_t* rows,
+                                    int64_t n_global, void* dq, void* dk, void* dv, int64_t n,
+                                    int Hq, int Hkv, int d, int64_t window, int n_landmarks,
+                                    float scale, msa_dtype in_dt, msa_dtype out_dt,
+                                    msa_dtype grad_dt, void* workspace, size_t workspace_bytes,
+                                    msa_stream_t stream) {
+  if (!rows) return fail(MSA_ERR_INVALID_ARG, "null rows pointer");
+  return attn_bwd_impl(q, k, v, k_lm, v_lm, out, lse, dout, rows, n_global, dq, dk, dv, n, Hq,
+                       Hkv, d, window, n_landmarks, scale, in_dt, out_dt, grad_dt, workspace,
+                       workspace_bytes, stream);
 }
 
 msa_status msa_attn_fwd_partial(const void* q, const void* k_chunk, const void* v_chunk,

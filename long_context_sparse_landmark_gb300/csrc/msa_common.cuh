@@ -196,6 +196,21 @@ struct BwdArgs {
   int lm_chunks, chunk_tiles;
   int* status;
   uint64_t wait_limit_ns;
+  // Global rows (compression-token pattern; null: none).  Mc = n_global *
+  // (Hq / Hkv) gathered M rows, padded to Mp (a multiple of 128); Qg / dOg
+  // [Mp][Hkv][d] bf16, gL2 / gD [Hkv][Mp], gpos [Mp]; dq_part
+  // [n_splits][Hkv][Mp][d] and extra_k / extra_v [n][Hkv][d] fp32.
+  const int64_t* rows;
+  int64_t n_global, Mc, Mp, span;
+  int n_splits;
+  void* Qg;
+  void* dOg;
+  float* gL2;
+  float* gD;
+  int* gpos;
+  float* dq_part;
+  float* extra_k;
+  float* extra_v;
 };
 bool attn_bwd_supported(int d, int in_bf16);
 cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why);

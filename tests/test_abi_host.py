@@ -307,3 +307,24 @@ def test_rows_validation(lib):
     assert call(klm=None) == 1
     assert call(G=7) == 1
     assert call(d=80) == 2
+
+
+def test_global_rows_backward_validation(lib):
+    size = lib.msa_attn_bwd_global_rows_workspace_size
+    need = size(1024, 4, 8, 2, 128, 32)
+    assert need > lib.msa_attn_bwd_workspace_size(1024, 8, 2, 128, 32) > 0
+    assert size(1024, 0, 8, 2, 128, 32) == 0
+    f = lib.msa_attn_bwd_global_rows
+
+    def call(**kw):
+        a = dict(rows=GOOD, ng=4, ws=GOOD, wsb=need, d=128, idt=1)
+        a.update(kw)
+        return f(GOOD, GOOD, GOOD, GOOD, GOOD, GOOD, GOOD, GOOD, a["rows"], a["ng"], GOOD, GOOD,
+                 GOOD, 1024, 8, 2, a["d"], 64, 32, ctypes.c_float(0.1), a["idt"], 0, 0, a["ws"],
+                 a["wsb"], None)
+
+    assert call(rows=None) == 1
+    assert call(rows=P((1 << 20) + 4)) == 1
+    assert call(ng=0) == 1
+    assert call(wsb=need - 1) == 1
+    assert call(idt=0) == 2

@@ -163,3 +163,60 @@ def test_backward_128k_layer_properties_and_sampled_dq():
     rq = oracle.attn_bwd_dq_rows(to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v),
                                  to_numpy_bits(do), wl.window, wl.G, wl.scale, rows)
     rel_compare(gq, rq, "128K dQ (sampled)")
+
+
+# ------------------------------------------------------------ compression-token pattern
+def gpu_compressed_backward(q, k, v, do, w, block, rows, grad_dtype=torch.float32):
+    import long_context_sparse_landmark_gb300.api as api
+    r = torch.as_tensor(rows, dtype=torch.int64, device=DEV)
+    out, lse = api.compressed_attention(q, k, v, w, block, r, out_dtype=torch.float32)
+    grads = api.compressed_attention_backward(q, k, v, out, lse, do, w, block, r,
+                                              grad_dtype=grad_dtype)
+    torch.cuda.synchronize()
+    assert binding().device_status() == 0
+    return grads
+
+
+@pytest.mark.parametrize("n,Hq,Hkv,w,block,rows", [
+    (2048, 8, 2, 300, 32, [499, 999, 1499, 1999]),
+    (1024, 4, 1, 100, 16, [0, 511, 1023, 300, 300]),
+    (4096, 16, 2, 1024, 32, [1023, 2047, 3071, 4095]),
+    (640, 4, 4, 64, 32, [639]),
+])
+def test_compressed_backward_parity(n, Hq, Hkv, w, block, rows):
+    wl = Workload("cbwd", n, Hq, Hkv, 128, w, n // block, "bf16", seed=n + len(rows))
+    q, k, v = generate(wl, device=DEV)
+    do = make_dout(wl, seed=n + 7)
+    dq, dk, dv = gpu_compressed_backward(q, k, v, do, w, block, rows)
+    rq, rk, rv = oracle.attn_bwd_compressed(to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v),
+                                            to_numpy_bits(do), w, block, np.unique(rows),
+                                            wl.scale)
+    rel_compare(dq.cpu().numpy(), rq, f"compressed dQ {wl}")
+    rel_compare(dk.cpu().numpy(), rk, f"compressed dK {wl}")
+    rel_compare(dv.cpu().numpy(), rv, f"compressed dV {wl}")
+
+
+def test_compress_128k_backward_properties_and_sampled_dq():
+    """The 128K compression workload: ΣdV = ΣdO and ΣdK = 0 at full size;
+    dQ on sampled rows (all global rows among them) against the oracle."""
+    from long_context_sparse_landmark_gb300.workloads import WORKLOADS
+    wl = WORKLOADS["compress_128k"]
+    q, k, v = generate(wl, device=DEV)
+    do = make_dout(wl, seed=1282)
+    glob = wl.global_rows()
+    dq, dk, dv = gpu_compressed_backward(q, k, v, do, wl.window, wl.block, glob)
+    g = wl.Hq // wl.Hkv
+    do4 = do.double().reshape(wl.n, wl.Hkv, g, wl.d)
+    bound_v = 2.0 ** -8 * do4.abs().sum(dim=(0, 2))
+    assert torch.all((dv.double().sum(dim=0) - do4.sum(dim=(0, 2))).abs() <= bound_v), "sum of dV"
+    assert torch.all(dk.double().sum(dim=0).abs() <= 2.0 ** -6 * dk.double().abs().sum(dim=0))
+    rows = np.union1d(sample_rows(wl, count=128).numpy(), glob)
+    idx = torch.as_tensor(rows, device=DEV)
+    gq = dq.index_select(0, idx).cpu().numpy()
+    del dq, dk, dv
+    qn, kn, vn, dn = (to_numpy_bits(t) for t in (q, k, v, do))
+    is_g = np.isin(rows, glob)
+    ref = np.empty_like(gq, dtype=np.float64)
+    ref[~is_g] = oracle.attn_bwd_dq_rows(qn, kn, vn, dn, wl.window, wl.G, wl.scale, rows[~is_g])
+    ref[is_g] = oracle.attn_bwd_dq_rows(qn, kn, vn, dn, wl.n, 0, wl.scale, rows[is_g])
+    rel_compare(gq, ref, "compress 128K dQ (sampled + global rows)")
