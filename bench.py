@@ -51,7 +51,7 @@ def load_peaks():
 # k2_attn_tc.cu); after any change the traffic is reported as null.
 ATTN_TRAFFIC = {"128k_70b_layer": {
     "bytes": 2.704536e9 + 2.141867e9,
-    "kernel_sha256": "e711af4599a96daa93891cce7463421cb01b18bdb6b519b5f43847f9b3902df1"}}
+    "kernel_sha256": "e167d44158e7b7aa069f73cd4874c5e66f5c8755f51d5af0cf7b48329263fc32"}}
 
 
 def kernel_sha256() -> str:

@@ -203,8 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
   // Register budget: the producer/MMA warpgroup needs few registers, the
   // two softmax warpgroups hold a 128-score row each.  Launch allocation is
-  // 384 x 168; 128 x 96 + 256 x 200 fits in it with no spills.  Each role
-  // raises or lowers its own budget inside its branch.
+  // 384 x 168; 128 x 96 + 256 x 200 fits in it.  At 200 the softmax keeps a
+  // 12-byte spill (3 stores, 1 reload) that only 232 would remove, which
+  // would starve the producer; the MMA issue rate, not the softmax, bounds
+  // this kernel.  Each role raises or lowers its own budget inside its branch.
   if (warp < 4) {
     ptx::reg_dealloc<96>();
   }
