@@ -25,15 +25,20 @@
 //   5. bwd_dq_tc_kernel: per (128-row query tile, head) over the landmark
 //      and window key tiles, as the forward.
 // Each tensor-core kernel: warps 0-3 elementwise (one TMEM lane = one row
-// each), warp 4 TMA producer, warp 5 TMEM allocation and MMA issue.  Every
-// 128-column tile is handled as two 64-column halves with their own TMEM
-// columns: the score-like MMAs of a half land, the elementwise warps turn
-// them into bf16 P / dS in the same columns, the half's gradient MMAs
-// accumulate in TMEM and the next tile's scores of that half follow at
-// once -- so the tensor pipe works on one half while the warps process the
-// other (tcgen05 MMAs from one thread execute in issue order, which makes
-// overwriting a half's columns after its gradient MMAs safe).  Every wait
-// is bounded; a wait that runs out aborts the CTA cleanly.
+// each), warp 4 TMA producer, warp 5 TMEM allocation and MMA issue.
+// tcgen05 MMAs from one thread execute in issue order, which makes
+// overwriting TMEM columns after the MMAs that read them safe.
+//   dK/dV: TMEM holds two accumulators, so every 128-column tile is handled
+//   as two 64-column halves with their own columns: the score-like MMAs of
+//   a half land, the elementwise warps turn them into bf16 P / dS in the
+//   same columns, the half's gradient MMAs accumulate in TMEM and the next
+//   tile's scores of that half follow at once -- the tensor pipe works on
+//   one half while the warps process the other.
+//   dQ: one accumulator leaves room for two full-width S buffers, so the
+//   next tile's S is computed during the elementwise pass and only its dP
+//   waits for the pass; K and V come through separate rings (three K
+//   stages, since K is read until the late dQ MMAs).
+// Every wait is bounded; a wait that runs out aborts the CTA cleanly.
 #include <cuda.h>
 #include <math.h>
 #include <string.h>
@@ -283,15 +288,175 @@ __device__ __forceinline__ bool mma_pipeline(uint32_t sb, int iters, Scores scor
 }
 
 // --------------------------------------------------------------------- dQ
-// CTA = (query tile, query head).  TMEM: S of key halves 0/1 at 0..63 /
-// 64..127 (dS over their first 32 columns), dP at 128..255, dQ 256..383.
+// The dQ kernel keeps one accumulator (dQ), so its 512 TMEM columns hold two
+// full-width score buffers and dP besides: S of even / odd key tiles at
+// 0..127 / 128..255 (dS over the first 64 columns of its tile's S), dQ at
+// 256..383, dP at 384..511.  Score MMAs are full width (N = 128).
+__device__ __forceinline__ uint32_t dq_col_s(int t) { return static_cast<uint32_t>(t & 1) * 128; }
+constexpr uint32_t kDqColQ = 256;
+constexpr uint32_t kDqColP = 384;
+
+// Shared memory of the dQ kernel: Q and dO (fixed), then separate K and V
+// rings -- K(t) is read until dQ(t), late in the pipeline, V(t) only by
+// dP(t), so K gets three stages and V two (224 KB of tiles in all).
+constexpr int kDqKStages = 3;
+constexpr int kDqVStages = 2;
+constexpr int kDqOffK = 2 * kTileBytes;
+constexpr int kDqOffV = kDqOffK + kDqKStages * kTileBytes;
+constexpr int kDqOffBar = kDqOffV + kDqVStages * kTileBytes;
+enum {
+  DQ_FIX = 0,      // Q, dO landed
+  DQ_FULLK0 = 1,   // K stage s landed (1..3)
+  DQ_EMPTYK0 = 4,  // K stage s consumed (4..6)
+  DQ_FULLV0 = 7,   // V stage s landed (7, 8)
+  DQ_EMPTYV0 = 9,  // V stage s consumed (9, 10)
+  DQ_SF = 11,      // S and dP of a tile computed
+  DQ_EF = 12,      // dS of a tile written, 4 warp arrivals
+  DQ_ACC = 13,     // dQ final
+  DQ_CLEAN = 14,
+  kDqNumBars = 15
+};
+constexpr int kDqOffTmemSlot = kDqOffBar + 8 * kDqNumBars;
+constexpr int kDqOffAbort = kDqOffTmemSlot + 8;
+constexpr int kDqSmemBytes = kDqOffAbort + 8 + 1024;
+static_assert(kDqSmemBytes <= 227 * 1024, "dQ kernel shared memory");
+
+__device__ __forceinline__ uint32_t dq_setup(uint8_t* smem, uint32_t sb, int warp) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDqNumBars; ++i) ptx::mbar_init(sb + kDqOffBar + 8 * i, i == DQ_EF ? 4 : 1);
+    *reinterpret_cast<volatile int*>(smem + kDqOffAbort) = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_async_shared();
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(ptx::smem_u32(smem + kDqOffTmemSlot), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  return *reinterpret_cast<uint32_t*>(smem + kDqOffTmemSlot);
+}
+
+// Producer of the dQ kernel: Q and dO once, then K(t) and V(t) of every key
+// tile into their rings; `coord(t, &map_k, &map_v, &row)` names tile t.
+template <typename Coord>
+__device__ __forceinline__ void dq_produce(uint32_t sb, const CUtensorMap* fq,
+                                           const CUtensorMap* fdo, int fy, int frow, int iters,
+                                           int c, Coord coord, const WaitCtl& ctl, int* status) {
+  auto bar = [&](int i) -> uint32_t { return sb + kDqOffBar + 8 * i; };
+  ptx::mbar_arrive_expect_tx(bar(DQ_FIX), 2 * kTileBytes);
+  for (int ch = 0; ch < 2; ++ch) {
+    ptx::tma_load_3d(sb + kOffFixA + ch * kChunkBytes, fq, bar(DQ_FIX), ch * 64, fy, frow);
+    ptx::tma_load_3d(sb + kOffFixB + ch * kChunkBytes, fdo, bar(DQ_FIX), ch * 64, fy, frow);
+  }
+  int nk = 0, nv = 0;  // K / V tiles issued
+  for (int t = 0; t < iters; ++t) {
+    const CUtensorMap *mk, *mv;
+    int row;
+    coord(t, &mk, &mv, &row);
+    const int sk = t % kDqKStages, sv = t % kDqVStages;
+    if (t >= kDqKStages &&
+        !wait_bar(bar(DQ_EMPTYK0 + sk), ((t / kDqKStages) - 1) & 1, ctl))
+      break;
+    ptx::mbar_arrive_expect_tx(bar(DQ_FULLK0 + sk), kTileBytes);
+    for (int ch = 0; ch < 2; ++ch)
+      ptx::tma_load_3d(sb + kDqOffK + sk * kTileBytes + ch * kChunkBytes, mk,
+                       bar(DQ_FULLK0 + sk), ch * 64, c, row);
+    nk = t + 1;
+    if (t >= kDqVStages &&
+        !wait_bar(bar(DQ_EMPTYV0 + sv), ((t / kDqVStages) - 1) & 1, ctl))
+      break;
+    ptx::mbar_arrive_expect_tx(bar(DQ_FULLV0 + sv), kTileBytes);
+    for (int ch = 0; ch < 2; ++ch)
+      ptx::tma_load_3d(sb + kDqOffV + sv * kTileBytes + ch * kChunkBytes, mv,
+                       bar(DQ_FULLV0 + sv), ch * 64, c, row);
+    nv = t + 1;
+  }
+  // Drain: every copy issued must have landed before the CTA exits.
+  drain_bar(bar(DQ_FIX), 0, status);
+  for (int st = 0; st < kDqKStages; ++st) {
+    const int last = nk - 1 - ((nk - 1 - st) % kDqKStages + kDqKStages) % kDqKStages;
+    if (last >= 0) drain_bar(bar(DQ_FULLK0 + st), (last / kDqKStages) & 1, status);
+  }
+  for (int st = 0; st < kDqVStages; ++st) {
+    const int last = nv - 1 - ((nv - 1 - st) % kDqVStages + kDqVStages) % kDqVStages;
+    if (last >= 0) drain_bar(bar(DQ_FULLV0 + st), (last / kDqVStages) & 1, status);
+  }
+}
+
+// D[128 x 128] = A[128 x 128] B[128 x 128]^T, both K-major: 8 SS MMAs.
+__device__ __forceinline__ void mma_scores_full(uint32_t d, uint32_t a_lo, uint32_t b_lo) {
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kT, kT, false);
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+    ptx::mma_ss_lohi(d, a_lo + off, ptx::kDescHiSw128, b_lo + off, ptx::kDescHiSw128, kIdesc,
+                     kk > 0 ? 1u : 0u);
+  }
+}
+
+// MMA issue order of the dQ kernel, tile t's elementwise pass running:
+// S(t+1) into the other S buffer (its dS(t-1) was read by dQ(t-1), issued
+// earlier), then -- once the pass is done with dP(t) -- dP(t+1), then
+// dQ += dS(t) K(t).  The tensor pipe computes dQ(t) and S(t+2) while the
+// warps process tile t+1; only dP(t+1) runs with the warps idle.
+__device__ __forceinline__ bool dq_pipeline(uint32_t sb, uint32_t tmem, int iters,
+                                            const WaitCtl& ctl) {
+  auto bar = [&](int i) -> uint32_t { return sb + kDqOffBar + 8 * i; };
+  constexpr uint32_t kIdescG = ptx::idesc_bf16_f32(kT, kD, true);
+  const uint32_t q_lo = ptx::desc_lo(sb + kOffFixA, 16);
+  const uint32_t do_lo = ptx::desc_lo(sb + kOffFixB, 16);
+  const uint32_t k_lo = ptx::desc_lo(sb + kDqOffK, 16);
+  const uint32_t v_lo = ptx::desc_lo(sb + kDqOffV, 16);
+  const uint32_t k_mn = ptx::desc_lo(sb + kDqOffK, kChunkBytes);
+  bool ok = wait_bar(bar(DQ_FIX), 0, ctl) && wait_bar(bar(DQ_FULLK0), 0, ctl) &&
+            wait_bar(bar(DQ_FULLV0), 0, ctl);
+  if (!ok) return false;
+  ptx::tc_fence_after();
+  mma_scores_full(tmem + dq_col_s(0), q_lo, k_lo);  // S  = Q K^T
+  mma_scores_full(tmem + kDqColP, do_lo, v_lo);     // dP = dO V^T
+  ptx::mma_commit(bar(DQ_SF));
+  ptx::mma_commit(bar(DQ_EMPTYV0));
+  for (int t = 0; t < iters; ++t) {
+    const bool next = t + 1 < iters;
+    if (next) {
+      const int sk = (t + 1) % kDqKStages;
+      if (!(ok = wait_bar(bar(DQ_FULLK0 + sk), ((t + 1) / kDqKStages) & 1, ctl))) break;
+      ptx::tc_fence_after();
+      mma_scores_full(tmem + dq_col_s(t + 1), q_lo, k_lo + sk * kTileLo);
+    }
+    if (!(ok = wait_bar(bar(DQ_EF), t & 1, ctl))) break;
+    ptx::tc_fence_after();
+    if (next) {
+      const int sv = (t + 1) % kDqVStages;
+      if (!(ok = wait_bar(bar(DQ_FULLV0 + sv), ((t + 1) / kDqVStages) & 1, ctl))) break;
+      ptx::tc_fence_after();
+      mma_scores_full(tmem + kDqColP, do_lo, v_lo + sv * kTileLo);
+      ptx::mma_commit(bar(DQ_SF));
+      ptx::mma_commit(bar(DQ_EMPTYV0 + sv));  // V(t+1) consumed
+    }
+    const int sk = t % kDqKStages;
+    const uint32_t a = tmem + dq_col_s(t);
+    const uint32_t kb = k_mn + sk * kTileLo;
+#pragma unroll
+    for (int kk = 0; kk < kT / 16; ++kk)
+      ptx::mma_ts_lohi(tmem + kDqColQ, a + kk * 8, kb + ((kk * 2048) >> 4), ptx::kDescHiSw128,
+                       kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+    ptx::mma_commit(bar(DQ_EMPTYK0 + sk));  // K(t) consumed
+  }
+  if (ok) ptx::mma_commit(bar(DQ_ACC));
+  return ok;
+}
+
+// CTA = (query tile, query head).
 template <bool kG>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sb = ptx::smem_u32(smem);
-  auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8 * i; };
+  auto bar = [&](int i) -> uint32_t { return sb + kDqOffBar + 8 * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Window mode: CTA (query tile, head); key tiles = landmark tiles, then the
   // window tiles of the rows.  Gathered mode: CTA (key split, M tile, KV
@@ -317,42 +482,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
     T = n_lm_tiles + static_cast<int>(q_last / kT) - kt_lo + 1;
   }
 
-  const uint32_t tmem = bwd_setup(smem, sb, warp);
-  WaitCtl ctl{reinterpret_cast<volatile int*>(smem + kOffAbort), p.status, p.wait_ns};
+  const uint32_t tmem = dq_setup(smem, sb, warp);
+  WaitCtl ctl{reinterpret_cast<volatile int*>(smem + kDqOffAbort), p.status, p.wait_ns};
 
   if (warp == 4) {
     if (lane == 0) {
-      auto coord = [&](int t, const CUtensorMap** ma, const CUtensorMap** mb, int* ya, int* yb,
-                       int* row) {
+      auto coord = [&](int t, const CUtensorMap** mk, const CUtensorMap** mv, int* row) {
         const bool lm = t < n_lm_tiles;
-        *ma = lm ? &p.tm_klm : &p.tm_k;
-        *mb = lm ? &p.tm_vlm : &p.tm_v;
-        *ya = *yb = c;
+        *mk = lm ? &p.tm_klm : &p.tm_k;
+        *mv = lm ? &p.tm_vlm : &p.tm_v;
         *row = lm ? t * kT : (kt_lo + t - n_lm_tiles) * kT;
       };
-      auto no_stats = [](int, const float**, const float**, const int**) {};
-      produce(sb, &p.tm_q, &p.tm_do, fy, static_cast<int>(qr0), T, coord, no_stats, ctl,
-              p.status);
+      dq_produce(sb, &p.tm_q, &p.tm_do, fy, static_cast<int>(qr0), T, c, coord, ctl, p.status);
     }
   } else if (warp == 5) {
     if (lane == 0) {
-      const uint32_t q_lo = ptx::desc_lo(sb + kOffFixA, 16);
-      const uint32_t do_lo = ptx::desc_lo(sb + kOffFixB, 16);
-      const uint32_t k_lo = ptx::desc_lo(sb + kOffRingA, 16);
-      const uint32_t v_lo = ptx::desc_lo(sb + kOffRingB, 16);
-      const uint32_t k_mn = ptx::desc_lo(sb + kOffRingA, kChunkBytes);
-      auto scores = [&](int t, int half) {
-        const uint32_t st = (t & 1) * kTileLo;
-        mma_scores_half(tmem + col_s(half), q_lo, k_lo + st, half);   // S  = Q K^T
-        mma_scores_half(tmem + col_p(half), do_lo, v_lo + st, half);  // dP = dO V^T
-      };
-      auto grads = [&](int t, int half) {  // dQ += dS K
-        mma_grad_half(tmem + 256, tmem + col_s(half), k_mn + (t & 1) * kTileLo, half,
-                      t == 0 && half == 0);
-      };
-      mma_pipeline(sb, T, scores, grads, ctl);
-      ptx::mma_commit(bar(BAR_CLEAN));
-      drain_bar(bar(BAR_CLEAN), 0, p.status);
+      dq_pipeline(sb, tmem, T, ctl);
+      ptx::mma_commit(bar(DQ_CLEAN));
+      drain_bar(bar(DQ_CLEAN), 0, p.status);
     }
   } else if (warp < 4) {
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
@@ -381,47 +528,45 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
         hi = i - kb + 1;
       }
       if (!row_ok) hi = lo;
-      for (int half = 0; half < 2; ++half) {
-        ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF0 + half), t & 1, ctl));
-        if (!ok) break;
-        ptx::tc_fence_after();
-        const int lo_c = static_cast<int>(max64(0, min64(kHalf, lo - half * kHalf)));
-        const int hi_c = static_cast<int>(max64(0, min64(kHalf, hi - half * kHalf)));
-        const bool full = lo_c == 0 && hi_c == kHalf;
+      ok = __all_sync(0xffffffffu, wait_bar(bar(DQ_SF), t & 1, ctl));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int lo_c = static_cast<int>(max64(0, min64(kT, lo)));
+      const int hi_c = static_cast<int>(max64(0, min64(kT, hi)));
+      const bool full = lo_c == 0 && hi_c == kT;
+      const uint32_t ts = tl + dq_col_s(t);
 #pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          float s[32], dp[32];
-          ptx::tmem_ld32(tl + col_s(half) + cc * 32, s);
-          ptx::tmem_ld32(tl + col_p(half) + cc * 32, dp);
-          ptx::tmem_wait_ld();
-          if (!full) {  // masked columns: weight 0
+      for (int cc = 0; cc < 4; ++cc) {
+        float s[32], dp[32];
+        ptx::tmem_ld32(ts + cc * 32, s);
+        ptx::tmem_ld32(tl + kDqColP + cc * 32, dp);
+        ptx::tmem_wait_ld();
+        if (!full) {  // masked columns: weight 0
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int col = cc * 32 + e;
-              s[e] = (col >= lo_c && col < hi_c) ? s[e] : -INFINITY;
-            }
+          for (int e = 0; e < 32; ++e) {
+            const int col = cc * 32 + e;
+            s[e] = (col >= lo_c && col < hi_c) ? s[e] : -INFINITY;
           }
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            // p = 2^(s scale log2e - lse log2e), dS = p (dP - D)
-            float x0, x1;
-            ptx::f2_split(ptx::fma2(ptx::f2(s[2 * e], s[2 * e + 1]), c2, nL22), x0, x1);
-            const uint64_t pr = ptx::f2(ptx::ex2(x0), ptx::ex2(x1));
-            float d0, d1;
-            ptx::f2_split(ptx::mul2(pr, ptx::add2(ptx::f2(dp[2 * e], dp[2 * e + 1]), nD2)), d0,
-                          d1);
-            pk[e] = ptx::pack_bf16x2(d0, d1);
-          }
-          ptx::tmem_st16(tl + col_s(half) + cc * 16, pk);  // dS over columns already read
         }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(BAR_EF0 + half));
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          // p = 2^(s scale log2e - lse log2e), dS = p (dP - D)
+          float x0, x1;
+          ptx::f2_split(ptx::fma2(ptx::f2(s[2 * e], s[2 * e + 1]), c2, nL22), x0, x1);
+          const uint64_t pr = ptx::f2(ptx::ex2(x0), ptx::ex2(x1));
+          float d0, d1;
+          ptx::f2_split(ptx::mul2(pr, ptx::add2(ptx::f2(dp[2 * e], dp[2 * e + 1]), nD2)), d0, d1);
+          pk[e] = ptx::pack_bf16x2(d0, d1);
+        }
+        ptx::tmem_st16(ts + cc * 16, pk);  // dS over S columns already read
       }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(DQ_EF));
     }
-    if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_ACC), 0, ctl));
+    if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(DQ_ACC), 0, ctl));
     if (ok) {
       ptx::tc_fence_after();
       // Gathered mode: this split's share of the row's dQ, fp32.
@@ -432,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         float o[32];
-        ptx::tmem_ld32(tl + 256 + cc * 32, o);
+        ptx::tmem_ld32(tl + kDqColQ + cc * 32, o);
         ptx::tmem_wait_ld();
         if (row_ok) store_row(dst, off + cc * 32, o, p.scale, kG ? 0 : p.grad_bf16);
       }
@@ -929,9 +1074,12 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why) 
         a.out, static_cast<const uint16_t*>(a.dout), a.lse, L2w, Dw, a.n, a.n_pad, a.Hq);
   cudaError_t e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
-  for (auto* k : {bwd_dkdv_tc_kernel<false>, bwd_dq_tc_kernel<false>, bwd_dkdv_tc_kernel<true>,
-                  bwd_dq_tc_kernel<true>}) {
+  for (auto* k : {bwd_dkdv_tc_kernel<false>, bwd_dkdv_tc_kernel<true>}) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+  }
+  for (auto* k : {bwd_dq_tc_kernel<false>, bwd_dq_tc_kernel<true>}) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmemBytes);
     if (e != cudaSuccess) return e;
   }
   const unsigned n_tiles = static_cast<unsigned>((a.n + kT - 1) / kT);
@@ -990,12 +1138,12 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why) 
   bwd_dkdv_tc_kernel<false><<<dim3(n_tiles, a.Hkv, 1), kThreads, kSmemBytes, s>>>(p);
   e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
-  bwd_dq_tc_kernel<false><<<dim3(n_tiles, a.Hq), kThreads, kSmemBytes, s>>>(p);
+  bwd_dq_tc_kernel<false><<<dim3(n_tiles, a.Hq), kThreads, kDqSmemBytes, s>>>(p);
   e = cudaPeekAtLastError();
   if (e != cudaSuccess || !a.rows) return e;
   // The global rows' dQ: per key split, then summed into their rows.
   bwd_dq_tc_kernel<true><<<dim3(a.n_splits, static_cast<unsigned>(a.Mp / kT), a.Hkv),
-                           kThreads, kSmemBytes, s>>>(pg);
+                           kThreads, kDqSmemBytes, s>>>(pg);
   e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
   dq_scatter_kernel<<<static_cast<unsigned>((a.n_global * a.Hq + 7) / 8), 256, 0, s>>>(
