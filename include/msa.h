@@ -436,11 +436,12 @@ msa_status msa_device_status(int clear);
 
 /*
  * Test hook: sets the limit, in nanoseconds, of every bounded wait in the
- * tensor-core kernel for launches made after the call (0 restores the
+ * tensor-core kernels for launches made after the call (0 restores the
  * default of 4 s).  A very small limit makes waits run out on purpose, to
- * check that the kernel then finishes early with MSA_ERR_TIMEOUT instead of
- * hanging.  Copies already in flight are still waited for with the default
- * limit before a kernel exits.
+ * check that a kernel then finishes early with MSA_ERR_TIMEOUT instead of
+ * hanging; with a limit of 1 ns every wait that its first, non-blocking
+ * probe does not find complete runs out.  Copies and MMAs already in flight
+ * are still waited for with the default limit before a kernel exits.
  */
 void msa_debug_set_wait_limit_ns(uint64_t ns);
 

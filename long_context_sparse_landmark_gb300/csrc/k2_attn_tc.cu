@@ -18,7 +18,8 @@
 // 128x128x128 MMA pairs).  One CTA per unit, 12 warps:
 //   warp 0      TMA producer: Q tiles once, then K and V tiles through a
 //               2-stage ring (landmark tiles first, then window tiles);
-//   warp 1      allocates 512 TMEM columns; one lane issues every MMA:
+//   warp 1      allocates 512 TMEM columns and issues every MMA (the
+//               whole warp runs the loop, one elected lane issues):
 //               S_s = Q_s K^T (SS: both from shared memory) and
 //               O_s += P_s V (TS: P from TMEM, V from shared memory);
 //   warps 4-7   softmax of head slot 0 (TMEM lanes 0..127, one row each);
@@ -28,7 +29,7 @@
 // MMA issue order per tile t: PV_0(t), S_0(t+1), PV_1(t), S_1(t+1), so the
 // tensor pipe works on one slot while the other slot's softmax runs.
 // S_s(t+1) is issued after PV_s(t), which reads P_s(t) from the same TMEM
-// columns; tcgen05 MMAs from one thread execute in issue order.
+// columns; tcgen05 MMAs from one warp execute in issue order.
 //
 // Softmax: scores are kept in log2 units (scale*log2(e) folded into one FMA);
 // the exponent base m is only raised when the row maximum exceeds it by more
@@ -297,7 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issuing loop; elect.sync picks the lane that
+    // issues each tcgen05 instruction.
+    {
       constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBM, kBN, false);
       constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kBM, kD, true);
       // Descriptor low halves of every operand base, computed once; per K
@@ -315,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-          ptx::mma_ss_lohi(d, qa + off, ptx::kDescHiSw128, kb + off, ptx::kDescHiSw128, kIdescS,
+          ptx::mma_ss_w(d, qa + off, ptx::kDescHiSw128, kb + off, ptx::kDescHiSw128, kIdescS,
                            kk > 0 ? 1u : 0u);
         }
       };
@@ -325,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const uint32_t pa = tmem + slot * 256;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          ptx::mma_ts_lohi(d, pa + kk * 8, vb + ((kk * 2048) >> 4), ptx::kDescHiSw128, kIdescO,
+          ptx::mma_ts_w(d, pa + kk * 8, vb + ((kk * 2048) >> 4), ptx::kDescHiSw128, kIdescO,
                            (!first || kk > 0) ? 1u : 0u);
         }
       };
@@ -338,10 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
         const Unit w = decode_unit(p, u);
         if (w.T == 0) continue;
-        if (!(ok = wait_bar(bar(BAR_Q), qn & 1, ctl))) break;
+        if (!(ok = wait_w(bar(BAR_Q), qn & 1, ctl))) break;
         const bool first_unit = first;
         if (first) {
-          if (!(ok = wait_bar(bar(BAR_K0), 0, ctl))) break;
+          if (!(ok = wait_w(bar(BAR_K0), 0, ctl))) break;
           first = false;
         }
         // (Otherwise K of this tile came with the previous unit's last pair,
@@ -349,46 +352,46 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         ptx::tc_fence_after();
         for (int s = 0; s < w.n_slots; ++s) {
           issue_s(s, g & 1);
-          ptx::mma_commit(bar(BAR_SF(s)));
+          ptx::commit_w(bar(BAR_SF(s)));
         }
         // The first K tile's buffer is refilled by pair 1: release it.
-        if (first_unit) ptx::mma_commit(bar(BAR_KVE(1)));
-        if (w.T == 1) ptx::mma_commit(bar(BAR_QE));  // the unit's last S MMA
+        if (first_unit) ptx::commit_w(bar(BAR_KVE(1)));
+        if (w.T == 1) ptx::commit_w(bar(BAR_QE));  // the unit's last S MMA
         if (pending >= 0) {
-          ptx::mma_commit(bar(BAR_KVE(pending & 1)));
+          ptx::commit_w(bar(BAR_KVE(pending & 1)));
           pending = -1;
         }
         for (int t = 0; ok && t < w.T; ++t, ++g) {
           const uint32_t b = g & 1;
           const bool nxt = t + 1 < w.T;
           // Pair g: V of this tile and K of the next one.
-          if (!(ok = wait_bar(bar(BAR_KVF(b)), (g >> 1) & 1, ctl))) break;
+          if (!(ok = wait_w(bar(BAR_KVF(b)), (g >> 1) & 1, ctl))) break;
           for (int s = 0; s < w.n_slots; ++s) {
-            if (!(ok = wait_bar(bar(BAR_PF(s)), (sc[s] + t) & 1, ctl))) break;
+            if (!(ok = wait_w(bar(BAR_PF(s)), (sc[s] + t) & 1, ctl))) break;
             ptx::tc_fence_after();
             // PV_s(t) reads P_s(t) from the S columns; S_s(t+1) overwrites
-            // them and is issued after it by this same thread.
+            // them and is issued after it by this same warp.
             issue_pv(s, b, t == 0);
             if (nxt) {
               issue_s(s, b ^ 1);
-              ptx::mma_commit(bar(BAR_SF(s)));
+              ptx::commit_w(bar(BAR_SF(s)));
             } else {
-              ptx::mma_commit(bar(BAR_OD(s)));
+              ptx::commit_w(bar(BAR_OD(s)));
             }
           }
           if (!ok) break;
-          if (t + 2 == w.T) ptx::mma_commit(bar(BAR_QE));  // S(T-1) was the last S
+          if (t + 2 == w.T) ptx::commit_w(bar(BAR_QE));  // S(T-1) was the last S
           if (nxt)
-            ptx::mma_commit(bar(BAR_KVE(b)));
+            ptx::commit_w(bar(BAR_KVE(b)));
           else
             pending = static_cast<int>(g);  // released after the next unit's S(0)
         }
         for (int s = 0; s < w.n_slots; ++s) sc[s] += w.T;
         ++qn;
       }
-      if (pending >= 0) ptx::mma_commit(bar(BAR_KVE(pending & 1)));
+      if (pending >= 0) ptx::commit_w(bar(BAR_KVE(pending & 1)));
       // Drain: all MMAs issued so far complete before TMEM is released.
-      ptx::mma_commit(bar(BAR_CLEAN));
+      ptx::commit_w(bar(BAR_CLEAN));
       drain_bar(bar(BAR_CLEAN), 0, p.status);
     }
   } else if (warp >= 4) {

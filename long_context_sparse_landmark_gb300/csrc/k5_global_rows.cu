@@ -22,7 +22,8 @@
 //              epilogue;
 //   warp 4     TMA producer of K/V tiles through a 2-stage ring;
 //   warp 5     allocates 256 TMEM columns (S: 0..127, P over its first 64;
-//              O: 128..255); one lane issues S = Q K^T and O += P V.
+//              O: 128..255); the warp issues S = Q K^T and O += P V (one elected
+//              lane per instruction).
 // Per tile: S MMA -> softmax -> P -> PV MMA, in order; S(t+1) is issued
 // after PV(t), so the completion of S(t+1) also means PV(t) is done and O
 // may be rescaled.  Every wait is bounded as in the attention kernel.
@@ -191,7 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (the whole warp runs the loop; elect.sync picks the issuing lane)
+    {
       constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBM, kBN, false);
       constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kBM, kD, true);
       constexpr uint32_t kTileLo = kTileBytes >> 4;
@@ -201,27 +203,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = 0; ok && t < T; ++t) {
         const int b = t & 1;
-        if (!(ok = wait_bar(bar(BAR_KVF0 + b), (t >> 1) & 1, ctl))) break;
+        if (!(ok = wait_w(bar(BAR_KVF0 + b), (t >> 1) & 1, ctl))) break;
         ptx::tc_fence_after();
         const uint32_t kb = k_lo0 + b * kTileLo;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-          ptx::mma_ss_lohi(tmem, q_lo + off, ptx::kDescHiSw128, kb + off, ptx::kDescHiSw128,
+          ptx::mma_ss_w(tmem, q_lo + off, ptx::kDescHiSw128, kb + off, ptx::kDescHiSw128,
                            kIdescS, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(bar(BAR_SF));
-        if (!(ok = wait_bar(bar(BAR_PF), t & 1, ctl))) break;
+        ptx::commit_w(bar(BAR_SF));
+        if (!(ok = wait_w(bar(BAR_PF), t & 1, ctl))) break;
         ptx::tc_fence_after();
         const uint32_t vb = v_lo0 + b * kTileLo;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          ptx::mma_ts_lohi(tmem + 128, tmem + kk * 8, vb + ((kk * 2048) >> 4), ptx::kDescHiSw128,
+          ptx::mma_ts_w(tmem + 128, tmem + kk * 8, vb + ((kk * 2048) >> 4), ptx::kDescHiSw128,
                            kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(bar(BAR_KVE0 + b));
+        ptx::commit_w(bar(BAR_KVE0 + b));
       }
-      if (ok) ptx::mma_commit(bar(BAR_OF));
-      ptx::mma_commit(bar(BAR_CLEAN));
+      if (ok) ptx::commit_w(bar(BAR_OF));
+      ptx::commit_w(bar(BAR_CLEAN));
       drain_bar(bar(BAR_CLEAN), 0, p.status);
     }
   } else {

@@ -26,7 +26,7 @@
 //      and window key tiles, as the forward.
 // Each tensor-core kernel: warps 0-3 elementwise (one TMEM lane = one row
 // each), warp 4 TMA producer, warp 5 TMEM allocation and MMA issue.
-// tcgen05 MMAs from one thread execute in issue order, which makes
+// tcgen05 MMAs from one warp execute in issue order, which makes
 // overwriting TMEM columns after the MMAs that read them safe.
 //   dK/dV: TMEM holds two accumulators, so every 128-column tile is handled
 //   as two 64-column halves with their own columns: the score-like MMAs of
@@ -228,7 +228,7 @@ __device__ __forceinline__ void mma_scores_half(uint32_t d, uint32_t a_lo, uint3
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk) {
     const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-    ptx::mma_ss_lohi(d, a_lo + off, ptx::kDescHiSw128, b_half + off, ptx::kDescHiSw128, kIdesc,
+    ptx::mma_ss_w(d, a_lo + off, ptx::kDescHiSw128, b_half + off, ptx::kDescHiSw128, kIdesc,
                      kk > 0 ? 1u : 0u);
   }
 }
@@ -241,7 +241,7 @@ __device__ __forceinline__ void mma_grad_half(uint32_t d, uint32_t a_tmem, uint3
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kT, kD, true);
 #pragma unroll
   for (int kk = 0; kk < kHalf / 16; ++kk)
-    ptx::mma_ts_lohi(d, a_tmem + kk * 8, b_mn + ((half * kHalf * 128 + kk * 2048) >> 4),
+    ptx::mma_ts_w(d, a_tmem + kk * 8, b_mn + ((half * kHalf * 128 + kk * 2048) >> 4),
                      ptx::kDescHiSw128, kIdesc, (!first || kk > 0) ? 1u : 0u);
 }
 
@@ -251,7 +251,8 @@ __device__ __forceinline__ void mma_grad_half(uint32_t d, uint32_t a_tmem, uint3
 __device__ __forceinline__ uint32_t col_s(int half) { return half * kHalf; }
 __device__ __forceinline__ uint32_t col_p(int half) { return 128 + half * kHalf; }
 
-// The MMA issuer's pipeline over `iters` ring stages.  Per stage: scores of
+// The MMA issuer's pipeline over `iters` ring stages (run by the whole MMA
+// warp).  Per stage: scores of
 // half 0 and half 1; then, as the elementwise warps finish each half, that
 // half's gradient MMAs followed by the next stage's scores of the same half,
 // so the tensor pipe works on one half while the warps process the other.
@@ -259,31 +260,31 @@ template <typename Scores, typename Grads>
 __device__ __forceinline__ bool mma_pipeline(uint32_t sb, int iters, Scores scores, Grads grads,
                                              const WaitCtl& ctl) {
   auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8 * i; };
-  bool ok = wait_bar(bar(BAR_FIX), 0, ctl) && wait_bar(bar(BAR_FULL0), 0, ctl);
+  bool ok = wait_w(bar(BAR_FIX), 0, ctl) && wait_w(bar(BAR_FULL0), 0, ctl);
   if (!ok) return false;
   ptx::tc_fence_after();
   for (int h = 0; h < 2; ++h) {
     scores(0, h);
-    ptx::mma_commit(bar(BAR_SF0 + h));
+    ptx::commit_w(bar(BAR_SF0 + h));
   }
   for (int it = 0; it < iters; ++it) {
     const int b = it & 1;
     const bool next = it + 1 < iters;
     for (int h = 0; h < 2; ++h) {
-      if (!(ok = wait_bar(bar(BAR_EF0 + h), it & 1, ctl))) break;
+      if (!(ok = wait_w(bar(BAR_EF0 + h), it & 1, ctl))) break;
       ptx::tc_fence_after();
       grads(it, h);
-      if (h == 1) ptx::mma_commit(bar(BAR_EMPTY0 + b));  // stage b fully consumed
+      if (h == 1) ptx::commit_w(bar(BAR_EMPTY0 + b));  // stage b fully consumed
       if (next) {
-        if (h == 0 && !(ok = wait_bar(bar(BAR_FULL0 + (b ^ 1)), ((it + 1) >> 1) & 1, ctl)))
+        if (h == 0 && !(ok = wait_w(bar(BAR_FULL0 + (b ^ 1)), ((it + 1) >> 1) & 1, ctl)))
           break;
         scores(it + 1, h);
-        ptx::mma_commit(bar(BAR_SF0 + h));
+        ptx::commit_w(bar(BAR_SF0 + h));
       }
     }
     if (!ok) break;
   }
-  if (ok) ptx::mma_commit(bar(BAR_ACC));
+  if (ok) ptx::commit_w(bar(BAR_ACC));
   return ok;
 }
 
@@ -391,12 +392,13 @@ __device__ __forceinline__ void mma_scores_full(uint32_t d, uint32_t a_lo, uint3
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk) {
     const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-    ptx::mma_ss_lohi(d, a_lo + off, ptx::kDescHiSw128, b_lo + off, ptx::kDescHiSw128, kIdesc,
-                     kk > 0 ? 1u : 0u);
+    ptx::mma_ss_w(d, a_lo + off, ptx::kDescHiSw128, b_lo + off, ptx::kDescHiSw128, kIdesc,
+             kk > 0 ? 1u : 0u);
   }
 }
 
-// MMA issue order of the dQ kernel, tile t's elementwise pass running:
+// MMA issue order of the dQ kernel (run by the whole MMA warp), tile t's
+// elementwise pass running:
 // S(t+1) into the other S buffer (its dS(t-1) was read by dQ(t-1), issued
 // earlier), then -- once the pass is done with dP(t) -- dP(t+1), then
 // dQ += dS(t) K(t).  The tensor pipe computes dQ(t) and S(t+2) while the
@@ -410,42 +412,42 @@ __device__ __forceinline__ bool dq_pipeline(uint32_t sb, uint32_t tmem, int iter
   const uint32_t k_lo = ptx::desc_lo(sb + kDqOffK, 16);
   const uint32_t v_lo = ptx::desc_lo(sb + kDqOffV, 16);
   const uint32_t k_mn = ptx::desc_lo(sb + kDqOffK, kChunkBytes);
-  bool ok = wait_bar(bar(DQ_FIX), 0, ctl) && wait_bar(bar(DQ_FULLK0), 0, ctl) &&
-            wait_bar(bar(DQ_FULLV0), 0, ctl);
+  bool ok = wait_w(bar(DQ_FIX), 0, ctl) && wait_w(bar(DQ_FULLK0), 0, ctl) &&
+            wait_w(bar(DQ_FULLV0), 0, ctl);
   if (!ok) return false;
   ptx::tc_fence_after();
   mma_scores_full(tmem + dq_col_s(0), q_lo, k_lo);  // S  = Q K^T
   mma_scores_full(tmem + kDqColP, do_lo, v_lo);     // dP = dO V^T
-  ptx::mma_commit(bar(DQ_SF));
-  ptx::mma_commit(bar(DQ_EMPTYV0));
+  ptx::commit_w(bar(DQ_SF));
+  ptx::commit_w(bar(DQ_EMPTYV0));
   for (int t = 0; t < iters; ++t) {
     const bool next = t + 1 < iters;
     if (next) {
       const int sk = (t + 1) % kDqKStages;
-      if (!(ok = wait_bar(bar(DQ_FULLK0 + sk), ((t + 1) / kDqKStages) & 1, ctl))) break;
+      if (!(ok = wait_w(bar(DQ_FULLK0 + sk), ((t + 1) / kDqKStages) & 1, ctl))) break;
       ptx::tc_fence_after();
       mma_scores_full(tmem + dq_col_s(t + 1), q_lo, k_lo + sk * kTileLo);
     }
-    if (!(ok = wait_bar(bar(DQ_EF), t & 1, ctl))) break;
+    if (!(ok = wait_w(bar(DQ_EF), t & 1, ctl))) break;
     ptx::tc_fence_after();
     if (next) {
       const int sv = (t + 1) % kDqVStages;
-      if (!(ok = wait_bar(bar(DQ_FULLV0 + sv), ((t + 1) / kDqVStages) & 1, ctl))) break;
+      if (!(ok = wait_w(bar(DQ_FULLV0 + sv), ((t + 1) / kDqVStages) & 1, ctl))) break;
       ptx::tc_fence_after();
       mma_scores_full(tmem + kDqColP, do_lo, v_lo + sv * kTileLo);
-      ptx::mma_commit(bar(DQ_SF));
-      ptx::mma_commit(bar(DQ_EMPTYV0 + sv));  // V(t+1) consumed
+      ptx::commit_w(bar(DQ_SF));
+      ptx::commit_w(bar(DQ_EMPTYV0 + sv));  // V(t+1) consumed
     }
     const int sk = t % kDqKStages;
     const uint32_t a = tmem + dq_col_s(t);
     const uint32_t kb = k_mn + sk * kTileLo;
 #pragma unroll
     for (int kk = 0; kk < kT / 16; ++kk)
-      ptx::mma_ts_lohi(tmem + kDqColQ, a + kk * 8, kb + ((kk * 2048) >> 4), ptx::kDescHiSw128,
+      ptx::mma_ts_w(tmem + kDqColQ, a + kk * 8, kb + ((kk * 2048) >> 4), ptx::kDescHiSw128,
                        kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
-    ptx::mma_commit(bar(DQ_EMPTYK0 + sk));  // K(t) consumed
+    ptx::commit_w(bar(DQ_EMPTYK0 + sk));  // K(t) consumed
   }
-  if (ok) ptx::mma_commit(bar(DQ_ACC));
+  if (ok) ptx::commit_w(bar(DQ_ACC));
   return ok;
 }
 
@@ -496,11 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
       dq_produce(sb, &p.tm_q, &p.tm_do, fy, static_cast<int>(qr0), T, c, coord, ctl, p.status);
     }
   } else if (warp == 5) {
-    if (lane == 0) {
-      dq_pipeline(sb, tmem, T, ctl);
-      ptx::mma_commit(bar(DQ_CLEAN));
-      drain_bar(bar(DQ_CLEAN), 0, p.status);
-    }
+    dq_pipeline(sb, tmem, T, ctl);
+    ptx::commit_w(bar(DQ_CLEAN));
+    drain_bar(bar(DQ_CLEAN), 0, p.status);
   } else if (warp < 4) {
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const int64_t i_row = qr0 + threadIdx.x;  // query row, or gathered M row
@@ -654,8 +654,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       produce(sb, p.lm_mode ? &p.tm_klm : &p.tm_k, p.lm_mode ? &p.tm_vlm : &p.tm_v, c,
               static_cast<int>(kb), iters, coord, stats, ctl, p.status);
     }
-  } else if (warp == 5) {
-    if (lane == 0) {
+  } else if (warp == 5) {  // the whole warp issues (elect.sync inside)
+    {
       const uint32_t k_lo = ptx::desc_lo(sb + kOffFixA, 16);
       const uint32_t v_lo = ptx::desc_lo(sb + kOffFixB, 16);
       const uint32_t q_lo = ptx::desc_lo(sb + kOffRingA, 16);
@@ -674,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_grad_half(tmem + 384, tmem + col_p(half), q_mn + st, half, first);   // dK += dS^T Q
       };
       mma_pipeline(sb, iters, scores, grads, ctl);
-      ptx::mma_commit(bar(BAR_CLEAN));
+      ptx::commit_w(bar(BAR_CLEAN));
       drain_bar(bar(BAR_CLEAN), 0, p.status);
     }
   } else if (warp < 4) {

@@ -18,19 +18,30 @@ struct WaitCtl {
 };
 
 // Bounded wait on phase `parity` of an mbarrier.  Returns false when the
-// CTA is aborting (flag set by another role, or this wait ran out).
+// CTA is aborting (flag set by another role, or this wait ran out).  The
+// first probe does not block; a limit of at most 1 ns (a test setting) makes
+// every wait that this probe does not find complete run out.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl& c) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer();
-  while (true) {
+  if (ptx::mbar_test_wait(bar, parity)) return true;
+  if (c.limit > 1) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*c.abort) return false;
-    if (ptx::globaltimer() - t0 > c.limit) {
-      *c.abort = 1;
-      record_status(c.status, MSA_ERR_TIMEOUT);
-      return false;
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if (*c.abort) return false;
+      if (ptx::globaltimer() - t0 > c.limit) break;
     }
+  } else if (*c.abort) {
+    return false;
   }
+  *c.abort = 1;
+  record_status(c.status, MSA_ERR_TIMEOUT);
+  return false;
+}
+
+// Bounded wait taken by a whole warp, with one verdict for all its lanes.
+__device__ __forceinline__ bool wait_w(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, ctl));
 }
 
 // Wait used while draining: ignores the abort flag, fixed limit.

@@ -3,8 +3,9 @@ dK/dV and dQ, global rows), made to happen on purpose without faulting,
 trapping or hanging the GPU.
 
 Every mbarrier wait in these kernels is bounded.  The test lowers the bound to
-1 ns so that waits run out although the copies and MMAs they wait for do
-complete: the kernel must then leave its loops, drain what is in flight,
+1 ns, which makes every wait that its first, non-blocking probe does not find
+complete run out although the copies and MMAs it waits for do complete: the
+kernel must then leave its loops, drain what is in flight,
 free tensor memory, return, and record MSA_ERR_TIMEOUT in the device status
 word -- and the CUDA context must stay usable, which the follow-up launch
 with the default bound checks against the oracle.
