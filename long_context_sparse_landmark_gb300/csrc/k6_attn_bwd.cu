@@ -24,16 +24,18 @@
 //      dK, dV;
 //   5. bwd_dq_tc_kernel: per (128-row query tile, head) over the landmark
 //      and window key tiles, as the forward.
-// Each tensor-core kernel: warps 0-3 elementwise (one TMEM lane = one row
-// each), warp 4 TMA producer, warp 5 TMEM allocation and MMA issue.
-// tcgen05 MMAs from one warp execute in issue order, which makes
-// overwriting TMEM columns after the MMAs that read them safe.
+// Each tensor-core kernel: warps 0-7 elementwise (TMEM lane = row; warps w
+// and w + 4 share a row quarter and split the columns), warp 8 TMA
+// producer, warp 9 TMEM allocation and MMA issue.  tcgen05 MMAs from one
+// warp execute in issue order, which makes overwriting TMEM columns after
+// the MMAs that read them safe.
 //   dK/dV: TMEM holds two accumulators, so every 128-column tile is handled
 //   as two 64-column halves with their own columns: the score-like MMAs of
 //   a half land, the elementwise warps turn them into bf16 P / dS in the
 //   same columns, the half's gradient MMAs accumulate in TMEM and the next
 //   tile's scores of that half follow at once -- the tensor pipe works on
-//   one half while the warps process the other.
+//   one half while the warps process the other.  Q and dO arrive in 64-row
+//   halves through a 4-stage ring, each half released by its own MMAs.
 //   dQ: one accumulator leaves room for two full-width S buffers, so the
 //   next tile's S is computed during the elementwise pass and only its dP
 //   waits for the pass; K and V come through separate rings (three K
@@ -57,37 +59,51 @@ constexpr int kHalf = 64;                    // columns per pipelined half
 constexpr int kChunkBytes = 128 * 128;       // 128 rows x 64 bf16
 constexpr int kTileBytes = 2 * kChunkBytes;  // 128 rows x 128 bf16
 constexpr uint32_t kTileLo = kTileBytes >> 4;
-constexpr int kThreads = 192;
+// Warps: 0-7 elementwise (warps w and w + 4 share TMEM lanes 32(w % 4)..+31,
+// i.e. the same 32 rows, and split each tile's columns), 8 TMA producer,
+// 9 TMEM allocation and MMA issue.
+constexpr int kEwWarps = 8;
+constexpr int kProdWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Shared memory of both kernels: a fixed pair of tiles (dQ: Q, dO; dK/dV:
-// K, V) and a 2-stage ring of tile pairs (dQ: K, V; dK/dV: Q, dO).
+// Shared memory: a fixed pair of tiles (dQ: Q, dO; dK/dV: K, V), then the
+// rings.  dK/dV: a 4-stage ring of 64-row halves of the query tiles (Q half,
+// dO half; 32 KB a stage): a half is released as soon as its own gradient
+// MMAs are done, so each copy has about one whole tile of time to land.
 constexpr int kOffFixA = 0;
 constexpr int kOffFixB = kTileBytes;
-constexpr int kOffRingA = 2 * kTileBytes;                 // 2 stages
-constexpr int kOffRingB = kOffRingA + 2 * kTileBytes;     // 2 stages
-constexpr int kOffBar = kOffRingB + 2 * kTileBytes;       // 192 KB
+constexpr int kHalfChunk = kChunkBytes / 2;              // 64 rows x 64 bf16
+constexpr int kHalfTileBytes = kTileBytes / 2;           // 64 rows x 128 bf16
+constexpr int kRing = 4;                                 // dK/dV half-tile stages
+constexpr int kOffRing = 2 * kTileBytes;
+constexpr int kRingStageBytes = 2 * kHalfTileBytes;      // Q half + dO half
+constexpr int kOffBar = kOffRing + kRing * kRingStageBytes;  // 192 KB
 enum {
   BAR_FIX = 0,      // fixed tiles landed
-  BAR_FULL0 = 1,    // ring stage b landed (1, 2)
-  BAR_EMPTY0 = 3,   // ring stage b consumed (3, 4)
-  BAR_SF0 = 5,      // score-like MMAs of half h done (5, 6)
-  BAR_EF0 = 7,      // elementwise results of half h written, 4 warp arrivals (7, 8)
-  BAR_ACC = 9,      // gradient accumulators final
-  BAR_CLEAN = 10,
-  kNumBars = 11
+  BAR_FULL0 = 1,    // ring stage s landed (1..4)
+  BAR_EMPTY0 = 5,   // ring stage s consumed (5..8)
+  BAR_SF0 = 9,      // score-like MMAs of half h done (9, 10)
+  BAR_EF0 = 11,     // elementwise results of half h written, one arrival per warp (11, 12)
+  BAR_ACC = 13,     // gradient accumulators final
+  BAR_CLEAN = 14,
+  kNumBars = 15
 };
-// dK/dV: [2 stages][L2, D, positions][128] 4-byte values, bulk-copied:
-// 128-byte aligned (positions only in the gathered global-row mode).
+// dK/dV: [4 stages][L2, D, positions][64] 4-byte values of the stage's
+// queries, bulk-copied: 128-byte aligned (positions only in the gathered
+// global-row mode).
 constexpr int kOffStats = (kOffBar + 8 * kNumBars + 127) / 128 * 128;
-constexpr int kStatBytes = 3 * kT * 4;  // one stage's L2, D and position rows
-constexpr int kOffTmemSlot = kOffStats + 2 * kStatBytes;
+constexpr int kHalfRows = kT / 2;
+constexpr int kStatBytes = 3 * kHalfRows * 4;  // one stage's L2, D and position rows
+constexpr int kOffTmemSlot = kOffStats + kRing * kStatBytes;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemUsed = kOffAbort + 8;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 
 struct BwdParams {
   CUtensorMap tm_q, tm_do, tm_k, tm_v, tm_klm, tm_vlm;
+  CUtensorMap tm_q64, tm_do64;  // Q, dO with 64-row boxes (the dK/dV ring)
   const float* L2;    // [Hq, n_pad] -lse * log2(e), -inf past n
   const float* D;     // [Hq, n_pad] -<dO, O>, 0 past n
   void* dq;           // [n, Hq, d]
@@ -137,13 +153,13 @@ __device__ __forceinline__ void store_row(void* base, int64_t off, const float (
 __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t sb, int warp) {
   if (threadIdx.x == 0) {
     ptx::mbar_init(sb + kOffBar + 8 * BAR_FIX, 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kRing; ++b) {
       ptx::mbar_init(sb + kOffBar + 8 * (BAR_FULL0 + b), 1);
       ptx::mbar_init(sb + kOffBar + 8 * (BAR_EMPTY0 + b), 1);
     }
     for (int h = 0; h < 2; ++h) {
       ptx::mbar_init(sb + kOffBar + 8 * (BAR_SF0 + h), 1);
-      ptx::mbar_init(sb + kOffBar + 8 * (BAR_EF0 + h), 4);
+      ptx::mbar_init(sb + kOffBar + 8 * (BAR_EF0 + h), kEwWarps);
     }
     ptx::mbar_init(sb + kOffBar + 8 * BAR_ACC, 1);
     ptx::mbar_init(sb + kOffBar + 8 * BAR_CLEAN, 1);
@@ -151,7 +167,7 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t sb, int wa
     ptx::fence_mbar_init();
     ptx::fence_async_shared();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(smem + kOffTmemSlot), 512);
     ptx::tmem_relinquish();
   }
@@ -164,16 +180,17 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t sb, int wa
 __device__ __forceinline__ void bwd_teardown(uint32_t tmem, int warp) {
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
 }
 
-// Producer: the fixed pair once, then `iters` ring pairs; `coord(it, &map_a,
-// &map_b, &y_a, &y_b, &row)` names the tensors and coordinates of pair it,
-// `stats(it, &l2, &d, &pos)` the statistics rows to copy with it (or none;
-// positions only in the gathered mode).
+// Producer of the dK/dV kernel: the fixed pair (K, V) once, then both
+// 64-row halves of `iters` query tiles; `coord(it, &map_a, &map_b, &y_a,
+// &y_b, &row)` names the tensors (64-row boxes) and coordinates of tile it,
+// `stats(it, &l2, &d, &pos)` the tile's statistics rows (positions only in
+// the gathered mode).  Half u = 2 it + h goes to ring stage u % kRing.
 template <typename Coord, typename Stats>
 __device__ __forceinline__ void produce(uint32_t sb, const CUtensorMap* fa, const CUtensorMap* fb,
                                         int fy, int frow, int iters, Coord coord, Stats stats,
@@ -185,104 +202,106 @@ __device__ __forceinline__ void produce(uint32_t sb, const CUtensorMap* fa, cons
     ptx::tma_load_3d(sb + kOffFixB + ch * kChunkBytes, fb, bar(BAR_FIX), ch * 64, fy, frow);
   }
   int issued = 0;
-  for (int it = 0; it < iters; ++it) {
-    const int b = it & 1;
-    if (it >= 2 && !wait_bar(bar(BAR_EMPTY0 + b), ((it >> 1) - 1) & 1, ctl)) break;
+  for (int u = 0; u < 2 * iters; ++u) {
+    const int it = u >> 1, h = u & 1, st = u % kRing;
+    if (u >= kRing && !wait_bar(bar(BAR_EMPTY0 + st), ((u / kRing) - 1) & 1, ctl)) break;
     const CUtensorMap *ma, *mb;
     int ya, yb, row;
     coord(it, &ma, &mb, &ya, &yb, &row);
+    row += h * kHalfRows;
     const float *sl = nullptr, *sd = nullptr;
     const int* sp = nullptr;
     stats(it, &sl, &sd, &sp);
-    ptx::mbar_arrive_expect_tx(bar(BAR_FULL0 + b),
-                               2 * kTileBytes + (sl ? 2 * kT * 4 : 0) + (sp ? kT * 4 : 0));
-    if (sl) {  // this stage's per-query lse and D rows (512 bytes each)
-      const uint32_t dst = sb + kOffStats + b * kStatBytes;
-      ptx::bulk_load(dst, sl, kT * 4, bar(BAR_FULL0 + b));
-      ptx::bulk_load(dst + kT * 4, sd, kT * 4, bar(BAR_FULL0 + b));
-      if (sp) ptx::bulk_load(dst + 2 * kT * 4, sp, kT * 4, bar(BAR_FULL0 + b));
+    const uint32_t full = bar(BAR_FULL0 + st);
+    ptx::mbar_arrive_expect_tx(
+        full, 2 * kHalfTileBytes + (sl ? 2 * kHalfRows * 4 : 0) + (sp ? kHalfRows * 4 : 0));
+    if (sl) {  // this half's per-query lse and D rows (256 bytes each)
+      const uint32_t dst = sb + kOffStats + st * kStatBytes;
+      ptx::bulk_load(dst, sl + h * kHalfRows, kHalfRows * 4, full);
+      ptx::bulk_load(dst + kHalfRows * 4, sd + h * kHalfRows, kHalfRows * 4, full);
+      if (sp) ptx::bulk_load(dst + 2 * kHalfRows * 4, sp + h * kHalfRows, kHalfRows * 4, full);
     }
+    const uint32_t base = sb + kOffRing + st * kRingStageBytes;
     for (int ch = 0; ch < 2; ++ch) {
-      ptx::tma_load_3d(sb + kOffRingA + b * kTileBytes + ch * kChunkBytes, ma,
-                       bar(BAR_FULL0 + b), ch * 64, ya, row);
-      ptx::tma_load_3d(sb + kOffRingB + b * kTileBytes + ch * kChunkBytes, mb,
-                       bar(BAR_FULL0 + b), ch * 64, yb, row);
+      ptx::tma_load_3d(base + ch * kHalfChunk, ma, full, ch * 64, ya, row);
+      ptx::tma_load_3d(base + kHalfTileBytes + ch * kHalfChunk, mb, full, ch * 64, yb, row);
     }
-    issued = it + 1;
+    issued = u + 1;
   }
   drain_bar(bar(BAR_FIX), 0, status);
-  for (int b = 0; b < 2; ++b) {
-    int last = issued - 1;
-    if (last >= 0 && (last & 1) != b) --last;
-    if (last >= 0) drain_bar(bar(BAR_FULL0 + b), (last >> 1) & 1, status);
+  for (int st = 0; st < kRing; ++st) {
+    const int last = issued - 1 - ((issued - 1 - st) % kRing + kRing) % kRing;
+    if (last >= 0) drain_bar(bar(BAR_FULL0 + st), (last / kRing) & 1, status);
   }
 }
 
-// Score-like MMAs of one half: D[128 x 64] = A[128 x 128] B_half[64 x 128]^T,
-// 8 SS MMAs (K = 128 in steps of 16); B_half = rows 64h..64h+63 of a K-major
-// tile (8 KB into each 64-column chunk).
-__device__ __forceinline__ void mma_scores_half(uint32_t d, uint32_t a_lo, uint32_t b_lo,
-                                                int half) {
+// Score-like MMAs of one half: D[128 x 64] = A[128 x 128] B[64 x 128]^T,
+// 8 SS MMAs (K = 128 in steps of 16); A a fixed 128-row tile, B a 64-row
+// half-tile of the ring (64-column chunks 8 KB apart).
+__device__ __forceinline__ void mma_scores_half(uint32_t d, uint32_t a_lo, uint32_t b_lo) {
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kT, kHalf, false);
-  const uint32_t b_half = b_lo + ((half * kHalf * 128) >> 4);
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk) {
-    const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-    ptx::mma_ss_w(d, a_lo + off, ptx::kDescHiSw128, b_half + off, ptx::kDescHiSw128, kIdesc,
-                     kk > 0 ? 1u : 0u);
+    const uint32_t a_off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+    const uint32_t b_off = ((kk >> 2) * kHalfChunk + (kk & 3) * 32) >> 4;
+    ptx::mma_ss_w(d, a_lo + a_off, ptx::kDescHiSw128, b_lo + b_off, ptx::kDescHiSw128, kIdesc,
+                  kk > 0 ? 1u : 0u);
   }
 }
 
-// Gradient MMAs of one half: D[128 x 128] += A (bf16 in TMEM columns
-// a..a+31: 128 x 64) B_half, B_half = rows 64h..64h+63 of an MN-major tile
-// (K = 64 in steps of 16).
+// Gradient MMAs of one half: D[128 x 128] += A (128 x 64 bf16 in TMEM: the
+// packed pairs of each 32-column chunk over the first 16 columns of that
+// chunk, i.e. columns a..a+15 and a+32..a+47) B, B a 64-row half-tile of
+// the ring read MN-major (K = 64 in steps of 16).
 __device__ __forceinline__ void mma_grad_half(uint32_t d, uint32_t a_tmem, uint32_t b_mn,
-                                              int half, bool first) {
+                                              bool first) {
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kT, kD, true);
 #pragma unroll
   for (int kk = 0; kk < kHalf / 16; ++kk)
-    ptx::mma_ts_w(d, a_tmem + kk * 8, b_mn + ((half * kHalf * 128 + kk * 2048) >> 4),
-                     ptx::kDescHiSw128, kIdesc, (!first || kk > 0) ? 1u : 0u);
+    ptx::mma_ts_w(d, a_tmem + (kk >> 1) * 32 + (kk & 1) * 8, b_mn + ((kk * 2048) >> 4),
+                  ptx::kDescHiSw128, kIdesc, (!first || kk > 0) ? 1u : 0u);
 }
 
 // TMEM columns of the two halves: scores of half h at [64h.. 64h+64) of
-// the first 128, the second score-like product at +128; bf16 results
-// overwrite the first 32 columns of each (already read).
+// the first 128, the second score-like product at +128; the bf16 results of
+// each 32-column chunk overwrite the chunk's own first 16 columns (already
+// read by the warp that owns the chunk).
 __device__ __forceinline__ uint32_t col_s(int half) { return half * kHalf; }
 __device__ __forceinline__ uint32_t col_p(int half) { return 128 + half * kHalf; }
 
-// The MMA issuer's pipeline over `iters` ring stages (run by the whole MMA
-// warp).  Per stage: scores of
-// half 0 and half 1; then, as the elementwise warps finish each half, that
-// half's gradient MMAs followed by the next stage's scores of the same half,
-// so the tensor pipe works on one half while the warps process the other.
+// The MMA issuer's pipeline of the dK/dV kernel over `iters` query tiles
+// (run by the whole MMA warp).  Scores of both halves of tile 0; then, as
+// the elementwise warps finish each half, that half's gradient MMAs (which
+// release its ring stage) followed by the next tile's scores of the same
+// half, so the tensor pipe works on one half while the warps process the
+// other.  `scores(it, h, stage)` / `grads(it, h, stage)` issue the MMAs.
 template <typename Scores, typename Grads>
 __device__ __forceinline__ bool mma_pipeline(uint32_t sb, int iters, Scores scores, Grads grads,
                                              const WaitCtl& ctl) {
   auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8 * i; };
-  bool ok = wait_w(bar(BAR_FIX), 0, ctl) && wait_w(bar(BAR_FULL0), 0, ctl);
-  if (!ok) return false;
-  ptx::tc_fence_after();
-  for (int h = 0; h < 2; ++h) {
-    scores(0, h);
+  bool ok = wait_w(bar(BAR_FIX), 0, ctl);
+  for (int h = 0; ok && h < 2; ++h) {
+    if (!(ok = wait_w(bar(BAR_FULL0 + h), 0, ctl))) break;
+    ptx::tc_fence_after();
+    scores(0, h, h);
     ptx::commit_w(bar(BAR_SF0 + h));
   }
-  for (int it = 0; it < iters; ++it) {
-    const int b = it & 1;
+  for (int it = 0; ok && it < iters; ++it) {
     const bool next = it + 1 < iters;
     for (int h = 0; h < 2; ++h) {
+      const int u = 2 * it + h;
       if (!(ok = wait_w(bar(BAR_EF0 + h), it & 1, ctl))) break;
       ptx::tc_fence_after();
-      grads(it, h);
-      if (h == 1) ptx::commit_w(bar(BAR_EMPTY0 + b));  // stage b fully consumed
+      grads(it, h, u % kRing);
+      ptx::commit_w(bar(BAR_EMPTY0 + u % kRing));  // this half's stage consumed
       if (next) {
-        if (h == 0 && !(ok = wait_w(bar(BAR_FULL0 + (b ^ 1)), ((it + 1) >> 1) & 1, ctl)))
-          break;
-        scores(it + 1, h);
+        const int v = u + 2;
+        if (!(ok = wait_w(bar(BAR_FULL0 + v % kRing), (v / kRing) & 1, ctl))) break;
+        ptx::tc_fence_after();
+        scores(it + 1, h, v % kRing);
         ptx::commit_w(bar(BAR_SF0 + h));
       }
     }
-    if (!ok) break;
   }
   if (ok) ptx::commit_w(bar(BAR_ACC));
   return ok;
@@ -291,8 +310,9 @@ __device__ __forceinline__ bool mma_pipeline(uint32_t sb, int iters, Scores scor
 // --------------------------------------------------------------------- dQ
 // The dQ kernel keeps one accumulator (dQ), so its 512 TMEM columns hold two
 // full-width score buffers and dP besides: S of even / odd key tiles at
-// 0..127 / 128..255 (dS over the first 64 columns of its tile's S), dQ at
-// 256..383, dP at 384..511.  Score MMAs are full width (N = 128).
+// 0..127 / 128..255 (the packed dS of each 32-key chunk over the first 16
+// columns of that chunk), dQ at 256..383, dP at 384..511.  Score MMAs are
+// full width (N = 128).
 __device__ __forceinline__ uint32_t dq_col_s(int t) { return static_cast<uint32_t>(t & 1) * 128; }
 constexpr uint32_t kDqColQ = 256;
 constexpr uint32_t kDqColP = 384;
@@ -312,7 +332,7 @@ enum {
   DQ_FULLV0 = 7,   // V stage s landed (7, 8)
   DQ_EMPTYV0 = 9,  // V stage s consumed (9, 10)
   DQ_SF = 11,      // S and dP of a tile computed
-  DQ_EF = 12,      // dS of a tile written, 4 warp arrivals
+  DQ_EF = 12,      // dS of a tile written, one arrival per elementwise warp
   DQ_ACC = 13,     // dQ final
   DQ_CLEAN = 14,
   kDqNumBars = 15
@@ -324,12 +344,13 @@ static_assert(kDqSmemBytes <= 227 * 1024, "dQ kernel shared memory");
 
 __device__ __forceinline__ uint32_t dq_setup(uint8_t* smem, uint32_t sb, int warp) {
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kDqNumBars; ++i) ptx::mbar_init(sb + kDqOffBar + 8 * i, i == DQ_EF ? 4 : 1);
+    for (int i = 0; i < kDqNumBars; ++i)
+      ptx::mbar_init(sb + kDqOffBar + 8 * i, i == DQ_EF ? kEwWarps : 1);
     *reinterpret_cast<volatile int*>(smem + kDqOffAbort) = 0;
     ptx::fence_mbar_init();
     ptx::fence_async_shared();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(smem + kDqOffTmemSlot), 512);
     ptx::tmem_relinquish();
   }
@@ -443,7 +464,8 @@ __device__ __forceinline__ bool dq_pipeline(uint32_t sb, uint32_t tmem, int iter
     const uint32_t kb = k_mn + sk * kTileLo;
 #pragma unroll
     for (int kk = 0; kk < kT / 16; ++kk)
-      ptx::mma_ts_w(tmem + kDqColQ, a + kk * 8, kb + ((kk * 2048) >> 4), ptx::kDescHiSw128,
+      ptx::mma_ts_w(tmem + kDqColQ, a + (kk >> 1) * 32 + (kk & 1) * 8, kb + ((kk * 2048) >> 4),
+                    ptx::kDescHiSw128,
                        kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
     ptx::commit_w(bar(DQ_EMPTYK0 + sk));  // K(t) consumed
   }
@@ -487,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
   const uint32_t tmem = dq_setup(smem, sb, warp);
   WaitCtl ctl{reinterpret_cast<volatile int*>(smem + kDqOffAbort), p.status, p.wait_ns};
 
-  if (warp == 4) {
+  if (warp == kProdWarp) {
     if (lane == 0) {
       auto coord = [&](int t, const CUtensorMap** mk, const CUtensorMap** mv, int* row) {
         const bool lm = t < n_lm_tiles;
@@ -497,13 +519,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
       };
       dq_produce(sb, &p.tm_q, &p.tm_do, fy, static_cast<int>(qr0), T, c, coord, ctl, p.status);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     dq_pipeline(sb, tmem, T, ctl);
     ptx::commit_w(bar(DQ_CLEAN));
     drain_bar(bar(DQ_CLEAN), 0, p.status);
-  } else if (warp < 4) {
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int64_t i_row = qr0 + threadIdx.x;  // query row, or gathered M row
+  } else if (warp < kEwWarps) {
+    const int quarter = warp & 3;  // TMEM lanes (rows) 32 quarter ..
+    const int cp = warp >> 2;      // key columns [64 cp, 64 cp + 64) of each tile
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int64_t i_row = qr0 + quarter * 32 + lane;  // query row, or gathered M row
     // Position of the row (its own index outside the gathered mode).
     const int64_t i = kG ? p.gpos[i_row] : i_row;
     const bool row_ok = kG ? i >= 0 : i < p.n;
@@ -536,7 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
       const bool full = lo_c == 0 && hi_c == kT;
       const uint32_t ts = tl + dq_col_s(t);
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int ci = 0; ci < 2; ++ci) {
+        const int cc = 2 * cp + ci;  // 32-column chunk
         float s[32], dp[32];
         ptx::tmem_ld32(ts + cc * 32, s);
         ptx::tmem_ld32(tl + kDqColP + cc * 32, dp);
@@ -559,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
           ptx::f2_split(ptx::mul2(pr, ptx::add2(ptx::f2(dp[2 * e], dp[2 * e + 1]), nD2)), d0, d1);
           pk[e] = ptx::pack_bf16x2(d0, d1);
         }
-        ptx::tmem_st16(ts + cc * 16, pk);  // dS over S columns already read
+        ptx::tmem_st16(ts + cc * 32, pk);  // dS over S columns this warp has read
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -575,7 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
           kG ? ((static_cast<int64_t>(split) * p.Hkv + c) * p.Mp + i_row) * kD
                   : (i_row * p.Hq + h) * static_cast<int64_t>(kD);
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int ci = 0; ci < 2; ++ci) {  // this warp's 64 of the 128 columns
+        const int cc = 2 * cp + ci;
         float o[32];
         ptx::tmem_ld32(tl + kDqColQ + cc * 32, o);
         ptx::tmem_wait_ld();
@@ -633,12 +659,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bwd_setup(smem, sb, warp);
   WaitCtl ctl{reinterpret_cast<volatile int*>(smem + kOffAbort), p.status, p.wait_ns};
 
-  if (warp == 4) {
+  if (warp == kProdWarp) {
     if (lane == 0) {
       auto coord = [&](int it, const CUtensorMap** ma, const CUtensorMap** mb, int* ya, int* yb,
                        int* row) {
-        *ma = &p.tm_q;
-        *mb = &p.tm_do;
+        *ma = &p.tm_q64;
+        *mb = &p.tm_do64;
         *ya = *yb = kG ? c : c * p.group + it % p.group;
         *row = static_cast<int>((qt_lo + it / hpi) * kT);
       };
@@ -654,42 +680,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       produce(sb, p.lm_mode ? &p.tm_klm : &p.tm_k, p.lm_mode ? &p.tm_vlm : &p.tm_v, c,
               static_cast<int>(kb), iters, coord, stats, ctl, p.status);
     }
-  } else if (warp == 5) {  // the whole warp issues (elect.sync inside)
+  } else if (warp == kMmaWarp) {  // the whole warp issues (elect.sync inside)
     {
       const uint32_t k_lo = ptx::desc_lo(sb + kOffFixA, 16);
       const uint32_t v_lo = ptx::desc_lo(sb + kOffFixB, 16);
-      const uint32_t q_lo = ptx::desc_lo(sb + kOffRingA, 16);
-      const uint32_t do_lo = ptx::desc_lo(sb + kOffRingB, 16);
-      const uint32_t q_mn = ptx::desc_lo(sb + kOffRingA, kChunkBytes);
-      const uint32_t do_mn = ptx::desc_lo(sb + kOffRingB, kChunkBytes);
-      auto scores = [&](int it, int half) {
-        const uint32_t st = (it & 1) * kTileLo;
-        mma_scores_half(tmem + col_s(half), k_lo, q_lo + st, half);   // S^T  = K Q^T
-        mma_scores_half(tmem + col_p(half), v_lo, do_lo + st, half);  // dP^T = V dO^T
+      constexpr uint32_t kStageLo = kRingStageBytes >> 4;
+      constexpr uint32_t kDoLo = kHalfTileBytes >> 4;
+      const uint32_t r_lo = ptx::desc_lo(sb + kOffRing, 16);            // K-major view
+      const uint32_t r_mn = ptx::desc_lo(sb + kOffRing, kHalfChunk);    // MN-major view
+      auto scores = [&](int it, int half, int st) {
+        (void)it;
+        const uint32_t q = r_lo + st * kStageLo;
+        mma_scores_half(tmem + col_s(half), k_lo, q);          // S^T  = K Q^T
+        mma_scores_half(tmem + col_p(half), v_lo, q + kDoLo);  // dP^T = V dO^T
       };
-      auto grads = [&](int it, int half) {
-        const uint32_t st = (it & 1) * kTileLo;
+      auto grads = [&](int it, int half, int st) {
+        const uint32_t q = r_mn + st * kStageLo;
         const bool first = it == 0 && half == 0;
-        mma_grad_half(tmem + 256, tmem + col_s(half), do_mn + st, half, first);  // dV += P^T dO
-        mma_grad_half(tmem + 384, tmem + col_p(half), q_mn + st, half, first);   // dK += dS^T Q
+        mma_grad_half(tmem + 256, tmem + col_s(half), q + kDoLo, first);  // dV += P^T dO
+        mma_grad_half(tmem + 384, tmem + col_p(half), q, first);          // dK += dS^T Q
       };
       mma_pipeline(sb, iters, scores, grads, ctl);
       ptx::commit_w(bar(BAR_CLEAN));
       drain_bar(bar(BAR_CLEAN), 0, p.status);
     }
-  } else if (warp < 4) {
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int64_t j = kb + threadIdx.x;  // key (window mode) or landmark (landmark mode)
+  } else if (warp < kEwWarps) {
+    const int quarter = warp & 3;  // TMEM lanes (rows) 32 quarter ..
+    const int cp = warp >> 2;      // query columns [32 cp, 32 cp + 32) of each half
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    // Key (window mode) or landmark (landmark mode) of this row.
+    const int64_t j = kb + quarter * 32 + lane;
     const uint64_t c2 = ptx::f2(p.scale_log2, p.scale_log2);
     bool ok = true;
     for (int it = 0; ok && it < iters; ++it) {
       const int64_t qr0 = (qt_lo + it / hpi) * kT;
-      // This iteration's per-query -lse (log2 units) and -D came with its
-      // Q / dO stage; the stage has landed once its scores exist, and it is
-      // not refilled before this iteration's results are in.
-      const float* sL = reinterpret_cast<const float*>(smem + kOffStats + (it & 1) * kStatBytes);
-      const float* sD = sL + kT;
-      const int* sP = reinterpret_cast<const int*>(sD + kT);  // positions (gathered mode)
+      // Each half's per-query -lse (log2 units) and -D came with its Q / dO
+      // stage; the stage has landed once its scores exist, and it is not
+      // refilled before this half's results are in.
       // Rows i of this query tile that see key/landmark j: [lo, hi) columns.
       int64_t lo, hi;
       if constexpr (kG) {  // per column below (each M row has its own position)
@@ -703,18 +730,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         hi = j + p.window - qr0;
       }
       for (int half = 0; half < 2; ++half) {
+        const int u = 2 * it + half;
         ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF0 + half), it & 1, ctl));
-        if (ok && half == 0)  // completed already; makes the copied rows visible here
-          ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_FULL0 + (it & 1)), (it >> 1) & 1, ctl));
+        if (ok)  // completed already; makes the copied rows visible here
+          ok = __all_sync(0xffffffffu,
+                          wait_bar(bar(BAR_FULL0 + u % kRing), (u / kRing) & 1, ctl));
         if (!ok) break;
+        const float* sL =
+            reinterpret_cast<const float*>(smem + kOffStats + (u % kRing) * kStatBytes);
+        const float* sD = sL + kHalfRows;
+        const int* sP = reinterpret_cast<const int*>(sD + kHalfRows);  // gathered mode
         ptx::tc_fence_after();
         const int lo_c = static_cast<int>(max64(0, min64(kHalf, lo - half * kHalf)));
         const int hi_c = static_cast<int>(max64(0, min64(kHalf, hi - half * kHalf)));
-        const float4* hL = reinterpret_cast<const float4*>(sL + half * kHalf);
-        const float4* hD = reinterpret_cast<const float4*>(sD + half * kHalf);
+        const float4* hL = reinterpret_cast<const float4*>(sL);
+        const float4* hD = reinterpret_cast<const float4*>(sD);
         const bool full = lo_c == 0 && hi_c == kHalf;
-#pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
+        {
+          const int cc = cp;  // this warp's 32-column chunk of the half
           float s[32], dp[32];
           ptx::tmem_ld32(tl + col_s(half) + cc * 32, s);
           ptx::tmem_ld32(tl + col_p(half) + cc * 32, dp);
@@ -727,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if constexpr (kG) {  // global row m sees key j iff j <= its position
-            const int* hp = sP + half * kHalf + cc * 32;
+            const int* hp = sP + cc * 32;
 #pragma unroll
             for (int e = 0; e < 32; ++e) s[e] = j <= hp[e] ? s[e] : -INFINITY;
           }
@@ -752,8 +785,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               dd[e] = ptx::pack_bf16x2(d0, d1);
             }
           }
-          ptx::tmem_st16(tl + col_s(half) + cc * 16, pp);  // P^T over columns already read
-          ptx::tmem_st16(tl + col_p(half) + cc * 16, dd);  // dS^T likewise
+          ptx::tmem_st16(tl + col_s(half) + cc * 32, pp);  // P^T over columns read above
+          ptx::tmem_st16(tl + col_p(half) + cc * 32, dd);  // dS^T likewise
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -767,29 +800,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kG) {  // the global rows' share of dK (scaled) and dV, fp32
         const bool row_ok = j < p.n;
         const int64_t off = (j * p.Hkv + c) * static_cast<int64_t>(kD);
-        for (int which = 0; which < 2; ++which) {
+        const int which = cp;  // 0: dK (warps 0-3), 1: dV (warps 4-7)
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            float o[32];
-            ptx::tmem_ld32(tl + (which == 0 ? 384 : 256) + cc * 32, o);
-            ptx::tmem_wait_ld();
-            if (row_ok)
-              store_row(which == 0 ? p.extra_k : p.extra_v, off + cc * 32, o,
-                        which == 0 ? p.scale : 1.f, 0);
-          }
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          ptx::tmem_ld32(tl + (which == 0 ? 384 : 256) + cc * 32, o);
+          ptx::tmem_wait_ld();
+          if (row_ok)
+            store_row(which == 0 ? p.extra_k : p.extra_v, off + cc * 32, o,
+                      which == 0 ? p.scale : 1.f, 0);
         }
       } else if (p.lm_mode) {
         const bool row_ok = j < p.G;
-        for (int which = 0; which < 2; ++which) {  // 0: dK_lm, 1: dV_lm
-          float* dst = p.lm_part + ((((static_cast<int64_t>(chunk) * 2 + which) * p.G + j) *
-                                     p.Hkv + c) * kD);
+        const int which = cp;  // 0: dK_lm (warps 0-3), 1: dV_lm (warps 4-7)
+        float* dst = p.lm_part + ((((static_cast<int64_t>(chunk) * 2 + which) * p.G + j) *
+                                   p.Hkv + c) * kD);
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            float o[32];
-            ptx::tmem_ld32(tl + (which == 0 ? 384 : 256) + cc * 32, o);
-            ptx::tmem_wait_ld();
-            if (row_ok) store_row(dst, cc * 32, o, which == 0 ? p.scale : 1.f, 0);
-          }
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          ptx::tmem_ld32(tl + (which == 0 ? 384 : 256) + cc * 32, o);
+          ptx::tmem_wait_ld();
+          if (row_ok) store_row(dst, cc * 32, o, which == 0 ? p.scale : 1.f, 0);
         }
       } else {
         const bool row_ok = j < p.n;
@@ -803,7 +834,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           lmv = p.lm_grad + ((static_cast<int64_t>(p.G) + l) * p.Hkv + c) * kD;
         }
         const float invB = 1.f / static_cast<float>(p.block);
-        for (int which = 0; which < 2; ++which) {  // 0: dK, 1: dV
+        {
+          const int which = cp;  // 0: dK (warps 0-3), 1: dV (warps 4-7)
           const float* lm = which == 0 ? lmk : lmv;
           const float w = which == 0 ? p.scale : 1.f;
 #pragma unroll 1
@@ -1035,6 +1067,11 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why) 
       return cudaErrorInvalidValue;
     }
   }
+  if (!encode_map(fn, &p.tm_q64, a.q, a.n, a.Hq, kHalfRows) ||
+      !encode_map(fn, &p.tm_do64, a.dout, a.n, a.Hq, kHalfRows)) {
+    *why = "cuTensorMapEncodeTiled rejected q or dout (64-row boxes)";
+    return cudaErrorInvalidValue;
+  }
   if (a.G == 0) {
     p.tm_klm = p.tm_k;
     p.tm_vlm = p.tm_v;
@@ -1103,7 +1140,9 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why) 
     if (e != cudaSuccess) return e;
     pg = p;
     if (!encode_map(fn, &pg.tm_q, a.Qg, a.Mp, a.Hkv) ||
-        !encode_map(fn, &pg.tm_do, a.dOg, a.Mp, a.Hkv)) {
+        !encode_map(fn, &pg.tm_do, a.dOg, a.Mp, a.Hkv) ||
+        !encode_map(fn, &pg.tm_q64, a.Qg, a.Mp, a.Hkv, kHalfRows) ||
+        !encode_map(fn, &pg.tm_do64, a.dOg, a.Mp, a.Hkv, kHalfRows)) {
       *why = "cuTensorMapEncodeTiled rejected the gathered rows";
       return cudaErrorInvalidValue;
     }

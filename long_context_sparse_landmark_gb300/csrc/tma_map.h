@@ -32,15 +32,16 @@ inline EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// [rows, H, 128] bf16 tensor, boxes of 64 (d) x 1 (head) x 128 (rows),
-// 128-byte swizzle: each box lands as 128 rows of 128 bytes, the canonical
-// K-major SW128 layout for Q/K and the MN-major SW128 layout for V.
-inline bool encode_map(EncodeTiledFn fn, CUtensorMap* m, const void* ptr, int64_t rows, int H) {
+// [rows, H, 128] bf16 tensor, boxes of 64 (d) x 1 (head) x box_rows (rows),
+// 128-byte swizzle: each box lands as box_rows rows of 128 bytes, the
+// canonical K-major SW128 layout for Q/K and the MN-major SW128 layout for V.
+inline bool encode_map(EncodeTiledFn fn, CUtensorMap* m, const void* ptr, int64_t rows, int H,
+                       uint32_t box_rows = 128) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kMapD), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(kMapD) * 2,
                            static_cast<cuuint64_t>(H) * kMapD * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
