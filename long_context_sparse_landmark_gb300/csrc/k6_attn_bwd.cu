@@ -335,7 +335,8 @@ enum {
   DQ_EF = 12,      // dS of a tile written, one arrival per elementwise warp
   DQ_ACC = 13,     // dQ final
   DQ_CLEAN = 14,
-  kDqNumBars = 15
+  DQ_PFREE = 15,   // every elementwise warp has read the tile's dP
+  kDqNumBars = 16
 };
 constexpr int kDqOffTmemSlot = kDqOffBar + 8 * kDqNumBars;
 constexpr int kDqOffAbort = kDqOffTmemSlot + 8;
@@ -345,7 +346,7 @@ static_assert(kDqSmemBytes <= 227 * 1024, "dQ kernel shared memory");
 __device__ __forceinline__ uint32_t dq_setup(uint8_t* smem, uint32_t sb, int warp) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDqNumBars; ++i)
-      ptx::mbar_init(sb + kDqOffBar + 8 * i, i == DQ_EF ? kEwWarps : 1);
+      ptx::mbar_init(sb + kDqOffBar + 8 * i, (i == DQ_EF || i == DQ_PFREE) ? kEwWarps : 1);
     *reinterpret_cast<volatile int*>(smem + kDqOffAbort) = 0;
     ptx::fence_mbar_init();
     ptx::fence_async_shared();
@@ -421,9 +422,10 @@ __device__ __forceinline__ void mma_scores_full(uint32_t d, uint32_t a_lo, uint3
 // MMA issue order of the dQ kernel (run by the whole MMA warp), tile t's
 // elementwise pass running:
 // S(t+1) into the other S buffer (its dS(t-1) was read by dQ(t-1), issued
-// earlier), then -- once the pass is done with dP(t) -- dP(t+1), then
-// dQ += dS(t) K(t).  The tensor pipe computes dQ(t) and S(t+2) while the
-// warps process tile t+1; only dP(t+1) runs with the warps idle.
+// earlier), then -- once every warp has read dP(t), before the pass ends --
+// dP(t+1), then, once dS(t) is written, dQ += dS(t) K(t).  The tensor pipe
+// computes dQ(t) and S(t+2) while the warps process tile t+1, and most of
+// dP(t+1) while they finish tile t.
 __device__ __forceinline__ bool dq_pipeline(uint32_t sb, uint32_t tmem, int iters,
                                             const WaitCtl& ctl) {
   auto bar = [&](int i) -> uint32_t { return sb + kDqOffBar + 8 * i; };
@@ -449,7 +451,7 @@ __device__ __forceinline__ bool dq_pipeline(uint32_t sb, uint32_t tmem, int iter
       ptx::tc_fence_after();
       mma_scores_full(tmem + dq_col_s(t + 1), q_lo, k_lo + sk * kTileLo);
     }
-    if (!(ok = wait_w(bar(DQ_EF), t & 1, ctl))) break;
+    if (!(ok = wait_w(bar(DQ_PFREE), t & 1, ctl))) break;
     ptx::tc_fence_after();
     if (next) {
       const int sv = (t + 1) % kDqVStages;
@@ -459,6 +461,8 @@ __device__ __forceinline__ bool dq_pipeline(uint32_t sb, uint32_t tmem, int iter
       ptx::commit_w(bar(DQ_SF));
       ptx::commit_w(bar(DQ_EMPTYV0 + sv));  // V(t+1) consumed
     }
+    if (!(ok = wait_w(bar(DQ_EF), t & 1, ctl))) break;
+    ptx::tc_fence_after();
     const int sk = t % kDqKStages;
     const uint32_t a = tmem + dq_col_s(t);
     const uint32_t kb = k_mn + sk * kTileLo;
@@ -566,6 +570,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
         ptx::tmem_ld32(ts + cc * 32, s);
         ptx::tmem_ld32(tl + kDqColP + cc * 32, dp);
         ptx::tmem_wait_ld();
+        if (ci == 1) {  // this warp's last read of dP: dP(t+1) may overwrite it
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(DQ_PFREE));
+        }
         if (!full) {  // masked columns: weight 0
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
