@@ -489,10 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         // p = 2^(s*scale*log2e - m) two at a time (packed FMA), rounded to
         // bf16 pairs for the PV MMA; the denominator sums those same
         // rounded weights (so O is normalised by exactly the weights it was
-        // built from), in two packed accumulators.
+        // built from), added to four fp32 partial sums as they are.
         const uint64_t c2 = ptx::f2(sl2, sl2);
         const uint64_t nb2 = ptx::f2(-mb, -mb);
-        uint64_t acc0 = ptx::f2(0.f, 0.f), acc1 = ptx::f2(0.f, 0.f);
+        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t pk[16];
@@ -503,21 +503,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             float x0, x1;
             ptx::f2_split(x, x0, x1);
             pk[e] = ptx::pack_bf16x2(ptx::ex2(x0), ptx::ex2(x1));
-            const uint64_t r =
-                ptx::f2(__uint_as_float(pk[e] << 16), __uint_as_float(pk[e] & 0xffff0000u));
             if (e & 1)
-              acc1 = ptx::add2(acc1, r);
+              ptx::acc_bf16x2(l2, l3, pk[e]);
             else
-              acc0 = ptx::add2(acc0, r);
+              ptx::acc_bf16x2(l0, l1, pk[e]);
           }
           ptx::tmem_st16(tS + cc * 16, pk);
         }
-        {
-          float l0, l1, l2, l3;
-          ptx::f2_split(acc0, l0, l1);
-          ptx::f2_split(acc1, l2, l3);
-          l += (l0 + l1) + (l2 + l3);
-        }
+        l += (l0 + l1) + (l2 + l3);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();

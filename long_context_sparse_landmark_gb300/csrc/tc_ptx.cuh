@@ -241,6 +241,18 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// a_lo += float(low bf16 of pk), a_hi += float(high bf16 of pk): the
+// mixed-precision f32 add takes the bf16 operand as it is (exact
+// widening), rounding only the f32 sum.
+__device__ __forceinline__ void acc_bf16x2(float& a_lo, float& a_hi, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\t"
+      "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(a_lo), "+f"(a_hi)
+      : "r"(pk));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
