@@ -581,8 +581,12 @@ static BwdPlan bwd_plan(int64_t n, int Hq, int Hkv, int d, int G) {
   BwdPlan P{};
   const int64_t n_qt = (n + 127) / 128;
   if (G > 0) {
+    // Landmark-mode grid: (landmark tile, KV head, query chunk).  Landmark
+    // tile l is seen only by the rows past its blocks, so about half of the
+    // CTAs find work; 2048 / per chunks make that several waves of the SMs
+    // (a ~256 MB partial buffer whatever G is).
     const int64_t per = ((G + 127) / 128) * static_cast<int64_t>(Hkv);
-    int64_t ch = (512 + per - 1) / per;
+    int64_t ch = (2048 + per - 1) / per;
     ch = ch < 1 ? 1 : (ch > n_qt ? n_qt : ch);
     P.chunk_tiles = static_cast<int>((n_qt + ch - 1) / ch);
     P.lm_chunks = static_cast<int>((n_qt + P.chunk_tiles - 1) / P.chunk_tiles);
