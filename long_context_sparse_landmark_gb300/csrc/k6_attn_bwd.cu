@@ -37,9 +37,10 @@
 //   one half while the warps process the other.  Q and dO arrive in 64-row
 //   halves through a 4-stage ring, each half released by its own MMAs.
 //   dQ: one accumulator leaves room for two full-width S buffers, so the
-//   next tile's S is computed during the elementwise pass and only its dP
-//   waits for the pass; K and V come through separate rings (three K
-//   stages, since K is read until the late dQ MMAs).
+//   next tile's S is computed during the elementwise pass and its dP as
+//   soon as every warp has read this tile's dP; K and V come through
+//   separate rings (three K stages, since K is read until the late dQ
+//   MMAs).
 // Every wait is bounded; a wait that runs out aborts the CTA cleanly.
 #include <cuda.h>
 #include <math.h>
@@ -149,7 +150,7 @@ __device__ __forceinline__ void store_row(void* base, int64_t off, const float (
   }
 }
 
-// Shared set-up of both kernels: barriers, TMEM (512 columns).
+// Set-up of the dK/dV kernel: barriers, TMEM (512 columns).
 __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t sb, int warp) {
   if (threadIdx.x == 0) {
     ptx::mbar_init(sb + kOffBar + 8 * BAR_FIX, 1);
@@ -177,6 +178,7 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t sb, int wa
   return *reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
 }
 
+// Teardown of both kernels: every role done with TMEM, then free it.
 __device__ __forceinline__ void bwd_teardown(uint32_t tmem, int warp) {
   ptx::tc_fence_before();
   __syncthreads();
