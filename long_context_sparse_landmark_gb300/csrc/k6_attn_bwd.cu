@@ -36,11 +36,11 @@
 //   tile's scores of that half follow at once -- the tensor pipe works on
 //   one half while the warps process the other.  Q and dO arrive in 64-row
 //   halves through a 4-stage ring, each half released by its own MMAs.
-//   dQ: one accumulator leaves room for two full-width S buffers, so the
-//   next tile's S is computed during the elementwise pass and its dP as
-//   soon as every warp has read this tile's dP; K and V come through
-//   separate rings (three K stages, since K is read until the late dQ
-//   MMAs).
+//   dQ: one accumulator leaves room for two full-width dP buffers (dS is
+//   written over its tile's dP), so the next tile's dP is computed during
+//   the elementwise pass and its S as soon as every warp has read this
+//   tile's S; K and V come through separate rings (three K stages, since K
+//   is read until the late dQ MMAs).
 // Every wait is bounded; a wait that runs out aborts the CTA cleanly.
 #include <cuda.h>
 #include <math.h>
@@ -310,14 +310,16 @@ __device__ __forceinline__ bool mma_pipeline(uint32_t sb, int iters, Scores scor
 }
 
 // --------------------------------------------------------------------- dQ
-// The dQ kernel keeps one accumulator (dQ), so its 512 TMEM columns hold two
-// full-width score buffers and dP besides: S of even / odd key tiles at
-// 0..127 / 128..255 (the packed dS of each 32-key chunk over the first 16
-// columns of that chunk), dQ at 256..383, dP at 384..511.  Score MMAs are
+// The dQ kernel keeps one accumulator (dQ), so its 512 TMEM columns hold S,
+// dQ and two full-width dP buffers: S at 0..127, dQ at 128..255, dP of even
+// / odd key tiles at 256..383 / 384..511 (the packed dS of each 32-key chunk
+// over the first 16 columns of that chunk of its tile's dP).  Score MMAs are
 // full width (N = 128).
-__device__ __forceinline__ uint32_t dq_col_s(int t) { return static_cast<uint32_t>(t & 1) * 128; }
-constexpr uint32_t kDqColQ = 256;
-constexpr uint32_t kDqColP = 384;
+constexpr uint32_t kDqColS = 0;
+constexpr uint32_t kDqColQ = 128;
+__device__ __forceinline__ uint32_t dq_col_p(int t) {
+  return 256 + static_cast<uint32_t>(t & 1) * 128;
+}
 
 // Shared memory of the dQ kernel: Q and dO (fixed), then separate K and V
 // rings -- K(t) is read until dQ(t), late in the pipeline, V(t) only by
@@ -337,7 +339,7 @@ enum {
   DQ_EF = 12,      // dS of a tile written, one arrival per elementwise warp
   DQ_ACC = 13,     // dQ final
   DQ_CLEAN = 14,
-  DQ_PFREE = 15,   // every elementwise warp has read the tile's dP
+  DQ_SFREE = 15,   // every elementwise warp has read the tile's S
   kDqNumBars = 16
 };
 constexpr int kDqOffTmemSlot = kDqOffBar + 8 * kDqNumBars;
@@ -348,7 +350,7 @@ static_assert(kDqSmemBytes <= 227 * 1024, "dQ kernel shared memory");
 __device__ __forceinline__ uint32_t dq_setup(uint8_t* smem, uint32_t sb, int warp) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDqNumBars; ++i)
-      ptx::mbar_init(sb + kDqOffBar + 8 * i, (i == DQ_EF || i == DQ_PFREE) ? kEwWarps : 1);
+      ptx::mbar_init(sb + kDqOffBar + 8 * i, (i == DQ_EF || i == DQ_SFREE) ? kEwWarps : 1);
     *reinterpret_cast<volatile int*>(smem + kDqOffAbort) = 0;
     ptx::fence_mbar_init();
     ptx::fence_async_shared();
@@ -422,12 +424,11 @@ __device__ __forceinline__ void mma_scores_full(uint32_t d, uint32_t a_lo, uint3
 }
 
 // MMA issue order of the dQ kernel (run by the whole MMA warp), tile t's
-// elementwise pass running:
-// S(t+1) into the other S buffer (its dS(t-1) was read by dQ(t-1), issued
-// earlier), then -- once every warp has read dP(t), before the pass ends --
-// dP(t+1), then, once dS(t) is written, dQ += dS(t) K(t).  The tensor pipe
-// computes dQ(t) and S(t+2) while the warps process tile t+1, and most of
-// dP(t+1) while they finish tile t.
+// elementwise pass running: dP(t+1) into the other dP buffer (its dS(t-1)
+// was read by dQ(t-1), issued earlier); S(t+1) as soon as every warp has
+// read S(t), at the start of the pass; dQ += dS(t) K(t) once dS(t) is
+// written.  Both score products of the next tile are done while the warps
+// process this one.
 __device__ __forceinline__ bool dq_pipeline(uint32_t sb, uint32_t tmem, int iters,
                                             const WaitCtl& ctl) {
   auto bar = [&](int i) -> uint32_t { return sb + kDqOffBar + 8 * i; };
@@ -441,38 +442,34 @@ __device__ __forceinline__ bool dq_pipeline(uint32_t sb, uint32_t tmem, int iter
             wait_w(bar(DQ_FULLV0), 0, ctl);
   if (!ok) return false;
   ptx::tc_fence_after();
-  mma_scores_full(tmem + dq_col_s(0), q_lo, k_lo);  // S  = Q K^T
-  mma_scores_full(tmem + kDqColP, do_lo, v_lo);     // dP = dO V^T
-  ptx::commit_w(bar(DQ_SF));
+  mma_scores_full(tmem + dq_col_p(0), do_lo, v_lo);  // dP = dO V^T
   ptx::commit_w(bar(DQ_EMPTYV0));
+  mma_scores_full(tmem + kDqColS, q_lo, k_lo);       // S  = Q K^T
+  ptx::commit_w(bar(DQ_SF));
   for (int t = 0; t < iters; ++t) {
     const bool next = t + 1 < iters;
-    if (next) {
-      const int sk = (t + 1) % kDqKStages;
-      if (!(ok = wait_w(bar(DQ_FULLK0 + sk), ((t + 1) / kDqKStages) & 1, ctl))) break;
-      ptx::tc_fence_after();
-      mma_scores_full(tmem + dq_col_s(t + 1), q_lo, k_lo + sk * kTileLo);
-    }
-    if (!(ok = wait_w(bar(DQ_PFREE), t & 1, ctl))) break;
-    ptx::tc_fence_after();
     if (next) {
       const int sv = (t + 1) % kDqVStages;
       if (!(ok = wait_w(bar(DQ_FULLV0 + sv), ((t + 1) / kDqVStages) & 1, ctl))) break;
       ptx::tc_fence_after();
-      mma_scores_full(tmem + kDqColP, do_lo, v_lo + sv * kTileLo);
-      ptx::commit_w(bar(DQ_SF));
+      mma_scores_full(tmem + dq_col_p(t + 1), do_lo, v_lo + sv * kTileLo);
       ptx::commit_w(bar(DQ_EMPTYV0 + sv));  // V(t+1) consumed
+      const int sk = (t + 1) % kDqKStages;
+      if (!(ok = wait_w(bar(DQ_FULLK0 + sk), ((t + 1) / kDqKStages) & 1, ctl))) break;
+      if (!(ok = wait_w(bar(DQ_SFREE), t & 1, ctl))) break;
+      ptx::tc_fence_after();
+      mma_scores_full(tmem + kDqColS, q_lo, k_lo + sk * kTileLo);
+      ptx::commit_w(bar(DQ_SF));
     }
     if (!(ok = wait_w(bar(DQ_EF), t & 1, ctl))) break;
     ptx::tc_fence_after();
     const int sk = t % kDqKStages;
-    const uint32_t a = tmem + dq_col_s(t);
+    const uint32_t a = tmem + dq_col_p(t);
     const uint32_t kb = k_mn + sk * kTileLo;
 #pragma unroll
     for (int kk = 0; kk < kT / 16; ++kk)
       ptx::mma_ts_w(tmem + kDqColQ, a + (kk >> 1) * 32 + (kk & 1) * 8, kb + ((kk * 2048) >> 4),
-                    ptx::kDescHiSw128,
-                       kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+                    ptx::kDescHiSw128, kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
     ptx::commit_w(bar(DQ_EMPTYK0 + sk));  // K(t) consumed
   }
   if (ok) ptx::commit_w(bar(DQ_ACC));
@@ -564,24 +561,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
       const int lo_c = static_cast<int>(max64(0, min64(kT, lo)));
       const int hi_c = static_cast<int>(max64(0, min64(kT, hi)));
       const bool full = lo_c == 0 && hi_c == kT;
-      const uint32_t ts = tl + dq_col_s(t);
-#pragma unroll 1
+      const uint32_t tp = tl + dq_col_p(t);
+      // This warp's two 32-column chunks of S and dP, all read before S is
+      // released for the next tile's S MMAs.
+      float s[2][32], dp[2][32];
+#pragma unroll
+      for (int ci = 0; ci < 2; ++ci) {
+        ptx::tmem_ld32(tl + kDqColS + (2 * cp + ci) * 32, s[ci]);
+        ptx::tmem_ld32(tp + (2 * cp + ci) * 32, dp[ci]);
+      }
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(DQ_SFREE));
+#pragma unroll
       for (int ci = 0; ci < 2; ++ci) {
         const int cc = 2 * cp + ci;  // 32-column chunk
-        float s[32], dp[32];
-        ptx::tmem_ld32(ts + cc * 32, s);
-        ptx::tmem_ld32(tl + kDqColP + cc * 32, dp);
-        ptx::tmem_wait_ld();
-        if (ci == 1) {  // this warp's last read of dP: dP(t+1) may overwrite it
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(bar(DQ_PFREE));
-        }
         if (!full) {  // masked columns: weight 0
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int col = cc * 32 + e;
-            s[e] = (col >= lo_c && col < hi_c) ? s[e] : -INFINITY;
+            s[ci][e] = (col >= lo_c && col < hi_c) ? s[ci][e] : -INFINITY;
           }
         }
         uint32_t pk[16];
@@ -589,13 +589,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
         for (int e = 0; e < 16; ++e) {
           // p = 2^(s scale log2e - lse log2e), dS = p (dP - D)
           float x0, x1;
-          ptx::f2_split(ptx::fma2(ptx::f2(s[2 * e], s[2 * e + 1]), c2, nL22), x0, x1);
+          ptx::f2_split(ptx::fma2(ptx::f2(s[ci][2 * e], s[ci][2 * e + 1]), c2, nL22), x0, x1);
           const uint64_t pr = ptx::f2(ptx::ex2(x0), ptx::ex2(x1));
           float d0, d1;
-          ptx::f2_split(ptx::mul2(pr, ptx::add2(ptx::f2(dp[2 * e], dp[2 * e + 1]), nD2)), d0, d1);
+          ptx::f2_split(
+              ptx::mul2(pr, ptx::add2(ptx::f2(dp[ci][2 * e], dp[ci][2 * e + 1]), nD2)), d0, d1);
           pk[e] = ptx::pack_bf16x2(d0, d1);
         }
-        ptx::tmem_st16(ts + cc * 32, pk);  // dS over S columns this warp has read
+        ptx::tmem_st16(tp + cc * 32, pk);  // dS over dP columns this warp has read
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
