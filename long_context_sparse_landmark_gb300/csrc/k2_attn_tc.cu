@@ -314,23 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       auto issue_s = [&](int slot, uint32_t stage) {
         const uint32_t qa = q_lo0 + slot * kTileLo;
         const uint32_t kb = k_lo0 + stage * kTileLo;
-        const uint32_t d = tmem + slot * 256;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-          ptx::mma_ss_w(d, qa + off, ptx::kDescHiSw128, kb + off, ptx::kDescHiSw128, kIdescS,
-                           kk > 0 ? 1u : 0u);
-        }
+        ptx::mma_ss_x8_w<(kChunkBytes >> 4)>(tmem + slot * 256, qa, kb, kIdescS, 0u);
       };
       auto issue_pv = [&](int slot, uint32_t stage, bool first) {
         const uint32_t vb = v_lo0 + stage * kTileLo;
-        const uint32_t d = tmem + slot * 256 + 128;
-        const uint32_t pa = tmem + slot * 256;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          ptx::mma_ts_w(d, pa + kk * 8, vb + ((kk * 2048) >> 4), ptx::kDescHiSw128, kIdescO,
-                           (!first || kk > 0) ? 1u : 0u);
-        }
+        ptx::mma_ts_x8_w(tmem + slot * 256 + 128, tmem + slot * 256, vb, kIdescO, first ? 0u : 1u);
       };
       uint32_t g = 0;                 // global tile index (K/V ring position)
       uint32_t qn = 0;                // units processed

@@ -226,6 +226,75 @@ __device__ __forceinline__ uint32_t desc_lo(uint32_t addr, uint32_t lbo) {
   return ((addr & 0x3FFFFu) >> 4) | ((lbo >> 4) << 16);
 }
 
+// Eight SS MMAs over K = 128 (8 steps of 16) from one elect.sync: both
+// operands K-major 128-byte-swizzled tiles whose 64-column chunks are
+// `kChunkLo` descriptor units (bytes >> 4) apart; step kk starts at chunk
+// kk / 4, 32 bytes x (kk % 4) into it.  The first MMA overwrites D unless
+// `accumulate`, the others accumulate.
+template <uint32_t kChunkLo>
+__device__ __forceinline__ void mma_ss_x8_w(uint32_t d, uint32_t a_lo, uint32_t b_lo,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p0;\n\t.reg .b64 da, db;\n\t.reg .b32 al, bl;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\t"
+      "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p0;\n\t"
+      "add.u32 al, %1, 2;\n\tadd.u32 bl, %2, 2;\n\t"
+      "mov.b64 da, {al, %5};\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 al, %1, 4;\n\tadd.u32 bl, %2, 4;\n\t"
+      "mov.b64 da, {al, %5};\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 al, %1, 6;\n\tadd.u32 bl, %2, 6;\n\t"
+      "mov.b64 da, {al, %5};\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 al, %1, %6;\n\tadd.u32 bl, %2, %6;\n\t"
+      "mov.b64 da, {al, %5};\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 al, al, 2;\n\tadd.u32 bl, bl, 2;\n\t"
+      "mov.b64 da, {al, %5};\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 al, al, 2;\n\tadd.u32 bl, bl, 2;\n\t"
+      "mov.b64 da, {al, %5};\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 al, al, 2;\n\tadd.u32 bl, bl, 2;\n\t"
+      "mov.b64 da, {al, %5};\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t}" ::"r"(d),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kDescHiSw128), "n"(kChunkLo)
+      : "memory");
+}
+
+// Eight TS MMAs over K = 128: A from tensor memory, columns a + 8 kk; B an
+// MN-major 128-byte-swizzled tile, 16 rows (2048 bytes) per step.
+__device__ __forceinline__ void mma_ts_x8_w(uint32_t d, uint32_t a_tmem, uint32_t b_lo,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p0;\n\t.reg .b64 db;\n\t.reg .b32 at, bl;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\t"
+      "mov.b64 db, {%2, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p0;\n\t"
+      "mov.b32 at, %1;\n\tmov.b32 bl, %2;\n\t"
+      "add.u32 at, at, 8;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t"
+      "add.u32 at, at, 8;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t"
+      "add.u32 at, at, 8;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t"
+      "add.u32 at, at, 8;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t"
+      "add.u32 at, at, 8;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t"
+      "add.u32 at, at, 8;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t"
+      "add.u32 at, at, 8;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t}" ::"r"(d),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kDescHiSw128)
+      : "memory");
+}
+
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D:
 // D format bits 4-5 = 1 (f32), A format bits 7-9 = 1 (bf16), B format bits
 // 10-12 = 1 (bf16), bit 15/16 = A/B major-ness (0 = K-major, 1 = MN-major),
