@@ -312,7 +312,10 @@ msa_status msa_attn_bwd(const void *q, const void *k, const void *v,
                         void *workspace, size_t workspace_bytes,
                         msa_stream_t stream);
 
-/* Bytes of workspace msa_attn_bwd needs (0 for invalid sizes). */
+/* Bytes of workspace msa_attn_bwd needs (0 for invalid sizes): about
+ * 8 * Hq * n bytes of row statistics, plus, with landmarks, per-query-chunk
+ * partial landmark gradients (up to about 256 MiB, fewer chunks for short
+ * sequences) and their sum (8 * n_landmarks * Hkv * d bytes). */
 size_t msa_attn_bwd_workspace_size(int64_t n, int Hq, int Hkv, int d,
                                    int n_landmarks);
 
