@@ -289,6 +289,26 @@ def test_backward_validation(lib):
     assert call(w=0) == 1
 
 
+def test_backward_workspace_size_matches_its_description(lib):
+    """msa.h: about 8*Hq*n bytes of row statistics, plus up to ~256 MiB of
+    per-chunk landmark-gradient partials and their 8*G*Hkv*d-byte sum."""
+    size = lib.msa_attn_bwd_workspace_size
+    mib = 1 << 20
+    for n, Hq, Hkv, G in ((131072, 64, 8, 512), (131072, 64, 8, 4096), (1 << 20, 64, 8, 512),
+                          (4096, 16, 2, 32), (8192, 8, 1, 0)):
+        stats = 8 * Hq * (-(-n // 128) * 128)
+        total = size(n, Hq, Hkv, 128, G)
+        extra = total - stats
+        assert stats <= total
+        if G == 0:
+            assert extra < mib
+        else:
+            lm_sum = 8 * G * Hkv * 128
+            assert lm_sum <= extra <= 257 * mib + lm_sum, (n, G, extra / mib)
+    # short sequences: as many chunks as query tiles at most
+    assert size(4096, 16, 2, 128, 32) - 8 * 16 * 4096 <= 32 * 8 * 32 * 2 * 128 + 8 * 32 * 2 * 128 + mib
+
+
 def test_rows_validation(lib):
     f = lib.msa_attn_fwd_rows
 
