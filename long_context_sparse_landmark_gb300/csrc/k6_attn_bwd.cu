@@ -237,18 +237,101 @@ __device__ __forceinline__ void produce(uint32_t sb, const CUtensorMap* fa, cons
   }
 }
 
+// Groups of MMAs issued from one asm block with one elect.sync (the whole
+// MMA warp calls them; constant descriptor steps inside).
+//
+// Eight SS MMAs over K = 128 (steps of 16): both operands K-major
+// 128-byte-swizzled tiles whose 64-column chunks are kA / kB descriptor
+// units (bytes >> 4) apart; step kk starts kk / 4 chunks in, 32 bytes x
+// (kk % 4) into the chunk.  The first MMA overwrites D.
+template <uint32_t kA, uint32_t kB>
+__device__ __forceinline__ void ss_x8_w(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b64 da, db;\n\t.reg .b32 al, bl;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "mov.b64 da, {%1, %4};\n\tmov.b64 db, {%2, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 0;\n\t"
+      "add.u32 al, %1, 2;\n\tadd.u32 bl, %2, 2;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 al, %1, 4;\n\tadd.u32 bl, %2, 4;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 al, %1, 6;\n\tadd.u32 bl, %2, 6;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 al, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 al, al, 2;\n\tadd.u32 bl, bl, 2;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 al, al, 2;\n\tadd.u32 bl, bl, 2;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t"
+      "add.u32 al, al, 2;\n\tadd.u32 bl, bl, 2;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, 1;\n\t}" ::"r"(d),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "n"(ptx::kDescHiSw128), "n"(kA), "n"(kB)
+      : "memory");
+}
+
+// TS MMAs over the 32-key chunks of A in tensor memory, two of K = 16 per
+// chunk: the packed bf16 pairs of each chunk sit in the first 16 columns of
+// that chunk (steps at a, a + 8, a + 32, a + 40, ...); B an MN-major
+// 128-byte-swizzled tile, 16 rows (2048 bytes) per step.  The first MMA
+// overwrites D unless `accumulate`.
+template <int kChunks>
+__device__ __forceinline__ void ts_chunked_w(uint32_t d, uint32_t a_tmem, uint32_t b_lo,
+                                             uint32_t idesc, uint32_t accumulate) {
+  static_assert(kChunks == 2 || kChunks == 4, "2 or 4 chunks");
+  if constexpr (kChunks == 2) {
+    asm volatile(
+        "{\n\t.reg .pred e, p0;\n\t.reg .b64 db;\n\t.reg .b32 at, bl;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\t"
+        "mov.b64 db, {%2, %5};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p0;\n\t"
+        "add.u32 at, %1, 8;\n\tadd.u32 bl, %2, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t"
+        "add.u32 at, %1, 32;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t"
+        "add.u32 at, %1, 40;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t}" ::"r"(d),
+        "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(ptx::kDescHiSw128)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred e, p0;\n\t.reg .b64 db;\n\t.reg .b32 at, bl;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\t"
+        "mov.b64 db, {%2, %5};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p0;\n\t"
+        "add.u32 at, %1, 8;\n\tadd.u32 bl, %2, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t"
+        "add.u32 at, %1, 32;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t"
+        "add.u32 at, %1, 40;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t"
+        "add.u32 at, %1, 64;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t"
+        "add.u32 at, %1, 72;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t"
+        "add.u32 at, %1, 96;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t"
+        "add.u32 at, %1, 104;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, 1;\n\t}" ::"r"(d),
+        "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(ptx::kDescHiSw128)
+        : "memory");
+  }
+}
+
 // Score-like MMAs of one half: D[128 x 64] = A[128 x 128] B[64 x 128]^T,
 // 8 SS MMAs (K = 128 in steps of 16); A a fixed 128-row tile, B a 64-row
 // half-tile of the ring (64-column chunks 8 KB apart).
 __device__ __forceinline__ void mma_scores_half(uint32_t d, uint32_t a_lo, uint32_t b_lo) {
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kT, kHalf, false);
-#pragma unroll
-  for (int kk = 0; kk < kD / 16; ++kk) {
-    const uint32_t a_off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-    const uint32_t b_off = ((kk >> 2) * kHalfChunk + (kk & 3) * 32) >> 4;
-    ptx::mma_ss_w(d, a_lo + a_off, ptx::kDescHiSw128, b_lo + b_off, ptx::kDescHiSw128, kIdesc,
-                  kk > 0 ? 1u : 0u);
-  }
+  ss_x8_w<(kChunkBytes >> 4), (kHalfChunk >> 4)>(d, a_lo, b_lo, kIdesc);
 }
 
 // Gradient MMAs of one half: D[128 x 128] += A (128 x 64 bf16 in TMEM: the
@@ -258,10 +341,7 @@ __device__ __forceinline__ void mma_scores_half(uint32_t d, uint32_t a_lo, uint3
 __device__ __forceinline__ void mma_grad_half(uint32_t d, uint32_t a_tmem, uint32_t b_mn,
                                               bool first) {
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kT, kD, true);
-#pragma unroll
-  for (int kk = 0; kk < kHalf / 16; ++kk)
-    ptx::mma_ts_w(d, a_tmem + (kk >> 1) * 32 + (kk & 1) * 8, b_mn + ((kk * 2048) >> 4),
-                  ptx::kDescHiSw128, kIdesc, (!first || kk > 0) ? 1u : 0u);
+  ts_chunked_w<2>(d, a_tmem, b_mn, kIdesc, first ? 0u : 1u);
 }
 
 // TMEM columns of the two halves: scores of half h at [64h.. 64h+64) of
@@ -415,12 +495,7 @@ __device__ __forceinline__ void dq_produce(uint32_t sb, const CUtensorMap* fq,
 // D[128 x 128] = A[128 x 128] B[128 x 128]^T, both K-major: 8 SS MMAs.
 __device__ __forceinline__ void mma_scores_full(uint32_t d, uint32_t a_lo, uint32_t b_lo) {
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kT, kT, false);
-#pragma unroll
-  for (int kk = 0; kk < kD / 16; ++kk) {
-    const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-    ptx::mma_ss_w(d, a_lo + off, ptx::kDescHiSw128, b_lo + off, ptx::kDescHiSw128, kIdesc,
-             kk > 0 ? 1u : 0u);
-  }
+  ss_x8_w<(kChunkBytes >> 4), (kChunkBytes >> 4)>(d, a_lo, b_lo, kIdesc);
 }
 
 // MMA issue order of the dQ kernel (run by the whole MMA warp), tile t's
@@ -466,10 +541,7 @@ __device__ __forceinline__ bool dq_pipeline(uint32_t sb, uint32_t tmem, int iter
     const int sk = t % kDqKStages;
     const uint32_t a = tmem + dq_col_p(t);
     const uint32_t kb = k_mn + sk * kTileLo;
-#pragma unroll
-    for (int kk = 0; kk < kT / 16; ++kk)
-      ptx::mma_ts_w(tmem + kDqColQ, a + (kk >> 1) * 32 + (kk & 1) * 8, kb + ((kk * 2048) >> 4),
-                    ptx::kDescHiSw128, kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+    ts_chunked_w<4>(tmem + kDqColQ, a, kb, kIdescG, t > 0 ? 1u : 0u);
     ptx::commit_w(bar(DQ_EMPTYK0 + sk));  // K(t) consumed
   }
   if (ok) ptx::commit_w(bar(DQ_ACC));
