@@ -238,7 +238,10 @@ __device__ __forceinline__ void produce(uint32_t sb, const CUtensorMap* fa, cons
 }
 
 // Groups of MMAs issued from one asm block with one elect.sync (the whole
-// MMA warp calls them; constant descriptor steps inside).
+// MMA warp calls them; constant descriptor steps inside).  Unlike the
+// forward kernel's groups, the operands here may have different chunk
+// strides (a 128-row tile against a 64-row ring half) and the TMEM operand
+// holds its packed pairs per 32-column chunk.
 //
 // Eight SS MMAs over K = 128 (steps of 16): both operands K-major
 // 128-byte-swizzled tiles whose 64-column chunks are kA / kB descriptor
