@@ -51,7 +51,7 @@ def load_peaks():
 # k2_attn_tc.cu); after any change the traffic is reported as null.
 ATTN_TRAFFIC = {"128k_70b_layer": {
     "bytes": 2.703023e9 + 2.144078e9,
-    "kernel_sha256": "e2bfc2039ea30500f71105df66e76c2606eae62d50b24dd97a0c00a1bf130a23"}}
+    "kernel_sha256": "a465ff28a22fa257e0938a7fa370c7490fbec936de84e085a08109784116437a"}}
 
 
 def kernel_sha256() -> str:

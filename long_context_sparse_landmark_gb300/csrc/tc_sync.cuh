@@ -39,7 +39,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
   return false;
 }
 
-// Bounded wait taken by a whole warp, with one verdict for all its lanes.
+// Bounded wait taken by a whole warp, with one result for all its lanes.
 __device__ __forceinline__ bool wait_w(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
   return __all_sync(0xffffffffu, wait_bar(bar, parity, ctl));
 }
