@@ -448,6 +448,15 @@ msa_status msa_device_status(int clear);
  */
 void msa_debug_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * Test hook: with `on` nonzero, launches made after the call run the
+ * single-CTA tensor-core attention kernel even where the CTA-pair kernel
+ * applies (bf16, d = 128, at least two query heads per KV head), so that
+ * tests can compare the two; 0 restores the normal choice.  Both kernels
+ * compute the same arithmetic in the same order and give the same bits.
+ */
+void msa_debug_force_single_cta(int on);
+
 #ifdef __cplusplus
 }
 #endif

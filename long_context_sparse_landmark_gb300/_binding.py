@@ -27,7 +27,8 @@ EXPORTS = ("msa_version", "msa_last_error_string", "msa_landmark_pool", "msa_att
            "msa_attn_bwd", "msa_attn_bwd_workspace_size", "msa_attn_bwd_global_rows",
            "msa_attn_bwd_global_rows_workspace_size", "msa_attn_fwd_partial",
            "msa_attn_fwd_partial_merge", "msa_lse_merge",
-           "msa_attn_uses_tensor_cores", "msa_device_status", "msa_debug_set_wait_limit_ns")
+           "msa_attn_uses_tensor_cores", "msa_device_status", "msa_debug_set_wait_limit_ns",
+           "msa_debug_force_single_cta")
 
 
 class MsaError(RuntimeError):
@@ -98,6 +99,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_device_status.restype = i32
     lib.msa_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.msa_debug_set_wait_limit_ns.restype = None
+    lib.msa_debug_force_single_cta.argtypes = [i32]
+    lib.msa_debug_force_single_cta.restype = None
     return lib
 
 
@@ -147,6 +150,12 @@ def device_status(clear: bool = True) -> int:
 
 def set_wait_limit_ns(ns: int) -> None:
     _lib.msa_debug_set_wait_limit_ns(int(ns))
+
+
+def force_single_cta(on: bool) -> None:
+    """Test hook: run the single-CTA tensor-core attention kernel where the
+    CTA-pair kernel would run (msa_debug_force_single_cta)."""
+    _lib.msa_debug_force_single_cta(1 if on else 0)
 
 
 def landmark_pool(k: torch.Tensor, v: torch.Tensor, k_lm: torch.Tensor, v_lm: torch.Tensor,

@@ -44,6 +44,7 @@ std::mutex g_status_mu;
 int* g_status_ptr[kMaxDevices] = {};
 
 std::atomic<uint64_t> g_wait_limit_ns{0};
+std::atomic<int> g_force_single_cta{0};
 constexpr uint64_t kDefaultWaitNs = 4000000000ull;
 
 msa_status device_status_ptr(int** out) {
@@ -99,6 +100,16 @@ msa_status run_attn(const msa::AttnArgs& a0, cudaStream_t stream) {
   a.wait_limit_ns = lim ? lim : kDefaultWaitNs;
   // Selected blocks map to whole 128-key tiles on the tensor-core path.
   const bool tiles_ok = !a.sel || a.block % 128 == 0;
+  // The CTA-pair kernel keeps per-row column bounds in 32 bits: up to 2^29
+  // keys (longer sequences take the single-CTA kernel).
+  const bool pair_sizes = a.n_kv <= (int64_t(1) << 29) && a.n_q <= (int64_t(1) << 29);
+  if (tiles_ok && pair_sizes && !g_force_single_cta.load() &&
+      msa::attn_tc2_supported(a.Hq, a.Hkv, a.d, a.in_bf16)) {
+    const char* why = nullptr;
+    cudaError_t e = msa::launch_attn_tc2(a, stream, &why);
+    if (e != cudaSuccess && why) return fail(MSA_ERR_CUDA, "tensor-core attention: %s", why);
+    return launched(e, "tensor-core attention (CTA pairs)");
+  }
   if (tiles_ok && msa::attn_tc_supported(a.Hq, a.Hkv, a.d, a.in_bf16)) {
     const char* why = nullptr;
     cudaError_t e = msa::launch_attn_tc(a, stream, &why);
@@ -913,5 +924,7 @@ msa_status msa_device_status(int clear) {
 }
 
 void msa_debug_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns); }
+
+void msa_debug_force_single_cta(int on) { g_force_single_cta.store(on ? 1 : 0); }
 
 }  // extern "C"

@@ -216,5 +216,8 @@ bool attn_bwd_supported(int d, int in_bf16);
 cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why);
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s, const char** why);
 bool attn_tc_supported(int Hq, int Hkv, int d, int in_bf16);
+// The CTA-pair variant (two SMs share each MMA; query heads per KV head >= 2).
+cudaError_t launch_attn_tc2(const AttnArgs& a, cudaStream_t s, const char** why);
+bool attn_tc2_supported(int Hq, int Hkv, int d, int in_bf16);
 
 }  // namespace msa

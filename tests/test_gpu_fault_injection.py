@@ -43,6 +43,23 @@ def test_wait_limit_runs_out_and_context_survives():
     compare(lse.index_select(1, idx).cpu().numpy(), rl, 1e-2, 1e-3, "lse after timeout")
 
 
+def test_single_cta_kernel_times_out_cleanly():
+    """The same for the single-CTA tensor-core kernel, forced where the
+    CTA-pair kernel would run."""
+    B = binding()
+    wl = Workload("fault1", 4096, 8, 2, 128, 1024, 16, "bf16", seed=22)
+    q, k, v = generate(wl, device="cuda")
+    ref = [t.clone() for t in run_gpu_attention(q, k, v, wl)]
+    torch.cuda.synchronize()
+    try:
+        B.force_single_cta(True)
+        got = _timeout_then_clean(B, lambda: run_gpu_attention(q, k, v, wl))
+    finally:
+        B.force_single_cta(False)
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+
+
 def _timeout_then_clean(B, launch):
     """Run `launch` with every bounded wait cut to 1 ns (expect
     MSA_ERR_TIMEOUT and a clean return), then with the default bound."""
