@@ -60,6 +60,9 @@ def _configure(lib):
     lib.oracle_attn_bwd_dq_rows.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, i32, i64, i32,
                                             dbl, vp, i64, vp]
     lib.oracle_attn_bwd_dq_rows.restype = i32
+    lib.oracle_attn_bwd_dkdv_keys.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, i32, i64, i32,
+                                              dbl, vp, vp, i64, vp, vp]
+    lib.oracle_attn_bwd_dkdv_keys.restype = i32
     lib.oracle_attn_band_rows.argtypes = [vp, vp, i64, vp, vp, i64, i32, i32,
                                           i32, i32, i64, i64, dbl, vp, vp]
     lib.oracle_attn_band_rows.restype = i32
@@ -357,6 +360,33 @@ def attn_bwd_dq_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarr
     if rc != 0:
         raise ValueError("attn_bwd_dq_rows: inconsistent arguments")
     return dq
+
+
+def attn_bwd_dkdv_keys(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray,
+                       window: int, n_landmarks: int, scale: float, keys, kv_heads):
+    """dK, dV [n_keys, d] (fp64) of the listed (key position, KV head) pairs
+    only, for window + landmark attention over the whole sequence (q, k, v,
+    dout whole): the window rows of each key plus its block's landmark
+    gradient divided by the block size; row statistics are computed only
+    for the rows that see a listed key or its landmark."""
+    q, k, v, dout = (np.ascontiguousarray(x) for x in (q, k, v, dout))
+    dt = _dtype_code(q)
+    if any(_dtype_code(x) != dt for x in (k, v, dout)):
+        raise TypeError("q, k, v, dout must share one dtype")
+    n, Hq, d = q.shape
+    keys = np.ascontiguousarray(np.asarray(keys, dtype=np.int64))
+    kv_heads = np.ascontiguousarray(np.asarray(kv_heads, dtype=np.int32))
+    if keys.shape != kv_heads.shape:
+        raise ValueError("one KV head per listed key")
+    dk = np.empty((len(keys), d), dtype=np.float64)
+    dv = np.empty((len(keys), d), dtype=np.float64)
+    rc = _load().oracle_attn_bwd_dkdv_keys(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), dt, n, Hq,
+                                           k.shape[1], d, int(window), int(n_landmarks),
+                                           float(scale), _ptr(keys), _ptr(kv_heads), len(keys),
+                                           _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError("attn_bwd_dkdv_keys: inconsistent arguments")
+    return dk, dv
 
 
 def attn_bwd_compressed(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray,

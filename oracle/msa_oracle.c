@@ -686,3 +686,178 @@ int oracle_attn_bwd_dq_rows(const void *q, const void *k, const void *v,
     free(v_lm);
     return 0;
 }
+
+/*
+ * lse_i and D_i = <dO_i, O_i> of one (row i, head h): the first pass of
+ * oracle_attn_bwd without dQ.  sc is scratch of window + G doubles, o of d.
+ */
+static void oracle_row_stats(const void *q, const void *k, const void *v,
+                             const void *dout, int dtype, int64_t i, int h,
+                             int Hq, int Hkv, int d, int64_t window, int G,
+                             int64_t B, const double *k_lm, const double *v_lm,
+                             double scale, double *sc, double *o,
+                             double *lse_out, double *D_out) {
+    const int c = h / (Hq / Hkv);
+    const int64_t j_lo = i - window + 1 > 0 ? i - window + 1 : 0;
+    const int64_t n_win = i - j_lo + 1;
+    const int64_t n_lm = G > 0 ? oracle_visible_landmarks(i, window, B, G) : 0;
+    const int64_t qoff = (i * Hq + h) * (int64_t)d;
+    double m = -INFINITY;
+    for (int64_t a = 0; a < n_win + n_lm; ++a) {
+        double dot = 0.0;
+        for (int e = 0; e < d; ++e) {
+            const double ke = a < n_win
+                ? oracle_load(k, ((j_lo + a) * Hkv + c) * (int64_t)d + e, dtype)
+                : k_lm[((a - n_win) * Hkv + c) * (int64_t)d + e];
+            dot += oracle_load(q, qoff + e, dtype) * ke;
+        }
+        sc[a] = scale * dot;
+        if (sc[a] > m) m = sc[a];
+    }
+    double denom = 0.0;
+    for (int e = 0; e < d; ++e) o[e] = 0.0;
+    for (int64_t a = 0; a < n_win + n_lm; ++a) {
+        const double p = exp(sc[a] - m);
+        denom += p;
+        for (int e = 0; e < d; ++e)
+            o[e] += p * (a < n_win
+                ? oracle_load(v, ((j_lo + a) * Hkv + c) * (int64_t)d + e, dtype)
+                : v_lm[((a - n_win) * Hkv + c) * (int64_t)d + e]);
+    }
+    double Di = 0.0;
+    for (int e = 0; e < d; ++e)
+        Di += oracle_load(dout, qoff + e, dtype) * (o[e] / denom);
+    *lse_out = m + log(denom);
+    *D_out = Di;
+}
+
+/*
+ * dK and dV of listed (key position, KV head) pairs only: the second and
+ * third passes of oracle_attn_bwd restricted to those keys, for checking
+ * layers whose full backward is out of reach on the host.  For key j of KV
+ * head c:
+ *   window part:   sum over rows i in [j, j+w-1] and the group's heads h of
+ *                  dk += scale dS_ij q_ih,  dv += P_ij dO_ih;
+ *   landmark part: the gradient of landmark l = j / B (rows with
+ *                  (l+1)B <= i-w+1), divided by B (a landmark is the mean of
+ *                  its B tokens).
+ * P and dS come from each row's lse and D, computed (first pass) only for
+ * the rows and heads that see a listed key or its block's landmark.
+ *   keys [n_keys] positions in [0, n), kv_heads [n_keys] in [0, Hkv)
+ *   dk, dv [n_keys][d] fp64, written
+ * Returns 0, or -1 on inconsistent arguments.
+ */
+int oracle_attn_bwd_dkdv_keys(const void *q, const void *k, const void *v,
+                              const void *dout, int dtype, int64_t n, int Hq,
+                              int Hkv, int d, int64_t window, int G,
+                              double scale, const int64_t *keys,
+                              const int32_t *kv_heads, int64_t n_keys,
+                              double *dk, double *dv) {
+    if (n < 1 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 ||
+        window < 1 || G < 0 || (G > 0 && n % G != 0) || n_keys < 0)
+        return -1;
+    for (int64_t r = 0; r < n_keys; ++r)
+        if (keys[r] < 0 || keys[r] >= n || kv_heads[r] < 0 || kv_heads[r] >= Hkv)
+            return -1;
+    const int group = Hq / Hkv;
+    const int64_t B = G > 0 ? n / G : 1;
+    const int64_t row_kv = (int64_t)Hkv * d;
+    double *k_lm = NULL, *v_lm = NULL;
+    if (G > 0) {
+        k_lm = (double *)malloc(sizeof(double) * (size_t)(G * row_kv));
+        v_lm = (double *)malloc(sizeof(double) * (size_t)(G * row_kv));
+        oracle_landmark_pool(k, dtype, n, Hkv, d, G, k_lm);
+        oracle_landmark_pool(v, dtype, n, Hkv, d, G, v_lm);
+    }
+    /* Which (row, KV group) pairs need their statistics. */
+    char *need = (char *)calloc((size_t)(n * Hkv), 1);
+    for (int64_t r = 0; r < n_keys; ++r) {
+        const int64_t j = keys[r];
+        const int c = kv_heads[r];
+        const int64_t i_hi = j + window - 1 < n - 1 ? j + window - 1 : n - 1;
+        for (int64_t i = j; i <= i_hi; ++i) need[i * Hkv + c] = 1;
+        if (G > 0)
+            for (int64_t i = (j / B + 1) * B + window - 1; i < n; ++i) need[i * Hkv + c] = 1;
+    }
+    double *lse = (double *)malloc(sizeof(double) * (size_t)(n * Hq));
+    double *Dv = (double *)malloc(sizeof(double) * (size_t)(n * Hq));
+#pragma omp parallel
+    {
+        double *sc = (double *)malloc(sizeof(double) * (size_t)(window + G));
+        double *o = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for collapse(2) schedule(dynamic, 16)
+        for (int64_t i = 0; i < n; ++i)
+            for (int c = 0; c < Hkv; ++c) {
+                if (!need[i * Hkv + c]) continue;
+                for (int h = c * group; h < (c + 1) * group; ++h)
+                    oracle_row_stats(q, k, v, dout, dtype, i, h, Hq, Hkv, d, window, G, B,
+                                     k_lm, v_lm, scale, sc, o, &lse[(int64_t)h * n + i],
+                                     &Dv[(int64_t)h * n + i]);
+            }
+        free(sc);
+        free(o);
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_keys; ++r) {
+        const int64_t j = keys[r];
+        const int c = kv_heads[r];
+        double *gk = dk + r * (int64_t)d;
+        double *gv = dv + r * (int64_t)d;
+        for (int e = 0; e < d; ++e) gk[e] = gv[e] = 0.0;
+        /* Window part: rows i in [j, j+w-1]. */
+        const int64_t koff = (j * Hkv + c) * (int64_t)d;
+        const int64_t i_hi = j + window - 1 < n - 1 ? j + window - 1 : n - 1;
+        for (int64_t i = j; i <= i_hi; ++i) {
+            for (int h = c * group; h < (c + 1) * group; ++h) {
+                const int64_t qoff = (i * Hq + h) * (int64_t)d;
+                double s = 0.0, dp = 0.0;
+                for (int e = 0; e < d; ++e) {
+                    s += oracle_load(q, qoff + e, dtype) * oracle_load(k, koff + e, dtype);
+                    dp += oracle_load(dout, qoff + e, dtype) * oracle_load(v, koff + e, dtype);
+                }
+                const double p = exp(scale * s - lse[(int64_t)h * n + i]);
+                const double ds = p * (dp - Dv[(int64_t)h * n + i]);
+                for (int e = 0; e < d; ++e) {
+                    gk[e] += scale * ds * oracle_load(q, qoff + e, dtype);
+                    gv[e] += p * oracle_load(dout, qoff + e, dtype);
+                }
+            }
+        }
+        /* Landmark part: landmark l = j / B, seen by rows (l+1)B <= i-w+1. */
+        if (G > 0) {
+            const int64_t l = j / B;
+            const double *kl = k_lm + (l * Hkv + c) * (int64_t)d;
+            const double *vl = v_lm + (l * Hkv + c) * (int64_t)d;
+            double *tk = (double *)calloc((size_t)d, sizeof(double));
+            double *tv = (double *)calloc((size_t)d, sizeof(double));
+            for (int64_t i = (l + 1) * B + window - 1; i < n; ++i) {
+                for (int h = c * group; h < (c + 1) * group; ++h) {
+                    const int64_t qoff = (i * Hq + h) * (int64_t)d;
+                    double s = 0.0, dp = 0.0;
+                    for (int e = 0; e < d; ++e) {
+                        s += oracle_load(q, qoff + e, dtype) * kl[e];
+                        dp += oracle_load(dout, qoff + e, dtype) * vl[e];
+                    }
+                    const double p = exp(scale * s - lse[(int64_t)h * n + i]);
+                    const double ds = p * (dp - Dv[(int64_t)h * n + i]);
+                    for (int e = 0; e < d; ++e) {
+                        tk[e] += scale * ds * oracle_load(q, qoff + e, dtype);
+                        tv[e] += p * oracle_load(dout, qoff + e, dtype);
+                    }
+                }
+            }
+            for (int e = 0; e < d; ++e) {
+                gk[e] += tk[e] / (double)B;
+                gv[e] += tv[e] / (double)B;
+            }
+            free(tk);
+            free(tv);
+        }
+    }
+    free(need);
+    free(lse);
+    free(Dv);
+    free(k_lm);
+    free(v_lm);
+    return 0;
+}

@@ -4,12 +4,15 @@ through the C ABI, against the fp64 oracle's gradients on the same inputs.
 Bar.  Gradients have no scale of their own and their rows differ widely in
 size (a query with few keys, or a key that few rows see but weight
 heavily, has gradients ten times the tensor's RMS), so each d-vector (one
-token, one head) is held to its own size: max |g - r| <= 2^-5 (max |r| of
+token, one head) is held to its own size: max |g - r| <= 2^-7 (max |r| of
 that vector + RMS of the tensor), and over the tensor mean |g - r| <=
-2^-8 RMS.  The kernels round P and dS to bf16 (relative 2^-9) before the
-gradient MMAs, accumulate in fp32, and take D from the forward's O, whose
-weights were bf16 too; summed over terms of either sign this stays a small
-multiple of 2^-9 of the vector's size.  A bf16 gradient output adds one
+2^-9 RMS.  The kernels round P and dS to bf16 (relative 2^-9) before the
+gradient MMAs and accumulate in fp32; summed over terms of either sign the
+error stays a small multiple of 2^-9 of the vector's size (measured: at
+most 2.9 x 2^-9 over these shapes with an fp32 forward output, mean at
+most 0.7 x 2^-9 of the RMS).  D = <dO, O> takes the forward's O: kept in
+bf16 (the autograd op) it adds that rounding to every dS (measured 4.1 x
+2^-9), so that path is held to 2^-6.  A bf16 gradient output adds one
 rounding (half a bf16 spacing per element)."""
 import numpy as np
 import pytest
@@ -23,7 +26,8 @@ from tests.gpu_helpers import bf16_ulp, binding
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
-MAX_REL, MEAN_REL = 2.0 ** -5, 2.0 ** -8
+MAX_REL, MEAN_REL = 2.0 ** -7, 2.0 ** -9
+MAX_REL_BF16_OUT = 2.0 ** -6  # forward output kept in bf16: D inherits its rounding
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -44,6 +48,7 @@ def rel_compare(gpu, ref, what, max_rel=MAX_REL, mean_rel=MEAN_REL, extra=None):
     vec_scale = np.abs(r).max(axis=-1, keepdims=True) + rms
     mx = float((err / vec_scale).max())
     mean = float(err.mean()) / rms
+    print(f"[bwd error] {what}: max {mx:.3e} mean {mean:.3e}")
     assert mx <= max_rel and mean <= mean_rel, (
         f"{what}: max-abs/(vector max + rms) {mx:.3e} (bar {max_rel:.1e}), mean-abs/rms "
         f"{mean:.3e} (bar {mean_rel:.1e}), rms {rms:.3e}")
@@ -116,7 +121,7 @@ def test_autograd_wrapper_matches_backward_call():
                            to_numpy_bits(do), wl.window, wl.G, wl.scale)
     for name, t, r in zip("QKV", (qa, ka, va), refs):
         rel_compare(t.grad.float().cpu().numpy(), r, f"autograd d{name}",
-                    extra=0.5 * bf16_ulp(r))
+                    max_rel=MAX_REL_BF16_OUT, extra=0.5 * bf16_ulp(r))
 
 
 def test_backward_16k_full():
@@ -133,11 +138,42 @@ def test_backward_16k_full():
     rel_compare(dv.cpu().numpy(), rv, "16K dV")
 
 
+def sampled_keys_128k(n, Hkv, block, window, rng):
+    """(key, KV head) pairs checked element by element on the 128K layer.
+    KV head 5: keys in the upper half of the sequence -- both sides of key
+    block and 128-key tile boundaries, the last keys, keys whose landmark
+    no row sees (blocks past n - window), and uniform draws -- so that
+    window rows, landmark gradients spread over the query-chunked grid
+    (rows from about 70K up) and their 1/B scatter are all exercised; the
+    other KV heads: keys in the last 1024 (window rows only), which keeps
+    the oracle's row statistics to about 0.6 M (row, head) pairs."""
+    keys, heads = [], []
+    for l in (256, 300, 384, 400, 450, 480, 495, 496, 500, 511):
+        for j in (l * block - 1, l * block, l * block + 1, l * block + 127, l * block + 128):
+            if 0 <= j < n:
+                keys.append(j)
+                heads.append(5)
+    for j in (n - 1, n - 2, n - 127, n - 128, n - 129, n - window, n - window - 1):
+        keys.append(j)
+        heads.append(5)
+    for j in rng.integers(n // 2, n, size=120):
+        keys.append(int(j))
+        heads.append(5)
+    for c in range(Hkv):
+        if c == 5:
+            continue
+        for j in rng.integers(n - 1024, n, size=6):
+            keys.append(int(j))
+            heads.append(c)
+    return np.asarray(keys, dtype=np.int64), np.asarray(heads, dtype=np.int32)
+
+
 def test_backward_128k_layer_properties_and_sampled_dq():
-    """The 128K 70B-style layer: dQ on sampled rows against the oracle, and
-    at full size the identities sum_j dV[j, c] = sum over the group's heads
-    of sum_i dO and sum_j dK[j, c] = 0 (rows of P sum to 1, rows of dS to
-    0, landmark gradients included)."""
+    """The 128K 70B-style layer: dQ on sampled rows and dK / dV on sampled
+    keys against the oracle, element by element, and at full size the
+    identities sum_j dV[j, c] = sum over the group's heads of sum_i dO and
+    sum_j dK[j, c] = 0 (rows of P sum to 1, rows of dS to 0, landmark
+    gradients included)."""
     from long_context_sparse_landmark_gb300.workloads import WORKLOADS
     wl = WORKLOADS["128k_70b_layer"]
     q, k, v = generate(wl, device=DEV)
@@ -159,10 +195,19 @@ def test_backward_128k_layer_properties_and_sampled_dq():
     rows = sample_rows(wl, count=256).numpy()
     idx = torch.as_tensor(rows, device=DEV)
     gq = dq.index_select(0, idx).cpu().numpy()
+    keys, heads = sampled_keys_128k(wl.n, wl.Hkv, wl.block, wl.window,
+                                    np.random.default_rng(1283))
+    kidx = torch.as_tensor(keys, device=DEV)
+    hidx = torch.as_tensor(heads.astype(np.int64), device=DEV)
+    gk = dk[kidx, hidx].cpu().numpy()
+    gv = dv[kidx, hidx].cpu().numpy()
     del dq, dk, dv
-    rq = oracle.attn_bwd_dq_rows(to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v),
-                                 to_numpy_bits(do), wl.window, wl.G, wl.scale, rows)
+    qn, kn, vn, dn = (to_numpy_bits(t) for t in (q, k, v, do))
+    rq = oracle.attn_bwd_dq_rows(qn, kn, vn, dn, wl.window, wl.G, wl.scale, rows)
     rel_compare(gq, rq, "128K dQ (sampled)")
+    rk, rv = oracle.attn_bwd_dkdv_keys(qn, kn, vn, dn, wl.window, wl.G, wl.scale, keys, heads)
+    rel_compare(gk, rk, "128K dK (sampled keys)")
+    rel_compare(gv, rv, "128K dV (sampled keys)")
 
 
 # ------------------------------------------------------------ compression-token pattern

@@ -9,8 +9,10 @@ set is unique and must match exactly; otherwise any set the GPU's rounding
 could have produced is accepted (every chosen block's exact score, plus the
 error bound, reaches every unchosen candidate's, minus it).  Attention is
 checked with the oracle's own selection fed to the GPU, and the fused
-pool -> select -> attend call with the GPU's selection on the (row, head)
-pairs whose KV group chose the oracle's set."""
+pool -> select -> attend call on every (row, head) pair: where the GPU's
+selection is the oracle's against the oracle end to end, and everywhere
+against the oracle's attention over the GPU's own selection, once that
+selection has been checked to be one the scores allow."""
 import math
 
 import numpy as np
@@ -223,20 +225,26 @@ def test_topk_fused_against_oracle(dt, d, n, G, w, top_k, Hq, Hkv):
     same = check_selection(sel, cnt, scores, score_error_bound(q, k, G), top_k)
     sel_o, cnt_o = oracle.select_top_k(scores, top_k)
     ro, rl = oracle.attn_select(qn, kn, vn, w, G, sel_o, cnt_o, wl.scale)
-    # (row, head) pairs whose KV group chose the oracle's set
+    # (row, head) pairs whose KV group chose the oracle's set: end to end
     g = Hq // Hkv
     keep = np.repeat(same, g, axis=1)[np.arange(n) // QB]          # [n, Hq]
     assert keep.mean() > 0.5, f"only {keep.mean():.2f} of (row, head) pairs comparable"
     mx, mean = tol(dt)
     o = out.cpu().numpy()
+    l_ = lse.cpu().numpy()
     compare(o[keep], ro[keep], mx, mean, f"fused O {wl}")
-    compare(lse.cpu().numpy()[keep.T], rl[keep.T], mx, mean, f"fused lse {wl}")
+    compare(l_[keep.T], rl[keep.T], mx, mean, f"fused lse {wl}")
+    # every pair: the oracle's attention over the GPU's (validated) selection
+    rg, rgl = oracle.attn_select(qn, kn, vn, w, G, sel, cnt, wl.scale)
+    compare(o, rg, mx, mean, f"fused O, GPU selection {wl}")
+    compare(l_, rgl, mx, mean, f"fused lse, GPU selection {wl}")
 
 
 def test_topk_128k_sampled_rows():
     """The 128K top-k workload in the benchmark's launch configuration:
     fused call == steps, selection valid on every unit, sampled rows equal
-    the oracle where the selection is the oracle's."""
+    the oracle where the selection is the oracle's, and every sampled row
+    and head equal to the oracle's attention over the GPU's selection."""
     wl = WORKLOADS["topk_128k"]
     q, k, v = generate(wl, device=DEV)
     sel, cnt, out, lse = _fused_vs_steps(q, k, v, wl)
@@ -254,6 +262,13 @@ def test_topk_128k_sampled_rows():
     keep = np.repeat(same, wl.Hq // wl.Hkv, axis=1)[rows // QB]      # [rows, Hq]
     compare(go[keep], ro[keep], 1e-2, 1e-3, "topk 128K O (sampled)")
     compare(gl[keep.T], rl[keep.T], 1e-2, 1e-3, "topk 128K lse (sampled)")
+    # every sampled row and head, units whose selection differs included
+    rg, rgl = oracle.attn_select(to_numpy_bits(q.index_select(0, idx)), kn, vn, wl.window, wl.G,
+                                 sel, cnt, wl.scale, q_positions=rows)
+    compare(go, rg, 1e-2, 1e-3, "topk 128K O, GPU selection (sampled)")
+    compare(gl, rgl, 1e-2, 1e-3, "topk 128K lse, GPU selection (sampled)")
+    print(f"128K top-k: {100 * (1 - same.mean()):.1f}% of units chose a set other than the "
+          "oracle's (each checked valid and compared through the oracle)")
 
 
 def test_attn_select_rejects_bad_selection_without_reading_out_of_bounds():

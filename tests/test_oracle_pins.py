@@ -788,6 +788,29 @@ def test_bwd_dq_rows_match_full_backward(oracle_mod):
                                   dq[rows])
 
 
+@pytest.mark.parametrize("n,Hq,Hkv,G,w", [(64, 4, 2, 8, 10), (96, 6, 3, 0, 7), (128, 2, 1, 128, 128),
+                                           (200, 8, 2, 25, 1), (256, 4, 4, 16, 300)])
+def test_bwd_dkdv_keys_match_full_backward(oracle_mod, n, Hq, Hkv, G, w):
+    """dK/dV of listed (key, KV head) pairs equal the full backward's rows,
+    for every key and head (window keys, landmark blocks seen by many rows,
+    by one row, by none; w = 1; w > n; G = 0 and G = n)."""
+    rng = np.random.default_rng(n + G + w)
+    d = 8
+    q, k, v = rand_qkv(rng, n, Hq, Hkv, d)
+    do = rng.standard_normal((n, Hq, d)).astype(np.float32)
+    _, dk, dv = oracle_mod.attn_bwd(q, k, v, do, w, G, 0.3)
+    keys = np.repeat(np.arange(n), Hkv)
+    heads = np.tile(np.arange(Hkv), n)
+    gk, gv = oracle_mod.attn_bwd_dkdv_keys(q, k, v, do, w, G, 0.3, keys, heads)
+    np.testing.assert_allclose(gk, dk.reshape(n * Hkv, d), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(gv, dv.reshape(n * Hkv, d), rtol=0, atol=1e-12)
+    # an arbitrary subset, in any order, gives the same rows
+    pick = rng.permutation(n * Hkv)[: n // 3]
+    sk, sv = oracle_mod.attn_bwd_dkdv_keys(q, k, v, do, w, G, 0.3, keys[pick], heads[pick])
+    np.testing.assert_array_equal(sk, gk[pick])
+    np.testing.assert_array_equal(sv, gv[pick])
+
+
 def compressed_torch_grads(q, k, v, dout, window, block, global_rows, scale):
     """Autograd (fp64) through the dense mask of the compression-token
     pattern, built element by element as in ``compressed_bruteforce``."""
