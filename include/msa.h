@@ -130,6 +130,46 @@ msa_status msa_attn_fwd_rows(const void *q_rows, const void *k, const void *v,
                              msa_dtype in_dt, msa_dtype out_dt,
                              msa_stream_t stream);
 
+/* Bytes of device workspace msa_attn_fwd_host needs (0 for invalid sizes):
+ * K and V whole, the landmarks, two chunks of Q and of O, the lse; about
+ * 2 n Hkv d + 4 chunk_rows Hq d elements plus 4 Hq n bytes. */
+size_t msa_attn_fwd_host_workspace_size(int64_t n, int Hq, int Hkv, int d,
+                                        int n_landmarks, int64_t chunk_rows,
+                                        msa_dtype in_dt, msa_dtype out_dt);
+
+/*
+ * msa_landmark_pool + msa_attn_fwd on HOST buffers, for a caller whose
+ * sequence lives in host memory (the end-to-end forward whose time
+ * "Scaling GPU Cluster for Million Token Context", section "Why Sparse
+ * Attention Changes the Game", quotes).  Rows [r0, r1) need only the
+ * K/V rows below r1 and the landmarks of the blocks inside them, so K, V
+ * and Q go to the device in chunks of chunk_rows rows (rounded up to a
+ * multiple of 128; 0 = about n/32, at least 4096) on `copy_in`, each
+ * chunk's landmarks are pooled and its rows attended on `stream`, and O
+ * comes back on `copy_out`, two chunks in flight, so that the copies
+ * overlap the kernels.  When chunk_rows is not a multiple of the landmark
+ * block n/G, K and V are copied and pooled whole before the first chunk.
+ *   q [n, Hq, d], k, v [n, Hkv, d] in `in_dt`: HOST memory (pinned memory
+ *     lets the copies run asynchronously), 16-byte aligned
+ *   out [n, Hq, d] in `out_dt`, lse [Hq, n] fp32: HOST memory, written
+ *   workspace: DEVICE memory, 256-byte aligned, at least
+ *     msa_attn_fwd_host_workspace_size bytes
+ *   copy_in, copy_out: streams for the copies (NULL: `stream`, no overlap)
+ * Unlike the other entry points this call waits for its streams: out and
+ * lse are final when it returns.  It creates and destroys eight CUDA
+ * events (no device memory).  The results equal msa_attn_fwd's bit for
+ * bit (the same kernels on the same rows).
+ * Errors: as msa_attn_fwd, plus INVALID_ARG for a negative chunk_rows or a
+ * null, misaligned or too small workspace; MSA_ERR_CUDA if a copy fails.
+ */
+msa_status msa_attn_fwd_host(const void *q, const void *k, const void *v,
+                             void *out, float *lse, int64_t n, int Hq, int Hkv,
+                             int d, int64_t window, int n_landmarks, float scale,
+                             msa_dtype in_dt, msa_dtype out_dt,
+                             int64_t chunk_rows, void *workspace,
+                             size_t workspace_bytes, msa_stream_t stream,
+                             msa_stream_t copy_in, msa_stream_t copy_out);
+
 /*
  * Block-band attention: the 2-D block-sparse mask of "Million Token Context
  * Window Optimization: What Actually Works", section "The indexing game:

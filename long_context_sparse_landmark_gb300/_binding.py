@@ -21,7 +21,7 @@ MAX_MERGE_PARTS = 64
 
 # Every symbol include/msa.h declares.
 EXPORTS = ("msa_version", "msa_last_error_string", "msa_landmark_pool", "msa_attn_fwd",
-           "msa_attn_fwd_rows", "msa_attn_fwd_band", "msa_block_select", "msa_attn_fwd_select",
+           "msa_attn_fwd_rows", "msa_attn_fwd_host", "msa_attn_fwd_host_workspace_size", "msa_attn_fwd_band", "msa_block_select", "msa_attn_fwd_select",
            "msa_attn_fwd_topk_workspace_size", "msa_attn_fwd_topk", "msa_attn_fwd_topk_noalloc",
            "msa_attn_fwd_global_rows", "msa_attn_fwd_global_rows_workspace_size",
            "msa_attn_bwd", "msa_attn_bwd_workspace_size", "msa_attn_bwd_global_rows",
@@ -56,6 +56,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_attn_fwd_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, i32,
                                       i64, i32, f32, i32, i32, vp]
     lib.msa_attn_fwd_rows.restype = i32
+    lib.msa_attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32, f32, i32,
+                                      i32, i64, vp, ctypes.c_size_t, vp, vp, vp]
+    lib.msa_attn_fwd_host.restype = i32
+    lib.msa_attn_fwd_host_workspace_size.argtypes = [i64, i32, i32, i32, i32, i64, i32, i32]
+    lib.msa_attn_fwd_host_workspace_size.restype = ctypes.c_size_t
     lib.msa_block_select.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i64, i32, i32, i32, vp]
     lib.msa_block_select.restype = i32
     lib.msa_attn_fwd_select.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32,
@@ -201,6 +206,42 @@ def attn_fwd_rows(q_rows, k, v, k_lm, v_lm, out_rows, lse, q_start: int, window:
                                   _ptr(out_rows), ctypes.c_void_p(lse_ptr), n, int(q_start), n_q,
                                   n, Hq, Hkv, d, int(window), int(n_landmarks), float(scale),
                                   _dt(q_rows), _dt(out_rows), _stream(stream)))
+
+
+def host_workspace_size(n: int, Hq: int, Hkv: int, d: int, n_landmarks: int, chunk_rows: int,
+                        in_dtype: torch.dtype, out_dtype: torch.dtype) -> int:
+    """msa_attn_fwd_host_workspace_size (bytes of device workspace)."""
+    ws = int(_lib.msa_attn_fwd_host_workspace_size(
+        n, Hq, Hkv, d, n_landmarks, int(chunk_rows),
+        MSA_BF16 if in_dtype == torch.bfloat16 else MSA_F32,
+        MSA_BF16 if out_dtype == torch.bfloat16 else MSA_F32))
+    if ws == 0:
+        raise MsaError(MSA_ERR_INVALID_ARG, "invalid sizes for msa_attn_fwd_host")
+    return ws
+
+
+def _host_ptr(t):
+    if t.is_cuda:
+        raise ValueError("msa_attn_fwd_host takes host tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def attn_fwd_host(hq, hk, hv, hout, hlse, window: int, n_landmarks: int, scale: float,
+                  chunk_rows: int, workspace: torch.Tensor, stream=None, copy_in=None,
+                  copy_out=None) -> None:
+    """msa_attn_fwd_host: host q [n, Hq, d], k, v [n, Hkv, d] -> host out
+    [n, Hq, d], lse [Hq, n], streamed through the device workspace; returns
+    with the results final."""
+    n, Hq, d = hq.shape
+    Hkv = hk.shape[1]
+    _check(_lib.msa_attn_fwd_host(
+        _host_ptr(hq), _host_ptr(hk), _host_ptr(hv), _host_ptr(hout), _host_ptr(hlse), n, Hq, Hkv,
+        d, int(window), int(n_landmarks), float(scale), _dt(hq), _dt(hout), int(chunk_rows),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream),
+        None if copy_in is None else ctypes.c_void_p(copy_in.cuda_stream),
+        None if copy_out is None else ctypes.c_void_p(copy_out.cuda_stream)))
 
 
 def block_select(q, k_lm, sel, cnt, window: int, top_k: int, stream=None) -> None:

@@ -221,96 +221,46 @@ def msa_attention_trainable(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, w
     return _MSAAttention.apply(q, k, v, window, n_landmarks, scale)
 
 
+_copy_streams = {}
+
+
+def _streams_for(dev: torch.device):
+    """Two copy streams per device, made once and reused by every call."""
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    if key not in _copy_streams:
+        _copy_streams[key] = (torch.cuda.Stream(key), torch.cuda.Stream(key))
+    return _copy_streams[key]
+
+
 def msa_attention_host(hq: torch.Tensor, hk: torch.Tensor, hv: torch.Tensor, window: int,
                        n_landmarks: int, scale: float | None = None, out: torch.Tensor | None = None,
                        lse: torch.Tensor | None = None, chunk_rows: int | None = None,
                        device=None):
-    """Window + landmark attention on host (pinned) tensors.
+    """Window + landmark attention on host (pinned) tensors: msa_attn_fwd_host.
 
-    Rows [r0, r1) of the result need only K/V rows [0, r1) and the landmarks
-    of the blocks inside them, so everything streams through the device in
-    chunks of ``chunk_rows`` rows (default: n/32, at least 4096): on one copy
-    stream chunk c of K, V and Q
-    goes in, on the compute stream the landmarks of chunk c are pooled and
-    msa_attn_fwd_rows runs on its queries, on a second copy stream O of chunk
-    c comes back -- Q and O double-buffered -- so the transfers overlap the
-    kernels.  (When the chunk is not a whole number of landmark blocks, K
-    and V are copied and pooled whole before the first chunk.)  Returns
-    host (out [n, Hq, d] in q's dtype, lse [Hq, n] fp32), complete when the
-    call returns.
+    The library streams K, V and Q through the device in row chunks (default
+    about n/32 rows, at least 4096), pools each chunk's landmarks, attends
+    its rows and copies O back, the copies overlapping the kernels; this
+    function allocates the device workspace and the pinned outputs and
+    passes the current stream and two reused copy streams.  Returns host
+    (out [n, Hq, d] in q's dtype, lse [Hq, n] fp32), complete when the call
+    returns.
     """
     dev = torch.device(device) if device is not None else torch.device("cuda")
     n, Hq, d = hq.shape
     Hkv = hk.shape[1]
-    G = int(n_landmarks)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    if chunk_rows is None:  # about 32 chunks, at least 4096 rows (4096 at 128K tokens)
-        chunk_rows = max(4096, -(-n // 32))
-    rows = max(128, (int(chunk_rows) + 127) // 128 * 128)
-    blk = n // G if G > 0 else 1
-    kv_stream = G == 0 or rows % blk == 0  # K/V (and pooling) per chunk
     if out is None:
         out = torch.empty((n, Hq, d), dtype=hq.dtype, pin_memory=True)
     if lse is None:
         lse = torch.empty((Hq, n), dtype=torch.float32, pin_memory=True)
-    comp = torch.cuda.current_stream(dev)
-    s_in = torch.cuda.Stream(dev)
-    s_out = torch.cuda.Stream(dev)
-    s_in.wait_stream(comp)
-    with torch.cuda.stream(s_in):
-        dk = torch.empty((n, Hkv, d), dtype=hk.dtype, device=dev)
-        dv = torch.empty_like(dk)
-        qbuf = [torch.empty((min(rows, n), Hq, d), dtype=hq.dtype, device=dev)
-                for _ in range(2)]
-        if not kv_stream:
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-    # Zeros: while streaming, a landmark tile can reach past the blocks pooled
-    # so far; those (masked) rows must hold finite values, as 0 * NaN in the
-    # PV product would not vanish.
-    k_lm = torch.zeros((max(G, 1), Hkv, d), dtype=hk.dtype, device=dev) if G else None
-    v_lm = torch.zeros_like(k_lm) if G else None
-    if G and not kv_stream:
-        kv_ready = torch.cuda.Event()
-        kv_ready.record(s_in)
-        comp.wait_event(kv_ready)
-        B.landmark_pool(dk, dv, k_lm, v_lm, stream=comp)
-    obuf = [torch.empty((min(rows, n), Hq, d), dtype=hq.dtype, device=dev) for _ in range(2)]
-    dlse = torch.empty((Hq, n), dtype=torch.float32, device=dev)
-    q_free = [None, None]  # compute of the chunk that last used the buffer
-    o_free = [None, None]  # copy-out of the chunk that last used the buffer
-    for c, r0 in enumerate(range(0, n, rows)):
-        r1 = min(n, r0 + rows)
-        m = r1 - r0
-        b = c & 1
-        if q_free[b] is not None:
-            s_in.wait_event(q_free[b])
-        with torch.cuda.stream(s_in):
-            if kv_stream:
-                dk[r0:r1].copy_(hk[r0:r1], non_blocking=True)
-                dv[r0:r1].copy_(hv[r0:r1], non_blocking=True)
-            qbuf[b][:m].copy_(hq[r0:r1], non_blocking=True)
-        in_ready = torch.cuda.Event()
-        in_ready.record(s_in)
-        comp.wait_event(in_ready)
-        if G and kv_stream:  # the landmarks of this chunk's blocks (r0, r1: whole blocks)
-            l0, l1 = r0 // blk, r1 // blk
-            B.landmark_pool(dk[r0:r1], dv[r0:r1], k_lm[l0:l1], v_lm[l0:l1], stream=comp)
-        if o_free[b] is not None:
-            comp.wait_event(o_free[b])
-        B.attn_fwd_rows(qbuf[b][:m], dk, dv, k_lm, v_lm, obuf[b][:m], dlse, r0, window, G,
-                        scale, stream=comp)
-        done = torch.cuda.Event()
-        done.record(comp)
-        q_free[b] = done
-        s_out.wait_event(done)
-        with torch.cuda.stream(s_out):
-            out[r0:r1].copy_(obuf[b][:m], non_blocking=True)
-        o_free[b] = torch.cuda.Event()
-        o_free[b].record(s_out)
-    with torch.cuda.stream(s_out):
-        lse.copy_(dlse, non_blocking=True)
-    s_out.synchronize()
+    rows = 0 if chunk_rows is None else int(chunk_rows)
+    with torch.cuda.device(dev):
+        ws = torch.empty((B.host_workspace_size(n, Hq, Hkv, d, int(n_landmarks), rows, hq.dtype,
+                                                out.dtype),), dtype=torch.uint8, device=dev)
+        s_in, s_out = _streams_for(dev)
+        B.attn_fwd_host(hq, hk, hv, out, lse, window, int(n_landmarks), scale, rows, ws,
+                        stream=torch.cuda.current_stream(dev), copy_in=s_in, copy_out=s_out)
     return out, lse
 
 

@@ -866,6 +866,210 @@ msa_status msa_attn_fwd_partial_merge(const void* q, const void* k_chunk, const 
   return run_attn(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// Row-chunk plan of msa_attn_fwd_host: chunks of `rows` query rows (a
+// multiple of 128; default about n/32, at least 4096), and the workspace:
+// K and V whole [n, Hkv, d] and the landmarks [G, Hkv, d] in the input
+// dtype, Q staging for two chunks, O staging for two chunks in the output
+// dtype, the whole lse [Hq, n] fp32; each piece 256-byte aligned.
+struct HostPlan {
+  int64_t rows;
+  size_t k, v, klm, vlm, q[2], o[2], lse, total;
+};
+
+static HostPlan host_plan(int64_t n, int Hq, int Hkv, int d, int G, int64_t chunk_rows,
+                          msa_dtype in_dt, msa_dtype out_dt) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  HostPlan P{};
+  int64_t rows = chunk_rows > 0 ? chunk_rows : msa::max64(4096, (n + 31) / 32);
+  rows = msa::max64(128, (rows + 127) / 128 * 128);
+  P.rows = rows;
+  const int64_t stage = msa::min64(rows, n);
+  const size_t es = in_dt == MSA_BF16 ? 2 : 4, eo = out_dt == MSA_BF16 ? 2 : 4;
+  const size_t kv = static_cast<size_t>(n) * Hkv * d * es;
+  const size_t lm = static_cast<size_t>(G > 0 ? G : 1) * Hkv * d * es;
+  size_t at = 0;
+  P.k = at;
+  at += up(kv);
+  P.v = at;
+  at += up(kv);
+  P.klm = at;
+  at += up(lm);
+  P.vlm = at;
+  at += up(lm);
+  for (int b = 0; b < 2; ++b) {
+    P.q[b] = at;
+    at += up(static_cast<size_t>(stage) * Hq * d * es);
+  }
+  for (int b = 0; b < 2; ++b) {
+    P.o[b] = at;
+    at += up(static_cast<size_t>(stage) * Hq * d * eo);
+  }
+  P.lse = at;
+  at += up(static_cast<size_t>(Hq) * n * sizeof(float));
+  P.total = at;
+  return P;
+}
+
+size_t msa_attn_fwd_host_workspace_size(int64_t n, int Hq, int Hkv, int d, int n_landmarks,
+                                        int64_t chunk_rows, msa_dtype in_dt, msa_dtype out_dt) {
+  if (n < 1 || n > kMaxRows || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (d != 64 && d != 128) ||
+      !valid_dtype(in_dt) || !valid_dtype(out_dt) || n_landmarks < 0 || n_landmarks > n ||
+      (n_landmarks > 0 && n % n_landmarks != 0))
+    return 0;
+  return host_plan(n, Hq, Hkv, d, n_landmarks, chunk_rows, in_dt, out_dt).total;
+}
+
+// The window + landmark forward on host buffers: K, V and Q go to the
+// device in row chunks on `copy_in`, each chunk's landmarks are pooled and
+// its rows attended (msa_attn_fwd_rows) on `stream`, and O comes back on
+// `copy_out`, double-buffered, so that the copies overlap the kernels.
+// Rows [r0, r1) need only K/V rows below r1 and the landmarks of the blocks
+// inside them; when a chunk is not a whole number of landmark blocks, K and
+// V are copied and pooled whole before the first chunk instead.
+msa_status msa_attn_fwd_host(const void* q, const void* k, const void* v, void* out, float* lse,
+                             int64_t n, int Hq, int Hkv, int d, int64_t window, int n_landmarks,
+                             float scale, msa_dtype in_dt, msa_dtype out_dt, int64_t chunk_rows,
+                             void* workspace, size_t workspace_bytes, msa_stream_t stream,
+                             msa_stream_t copy_in, msa_stream_t copy_out) {
+  msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, window, scale, in_dt);
+  if (st != MSA_OK) return st;
+  if (n < 1 || n > kMaxRows) return fail(MSA_ERR_INVALID_ARG, "n=%lld out of range", (long long)n);
+  if (!valid_dtype(out_dt)) return fail(MSA_ERR_INVALID_ARG, "bad output dtype %d", (int)out_dt);
+  if (n_landmarks < 0 || n_landmarks > n || (n_landmarks > 0 && n % n_landmarks != 0))
+    return fail(MSA_ERR_INVALID_ARG, "G=%d must satisfy 0 <= G <= n and n %% G == 0 (n=%lld)",
+                n_landmarks, (long long)n);
+  if (chunk_rows < 0) return fail(MSA_ERR_INVALID_ARG, "chunk_rows=%lld", (long long)chunk_rows);
+  const HostPlan P = host_plan(n, Hq, Hkv, d, n_landmarks, chunk_rows, in_dt, out_dt);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(MSA_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
+  if (workspace_bytes < P.total)
+    return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                P.total);
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const cudaStream_t si = copy_in ? reinterpret_cast<cudaStream_t>(copy_in) : cs;
+  const cudaStream_t so = copy_out ? reinterpret_cast<cudaStream_t>(copy_out) : cs;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int G = n_landmarks;
+  const int64_t blk = G > 0 ? n / G : 1;
+  const int64_t rows = P.rows;
+  const bool kv_stream = G == 0 || rows % blk == 0;  // K/V and pooling per chunk
+  const size_t es = in_dt == MSA_BF16 ? 2 : 4, eo = out_dt == MSA_BF16 ? 2 : 4;
+  const size_t tok_kv = static_cast<size_t>(Hkv) * d * es;
+  const size_t tok_q = static_cast<size_t>(Hq) * d * es, tok_o = static_cast<size_t>(Hq) * d * eo;
+  const uint8_t* hk = static_cast<const uint8_t*>(k);
+  const uint8_t* hv = static_cast<const uint8_t*>(v);
+  const uint8_t* hq = static_cast<const uint8_t*>(q);
+  uint8_t* ho = static_cast<uint8_t*>(out);
+  float* dlse = reinterpret_cast<float*>(ws + P.lse);
+
+  // Events: start (prior work on `stream`), K/V whole, and per staging
+  // buffer: inputs landed, chunk computed, output copied back.
+  cudaEvent_t ev[8] = {};
+  int n_ev = 0;
+  cudaError_t e = cudaSuccess;
+  for (; n_ev < 8 && e == cudaSuccess; ++n_ev)
+    e = cudaEventCreateWithFlags(&ev[n_ev], cudaEventDisableTiming);
+  auto finish = [&](msa_status result) {
+    cudaStreamSynchronize(si);
+    cudaStreamSynchronize(cs);
+    cudaStreamSynchronize(so);
+    for (int i = 0; i < 8; ++i)
+      if (ev[i]) cudaEventDestroy(ev[i]);
+    return result;
+  };
+  if (e != cudaSuccess) return finish(fail(MSA_ERR_CUDA, "cudaEventCreate: %s", cudaGetErrorString(e)));
+  cudaEvent_t ev_start = ev[0], ev_kv = ev[1];
+  cudaEvent_t* ev_in = &ev[2];
+  cudaEvent_t* ev_done = &ev[4];
+  cudaEvent_t* ev_ofree = &ev[6];
+  bool have_done[2] = {false, false}, have_ofree[2] = {false, false};
+#define MSA_HOST_CHECK(call)                                                                 \
+  do {                                                                                       \
+    cudaError_t e_ = (call);                                                                 \
+    if (e_ != cudaSuccess)                                                                   \
+      return finish(fail(MSA_ERR_CUDA, "host path, %s: %s", #call, cudaGetErrorString(e_))); \
+  } while (0)
+  MSA_HOST_CHECK(cudaEventRecord(ev_start, cs));
+  MSA_HOST_CHECK(cudaStreamWaitEvent(si, ev_start, 0));
+  MSA_HOST_CHECK(cudaStreamWaitEvent(so, ev_start, 0));
+  if (G > 0) {
+    // Landmark tiles can reach past the blocks pooled so far; those masked
+    // rows must hold finite values (0 times NaN would not vanish in PV).
+    const size_t lm_bytes = static_cast<size_t>(G) * tok_kv;
+    MSA_HOST_CHECK(cudaMemsetAsync(ws + P.klm, 0, lm_bytes, cs));
+    MSA_HOST_CHECK(cudaMemsetAsync(ws + P.vlm, 0, lm_bytes, cs));
+  }
+  if (!kv_stream) {
+    MSA_HOST_CHECK(cudaMemcpyAsync(ws + P.k, hk, n * tok_kv, cudaMemcpyHostToDevice, si));
+    MSA_HOST_CHECK(cudaMemcpyAsync(ws + P.v, hv, n * tok_kv, cudaMemcpyHostToDevice, si));
+    MSA_HOST_CHECK(cudaEventRecord(ev_kv, si));
+    MSA_HOST_CHECK(cudaStreamWaitEvent(cs, ev_kv, 0));
+    msa::PoolArgs pa{ws + P.k, ws + P.v, ws + P.klm, ws + P.vlm, n, Hkv * d, G,
+                     in_dt == MSA_BF16 ? 1 : 0};
+    MSA_HOST_CHECK(msa::launch_landmark_pool(pa, cs));
+  }
+  for (int64_t r0 = 0, c = 0; r0 < n; r0 += rows, ++c) {
+    const int64_t r1 = msa::min64(n, r0 + rows), m = r1 - r0;
+    const int b = static_cast<int>(c & 1);
+    if (have_done[b]) MSA_HOST_CHECK(cudaStreamWaitEvent(si, ev_done[b], 0));
+    if (kv_stream) {
+      MSA_HOST_CHECK(cudaMemcpyAsync(ws + P.k + r0 * tok_kv, hk + r0 * tok_kv, m * tok_kv,
+                                     cudaMemcpyHostToDevice, si));
+      MSA_HOST_CHECK(cudaMemcpyAsync(ws + P.v + r0 * tok_kv, hv + r0 * tok_kv, m * tok_kv,
+                                     cudaMemcpyHostToDevice, si));
+    }
+    MSA_HOST_CHECK(cudaMemcpyAsync(ws + P.q[b], hq + r0 * tok_q, m * tok_q,
+                                   cudaMemcpyHostToDevice, si));
+    MSA_HOST_CHECK(cudaEventRecord(ev_in[b], si));
+    MSA_HOST_CHECK(cudaStreamWaitEvent(cs, ev_in[b], 0));
+    if (G > 0 && kv_stream) {  // the landmarks of this chunk's (whole) blocks
+      const int64_t l0 = r0 / blk, l1 = r1 / blk;
+      msa::PoolArgs pa{ws + P.k + r0 * tok_kv, ws + P.v + r0 * tok_kv, ws + P.klm + l0 * tok_kv,
+                       ws + P.vlm + l0 * tok_kv, m, Hkv * d, static_cast<int>(l1 - l0),
+                       in_dt == MSA_BF16 ? 1 : 0};
+      MSA_HOST_CHECK(msa::launch_landmark_pool(pa, cs));
+    }
+    if (have_ofree[b]) MSA_HOST_CHECK(cudaStreamWaitEvent(cs, ev_ofree[b], 0));
+    msa::AttnArgs a{};
+    a.q = ws + P.q[b];
+    a.k = ws + P.k;
+    a.v = ws + P.v;
+    a.k_lm = G > 0 ? ws + P.klm : nullptr;
+    a.v_lm = G > 0 ? ws + P.vlm : nullptr;
+    a.out = ws + P.o[b];
+    a.lse = dlse + r0;
+    a.lse_ld = n;
+    a.n_q = m;
+    a.q_start = r0;
+    a.n_kv = n;
+    a.kv_start = 0;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.window = window;
+    a.G = G;
+    a.block = blk;
+    a.scale = scale;
+    a.in_bf16 = in_dt == MSA_BF16;
+    a.out_bf16 = out_dt == MSA_BF16;
+    st = run_attn(a, cs);
+    if (st != MSA_OK) return finish(st);
+    MSA_HOST_CHECK(cudaEventRecord(ev_done[b], cs));
+    have_done[b] = true;
+    MSA_HOST_CHECK(cudaStreamWaitEvent(so, ev_done[b], 0));
+    MSA_HOST_CHECK(cudaMemcpyAsync(ho + r0 * tok_o, ws + P.o[b], m * tok_o,
+                                   cudaMemcpyDeviceToHost, so));
+    MSA_HOST_CHECK(cudaEventRecord(ev_ofree[b], so));
+    have_ofree[b] = true;
+  }
+  // lse of every chunk (the last chunk's compute, which `so` waited for,
+  // comes after all the others on `stream`).
+  MSA_HOST_CHECK(cudaMemcpyAsync(lse, dlse, static_cast<size_t>(Hq) * n * sizeof(float),
+                                 cudaMemcpyDeviceToHost, so));
+#undef MSA_HOST_CHECK
+  return finish(ok());
+}
+
 msa_status msa_lse_merge(const float* const* o_parts, const float* const* lse_parts, int n_parts,
                          void* out, float* lse, int64_t n, int Hq, int d, msa_dtype out_dt,
                          msa_stream_t stream) {

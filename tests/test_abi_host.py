@@ -348,3 +348,30 @@ def test_global_rows_backward_validation(lib):
     assert call(ng=0) == 1
     assert call(wsb=need - 1) == 1
     assert call(idt=0) == 2
+
+
+def test_host_path_validation(lib):
+    """msa_attn_fwd_host: argument and workspace checks before any copy."""
+    size = lib.msa_attn_fwd_host_workspace_size
+    assert size(0, 4, 2, 128, 4, 0, 1, 0) == 0                  # n < 1
+    assert size(256, 4, 3, 128, 4, 0, 1, 0) == 0                # Hq % Hkv
+    assert size(256, 4, 2, 96, 4, 0, 1, 0) == 0                 # d
+    assert size(256, 4, 2, 128, 3, 0, 1, 0) == 0                # n % G
+    need = size(256, 4, 2, 128, 4, 0, 1, 0)
+    # K, V whole + landmarks + two chunks of Q and O (256 rows: one chunk) + lse
+    assert need >= 2 * 256 * 2 * 128 * 2 + 2 * 256 * 4 * 128 * 2 + 2 * 256 * 4 * 128 * 4
+    f = lib.msa_attn_fwd_host
+
+    def call(**kw):
+        a = dict(q=GOOD, ws=GOOD, ws_bytes=need, chunk=0, G=4)
+        a.update(kw)
+        return f(a["q"], GOOD, GOOD, GOOD, GOOD, 256, 4, 2, 128, 16, a["G"], ctypes.c_float(0.1),
+                 1, 0, a["chunk"], a["ws"], a["ws_bytes"], None, None, None)
+
+    assert call(q=None) == 1
+    assert call(G=3) == 1
+    assert call(chunk=-1) == 1
+    assert call(ws=None) == 1
+    assert call(ws=P((1 << 20) + 128)) == 1                      # not 256-byte aligned
+    assert call(ws_bytes=need - 1) == 1
+    assert "needed" in _err(lib)

@@ -1,5 +1,5 @@
-"""Query-row ranges (msa_attn_fwd_rows) and the host streaming API
-(msa_attention_host): row chunks reproduce the whole-sequence call bit for
+"""Query-row ranges (msa_attn_fwd_rows) and the host streaming entry point
+(msa_attn_fwd_host, and msa_attention_host above it): row chunks reproduce the whole-sequence call bit for
 bit when they start on 128-row tiles (the same tiles run the same
 arithmetic), ragged chunks match the oracle at their global positions, and
 the host API returns exactly the device API's results (K/V and landmarks
@@ -66,14 +66,39 @@ def test_ragged_row_range_matches_oracle(dt, d, q_start, n_q):
 
 @pytest.mark.parametrize("name,chunk", [("32k_outliers", 4096), ("128k_70b_layer", 16384),
                                         ("pr1_2k", 300), ("32k_outliers", 4160),
-                                        ("ring_128k", 20000), ("128k_70b_layer", None)])
+                                        ("ring_128k", 20000), ("128k_70b_layer", None),
+                                        ("128k_70b_layer", 4224)])
 def test_host_api_equals_device_api(name, chunk):
+    """msa_attn_fwd_host through the Python API (copy streams, pinned
+    buffers): whole landmark blocks per chunk (K/V streamed), chunks that
+    are not (K/V copied and pooled whole first: 4224 rows at B = 256),
+    ragged last chunks, no landmarks, the fp32 CUDA-core path."""
     import long_context_sparse_landmark_gb300.api as api
     wl = WORKLOADS[name]
     q, k, v = generate(wl, device=DEV)
     ref_o, ref_l = api.msa_attention(q, k, v, wl.window, wl.G, wl.scale)
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
     ho, hl = api.msa_attention_host(hq, hk, hv, wl.window, wl.G, wl.scale, chunk_rows=chunk)
+    assert torch.equal(ho, ref_o.cpu()) and torch.equal(hl, ref_l.cpu())
+
+
+@pytest.mark.parametrize("dt,d,n,G,w,chunk", [("bf16", 128, 3000, 12, 700, 640),
+                                              ("f32", 64, 2048, 16, 256, 128),
+                                              ("bf16", 128, 1000, 0, 1000, 0)])
+def test_host_entry_point_one_stream(dt, d, n, G, w, chunk):
+    """The C entry point called directly with no copy streams (everything on
+    one stream) and pageable host memory: same bits as msa_attn_fwd."""
+    B = binding()
+    wl = Workload("host1", n, 8, 2, d, w, G, dt, seed=n + G)
+    q, k, v = generate(wl, device=DEV)
+    ref_o, ref_l = run_gpu_attention(q, k, v, wl)
+    hq, hk, hv = (t.cpu() for t in (q, k, v))
+    ho = torch.full((n, 8, d), float("nan"))
+    hl = torch.full((8, n), float("nan"))
+    ws = torch.empty((B.host_workspace_size(n, 8, 2, d, G, chunk, q.dtype, torch.float32),),
+                     dtype=torch.uint8, device=DEV)
+    B.attn_fwd_host(hq, hk, hv, ho, hl, w, G, wl.scale, chunk, ws)
+    assert B.device_status() == 0
     assert torch.equal(ho, ref_o.cpu()) and torch.equal(hl, ref_l.cpu())
 
 
