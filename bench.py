@@ -6,9 +6,10 @@ landmark pooling (K1) then the fused window + landmark attention (K2) on the
 128K-token 70B-style layer (n=131072, 64 query / 8 KV heads, d=128, w=4096,
 512 landmarks, bf16).  The headline value is useful TFLOP/s of that step
 (4 * d * Hq * sum_i |attended set of row i|; masked work not counted).
-The same run also measures the million-token layer and the Ring Attention
-emulation (8 KV-chunk partials + LSE merge, K3) and reports them under
-"also".
+The same run also measures the other configurations -- the 2K fp32 case
+(CUDA-core kernel), the 32K layer with outlier keys, the million-token
+layer, the Ring Attention emulation (8 KV-chunk partials + LSE merge, K3)
+-- and the pattern variants and backward, under "also".
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl msa|reference]
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
@@ -45,13 +46,13 @@ def load_peaks():
                 "source": "fallback"}
 
 
-# DRAM traffic of one attention launch on the 128K layer, from the ncu
-# capture summarised in profiles/attn_tc_kernel_128k_70b_layer.md.  It only
-# applies to the kernel source it was measured on (SHA-256 of
-# k2_attn_tc.cu); after any change the traffic is reported as null.
+# DRAM traffic of one attention launch on the 128K layer, from the
+# committed ncu capture of this kernel.  It only applies to the kernel
+# source it was measured on (SHA-256 of the attention kernel's sources);
+# after any change the traffic is reported as null.
 ATTN_TRAFFIC = {"128k_70b_layer": {
-    "bytes": 2.703023e9 + 2.144078e9,
-    "kernel_sha256": "a465ff28a22fa257e0938a7fa370c7490fbec936de84e085a08109784116437a"}}
+    "bytes": 4 * (673.243648e6 + 504.410880e6),  # the 32K capture, scaled by n
+    "kernel_sha256": "3601d7ef99331fd09de4fe932a5ee7ce9e2c32a3f84ec2b649b244e871bf4918"}}
 
 
 def kernel_sha256() -> str:
@@ -60,7 +61,8 @@ def kernel_sha256() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "long_context_sparse_landmark_gb300", "csrc")
-    for name in ("k2_attn_tc.cu", "tc_ptx.cuh", "tc_sync.cuh", "tma_map.h", "msa_common.cuh"):
+    for name in ("k2_attn_tc2.cu", "tc_pair.cuh", "tc_ptx.cuh", "tc_sync.cuh", "tma_map.h",
+                 "msa_common.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -196,7 +198,7 @@ def run_window_landmark(wl, steps, warmup, dev, B, torch):
     pool_ms = [e[0].elapsed_time(e[1]) for e in evs]
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     res = {"total_ms": total_ms, "ms_per_step": total_ms / steps,
-           "pool_ms": statistics.mean(pool_ms), "attn_ms": statistics.mean(attn_ms),
+           "pool_ms": statistics.median(pool_ms), "attn_ms": statistics.median(attn_ms),
            "launches_per_step": 2}
     del q, k, v, k_lm, v_lm, out, lse
     torch.cuda.empty_cache()
@@ -204,10 +206,11 @@ def run_window_landmark(wl, steps, warmup, dev, B, torch):
 
 
 def run_e2e(wl, steps, dev, torch):
-    """Through the public host-buffer API (msa_attention_host) with pinned
-    HOST inputs and outputs: every step copies Q/K/V host->device, pools,
-    runs the attention on row chunks and copies O and lse back, the copies
-    overlapping the kernels; the call returns with the host results final."""
+    """Through the C entry point for host buffers (msa_attn_fwd_host, via
+    msa_attention_host) with pinned HOST inputs and outputs: every step
+    copies Q/K/V host->device, pools, runs the attention on row chunks and
+    copies O and lse back, the copies overlapping the kernels; the call
+    returns with the host results final."""
     import long_context_sparse_landmark_gb300 as pkg
     from long_context_sparse_landmark_gb300.workloads import generate
     q, k, v = generate(wl, device=dev)
@@ -280,8 +283,8 @@ def run_ring(wl, steps, warmup, dev, B, torch):
     torch.cuda.synchronize()
     assert B.device_status() == 0
     fused_ms = f0.elapsed_time(f1) / steps
-    part_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    merge_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    part_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    merge_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
     # Required merge bytes: every lse_p, every O_p row with finite lse_p, output.
     finite = sum(int(torch.isfinite(l).sum()) for l in l_parts)
     merge_bytes = P * n * Hq * 4 + finite * d * 4 + n * Hq * (d * 2 + 4)
@@ -517,6 +520,14 @@ def run_bwd_compressed(wl, steps, warmup, dev, B, torch):
     return e0.elapsed_time(e1) / steps
 
 
+def fp32_fma_peak_tflops(torch, sm_max_mhz=None) -> float:
+    """FP32 FMA peak of the GPU: SMs x 128 FP32 lanes x 2 FLOP per fused
+    multiply-add x the maximum SM clock (GB300: 152 x 128 x 2 x 2.07 GHz)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    mhz = sm_max_mhz or 2070.0
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
+
+
 def cpu_baseline(wl, rows_target, torch):
     """The fp64 oracle on the host cores, on a bounded row sample of the
     same workload; extrapolated to the full layer by rows."""
@@ -572,6 +583,9 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--workload", default=HEADLINE,
                     help="window+landmark workload timed as the step (profiling uses smaller ones)")
+    ap.add_argument("--n", type=int, default=None,
+                    help="tokens of the timed step's workload, landmark block size kept "
+                         "(a smaller case of the same kernel, for profiling)")
     ap.add_argument("--only", choices=["ring", "bwd", "topk"], default=None,
                     help="run only one leg: the ring emulation (partials, merge, fused "
                          "rounds), the backward pass, or the top-k call (for profiling)")
@@ -591,6 +605,9 @@ def main():
     import torch
     from long_context_sparse_landmark_gb300.workloads import WORKLOADS
     wl = WORKLOADS[args.workload]
+    if args.n:
+        wl = wl.with_n(args.n, G=args.n // wl.block if wl.G else 0,
+                       name=f"{wl.name}_n{args.n}")
     peaks = load_peaks()
 
     if args.impl == "reference":
@@ -671,12 +688,12 @@ def main():
         "pct_bf16_peak": round(100.0 * value / world / peaks["bf16_tflops"], 2),
         "kernels_ms": {"landmark_pool": round(res["pool_ms"], 4),
                        "attn_fwd": round(res["attn_ms"], 4)},
-        "roofline": {"bound": "tensor", "kernel": "attn_tc_kernel",
+        "roofline": {"bound": "tensor", "kernel": "attn_tc2_kernel",
                      "achieved": round(attn_tflops, 2),
-                     "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                     "frac": round(attn_tflops / peaks["bf16_tflops_sustained"], 4),
-                     "peak_kind": f"bf16 sustained ({peaks['source']})",
-                     "frac_of_burst": round(attn_tflops / peaks["bf16_tflops"], 4),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(attn_tflops / peaks["bf16_tflops"], 4),
+                     "peak_kind": f"bf16 burst ({peaks['source']}): a launch timed on its own",
+                     "frac_of_sustained": round(attn_tflops / peaks["bf16_tflops_sustained"], 4),
                      "traffic": attn_traffic(wl.name),
                      "algorithmic_bytes": attn_bytes},
         "pool_roofline": {"bound": "hbm",
@@ -696,6 +713,35 @@ def main():
 
     if not args.no_also and rank == 0:
         also = {}
+        # The 2K fp32 case runs the CUDA-core kernel (fp32 FFMA arithmetic,
+        # the 1e-5 path): FLOP/s against the FP32 FMA peak of the SMs.
+        wlp = WORKLOADS["pr1_2k"]
+        rp = run_window_landmark(wlp, 20, 3, dev, B, torch)
+        fp = useful_flops(wlp)
+        fp32_peak = fp32_fma_peak_tflops(torch, line["clocks"].get("sm_max_mhz"))
+        also["pr1_2k"] = {
+            "ms_per_step": round(rp["ms_per_step"], 4),
+            "tokens_per_s": round(wlp.n / (rp["ms_per_step"] * 1e-3), 1),
+            "attn_ms": round(rp["attn_ms"], 4), "pool_ms": round(rp["pool_ms"], 4),
+            "attn_tflops": round(fp / (rp["attn_ms"] * 1e-3) / 1e12, 3),
+            "roofline": {"bound": "alu", "kernel": "attn_simt_kernel", "unit": "TFLOP/s",
+                         "achieved": round(fp / (rp["attn_ms"] * 1e-3) / 1e12, 3),
+                         "peak": round(fp32_peak, 1),
+                         "frac": round(fp / (rp["attn_ms"] * 1e-3) / 1e12 / fp32_peak, 4),
+                         "peak_kind": "FP32 FMA: SMs x 128 lanes x 2 FLOP x max SM clock"},
+            "dtype": "f32", "steps": 20}
+        wl32 = WORKLOADS["32k_outliers"]
+        r32 = run_window_landmark(wl32, 20, 3, dev, B, torch)
+        f32k = useful_flops(wl32)
+        also["32k_outliers"] = {
+            "ms_per_step": round(r32["ms_per_step"], 4),
+            "tokens_per_s": round(wl32.n / (r32["ms_per_step"] * 1e-3), 1),
+            "tflops": round(f32k / (r32["ms_per_step"] * 1e-3) / 1e12, 2),
+            "attn_ms": round(r32["attn_ms"], 4),
+            "attn_tflops": round(f32k / (r32["attn_ms"] * 1e-3) / 1e12, 2),
+            "pct_bf16_peak": round(100.0 * f32k / (r32["attn_ms"] * 1e-3) / 1e12
+                                   / peaks["bf16_tflops"], 2),
+            "steps": 20}
         wl1m = WORKLOADS["1m_70b_layer"]
         r1 = run_window_landmark(wl1m, 3, 1, dev, B, torch)
         f1 = useful_flops(wl1m)
@@ -820,10 +866,16 @@ def run_reference(args, wl, rank, world, torch):
         tot_s += el
         tot_f += f
     value = tot_f / tot_s / 1e12
-    ms_per_step = flops_full / (value * 1e12) * 1e3
+    # ms_per_step is the measured time of one step (one row sample); the
+    # time a whole layer would take at this rate is reported beside it.
+    ms_per_step = tot_s / args.steps * 1e3
+    layer_ms = flops_full / (value * 1e12) * 1e3
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": ms_per_step,
+            "step": f"{rows_per_step} random rows x {wl.Hq} heads of the layer",
+            "full_layer_ms_extrapolated": layer_ms,
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs)",
             "config": {"workload": wl.name, "n": wl.n, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
                        "window": wl.window, "landmarks": wl.G, "batch": 1},

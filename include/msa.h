@@ -271,9 +271,15 @@ msa_status msa_attn_fwd_topk(const void *q, const void *k, const void *v,
  * the same kernels and results as msa_attn_fwd_topk.
  * The intermediates live in one fixed, file-scope device array of
  * MSA_NOALLOC_SCRATCH_BYTES per device; nothing is allocated or freed.
- *   - The first call on a device looks up that array's address (with the
- *     device current) and caches it; make that first call, on each device,
- *     before any stream capture begins.
+ *   - The array belongs to the library's device code: once that code is
+ *     loaded on a device (by the first call of any entry point there), the
+ *     device holds its MSA_NOALLOC_SCRATCH_BYTES (16 MiB) whether or not
+ *     this entry point is ever called, until the context is destroyed.
+ *   - Every call looks up the array's address in the current context (no
+ *     address is kept between calls, so a cudaDeviceReset in between is
+ *     harmless).  The first call on a device may load the library's device
+ *     code; make one call of the library on each device before any stream
+ *     capture begins.
  *   - The scratch is shared by every call on a device: calls whose work can
  *     overlap (unordered streams, several host threads) race on it and give
  *     wrong results.  Order them on one stream.

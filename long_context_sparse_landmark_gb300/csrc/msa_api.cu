@@ -8,7 +8,6 @@
 #include <string.h>
 
 #include <atomic>
-#include <mutex>
 #include <string>
 
 #include "msa_common.cuh"
@@ -39,28 +38,18 @@ bool valid_dtype(msa_dtype d) { return d == MSA_F32 || d == MSA_BF16; }
 // Per-device status word written by kernels when a bounded wait runs out.
 __device__ int g_device_status;
 
-constexpr int kMaxDevices = 64;
-std::mutex g_status_mu;
-int* g_status_ptr[kMaxDevices] = {};
-
 std::atomic<uint64_t> g_wait_limit_ns{0};
 std::atomic<int> g_force_single_cta{0};
 constexpr uint64_t kDefaultWaitNs = 4000000000ull;
 
+// Address of the status word in the current context, looked up on every
+// call: a cached address would dangle after cudaDeviceReset.
 msa_status device_status_ptr(int** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return fail(MSA_ERR_UNSUPPORTED, "device ordinal %d", dev);
-  std::lock_guard<std::mutex> lk(g_status_mu);
-  if (!g_status_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_device_status);
-    if (e != cudaSuccess)
-      return fail(MSA_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-    g_status_ptr[dev] = static_cast<int*>(p);
-  }
-  *out = g_status_ptr[dev];
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_device_status);
+  if (e != cudaSuccess)
+    return fail(MSA_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+  *out = static_cast<int*>(p);
   return MSA_OK;
 }
 
@@ -166,25 +155,15 @@ static __device__ __align__(256) uint8_t g_topk_scratch[MSA_NOALLOC_SCRATCH_BYTE
 
 namespace {
 
-std::mutex g_scratch_mu;
-uint8_t* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
+// Device address of the scratch on the current device, looked up on every
+// call (a table lookup once the module is loaded): an address kept from an
+// earlier call would dangle after cudaDeviceReset or in another context.
 msa_status topk_scratch_ptr(uint8_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return fail(MSA_ERR_UNSUPPORTED, "device ordinal %d", dev);
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_topk_scratch);
-    if (e != cudaSuccess)
-      return fail(MSA_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-    g_scratch_ptr[dev] = static_cast<uint8_t*>(p);
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_topk_scratch);
+  if (e != cudaSuccess)
+    return fail(MSA_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+  *out = static_cast<uint8_t*>(p);
   return MSA_OK;
 }
 

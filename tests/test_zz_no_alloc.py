@@ -2,8 +2,9 @@
 per-device scratch gives the results of msa_attn_fwd_topk with a caller
 workspace, call after call, and refuses sizes its scratch cannot hold.
 
-Named to be collected last, so that it also runs after every other GPU test
-has used the library in the same process."""
+The test first runs a larger shape, which writes more of the scratch than
+any later case, so every later call starts on bytes left by another call;
+it does not depend on what ran before it in the process."""
 import ctypes
 
 import numpy as np
@@ -15,6 +16,10 @@ from tests.gpu_helpers import binding, compare, tol
 
 DEV = "cuda"
 SCRATCH_BYTES = 16 << 20
+
+# Written first: 32K tokens, 128 blocks, top-48 over 4 KV heads fills more of
+# the scratch (block-mean keys, selection, counts) than any case below.
+LARGER = ("bf16", 128, 32768, 128, 1024, 48, 16, 4)
 
 CASES = [
     # dt, d, n, G, w, top_k, Hq, Hkv   (tensor-core path, then CUDA-core paths)
@@ -37,7 +42,12 @@ def _with_workspace(q, k, v, wl, out_dtype):
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
     B = binding()
+    big = B.topk_workspace_size(LARGER[2], LARGER[7], LARGER[1], LARGER[3], LARGER[5],
+                                torch.bfloat16)
     for dt, d, n, G, w, top_k, Hq, Hkv in CASES:
+        dtype = torch.bfloat16 if dt == "bf16" else torch.float32
+        assert B.topk_workspace_size(n, Hkv, d, G, top_k, dtype) < big
+    for dt, d, n, G, w, top_k, Hq, Hkv in [LARGER] + CASES:
         wl = Workload("noalloc", n, Hq, Hkv, d, w, G, dt, seed=n + G, top_k=top_k)
         q, k, v = generate(wl, device=DEV)
         ref_o, ref_l = _with_workspace(q, k, v, wl, torch.float32)
