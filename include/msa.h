@@ -470,10 +470,23 @@ msa_status msa_lse_merge(const float *const *o_parts,
                          msa_dtype out_dt, msa_stream_t stream);
 
 /*
- * Which attention kernel msa_attn_fwd / msa_attn_fwd_partial run for these
- * arguments: 1 = tensor-core kernel (TMA + tcgen05), 0 = CUDA-core kernel.
+ * Which attention kernel msa_attn_fwd, msa_attn_fwd_partial,
+ * msa_attn_fwd_band, msa_attn_fwd_rows and msa_attn_fwd_host run for these
+ * arguments: 1 = a tensor-core kernel (TMA + tcgen05), 0 = the CUDA-core
+ * kernel (fp32 FFMA).  The tensor-core kernels take bf16 inputs with
+ * d = 128; fp32 inputs, and bf16 with d = 64, run on CUDA cores (many
+ * times slower for bf16).
  */
 int msa_attn_uses_tensor_cores(int Hq, int Hkv, int d, msa_dtype in_dt);
+
+/*
+ * The same for msa_attn_fwd_topk and msa_attn_fwd_topk_noalloc, whose
+ * attention also needs the key block n / n_landmarks to be a whole number
+ * of 128-key tiles: 1 = tensor cores, 0 = CUDA cores (also for
+ * n_landmarks < 1 or n < n_landmarks, which the call itself refuses).
+ */
+int msa_attn_fwd_topk_uses_tensor_cores(int64_t n, int Hq, int Hkv, int d,
+                                        int n_landmarks, msa_dtype in_dt);
 
 /*
  * Reads (and, if `clear` is nonzero, resets) the status word that the

@@ -27,7 +27,7 @@ EXPORTS = ("msa_version", "msa_last_error_string", "msa_landmark_pool", "msa_att
            "msa_attn_bwd", "msa_attn_bwd_workspace_size", "msa_attn_bwd_global_rows",
            "msa_attn_bwd_global_rows_workspace_size", "msa_attn_fwd_partial",
            "msa_attn_fwd_partial_merge", "msa_lse_merge",
-           "msa_attn_uses_tensor_cores", "msa_device_status", "msa_debug_set_wait_limit_ns",
+           "msa_attn_uses_tensor_cores", "msa_attn_fwd_topk_uses_tensor_cores", "msa_device_status", "msa_debug_set_wait_limit_ns",
            "msa_debug_force_single_cta")
 
 
@@ -100,6 +100,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_lse_merge.restype = i32
     lib.msa_attn_uses_tensor_cores.argtypes = [i32, i32, i32, i32]
     lib.msa_attn_uses_tensor_cores.restype = i32
+    lib.msa_attn_fwd_topk_uses_tensor_cores.argtypes = [i64, i32, i32, i32, i32, i32]
+    lib.msa_attn_fwd_topk_uses_tensor_cores.restype = i32
     lib.msa_device_status.argtypes = [i32]
     lib.msa_device_status.restype = i32
     lib.msa_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
@@ -147,6 +149,12 @@ def version() -> int:
 def uses_tensor_cores(Hq: int, Hkv: int, d: int, dtype: torch.dtype) -> bool:
     return bool(_lib.msa_attn_uses_tensor_cores(Hq, Hkv, d, MSA_BF16 if dtype == torch.bfloat16
                                                 else MSA_F32))
+
+
+def topk_uses_tensor_cores(n: int, Hq: int, Hkv: int, d: int, n_landmarks: int,
+                           dtype: torch.dtype) -> bool:
+    return bool(_lib.msa_attn_fwd_topk_uses_tensor_cores(
+        n, Hq, Hkv, d, n_landmarks, MSA_BF16 if dtype == torch.bfloat16 else MSA_F32))
 
 
 def device_status(clear: bool = True) -> int:

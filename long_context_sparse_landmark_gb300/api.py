@@ -8,10 +8,39 @@ arguments: every arithmetic step runs in libmsa's CUDA kernels.
 from __future__ import annotations
 
 import math
+import warnings
 
 import torch
 
 from . import _binding as B
+
+
+class CudaCorePathWarning(RuntimeWarning):
+    """A bf16 attention runs on the CUDA-core (fp32 FFMA) kernel, many times
+    slower than the tensor-core kernels, because of its shape."""
+
+
+_warned = set()
+
+
+def _check_tensor_cores(q: torch.Tensor, Hkv: int, topk_landmarks: int | None = None):
+    """Warn (once per shape) when bf16 input is routed to the CUDA-core
+    kernel: d other than 128, or (top-k) a key block that is not a whole
+    number of 128-key tiles.  fp32 input always runs there, by design."""
+    if q.dtype != torch.bfloat16:
+        return
+    n, Hq, d = q.shape
+    if topk_landmarks is None:
+        tc = B.uses_tensor_cores(Hq, Hkv, d, q.dtype)
+    else:
+        tc = B.topk_uses_tensor_cores(n, Hq, Hkv, d, topk_landmarks, q.dtype)
+    key = (n if topk_landmarks is not None else 0, Hq, Hkv, d, topk_landmarks)
+    if not tc and key not in _warned:
+        _warned.add(key)
+        why = (f"d={d} (the tensor-core kernels take d=128)" if d != 128 else
+               f"key blocks of {n // max(topk_landmarks, 1)} tokens are not a multiple of 128")
+        warnings.warn(f"bf16 attention on the CUDA-core kernel: {why}", CudaCorePathWarning,
+                      stacklevel=3)
 
 
 def landmarks(k: torch.Tensor, v: torch.Tensor, n_landmarks: int, stream=None):
@@ -40,6 +69,7 @@ def msa_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int
         k_lm, v_lm = landmarks(k, v, n_landmarks, stream=stream)
     else:
         k_lm = v_lm = None
+    _check_tensor_cores(q, k.shape[1])
     B.attn_fwd(q, k, v, k_lm, v_lm, out, lse, window, n_landmarks, scale, stream=stream)
     return out, lse
 
@@ -53,6 +83,7 @@ def band_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, band_block
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     out = torch.empty((n, Hq, d), dtype=out_dtype or q.dtype, device=q.device)
     lse = torch.empty((Hq, n), dtype=torch.float32, device=q.device)
+    _check_tensor_cores(q, k.shape[1])
     B.attn_fwd_band(q, k, v, out, lse, band_block, band_half, scale, stream=stream)
     return out, lse
 
@@ -68,6 +99,7 @@ def topk_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: in
     lse = torch.empty((Hq, n), dtype=torch.float32, device=q.device)
     nbytes = B.topk_workspace_size(n, k.shape[1], d, n_landmarks, top_k, q.dtype)
     ws = torch.empty((nbytes,), dtype=torch.uint8, device=q.device)
+    _check_tensor_cores(q, k.shape[1], n_landmarks)
     B.attn_fwd_topk(q, k, v, out, lse, window, n_landmarks, top_k, scale, ws, stream=stream)
     return out, lse
 
@@ -89,6 +121,7 @@ def compressed_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, wind
     B.landmark_pool(k, v, k_lm, v_lm, stream=stream)
     out = torch.empty((n, Hq, d), dtype=out_dtype or q.dtype, device=q.device)
     lse = torch.empty((Hq, n), dtype=torch.float32, device=q.device)
+    _check_tensor_cores(q, Hkv)
     B.attn_fwd(q, k, v, k_lm, v_lm, out, lse, window, G, scale, stream=stream)
     if global_rows.numel() > 0:
         ws = torch.empty((B.global_rows_workspace_size(n, global_rows.numel(), Hq, Hkv, d),),
@@ -113,6 +146,7 @@ def ring_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_chunks: 
     window = n if window is None else window
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     c = n // n_chunks
+    _check_tensor_cores(q, k.shape[1])
     if fused:
         # The first round writes the running result (rows with no key get
         # lse = -inf, which later rounds treat as empty); the others merge.
@@ -255,6 +289,7 @@ def msa_attention_host(hq: torch.Tensor, hk: torch.Tensor, hv: torch.Tensor, win
     if lse is None:
         lse = torch.empty((Hq, n), dtype=torch.float32, pin_memory=True)
     rows = 0 if chunk_rows is None else int(chunk_rows)
+    _check_tensor_cores(hq, Hkv)
     with torch.cuda.device(dev):
         ws = torch.empty((B.host_workspace_size(n, Hq, Hkv, d, int(n_landmarks), rows, hq.dtype,
                                                 out.dtype),), dtype=torch.uint8, device=dev)

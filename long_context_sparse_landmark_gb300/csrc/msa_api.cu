@@ -1087,6 +1087,14 @@ int msa_attn_uses_tensor_cores(int Hq, int Hkv, int d, msa_dtype in_dt) {
   return msa::attn_tc_supported(Hq, Hkv, d, in_dt == MSA_BF16) ? 1 : 0;
 }
 
+int msa_attn_fwd_topk_uses_tensor_cores(int64_t n, int Hq, int Hkv, int d, int n_landmarks,
+                                        msa_dtype in_dt) {
+  if (n_landmarks < 1 || n < n_landmarks) return 0;
+  // Selected key blocks map to whole 128-key tiles on the tensor-core path.
+  const bool tiles_ok = (n / n_landmarks) % 128 == 0;
+  return tiles_ok && msa::attn_tc_supported(Hq, Hkv, d, in_dt == MSA_BF16) ? 1 : 0;
+}
+
 msa_status msa_device_status(int clear) {
   int* ptr = nullptr;
   msa_status st = device_status_ptr(&ptr);

@@ -375,3 +375,39 @@ def test_host_path_validation(lib):
     assert call(ws=P((1 << 20) + 128)) == 1                      # not 256-byte aligned
     assert call(ws_bytes=need - 1) == 1
     assert "needed" in _err(lib)
+
+
+def test_tensor_core_queries(lib):
+    """Which kernel a shape gets: tensor cores for bf16 with d = 128, and
+    for top-k only when the key block n / n_landmarks is a whole number of
+    128-key tiles; fp32, and bf16 with d = 64, run on CUDA cores."""
+    q = lib.msa_attn_uses_tensor_cores
+    assert q(64, 8, 128, 1) == 1 and q(64, 8, 128, 0) == 0 and q(8, 8, 64, 1) == 0
+    t = lib.msa_attn_fwd_topk_uses_tensor_cores
+    assert t(131072, 64, 8, 128, 512, 1) == 1           # blocks of 256
+    assert t(131072, 64, 8, 128, 2048, 1) == 0          # blocks of 64
+    assert t(131072, 64, 8, 128, 512, 0) == 0           # fp32
+    assert t(131072, 64, 8, 64, 512, 1) == 0            # d = 64
+    assert t(100, 4, 1, 128, 0, 1) == 0 and t(100, 4, 1, 128, 200, 1) == 0
+
+
+def test_python_api_warns_on_cuda_core_bf16():
+    """The user-facing calls warn once per shape when bf16 input is routed
+    to the CUDA-core kernel (host-side check only: no kernel runs here)."""
+    import warnings
+
+    import torch
+
+    from long_context_sparse_landmark_gb300 import api
+    api._warned.clear()
+    q = torch.zeros((2048, 4, 64), dtype=torch.bfloat16)
+    with pytest.warns(api.CudaCorePathWarning, match="d=64"):
+        api._check_tensor_cores(q, 1)
+    with warnings.catch_warnings():
+        warnings.simplefilter("error")
+        api._check_tensor_cores(q, 1)                                   # once per shape
+        api._check_tensor_cores(torch.zeros((2048, 4, 128), dtype=torch.bfloat16), 1)
+        api._check_tensor_cores(torch.zeros((2048, 4, 64)), 1)          # fp32: by design
+        api._check_tensor_cores(torch.zeros((4096, 8, 128), dtype=torch.bfloat16), 1, 16)
+    with pytest.warns(api.CudaCorePathWarning, match="not a multiple of 128"):
+        api._check_tensor_cores(torch.zeros((4096, 8, 128), dtype=torch.bfloat16), 1, 64)
