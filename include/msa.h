@@ -470,6 +470,20 @@ msa_status msa_lse_merge(const float *const *o_parts,
                          msa_dtype out_dt, msa_stream_t stream);
 
 /*
+ * 1 in the bounds-checked build of the library (compiled with
+ * -DMSA_DEBUG_BOUNDS, shipped as libmsa_debug.so), 0 in the normal one.  In
+ * the bounds-checked build every kernel tests each computed global offset
+ * against the extent the entry point's contract gives that buffer, and each
+ * TMA box origin against its tensor (x 16-byte aligned and inside the row,
+ * head in range, box overlapping the rows).  A violation records
+ * MSA_ERR_INVALID_ARG in the device status word (msa_device_status), prints
+ * the source line once, and the access is skipped (a TMA copy is still
+ * issued: out-of-range rows only read the fill value); nothing traps.  The
+ * results are otherwise those of the normal build, more slowly.
+ */
+int msa_debug_bounds_build(void);
+
+/*
  * Which attention kernel msa_attn_fwd, msa_attn_fwd_partial,
  * msa_attn_fwd_band, msa_attn_fwd_rows and msa_attn_fwd_host run for these
  * arguments: 1 = a tensor-core kernel (TMA + tcgen05), 0 = the CUDA-core

@@ -13,7 +13,10 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libmsa.so")
+# MSA_DEBUG_BOUNDS=1 loads the bounds-checked build (libmsa_debug.so, from
+# build.build(debug_bounds=True)) instead of the normal library.
+DEBUG_BOUNDS = os.environ.get("MSA_DEBUG_BOUNDS") == "1"
+LIB_PATH = os.path.join(_PKG, "libmsa_debug.so" if DEBUG_BOUNDS else "libmsa.so")
 
 MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_CUDA, MSA_ERR_TIMEOUT = range(5)
 MSA_F32, MSA_BF16 = 0, 1
@@ -21,13 +24,15 @@ MAX_MERGE_PARTS = 64
 
 # Every symbol include/msa.h declares.
 EXPORTS = ("msa_version", "msa_last_error_string", "msa_landmark_pool", "msa_attn_fwd",
-           "msa_attn_fwd_rows", "msa_attn_fwd_host", "msa_attn_fwd_host_workspace_size", "msa_attn_fwd_band", "msa_block_select", "msa_attn_fwd_select",
+           "msa_attn_fwd_rows", "msa_attn_fwd_host", "msa_attn_fwd_host_workspace_size",
+           "msa_attn_fwd_band", "msa_block_select", "msa_attn_fwd_select",
            "msa_attn_fwd_topk_workspace_size", "msa_attn_fwd_topk", "msa_attn_fwd_topk_noalloc",
            "msa_attn_fwd_global_rows", "msa_attn_fwd_global_rows_workspace_size",
            "msa_attn_bwd", "msa_attn_bwd_workspace_size", "msa_attn_bwd_global_rows",
            "msa_attn_bwd_global_rows_workspace_size", "msa_attn_fwd_partial",
            "msa_attn_fwd_partial_merge", "msa_lse_merge",
-           "msa_attn_uses_tensor_cores", "msa_attn_fwd_topk_uses_tensor_cores", "msa_device_status", "msa_debug_set_wait_limit_ns",
+           "msa_attn_uses_tensor_cores", "msa_attn_fwd_topk_uses_tensor_cores",
+           "msa_debug_bounds_build", "msa_device_status", "msa_debug_set_wait_limit_ns",
            "msa_debug_force_single_cta")
 
 
@@ -108,10 +113,19 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_debug_set_wait_limit_ns.restype = None
     lib.msa_debug_force_single_cta.argtypes = [i32]
     lib.msa_debug_force_single_cta.restype = None
+    lib.msa_debug_bounds_build.argtypes = []
+    lib.msa_debug_bounds_build.restype = i32
     return lib
 
 
 _lib = load_library()
+if DEBUG_BOUNDS and _lib.msa_debug_bounds_build() != 1:
+    raise ImportError(f"{LIB_PATH} is not the bounds-checked build")
+
+
+def debug_bounds_build() -> bool:
+    """True when the loaded library is the bounds-checked build."""
+    return bool(_lib.msa_debug_bounds_build())
 
 
 def _check(status: int) -> None:

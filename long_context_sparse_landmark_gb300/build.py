@@ -3,6 +3,12 @@
 Each CUDA translation unit is compiled in parallel into ``_build/`` and the
 objects are linked into ``libmsa.so`` next to this file (CUDA runtime linked
 statically, so the library loads on hosts without a GPU driver too).
+
+``build(debug_bounds=True)`` builds the bounds-checked variant instead
+(``-DMSA_DEBUG_BOUNDS``, objects in ``_build/debug_bounds/``, library
+``libmsa_debug.so``): every kernel range-checks its global offsets and TMA
+box origins and records a violation in the device status word.  It is slower
+and is only loaded when MSA_DEBUG_BOUNDS=1 is set in the environment.
 """
 from __future__ import annotations
 
@@ -18,6 +24,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmsa.so")
+LIB_DEBUG = os.path.join(PKG, "libmsa_debug.so")
 
 SOURCES = ["msa_api.cu", "k1_landmark_pool.cu", "k2_attn_simt.cu", "k2_attn_tc.cu",
            "k2_attn_tc2.cu", "k3_lse_merge.cu", "k4_block_select.cu", "k5_global_rows.cu",
@@ -40,17 +47,23 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile and link libmsa.so; returns its path.  Skips work when the
-    library is newer than every source and header."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          debug_bounds: bool = False) -> str:
+    """Compile and link libmsa.so (or, with debug_bounds, libmsa_debug.so);
+    returns its path.  Skips work when the library is newer than every
+    source and header."""
+    lib = LIB_DEBUG if debug_bounds else LIB
+    out_dir = os.path.join(BUILD, "debug_bounds") if debug_bounds else BUILD
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime():
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if debug_bounds:
+        extra.append("-DMSA_DEBUG_BOUNDS")
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -61,14 +74,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                debug_bounds="--debug-bounds" in sys.argv))

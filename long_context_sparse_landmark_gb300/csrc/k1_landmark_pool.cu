@@ -43,7 +43,7 @@ template <bool kBf16>
 __global__ void __launch_bounds__(kPoolWarps * 32)
     landmark_pool_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
                          uint8_t* __restrict__ k_lm, uint8_t* __restrict__ v_lm, int64_t B,
-                         int C, int strips) {
+                         int C, int strips, int64_t n, int* status) {
   constexpr int VN = Vec<kBf16>::N;
   constexpr int ES = kBf16 ? 2 : 4;
   __shared__ float red[kPoolWarps][32][VN + 1];
@@ -70,8 +70,10 @@ __global__ void __launch_bounds__(kPoolWarps * 32)
 #pragma unroll
       for (int u = 0; u < kPoolUnroll; ++u) {
         const int64_t r = r0 + static_cast<int64_t>(u) * kPoolWarps;
-        buf[u] = r < B ? __ldg(reinterpret_cast<const uint4*>(base + r * row_bytes))
-                       : make_uint4(0, 0, 0, 0);
+        buf[u] = r < B && MSA_IN_RANGE((l * B + r) * row_bytes + static_cast<int64_t>(col) * ES,
+                                       16, n * row_bytes, status)
+                     ? __ldg(reinterpret_cast<const uint4*>(base + r * row_bytes))
+                     : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < kPoolUnroll; ++u) accumulate<kBf16>(acc, buf[u]);
@@ -90,6 +92,9 @@ __global__ void __launch_bounds__(kPoolWarps * 32)
     }
     const float fb = static_cast<float>(B);
     uint8_t* out = dst + (l * C + col) * ES;
+    if (!MSA_IN_RANGE((l * C + col) * ES, 16,
+                      static_cast<int64_t>(gridDim.x / strips) * C * ES, status))
+      return;
     if constexpr (kBf16) {
       uint32_t w[4];
 #pragma unroll
@@ -118,11 +123,13 @@ cudaError_t launch_landmark_pool(const PoolArgs& a, cudaStream_t s) {
   if (a.bf16) {
     landmark_pool_kernel<true><<<grid, block, 0, s>>>(
         static_cast<const uint8_t*>(a.k), static_cast<const uint8_t*>(a.v),
-        static_cast<uint8_t*>(a.k_lm), static_cast<uint8_t*>(a.v_lm), B, a.C, strips);
+        static_cast<uint8_t*>(a.k_lm), static_cast<uint8_t*>(a.v_lm), B, a.C, strips, a.n,
+        a.status);
   } else {
     landmark_pool_kernel<false><<<grid, block, 0, s>>>(
         static_cast<const uint8_t*>(a.k), static_cast<const uint8_t*>(a.v),
-        static_cast<uint8_t*>(a.k_lm), static_cast<uint8_t*>(a.v_lm), B, a.C, strips);
+        static_cast<uint8_t*>(a.k_lm), static_cast<uint8_t*>(a.v_lm), B, a.C, strips, a.n,
+        a.status);
   }
   return cudaPeekAtLastError();
 }

@@ -53,12 +53,20 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnArgs a) {
   const int64_t i = a.q_start + i_loc;  // global position
   const int64_t kv_end = a.kv_start + a.n_kv;
 
+  // Extents (elements) of the buffers, as the entry points define them.
+  const int64_t q_ext = a.n_q * a.Hq * static_cast<int64_t>(D);
+  const int64_t kv_ext = a.n_kv * a.Hkv * static_cast<int64_t>(D);
+  const int64_t lm_ext = static_cast<int64_t>(a.G) * a.Hkv * D;
+  const int64_t n_qb_all = (a.n_q + kSelQBlock - 1) / kSelQBlock;
+  (void)q_ext, (void)kv_ext, (void)lm_ext, (void)n_qb_all;
+
   // Stage the query tile.
   for (int x = tid; x < kBQ * D; x += kThreads) {
     const int rr = x / D, e = x % D;
     const int64_t row = qr0 + rr;
+    const int64_t off = (row * a.Hq + h) * static_cast<int64_t>(D) + e;
     Qs[rr * (D + 1) + e] =
-        row < a.n_q ? ld_in<kBf16In>(a.q, (row * a.Hq + h) * static_cast<int64_t>(D) + e) : 0.f;
+        row < a.n_q && MSA_IN_RANGE(off, 1, q_ext, a.status) ? ld_in<kBf16In>(a.q, off) : 0.f;
   }
 
   // Key ranges of the whole tile (global positions).
@@ -81,7 +89,9 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnArgs a) {
   const int32_t* sel_list =
       a.sel ? a.sel + (qb * a.Hkv + c) * static_cast<int64_t>(a.top_k) : nullptr;
   const int64_t n_lm =
-      a.sel ? sel_count_checked(a.sel_cnt[qb * a.Hkv + c], a.top_k, n_cand, a.status) * a.block
+      a.sel ? (MSA_IN_RANGE(qb * a.Hkv + c, 1, n_qb_all * a.Hkv, a.status)
+                   ? sel_count_checked(a.sel_cnt[qb * a.Hkv + c], a.top_k, n_cand, a.status)
+                   : 0) * a.block
             : visible_landmarks(g_last, a.window, a.block, a.G);
   const int64_t lm_tiles = (n_lm + kBK - 1) / kBK;
   const int64_t win_tiles = (n_win + kBK - 1) / kBK;
@@ -113,20 +123,29 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnArgs a) {
       float kv = 0.f, vv = 0.f;
       if (key < limit) {
         if (is_lm && sel_list) {
+          const int64_t si = (qb * a.Hkv + c) * static_cast<int64_t>(a.top_k) + key / a.block;
           const int64_t tok =
-              sel_block_checked(sel_list[key / a.block], n_cand, a.status) * a.block +
-              key % a.block;
+              MSA_IN_RANGE(si, 1, n_qb_all * a.Hkv * a.top_k, a.status)
+                  ? sel_block_checked(sel_list[key / a.block], n_cand, a.status) * a.block +
+                        key % a.block
+                  : 0;
           const int64_t off = (tok * a.Hkv + c) * static_cast<int64_t>(D) + e;
-          kv = ld_in<kBf16In>(a.k, off);
-          vv = ld_in<kBf16In>(a.v, off);
+          if (MSA_IN_RANGE(off, 1, kv_ext, a.status)) {
+            kv = ld_in<kBf16In>(a.k, off);
+            vv = ld_in<kBf16In>(a.v, off);
+          }
         } else if (is_lm) {
           const int64_t off = (key * a.Hkv + c) * static_cast<int64_t>(D) + e;
-          kv = ld_in<kBf16In>(a.k_lm, off);
-          vv = ld_in<kBf16In>(a.v_lm, off);
+          if (MSA_IN_RANGE(off, 1, lm_ext, a.status)) {
+            kv = ld_in<kBf16In>(a.k_lm, off);
+            vv = ld_in<kBf16In>(a.v_lm, off);
+          }
         } else {
           const int64_t off = ((key - a.kv_start) * a.Hkv + c) * static_cast<int64_t>(D) + e;
-          kv = ld_in<kBf16In>(a.k, off);
-          vv = ld_in<kBf16In>(a.v, off);
+          if (MSA_IN_RANGE(off, 1, kv_ext, a.status)) {
+            kv = ld_in<kBf16In>(a.k, off);
+            vv = ld_in<kBf16In>(a.v, off);
+          }
         }
       }
       Ks[kk * (D + 1) + e] = kv;
@@ -184,6 +203,8 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnArgs a) {
 
   if (!row_ok) return;
   const int64_t lse_idx = static_cast<int64_t>(h) * a.lse_ld + i_loc;
+  if (!MSA_IN_RANGE(lse_idx, 1, (a.Hq - 1) * a.lse_ld + a.n_q, a.status)) return;
+  if (!MSA_IN_RANGE((i_loc * a.Hq + h) * static_cast<int64_t>(D), D, q_ext, a.status)) return;
   if (l == 0.f) {  // no key for this row (only possible for a partial)
     if (a.merge) return;  // a running merge leaves the row untouched
     if (qd == 0) a.lse[lse_idx] = -INFINITY;

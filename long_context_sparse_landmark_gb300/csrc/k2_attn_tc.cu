@@ -147,9 +147,12 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
     n_win = static_cast<int>((j_hi - p.kv_start) / kBN) - w.kt_lo + 1;
   }
   if (p.select) {  // the unit's selected key blocks, each block/128 full tiles
+    const int64_t ci = static_cast<int64_t>(qt) * p.Hkv + w.kvh;
     const int64_t cnt =
-        sel_count_checked(p.sel_cnt[static_cast<int64_t>(qt) * p.Hkv + w.kvh], p.top_k,
-                          visible_landmarks(g0, p.window, p.block, p.G), p.status);
+        MSA_IN_RANGE(ci, 1, static_cast<int64_t>(p.n_qtiles) * p.Hkv, p.status)
+            ? sel_count_checked(p.sel_cnt[ci], p.top_k,
+                                visible_landmarks(g0, p.window, p.block, p.G), p.status)
+            : 0;
     w.n_lm_tiles = static_cast<int>(cnt * (p.block / kBN));
   } else {
     const int64_t n_lm = visible_landmarks(g_last, p.window, p.block, p.G);
@@ -227,17 +230,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const CUtensorMap* m;
         if (lm && p.select) {  // tile of a selected block, from K/V themselves
           const int tpb = static_cast<int>(p.block / kBN);
-          const int64_t blk = sel_block_checked(
-              p.sel[(w.qr0 / kBM * p.Hkv + w.kvh) * p.top_k + t / tpb],
-              visible_landmarks(w.qr0, p.window, p.block, p.G), p.status);
+          const int64_t si = (w.qr0 / kBM * p.Hkv + w.kvh) * p.top_k + t / tpb;
+          const int64_t blk =
+              MSA_IN_RANGE(si, 1, static_cast<int64_t>(p.n_qtiles) * p.Hkv * p.top_k, p.status)
+                  ? sel_block_checked(p.sel[si], visible_landmarks(w.qr0, p.window, p.block, p.G),
+                                      p.status)
+                  : 0;
           row = static_cast<int>(blk * p.block) + (t % tpb) * kBN;
           m = is_k ? &p.tm_k : &p.tm_v;
         } else {
           m = is_k ? (lm ? &p.tm_klm : &p.tm_k) : (lm ? &p.tm_vlm : &p.tm_v);
           row = lm ? t * kBN : (w.kt_lo + t - w.n_lm_tiles) * kBN;
         }
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 2; ++c) {
+          // Box origins are only recorded when out of range: the copy is
+          // issued all the same (out-of-range rows read the fill value).
+          (void)MSA_TMA_OK(c * 64, w.kvh, row, kD, p.Hkv, lm && !p.select ? p.G : p.n_kv, kBN,
+                           p.status);
           ptx::tma_load_3d(dst + c * kChunkBytes, m, mbar, c * 64, w.kvh, row);
+        }
       };
       for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
         const Unit w = decode_unit(p, u);
@@ -256,9 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (qn > 0 && !(ok = wait_bar(bar(BAR_QE), (qn - 1) & 1, ctl))) break;
         ptx::mbar_arrive_expect_tx(bar(BAR_Q), w.n_slots * kTileBytes);
         for (int s = 0; s < w.n_slots; ++s)
-          for (int c = 0; c < 2; ++c)
+          for (int c = 0; c < 2; ++c) {
+            (void)MSA_TMA_OK(c * 64, w.h0 + s, w.qr0, kD, p.Hq, p.n_q, kBM, p.status);
             ptx::tma_load_3d(sb + kOffQ + s * kTileBytes + c * kChunkBytes, &p.tm_q, bar(BAR_Q),
                              c * 64, w.h0 + s, static_cast<int>(w.qr0));
+          }
         ++qn;
         // Warm L2 with this CTA's next Q tiles: they are read once, from
         // HBM, exactly when the tensor pipe waits for them.
@@ -401,7 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const int64_t i = p.q_start + i_loc;
       const int h = w.h0 + slot;
       if (w.T == 0) {  // no key for any row of this unit (partial chunks only)
-        if (row_ok && !p.merge) p.lse[static_cast<int64_t>(h) * p.lse_ld + i_loc] = -INFINITY;
+        const int64_t lse_idx = static_cast<int64_t>(h) * p.lse_ld + i_loc;
+        if (row_ok && !p.merge && MSA_IN_RANGE(lse_idx, 1, (p.Hq - 1) * p.lse_ld + p.n_q, p.status))
+          p.lse[lse_idx] = -INFINITY;
         continue;
       }
       int64_t my_lo, my_hi;
@@ -512,13 +527,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       // before the next unit's first PV overwrites O.
       const bool has = row_ok && l > 0.f;
       const int64_t lse_idx = static_cast<int64_t>(h) * p.lse_ld + i_loc;
+      const int64_t obase = (i_loc * p.Hq + h) * static_cast<int64_t>(kD);
+      // Offsets of this row against the extents of O [n_q, Hq, d] and lse
+      // [Hq][lse_ld] (checked in the bounds-checked build only).
+      const bool io_ok =
+          !row_ok ||
+          (MSA_IN_RANGE(lse_idx, 1, (p.Hq - 1) * p.lse_ld + p.n_q, p.status) &&
+           MSA_IN_RANGE(obase, kD, p.n_q * p.Hq * static_cast<int64_t>(kD), p.status));
       // O = acc * w_new (+ running O * w_run when merging into a running
       // result: lse_run <- ln(e^lse_run + e^lse_p)).
       const float lse_p = has ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
       float w_new = has ? 1.f / l : 0.f;
       float w_run = 0.f;
       float lse_out = lse_p;
-      if (p.merge && has) {
+      if (p.merge && has && io_ok) {
         const float L = p.lse[lse_idx];
         if (L != -INFINITY) {
           const float mx = fmaxf(L, lse_p);
@@ -527,13 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           w_new *= expf(lse_p - lse_out);
         }
       }
-      const int64_t obase = (i_loc * p.Hq + h) * static_cast<int64_t>(kD);
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         float o[32];
         ptx::tmem_ld32(tO + cc * 32, o);
         ptx::tmem_wait_ld();
-        if (has) {
+        if (has && io_ok) {
           if (p.out_bf16) {
             uint4* dst =
                 reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + obase + cc * 32);
@@ -567,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         }
       }
       // Rows without a key: -inf (a partial), or untouched (a running merge).
-      if (row_ok && (has || !p.merge)) p.lse[lse_idx] = lse_out;
+      if (row_ok && io_ok && (has || !p.merge)) p.lse[lse_idx] = lse_out;
       sc += w.T;
       oc += 1;
     }

@@ -160,9 +160,12 @@ __device__ __forceinline__ Unit decode_unit(const Tc2Params& p, int u) {
     n_win = static_cast<int>((j_hi - p.kv_start) / kBN) - w.kt_lo + 1;
   }
   if (p.select) {  // the unit's selected key blocks, each block/128 full tiles
+    const int64_t ci = static_cast<int64_t>(qt) * p.Hkv + w.kvh;
     const int64_t cnt =
-        sel_count_checked(p.sel_cnt[static_cast<int64_t>(qt) * p.Hkv + w.kvh], p.top_k,
-                          visible_landmarks(g0, p.window, p.block, p.G), p.status);
+        MSA_IN_RANGE(ci, 1, static_cast<int64_t>(p.n_qtiles) * p.Hkv, p.status)
+            ? sel_count_checked(p.sel_cnt[ci], p.top_k,
+                                visible_landmarks(g0, p.window, p.block, p.G), p.status)
+            : 0;
     w.n_lm_tiles = static_cast<int>(cnt * (p.block / kBN));
   } else {
     const int64_t n_lm = visible_landmarks(g_last, p.window, p.block, p.G);
@@ -304,10 +307,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
         if (rank == 0) ptx::mbar_arrive_expect_tx(bar(BAR_QF), w.n_heads * kQBytes);
         for (int s = 0; s < w.n_slots; ++s)
           if (2 * s + static_cast<int>(rank) < w.n_heads)
-            for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < 2; ++c) {
+              // Box origins are only recorded when out of range: the copy is
+              // issued all the same (out-of-range rows read the fill value).
+              (void)MSA_TMA_OK(c * 64, w.h0 + 2 * s + static_cast<int>(rank), w.qr0, kD, p.Hq,
+                               p.n_q, kBM, p.status);
               pair::tma_load_3d(sb + kOffQ + s * kQBytes + c * kQChunk, &p.tm_q, lead(BAR_QF),
                                 c * 64, w.h0 + 2 * s + static_cast<int>(rank),
                                 static_cast<int>(w.qr0));
+            }
         // Warm L2 with this CTA's next Q tiles: they are read once, from HBM.
         for (int un = u + n_clusters; un < p.units; un += n_clusters) {
           const Unit nw = decode_unit(p, un);
@@ -331,9 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
           const CUtensorMap* mv;
           if (lm && p.select) {  // a selected block's tile, from K/V themselves
             const int tpb = static_cast<int>(p.block / kBN);
-            const int64_t blk = sel_block_checked(
-                p.sel[(w.qr0 / kBM * p.Hkv + w.kvh) * p.top_k + t / tpb],
-                visible_landmarks(w.qr0, p.window, p.block, p.G), p.status);
+            const int64_t si = (w.qr0 / kBM * p.Hkv + w.kvh) * p.top_k + t / tpb;
+            const int64_t blk =
+                MSA_IN_RANGE(si, 1, static_cast<int64_t>(p.n_qtiles) * p.Hkv * p.top_k, p.status)
+                    ? sel_block_checked(p.sel[si],
+                                        visible_landmarks(w.qr0, p.window, p.block, p.G),
+                                        p.status)
+                    : 0;
             row = static_cast<int>(blk * p.block) + (t % tpb) * kBN;
             mk = &p.tm_k;
             mv = &p.tm_v;
@@ -344,9 +356,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
           }
           const uint32_t kdst = sb + kOffKV + s * kStageBytes;
           const uint32_t full = lead(BAR_KVF(s));
-          for (int c = 0; c < 2; ++c)
+          const int64_t rows_ext = lm && !p.select ? p.G : p.n_kv;
+          (void)rows_ext;
+          for (int c = 0; c < 2; ++c) {
+            // The tile (not this CTA's half, which may lie wholly past the
+            // end of a ragged last tile) must overlap the rows.
+            (void)MSA_TMA_OK(c * 64, w.kvh, row, kD, p.Hkv, rows_ext, kBN, p.status);
             pair::tma_load_3d(kdst + c * kKChunk, mk, full, c * 64, w.kvh,
                               row + 64 * static_cast<int>(rank));
+          }
+          (void)MSA_TMA_OK(64 * static_cast<int>(rank), w.kvh, row, kD, p.Hkv, rows_ext, kBN,
+                           p.status);
           pair::tma_load_3d(kdst + kKBytes, mv, full, 64 * static_cast<int>(rank), w.kvh, row);
         }
         ++ul;
@@ -453,7 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
       const bool row_ok = i_loc < p.n_q;
       const int64_t i = p.q_start + i_loc;
       if (w.T == 0) {  // no key for any row of this unit (partial chunks only)
-        if (has && row_ok && !p.merge) p.lse[static_cast<int64_t>(h) * p.lse_ld + i_loc] = -INFINITY;
+        const int64_t lse_idx = static_cast<int64_t>(h) * p.lse_ld + i_loc;
+        if (has && row_ok && !p.merge &&
+            MSA_IN_RANGE(lse_idx, 1, (p.Hq - 1) * p.lse_ld + p.n_q, p.status))
+          p.lse[lse_idx] = -INFINITY;
         continue;
       }
       int64_t my_lo, my_hi;
@@ -567,13 +590,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
       // next unit's first PV overwrites O.
       const bool hv = has && row_ok && l > 0.f;
       const int64_t lse_idx = static_cast<int64_t>(h) * p.lse_ld + i_loc;
+      const int64_t obase = (i_loc * p.Hq + h) * static_cast<int64_t>(kD);
+      // Offsets of a row this CTA writes, against the extents of O [n_q, Hq,
+      // d] and lse [Hq][lse_ld] (checked in the bounds-checked build only).
+      const bool io_ok =
+          !(has && row_ok) ||
+          (MSA_IN_RANGE(lse_idx, 1, (p.Hq - 1) * p.lse_ld + p.n_q, p.status) &&
+           MSA_IN_RANGE(obase, kD, p.n_q * p.Hq * static_cast<int64_t>(kD), p.status));
       // O = acc * w_new (+ running O * w_run when merging into a running
       // result: lse_run <- ln(e^lse_run + e^lse_p)).
       const float lse_p = hv ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
       float w_new = hv ? 1.f / l : 0.f;
       float w_run = 0.f;
       float lse_out = lse_p;
-      if (p.merge && hv) {
+      if (p.merge && hv && io_ok) {
         const float L = p.lse[lse_idx];
         if (L != -INFINITY) {
           const float mx = fmaxf(L, lse_p);
@@ -582,13 +612,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
           w_new *= expf(lse_p - lse_out);
         }
       }
-      const int64_t obase = (i_loc * p.Hq + h) * static_cast<int64_t>(kD);
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         float o[32];
         ptx::tmem_ld32(tO + cc * 32, o);
         ptx::tmem_wait_ld();
-        if (hv) {
+        if (hv && io_ok) {
           if (p.out_bf16) {
             uint4* dst =
                 reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + obase + cc * 32);
@@ -622,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
         }
       }
       // Rows without a key: -inf (a partial), or untouched (a running merge).
-      if (has && row_ok && (hv || !p.merge)) p.lse[lse_idx] = lse_out;
+      if (has && row_ok && io_ok && (hv || !p.merge)) p.lse[lse_idx] = lse_out;
       sc += w.T;
       oc += 1;
     }
@@ -725,10 +754,13 @@ cudaError_t launch_attn_tc2(const AttnArgs& a, cudaStream_t s, const char** why)
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // Function attributes belong to the context: set on every launch (a
+  // cudaDeviceReset in between would drop them); only the occupancy figure,
+  // a property of the device, is cached.
+  e = cudaFuncSetAttribute(attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes);
+  if (e != cudaSuccess) return e;
   if (max_clusters == 0) {
-    e = cudaFuncSetAttribute(attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
-    if (e != cudaSuccess) return e;
     // The register split (setmaxnreg) assumes the launch allocation of
     // 168 registers per thread; refuse to launch a build that differs.
     cudaFuncAttributes fa;

@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(kMergeThreads)
     const int r = x % R;
     if (r >= rows) continue;
     const int64_t li = static_cast<int64_t>(h) * a.n + r0 + r;
+    if (!MSA_IN_RANGE(li, 1, static_cast<int64_t>(Hq) * a.n, a.status)) continue;
     float mx = -INFINITY;
     for (int p = 0; p < P; ++p) mx = fmaxf(mx, a.lse_parts[p][li]);
     if (mx == -INFINITY) {
@@ -63,6 +64,8 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int d4 = a.d / 4;
   const int64_t tile_f4 = static_cast<int64_t>(rows) * Hq * d4;
   const int64_t base_f4 = r0 * Hq * d4;
+  const int64_t all_f4 = a.n * Hq * d4;  // float4s of each O_p and of O
+  (void)all_f4;
   for (int64_t f0 = threadIdx.x; f0 < tile_f4; f0 += static_cast<int64_t>(blockDim.x) * kMergeUnroll) {
     float4 acc[kMergeUnroll];
     int widx[kMergeUnroll];
@@ -83,7 +86,9 @@ __global__ void __launch_bounds__(kMergeThreads)
       for (int u = 0; u < kMergeUnroll; ++u) {
         const int64_t f = f0 + static_cast<int64_t>(u) * blockDim.x;
         w[u] = widx[u] >= 0 ? wsm[p * HR + widx[u]] : -1.f;
-        x[u] = w[u] >= 0.f ? src[f] : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[u] = w[u] >= 0.f && MSA_IN_RANGE(base_f4 + f, 1, all_f4, a.status)
+                   ? src[f]
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < kMergeUnroll; ++u) {
@@ -98,7 +103,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 #pragma unroll
     for (int u = 0; u < kMergeUnroll; ++u) {
       const int64_t f = f0 + static_cast<int64_t>(u) * blockDim.x;
-      if (f >= tile_f4) continue;
+      if (f >= tile_f4 || !MSA_IN_RANGE(base_f4 + f, 1, all_f4, a.status)) continue;
       if (a.out_bf16) {
         __nv_bfloat162 lo = __floats2bfloat162_rn(acc[u].x, acc[u].y);
         __nv_bfloat162 hi = __floats2bfloat162_rn(acc[u].z, acc[u].w);

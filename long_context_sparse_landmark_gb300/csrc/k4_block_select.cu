@@ -53,8 +53,10 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectA
     for (int64_t pr = ps; pr < npairs; pr += slots) {
       const int64_t i = r0 + pr / g;
       const int hh = static_cast<int>(pr % g);
-      const uint4 x = __ldg(reinterpret_cast<const uint4*>(
-          qb + ((i * a.Hq + c * g + hh) * static_cast<int64_t>(d) + vi * V) * ES));
+      const int64_t off = (i * a.Hq + c * g + hh) * static_cast<int64_t>(d) + vi * V;
+      const uint4 x = MSA_IN_RANGE(off, V, a.n * a.Hq * static_cast<int64_t>(d), a.status)
+                          ? __ldg(reinterpret_cast<const uint4*>(qb + off * ES))
+                          : make_uint4(0, 0, 0, 0);
       if constexpr (kBf16) {
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
@@ -92,6 +94,11 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectA
                                                       (l * a.Hkv + c) * static_cast<int64_t>(d) *
                                                           ES);
     float s = 0.f;
+    if (!MSA_IN_RANGE((l * a.Hkv + c) * static_cast<int64_t>(d), d,
+                      static_cast<int64_t>(a.G) * a.Hkv * d, a.status)) {
+      score[l] = -INFINITY;
+      continue;
+    }
 #pragma unroll 4
     for (int v0 = 0; v0 < d / V; ++v0) {
       const uint4 x = __ldg(row + v0);
@@ -138,10 +145,15 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectA
       const bool f = l < n_cand && flag[l];
       const unsigned m = __ballot_sync(0xffffffffu, f);
       const int slot = base + __popc(m & ((1u << lane) - 1u));
-      if (f && slot < a.top_k) out[slot] = static_cast<int32_t>(l);
+      if (f && slot < a.top_k &&
+          MSA_IN_RANGE((static_cast<int64_t>(t) * a.Hkv + c) * a.top_k + slot, 1,
+                       static_cast<int64_t>(gridDim.x) * a.Hkv * a.top_k, a.status))
+        out[slot] = static_cast<int32_t>(l);
       base += __popc(m);
     }
-    if (lane == 0) a.cnt[static_cast<int64_t>(t) * a.Hkv + c] = min(base, a.top_k);
+    if (lane == 0 && MSA_IN_RANGE(static_cast<int64_t>(t) * a.Hkv + c, 1,
+                                  static_cast<int64_t>(gridDim.x) * a.Hkv, a.status))
+      a.cnt[static_cast<int64_t>(t) * a.Hkv + c] = min(base, a.top_k);
   }
 }
 

@@ -77,6 +77,7 @@ struct GrParams {
 __device__ __forceinline__ int64_t row_position(const int64_t* rows, int64_t m, int64_t Mc,
                                                 int group, int64_t n, int* status) {
   if (m >= Mc) return -1;
+  if (!MSA_IN_RANGE(m / group, 1, Mc / group, status)) return -1;
   const int64_t pos = rows[m / group];
   if (pos < 0 || pos >= n) {
     record_status(status, MSA_ERR_INVALID_ARG);
@@ -109,8 +110,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t pos = row_position(p.rows, m0 + t, p.Mc, p.group, p.n, p.status);
     spos[t] = pos;
     uint4 g16[16];
-    if (pos >= 0) {
-      const int h = c * p.group + static_cast<int>((m0 + t) % p.group);
+    const int h = c * p.group + static_cast<int>((m0 + t) % p.group);
+    if (pos >= 0 && MSA_IN_RANGE((pos * p.Hq + h) * static_cast<int64_t>(kD), kD,
+                                 p.n * p.Hq * static_cast<int64_t>(kD), p.status)) {
       const uint4* src =
           reinterpret_cast<const uint4*>(p.q + (pos * p.Hq + h) * static_cast<int64_t>(kD));
 #pragma unroll
@@ -148,7 +150,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t key_end = min64(key_lo + p.span, max_pos + 1);
   const int T = key_end > key_lo ? static_cast<int>((key_end - key_lo + kBN - 1) / kBN) : 0;
   if (T == 0) {  // no row of the tile reaches this split
-    if (threadIdx.x < kBM && m0 + threadIdx.x < p.Mc)
+    if (threadIdx.x < kBM && m0 + threadIdx.x < p.Mc &&
+        MSA_IN_RANGE(part * p.Mc + m0 + threadIdx.x, 1,
+                     static_cast<int64_t>(gridDim.x) * p.Hkv * p.Mc, p.status))
       p.lse_part[part * p.Mc + m0 + threadIdx.x] = -INFINITY;
     return;
   }
@@ -176,6 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive_expect_tx(full, 2 * kTileBytes);
         const int row = static_cast<int>(key_lo + static_cast<int64_t>(t) * kBN);
         for (int ch = 0; ch < 2; ++ch) {
+          // Box origins are only recorded when out of range: the copy is
+          // issued all the same (out-of-range rows read the fill value).
+          (void)MSA_TMA_OK(ch * 64, c, row, kD, p.Hkv, p.n, kBN, p.status);
           ptx::tma_load_3d(sb + kOffK + b * kTileBytes + ch * kChunkBytes, &p.tm_k, full, ch * 64,
                            c, row);
           ptx::tma_load_3d(sb + kOffV + b * kTileBytes + ch * kChunkBytes, &p.tm_v, full, ch * 64,
@@ -312,7 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_OF), 0, ctl));
     if (ok) {
       ptx::tc_fence_after();
-      const bool has = pos >= 0 && l > 0.f;
+      const int64_t all_m = static_cast<int64_t>(gridDim.x) * p.Hkv * p.Mc;
+      (void)all_m;
+      const bool has = pos >= 0 && l > 0.f &&
+                       MSA_IN_RANGE((part * p.Mc + m) * static_cast<int64_t>(kD), kD,
+                                    all_m * kD, p.status);
       const float w = has ? 1.f / l : 0.f;
       float* dst = p.o_part + (part * p.Mc + m) * static_cast<int64_t>(kD);
 #pragma unroll 1
@@ -328,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 o[4 * v + 3] * w);
         }
       }
-      if (m < p.Mc)
+      if (m < p.Mc && MSA_IN_RANGE(part * p.Mc + m, 1, all_m, p.status))
         p.lse_part[part * p.Mc + m] =
             has ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
     }
@@ -368,14 +379,20 @@ __global__ void __launch_bounds__(128)
   };
   float qv[E], o[E];
   const int h = c * group + static_cast<int>(m % group);
+  const bool q_ok = pos >= 0 && MSA_IN_RANGE((pos * Hq + h) * static_cast<int64_t>(D), D,
+                                             n * Hq * static_cast<int64_t>(D), status);
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    qv[e] = pos >= 0 ? ld(q, (pos * Hq + h) * static_cast<int64_t>(D) + lane * E + e) : 0.f;
+    qv[e] = q_ok ? ld(q, (pos * Hq + h) * static_cast<int64_t>(D) + lane * E + e) : 0.f;
     o[e] = 0.f;
   }
   float mrun = -INFINITY, l = 0.f;
   for (int64_t j = key_lo; j < key_end; ++j) {
     const int64_t base = (j * Hkv + c) * static_cast<int64_t>(D) + lane * E;
+    // The whole key row, so that every lane takes the same branch.
+    if (!MSA_IN_RANGE((j * Hkv + c) * static_cast<int64_t>(D), D,
+                      n * Hkv * static_cast<int64_t>(D), status))
+      break;
     float dot = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) dot = fmaf(qv[e], ld(k, base + e), dot);
@@ -390,6 +407,9 @@ __global__ void __launch_bounds__(128)
     for (int e = 0; e < E; ++e) o[e] = fmaf(pj, ld(v, base + e), o[e] * alpha);
     mrun = m_new;
   }
+  const int64_t all_m = static_cast<int64_t>(gridDim.x) * Hkv * Mc;
+  (void)all_m;
+  if (!MSA_IN_RANGE(part * Mc + m, 1, all_m, status)) return;
   const bool has = l > 0.f;
   if (has) {
     const float w = 1.f / l;
@@ -408,7 +428,8 @@ template <int D>
 __global__ void __launch_bounds__(128)
     global_rows_merge_kernel(const int64_t* rows, const float* o_part, const float* lse_part,
                              void* out, float* lse, int64_t n, int64_t n_global, int64_t Mc,
-                             int n_splits, int Hq, int Hkv, int group, int out_bf16) {
+                             int n_splits, int Hq, int Hkv, int group, int out_bf16,
+                             int* status) {
   constexpr int E = D / 32;
   const int64_t pair = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -419,6 +440,13 @@ __global__ void __launch_bounds__(128)
   const int64_t m = r * group + h % group;
   const int64_t pos = rows[r];
   if (pos < 0 || pos >= n) return;
+  // Every partial index below is (s * Hkv + c) * Mc + m with s < n_splits.
+  if (!MSA_IN_RANGE((static_cast<int64_t>(n_splits - 1) * Hkv + c) * Mc + m, 1,
+                    static_cast<int64_t>(n_splits) * Hkv * Mc, status) ||
+      !MSA_IN_RANGE((pos * Hq + h) * static_cast<int64_t>(D), D, n * Hq * static_cast<int64_t>(D),
+                    status) ||
+      !MSA_IN_RANGE(static_cast<int64_t>(h) * n + pos, 1, static_cast<int64_t>(Hq) * n, status))
+    return;
   float mx = -INFINITY;
   for (int s = lane; s < n_splits; s += 32)
     mx = fmaxf(mx, lse_part[(static_cast<int64_t>(s) * Hkv + c) * Mc + m]);
@@ -513,11 +541,11 @@ cudaError_t launch_global_rows(const GlobalRowsArgs& a, cudaStream_t s, const ch
   if (a.d == 64)
     global_rows_merge_kernel<64><<<mblocks, 128, 0, s>>>(a.rows, a.o_part, a.lse_part, a.out,
                                                          a.lse, a.n, a.n_global, Mc, a.n_splits,
-                                                         a.Hq, a.Hkv, group, a.out_bf16);
+                                                         a.Hq, a.Hkv, group, a.out_bf16, a.status);
   else
     global_rows_merge_kernel<128><<<mblocks, 128, 0, s>>>(a.rows, a.o_part, a.lse_part, a.out,
                                                           a.lse, a.n, a.n_global, Mc, a.n_splits,
-                                                          a.Hq, a.Hkv, group, a.out_bf16);
+                                                          a.Hq, a.Hkv, group, a.out_bf16, a.status);
   return cudaPeekAtLastError();
 }
 

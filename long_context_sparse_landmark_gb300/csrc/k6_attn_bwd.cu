@@ -193,13 +193,61 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem, int warp) {
 // &y_b, &row)` names the tensors (64-row boxes) and coordinates of tile it,
 // `stats(it, &l2, &d, &pos)` the tile's statistics rows (positions only in
 // the gathered mode).  Half u = 2 it + h goes to ring stage u % kRing.
-template <typename Coord, typename Stats>
+// Bounds-checked build: a TMA box origin against the tensor its map covers
+// -- K / V [n][Hkv], the landmarks [G][Hkv], Q / dO [n][Hq], or in the
+// gathered mode the global rows [Mp][Hkv].  Recorded only; the copy is issued
+// all the same (out-of-range rows read the fill value).  Empty otherwise.
+template <bool kG>
+__device__ __forceinline__ void check_box(const BwdParams& p, const CUtensorMap* m, int x, int y,
+                                          int64_t z, int box) {
+#ifdef MSA_DEBUG_BOUNDS
+  int64_t rows;
+  int heads;
+  if (m == &p.tm_k || m == &p.tm_v) {
+    rows = p.n;
+    heads = p.Hkv;
+  } else if (m == &p.tm_klm || m == &p.tm_vlm) {
+    rows = p.G > 0 ? p.G : p.n;
+    heads = p.Hkv;
+  } else {
+    rows = kG ? p.Mp : p.n;
+    heads = kG ? p.Hkv : p.Hq;
+  }
+  (void)MSA_TMA_OK(x, y, z, kD, heads, rows, box, p.status);
+#else
+  (void)p, (void)m, (void)x, (void)y, (void)z, (void)box;
+#endif
+}
+
+// Bounds-checked build: `count` 4-byte values at `src` lie in the row
+// statistics (L2 / D: [Hq][n_pad], or [Hkv][Mp] gathered; positions [Mp]).
+template <bool kG>
+__device__ __forceinline__ bool stats_ok(const BwdParams& p, const void* src, int count) {
+#ifdef MSA_DEBUG_BOUNDS
+  const int64_t ext = kG ? static_cast<int64_t>(p.Hkv) * p.Mp : static_cast<int64_t>(p.Hq) * p.n_pad;
+  const char* c = static_cast<const char*>(src);
+  const char* bases[3] = {reinterpret_cast<const char*>(p.L2), reinterpret_cast<const char*>(p.D),
+                          reinterpret_cast<const char*>(p.gpos)};
+  const int64_t exts[3] = {ext, ext, kG ? p.Mp : 0};
+  for (int k = 0; k < 3; ++k)
+    if (bases[k] && c >= bases[k] && c < bases[k] + 4 * exts[k])
+      return MSA_IN_RANGE((c - bases[k]) / 4, count, exts[k], p.status);
+  return MSA_IN_RANGE(-1, count, 0, p.status);
+#else
+  (void)p, (void)src, (void)count;
+  return true;
+#endif
+}
+
+template <bool kG, typename Coord, typename Stats>
 __device__ __forceinline__ void produce(uint32_t sb, const CUtensorMap* fa, const CUtensorMap* fb,
                                         int fy, int frow, int iters, Coord coord, Stats stats,
-                                        const WaitCtl& ctl, int* status) {
+                                        const WaitCtl& ctl, int* status, const BwdParams& p) {
   auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8 * i; };
   ptx::mbar_arrive_expect_tx(bar(BAR_FIX), 2 * kTileBytes);
   for (int ch = 0; ch < 2; ++ch) {
+    check_box<kG>(p, fa, ch * 64, fy, frow, kT);
+    check_box<kG>(p, fb, ch * 64, fy, frow, kT);
     ptx::tma_load_3d(sb + kOffFixA + ch * kChunkBytes, fa, bar(BAR_FIX), ch * 64, fy, frow);
     ptx::tma_load_3d(sb + kOffFixB + ch * kChunkBytes, fb, bar(BAR_FIX), ch * 64, fy, frow);
   }
@@ -219,12 +267,21 @@ __device__ __forceinline__ void produce(uint32_t sb, const CUtensorMap* fa, cons
         full, 2 * kHalfTileBytes + (sl ? 2 * kHalfRows * 4 : 0) + (sp ? kHalfRows * 4 : 0));
     if (sl) {  // this half's per-query lse and D rows (256 bytes each)
       const uint32_t dst = sb + kOffStats + st * kStatBytes;
-      ptx::bulk_load(dst, sl + h * kHalfRows, kHalfRows * 4, full);
-      ptx::bulk_load(dst + kHalfRows * 4, sd + h * kHalfRows, kHalfRows * 4, full);
-      if (sp) ptx::bulk_load(dst + 2 * kHalfRows * 4, sp + h * kHalfRows, kHalfRows * 4, full);
+      // An untiled copy has no bounds of its own: the bounds-checked build
+      // skips one whose source leaves the statistics (the stage's wait then
+      // runs out and the launch ends with a status).
+      if (stats_ok<kG>(p, sl + h * kHalfRows, kHalfRows))
+        ptx::bulk_load(dst, sl + h * kHalfRows, kHalfRows * 4, full);
+      if (stats_ok<kG>(p, sd + h * kHalfRows, kHalfRows))
+        ptx::bulk_load(dst + kHalfRows * 4, sd + h * kHalfRows, kHalfRows * 4, full);
+      if (sp && stats_ok<kG>(p, sp + h * kHalfRows, kHalfRows))
+        ptx::bulk_load(dst + 2 * kHalfRows * 4, sp + h * kHalfRows, kHalfRows * 4, full);
     }
     const uint32_t base = sb + kOffRing + st * kRingStageBytes;
     for (int ch = 0; ch < 2; ++ch) {
+      // The whole query tile (its second half may lie wholly past the end).
+      check_box<kG>(p, ma, ch * 64, ya, row - h * kHalfRows, kT);
+      check_box<kG>(p, mb, ch * 64, yb, row - h * kHalfRows, kT);
       ptx::tma_load_3d(base + ch * kHalfChunk, ma, full, ch * 64, ya, row);
       ptx::tma_load_3d(base + kHalfTileBytes + ch * kHalfChunk, mb, full, ch * 64, yb, row);
     }
@@ -450,13 +507,16 @@ __device__ __forceinline__ uint32_t dq_setup(uint8_t* smem, uint32_t sb, int war
 
 // Producer of the dQ kernel: Q and dO once, then K(t) and V(t) of every key
 // tile into their rings; `coord(t, &map_k, &map_v, &row)` names tile t.
-template <typename Coord>
+template <bool kG, typename Coord>
 __device__ __forceinline__ void dq_produce(uint32_t sb, const CUtensorMap* fq,
                                            const CUtensorMap* fdo, int fy, int frow, int iters,
-                                           int c, Coord coord, const WaitCtl& ctl, int* status) {
+                                           int c, Coord coord, const WaitCtl& ctl, int* status,
+                                           const BwdParams& p) {
   auto bar = [&](int i) -> uint32_t { return sb + kDqOffBar + 8 * i; };
   ptx::mbar_arrive_expect_tx(bar(DQ_FIX), 2 * kTileBytes);
   for (int ch = 0; ch < 2; ++ch) {
+    check_box<kG>(p, fq, ch * 64, fy, frow, kT);
+    check_box<kG>(p, fdo, ch * 64, fy, frow, kT);
     ptx::tma_load_3d(sb + kOffFixA + ch * kChunkBytes, fq, bar(DQ_FIX), ch * 64, fy, frow);
     ptx::tma_load_3d(sb + kOffFixB + ch * kChunkBytes, fdo, bar(DQ_FIX), ch * 64, fy, frow);
   }
@@ -470,17 +530,21 @@ __device__ __forceinline__ void dq_produce(uint32_t sb, const CUtensorMap* fq,
         !wait_bar(bar(DQ_EMPTYK0 + sk), ((t / kDqKStages) - 1) & 1, ctl))
       break;
     ptx::mbar_arrive_expect_tx(bar(DQ_FULLK0 + sk), kTileBytes);
-    for (int ch = 0; ch < 2; ++ch)
+    for (int ch = 0; ch < 2; ++ch) {
+      check_box<kG>(p, mk, ch * 64, c, row, kT);
       ptx::tma_load_3d(sb + kDqOffK + sk * kTileBytes + ch * kChunkBytes, mk,
                        bar(DQ_FULLK0 + sk), ch * 64, c, row);
+    }
     nk = t + 1;
     if (t >= kDqVStages &&
         !wait_bar(bar(DQ_EMPTYV0 + sv), ((t / kDqVStages) - 1) & 1, ctl))
       break;
     ptx::mbar_arrive_expect_tx(bar(DQ_FULLV0 + sv), kTileBytes);
-    for (int ch = 0; ch < 2; ++ch)
+    for (int ch = 0; ch < 2; ++ch) {
+      check_box<kG>(p, mv, ch * 64, c, row, kT);
       ptx::tma_load_3d(sb + kDqOffV + sv * kTileBytes + ch * kChunkBytes, mv,
                        bar(DQ_FULLV0 + sv), ch * 64, c, row);
+    }
     nv = t + 1;
   }
   // Drain: every copy issued must have landed before the CTA exits.
@@ -595,7 +659,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
         *mv = lm ? &p.tm_vlm : &p.tm_v;
         *row = lm ? t * kT : (kt_lo + t - n_lm_tiles) * kT;
       };
-      dq_produce(sb, &p.tm_q, &p.tm_do, fy, static_cast<int>(qr0), T, c, coord, ctl, p.status);
+      dq_produce<kG>(sb, &p.tm_q, &p.tm_do, fy, static_cast<int>(qr0), T, c, coord, ctl,
+                     p.status, p);
     }
   } else if (warp == kMmaWarp) {
     dq_pipeline(sb, tmem, T, ctl);
@@ -607,12 +672,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int64_t i_row = qr0 + quarter * 32 + lane;  // query row, or gathered M row
     // Position of the row (its own index outside the gathered mode).
-    const int64_t i = kG ? p.gpos[i_row] : i_row;
-    const bool row_ok = kG ? i >= 0 : i < p.n;
+    const int64_t i =
+        kG ? (MSA_IN_RANGE(i_row, 1, p.Mp, p.status) ? p.gpos[i_row] : -1) : i_row;
     const int64_t st = kG ? static_cast<int64_t>(c) * p.Mp + i_row
                                : static_cast<int64_t>(h) * p.n_pad + i_row;
-    const float nL2 = p.L2[st];
-    const float nD = p.D[st];
+    const bool st_ok = MSA_IN_RANGE(
+        st, 1, kG ? static_cast<int64_t>(p.Hkv) * p.Mp : static_cast<int64_t>(p.Hq) * p.n_pad,
+        p.status);
+    const bool row_ok = (kG ? i >= 0 : i < p.n) && st_ok;
+    const float nL2 = st_ok ? p.L2[st] : -INFINITY;
+    const float nD = st_ok ? p.D[st] : 0.f;
     const uint64_t c2 = ptx::f2(p.scale_log2, p.scale_log2);
     const uint64_t nL22 = ptx::f2(nL2, nL2);
     const uint64_t nD2 = ptx::f2(nD, nD);
@@ -686,13 +755,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
       const int64_t off =
           kG ? ((static_cast<int64_t>(split) * p.Hkv + c) * p.Mp + i_row) * kD
                   : (i_row * p.Hq + h) * static_cast<int64_t>(kD);
+      const bool out_ok =
+          !row_ok ||
+          MSA_IN_RANGE(off, kD,
+                       kG ? static_cast<int64_t>(gridDim.x) * p.Hkv * p.Mp * kD
+                          : p.n * p.Hq * static_cast<int64_t>(kD),
+                       p.status);
 #pragma unroll 1
       for (int ci = 0; ci < 2; ++ci) {  // this warp's 64 of the 128 columns
         const int cc = 2 * cp + ci;
         float o[32];
         ptx::tmem_ld32(tl + kDqColQ + cc * 32, o);
         ptx::tmem_wait_ld();
-        if (row_ok) store_row(dst, off + cc * 32, o, p.scale, kG ? 0 : p.grad_bf16);
+        if (row_ok && out_ok) store_row(dst, off + cc * 32, o, p.scale, kG ? 0 : p.grad_bf16);
       }
     }
   }
@@ -735,8 +810,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (iters == 0) {  // landmark chunk beyond the last row: a zero partial
     if (p.lm_mode && threadIdx.x < kT && kb + threadIdx.x < p.G) {
       for (int which = 0; which < 2; ++which) {
-        float* dst = p.lm_part + ((((static_cast<int64_t>(chunk) * 2 + which) * p.G + kb +
-                                    threadIdx.x) * p.Hkv + c) * kD);
+        const int64_t o = (((static_cast<int64_t>(chunk) * 2 + which) * p.G + kb + threadIdx.x) *
+                               p.Hkv + c) * kD;
+        if (!MSA_IN_RANGE(o, kD, static_cast<int64_t>(gridDim.z) * 2 * p.G * p.Hkv * kD,
+                          p.status))
+          continue;
+        float* dst = p.lm_part + o;
         for (int e = 0; e < kD; ++e) dst[e] = 0.f;
       }
     }
@@ -764,8 +843,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         *sd = p.D + off;
         if (kG) *sp = p.gpos + row;
       };
-      produce(sb, p.lm_mode ? &p.tm_klm : &p.tm_k, p.lm_mode ? &p.tm_vlm : &p.tm_v, c,
-              static_cast<int>(kb), iters, coord, stats, ctl, p.status);
+      produce<kG>(sb, p.lm_mode ? &p.tm_klm : &p.tm_k, p.lm_mode ? &p.tm_vlm : &p.tm_v, c,
+                  static_cast<int>(kb), iters, coord, stats, ctl, p.status, p);
     }
   } else if (warp == kMmaWarp) {  // the whole warp issues (elect.sync inside)
     {
@@ -885,8 +964,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       ptx::tc_fence_after();
       if constexpr (kG) {  // the global rows' share of dK (scaled) and dV, fp32
-        const bool row_ok = j < p.n;
         const int64_t off = (j * p.Hkv + c) * static_cast<int64_t>(kD);
+        const bool row_ok =
+            j < p.n && MSA_IN_RANGE(off, kD, p.n * p.Hkv * static_cast<int64_t>(kD), p.status);
         const int which = cp;  // 0: dK (warps 0-3), 1: dV (warps 4-7)
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
@@ -898,10 +978,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                       which == 0 ? p.scale : 1.f, 0);
         }
       } else if (p.lm_mode) {
-        const bool row_ok = j < p.G;
         const int which = cp;  // 0: dK_lm (warps 0-3), 1: dV_lm (warps 4-7)
-        float* dst = p.lm_part + ((((static_cast<int64_t>(chunk) * 2 + which) * p.G + j) *
-                                   p.Hkv + c) * kD);
+        const int64_t o =
+            (((static_cast<int64_t>(chunk) * 2 + which) * p.G + j) * p.Hkv + c) * kD;
+        const bool row_ok =
+            j < p.G && MSA_IN_RANGE(o, kD, static_cast<int64_t>(gridDim.z) * 2 * p.G * p.Hkv * kD,
+                                    p.status);
+        float* dst = p.lm_part + o;
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
           float o[32];
@@ -910,12 +993,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (row_ok) store_row(dst, cc * 32, o, which == 0 ? p.scale : 1.f, 0);
         }
       } else {
-        const bool row_ok = j < p.n;
         const int64_t off = (j * p.Hkv + c) * static_cast<int64_t>(kD);
+        const bool row_ok =
+            j < p.n && MSA_IN_RANGE(off, kD, p.n * p.Hkv * static_cast<int64_t>(kD), p.status);
         // The token's share of its landmark's gradient.
         const float* lmk = nullptr;
         const float* lmv = nullptr;
-        if (p.G > 0 && row_ok) {
+        if (p.G > 0 && row_ok &&
+            MSA_IN_RANGE((j / p.block * p.Hkv + c) * kD, kD,
+                         static_cast<int64_t>(p.G) * p.Hkv * kD, p.status)) {
           const int64_t l = j / p.block;
           lmk = p.lm_grad + (l * p.Hkv + c) * kD;
           lmv = p.lm_grad + ((static_cast<int64_t>(p.G) + l) * p.Hkv + c) * kD;
@@ -957,14 +1043,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool kOutBf16>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const void* out, const uint16_t* dout, const float* lse, float* L2,
-                          float* D, int64_t n, int64_t n_pad, int Hq) {
+                          float* D, int64_t n, int64_t n_pad, int Hq, int* status) {
   const int64_t pair = static_cast<int64_t>(blockIdx.x) * 32 + (threadIdx.x >> 3);
   const int sub = threadIdx.x & 7;  // lane within the pair's 8
   if (pair >= n_pad * Hq) return;  // whole 8-lane groups leave together
   const int64_t i = pair / Hq;
   const int h = static_cast<int>(pair % Hq);
   float acc = 0.f;
-  if (i < n) {
+  // Rows past n read nothing; a row of O / dO [n][Hq][d] and of lse [Hq][n].
+  const bool in_ok = i >= n || (MSA_IN_RANGE(pair * kD, kD, n * Hq * static_cast<int64_t>(kD),
+                                             status) &&
+                                MSA_IN_RANGE(static_cast<int64_t>(h) * n + i, 1,
+                                             static_cast<int64_t>(Hq) * n, status));
+  if (i < n && in_ok) {
     const int64_t base = pair * kD + sub * 16;
     const uint4* g4 = reinterpret_cast<const uint4*>(dout + base);
 #pragma unroll
@@ -998,8 +1089,9 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int off = 4; off > 0; off >>= 1) acc += __shfl_xor_sync(gmask, acc, off);
   }
-  if (sub == 0) {
+  if (sub == 0 && in_ok) {
     const int64_t at = static_cast<int64_t>(h) * n_pad + i;
+    if (!MSA_IN_RANGE(at, 1, static_cast<int64_t>(Hq) * n_pad, status)) return;
     D[at] = -acc;
     L2[at] = i < n ? -lse[static_cast<int64_t>(h) * n + i] * kLog2e : -INFINITY;
   }
@@ -1007,9 +1099,13 @@ __global__ void __launch_bounds__(256)
 
 // lm_grad[e] = sum over chunks of lm_part[chunk][e] (fixed order).
 __global__ void __launch_bounds__(256)
-    lm_grad_reduce_kernel(const float* part, float* grad, int64_t per_chunk, int chunks) {
+    lm_grad_reduce_kernel(const float* part, float* grad, int64_t per_chunk, int chunks,
+                          int* status) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= per_chunk) return;
+  if (!MSA_IN_RANGE(static_cast<int64_t>(chunks - 1) * per_chunk + e, 1, chunks * per_chunk,
+                    status))
+    return;
   float s = 0.f;
   for (int ch = 0; ch < chunks; ++ch) s += part[ch * per_chunk + e];
   grad[e] = s;
@@ -1026,12 +1122,15 @@ __device__ __forceinline__ bool repeated_row(const int64_t* rows, int64_t r, int
 // The window pass gives the global rows no weight: L2 = -inf, D = 0.
 __global__ void __launch_bounds__(256)
     suppress_rows_kernel(const int64_t* rows, int64_t n_global, float* L2, float* D, int64_t n,
-                         int64_t n_pad, int Hq) {
+                         int64_t n_pad, int Hq, int* status) {
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= n_global * Hq) return;
   const int64_t pos = rows[idx / Hq];
   const int h = static_cast<int>(idx % Hq);
   if (pos < 0 || pos >= n) return;
+  if (!MSA_IN_RANGE(static_cast<int64_t>(h) * n_pad + pos, 1, static_cast<int64_t>(Hq) * n_pad,
+                    status))
+    return;
   L2[static_cast<int64_t>(h) * n_pad + pos] = -INFINITY;
   D[static_cast<int64_t>(h) * n_pad + pos] = 0.f;
 }
@@ -1064,6 +1163,10 @@ __global__ void __launch_bounds__(256)
   }
   const int h = c * group + static_cast<int>(m % group);
   const int64_t dst = (m * Hkv + c) * kD;
+  if (!MSA_IN_RANGE(dst, kD, Mp * Hkv * kD, status)) return;  // whole warps leave together
+  if (pos >= 0 && !(MSA_IN_RANGE((pos * Hq + h) * kD, kD, n * Hq * kD, status) &&
+                    MSA_IN_RANGE(static_cast<int64_t>(h) * n + pos, 1, Hq * n, status)))
+    pos = -1;
   const int half = lane >> 4;
   uint4* gdst = reinterpret_cast<uint4*>((half ? dOg : Qg) + dst) + (lane & 15);
   float acc = 0.f;
@@ -1095,7 +1198,7 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     dq_scatter_kernel(const float* dq_part, const int64_t* rows, int64_t n_global, int64_t Mp,
                       int n_splits, int64_t span, int64_t n, int Hq, int Hkv, int group, void* dq,
-                      int grad_bf16) {
+                      int grad_bf16, int* status) {
   const int64_t pair = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (pair >= n_global * Hq) return;
@@ -1105,6 +1208,10 @@ __global__ void __launch_bounds__(256)
   if (pos < 0 || pos >= n || repeated_row(rows, r, pos)) return;
   const int c = h / group;
   const int64_t m = r * group + h % group;
+  if (!MSA_IN_RANGE(((static_cast<int64_t>(n_splits - 1) * Hkv + c) * Mp + m) * kD, kD,
+                    static_cast<int64_t>(n_splits) * Hkv * Mp * kD, status) ||
+      !MSA_IN_RANGE((pos * Hq + h) * kD, kD, n * Hq * kD, status))
+    return;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int sp = 0; sp < n_splits && static_cast<int64_t>(sp) * span <= pos; ++sp) {
     const float4 x = *reinterpret_cast<const float4*>(
@@ -1192,10 +1299,12 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why) 
   float* Dw = a.stats + static_cast<int64_t>(a.Hq) * a.n_pad;
   if (a.out_bf16)
     bwd_preprocess_kernel<true><<<pre_blocks, 256, 0, s>>>(
-        a.out, static_cast<const uint16_t*>(a.dout), a.lse, L2w, Dw, a.n, a.n_pad, a.Hq);
+        a.out, static_cast<const uint16_t*>(a.dout), a.lse, L2w, Dw, a.n, a.n_pad, a.Hq,
+        a.status);
   else
     bwd_preprocess_kernel<false><<<pre_blocks, 256, 0, s>>>(
-        a.out, static_cast<const uint16_t*>(a.dout), a.lse, L2w, Dw, a.n, a.n_pad, a.Hq);
+        a.out, static_cast<const uint16_t*>(a.dout), a.lse, L2w, Dw, a.n, a.n_pad, a.Hq,
+        a.status);
   cudaError_t e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
   for (auto* k : {bwd_dkdv_tc_kernel<false>, bwd_dkdv_tc_kernel<true>}) {
@@ -1211,7 +1320,7 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why) 
   BwdParams pg;  // the gathered global-row launches
   if (a.rows) {
     suppress_rows_kernel<<<static_cast<unsigned>((a.n_global * a.Hq + 255) / 256), 256, 0, s>>>(
-        a.rows, a.n_global, L2w, Dw, a.n, a.n_pad, a.Hq);
+        a.rows, a.n_global, L2w, Dw, a.n, a.n_pad, a.Hq, a.status);
     const unsigned gblocks = static_cast<unsigned>((a.Mp * a.Hkv + 7) / 8);
     if (a.out_bf16)
       gather_rows_kernel<true><<<gblocks, 256, 0, s>>>(
@@ -1254,7 +1363,7 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why) 
     if (e != cudaSuccess) return e;
     const int64_t per_chunk = 2 * static_cast<int64_t>(a.G) * a.Hkv * kD;
     lm_grad_reduce_kernel<<<static_cast<unsigned>((per_chunk + 255) / 256), 256, 0, s>>>(
-        a.lm_part, a.lm_grad, per_chunk, a.lm_chunks);
+        a.lm_part, a.lm_grad, per_chunk, a.lm_chunks, a.status);
     e = cudaPeekAtLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1274,7 +1383,7 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why) 
   if (e != cudaSuccess) return e;
   dq_scatter_kernel<<<static_cast<unsigned>((a.n_global * a.Hq + 7) / 8), 256, 0, s>>>(
       a.dq_part, a.rows, a.n_global, a.Mp, a.n_splits, a.span, a.n, a.Hq, a.Hkv, group, a.dq,
-      a.grad_bf16);
+      a.grad_bf16, a.status);
   return cudaPeekAtLastError();
 }
 

@@ -53,6 +53,14 @@ msa_status device_status_ptr(int** out) {
   return MSA_OK;
 }
 
+// The status word for launches that only record range-check failures of
+// the bounds-checked build (null if the lookup fails: those checks then
+// only print).
+int* status_word() {
+  int* p = nullptr;
+  return device_status_ptr(&p) == MSA_OK ? p : nullptr;
+}
+
 msa_status launched(cudaError_t e, const char* what) {
   if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
   return ok();
@@ -114,11 +122,12 @@ msa_status topk_forward(const void* q, const void* k, const void* v, void* out, 
                         int64_t n, int Hq, int Hkv, int d, int64_t window, int G, int top_k,
                         float scale, msa_dtype in_dt, msa_dtype out_dt, void* k_lm, int32_t* sel,
                         int32_t* cnt, cudaStream_t stream) {
-  msa::PoolArgs pa{k, nullptr, k_lm, nullptr, n, Hkv * d, G, in_dt == MSA_BF16 ? 1 : 0};
+  msa::PoolArgs pa{k, nullptr, k_lm, nullptr, n, Hkv * d, G, in_dt == MSA_BF16 ? 1 : 0,
+                   status_word()};
   msa_status st = launched(msa::launch_landmark_pool(pa, stream), "landmark pool");
   if (st != MSA_OK) return st;
   msa::SelectArgs sa{q, k_lm, sel, cnt, n, Hq, Hkv, d, window, G, n / G, top_k,
-                     in_dt == MSA_BF16 ? 1 : 0};
+                     in_dt == MSA_BF16 ? 1 : 0, status_word()};
   st = launched(msa::launch_block_select(sa, stream), "block select");
   if (st != MSA_OK) return st;
   msa::AttnArgs a{};
@@ -173,6 +182,14 @@ extern "C" {
 
 int msa_version(void) { return 100; }
 
+int msa_debug_bounds_build(void) {
+#ifdef MSA_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 const char* msa_last_error_string(void) { return g_last_error.c_str(); }
 
 msa_status msa_landmark_pool(const void* k, const void* v, void* k_lm, void* v_lm, int64_t n,
@@ -186,7 +203,8 @@ msa_status msa_landmark_pool(const void* k, const void* v, void* k_lm, void* v_l
                 n_landmarks, (long long)n);
   if (!valid_dtype(dt)) return fail(MSA_ERR_INVALID_ARG, "bad dtype %d", (int)dt);
   if (d != 64 && d != 128) return fail(MSA_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
-  msa::PoolArgs a{k, v, k_lm, v_lm, n, Hkv * d, n_landmarks, dt == MSA_BF16 ? 1 : 0};
+  msa::PoolArgs a{k, v, k_lm, v_lm, n, Hkv * d, n_landmarks, dt == MSA_BF16 ? 1 : 0,
+                  status_word()};
   return launched(msa::launch_landmark_pool(a, reinterpret_cast<cudaStream_t>(stream)),
                   "landmark pool");
 }
@@ -340,7 +358,7 @@ msa_status msa_block_select(const void* q, const void* k_lm, int32_t* sel, int32
   msa_status st = check_topk(n, n_landmarks, top_k);
   if (st != MSA_OK) return st;
   msa::SelectArgs a{q, k_lm, sel, cnt, n, Hq, Hkv, d, window, n_landmarks, n / n_landmarks, top_k,
-                    in_dt == MSA_BF16 ? 1 : 0};
+                    in_dt == MSA_BF16 ? 1 : 0, status_word()};
   return launched(msa::launch_block_select(a, reinterpret_cast<cudaStream_t>(stream)),
                   "block select");
 }
@@ -984,7 +1002,7 @@ msa_status msa_attn_fwd_host(const void* q, const void* k, const void* v, void* 
     MSA_HOST_CHECK(cudaEventRecord(ev_kv, si));
     MSA_HOST_CHECK(cudaStreamWaitEvent(cs, ev_kv, 0));
     msa::PoolArgs pa{ws + P.k, ws + P.v, ws + P.klm, ws + P.vlm, n, Hkv * d, G,
-                     in_dt == MSA_BF16 ? 1 : 0};
+                     in_dt == MSA_BF16 ? 1 : 0, status_word()};
     MSA_HOST_CHECK(msa::launch_landmark_pool(pa, cs));
   }
   for (int64_t r0 = 0, c = 0; r0 < n; r0 += rows, ++c) {
@@ -1005,7 +1023,7 @@ msa_status msa_attn_fwd_host(const void* q, const void* k, const void* v, void* 
       const int64_t l0 = r0 / blk, l1 = r1 / blk;
       msa::PoolArgs pa{ws + P.k + r0 * tok_kv, ws + P.v + r0 * tok_kv, ws + P.klm + l0 * tok_kv,
                        ws + P.vlm + l0 * tok_kv, m, Hkv * d, static_cast<int>(l1 - l0),
-                       in_dt == MSA_BF16 ? 1 : 0};
+                       in_dt == MSA_BF16 ? 1 : 0, status_word()};
       MSA_HOST_CHECK(msa::launch_landmark_pool(pa, cs));
     }
     if (have_ofree[b]) MSA_HOST_CHECK(cudaStreamWaitEvent(cs, ev_ofree[b], 0));
@@ -1080,6 +1098,7 @@ msa_status msa_lse_merge(const float* const* o_parts, const float* const* lse_pa
   a.Hq = Hq;
   a.d = d;
   a.out_bf16 = out_dt == MSA_BF16;
+  a.status = status_word();
   return launched(msa::launch_lse_merge(a, reinterpret_cast<cudaStream_t>(stream)), "lse merge");
 }
 

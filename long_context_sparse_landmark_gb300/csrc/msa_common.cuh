@@ -7,6 +7,10 @@
 
 #include "msa.h"
 
+#ifdef MSA_DEBUG_BOUNDS
+#include <stdio.h>
+#endif
+
 namespace msa {
 
 __host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -30,6 +34,54 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
 __device__ __forceinline__ void record_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
+
+// Range checks of the bounds-checked build.  Compiled with -DMSA_DEBUG_BOUNDS
+// (libmsa_debug.so), MSA_IN_RANGE(off, count, extent, status) holds when the
+// element (or byte) range [off, off + count) of a plain global access lies in
+// [0, extent), the extent the entry point's contract gives that buffer; and
+// MSA_TMA_OK(x, y, z, x_ext, y_ext, z_ext, box_z, status) holds when a 3-D
+// TMA box origin has x (elements within a row, 16-bit data) 16-byte aligned
+// and in [0, x_ext), y (head) in [0, y_ext), and its box_z rows overlapping
+// [0, z_ext).  A failed check records MSA_ERR_INVALID_ARG in the status word,
+// prints its site once, and the caller skips the access.  In the normal
+// build both are the constant true and their arguments are not evaluated.
+#ifdef MSA_DEBUG_BOUNDS
+__device__ __noinline__ inline void range_fail(const char* file, int line, long long v,
+                                               long long lo, long long hi, int* status) {
+  if (status == nullptr || atomicCAS(status, 0, MSA_ERR_INVALID_ARG) == 0)
+    printf("msa bounds check: %s:%d: %lld outside [%lld, %lld)\n", file, line, v, lo, hi);
+}
+__device__ __forceinline__ bool in_range(int64_t off, int64_t count, int64_t extent, int* status,
+                                         const char* file, int line) {
+  if (off >= 0 && count >= 0 && off + count <= extent) return true;
+  range_fail(file, line, off < 0 ? off : off + count, 0, extent + 1, status);
+  return false;
+}
+__device__ __forceinline__ bool tma_ok(int x, int y, int64_t z, int x_ext, int y_ext,
+                                       int64_t z_ext, int box_z, int* status, const char* file,
+                                       int line) {
+  if (x % 8 != 0 || x < 0 || x >= x_ext) {
+    range_fail(file, line, x, 0, x_ext, status);
+    return false;
+  }
+  if (y < 0 || y >= y_ext) {
+    range_fail(file, line, y, 0, y_ext, status);
+    return false;
+  }
+  if (z <= -box_z || z >= z_ext) {
+    range_fail(file, line, z, 1 - box_z, z_ext, status);
+    return false;
+  }
+  return true;
+}
+#define MSA_IN_RANGE(off, count, extent, status) \
+  (::msa::in_range((off), (count), (extent), (status), __FILE__, __LINE__))
+#define MSA_TMA_OK(x, y, z, x_ext, y_ext, z_ext, box_z, status) \
+  (::msa::tma_ok((x), (y), (z), (x_ext), (y_ext), (z_ext), (box_z), (status), __FILE__, __LINE__))
+#else
+#define MSA_IN_RANGE(off, count, extent, status) true
+#define MSA_TMA_OK(x, y, z, x_ext, y_ext, z_ext, box_z, status) true
+#endif
 
 // Selection entries are device data the caller may have written: a count
 // outside [0, min(top_k, candidates)] or a block index that is not a
@@ -73,6 +125,7 @@ struct PoolArgs {
   int C;  // Hkv * d elements per token
   int G;
   int bf16;
+  int* status;  // device status word (range checks of the bounds-checked build)
 };
 cudaError_t launch_landmark_pool(const PoolArgs& a, cudaStream_t s);
 
@@ -86,6 +139,7 @@ struct MergeArgs {
   int Hq;
   int d;
   int out_bf16;
+  int* status;  // device status word (range checks of the bounds-checked build)
 };
 cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t s);
 
@@ -141,6 +195,7 @@ struct SelectArgs {
   int64_t block;  // tokens per key block (n / G)
   int top_k;
   int bf16;
+  int* status;  // device status word (range checks of the bounds-checked build)
 };
 cudaError_t launch_block_select(const SelectArgs& a, cudaStream_t s);
 size_t block_select_smem(int d, int G);

@@ -15,6 +15,60 @@ BF16_MAX_ABS, BF16_MEAN_ABS = 1e-2, 1e-3
 F32_MAX_ABS = 1e-5
 
 
+# Canary guards: every output and workspace buffer of the GPU tests lives
+# inside a larger allocation with GUARD_BYTES of a fixed byte pattern before
+# and after it; check_guards() (run after each GPU test by conftest, and by
+# the helpers after each call) fails if a kernel wrote outside its buffer.
+GUARD_BYTES = 4096
+GUARD_BYTE = 0xA5
+_guarded: list = []
+
+
+def gempty(shape, dtype=torch.float32, device="cuda"):
+    """torch.empty inside a guarded allocation (16-byte aligned start)."""
+    shape = tuple(shape) if not isinstance(shape, int) else (shape,)
+    numel = math.prod(shape)
+    nbytes = numel * torch.tensor([], dtype=dtype).element_size()
+    raw = torch.empty((2 * GUARD_BYTES + nbytes,), dtype=torch.uint8, device=device)
+    raw[:GUARD_BYTES].fill_(GUARD_BYTE)
+    raw[GUARD_BYTES + nbytes:].fill_(GUARD_BYTE)
+    _guarded.append((raw, nbytes, f"{tuple(shape)} {dtype}"))
+    return raw[GUARD_BYTES:GUARD_BYTES + nbytes].view(dtype).view(shape)
+
+
+def gempty_like(t):
+    return gempty(t.shape, t.dtype, t.device)
+
+
+def gfull(shape, value, dtype=torch.float32, device="cuda"):
+    t = gempty(shape, dtype, device)
+    t.fill_(value)
+    return t
+
+
+def gfull_like(t, value):
+    return gfull(t.shape, value, t.dtype, t.device)
+
+
+def gzeros(shape, dtype=torch.float32, device="cuda"):
+    return gfull(shape, 0, dtype, device)
+
+
+def check_guards(forget: bool = False):
+    """Assert that no guard byte of any live guarded buffer changed."""
+    bad = []
+    for raw, nbytes, what in _guarded:
+        head = raw[:GUARD_BYTES]
+        tail = raw[GUARD_BYTES + nbytes:]
+        nh = int((head != GUARD_BYTE).sum())
+        nt = int((tail != GUARD_BYTE).sum())
+        if nh or nt:
+            bad.append(f"{what}: {nh} bytes before, {nt} bytes after changed")
+    if forget:
+        _guarded.clear()
+    assert not bad, "write outside a buffer: " + "; ".join(bad)
+
+
 def binding():
     from long_context_sparse_landmark_gb300 import _binding
     return _binding
@@ -56,15 +110,17 @@ def run_gpu_attention(q, k, v, wl: Workload, out_dtype=torch.float32):
     """Pool landmarks and run the fused attention through the C ABI."""
     B = binding()
     n, Hq, d = q.shape
-    out = torch.empty((n, Hq, d), dtype=out_dtype, device=q.device)
-    lse = torch.empty((Hq, n), dtype=torch.float32, device=q.device)
+    out = gempty((n, Hq, d), dtype=out_dtype, device=q.device)
+    lse = gempty((Hq, n), dtype=torch.float32, device=q.device)
     if wl.G > 0:
-        k_lm = torch.empty((wl.G, wl.Hkv, d), dtype=k.dtype, device=k.device)
-        v_lm = torch.empty_like(k_lm)
+        k_lm = gempty((wl.G, wl.Hkv, d), dtype=k.dtype, device=k.device)
+        v_lm = gempty_like(k_lm)
         B.landmark_pool(k, v, k_lm, v_lm)
+        check_guards()
     else:
         k_lm = v_lm = None
     B.attn_fwd(q, k, v, k_lm, v_lm, out, lse, wl.window, wl.G, wl.scale)
+    check_guards()
     return out, lse
 
 

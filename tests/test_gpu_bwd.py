@@ -14,6 +14,8 @@ most 0.7 x 2^-9 of the RMS).  D = <dO, O> takes the forward's O: kept in
 bf16 (the autograd op) it adds that rounding to every dS (measured 4.1 x
 2^-9), so that path is held to 2^-6.  A bf16 gradient output adds one
 rounding (half a bf16 spacing per element)."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -21,7 +23,7 @@ import torch
 import oracle
 from long_context_sparse_landmark_gb300.workloads import (Workload, generate, sample_rows,
                                                           to_numpy_bits)
-from tests.gpu_helpers import bf16_ulp, binding
+from tests.gpu_helpers import bf16_ulp, binding, check_guards, gempty, gempty_like
 
 pytestmark = pytest.mark.gpu
 
@@ -62,13 +64,29 @@ def make_dout(wl, seed):
 
 
 def gpu_backward(q, k, v, do, wl, grad_dtype=torch.float32):
-    import long_context_sparse_landmark_gb300.api as api
-    out, lse = api.msa_attention(q, k, v, wl.window, wl.G, wl.scale, out_dtype=torch.float32)
-    grads = api.msa_attention_backward(q, k, v, out, lse, do, wl.window, wl.G, wl.scale,
-                                       grad_dtype=grad_dtype)
+    """Forward then backward through the C ABI, every output and the
+    workspace in guarded buffers."""
+    B = binding()
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    out = gempty((n, Hq, d), torch.float32)
+    lse = gempty((Hq, n), torch.float32)
+    if wl.G > 0:
+        k_lm = gempty((wl.G, Hkv, d), k.dtype)
+        v_lm = gempty_like(k_lm)
+        B.landmark_pool(k, v, k_lm, v_lm)
+    else:
+        k_lm = v_lm = None
+    B.attn_fwd(q, k, v, k_lm, v_lm, out, lse, wl.window, wl.G, wl.scale)
+    dq = gempty((n, Hq, d), grad_dtype)
+    dk = gempty((n, Hkv, d), grad_dtype)
+    dv = gempty_like(dk)
+    ws = gempty((B.attn_bwd_workspace_size(n, Hq, Hkv, d, wl.G),), torch.uint8)
+    B.attn_bwd(q, k, v, k_lm, v_lm, out, lse, do, dq, dk, dv, wl.window, wl.G, wl.scale, ws)
     torch.cuda.synchronize()
-    assert binding().device_status() == 0
-    return grads
+    assert B.device_status() == 0
+    check_guards()
+    return dq, dk, dv
 
 
 BWD_CASES = [
@@ -124,6 +142,7 @@ def test_autograd_wrapper_matches_backward_call():
                     max_rel=MAX_REL_BF16_OUT, extra=0.5 * bf16_ulp(r))
 
 
+@pytest.mark.large
 def test_backward_16k_full():
     """A 16K-token layer slice (8 query heads on one KV head, w = 2048, 64
     landmarks of 256 tokens): every gradient element against the oracle."""
@@ -168,6 +187,7 @@ def sampled_keys_128k(n, Hkv, block, window, rng):
     return np.asarray(keys, dtype=np.int64), np.asarray(heads, dtype=np.int32)
 
 
+@pytest.mark.large
 def test_backward_128k_layer_properties_and_sampled_dq():
     """The 128K 70B-style layer: dQ on sampled rows and dK / dV on sampled
     keys against the oracle, element by element, and at full size the
@@ -212,14 +232,32 @@ def test_backward_128k_layer_properties_and_sampled_dq():
 
 # ------------------------------------------------------------ compression-token pattern
 def gpu_compressed_backward(q, k, v, do, w, block, rows, grad_dtype=torch.float32):
-    import long_context_sparse_landmark_gb300.api as api
+    """Compression-token forward and backward through the C ABI, every
+    output and workspace in guarded buffers."""
+    B = binding()
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    G = n // block
     r = torch.as_tensor(rows, dtype=torch.int64, device=DEV)
-    out, lse = api.compressed_attention(q, k, v, w, block, r, out_dtype=torch.float32)
-    grads = api.compressed_attention_backward(q, k, v, out, lse, do, w, block, r,
-                                              grad_dtype=grad_dtype)
+    k_lm = gempty((G, Hkv, d), k.dtype)
+    v_lm = gempty_like(k_lm)
+    B.landmark_pool(k, v, k_lm, v_lm)
+    out = gempty((n, Hq, d), torch.float32)
+    lse = gempty((Hq, n), torch.float32)
+    B.attn_fwd(q, k, v, k_lm, v_lm, out, lse, w, G, 1.0 / math.sqrt(d))
+    wsf = gempty((B.global_rows_workspace_size(n, len(rows), Hq, Hkv, d),), torch.uint8)
+    B.attn_fwd_global_rows(q, k, v, r, out, lse, 1.0 / math.sqrt(d), wsf)
+    dq = gempty((n, Hq, d), grad_dtype)
+    dk = gempty((n, Hkv, d), grad_dtype)
+    dv = gempty_like(dk)
+    ws = gempty((B.attn_bwd_global_rows_workspace_size(n, len(rows), Hq, Hkv, d, G),),
+                torch.uint8)
+    B.attn_bwd_global_rows(q, k, v, k_lm, v_lm, out, lse, do, r, dq, dk, dv, w, G,
+                           1.0 / math.sqrt(d), ws)
     torch.cuda.synchronize()
-    assert binding().device_status() == 0
-    return grads
+    assert B.device_status() == 0
+    check_guards()
+    return dq, dk, dv
 
 
 @pytest.mark.parametrize("n,Hq,Hkv,w,block,rows", [
@@ -241,6 +279,7 @@ def test_compressed_backward_parity(n, Hq, Hkv, w, block, rows):
     rel_compare(dv.cpu().numpy(), rv, f"compressed dV {wl}")
 
 
+@pytest.mark.large
 def test_compress_128k_backward_properties_and_sampled_dq():
     """The 128K compression workload: ΣdV = ΣdO and ΣdK = 0 at full size;
     dQ on sampled rows (all global rows among them) against the oracle."""

@@ -11,7 +11,7 @@ import torch
 import oracle
 from long_context_sparse_landmark_gb300.workloads import (WORKLOADS, Workload, generate,
                                                           sample_rows, to_numpy_bits)
-from tests.gpu_helpers import binding, compare, gather_rows, tol
+from tests.gpu_helpers import binding, compare, gather_rows, gempty, gfull, tol
 
 pytestmark = pytest.mark.gpu
 
@@ -28,11 +28,11 @@ def _oracle_threads():
 def _run_global_rows(q, k, v, rows, scale):
     B = binding()
     n, Hq, d = q.shape
-    out = torch.full((n, Hq, d), SENTINEL, dtype=torch.float32, device=DEV)
-    lse = torch.full((Hq, n), SENTINEL, dtype=torch.float32, device=DEV)
+    out = gfull((n, Hq, d), SENTINEL, dtype=torch.float32, device=DEV)
+    lse = gfull((Hq, n), SENTINEL, dtype=torch.float32, device=DEV)
     r = torch.as_tensor(rows, dtype=torch.int64, device=DEV)
-    ws = torch.empty((B.global_rows_workspace_size(n, len(rows), Hq, k.shape[1], d),),
-                     dtype=torch.uint8, device=DEV)
+    ws = gempty((B.global_rows_workspace_size(n, len(rows), Hq, k.shape[1], d),),
+                dtype=torch.uint8, device=DEV)
     B.attn_fwd_global_rows(q, k, v, r, out, lse, 1.0 / np.sqrt(d), ws)
     torch.cuda.synchronize()
     return out, lse
@@ -113,6 +113,7 @@ def test_compressed_small(dt, d, n, w, block, every):
     compare(lse.cpu().numpy(), rl, mx, mean, f"compressed lse {wl}")
 
 
+@pytest.mark.large
 def test_compress_128k_sampled_rows():
     import long_context_sparse_landmark_gb300.api as api
     wl = WORKLOADS["compress_128k"]

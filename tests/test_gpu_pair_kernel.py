@@ -14,7 +14,8 @@ import torch
 import oracle
 from long_context_sparse_landmark_gb300.workloads import (WORKLOADS, Workload, generate,
                                                           sample_rows, to_numpy_bits)
-from tests.gpu_helpers import binding, compare, gather_rows, oracle_attention, run_gpu_attention
+from tests.gpu_helpers import (binding, compare, gather_rows, gempty, gempty_like, gfull, gzeros,
+                               oracle_attention, run_gpu_attention)
 
 pytestmark = pytest.mark.gpu
 
@@ -96,13 +97,13 @@ def test_pair_equals_single_rows():
     B = binding()
     wl = Workload("pair_rows", 3000, 8, 2, 128, 500, 12, "bf16", seed=41)
     q, k, v = generate(wl, device=DEV)
-    k_lm = torch.empty((wl.G, wl.Hkv, 128), dtype=k.dtype, device=DEV)
-    v_lm = torch.empty_like(k_lm)
+    k_lm = gempty((wl.G, wl.Hkv, 128), dtype=k.dtype, device=DEV)
+    v_lm = gempty_like(k_lm)
     B.landmark_pool(k, v, k_lm, v_lm)
 
     def run():
-        out = torch.full((wl.n, wl.Hq, 128), 7.0, device=DEV)
-        lse = torch.full((wl.Hq, wl.n), 7.0, device=DEV)
+        out = gfull((wl.n, wl.Hq, 128), 7.0, device=DEV)
+        lse = gfull((wl.Hq, wl.n), 7.0, device=DEV)
         for r0, r1 in ((0, 1), (1, 700), (700, 2048), (2048, 3000)):
             B.attn_fwd_rows(q[r0:r1], k, v, k_lm, v_lm, out[r0:r1], lse, r0, wl.window, wl.G,
                             wl.scale)
@@ -123,8 +124,8 @@ def test_pair_equals_single_partials_and_merge():
     def run_partials():
         outs = []
         for p_ in range(4):
-            o = torch.full((wl.n, wl.Hq, 128), 3.0, device=DEV)
-            l_ = torch.empty((wl.Hq, wl.n), device=DEV)
+            o = gfull((wl.n, wl.Hq, 128), 3.0, device=DEV)
+            l_ = gempty((wl.Hq, wl.n), device=DEV)
             B.attn_fwd_partial(q, k[p_ * c:(p_ + 1) * c], v[p_ * c:(p_ + 1) * c], o, l_, 0, p_ * c,
                                wl.window, wl.scale)
             outs += [o, l_]
@@ -134,8 +135,8 @@ def test_pair_equals_single_partials_and_merge():
     assert_same_bits(a, b, "partials")
 
     def run_merge():
-        o = torch.zeros((wl.n, wl.Hq, 128), device=DEV)
-        l_ = torch.full((wl.Hq, wl.n), float("-inf"), device=DEV)
+        o = gzeros((wl.n, wl.Hq, 128), device=DEV)
+        l_ = gfull((wl.Hq, wl.n), float("-inf"), device=DEV)
         for p_ in (2, 0, 3, 1):
             B.attn_fwd_partial_merge(q, k[p_ * c:(p_ + 1) * c], v[p_ * c:(p_ + 1) * c], o, l_, 0,
                                      p_ * c, 1500, wl.scale)
@@ -152,8 +153,8 @@ def test_pair_equals_single_band(n, bb, hw):
     q, k, v = generate(wl, device=DEV)
 
     def run():
-        out = torch.empty((n, 8, 128), device=DEV)
-        lse = torch.empty((8, n), device=DEV)
+        out = gempty((n, 8, 128), device=DEV)
+        lse = gempty((8, n), device=DEV)
         B.attn_fwd_band(q, k, v, out, lse, bb, hw, wl.scale)
         return out, lse
 
@@ -167,16 +168,16 @@ def test_pair_equals_single_select(n, G, w, top_k, Hq, Hkv):
     B = binding()
     wl = Workload("pair_sel", n, Hq, Hkv, 128, w, G, "bf16", seed=n + G + top_k)
     q, k, v = generate(wl, device=DEV)
-    k_lm = torch.empty((G, Hkv, 128), dtype=k.dtype, device=DEV)
-    B.landmark_pool(k, v, k_lm, torch.empty_like(k_lm))
+    k_lm = gempty((G, Hkv, 128), dtype=k.dtype, device=DEV)
+    B.landmark_pool(k, v, k_lm, gempty_like(k_lm))
     n_qb = (n + 127) // 128
-    sel = torch.empty((n_qb, Hkv, top_k), dtype=torch.int32, device=DEV)
-    cnt = torch.empty((n_qb, Hkv), dtype=torch.int32, device=DEV)
+    sel = gempty((n_qb, Hkv, top_k), dtype=torch.int32, device=DEV)
+    cnt = gempty((n_qb, Hkv), dtype=torch.int32, device=DEV)
     B.block_select(q, k_lm, sel, cnt, w, top_k)
 
     def run():
-        out = torch.empty((n, Hq, 128), dtype=torch.bfloat16, device=DEV)
-        lse = torch.empty((Hq, n), device=DEV)
+        out = gempty((n, Hq, 128), dtype=torch.bfloat16, device=DEV)
+        lse = gempty((Hq, n), device=DEV)
         B.attn_fwd_select(q, k, v, sel, cnt, out, lse, w, G, top_k, wl.scale)
         return out, lse
 
@@ -184,6 +185,7 @@ def test_pair_equals_single_select(n, G, w, top_k, Hq, Hkv):
     assert_same_bits(a, b, f"select {wl}")
 
 
+@pytest.mark.large
 def test_pair_128k_layer_sampled_rows_and_bits():
     """The 128K layer in the benchmark's launch configuration: the pair
     kernel's sampled rows against the oracle, and every row bit-equal to the

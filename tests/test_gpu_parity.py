@@ -12,8 +12,8 @@ import torch
 import oracle
 from long_context_sparse_landmark_gb300.workloads import (WORKLOADS, Workload, generate,
                                                           sample_rows, to_numpy_bits)
-from tests.gpu_helpers import (bf16_round, bf16_ulp, binding, compare, gather_rows,
-                               oracle_attention, run_gpu_attention, tol)
+from tests.gpu_helpers import (bf16_round, bf16_ulp, binding, compare, gather_rows, gempty,
+                               gempty_like, gfull, oracle_attention, run_gpu_attention, tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -29,7 +29,7 @@ def _oracle_threads():
 # ------------------------------------------------------------------ pooling
 POOL_CASES = [(2048, 1, 64, 16, "f32"), (2048, 2, 128, 16, "bf16"), (32768, 1, 128, 512, "bf16"),
               (1000, 2, 64, 8, "f32"), (129, 1, 128, 129, "bf16"), (128, 3, 64, 1, "bf16"),
-              (131072, 8, 128, 512, "bf16")]
+              pytest.param(131072, 8, 128, 512, "bf16", marks=pytest.mark.large)]
 
 
 @pytest.mark.parametrize("n,Hkv,d,G,dt", POOL_CASES)
@@ -37,8 +37,8 @@ def test_landmark_pool_parity(n, Hkv, d, G, dt):
     B = binding()
     wl = Workload("pool", n, Hkv, Hkv, d, 1, G, dt, seed=n + G)
     _, k, v = generate(wl, device=DEV)
-    k_lm = torch.empty((G, Hkv, d), dtype=k.dtype, device=DEV)
-    v_lm = torch.empty_like(k_lm)
+    k_lm = gempty((G, Hkv, d), dtype=k.dtype, device=DEV)
+    v_lm = gempty_like(k_lm)
     B.landmark_pool(k, v, k_lm, v_lm)
     torch.cuda.synchronize()
     for got, src in ((k_lm, k), (v_lm, v)):
@@ -103,6 +103,7 @@ def test_32k_outliers_all_rows():
 
 
 @pytest.mark.parametrize("name", ["128k_70b_layer", "1m_70b_layer"])
+@pytest.mark.large
 def test_large_workload_sampled_rows(name):
     wl = WORKLOADS[name]
     q, k, v = generate(wl, device=DEV)
@@ -116,6 +117,7 @@ def test_large_workload_sampled_rows(name):
     compare(gl, rl, 1e-2, 1e-3, f"{name} lse (sampled)")
 
 
+@pytest.mark.large
 def test_ring_128k_partials_and_merge():
     """8 KV chunks -> per-chunk partials -> LSE merge; equals the oracle's
     single-pass causal attention on sampled rows, and the GPU single pass
@@ -125,15 +127,15 @@ def test_ring_128k_partials_and_merge():
     q, k, v = generate(wl, device=DEV)
     n, Hq, d = q.shape
     c = n // wl.ring_chunks
-    o_parts = [torch.empty((n, Hq, d), dtype=torch.float32, device=DEV)
+    o_parts = [gempty((n, Hq, d), dtype=torch.float32, device=DEV)
                for _ in range(wl.ring_chunks)]
-    l_parts = [torch.empty((Hq, n), dtype=torch.float32, device=DEV)
+    l_parts = [gempty((Hq, n), dtype=torch.float32, device=DEV)
                for _ in range(wl.ring_chunks)]
     for p in range(wl.ring_chunks):
         B.attn_fwd_partial(q, k[p * c:(p + 1) * c], v[p * c:(p + 1) * c], o_parts[p], l_parts[p],
                            0, p * c, wl.window, wl.scale)
-    merged = torch.empty((n, Hq, d), dtype=torch.float32, device=DEV)
-    mlse = torch.empty((Hq, n), dtype=torch.float32, device=DEV)
+    merged = gempty((n, Hq, d), dtype=torch.float32, device=DEV)
+    mlse = gempty((Hq, n), dtype=torch.float32, device=DEV)
     B.lse_merge(o_parts, l_parts, merged, mlse)
     # rows before a chunk have no key in it
     for p in range(1, wl.ring_chunks):
@@ -161,8 +163,8 @@ def test_partial_merge_small(dt, d, n, chunks, w):
     bounds = np.linspace(0, n, chunks + 1).astype(int)
     o_parts, l_parts = [], []
     for lo, hi in zip(bounds[:-1], bounds[1:]):
-        o = torch.full((n, 4, d), 7.0, dtype=torch.float32, device=DEV)
-        l = torch.empty((4, n), dtype=torch.float32, device=DEV)
+        o = gfull((n, 4, d), 7.0, dtype=torch.float32, device=DEV)
+        l = gempty((4, n), dtype=torch.float32, device=DEV)
         B.attn_fwd_partial(q, k[lo:hi], v[lo:hi], o, l, 0, int(lo), w, wl.scale)
         o_parts.append(o)
         l_parts.append(l)
@@ -176,8 +178,8 @@ def test_partial_merge_small(dt, d, n, chunks, w):
         go = o.cpu().numpy()
         compare(go[has], ro[has], mx, mean, f"partial O [{lo},{hi})")
         assert np.all(go[~has] == 7.0), "rows without keys must be left untouched"
-    out = torch.empty((n, 4, d), dtype=torch.float32, device=DEV)
-    lse = torch.empty((4, n), dtype=torch.float32, device=DEV)
+    out = gempty((n, 4, d), dtype=torch.float32, device=DEV)
+    lse = gempty((4, n), dtype=torch.float32, device=DEV)
     B.lse_merge(o_parts, l_parts, out, lse)
     torch.cuda.synchronize()
     ro, rl = oracle.attn(qn, kn, vn, w, 0, wl.scale)
@@ -193,8 +195,8 @@ def test_band_small(dt, d, n, bb, hw):
     B = binding()
     wl = Workload("band_small", n, 8, 2, d, 1, 0, dt, seed=n + 17 * bb + hw)
     q, k, v = generate(wl, device=DEV)
-    out = torch.empty((n, 8, d), dtype=torch.float32, device=DEV)
-    lse = torch.empty((8, n), dtype=torch.float32, device=DEV)
+    out = gempty((n, 8, d), dtype=torch.float32, device=DEV)
+    lse = gempty((8, n), dtype=torch.float32, device=DEV)
     B.attn_fwd_band(q, k, v, out, lse, bb, hw, wl.scale)
     torch.cuda.synchronize()
     ro, rl = oracle.attn_band(to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v), bb, hw,
@@ -204,6 +206,7 @@ def test_band_small(dt, d, n, bb, hw):
     compare(lse.cpu().numpy(), rl, mx, mean, f"band lse n={n} bb={bb} hw={hw}")
 
 
+@pytest.mark.large
 def test_band_128k_sampled_rows():
     import long_context_sparse_landmark_gb300.api as api
     wl = WORKLOADS["band_128k"]
@@ -237,8 +240,8 @@ def test_partial_merge_running_result(dt, d, n, chunks, w, order):
         pieces = pieces[::-1]
     elif order == "mixed":
         pieces = pieces[1::2] + pieces[0::2]
-    out = torch.full((n, 4, d), float("nan"), dtype=torch.float32, device=DEV)
-    lse = torch.full((4, n), -float("inf"), dtype=torch.float32, device=DEV)
+    out = gfull((n, 4, d), float("nan"), dtype=torch.float32, device=DEV)
+    lse = gfull((4, n), -float("inf"), dtype=torch.float32, device=DEV)
     for lo, hi in pieces:
         B.attn_fwd_partial_merge(q, k[lo:hi], v[lo:hi], out, lse, 0, int(lo), w, wl.scale)
     torch.cuda.synchronize()
@@ -248,6 +251,7 @@ def test_partial_merge_running_result(dt, d, n, chunks, w, order):
     compare(lse.cpu().numpy(), rl, mx, mean, "running lse")
 
 
+@pytest.mark.large
 def test_ring_128k_fused_rounds():
     """The ring workload through eight fused rounds equals the oracle on
     sampled rows and the separate partial + merge path on every row."""
@@ -285,8 +289,8 @@ def test_lse_merge_parity(P, n, Hq, d, out_dt):
     o_d = [o[p].contiguous().to(DEV) for p in range(P)]
     l_d = [l[p].contiguous().to(DEV) for p in range(P)]
     tdt = torch.float32 if out_dt == "f32" else torch.bfloat16
-    out = torch.empty((n, Hq, d), dtype=tdt, device=DEV)
-    lse = torch.empty((Hq, n), dtype=torch.float32, device=DEV)
+    out = gempty((n, Hq, d), dtype=tdt, device=DEV)
+    lse = gempty((Hq, n), dtype=torch.float32, device=DEV)
     B.lse_merge(o_d, l_d, out, lse)
     torch.cuda.synchronize()
     ro, rl = oracle.lse_merge(o.double().numpy(), l.double().numpy())

@@ -12,7 +12,8 @@ import torch
 import oracle
 from long_context_sparse_landmark_gb300.workloads import (WORKLOADS, Workload, generate,
                                                           to_numpy_bits)
-from tests.gpu_helpers import binding, compare, run_gpu_attention, tol
+from tests.gpu_helpers import (binding, compare, gempty, gempty_like, gfull, gfull_like,
+                               run_gpu_attention, tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -25,11 +26,11 @@ def test_row_chunks_equal_whole_call(dt, d):
     wl = Workload("rows", 4096, 8, 2, d, 700, 16, dt, seed=41)
     q, k, v = generate(wl, device=DEV)
     ref_o, ref_l = run_gpu_attention(q, k, v, wl)
-    k_lm = torch.empty((wl.G, wl.Hkv, d), dtype=k.dtype, device=DEV)
-    v_lm = torch.empty_like(k_lm)
+    k_lm = gempty((wl.G, wl.Hkv, d), dtype=k.dtype, device=DEV)
+    v_lm = gempty_like(k_lm)
     B.landmark_pool(k, v, k_lm, v_lm)
-    out = torch.full_like(ref_o, float("nan"))
-    lse = torch.full_like(ref_l, float("nan"))
+    out = gfull_like(ref_o, float("nan"))
+    lse = gfull_like(ref_l, float("nan"))
     for r0 in range(0, wl.n, 1024):
         B.attn_fwd_rows(q[r0:r0 + 1024], k, v, k_lm, v_lm, out[r0:r0 + 1024], lse, r0,
                         wl.window, wl.G, wl.scale)
@@ -44,12 +45,12 @@ def test_ragged_row_range_matches_oracle(dt, d, q_start, n_q):
     B = binding()
     wl = Workload("rr", 4096, 4, 1, d, 300, 32, dt, seed=q_start + n_q)
     q, k, v = generate(wl, device=DEV)
-    k_lm = torch.empty((wl.G, wl.Hkv, d), dtype=k.dtype, device=DEV)
-    v_lm = torch.empty_like(k_lm)
+    k_lm = gempty((wl.G, wl.Hkv, d), dtype=k.dtype, device=DEV)
+    v_lm = gempty_like(k_lm)
     B.landmark_pool(k, v, k_lm, v_lm)
     qr = q[q_start:q_start + n_q].contiguous()
-    out = torch.empty((n_q, wl.Hq, d), dtype=torch.float32, device=DEV)
-    lse = torch.full((wl.Hq, wl.n), float("nan"), dtype=torch.float32, device=DEV)
+    out = gempty((n_q, wl.Hq, d), dtype=torch.float32, device=DEV)
+    lse = gfull((wl.Hq, wl.n), float("nan"), dtype=torch.float32, device=DEV)
     B.attn_fwd_rows(qr, k, v, k_lm, v_lm, out, lse, q_start, wl.window, wl.G, wl.scale)
     torch.cuda.synchronize()
     rows = np.arange(q_start, q_start + n_q)
@@ -64,10 +65,15 @@ def test_ragged_row_range_matches_oracle(dt, d, q_start, n_q):
     assert np.isnan(got_l[:, others]).all(), "lse columns outside the range were written"
 
 
-@pytest.mark.parametrize("name,chunk", [("32k_outliers", 4096), ("128k_70b_layer", 16384),
+_L = pytest.mark.large
+
+
+@pytest.mark.parametrize("name,chunk", [("32k_outliers", 4096),
+                                        pytest.param("128k_70b_layer", 16384, marks=_L),
                                         ("pr1_2k", 300), ("32k_outliers", 4160),
-                                        ("ring_128k", 20000), ("128k_70b_layer", None),
-                                        ("128k_70b_layer", 4224)])
+                                        pytest.param("ring_128k", 20000, marks=_L),
+                                        pytest.param("128k_70b_layer", None, marks=_L),
+                                        pytest.param("128k_70b_layer", 4224, marks=_L)])
 def test_host_api_equals_device_api(name, chunk):
     """msa_attn_fwd_host through the Python API (copy streams, pinned
     buffers): whole landmark blocks per chunk (K/V streamed), chunks that
@@ -95,8 +101,8 @@ def test_host_entry_point_one_stream(dt, d, n, G, w, chunk):
     hq, hk, hv = (t.cpu() for t in (q, k, v))
     ho = torch.full((n, 8, d), float("nan"))
     hl = torch.full((8, n), float("nan"))
-    ws = torch.empty((B.host_workspace_size(n, 8, 2, d, G, chunk, q.dtype, torch.float32),),
-                     dtype=torch.uint8, device=DEV)
+    ws = gempty((B.host_workspace_size(n, 8, 2, d, G, chunk, q.dtype, torch.float32),),
+                dtype=torch.uint8, device=DEV)
     B.attn_fwd_host(hq, hk, hv, ho, hl, w, G, wl.scale, chunk, ws)
     assert B.device_status() == 0
     assert torch.equal(ho, ref_o.cpu()) and torch.equal(hl, ref_l.cpu())

@@ -22,7 +22,7 @@ import torch
 import oracle
 from long_context_sparse_landmark_gb300.workloads import (WORKLOADS, Workload, generate,
                                                           sample_rows, to_numpy_bits)
-from tests.gpu_helpers import binding, compare, gather_rows, tol
+from tests.gpu_helpers import binding, compare, gather_rows, gempty, gempty_like, gfull, tol
 
 pytestmark = pytest.mark.gpu
 
@@ -41,12 +41,12 @@ def gpu_select(q, k, v, G, window, top_k):
     B = binding()
     n, Hq, d = q.shape
     Hkv = k.shape[1]
-    k_lm = torch.empty((G, Hkv, d), dtype=k.dtype, device=DEV)
-    v_lm = torch.empty_like(k_lm)
+    k_lm = gempty((G, Hkv, d), dtype=k.dtype, device=DEV)
+    v_lm = gempty_like(k_lm)
     B.landmark_pool(k, v, k_lm, v_lm)
     n_qb = (n + QB - 1) // QB
-    sel = torch.full((n_qb, Hkv, top_k), -7, dtype=torch.int32, device=DEV)
-    cnt = torch.full((n_qb, Hkv), -7, dtype=torch.int32, device=DEV)
+    sel = gfull((n_qb, Hkv, top_k), -7, dtype=torch.int32, device=DEV)
+    cnt = gfull((n_qb, Hkv), -7, dtype=torch.int32, device=DEV)
     B.block_select(q, k_lm, sel, cnt, window, top_k)
     return sel, cnt
 
@@ -185,8 +185,8 @@ def test_attn_select_oracle_selection(dt, d, n, G, w, top_k, Hq, Hkv):
     sel_o, cnt_o = oracle.select_top_k(oracle.block_scores(qn, kn, G, w), top_k)
     sel = torch.from_numpy(np.ascontiguousarray(sel_o)).to(DEV)
     cnt = torch.from_numpy(np.ascontiguousarray(cnt_o)).to(DEV)
-    out = torch.empty((n, Hq, d), dtype=torch.float32, device=DEV)
-    lse = torch.empty((Hq, n), dtype=torch.float32, device=DEV)
+    out = gempty((n, Hq, d), dtype=torch.float32, device=DEV)
+    lse = gempty((Hq, n), dtype=torch.float32, device=DEV)
     B.attn_fwd_select(q, k, v, sel, cnt, out, lse, w, G, top_k, wl.scale)
     torch.cuda.synchronize()
     assert B.device_status() == 0
@@ -205,8 +205,8 @@ def _fused_vs_steps(q, k, v, wl):
     out_f, lse_f = api.topk_attention(q, k, v, wl.window, wl.G, wl.top_k, wl.scale,
                                       out_dtype=torch.float32)
     sel, cnt = gpu_select(q, k, v, wl.G, wl.window, wl.top_k)
-    out = torch.empty_like(out_f)
-    lse = torch.empty_like(lse_f)
+    out = gempty_like(out_f)
+    lse = gempty_like(lse_f)
     B.attn_fwd_select(q, k, v, sel, cnt, out, lse, wl.window, wl.G, wl.top_k, wl.scale)
     torch.cuda.synchronize()
     assert B.device_status() == 0
@@ -240,6 +240,7 @@ def test_topk_fused_against_oracle(dt, d, n, G, w, top_k, Hq, Hkv):
     compare(l_, rgl, mx, mean, f"fused lse, GPU selection {wl}")
 
 
+@pytest.mark.large
 def test_topk_128k_sampled_rows():
     """The 128K top-k workload in the benchmark's launch configuration:
     fused call == steps, selection valid on every unit, sampled rows equal
@@ -280,10 +281,10 @@ def test_attn_select_rejects_bad_selection_without_reading_out_of_bounds():
         wl = Workload("bad", n, Hq, Hkv, d, w, G, dt, seed=1)
         q, k, v = generate(wl, device=DEV)
         n_qb = n // QB
-        sel = torch.full((n_qb, Hkv, top_k), 10 ** 6, dtype=torch.int32, device=DEV)
-        cnt = torch.full((n_qb, Hkv), 99, dtype=torch.int32, device=DEV)
-        out = torch.empty((n, Hq, d), dtype=torch.float32, device=DEV)
-        lse = torch.empty((Hq, n), dtype=torch.float32, device=DEV)
+        sel = gfull((n_qb, Hkv, top_k), 10 ** 6, dtype=torch.int32, device=DEV)
+        cnt = gfull((n_qb, Hkv), 99, dtype=torch.int32, device=DEV)
+        out = gempty((n, Hq, d), dtype=torch.float32, device=DEV)
+        lse = gempty((Hq, n), dtype=torch.float32, device=DEV)
         B.device_status(clear=True)
         B.attn_fwd_select(q, k, v, sel, cnt, out, lse, w, G, top_k, wl.scale)
         torch.cuda.synchronize()

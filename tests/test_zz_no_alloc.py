@@ -12,7 +12,7 @@ import pytest
 import torch
 
 from long_context_sparse_landmark_gb300.workloads import Workload, generate
-from tests.gpu_helpers import binding, compare, tol
+from tests.gpu_helpers import binding, compare, gempty, gfull, tol
 
 DEV = "cuda"
 SCRATCH_BYTES = 16 << 20
@@ -31,10 +31,10 @@ CASES = [
 
 def _with_workspace(q, k, v, wl, out_dtype):
     B = binding()
-    out = torch.empty((wl.n, wl.Hq, wl.d), dtype=out_dtype, device=DEV)
-    lse = torch.empty((wl.Hq, wl.n), dtype=torch.float32, device=DEV)
-    ws = torch.empty((B.topk_workspace_size(wl.n, wl.Hkv, wl.d, wl.G, wl.top_k, q.dtype),),
-                     dtype=torch.uint8, device=DEV)
+    out = gempty((wl.n, wl.Hq, wl.d), dtype=out_dtype, device=DEV)
+    lse = gempty((wl.Hq, wl.n), dtype=torch.float32, device=DEV)
+    ws = gempty((B.topk_workspace_size(wl.n, wl.Hkv, wl.d, wl.G, wl.top_k, q.dtype),),
+                dtype=torch.uint8, device=DEV)
     B.attn_fwd_topk(q, k, v, out, lse, wl.window, wl.G, wl.top_k, wl.scale, ws)
     return out, lse
 
@@ -54,8 +54,8 @@ def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
         torch.cuda.synchronize()
         mx, mean = tol(dt)
         for call in range(2):
-            out = torch.full((n, Hq, d), float("nan"), dtype=torch.float32, device=DEV)
-            lse = torch.full((Hq, n), float("nan"), dtype=torch.float32, device=DEV)
+            out = gfull((n, Hq, d), float("nan"), dtype=torch.float32, device=DEV)
+            lse = gfull((Hq, n), float("nan"), dtype=torch.float32, device=DEV)
             B.attn_fwd_topk_noalloc(q, k, v, out, lse, w, G, top_k, wl.scale)
             torch.cuda.synchronize()
             assert B.device_status() == 0
