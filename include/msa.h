@@ -523,10 +523,12 @@ void msa_debug_set_wait_limit_ns(uint64_t ns);
 
 /*
  * Test hook: with `on` nonzero, launches made after the call run the
- * single-CTA tensor-core attention kernel even where the CTA-pair kernel
- * applies (bf16, d = 128, at least two query heads per KV head), so that
- * tests can compare the two; 0 restores the normal choice.  Both kernels
- * compute the same arithmetic in the same order and give the same bits.
+ * single-CTA tensor-core kernels even where a CTA-pair kernel applies -- the
+ * attention forward (bf16, d = 128, at least two query heads per KV head)
+ * and the dQ kernel of msa_attn_bwd (an even number of query heads per KV
+ * head) -- so that tests can compare the two; 0 restores the normal
+ * choice.  Each pair kernel computes the same arithmetic in the same order
+ * as its single-CTA form and gives the same bits.
  */
 void msa_debug_force_single_cta(int on);
 

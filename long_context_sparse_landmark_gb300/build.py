@@ -28,7 +28,7 @@ LIB_DEBUG = os.path.join(PKG, "libmsa_debug.so")
 
 SOURCES = ["msa_api.cu", "k1_landmark_pool.cu", "k2_attn_simt.cu", "k2_attn_tc.cu",
            "k2_attn_tc2.cu", "k3_lse_merge.cu", "k4_block_select.cu", "k5_global_rows.cu",
-           "k6_attn_bwd.cu"]
+           "k6_attn_bwd.cu", "k6_bwd_dq_pair.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -175,73 +175,6 @@ __device__ __forceinline__ Unit decode_unit(const Tc2Params& p, int u) {
   return w;
 }
 
-struct PairWait {
-  volatile int* abort;       // this CTA's flag
-  uint32_t peer_abort;       // the peer's flag (cluster address)
-  int* status;
-  uint64_t limit;
-};
-
-__device__ __forceinline__ int peer_flag(uint32_t a) {
-  int v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-  return v;
-}
-
-// Bounded wait on phase `parity` of one of this CTA's mbarriers.  Returns
-// false when the pair is aborting (this CTA's or the peer's flag set, or
-// this wait ran out).  The first probe does not block; a limit of at most
-// 1 ns makes every wait that this probe does not find complete run out.
-// The peer's flag (a load from the other SM) is read every 8th round only.
-// `backoff_ns` > 0 (the producer, whose ring gives it slack) sleeps between
-// probes, leaving the issue slots of its SM sub-partition to the softmax.
-__device__ __forceinline__ bool wait_pair(uint32_t bar, uint32_t parity, const PairWait& c,
-                                          uint32_t backoff_ns = 0) {
-  if (pair::test_wait_cluster(bar, parity)) return true;
-  if (c.limit > 1) {
-    const uint64_t t0 = ptx::globaltimer();
-    for (uint32_t round = 0;; ++round) {
-      if (backoff_ns) {
-        __nanosleep(backoff_ns);
-        if (pair::test_wait_cluster(bar, parity)) return true;
-      } else if (pair::try_wait_cluster(bar, parity)) {
-        return true;
-      }
-      if (*c.abort || ((round & 7) == 7 && peer_flag(c.peer_abort))) {
-        *c.abort = 1;
-        return false;
-      }
-      if (ptx::globaltimer() - t0 > c.limit) break;
-    }
-  } else if (*c.abort || peer_flag(c.peer_abort)) {
-    *c.abort = 1;
-    return false;
-  }
-  *c.abort = 1;
-  record_status(c.status, MSA_ERR_TIMEOUT);
-  return false;
-}
-
-// The same for a whole warp: every lane probes, so the warp's control flow
-// stays converged (waits taken by one lane in a divergent branch measured
-// far slower: branch-resolution stalls), with one result for all lanes.
-__device__ __forceinline__ bool wait_pair_w(uint32_t bar, uint32_t parity, const PairWait& c) {
-  return __all_sync(0xffffffffu, wait_pair(bar, parity, c));
-}
-
-// Wait used while draining: ignores the abort flags, limit `ns`.
-__device__ __forceinline__ void drain_for(uint32_t bar, uint32_t parity, int* status,
-                                          uint64_t ns) {
-  if (pair::try_wait_cluster(bar, parity)) return;
-  const uint64_t t0 = ptx::globaltimer();
-  while (!pair::try_wait_cluster(bar, parity)) {
-    if (ptx::globaltimer() - t0 > ns) {
-      record_status(status, MSA_ERR_TIMEOUT);
-      return;
-    }
-  }
-}
-
 __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_constant__ Tc2Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(

@@ -1373,8 +1373,12 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why) 
   bwd_dkdv_tc_kernel<false><<<dim3(n_tiles, a.Hkv, 1), kThreads, kSmemBytes, s>>>(p);
   e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
-  bwd_dq_tc_kernel<false><<<dim3(n_tiles, a.Hq), kThreads, kDqSmemBytes, s>>>(p);
-  e = cudaPeekAtLastError();
+  if (!a.no_pair && bwd_dq_pair_supported(a)) {
+    e = launch_bwd_dq_pair(a, s, why);
+  } else {
+    bwd_dq_tc_kernel<false><<<dim3(n_tiles, a.Hq), kThreads, kDqSmemBytes, s>>>(p);
+    e = cudaPeekAtLastError();
+  }
   if (e != cudaSuccess || !a.rows) return e;
   // The global rows' dQ: per key split, then summed into their rows.
   bwd_dq_tc_kernel<true><<<dim3(a.n_splits, static_cast<unsigned>(a.Mp / kT), a.Hkv),

@@ -749,6 +749,7 @@ static msa_status attn_bwd_impl(const void* q, const void* k, const void* v, con
   if (st != MSA_OK) return st;
   const uint64_t lim = g_wait_limit_ns.load();
   a.wait_limit_ns = lim ? lim : kDefaultWaitNs;
+  a.no_pair = g_force_single_cta.load();
   const char* why = nullptr;
   cudaError_t e = msa::launch_attn_bwd(a, reinterpret_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess && why) return fail(MSA_ERR_CUDA, "backward: %s", why);

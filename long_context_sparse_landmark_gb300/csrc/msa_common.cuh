@@ -266,9 +266,14 @@ struct BwdArgs {
   float* dq_part;
   float* extra_k;
   float* extra_v;
+  int no_pair;  // 1: the single-CTA dQ kernel even where the pair kernel applies
 };
 bool attn_bwd_supported(int d, int in_bf16);
 cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why);
+// The CTA-pair dQ kernel (plain backward, an even number of query heads per
+// KV head); launched by launch_attn_bwd.
+bool bwd_dq_pair_supported(const BwdArgs& a);
+cudaError_t launch_bwd_dq_pair(const BwdArgs& a, cudaStream_t s, const char** why);
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s, const char** why);
 bool attn_tc_supported(int Hq, int Hkv, int d, int in_bf16);
 // The CTA-pair variant (two SMs share each MMA; query heads per KV head >= 2).

@@ -11,6 +11,7 @@
 
 #include <stdint.h>
 
+#include "msa_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace msa {
@@ -192,5 +193,106 @@ __device__ __forceinline__ void mma_ts_x8(uint32_t d, uint32_t a_tmem, uint32_t 
       : "memory");
 }
 
+// Eight pair TS MMAs over K = 128 whose A operand sits in tensor memory as
+// four 32-column chunks, each holding its 16 packed bf16 pairs in the
+// chunk's first 16 columns (steps at a, a + 8, a + 32, a + 40, ...); B each
+// CTA's half of N, an MN-major SW128 tile, 16 rows (2048 bytes) per step.
+__device__ __forceinline__ void mma_ts_chunked_x8(uint32_t d, uint32_t a_tmem, uint32_t b_lo,
+                                                  uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p0;\n\t.reg .b64 db;\n\t.reg .b32 at, bl;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\t"
+      "mov.b64 db, {%2, %5};\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], db, %3, p0;\n\t"
+      "add.u32 at, %1, 8;\n\tadd.u32 bl, %2, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [at], db, %3, 1;\n\t"
+      "add.u32 at, %1, 32;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [at], db, %3, 1;\n\t"
+      "add.u32 at, %1, 40;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [at], db, %3, 1;\n\t"
+      "add.u32 at, %1, 64;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [at], db, %3, 1;\n\t"
+      "add.u32 at, %1, 72;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [at], db, %3, 1;\n\t"
+      "add.u32 at, %1, 96;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [at], db, %3, 1;\n\t"
+      "add.u32 at, %1, 104;\n\tadd.u32 bl, bl, 128;\n\tmov.b64 db, {bl, %5};\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [at], db, %3, 1;\n\t}" ::"r"(d),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(ptx::kDescHiSw128)
+      : "memory");
+}
+
 }  // namespace pair
+
+// Bounded waits of a CTA pair.  Each CTA has an abort flag in its shared
+// memory; a wait also gives up when the peer's flag is set, so both CTAs
+// leave their loops together.
+struct PairWait {
+  volatile int* abort;       // this CTA's flag
+  uint32_t peer_abort;       // the peer's flag (cluster address)
+  int* status;
+  uint64_t limit;
+};
+
+__device__ __forceinline__ int peer_flag(uint32_t a) {
+  int v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
+// Bounded wait on phase `parity` of one of this CTA's mbarriers.  Returns
+// false when the pair is aborting (this CTA's or the peer's flag set, or
+// this wait ran out).  The first probe does not block; a limit of at most
+// 1 ns makes every wait that this probe does not find complete run out.
+// The peer's flag (a load from the other SM) is read every 8th round only.
+// `backoff_ns` > 0 (the producer, whose ring gives it slack) sleeps between
+// probes, leaving the issue slots of its SM sub-partition to the softmax.
+__device__ __forceinline__ bool wait_pair(uint32_t bar, uint32_t parity, const PairWait& c,
+                                          uint32_t backoff_ns = 0) {
+  if (pair::test_wait_cluster(bar, parity)) return true;
+  if (c.limit > 1) {
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t round = 0;; ++round) {
+      if (backoff_ns) {
+        __nanosleep(backoff_ns);
+        if (pair::test_wait_cluster(bar, parity)) return true;
+      } else if (pair::try_wait_cluster(bar, parity)) {
+        return true;
+      }
+      if (*c.abort || ((round & 7) == 7 && peer_flag(c.peer_abort))) {
+        *c.abort = 1;
+        return false;
+      }
+      if (ptx::globaltimer() - t0 > c.limit) break;
+    }
+  } else if (*c.abort || peer_flag(c.peer_abort)) {
+    *c.abort = 1;
+    return false;
+  }
+  *c.abort = 1;
+  record_status(c.status, MSA_ERR_TIMEOUT);
+  return false;
+}
+
+// The same for a whole warp: every lane probes, so the warp's control flow
+// stays converged (waits taken by one lane in a divergent branch measured
+// far slower: branch-resolution stalls), with one result for all lanes.
+__device__ __forceinline__ bool wait_pair_w(uint32_t bar, uint32_t parity, const PairWait& c) {
+  return __all_sync(0xffffffffu, wait_pair(bar, parity, c));
+}
+
+// Wait used while draining: ignores the abort flags, limit `ns`.
+__device__ __forceinline__ void drain_for(uint32_t bar, uint32_t parity, int* status,
+                                          uint64_t ns) {
+  if (pair::try_wait_cluster(bar, parity)) return;
+  const uint64_t t0 = ptx::globaltimer();
+  while (!pair::try_wait_cluster(bar, parity)) {
+    if (ptx::globaltimer() - t0 > ns) {
+      record_status(status, MSA_ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
 }  // namespace msa

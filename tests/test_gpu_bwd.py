@@ -304,3 +304,23 @@ def test_compress_128k_backward_properties_and_sampled_dq():
     ref[~is_g] = oracle.attn_bwd_dq_rows(qn, kn, vn, dn, wl.window, wl.G, wl.scale, rows[~is_g])
     ref[is_g] = oracle.attn_bwd_dq_rows(qn, kn, vn, dn, wl.n, 0, wl.scale, rows[is_g])
     rel_compare(gq, ref, "compress 128K dQ (sampled + global rows)")
+
+
+@pytest.mark.parametrize("n,Hq,Hkv,w,G", [(1000, 4, 2, 100, 8), (2048, 8, 1, 300, 16),
+                                        (640, 4, 4, 640, 0), (4096, 16, 2, 1024, 32),
+                                        (129, 2, 1, 7, 3)])
+def test_dq_pair_kernel_equals_single_cta(n, Hq, Hkv, w, G):
+    """The CTA-pair dQ kernel (two heads of a KV group share every MMA) gives
+    the bits of the single-CTA dQ kernel; dK / dV are unaffected."""
+    B = binding()
+    wl = Workload("dqpair", n, Hq, Hkv, 128, w, G, "bf16", seed=n + Hq + G)
+    q, k, v = generate(wl, device=DEV)
+    do = make_dout(wl, seed=n + 5)
+    try:
+        B.force_single_cta(True)
+        single = gpu_backward(q, k, v, do, wl)
+    finally:
+        B.force_single_cta(False)
+    pair = gpu_backward(q, k, v, do, wl)
+    for a, b, name in zip(pair, single, ("dQ", "dK", "dV")):
+        assert torch.equal(a, b), f"{name} differs between the pair and single-CTA kernels"
