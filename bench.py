@@ -792,10 +792,14 @@ def main():
         # Standard backward count: five GEMMs per attended pair (S, dP, dV,
         # dK, dQ), 2.5 x the forward's useful FLOPs.
         fbw = 2.5 * flops
+        # Executed: the dK/dV kernels take S, dP, dV, dK (8 d per attended
+        # pair) and the dQ kernel recomputes S and dP besides dQ (6 d):
+        # 1.4 x the useful count.
         also["bwd_" + wl.name] = {"ms_per_step": round(bms, 3),
                                   "tflops": round(fbw / (bms * 1e-3) / 1e12, 2),
                                   "pct_bf16_peak": round(100.0 * fbw / (bms * 1e-3) / 1e12
                                                          / peaks["bf16_tflops"], 2),
+                                  "executed_tflops": round(1.4 * fbw / (bms * 1e-3) / 1e12, 2),
                                   "launches_per_step": 5, "steps": 3}
         cms = run_bwd_compressed(wlc, 3, 1, dev, B, torch)
         fcb = 2.5 * fc

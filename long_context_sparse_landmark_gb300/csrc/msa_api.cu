@@ -12,6 +12,18 @@
 
 #include "msa_common.cuh"
 
+#include <nvtx3/nvToolsExt.h>
+
+// Every entry point opens an NVTX range named after itself for the
+// duration of the call (host side: argument checks and launches), so that
+// profiler timelines group each call's kernels; without a tool attached the
+// push and pop cost nanoseconds.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+#define MSA_NVTX_RANGE() NvtxRange msa_nvtx_range_(__func__)
+
 namespace {
 
 thread_local std::string g_last_error;
@@ -194,6 +206,7 @@ const char* msa_last_error_string(void) { return g_last_error.c_str(); }
 
 msa_status msa_landmark_pool(const void* k, const void* v, void* k_lm, void* v_lm, int64_t n,
                              int Hkv, int d, int n_landmarks, msa_dtype dt, msa_stream_t stream) {
+  MSA_NVTX_RANGE();
   if (!k || !v || !k_lm || !v_lm) return fail(MSA_ERR_INVALID_ARG, "null tensor pointer");
   if (!aligned16(k) || !aligned16(v) || !aligned16(k_lm) || !aligned16(v_lm))
     return fail(MSA_ERR_INVALID_ARG, "tensor pointer not 16-byte aligned");
@@ -213,6 +226,7 @@ msa_status msa_attn_fwd(const void* q, const void* k, const void* v, const void*
                         const void* v_lm, void* out, float* lse, int64_t n, int Hq, int Hkv, int d,
                         int64_t window, int n_landmarks, float scale, msa_dtype in_dt,
                         msa_dtype out_dt, msa_stream_t stream) {
+  MSA_NVTX_RANGE();
   msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, window, scale, in_dt);
   if (st != MSA_OK) return st;
   if (n < 1 || n > kMaxRows) return fail(MSA_ERR_INVALID_ARG, "n=%lld out of range", (long long)n);
@@ -255,6 +269,7 @@ msa_status msa_attn_fwd_rows(const void* q_rows, const void* k, const void* v, c
                              int64_t q_start, int64_t n_q, int64_t n, int Hq, int Hkv, int d,
                              int64_t window, int n_landmarks, float scale, msa_dtype in_dt,
                              msa_dtype out_dt, msa_stream_t stream) {
+  MSA_NVTX_RANGE();
   msa_status st = check_attn_common(q_rows, k, v, out_rows, lse, Hq, Hkv, d, window, scale,
                                     in_dt, 4);
   if (st != MSA_OK) return st;
@@ -301,6 +316,7 @@ msa_status msa_attn_fwd_band(const void* q, const void* k, const void* v, void* 
                              int64_t n, int Hq, int Hkv, int d, int64_t band_block,
                              int64_t band_half, float scale, msa_dtype in_dt, msa_dtype out_dt,
                              msa_stream_t stream) {
+  MSA_NVTX_RANGE();
   msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, 1, scale, in_dt);
   if (st != MSA_OK) return st;
   if (n < 1 || n > kMaxRows) return fail(MSA_ERR_INVALID_ARG, "n=%lld out of range", (long long)n);
@@ -347,6 +363,7 @@ static msa_status check_topk(int64_t n, int G, int top_k) {
 msa_status msa_block_select(const void* q, const void* k_lm, int32_t* sel, int32_t* cnt, int64_t n,
                             int Hq, int Hkv, int d, int64_t window, int n_landmarks, int top_k,
                             msa_dtype in_dt, msa_stream_t stream) {
+  MSA_NVTX_RANGE();
   if (!q || !k_lm || !sel || !cnt) return fail(MSA_ERR_INVALID_ARG, "null tensor pointer");
   if (!aligned16(q) || !aligned16(k_lm) || !aligned16(sel) || !aligned16(cnt))
     return fail(MSA_ERR_INVALID_ARG, "tensor pointer not 16-byte aligned");
@@ -368,6 +385,7 @@ msa_status msa_attn_fwd_select(const void* q, const void* k, const void* v, cons
                                int Hkv, int d, int64_t window, int n_landmarks, int top_k,
                                float scale, msa_dtype in_dt, msa_dtype out_dt,
                                msa_stream_t stream) {
+  MSA_NVTX_RANGE();
   msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, window, scale, in_dt);
   if (st != MSA_OK) return st;
   if (!sel || !cnt) return fail(MSA_ERR_INVALID_ARG, "null selection pointer");
@@ -428,6 +446,7 @@ msa_status msa_attn_fwd_topk(const void* q, const void* k, const void* v, void* 
                              int64_t n, int Hq, int Hkv, int d, int64_t window, int n_landmarks,
                              int top_k, float scale, msa_dtype in_dt, msa_dtype out_dt,
                              void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  MSA_NVTX_RANGE();
   msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, window, scale, in_dt);
   if (st != MSA_OK) return st;
   if (!valid_dtype(out_dt)) return fail(MSA_ERR_INVALID_ARG, "bad output dtype %d", (int)out_dt);
@@ -456,6 +475,7 @@ msa_status msa_attn_fwd_topk_noalloc(const void* q, const void* k, const void* v
                                      float* lse, int64_t n, int Hq, int Hkv, int d,
                                      int64_t window, int n_landmarks, int top_k, float scale,
                                      msa_dtype in_dt, msa_dtype out_dt, msa_stream_t stream) {
+  MSA_NVTX_RANGE();
   msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, window, scale, in_dt);
   if (st != MSA_OK) return st;
   if (!valid_dtype(out_dt)) return fail(MSA_ERR_INVALID_ARG, "bad output dtype %d", (int)out_dt);
@@ -532,6 +552,7 @@ msa_status msa_attn_fwd_global_rows(const void* q, const void* k, const void* v,
                                     int64_t n, int Hq, int Hkv, int d, float scale,
                                     msa_dtype in_dt, msa_dtype out_dt, void* workspace,
                                     size_t workspace_bytes, msa_stream_t stream) {
+  MSA_NVTX_RANGE();
   msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, 1, scale, in_dt);
   if (st != MSA_OK) return st;
   if (!rows || (reinterpret_cast<uintptr_t>(rows) & 7u) != 0)
@@ -762,6 +783,7 @@ msa_status msa_attn_bwd(const void* q, const void* k, const void* v, const void*
                         int64_t window, int n_landmarks, float scale, msa_dtype in_dt,
                         msa_dtype out_dt, msa_dtype grad_dt, void* workspace,
                         size_t workspace_bytes, msa_stream_t stream) {
+  MSA_NVTX_RANGE();
   return attn_bwd_impl(q, k, v, k_lm, v_lm, out, lse, dout, nullptr, 0, dq, dk, dv, n, Hq, Hkv,
                        d, window, n_landmarks, scale, in_dt, out_dt, grad_dt, workspace,
                        workspace_bytes, stream);
@@ -783,6 +805,7 @@ msa_status msa_attn_bwd_global_rows(const void* q, const void* k, const void* v,
                                     float scale, msa_dtype in_dt, msa_dtype out_dt,
                                     msa_dtype grad_dt, void* workspace, size_t workspace_bytes,
                                     msa_stream_t stream) {
+  MSA_NVTX_RANGE();
   if (!rows) return fail(MSA_ERR_INVALID_ARG, "null rows pointer");
   return attn_bwd_impl(q, k, v, k_lm, v_lm, out, lse, dout, rows, n_global, dq, dk, dv, n, Hq,
                        Hkv, d, window, n_landmarks, scale, in_dt, out_dt, grad_dt, workspace,
@@ -794,6 +817,7 @@ msa_status msa_attn_fwd_partial(const void* q, const void* k_chunk, const void* 
                                  int64_t n_kv, int64_t kv_start, int Hq, int Hkv, int d,
                                  int64_t window, float scale, msa_dtype in_dt,
                                  msa_stream_t stream) {
+  MSA_NVTX_RANGE();
   msa_status st =
       check_attn_common(q, k_chunk, v_chunk, out_part, lse_part, Hq, Hkv, d, window, scale, in_dt);
   if (st != MSA_OK) return st;
@@ -831,6 +855,7 @@ msa_status msa_attn_fwd_partial_merge(const void* q, const void* k_chunk, const 
                                        int64_t q_start, int64_t n_kv, int64_t kv_start, int Hq,
                                        int Hkv, int d, int64_t window, float scale,
                                        msa_dtype in_dt, msa_stream_t stream) {
+  MSA_NVTX_RANGE();
   msa_status st =
       check_attn_common(q, k_chunk, v_chunk, out_run, lse_run, Hq, Hkv, d, window, scale, in_dt);
   if (st != MSA_OK) return st;
@@ -929,6 +954,7 @@ msa_status msa_attn_fwd_host(const void* q, const void* k, const void* v, void* 
                              float scale, msa_dtype in_dt, msa_dtype out_dt, int64_t chunk_rows,
                              void* workspace, size_t workspace_bytes, msa_stream_t stream,
                              msa_stream_t copy_in, msa_stream_t copy_out) {
+  MSA_NVTX_RANGE();
   msa_status st = check_attn_common(q, k, v, out, lse, Hq, Hkv, d, window, scale, in_dt);
   if (st != MSA_OK) return st;
   if (n < 1 || n > kMaxRows) return fail(MSA_ERR_INVALID_ARG, "n=%lld out of range", (long long)n);
@@ -1071,6 +1097,7 @@ msa_status msa_attn_fwd_host(const void* q, const void* k, const void* v, void* 
 msa_status msa_lse_merge(const float* const* o_parts, const float* const* lse_parts, int n_parts,
                          void* out, float* lse, int64_t n, int Hq, int d, msa_dtype out_dt,
                          msa_stream_t stream) {
+  MSA_NVTX_RANGE();
   if (!o_parts || !lse_parts || !out || !lse)
     return fail(MSA_ERR_INVALID_ARG, "null array or output pointer");
   if (n_parts < 1 || n_parts > MSA_MAX_MERGE_PARTS)
@@ -1116,6 +1143,7 @@ int msa_attn_fwd_topk_uses_tensor_cores(int64_t n, int Hq, int Hkv, int d, int n
 }
 
 msa_status msa_device_status(int clear) {
+  MSA_NVTX_RANGE();
   int* ptr = nullptr;
   msa_status st = device_status_ptr(&ptr);
   if (st != MSA_OK) return st;

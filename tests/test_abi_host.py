@@ -411,3 +411,19 @@ def test_python_api_warns_on_cuda_core_bf16():
         api._check_tensor_cores(torch.zeros((4096, 8, 128), dtype=torch.bfloat16), 1, 16)
     with pytest.warns(api.CudaCorePathWarning, match="not a multiple of 128"):
         api._check_tensor_cores(torch.zeros((4096, 8, 128), dtype=torch.bfloat16), 1, 64)
+
+
+def test_every_entry_point_opens_an_nvtx_range():
+    """Each msa_status entry point of the C ABI opens an NVTX range named
+    after itself first thing, so profiler timelines group each call's
+    kernels under the call."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = open(os.path.join(root, "long_context_sparse_landmark_gb300", "csrc",
+                            "msa_api.cu")).read()
+    header = open(os.path.join(root, "include", "msa.h")).read()
+    declared = set(re.findall(r"^msa_status (msa_\w+)\(", header, re.M))
+    assert len(declared) >= 16
+    for name in sorted(declared):
+        m = re.search(r"^msa_status " + name + r"\([^{]*\{\n(.*)\n", src, re.M)
+        assert m, f"{name}: no definition"
+        assert m.group(1).strip() == "MSA_NVTX_RANGE();", f"{name} opens no NVTX range"
