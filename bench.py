@@ -274,15 +274,14 @@ def run_ring(wl, steps, warmup, dev, B, torch):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     for s in range(steps):
         step(evs[s])
-    f0 = torch.cuda.Event(enable_timing=True)
-    f1 = torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
+    fev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     for s in range(steps):
+        fev[s][0].record(stream)
         fused_step()
-    f1.record(stream)
+        fev[s][1].record(stream)
     torch.cuda.synchronize()
     assert B.device_status() == 0
-    fused_ms = f0.elapsed_time(f1) / steps
+    fused_ms = statistics.median(e[0].elapsed_time(e[1]) for e in fev)
     part_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
     merge_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
     # Required merge bytes: every lse_p, every O_p row with finite lse_p, output.
@@ -743,7 +742,7 @@ def main():
                                    / peaks["bf16_tflops"], 2),
             "steps": 20}
         wl1m = WORKLOADS["1m_70b_layer"]
-        r1 = run_window_landmark(wl1m, 3, 1, dev, B, torch)
+        r1 = run_window_landmark(wl1m, 5, 1, dev, B, torch)  # medians of 5 at 1M
         f1 = useful_flops(wl1m)
         also["1m_70b_layer"] = {
             "ms_per_step": round(r1["ms_per_step"], 3),
@@ -754,7 +753,7 @@ def main():
                                    / peaks["bf16_tflops"], 2),
             "pool_gbs": round((2 * wl1m.n * wl1m.Hkv * wl1m.d * 2 + 2 * wl1m.G * wl1m.Hkv
                                * wl1m.d * 2) / (r1["pool_ms"] * 1e-3) / 1e9, 1),
-            "steps": 3}
+            "steps": 5}
         wlb = WORKLOADS["band_128k"]
         bms = run_band(wlb, 3, 1, dev, B, torch)
         fb = band_flops(wlb)
@@ -809,7 +808,7 @@ def main():
                                                             / peaks["bf16_tflops"], 2),
                                      "launches_per_step": 9, "steps": 3}
         wlr = WORKLOADS["ring_128k"]
-        rr = run_ring(wlr, 3, 1, dev, B, torch)
+        rr = run_ring(wlr, 10, 1, dev, B, torch)  # medians of 10
         fr = useful_flops(wlr)
         also["ring_128k"] = {
             "partials_ms": round(rr["partials_ms"], 3), "merge_ms": round(rr["merge_ms"], 3),
@@ -819,7 +818,7 @@ def main():
                                     / peaks["hbm_gbs"], 4),
             "fused_rounds_ms": round(rr["fused_ms"], 3),
             "fused_rounds_tflops": round(fr / (rr["fused_ms"] * 1e-3) / 1e12, 2),
-            "steps": 3}
+            "steps": 10}
         line["also"] = also
 
     if not args.no_cpu and rank == 0:
