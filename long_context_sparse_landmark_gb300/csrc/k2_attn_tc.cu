@@ -35,11 +35,9 @@
 // the exponent base m is only raised when the row maximum exceeds it by more
 // than kTau (then O and l are rescaled in TMEM/registers), so p <= 2^kTau;
 // O/l and lse = (m + log2 l) ln 2 are exact for any base.  P enters the PV
-// MMA rounded to bf16; l sums the weights before rounding (packed f32x2
-// adds) plus, per tile, the rounding of the tile's largest weight, so a key
-// that dominates a row is normalised by exactly the weight its V row is
-// multiplied by (it then reproduces its V row without the bf16 rounding of
-// its weight) and the other keys' roundings enter l only as zero-mean noise.
+// MMA rounded to bf16 and l sums those same rounded values, so each output
+// row is an exactly normalised combination of V rows (a key that dominates
+// a row then reproduces its V row without the bf16 rounding of its weight).
 //
 // Every mbarrier wait is bounded (globaltimer); a wait that runs out sets a
 // CTA-wide abort flag and the device status word, all roles leave their
@@ -492,11 +490,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (need) m_used = m_new;
         const float mb = (m_used == -INFINITY) ? 0.f : m_used;
         // p = 2^(s*scale*log2e - m) two at a time (packed FMA), rounded to
-        // bf16 pairs for the PV MMA; the denominator adds the weights before
-        // rounding into two packed fp32 sums.
+        // bf16 pairs for the PV MMA; the denominator sums those same
+        // rounded weights (so O is normalised by exactly the weights it was
+        // built from), added to four fp32 partial sums as they are.
         const uint64_t c2 = ptx::f2(sl2, sl2);
         const uint64_t nb2 = ptx::f2(-mb, -mb);
-        uint64_t la = ptx::f2(0.f, 0.f), lb = ptx::f2(0.f, 0.f);
+        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t pk[16];
@@ -506,25 +505,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 ptx::fma2(ptx::f2(s[cc * 32 + 2 * e], s[cc * 32 + 2 * e + 1]), c2, nb2);
             float x0, x1;
             ptx::f2_split(x, x0, x1);
-            const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-            pk[e] = ptx::pack_bf16x2(p0, p1);
+            pk[e] = ptx::pack_bf16x2(ptx::ex2(x0), ptx::ex2(x1));
             if (e & 1)
-              lb = ptx::add2(lb, ptx::f2(p0, p1));
+              ptx::acc_bf16x2(l2, l3, pk[e]);
             else
-              la = ptx::add2(la, ptx::f2(p0, p1));
+              ptx::acc_bf16x2(l0, l1, pk[e]);
           }
           ptx::tmem_st16(tS + cc * 16, pk);
         }
-        float l0, l1, l2, l3;
-        ptx::f2_split(la, l0, l1);
-        ptx::f2_split(lb, l2, l3);
-        // The sums above take the weights before their bf16 rounding; the
-        // tile's largest weight (computed as in the loop: same FMA, same ex2)
-        // enters with its rounding, so a key that dominates the row is
-        // normalised by exactly the weight its V row is multiplied by.
-        const float pm = ptx::ex2(fmaf(mx, sl2, -mb));
-        const float pm_r = __uint_as_float(ptx::pack_bf16x2(pm, 0.f) << 16);
-        l += ((l0 + l1) + (l2 + l3)) + (pm_r - pm);
+        l += (l0 + l1) + (l2 + l3);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();

@@ -487,11 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
           if (need) m_used = m_new;
           const float mb = (m_used == -INFINITY) ? 0.f : m_used;
           // p = 2^(s*scale*log2e - m), rounded to bf16 pairs for the PV MMA;
-          // the denominator adds the weights before rounding into two packed
-          // fp32 sums.
+          // the denominator sums those same rounded weights.
           const uint64_t c2 = ptx::f2(sl2, sl2);
           const uint64_t nb2 = ptx::f2(-mb, -mb);
-          uint64_t la = ptx::f2(0.f, 0.f), lb = ptx::f2(0.f, 0.f);
+          float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t pk[16];
@@ -501,25 +500,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
                   ptx::fma2(ptx::f2(s[cc * 32 + 2 * e], s[cc * 32 + 2 * e + 1]), c2, nb2);
               float x0, x1;
               ptx::f2_split(x, x0, x1);
-              const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-              pk[e] = ptx::pack_bf16x2(p0, p1);
+              pk[e] = ptx::pack_bf16x2(ptx::ex2(x0), ptx::ex2(x1));
               if (e & 1)
-                lb = ptx::add2(lb, ptx::f2(p0, p1));
+                ptx::acc_bf16x2(l2, l3, pk[e]);
               else
-                la = ptx::add2(la, ptx::f2(p0, p1));
+                ptx::acc_bf16x2(l0, l1, pk[e]);
             }
             ptx::tmem_st16(tS + cc * 16, pk);
           }
-          float l0, l1, l2, l3;
-          ptx::f2_split(la, l0, l1);
-          ptx::f2_split(lb, l2, l3);
-          // The sums above take the weights before their bf16 rounding; the
-          // tile's largest weight (computed as in the loop: same FMA, same ex2)
-          // enters with its rounding, so a key that dominates the row is
-          // normalised by exactly the weight its V row is multiplied by.
-          const float pm = ptx::ex2(fmaf(mx, sl2, -mb));
-          const float pm_r = __uint_as_float(ptx::pack_bf16x2(pm, 0.f) << 16);
-          l += ((l0 + l1) + (l2 + l3)) + (pm_r - pm);
+          l += (l0 + l1) + (l2 + l3);
           ptx::tmem_wait_st();
         }
         ptx::tc_fence_before();
