@@ -25,7 +25,10 @@
 // peer also watches, and both CTAs drain and free their tensor memory.
 #include <cuda.h>
 #include <math.h>
+#include <stdint.h>
 #include <string.h>
+
+#include <mutex>
 
 #include "msa_common.cuh"
 #include "tc_pair.cuh"
@@ -71,7 +74,9 @@ enum {
   B_ACC = 13,      // both: dQ final
   B_CLEAN = 14,    // both: every MMA done
   B_SFREE = 15,    // lead: every elementwise warp has read S (8 x 2)
-  kNumBars = 16
+  B_QE = 16,       // both: the unit's last S MMA done (Q, dO free)
+  B_DQFREE = 17,   // lead: every elementwise warp has read the unit's dQ (8 x 2)
+  kNumBars = 18
 };
 constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
 constexpr int kOffAbort = kOffTmemSlot + 8;
@@ -95,6 +100,7 @@ struct DqPairParams {
   void* dq;                         // [n, Hq, d]
   int64_t n, n_pad, window, block;
   int Hq, Hkv, G, group, grad_bf16;
+  int n_tiles, units;               // query tiles; units = n_tiles x Hq / 2
   float scale, scale_log2;
   int* status;
   uint64_t wait_ns;
@@ -121,6 +127,32 @@ __device__ __forceinline__ void store_row(void* base, int64_t off, const float (
   }
 }
 
+// One work unit: a 128-row query tile of one head pair.  Units run from the
+// last query tile down (the longest windows first), head pairs outermost.
+// T depends on the query tile alone, so both CTAs of a pair run as many
+// tiles.
+struct DqUnit {
+  int64_t qr0;
+  int h, c, n_lm_tiles, kt_lo, T;
+};
+
+__device__ __forceinline__ DqUnit decode_dq_unit(const DqPairParams& p, int u, uint32_t rank) {
+  DqUnit w;
+  const int qt = p.n_tiles - 1 - (u % p.n_tiles);
+  const int hp = u / p.n_tiles;
+  w.qr0 = static_cast<int64_t>(qt) * kT;
+  w.h = 2 * hp + static_cast<int>(rank);
+  w.c = w.h / p.group;  // the same for both CTAs: the group size is even
+  // Key tiles of the query tile (the same for both heads): landmark tiles,
+  // then the window tiles of its rows.
+  const int64_t q_last = min64(w.qr0 + kT, p.n) - 1;
+  const int64_t n_lm = visible_landmarks(q_last, p.window, p.block, p.G);
+  w.n_lm_tiles = static_cast<int>((n_lm + kT - 1) / kT);
+  w.kt_lo = static_cast<int>(max64(w.qr0 - p.window + 1, 0) / kT);
+  w.T = w.n_lm_tiles + static_cast<int>(q_last / kT) - w.kt_lo + 1;
+  return w;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_pair_kernel(const __grid_constant__ DqPairParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -134,20 +166,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = pair::cta_rank();
-  const int64_t qr0 = static_cast<int64_t>(blockIdx.x >> 1) * kT;
-  const int h = 2 * static_cast<int>(blockIdx.y) + static_cast<int>(rank);
-  const int c = h / p.group;  // the same for both CTAs: the group size is even
-  // Key tiles of the query tile (the same for both heads): landmark tiles,
-  // then the window tiles of its rows.
-  const int64_t q_last = min64(qr0 + kT, p.n) - 1;
-  const int64_t n_lm = visible_landmarks(q_last, p.window, p.block, p.G);
-  const int n_lm_tiles = static_cast<int>((n_lm + kT - 1) / kT);
-  const int kt_lo = static_cast<int>(max64(qr0 - p.window + 1, 0) / kT);
-  const int T = n_lm_tiles + static_cast<int>(q_last / kT) - kt_lo + 1;
+  const int cid = static_cast<int>(blockIdx.x >> 1);
+  const int n_clusters = static_cast<int>(gridDim.x >> 1);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i)
-      ptx::mbar_init(bar(i), (i == B_EF || i == B_SFREE) ? 2 * kEwWarps : 1);
+      ptx::mbar_init(bar(i), (i == B_EF || i == B_SFREE || i == B_DQFREE) ? 2 * kEwWarps : 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::fence_async_shared();
@@ -167,42 +191,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      if (rank == 0) ptx::mbar_arrive_expect_tx(bar(B_FIX), 2 * 2 * kTile);
-      for (int ch = 0; ch < 2; ++ch) {
-        (void)MSA_TMA_OK(ch * 64, h, qr0, kD, p.Hq, p.n, kT, p.status);
-        pair::tma_load_3d(sb + kOffQ + ch * kChunk, &p.tm_q, lead(B_FIX), ch * 64, h,
-                          static_cast<int>(qr0));
-        pair::tma_load_3d(sb + kOffDo + ch * kChunk, &p.tm_do, lead(B_FIX), ch * 64, h,
-                          static_cast<int>(qr0));
-      }
       bool ok = true;
-      int nk = 0, nv = 0;
-      for (int t = 0; ok && t < T; ++t) {
-        const bool lm = t < n_lm_tiles;
-        const int row = lm ? t * kT : (kt_lo + t - n_lm_tiles) * kT;
-        (void)MSA_TMA_OK(0, c, row, kD, p.Hkv, lm ? p.G : p.n, kT, p.status);
-        const int sk = t % kKStages, sv = t % kVStages;
-        if (t >= kKStages &&
-            !(ok = wait_pair(bar(B_EMPTYK0 + sk), ((t / kKStages) - 1) & 1, ctl, kBackoffNs)))
-          break;
-        if (rank == 0) ptx::mbar_arrive_expect_tx(bar(B_FULLK0 + sk), 2 * kKStage);
-        const uint32_t kdst = sb + kOffK + sk * kKStage;
-        for (int ch = 0; ch < 2; ++ch)  // key rows 64 rank .. + 64, all columns
-          pair::tma_load_3d(kdst + ch * kHalfChunk, lm ? &p.tm_klm64 : &p.tm_k64,
-                            lead(B_FULLK0 + sk), ch * 64, c, row + 64 * static_cast<int>(rank));
-        // all 128 keys, columns 64 rank .. + 64
-        pair::tma_load_3d(kdst + kRowsHalf, lm ? &p.tm_klm128 : &p.tm_k128, lead(B_FULLK0 + sk),
-                          64 * static_cast<int>(rank), c, row);
-        nk = t + 1;
-        if (t >= kVStages &&
-            !(ok = wait_pair(bar(B_EMPTYV0 + sv), ((t / kVStages) - 1) & 1, ctl, kBackoffNs)))
-          break;
-        if (rank == 0) ptx::mbar_arrive_expect_tx(bar(B_FULLV0 + sv), 2 * kVStage);
-        for (int ch = 0; ch < 2; ++ch)
-          pair::tma_load_3d(sb + kOffV + sv * kVStage + ch * kHalfChunk,
-                            lm ? &p.tm_vlm64 : &p.tm_v64, lead(B_FULLV0 + sv), ch * 64, c,
-                            row + 64 * static_cast<int>(rank));
-        nv = t + 1;
+      uint32_t g = 0;                  // key tiles this cluster has started
+      int nfix = 0, nk = 0, nv = 0;    // Q/dO, K and V fills issued
+      for (int u = cid; ok && u < p.units; u += n_clusters) {
+        const DqUnit w = decode_dq_unit(p, u, rank);
+        // Q and dO of the previous unit are free once its last S MMA is done.
+        if (nfix >= 1 && !(ok = wait_pair(bar(B_QE), (nfix - 1) & 1, ctl, kBackoffNs))) break;
+        if (rank == 0) ptx::mbar_arrive_expect_tx(bar(B_FIX), 2 * 2 * kTile);
+        for (int ch = 0; ch < 2; ++ch) {
+          (void)MSA_TMA_OK(ch * 64, w.h, w.qr0, kD, p.Hq, p.n, kT, p.status);
+          pair::tma_load_3d(sb + kOffQ + ch * kChunk, &p.tm_q, lead(B_FIX), ch * 64, w.h,
+                            static_cast<int>(w.qr0));
+          pair::tma_load_3d(sb + kOffDo + ch * kChunk, &p.tm_do, lead(B_FIX), ch * 64, w.h,
+                            static_cast<int>(w.qr0));
+        }
+        ++nfix;
+        for (int t = 0; t < w.T; ++t, ++g) {
+          const bool lm = t < w.n_lm_tiles;
+          const int row = lm ? t * kT : (w.kt_lo + t - w.n_lm_tiles) * kT;
+          (void)MSA_TMA_OK(0, w.c, row, kD, p.Hkv, lm ? p.G : p.n, kT, p.status);
+          const int sk = static_cast<int>(g % kKStages), sv = static_cast<int>(g % kVStages);
+          if (g >= kKStages &&
+              !(ok = wait_pair(bar(B_EMPTYK0 + sk), ((g / kKStages) - 1) & 1, ctl, kBackoffNs)))
+            break;
+          if (rank == 0) ptx::mbar_arrive_expect_tx(bar(B_FULLK0 + sk), 2 * kKStage);
+          const uint32_t kdst = sb + kOffK + sk * kKStage;
+          for (int ch = 0; ch < 2; ++ch)  // key rows 64 rank .. + 64, all columns
+            pair::tma_load_3d(kdst + ch * kHalfChunk, lm ? &p.tm_klm64 : &p.tm_k64,
+                              lead(B_FULLK0 + sk), ch * 64, w.c,
+                              row + 64 * static_cast<int>(rank));
+          // all 128 keys, columns 64 rank .. + 64
+          pair::tma_load_3d(kdst + kRowsHalf, lm ? &p.tm_klm128 : &p.tm_k128,
+                            lead(B_FULLK0 + sk), 64 * static_cast<int>(rank), w.c, row);
+          nk = static_cast<int>(g) + 1;
+          if (g >= kVStages &&
+              !(ok = wait_pair(bar(B_EMPTYV0 + sv), ((g / kVStages) - 1) & 1, ctl, kBackoffNs)))
+            break;
+          if (rank == 0) ptx::mbar_arrive_expect_tx(bar(B_FULLV0 + sv), 2 * kVStage);
+          for (int ch = 0; ch < 2; ++ch)
+            pair::tma_load_3d(sb + kOffV + sv * kVStage + ch * kHalfChunk,
+                              lm ? &p.tm_vlm64 : &p.tm_v64, lead(B_FULLV0 + sv), ch * 64, w.c,
+                              row + 64 * static_cast<int>(rank));
+          nv = static_cast<int>(g) + 1;
+        }
       }
       // Drain (lead): an armed phase completes once both CTAs' bytes have
       // landed.  After an abort the peer may not have issued its copies of
@@ -210,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the drain then waits 50 ms per barrier.
       if (rank == 0) {
         const uint64_t lim = *abort_flag ? 50000000ull : kDrainLimitNs;
-        drain_for(bar(B_FIX), 0, p.status, lim);
+        if (nfix >= 1) drain_for(bar(B_FIX), (nfix - 1) & 1, p.status, lim);
         for (int st = 0; st < kKStages; ++st) {
           const int last = nk - 1 - ((nk - 1 - st) % kKStages + kKStages) % kKStages;
           if (last >= 0) drain_for(bar(B_FULLK0 + st), (last / kKStages) & 1, p.status, lim);
@@ -236,37 +268,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto scores = [&](uint32_t d, uint32_t a_lo, uint32_t b_lo) {
         pair::mma_ss_x8<(kChunk >> 4), (kHalfChunk >> 4)>(d, a_lo, b_lo, kIdescS, 0u);
       };
-      bool ok = wait_pair_w(bar(B_FIX), 0, ctl) && wait_pair_w(bar(B_FULLK0), 0, ctl) &&
-                wait_pair_w(bar(B_FULLV0), 0, ctl);
-      if (ok) {
+      // dP(g) then S(g) of key tile g.  S's columns are free once every
+      // elementwise warp has read S(g - 1); dP(g) overwrites dS(g - 2), which
+      // the dQ MMA of tile g - 2, issued earlier by this warp, has read.
+      auto tile_scores = [&](uint32_t gg) -> bool {
+        const int sv = static_cast<int>(gg % kVStages), sk = static_cast<int>(gg % kKStages);
+        if (!wait_pair_w(bar(B_FULLV0 + sv), (gg / kVStages) & 1, ctl)) return false;
         ptx::tc_fence_after();
-        scores(tmem + col_p(0), do_lo, v_lo);  // dP = dO V^T
-        pair::commit_both(bar(B_EMPTYV0));
-        scores(tmem + kColS, q_lo, k_lo);      // S = Q K^T
+        scores(tmem + col_p(static_cast<int>(gg)), do_lo, v_lo + sv * (kVStage >> 4));
+        pair::commit_both(bar(B_EMPTYV0 + sv));  // V(gg) consumed
+        if (!wait_pair_w(bar(B_FULLK0 + sk), (gg / kKStages) & 1, ctl)) return false;
+        if (gg >= 1 && !wait_pair_w(bar(B_SFREE), (gg - 1) & 1, ctl)) return false;
+        ptx::tc_fence_after();
+        scores(tmem + kColS, q_lo, k_lo + sk * (kKStage >> 4));
         pair::commit_both(bar(B_SF));
-      }
-      for (int t = 0; ok && t < T; ++t) {
-        if (t + 1 < T) {
-          const int sv = (t + 1) % kVStages;
-          if (!(ok = wait_pair_w(bar(B_FULLV0 + sv), ((t + 1) / kVStages) & 1, ctl))) break;
+        return true;
+      };
+      bool ok = true;
+      uint32_t g = 0, ul = 0;  // key tiles / units this cluster has processed
+      for (int u = cid; ok && u < p.units; u += n_clusters, ++ul) {
+        const int T = decode_dq_unit(p, u, 0).T;
+        if (!(ok = wait_pair_w(bar(B_FIX), ul & 1, ctl))) break;
+        if (!(ok = tile_scores(g))) break;
+        if (T == 1) pair::commit_both(bar(B_QE));  // the unit's last S MMA
+        for (int t = 0; ok && t < T; ++t) {
+          const uint32_t gt = g + t;
+          if (t + 1 < T) {
+            if (!(ok = tile_scores(gt + 1))) break;
+            if (t + 2 == T) pair::commit_both(bar(B_QE));  // the unit's last S MMA
+          }
+          if (!(ok = wait_pair_w(bar(B_EF), gt & 1, ctl))) break;
+          // The first dQ MMA of a unit overwrites the accumulator that the
+          // previous unit's epilogue reads.
+          if (t == 0 && ul >= 1 && !(ok = wait_pair_w(bar(B_DQFREE), (ul - 1) & 1, ctl))) break;
           ptx::tc_fence_after();
-          scores(tmem + col_p(t + 1), do_lo, v_lo + sv * (kVStage >> 4));
-          pair::commit_both(bar(B_EMPTYV0 + sv));  // V(t+1) consumed
-          const int sk = (t + 1) % kKStages;
-          if (!(ok = wait_pair_w(bar(B_FULLK0 + sk), ((t + 1) / kKStages) & 1, ctl))) break;
-          if (!(ok = wait_pair_w(bar(B_SFREE), t & 1, ctl))) break;
-          ptx::tc_fence_after();
-          scores(tmem + kColS, q_lo, k_lo + sk * (kKStage >> 4));
-          pair::commit_both(bar(B_SF));
+          const int sk = static_cast<int>(gt % kKStages);
+          pair::mma_ts_chunked_x8(tmem + kColQ, tmem + col_p(static_cast<int>(gt)),
+                                  k_mn + sk * (kKStage >> 4), kIdescG, t > 0 ? 1u : 0u);
+          pair::commit_both(bar(B_EMPTYK0 + sk));  // K(gt) consumed
         }
-        if (!(ok = wait_pair_w(bar(B_EF), t & 1, ctl))) break;
-        ptx::tc_fence_after();
-        const int sk = t % kKStages;
-        pair::mma_ts_chunked_x8(tmem + kColQ, tmem + col_p(t), k_mn + sk * (kKStage >> 4),
-                                kIdescG, t > 0 ? 1u : 0u);
-        pair::commit_both(bar(B_EMPTYK0 + sk));  // K(t) consumed
+        if (!ok) break;
+        pair::commit_both(bar(B_ACC));
+        g += T;
       }
-      if (ok) pair::commit_both(bar(B_ACC));
       pair::commit_both(bar(B_CLEAN));
     }
   } else if (warp < kEwWarps) {
@@ -274,91 +318,102 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;  // TMEM lanes (rows) 32 quarter ..
     const int cp = warp >> 2;      // key columns [64 cp, 64 cp + 64) of each tile
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int64_t i = qr0 + quarter * 32 + lane;  // query row
-    const int64_t st = static_cast<int64_t>(h) * p.n_pad + i;
-    const bool st_ok = MSA_IN_RANGE(st, 1, static_cast<int64_t>(p.Hq) * p.n_pad, p.status);
-    const bool row_ok = i < p.n && st_ok;
-    const float nL2 = st_ok ? p.L2[st] : -INFINITY;
-    const float nD = st_ok ? p.D[st] : 0.f;
     const uint64_t c2 = ptx::f2(p.scale_log2, p.scale_log2);
-    const uint64_t nL22 = ptx::f2(nL2, nL2);
-    const uint64_t nD2 = ptx::f2(nD, nD);
-    const int64_t my_lm = visible_landmarks(i, p.window, p.block, p.G);
-    const int64_t my_lo = max64(i - p.window + 1, 0);
-    const uint32_t ef = lead(B_EF), sfree = lead(B_SFREE);
+    const uint32_t ef = lead(B_EF), sfree = lead(B_SFREE), dqfree = lead(B_DQFREE);
     bool ok = true;
-    for (int t = 0; ok && t < T; ++t) {
-      int64_t lo, hi;  // valid columns [lo, hi) of this key tile for row i
-      if (t < n_lm_tiles) {
-        lo = 0;
-        hi = my_lm - static_cast<int64_t>(t) * kT;
-      } else {
-        const int64_t kb = static_cast<int64_t>(kt_lo + t - n_lm_tiles) * kT;
-        lo = my_lo - kb;
-        hi = i - kb + 1;
-      }
-      if (!row_ok) hi = lo;
-      if (!(ok = wait_pair_w(bar(B_SF), t & 1, ctl))) break;
-      ptx::tc_fence_after();
-      const int lo_c = static_cast<int>(max64(0, min64(kT, lo)));
-      const int hi_c = static_cast<int>(max64(0, min64(kT, hi)));
-      const bool full = lo_c == 0 && hi_c == kT;
-      const uint32_t tp = tl + col_p(t);
-      // This warp's two 32-column chunks of S and dP, all read before S is
-      // released for the next tile's S MMAs.
-      float s[2][32], dp[2][32];
+    uint32_t g = 0, ul = 0;
+    for (int u = cid; ok && u < p.units; u += n_clusters, ++ul) {
+      const DqUnit w = decode_dq_unit(p, u, rank);
+      const int64_t i = w.qr0 + quarter * 32 + lane;  // query row
+      const int64_t st = static_cast<int64_t>(w.h) * p.n_pad + i;
+      const bool st_ok = MSA_IN_RANGE(st, 1, static_cast<int64_t>(p.Hq) * p.n_pad, p.status);
+      const bool row_ok = i < p.n && st_ok;
+      const float nL2 = st_ok ? p.L2[st] : -INFINITY;
+      const float nD = st_ok ? p.D[st] : 0.f;
+      const uint64_t nL22 = ptx::f2(nL2, nL2);
+      const uint64_t nD2 = ptx::f2(nD, nD);
+      const int64_t my_lm = visible_landmarks(i, p.window, p.block, p.G);
+      const int64_t my_lo = max64(i - p.window + 1, 0);
+      for (int t = 0; ok && t < w.T; ++t) {
+        const uint32_t gt = g + t;
+        int64_t lo, hi;  // valid columns [lo, hi) of this key tile for row i
+        if (t < w.n_lm_tiles) {
+          lo = 0;
+          hi = my_lm - static_cast<int64_t>(t) * kT;
+        } else {
+          const int64_t kb = static_cast<int64_t>(w.kt_lo + t - w.n_lm_tiles) * kT;
+          lo = my_lo - kb;
+          hi = i - kb + 1;
+        }
+        if (!row_ok) hi = lo;
+        if (!(ok = wait_pair_w(bar(B_SF), gt & 1, ctl))) break;
+        ptx::tc_fence_after();
+        const int lo_c = static_cast<int>(max64(0, min64(kT, lo)));
+        const int hi_c = static_cast<int>(max64(0, min64(kT, hi)));
+        const bool full = lo_c == 0 && hi_c == kT;
+        const uint32_t tp = tl + col_p(static_cast<int>(gt));
+        // This warp's two 32-column chunks of S and dP, all read before S is
+        // released for the next tile's S MMAs.
+        float s[2][32], dp[2][32];
 #pragma unroll
-      for (int ci = 0; ci < 2; ++ci) {
-        ptx::tmem_ld32(tl + kColS + (2 * cp + ci) * 32, s[ci]);
-        ptx::tmem_ld32(tp + (2 * cp + ci) * 32, dp[ci]);
+        for (int ci = 0; ci < 2; ++ci) {
+          ptx::tmem_ld32(tl + kColS + (2 * cp + ci) * 32, s[ci]);
+          ptx::tmem_ld32(tp + (2 * cp + ci) * 32, dp[ci]);
+        }
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        __syncwarp();
+        pair::arrive_cluster_w(sfree);
+#pragma unroll
+        for (int ci = 0; ci < 2; ++ci) {
+          const int cc = 2 * cp + ci;  // 32-column chunk
+          if (!full) {  // masked columns: weight 0
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int col = cc * 32 + e;
+              s[ci][e] = (col >= lo_c && col < hi_c) ? s[ci][e] : -INFINITY;
+            }
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            // p = 2^(s scale log2e - lse log2e), dS = p (dP - D)
+            float x0, x1;
+            ptx::f2_split(ptx::fma2(ptx::f2(s[ci][2 * e], s[ci][2 * e + 1]), c2, nL22), x0, x1);
+            const uint64_t pr = ptx::f2(ptx::ex2(x0), ptx::ex2(x1));
+            float d0, d1;
+            ptx::f2_split(
+                ptx::mul2(pr, ptx::add2(ptx::f2(dp[ci][2 * e], dp[ci][2 * e + 1]), nD2)), d0,
+                d1);
+            pk[e] = ptx::pack_bf16x2(d0, d1);
+          }
+          ptx::tmem_st16(tp + cc * 32, pk);  // dS over dP columns this warp has read
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        pair::arrive_cluster_w(ef);
       }
+      if (ok) ok = wait_pair_w(bar(B_ACC), ul & 1, ctl);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      // This warp's 64 of the 128 columns, read before the next unit's first
+      // dQ MMA may overwrite them; the global stores follow.
+      float o[2][32];
+      ptx::tmem_ld32(tl + kColQ + (2 * cp) * 32, o[0]);
+      ptx::tmem_ld32(tl + kColQ + (2 * cp + 1) * 32, o[1]);
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       __syncwarp();
-      pair::arrive_cluster_w(sfree);
-#pragma unroll
-      for (int ci = 0; ci < 2; ++ci) {
-        const int cc = 2 * cp + ci;  // 32-column chunk
-        if (!full) {  // masked columns: weight 0
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int col = cc * 32 + e;
-            s[ci][e] = (col >= lo_c && col < hi_c) ? s[ci][e] : -INFINITY;
-          }
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          // p = 2^(s scale log2e - lse log2e), dS = p (dP - D)
-          float x0, x1;
-          ptx::f2_split(ptx::fma2(ptx::f2(s[ci][2 * e], s[ci][2 * e + 1]), c2, nL22), x0, x1);
-          const uint64_t pr = ptx::f2(ptx::ex2(x0), ptx::ex2(x1));
-          float d0, d1;
-          ptx::f2_split(
-              ptx::mul2(pr, ptx::add2(ptx::f2(dp[ci][2 * e], dp[ci][2 * e + 1]), nD2)), d0, d1);
-          pk[e] = ptx::pack_bf16x2(d0, d1);
-        }
-        ptx::tmem_st16(tp + cc * 32, pk);  // dS over dP columns this warp has read
-      }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      pair::arrive_cluster_w(ef);
-    }
-    if (ok) ok = wait_pair_w(bar(B_ACC), 0, ctl);
-    if (ok) {
-      ptx::tc_fence_after();
-      const int64_t off = (i * p.Hq + h) * static_cast<int64_t>(kD);
+      pair::arrive_cluster_w(dqfree);
+      const int64_t off = (i * p.Hq + w.h) * static_cast<int64_t>(kD);
       const bool out_ok =
           !row_ok || MSA_IN_RANGE(off, kD, p.n * p.Hq * static_cast<int64_t>(kD), p.status);
-#pragma unroll 1
-      for (int ci = 0; ci < 2; ++ci) {  // this warp's 64 of the 128 columns
-        const int cc = 2 * cp + ci;
-        float o[32];
-        ptx::tmem_ld32(tl + kColQ + cc * 32, o);
-        ptx::tmem_wait_ld();
-        if (row_ok && out_ok) store_row(p.dq, off + cc * 32, o, p.scale, p.grad_bf16);
+      if (row_ok && out_ok) {
+        store_row(p.dq, off + (2 * cp) * 32, o[0], p.scale, p.grad_bf16);
+        store_row(p.dq, off + (2 * cp + 1) * 32, o[1], p.scale, p.grad_bf16);
       }
+      g += w.T;
     }
   }
 
@@ -372,6 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     pair::tmem_dealloc(tmem, 512);
   }
 }
+
+constexpr int kMaxDev = 64;
+std::mutex g_occ_mu;
+int g_max_clusters[kMaxDev] = {};
 
 }  // namespace
 
@@ -427,18 +486,54 @@ cudaError_t launch_bwd_dq_pair(const BwdArgs& a, cudaStream_t s, const char** wh
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t n_tiles = (a.n + kT - 1) / kT;
+  const int64_t units = n_tiles * (a.Hq / 2);
+  if (units > INT32_MAX) {
+    *why = "too many query tiles x head pairs for the dQ pair kernel";
+    return cudaErrorInvalidValue;
+  }
+  p.n_tiles = static_cast<int>(n_tiles);
+  p.units = static_cast<int>(units);
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) {
+    *why = "device ordinal out of range";
+    return cudaErrorInvalidDevice;
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * n_tiles), static_cast<unsigned>(a.Hq / 2));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // Persistent: one cluster per CTA pair that fits at once (a property of
+  // the device, cached), each looping over units.
+  int max_clusters = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    max_clusters = g_max_clusters[dev];
+  }
+  if (max_clusters == 0) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+    e = cudaOccupancyMaxActiveClusters(&max_clusters, bwd_dq_pair_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (max_clusters < 1) {
+      *why = "no CTA pair of the dQ kernel fits on this device";
+      return cudaErrorInvalidConfiguration;
+    }
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    g_max_clusters[dev] = max_clusters;
+  }
+  const int64_t clusters = units < max_clusters ? units : max_clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
   e = cudaLaunchKernelEx(&cfg, bwd_dq_pair_kernel, p);
   if (e != cudaSuccess) return e;
   return cudaPeekAtLastError();
