@@ -84,6 +84,36 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* desc, uint
 }
 
 
+// 3-D tiled tensor copy shared -> global in the issuing thread's bulk
+// async-group; elements outside the tensor are not written.  The thread's
+// shared-memory writes must be made visible to the async proxy first
+// (fence_async_shared), and the source may be reused once bulk_wait_read
+// returns.
+__device__ __forceinline__ void tma_store_3d(const void* desc, uint32_t src, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(desc)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The issuing thread's committed bulk stores have read their sources.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// The issuing thread's committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
 // Prefetch a 3-D tile of a tensor map into L2 (no shared memory written).
 __device__ __forceinline__ void tma_prefetch_3d(const void* desc, int x, int y, int z) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
