@@ -476,21 +476,32 @@ enum {
   DQ_FULLV0 = 7,   // V stage s landed (7, 8)
   DQ_EMPTYV0 = 9,  // V stage s consumed (9, 10)
   DQ_SF = 11,      // S and dP of a tile computed
-  DQ_EF = 12,      // dS of a tile written, one arrival per elementwise warp
+  DQ_EF = 12,      // dS of an even tile written, one arrival per elementwise warp
   DQ_ACC = 13,     // dQ final
   DQ_CLEAN = 14,
   DQ_SFREE = 15,   // every elementwise warp has read the tile's S
-  kDqNumBars = 16
+  DQ_EF1 = 16,     // dS of an odd tile written (see dq_ef)
+  kDqNumBars = 17
 };
 constexpr int kDqOffTmemSlot = kDqOffBar + 8 * kDqNumBars;
 constexpr int kDqOffAbort = kDqOffTmemSlot + 8;
 constexpr int kDqSmemBytes = kDqOffAbort + 8 + 1024;
 static_assert(kDqSmemBytes <= 227 * 1024, "dQ kernel shared memory");
 
+// The "dS written" barrier of tile t, and the phase to wait for.  Tiles
+// alternate between two barriers: S(t + 1) needs only every warp's read of
+// S(t), so a fast warp may finish tile t + 1 before a slow one has written
+// dS(t); with one barrier its arrival could complete tile t's phase.  Tile
+// t + 2 needs every warp's read of S(t + 1), which follows its tile-t
+// arrival, so each barrier's phase counts arrivals of one tile only.
+__device__ __forceinline__ int dq_ef(int t) { return (t & 1) ? DQ_EF1 : DQ_EF; }
+__device__ __forceinline__ uint32_t dq_ef_phase(int t) { return (static_cast<uint32_t>(t) >> 1) & 1; }
+
 __device__ __forceinline__ uint32_t dq_setup(uint8_t* smem, uint32_t sb, int warp) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDqNumBars; ++i)
-      ptx::mbar_init(sb + kDqOffBar + 8 * i, (i == DQ_EF || i == DQ_SFREE) ? kEwWarps : 1);
+      ptx::mbar_init(sb + kDqOffBar + 8 * i,
+                     (i == DQ_EF || i == DQ_EF1 || i == DQ_SFREE) ? kEwWarps : 1);
     *reinterpret_cast<volatile int*>(smem + kDqOffAbort) = 0;
     ptx::fence_mbar_init();
     ptx::fence_async_shared();
@@ -603,7 +614,7 @@ __device__ __forceinline__ bool dq_pipeline(uint32_t sb, uint32_t tmem, int iter
       mma_scores_full(tmem + kDqColS, q_lo, k_lo + sk * kTileLo);
       ptx::commit_w(bar(DQ_SF));
     }
-    if (!(ok = wait_w(bar(DQ_EF), t & 1, ctl))) break;
+    if (!(ok = wait_w(bar(dq_ef(t)), dq_ef_phase(t), ctl))) break;
     ptx::tc_fence_after();
     const int sk = t % kDqKStages;
     const uint32_t a = tmem + dq_col_p(t);
@@ -745,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_tc_kernel(const __grid_con
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(DQ_EF));
+      if (lane == 0) ptx::mbar_arrive(bar(dq_ef(t)));
     }
     if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(DQ_ACC), 0, ctl));
     if (ok) {

@@ -60,7 +60,11 @@ constexpr int kOffQ = 0;
 constexpr int kOffDo = kTile;
 constexpr int kOffK = 2 * kTile;
 constexpr int kOffV = kOffK + kKStages * kKStage;
-constexpr int kOffBar = kOffV + kVStages * kVStage;
+// bf16 dQ leaves through shared memory: per elementwise warp its 32 rows x
+// 64 columns (one 128-byte swizzle span), stored by one bulk tensor copy.
+constexpr int kOutStageBytes = 32 * 128;
+constexpr int kOffOut = kOffV + kVStages * kVStage;
+constexpr int kOffBar = kOffOut + kEwWarps * kOutStageBytes;
 // Barriers: "lead" collects bytes or arrivals of both CTAs on the lead's
 // copy; "both" is completed on each CTA's copy by a multicast commit.
 enum {
@@ -70,13 +74,14 @@ enum {
   B_FULLV0 = 7,    // lead: V stage landed (7, 8)
   B_EMPTYV0 = 9,   // both: V stage consumed (9, 10)
   B_SF = 11,       // both: S and dP of a tile computed
-  B_EF = 12,       // lead: dS of a tile written (8 warps x 2 CTAs)
+  B_EF = 12,       // lead: dS of an even key tile written (8 warps x 2 CTAs)
   B_ACC = 13,      // both: dQ final
   B_CLEAN = 14,    // both: every MMA done
   B_SFREE = 15,    // lead: every elementwise warp has read S (8 x 2)
   B_QE = 16,       // both: the unit's last S MMA done (Q, dO free)
   B_DQFREE = 17,   // lead: every elementwise warp has read the unit's dQ (8 x 2)
-  kNumBars = 18
+  B_EF1 = 18,      // lead: dS of an odd key tile written (8 x 2); see ef_bar
+  kNumBars = 19
 };
 constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
 constexpr int kOffAbort = kOffTmemSlot + 8;
@@ -89,12 +94,22 @@ static_assert(kSmemBytes <= 227 * 1024, "dQ pair kernel shared memory");
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColQ = 128;
 __device__ __forceinline__ uint32_t col_p(int t) { return 256 + static_cast<uint32_t>(t & 1) * 128; }
+// The "dS written" barrier of key tile g, and the phase to wait for.  Tiles
+// alternate between two barriers: S(g + 1) needs only every warp's read of
+// S(g), so a fast warp may finish tile g + 1 before a slow one has written
+// dS(g); with one barrier its arrival could complete tile g's phase and let
+// the dQ MMA read dP bits as dS.  Tile g + 2 needs every warp's read of
+// S(g + 1), which follows its tile-g arrival, so each barrier's phase counts
+// arrivals of one tile only.
+__device__ __forceinline__ int ef_bar(uint32_t g) { return (g & 1) ? B_EF1 : B_EF; }
+__device__ __forceinline__ uint32_t ef_phase(uint32_t g) { return (g >> 1) & 1; }
 
 struct DqPairParams {
   CUtensorMap tm_q, tm_do;          // [n, Hq, d], 128-row boxes
   CUtensorMap tm_k64, tm_v64;       // [n, Hkv, d], 64-row boxes (key-row halves)
   CUtensorMap tm_k128;              // K, 128-row boxes (one 64-column half)
   CUtensorMap tm_klm64, tm_vlm64, tm_klm128;  // landmarks, same boxes
+  CUtensorMap tm_dq;                // dQ when bf16, 32-row boxes (stores)
   const float* L2;                  // [Hq, n_pad] -lse log2e
   const float* D;                   // [Hq, n_pad] -<dO, O>
   void* dq;                         // [n, Hq, d]
@@ -171,7 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i)
-      ptx::mbar_init(bar(i), (i == B_EF || i == B_SFREE || i == B_DQFREE) ? 2 * kEwWarps : 1);
+      ptx::mbar_init(bar(i), (i == B_EF || i == B_EF1 || i == B_SFREE || i == B_DQFREE)
+                                 ? 2 * kEwWarps
+                                 : 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::fence_async_shared();
@@ -297,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = tile_scores(gt + 1))) break;
             if (t + 2 == T) pair::commit_both(bar(B_QE));  // the unit's last S MMA
           }
-          if (!(ok = wait_pair_w(bar(B_EF), gt & 1, ctl))) break;
+          if (!(ok = wait_pair_w(bar(ef_bar(gt)), ef_phase(gt), ctl))) break;
           // The first dQ MMA of a unit overwrites the accumulator that the
           // previous unit's epilogue reads.
           if (t == 0 && ul >= 1 && !(ok = wait_pair_w(bar(B_DQFREE), (ul - 1) & 1, ctl))) break;
@@ -319,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cp = warp >> 2;      // key columns [64 cp, 64 cp + 64) of each tile
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint64_t c2 = ptx::f2(p.scale_log2, p.scale_log2);
-    const uint32_t ef = lead(B_EF), sfree = lead(B_SFREE), dqfree = lead(B_DQFREE);
+    const uint32_t sfree = lead(B_SFREE), dqfree = lead(B_DQFREE);
     bool ok = true;
     uint32_t g = 0, ul = 0;
     for (int u = cid; ok && u < p.units; u += n_clusters, ++ul) {
@@ -392,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
-        pair::arrive_cluster_w(ef);
+        pair::arrive_cluster_w(lead(ef_bar(gt)));
       }
       if (ok) ok = wait_pair_w(bar(B_ACC), ul & 1, ctl);
       if (!ok) break;
@@ -409,12 +426,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t off = (i * p.Hq + w.h) * static_cast<int64_t>(kD);
       const bool out_ok =
           !row_ok || MSA_IN_RANGE(off, kD, p.n * p.Hq * static_cast<int64_t>(kD), p.status);
-      if (row_ok && out_ok) {
+      const int row0 = static_cast<int>(w.qr0) + quarter * 32;
+      if (p.grad_bf16 && __all_sync(0xffffffffu, out_ok)) {
+        // Staged in shared memory (the 128-byte swizzle of tm_dq's 32 x 64
+        // box) and written by one bulk tensor store; rows past n are
+        // clipped.  Each thread storing its own row would touch 32 lines
+        // per instruction and hold the warp from the next unit's first tile.
+        if (row0 < p.n) {
+          (void)MSA_TMA_OK(64 * cp, w.h, row0, kD, p.Hq, p.n, 32, p.status);
+          const uint32_t stg = sb + kOffOut + static_cast<uint32_t>(warp * kOutStageBytes);
+          const uint32_t my = stg + static_cast<uint32_t>(lane * 128);
+          if (lane == 0) ptx::bulk_wait_read();  // the buffer's last store has read it
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {  // 16-byte chunk j of row `lane`, swizzled
+            const float* c8 = &o[j >> 2][(j & 3) * 8];
+            ptx::st_shared_v4(my + static_cast<uint32_t>(((j ^ lane) & 7) << 4),
+                              ptx::pack_bf16x2(c8[0] * p.scale, c8[1] * p.scale),
+                              ptx::pack_bf16x2(c8[2] * p.scale, c8[3] * p.scale),
+                              ptx::pack_bf16x2(c8[4] * p.scale, c8[5] * p.scale),
+                              ptx::pack_bf16x2(c8[6] * p.scale, c8[7] * p.scale));
+          }
+          ptx::fence_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&p.tm_dq, stg, 64 * cp, w.h, row0);
+            ptx::bulk_commit();
+          }
+        }
+      } else if (row_ok && out_ok) {
         store_row(p.dq, off + (2 * cp) * 32, o[0], p.scale, p.grad_bf16);
         store_row(p.dq, off + (2 * cp + 1) * 32, o[1], p.scale, p.grad_bf16);
       }
       g += w.T;
     }
+    // This warp's bulk stores of dQ complete before shared memory is released.
+    if (lane == 0) ptx::bulk_wait_all();
   }
 
   ptx::tc_fence_before();
@@ -455,11 +502,13 @@ cudaError_t launch_bwd_dq_pair(const BwdArgs& a, cudaStream_t s, const char** wh
                   (a.G > 0 ? encode_map(fn, &p.tm_klm64, a.k_lm, a.G, a.Hkv, 64) &&
                                  encode_map(fn, &p.tm_klm128, a.k_lm, a.G, a.Hkv, 128) &&
                                  encode_map(fn, &p.tm_vlm64, a.v_lm, a.G, a.Hkv, 64)
-                           : true);
+                           : true) &&
+                  (a.grad_bf16 ? encode_map(fn, &p.tm_dq, a.dq, a.n, a.Hq, 32) : true);
   if (!ok) {
     *why = "cuTensorMapEncodeTiled rejected a tensor of the dQ pair kernel";
     return cudaErrorInvalidValue;
   }
+  if (!a.grad_bf16) p.tm_dq = p.tm_q;  // not used: fp32 dQ is stored by the threads
   if (a.G == 0) {  // no landmark tensors read
     p.tm_klm64 = p.tm_k64;
     p.tm_klm128 = p.tm_k128;

@@ -306,21 +306,24 @@ def test_compress_128k_backward_properties_and_sampled_dq():
     rel_compare(gq, ref, "compress 128K dQ (sampled + global rows)")
 
 
+@pytest.mark.parametrize("grad_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("n,Hq,Hkv,w,G", [(1000, 4, 2, 100, 8), (2048, 8, 1, 300, 16),
                                         (640, 4, 4, 640, 0), (4096, 16, 2, 1024, 32),
                                         (129, 2, 1, 7, 3)])
-def test_dq_pair_kernel_equals_single_cta(n, Hq, Hkv, w, G):
+def test_dq_pair_kernel_equals_single_cta(n, Hq, Hkv, w, G, grad_dtype):
     """The CTA-pair dQ kernel (two heads of a KV group share every MMA) gives
-    the bits of the single-CTA dQ kernel; dK / dV are unaffected."""
+    the bits of the single-CTA dQ kernel, fp32 gradients stored by the
+    threads and bf16 ones by bulk tensor stores (n = 129: a last tile of one
+    row); dK / dV are unaffected."""
     B = binding()
     wl = Workload("dqpair", n, Hq, Hkv, 128, w, G, "bf16", seed=n + Hq + G)
     q, k, v = generate(wl, device=DEV)
     do = make_dout(wl, seed=n + 5)
     try:
         B.force_single_cta(True)
-        single = gpu_backward(q, k, v, do, wl)
+        single = gpu_backward(q, k, v, do, wl, grad_dtype=grad_dtype)
     finally:
         B.force_single_cta(False)
-    pair = gpu_backward(q, k, v, do, wl)
+    pair = gpu_backward(q, k, v, do, wl, grad_dtype=grad_dtype)
     for a, b, name in zip(pair, single, ("dQ", "dK", "dV")):
         assert torch.equal(a, b), f"{name} differs between the pair and single-CTA kernels"
