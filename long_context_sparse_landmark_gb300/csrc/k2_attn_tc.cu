@@ -69,12 +69,17 @@ constexpr float kTau = 8.0f;
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kSlots * kTileBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffBar = kOffV + kStages * kTileBytes;
+// bf16 O leaves through shared memory: per softmax warp its 32 rows x 64
+// columns (one 128-byte swizzle span), stored by one bulk tensor copy.
+constexpr int kOutStageBytes = 32 * 128;
+constexpr int kOffOut = kOffV + kStages * kTileBytes;
+constexpr int kOffBar = kOffOut + 8 * kOutStageBytes;
 constexpr int kNumBars = 14;
 constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemUsed = kOffAbort + 8;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // alignment slack
+static_assert(kSmemBytes <= 232448, "attention kernel shared memory");
 
 // Barrier indices.  The K/V ring is organised in pairs: pair g carries V of
 // global tile g together with K of tile g+1 (which may be the first tile of
@@ -96,6 +101,7 @@ struct TcParams {
   CUtensorMap tm_v;
   CUtensorMap tm_klm;
   CUtensorMap tm_vlm;
+  CUtensorMap tm_o;  // O when bf16, 32-row boxes (stores)
   void* out;
   float* lse;
   int64_t n_q, q_start, n_kv, kv_start, window, block, lse_ld;
@@ -549,40 +555,74 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           w_new *= expf(lse_p - lse_out);
         }
       }
+      // bf16 O of a warp whose valid rows all have a key: staged in shared
+      // memory (the 128-byte swizzle of tm_o's 32 x 64 box) and written by
+      // one bulk tensor store per 64 columns; rows past n_q are clipped.
+      const int row0 = static_cast<int>(w.qr0) + wq * 32;
+      if (p.out_bf16 && !p.merge && __all_sync(0xffffffffu, (has || !row_ok) && io_ok)) {
+        if (row0 < p.n_q) {
+          (void)MSA_TMA_OK(0, h, row0, kD, p.Hq, p.n_q, 32, p.status);
+          const uint32_t stg = sb + kOffOut + static_cast<uint32_t>((warp - 4) * kOutStageBytes);
+          const uint32_t my = stg + static_cast<uint32_t>(lane * 128);
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        float o[32];
-        ptx::tmem_ld32(tO + cc * 32, o);
-        ptx::tmem_wait_ld();
-        if (has && io_ok) {
-          if (p.out_bf16) {
-            uint4* dst =
-                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + obase + cc * 32);
+          for (int hh = 0; hh < 2; ++hh) {
+            float o[64];
+            ptx::tmem_ld32(tO + hh * 64, *reinterpret_cast<float(*)[32]>(&o[0]));
+            ptx::tmem_ld32(tO + hh * 64 + 32, *reinterpret_cast<float(*)[32]>(&o[32]));
+            ptx::tmem_wait_ld();
+            if (lane == 0) ptx::bulk_wait_read();  // the buffer's last store has read it
+            __syncwarp();
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 q4;
-              q4.x = ptx::pack_bf16x2(o[8 * v + 0] * w_new, o[8 * v + 1] * w_new);
-              q4.y = ptx::pack_bf16x2(o[8 * v + 2] * w_new, o[8 * v + 3] * w_new);
-              q4.z = ptx::pack_bf16x2(o[8 * v + 4] * w_new, o[8 * v + 5] * w_new);
-              q4.w = ptx::pack_bf16x2(o[8 * v + 6] * w_new, o[8 * v + 7] * w_new);
-              dst[v] = q4;
+            for (int j = 0; j < 8; ++j)  // 16-byte chunk j of row `lane`, swizzled
+              ptx::st_shared_v4(my + static_cast<uint32_t>(((j ^ lane) & 7) << 4),
+                                ptx::pack_bf16x2(o[8 * j + 0] * w_new, o[8 * j + 1] * w_new),
+                                ptx::pack_bf16x2(o[8 * j + 2] * w_new, o[8 * j + 3] * w_new),
+                                ptx::pack_bf16x2(o[8 * j + 4] * w_new, o[8 * j + 5] * w_new),
+                                ptx::pack_bf16x2(o[8 * j + 6] * w_new, o[8 * j + 7] * w_new));
+            ptx::fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_3d(&p.tm_o, stg, hh * 64, h, row0);
+              ptx::bulk_commit();
             }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + cc * 32);
-            if (w_run != 0.f) {
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          ptx::tmem_ld32(tO + cc * 32, o);
+          ptx::tmem_wait_ld();
+          if (has && io_ok) {
+            if (p.out_bf16) {
+              uint4* dst =
+                  reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + obase + cc * 32);
 #pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                const float4 r = dst[v];
-                dst[v] = make_float4(fmaf(r.x, w_run, o[4 * v] * w_new),
-                                     fmaf(r.y, w_run, o[4 * v + 1] * w_new),
-                                     fmaf(r.z, w_run, o[4 * v + 2] * w_new),
-                                     fmaf(r.w, w_run, o[4 * v + 3] * w_new));
+              for (int v = 0; v < 4; ++v) {
+                uint4 q4;
+                q4.x = ptx::pack_bf16x2(o[8 * v + 0] * w_new, o[8 * v + 1] * w_new);
+                q4.y = ptx::pack_bf16x2(o[8 * v + 2] * w_new, o[8 * v + 3] * w_new);
+                q4.z = ptx::pack_bf16x2(o[8 * v + 4] * w_new, o[8 * v + 5] * w_new);
+                q4.w = ptx::pack_bf16x2(o[8 * v + 6] * w_new, o[8 * v + 7] * w_new);
+                dst[v] = q4;
               }
             } else {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + cc * 32);
+              if (w_run != 0.f) {
 #pragma unroll
-              for (int v = 0; v < 8; ++v)
-                dst[v] = make_float4(o[4 * v] * w_new, o[4 * v + 1] * w_new, o[4 * v + 2] * w_new,
-                                     o[4 * v + 3] * w_new);
+                for (int v = 0; v < 8; ++v) {
+                  const float4 r = dst[v];
+                  dst[v] = make_float4(fmaf(r.x, w_run, o[4 * v] * w_new),
+                                       fmaf(r.y, w_run, o[4 * v + 1] * w_new),
+                                       fmaf(r.z, w_run, o[4 * v + 2] * w_new),
+                                       fmaf(r.w, w_run, o[4 * v + 3] * w_new));
+                }
+              } else {
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                  dst[v] = make_float4(o[4 * v] * w_new, o[4 * v + 1] * w_new, o[4 * v + 2] * w_new,
+                                       o[4 * v + 3] * w_new);
+              }
             }
           }
         }
@@ -592,6 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       sc += w.T;
       oc += 1;
     }
+    // This warp's bulk stores of O complete before shared memory is released.
+    if (lane == 0) ptx::bulk_wait_all();
   }
 
   ptx::tc_fence_before();
@@ -623,11 +665,13 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s, const char** why) 
                   encode_map(fn, &p.tm_v, a.v, a.n_kv, a.Hkv) &&
                   (a.G > 0 && !a.sel ? encode_map(fn, &p.tm_klm, a.k_lm, a.G, a.Hkv) &&
                                            encode_map(fn, &p.tm_vlm, a.v_lm, a.G, a.Hkv)
-                                     : true);
+                                     : true) &&
+                  (a.out_bf16 ? encode_map(fn, &p.tm_o, a.out, a.n_q, a.Hq, 32) : true);
   if (!ok) {
     *why = "cuTensorMapEncodeTiled rejected a tensor (alignment or size)";
     return cudaErrorInvalidValue;
   }
+  if (!a.out_bf16) p.tm_o = p.tm_q;  // not used: fp32 O is stored by the threads
   if (a.G == 0 || a.sel) {  // no landmark tensors read
     p.tm_klm = p.tm_k;
     p.tm_vlm = p.tm_v;
