@@ -112,7 +112,7 @@ struct Tc2Params {
   CUtensorMap tm_v;    // V, 128-row boxes (64 columns: one CTA's half)
   CUtensorMap tm_klm;  // landmark keys, 64-row boxes
   CUtensorMap tm_vlm;  // landmark values, 128-row boxes
-  CUtensorMap tm_o;    // O when bf16, 32-row boxes (stores)
+  CUtensorMap tm_o;    // O (bf16 or fp32), 32-row boxes (stores)
   void* out;
   float* lse;
   int64_t n_q, q_start, n_kv, kv_start, window, block, lse_ld;
@@ -551,18 +551,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
           w_new *= expf(lse_p - lse_out);
         }
       }
-      // bf16 O of a warp whose valid rows all have a key: staged in shared
-      // memory (the 128-byte swizzle of tm_o's 32 x 64 box) and written by
-      // one bulk tensor store per 64 columns; rows past n_q are clipped.
+      // O of a warp whose valid rows all have a key (bf16, or fp32 when not
+      // merging into a running result): staged in shared memory (the
+      // 128-byte swizzle of tm_o's box: 32 rows x 64 bf16 or 32 fp32) and
+      // written by one bulk tensor store per box; rows past n_q are clipped.
       // Stores of global memory from each thread's own row would touch 32
       // lines per instruction and hold the warp in the epilogue.
       const int row0 = static_cast<int>(w.qr0) + wq * 32;
-      if (has && p.out_bf16 && !p.merge &&
-          __all_sync(0xffffffffu, (hv || !row_ok) && io_ok)) {
-        if (row0 < p.n_q) {
+      if (has && !p.merge && __all_sync(0xffffffffu, (hv || !row_ok) && io_ok)) {
+        const uint32_t stg = sb + kOffOut + static_cast<uint32_t>((warp - 4) * kOutStageBytes);
+        const uint32_t my = stg + static_cast<uint32_t>(lane * 128);
+        if (row0 < p.n_q && !p.out_bf16) {
           (void)MSA_TMA_OK(0, h, row0, kD, p.Hq, p.n_q, 32, p.status);
-          const uint32_t stg = sb + kOffOut + static_cast<uint32_t>((warp - 4) * kOutStageBytes);
-          const uint32_t my = stg + static_cast<uint32_t>(lane * 128);
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            float o[32];
+            ptx::tmem_ld32(tO + cc * 32, o);
+            ptx::tmem_wait_ld();
+            if (lane == 0) ptx::bulk_wait_read();  // the buffer's last store has read it
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)  // 16-byte chunk j of row `lane`, swizzled
+              ptx::st_shared_v4(my + static_cast<uint32_t>(((j ^ lane) & 7) << 4),
+                                __float_as_uint(o[4 * j + 0] * w_new),
+                                __float_as_uint(o[4 * j + 1] * w_new),
+                                __float_as_uint(o[4 * j + 2] * w_new),
+                                __float_as_uint(o[4 * j + 3] * w_new));
+            ptx::fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_3d(&p.tm_o, stg, cc * 32, h, row0);
+              ptx::bulk_commit();
+            }
+          }
+        } else if (row0 < p.n_q) {
+          (void)MSA_TMA_OK(0, h, row0, kD, p.Hq, p.n_q, 32, p.status);
 #pragma unroll 1
           for (int hh = 0; hh < 2; ++hh) {
             float o[64];
@@ -671,12 +694,12 @@ cudaError_t launch_attn_tc2(const AttnArgs& a, cudaStream_t s, const char** why)
                   (lm_maps ? encode_map(fn, &p.tm_klm, a.k_lm, a.G, a.Hkv, 64) &&
                                  encode_map(fn, &p.tm_vlm, a.v_lm, a.G, a.Hkv, 128)
                            : true) &&
-                  (a.out_bf16 ? encode_map(fn, &p.tm_o, a.out, a.n_q, a.Hq, 32) : true);
+                  (a.out_bf16 ? encode_map(fn, &p.tm_o, a.out, a.n_q, a.Hq, 32)
+                              : encode_map_f32(fn, &p.tm_o, a.out, a.n_q, a.Hq, 32));
   if (!ok) {
     *why = "cuTensorMapEncodeTiled rejected a tensor (alignment or size)";
     return cudaErrorInvalidValue;
   }
-  if (!a.out_bf16) p.tm_o = p.tm_q;  // not used: fp32 O is stored by the threads
   if (!lm_maps) {  // no landmark tensors read
     p.tm_klm = p.tm_k;
     p.tm_vlm = p.tm_v;
