@@ -87,7 +87,7 @@ constexpr int kOffKV = kOffQ + kSlots * kQBytes;          // stage s: K half, th
 constexpr int kOutStageBytes = 32 * 128;
 constexpr int kOffOut = kOffKV + kStages * kStageBytes;
 constexpr int kOffBar = kOffOut + 8 * kOutStageBytes;
-constexpr int kNumBars = 17;
+constexpr int kNumBars = 25;
 constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemUsed = kOffAbort + 8;
@@ -105,6 +105,8 @@ __host__ __device__ constexpr int BAR_SF(int s) { return 10 + s; }     // both: 
 __host__ __device__ constexpr int BAR_PF(int s) { return 12 + s; }     // lead: P of slot s written (8 warps)
 __host__ __device__ constexpr int BAR_OD(int s) { return 14 + s; }     // both: O of slot s final
 constexpr int BAR_CLEAN = 16;                                          // both: all MMAs done
+// local: the running O box that softmax warp w (4..11) loads when merging landed
+__host__ __device__ constexpr int BAR_OL(int w) { return 17 + (w - 4); }
 
 struct Tc2Params {
   CUtensorMap tm_q;    // Q, 128-row boxes
@@ -209,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
       ptx::mbar_init(bar(BAR_OD(s)), 1);
     }
     ptx::mbar_init(bar(BAR_CLEAN), 1);
+    for (int w = 4; w < 12; ++w) ptx::mbar_init(bar(BAR_OL(w)), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::fence_async_shared();
@@ -401,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
     const float sl2 = p.scale_log2;
     const uint32_t pf = lead(BAR_PF(slot));
     uint32_t sc = 0, oc = 0;  // tiles / units this slot has processed
+    uint32_t ol_issued = 0, ol_done = 0;  // running-O box loads (merge mode)
     bool ok = true;
     for (int u = cid; ok && u < p.units; u += n_clusters) {
       const Unit w = decode_unit(p, u);
@@ -558,7 +562,53 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
       // Stores of global memory from each thread's own row would touch 32
       // lines per instruction and hold the warp in the epilogue.
       const int row0 = static_cast<int>(w.qr0) + wq * 32;
-      if (has && !p.merge && __all_sync(0xffffffffu, (hv || !row_ok) && io_ok)) {
+      if (has && p.merge && !p.out_bf16 && __all_sync(0xffffffffu, io_ok)) {
+        // Running merge: each 32 x 32 fp32 box of the running O is loaded
+        // into the buffer (TMA, this warp's barrier), combined there with
+        // this chunk's O row by row, and stored back; rows without a key in
+        // this chunk write back what they loaded.
+        if (row0 < p.n_q) {
+          (void)MSA_TMA_OK(0, h, row0, kD, p.Hq, p.n_q, 32, p.status);
+          const uint32_t stg = sb + kOffOut + static_cast<uint32_t>((warp - 4) * kOutStageBytes);
+          const uint32_t my = stg + static_cast<uint32_t>(lane * 128);
+          const uint32_t lbar = bar(BAR_OL(warp));
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            if (lane == 0) {
+              ptx::bulk_wait_read();  // the buffer's last store has read it
+              ptx::mbar_arrive_expect_tx(lbar, kOutStageBytes);
+              ptx::tma_load_3d(stg, &p.tm_o, lbar, cc * 32, h, row0);
+            }
+            ++ol_issued;
+            float o[32];
+            ptx::tmem_ld32(tO + cc * 32, o);
+            ptx::tmem_wait_ld();
+            if (!(ok = wait_pair_w(lbar, ol_done & 1, ctl))) break;
+            ++ol_done;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {  // 16-byte chunk j of row `lane`, swizzled
+              const uint32_t a = my + static_cast<uint32_t>(((j ^ lane) & 7) << 4);
+              uint32_t r[4];
+              ptx::ld_shared_v4(a, r[0], r[1], r[2], r[3]);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float rv = __uint_as_float(r[e]);
+                const float nv = w_run != 0.f ? fmaf(rv, w_run, o[4 * j + e] * w_new)
+                                              : o[4 * j + e] * w_new;
+                r[e] = hv ? __float_as_uint(nv) : r[e];
+              }
+              ptx::st_shared_v4(a, r[0], r[1], r[2], r[3]);
+            }
+            ptx::fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_3d(&p.tm_o, stg, cc * 32, h, row0);
+              ptx::bulk_commit();
+            }
+          }
+          if (!ok) break;
+        }
+      } else if (has && !p.merge && __all_sync(0xffffffffu, (hv || !row_ok) && io_ok)) {
         const uint32_t stg = sb + kOffOut + static_cast<uint32_t>((warp - 4) * kOutStageBytes);
         const uint32_t my = stg + static_cast<uint32_t>(lane * 128);
         if (row0 < p.n_q && !p.out_bf16) {
@@ -654,8 +704,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
       sc += w.T;
       oc += 1;
     }
-    // This warp's bulk stores of O complete before shared memory is released.
-    if (lane == 0) ptx::bulk_wait_all();
+    // This warp's bulk stores of O complete before shared memory is released,
+    // and a running-O load left waiting by an abort lands first.
+    if (lane == 0) {
+      if (ol_issued != ol_done)
+        drain_for(bar(BAR_OL(warp)), ol_done & 1, p.status, kDrainLimitNs);
+      ptx::bulk_wait_all();
+    }
   }
 
   ptx::tc_fence_before();
