@@ -458,11 +458,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           hi = my_hi - kb + 1;
         }
         if (!row_ok) hi = lo;
-        if (lo > 0 || hi < kBN) {
-          const int lo_c = static_cast<int>(max64(0, min64(kBN, lo)));
-          const int hi_c = static_cast<int>(max64(0, min64(kBN, hi)));
+        // Boundary tiles only, each side on its own (one compare with a
+        // constant and one select per score); the branches are uniform
+        // across the warp.
+        const int lo_c = static_cast<int>(max64(0, min64(kBN, lo)));
+        const int hi_c = static_cast<int>(max64(0, min64(kBN, hi)));
+        if (__builtin_expect(__any_sync(0xffffffffu, lo_c > 0), 0)) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = (c >= lo_c && c < hi_c) ? s[c] : -INFINITY;
+          for (int c = 0; c < 128; ++c) s[c] = c >= lo_c ? s[c] : -INFINITY;
+        }
+        if (__builtin_expect(__any_sync(0xffffffffu, hi_c < kBN), 0)) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = c < hi_c ? s[c] : -INFINITY;
         }
         // Row maximum: four independent chains of three-input maxima.
         float a0 = fmaxf(s[0], s[1]), a1 = fmaxf(s[2], s[3]);

@@ -405,23 +405,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
     const uint32_t pf = lead(BAR_PF(slot));
     uint32_t sc = 0, oc = 0;  // tiles / units this slot has processed
     uint32_t ol_issued = 0, ol_done = 0;  // running-O box loads (merge mode)
-    bool ok = true;
-    for (int u = cid; ok && u < p.units; u += n_clusters) {
-      const Unit w = decode_unit(p, u);
-      if (slot >= w.n_slots) continue;
+    // A unit as this thread's row sees it.  The next unit's is computed while
+    // the current unit's last PV runs (its divisions would otherwise sit
+    // between the epilogue and the next unit's first softmax).
+    struct RowUnit {
+      Unit w;
+      int h, lo0, hi0, lm0;
+      int64_t i_loc;
+      bool has, row_ok;
+    };
+    auto row_unit = [&](int u) -> RowUnit {
+      RowUnit r;
+      r.w = decode_unit(p, u);
       const int hh = 2 * slot + static_cast<int>(rank);
-      const bool has = hh < w.n_heads;  // this CTA holds a head in this slot
-      const int h = w.h0 + hh;
-      const int64_t i_loc = w.qr0 + wq * 32 + lane;
-      const bool row_ok = i_loc < p.n_q;
-      const int64_t i = p.q_start + i_loc;
-      if (w.T == 0) {  // no key for any row of this unit (partial chunks only)
-        const int64_t lse_idx = static_cast<int64_t>(h) * p.lse_ld + i_loc;
-        if (has && row_ok && !p.merge &&
-            MSA_IN_RANGE(lse_idx, 1, (p.Hq - 1) * p.lse_ld + p.n_q, p.status))
-          p.lse[lse_idx] = -INFINITY;
-        continue;
-      }
+      r.has = hh < r.w.n_heads;  // this CTA holds a head in this slot
+      r.h = r.w.h0 + hh;
+      r.i_loc = r.w.qr0 + wq * 32 + lane;
+      r.row_ok = r.i_loc < p.n_q;
+      const int64_t i = p.q_start + r.i_loc;
       int64_t my_lo, my_hi;
       if (p.band) {
         band_keys(i, p.band_block, p.band_half, p.n_kv, &my_lo, &my_hi);
@@ -429,21 +430,44 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
         my_lo = max64(i - p.window + 1, p.kv_start);
         my_hi = min64(i, kv_end - 1);
       }
-      // This row's valid columns of tile t are [lo0 - 128 t, hi0 - 128 t) for
-      // a window tile and [0, lm0 - 128 t) for a landmark tile, each clamped
-      // to [0, 128).  32-bit values keep the tile loop light: with at most
-      // 2^29 keys (the launch checks it) lo0 lies in [0, 2^30) and hi0 below
-      // it; a very negative hi0 (a row before the chunk) is clamped.
-      // Selected blocks lie wholly before every row's window: no mask.
-      const int64_t wbase = p.kv_start + static_cast<int64_t>(w.kt_lo - w.n_lm_tiles) * kBN;
-      int lo0 = static_cast<int>(my_lo - wbase);
-      int hi0 = static_cast<int>(max64(-(int64_t(1) << 30), my_hi - wbase + 1));
-      int lm0 = p.select ? (1 << 30)
-                         : static_cast<int>(visible_landmarks(i, p.window, p.block, p.G));
-      if (!row_ok) {  // no valid column
-        hi0 = lo0 = 1 << 30;
-        lm0 = 0;
+      // This row's valid columns of tile t are [lo0 - 128 t, hi0 - 128 t)
+      // for a window tile and [0, lm0 - 128 t) for a landmark tile, each
+      // clamped to [0, 128).  32-bit values keep the tile loop light: with
+      // at most 2^29 keys (the launch checks it) lo0 lies in [0, 2^30) and
+      // hi0 below it; a very negative hi0 (a row before the chunk) is
+      // clamped.  Selected blocks lie wholly before every row's window: no
+      // mask.
+      const int64_t wbase =
+          p.kv_start + static_cast<int64_t>(r.w.kt_lo - r.w.n_lm_tiles) * kBN;
+      r.lo0 = static_cast<int>(my_lo - wbase);
+      r.hi0 = static_cast<int>(max64(-(int64_t(1) << 30), my_hi - wbase + 1));
+      r.lm0 = p.select ? (1 << 30)
+                       : static_cast<int>(visible_landmarks(i, p.window, p.block, p.G));
+      if (!r.row_ok) {  // no valid column
+        r.hi0 = r.lo0 = 1 << 30;
+        r.lm0 = 0;
       }
+      return r;
+    };
+    RowUnit nx;
+    int nx_u = -1;
+    bool ok = true;
+    for (int u = cid; ok && u < p.units; u += n_clusters) {
+      const RowUnit ru = nx_u == u ? nx : row_unit(u);
+      const Unit& w = ru.w;
+      if (slot >= w.n_slots) continue;
+      const bool has = ru.has;
+      const int h = ru.h;
+      const int64_t i_loc = ru.i_loc;
+      const bool row_ok = ru.row_ok;
+      if (w.T == 0) {  // no key for any row of this unit (partial chunks only)
+        const int64_t lse_idx = static_cast<int64_t>(h) * p.lse_ld + i_loc;
+        if (has && row_ok && !p.merge &&
+            MSA_IN_RANGE(lse_idx, 1, (p.Hq - 1) * p.lse_ld + p.n_q, p.status))
+          p.lse[lse_idx] = -INFINITY;
+        continue;
+      }
+      const int lo0 = ru.lo0, hi0 = ru.hi0, lm0 = ru.lm0;
       float m_used = -INFINITY;
       float l = 0.f;
       for (int t = 0; t < w.T; ++t) {
@@ -459,12 +483,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
           // Valid columns [lo, hi) of this tile for this row.
           const int lo = t < w.n_lm_tiles ? 0 : lo0 - t * kBN;
           const int hi = (t < w.n_lm_tiles ? lm0 : hi0) - t * kBN;
-          // Boundary tiles only; the branch is uniform across the warp.
-          if (__builtin_expect(__any_sync(0xffffffffu, lo > 0 || hi < kBN), 0)) {
-            const int lo_c = min(kBN, max(0, lo));
-            const int hi_c = min(kBN, max(0, hi));
+          // Boundary tiles only, each side on its own (the diagonal and the
+          // last landmark tile cut only above, the first window tile only
+          // below): one compare with a constant and one select per score.
+          // Both branches are uniform across the warp.
+          const int lo_c = min(kBN, max(0, lo));
+          const int hi_c = min(kBN, max(0, hi));
+          if (__builtin_expect(__any_sync(0xffffffffu, lo_c > 0), 0)) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) s[c] = (c >= lo_c && c < hi_c) ? s[c] : -INFINITY;
+            for (int c = 0; c < 128; ++c) s[c] = c >= lo_c ? s[c] : -INFINITY;
+          }
+          if (__builtin_expect(__any_sync(0xffffffffu, hi_c < kBN), 0)) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) s[c] = c < hi_c ? s[c] : -INFINITY;
           }
           // Row maximum: four independent chains of three-input maxima.
           float a0 = fmaxf(s[0], s[1]), a1 = fmaxf(s[2], s[3]);
@@ -524,6 +555,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc2_kernel(const __grid_cons
         ptx::tc_fence_before();
         __syncwarp();
         pair::arrive_cluster_w(pf);
+        if (t + 1 == w.T && u + n_clusters < p.units) {
+          nx_u = u + n_clusters;
+          nx = row_unit(nx_u);
+        }
       }
       if (ok) ok = wait_pair_w(bar(BAR_OD(slot)), oc & 1, ctl);
       if (!ok) break;
