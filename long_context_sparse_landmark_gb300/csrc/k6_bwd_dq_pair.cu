@@ -367,7 +367,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const int lo_c = static_cast<int>(max64(0, min64(kT, lo)));
         const int hi_c = static_cast<int>(max64(0, min64(kT, hi)));
-        const bool full = lo_c == 0 && hi_c == kT;
         const uint32_t tp = tl + col_p(static_cast<int>(gt));
         // This warp's two 32-column chunks of S and dP, all read before S is
         // released for the next tile's S MMAs.
@@ -384,12 +383,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ci = 0; ci < 2; ++ci) {
           const int cc = 2 * cp + ci;  // 32-column chunk
-          if (!full) {  // masked columns: weight 0
+          // Masked columns get weight 0, each side on its own in branches
+          // uniform across the warp: one compare with a constant and one
+          // select per score.
+          const int lo_e = lo_c - cc * 32, hi_e = hi_c - cc * 32;
+          if (__any_sync(0xffffffffu, lo_e > 0)) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int col = cc * 32 + e;
-              s[ci][e] = (col >= lo_c && col < hi_c) ? s[ci][e] : -INFINITY;
-            }
+            for (int e = 0; e < 32; ++e) s[ci][e] = e >= lo_e ? s[ci][e] : -INFINITY;
+          }
+          if (__any_sync(0xffffffffu, hi_e < 32)) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s[ci][e] = e < hi_e ? s[ci][e] : -INFINITY;
           }
           uint32_t pk[16];
 #pragma unroll
