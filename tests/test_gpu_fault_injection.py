@@ -77,6 +77,21 @@ def _timeout_then_clean(B, launch):
     return out
 
 
+def test_fused_ring_rounds_time_out_cleanly():
+    """Fused ring rounds (a partial round, then running merges whose epilogue
+    loads, combines and stores O through shared memory) leave cleanly when
+    their waits run out; rounds run afresh afterwards give the same bits."""
+    import long_context_sparse_landmark_gb300.api as api
+    B = binding()
+    wl = Workload("fault_ring", 4096, 8, 2, 128, 4096, 0, "bf16", seed=26)
+    q, k, v = generate(wl, device="cuda")
+    ref = [t.clone() for t in api.ring_attention(q, k, v, 4, fused=True)]
+    torch.cuda.synchronize()
+    got = _timeout_then_clean(B, lambda: api.ring_attention(q, k, v, 4, fused=True))
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+
+
 def test_backward_kernels_time_out_cleanly():
     """The dK/dV (both modes) and dQ kernels leave their pipelines, drain and
     free TMEM when their waits run out; the next call is exact again."""
