@@ -39,6 +39,11 @@
  *     kernel finish early and record MSA_ERR_TIMEOUT in a per-device status
  *     word that msa_device_status() reads.
  *   - lse is always fp32, natural log.
+ *   - Outputs and workspaces must not overlap any input, unless an entry
+ *     point states otherwise (the running (O, lse) of a merge is both read
+ *     and written).  Outputs are written by asynchronous bulk copies from
+ *     shared memory as well as by the threads, in no order relative to other
+ *     CTAs' reads of the inputs.
  */
 #ifndef MSA_H_
 #define MSA_H_
