@@ -20,6 +20,13 @@ namespace {
 
 constexpr int kSelThreads = 256;
 
+// Sort buffer size of the rank pass: the least power of two >= G.
+__host__ __device__ inline int sel_sort_size(int G) {
+  int P = 1;
+  while (P < G) P <<= 1;
+  return P;
+}
+
 template <bool kBf16>
 __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectArgs a) {
   constexpr int V = kBf16 ? 8 : 4;  // elements per 16-byte load
@@ -28,6 +35,9 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectA
   float* part = qsum + a.d;             // [kSelThreads * V] partial sums
   float* score = part + kSelThreads * 8;  // [G]
   int* flag = reinterpret_cast<int*>(score + a.G);  // [G]
+  const int P = sel_sort_size(a.G);                  // power of two >= G
+  float* key = reinterpret_cast<float*>(flag + a.G);  // [P] sort keys
+  int* idx = reinterpret_cast<int*>(key + P);         // [P] their block indices
   const int t = blockIdx.x;        // query block
   const int c = blockIdx.y;        // KV group
   const int d = a.d;
@@ -49,10 +59,12 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectA
     for (int k = 0; k < V; ++k) acc[k] = 0.f;
     const uint8_t* qb = static_cast<const uint8_t*>(a.q);
     constexpr int ES = kBf16 ? 2 : 4;
-#pragma unroll 4
+    // (row, head) of pair pr = ps + slots * k, stepped without divisions.
+    int64_t i = r0 + ps / g;
+    int hh = ps % g;
+    const int di = slots / g, dh = slots % g;
+#pragma unroll 16
     for (int64_t pr = ps; pr < npairs; pr += slots) {
-      const int64_t i = r0 + pr / g;
-      const int hh = static_cast<int>(pr % g);
       const int64_t off = (i * a.Hq + c * g + hh) * static_cast<int64_t>(d) + vi * V;
       const uint4 x = MSA_IN_RANGE(off, V, a.n * a.Hq * static_cast<int64_t>(d), a.status)
                           ? __ldg(reinterpret_cast<const uint4*>(qb + off * ES))
@@ -69,6 +81,12 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectA
         acc[1] += __uint_as_float(x.y);
         acc[2] += __uint_as_float(x.z);
         acc[3] += __uint_as_float(x.w);
+      }
+      i += di;
+      hh += dh;
+      if (hh >= g) {
+        hh -= g;
+        ++i;
       }
     }
 #pragma unroll
@@ -124,16 +142,39 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectA
   __syncthreads();
 
   // Rank: block l is chosen iff fewer than top_k blocks beat it (higher
-  // score, or equal score and lower index).
-  for (int64_t l = threadIdx.x; l < n_cand; l += blockDim.x) {
-    const float sl = score[l];
-    int beaten = 0;
-    for (int64_t m = 0; m < n_cand && beaten < a.top_k; ++m) {
-      const float sm = score[m];
-      beaten += (sm > sl || (sm == sl && m < l)) ? 1 : 0;
-    }
-    flag[l] = beaten < a.top_k ? 1 : 0;
+  // score, or equal score and lower index), i.e. iff its position in the
+  // order (score descending, index ascending) is below top_k.  A bitonic
+  // sort of (score, index) over the next power of two gives the order
+  // (padding: -inf at indices past the candidates, which sort last).
+  const int nc = static_cast<int>(n_cand);
+  int pn = 1;
+  while (pn < nc) pn <<= 1;
+  for (int e = threadIdx.x; e < pn; e += blockDim.x) {
+    key[e] = e < nc ? score[e] : -INFINITY;
+    idx[e] = e;
   }
+  for (int e = threadIdx.x; e < nc; e += blockDim.x) flag[e] = 0;
+  __syncthreads();
+  for (int kk = 2; kk <= pn; kk <<= 1) {
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      for (int e = threadIdx.x; e < pn; e += blockDim.x) {
+        const int o = e ^ j;
+        if (o > e) {
+          const float ka = key[e], kb = key[o];
+          const int ia = idx[e], ib = idx[o];
+          const bool a_first = ka > kb || (ka == kb && ia < ib);
+          if (((e & kk) == 0) != a_first) {  // this run is built in the other order
+            key[e] = kb;
+            key[o] = ka;
+            idx[e] = ib;
+            idx[o] = ia;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int e = threadIdx.x; e < a.top_k && e < nc; e += blockDim.x) flag[idx[e]] = 1;
   __syncthreads();
 
   // Compact the chosen indices in ascending order (one warp, ballots).
@@ -160,8 +201,9 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const SelectA
 }  // namespace
 
 size_t block_select_smem(int d, int G) {
-  return sizeof(float) * (static_cast<size_t>(d) + kSelThreads * 8 + G) +
-         sizeof(int) * static_cast<size_t>(G);
+  const size_t P = static_cast<size_t>(sel_sort_size(G));
+  return sizeof(float) * (static_cast<size_t>(d) + kSelThreads * 8 + G + P) +
+         sizeof(int) * (static_cast<size_t>(G) + P);
 }
 
 cudaError_t launch_block_select(const SelectArgs& a, cudaStream_t s) {
