@@ -7,8 +7,14 @@
 // over the landmark tiles and the window tiles of the row, as the
 // single-CTA dQ kernel in k6_attn_bwd.cu computes it.
 //
-// A pair = one 128-row query tile of two query heads (2j, 2j+1) of one KV
-// group: CTA rank r holds head 2j + r, its own Q and dO tiles, and its own
+// Persistent: one cluster per CTA pair that fits on the device loops over
+// units, a unit being one 128-row query tile of two query heads (2j, 2j+1)
+// of one KV group.  The K/V rings and every barrier phase carry across
+// units; Q and dO are refilled once a unit's last S MMA is done, and the
+// dQ accumulator is released as soon as the elementwise warps have read it,
+// so the next unit's first MMAs overlap the epilogue.
+//
+// In a unit, CTA rank r holds head 2j + r, its own Q and dO tiles, and its own
 // TMEM (S, dQ, two dP buffers, as the single-CTA kernel).  Every MMA is a
 // pair MMA with M = 256, issued by the lead CTA: the score products S = Q K^T
 // and dP = dO V^T take B = K and V split by key rows (each CTA holds 64 of
