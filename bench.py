@@ -52,7 +52,7 @@ def load_peaks():
 # after any change the traffic is reported as null.
 ATTN_TRAFFIC = {"128k_70b_layer": {
     "bytes": 4 * (672.230144e6 + 507.900928e6),  # the 32K capture, scaled by n
-    "kernel_sha256": "148a087c75a5d378d41045174fe287d86a31f814ed81870dd25965a56dea72ac"}}
+    "kernel_sha256": "75056ccce413a4020ec620ad1ccfae09bfaa807c4fd31fe0f1901b520979d786"}}
 
 
 def kernel_sha256() -> str:

@@ -31,6 +31,9 @@
 // of both SMs.
 // Tensor memory per CTA: slot s uses [256s, 256s+128) for S (P over its
 // first 64 columns as packed bf16) and [256s+128, 256s+256) for O.
+// O leaves through shared memory: each softmax warp stages its 32 rows in
+// a 4 KB buffer and one lane issues bulk tensor stores (a running merge
+// first loads the running O box into the buffer the same way).
 //
 // Roles (12 warps per CTA):
 //   warp 0      TMA producer (both CTAs): its own heads' Q tiles, and its
