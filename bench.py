@@ -52,7 +52,7 @@ def load_peaks():
 # after any change the traffic is reported as null.
 ATTN_TRAFFIC = {"128k_70b_layer": {
     "bytes": 4 * (672.230144e6 + 507.900928e6),  # the 32K capture, scaled by n
-    "kernel_sha256": "75056ccce413a4020ec620ad1ccfae09bfaa807c4fd31fe0f1901b520979d786"}}
+    "kernel_sha256": "1e0c40a0ab7c324000a3459add74a9af9d38bd2eab99a186c9dfae4a5cbbee51"}}
 
 
 def kernel_sha256() -> str:

@@ -537,6 +537,16 @@ void msa_debug_set_wait_limit_ns(uint64_t ns);
  */
 void msa_debug_force_single_cta(int on);
 
+/*
+ * Test hook: with n > 0, launches made after the call run the persistent
+ * CTA-pair kernels (the attention forward and the dQ kernel of
+ * msa_attn_bwd) on at most n CTA pairs instead of as many as fit on the
+ * device, so that each pair works through many units in turn; 0 (or a
+ * negative n) restores the normal grid.  Results do not depend on the
+ * grid: every unit computes the same arithmetic whichever pair takes it.
+ */
+void msa_debug_set_max_clusters(int n);
+
 #ifdef __cplusplus
 }
 #endif

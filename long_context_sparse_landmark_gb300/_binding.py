@@ -33,7 +33,7 @@ EXPORTS = ("msa_version", "msa_last_error_string", "msa_landmark_pool", "msa_att
            "msa_attn_fwd_partial_merge", "msa_lse_merge",
            "msa_attn_uses_tensor_cores", "msa_attn_fwd_topk_uses_tensor_cores",
            "msa_debug_bounds_build", "msa_device_status", "msa_debug_set_wait_limit_ns",
-           "msa_debug_force_single_cta")
+           "msa_debug_force_single_cta", "msa_debug_set_max_clusters")
 
 
 class MsaError(RuntimeError):
@@ -113,6 +113,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msa_debug_set_wait_limit_ns.restype = None
     lib.msa_debug_force_single_cta.argtypes = [i32]
     lib.msa_debug_force_single_cta.restype = None
+    lib.msa_debug_set_max_clusters.argtypes = [i32]
+    lib.msa_debug_set_max_clusters.restype = None
     lib.msa_debug_bounds_build.argtypes = []
     lib.msa_debug_bounds_build.restype = i32
     return lib
@@ -183,6 +185,12 @@ def force_single_cta(on: bool) -> None:
     """Test hook: run the single-CTA tensor-core attention kernel where the
     CTA-pair kernel would run (msa_debug_force_single_cta)."""
     _lib.msa_debug_force_single_cta(1 if on else 0)
+
+
+def set_max_clusters(n: int) -> None:
+    """Test hook: run the persistent CTA-pair kernels on at most n pairs
+    (0: as many as fit) (msa_debug_set_max_clusters)."""
+    _lib.msa_debug_set_max_clusters(int(n))
 
 
 def landmark_pool(k: torch.Tensor, v: torch.Tensor, k_lm: torch.Tensor, v_lm: torch.Tensor,

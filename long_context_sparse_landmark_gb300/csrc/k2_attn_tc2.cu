@@ -879,7 +879,8 @@ cudaError_t launch_attn_tc2(const AttnArgs& a, cudaStream_t s, const char** why)
     std::lock_guard<std::mutex> lk(g_occ_mu);
     g_max_clusters[dev] = max_clusters;
   }
-  const int64_t clusters = units < max_clusters ? units : max_clusters;
+  int64_t clusters = units < max_clusters ? units : max_clusters;
+  if (a.max_clusters > 0 && clusters > a.max_clusters) clusters = a.max_clusters;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
   e = cudaLaunchKernelEx(&cfg, attn_tc2_kernel, p);
   if (e != cudaSuccess) return e;

@@ -52,6 +52,7 @@ __device__ int g_device_status;
 
 std::atomic<uint64_t> g_wait_limit_ns{0};
 std::atomic<int> g_force_single_cta{0};
+std::atomic<int> g_max_clusters_cap{0};
 constexpr uint64_t kDefaultWaitNs = 4000000000ull;
 
 // Address of the status word in the current context, looked up on every
@@ -107,6 +108,7 @@ msa_status run_attn(const msa::AttnArgs& a0, cudaStream_t stream) {
   if (st != MSA_OK) return st;
   const uint64_t lim = g_wait_limit_ns.load();
   a.wait_limit_ns = lim ? lim : kDefaultWaitNs;
+  a.max_clusters = g_max_clusters_cap.load();
   // Selected blocks map to whole 128-key tiles on the tensor-core path.
   const bool tiles_ok = !a.sel || a.block % 128 == 0;
   // The CTA-pair kernel keeps per-row column bounds in 32 bits: up to 2^29
@@ -771,6 +773,7 @@ static msa_status attn_bwd_impl(const void* q, const void* k, const void* v, con
   const uint64_t lim = g_wait_limit_ns.load();
   a.wait_limit_ns = lim ? lim : kDefaultWaitNs;
   a.no_pair = g_force_single_cta.load();
+  a.max_clusters = g_max_clusters_cap.load();
   const char* why = nullptr;
   cudaError_t e = msa::launch_attn_bwd(a, reinterpret_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess && why) return fail(MSA_ERR_CUDA, "backward: %s", why);
@@ -1165,5 +1168,7 @@ msa_status msa_device_status(int clear) {
 void msa_debug_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns); }
 
 void msa_debug_force_single_cta(int on) { g_force_single_cta.store(on ? 1 : 0); }
+
+void msa_debug_set_max_clusters(int n) { g_max_clusters_cap.store(n > 0 ? n : 0); }
 
 }  // extern "C"

@@ -177,6 +177,7 @@ struct AttnArgs {
   int top_k;
   int* status;  // device status word
   uint64_t wait_limit_ns;
+  int max_clusters;  // > 0: the CTA-pair kernel runs on at most this many pairs (test hook)
 };
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t s);
 
@@ -267,6 +268,7 @@ struct BwdArgs {
   float* extra_k;
   float* extra_v;
   int no_pair;  // 1: the single-CTA dQ kernel even where the pair kernel applies
+  int max_clusters;  // > 0: the dQ pair kernel runs on at most this many pairs (test hook)
 };
 bool attn_bwd_supported(int d, int in_bf16);
 cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t s, const char** why);

@@ -203,3 +203,88 @@ def test_pair_128k_layer_sampled_rows_and_bits():
     err = np.abs(go - ro) - 0.5 * 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ro), 1e-30))) - 7)
     assert float(np.maximum(err, 0).max()) <= 1e-2
     compare(gl, rl, 1e-2, 1e-3, "128K lse (sampled)")
+
+
+# ------------------------------------------------------------------ the persistent loop
+def on_clusters(run, cap):
+    """run() -> tuple of tensors, with the persistent pair kernels on at most
+    `cap` CTA pairs (cap 0: as many as fit)."""
+    B = binding()
+    try:
+        B.set_max_clusters(cap)
+        r = [t.clone() for t in run()]
+        torch.cuda.synchronize()
+        assert B.device_status() == 0
+    finally:
+        B.set_max_clusters(0)
+    return r
+
+
+@pytest.mark.parametrize("cap", [1, 3])
+def test_pair_kernels_on_few_clusters_equal_full_grid(cap):
+    """On one or three CTA pairs every pair works through dozens of units in
+    turn: barrier phases and tensor-memory slots carried from unit to unit,
+    units of four heads next to units of one (a group of five), a slot idle
+    on one CTA (a group of three), ring partials whose early query tiles
+    have no key, a running merge, and the dQ kernel's units.  Each unit's
+    arithmetic does not depend on which pair runs it, so every result equals
+    the full grid's bit for bit."""
+    B = binding()
+    # window + landmarks, groups of five and of three
+    for n, Hq, Hkv, w, G, odt in ((2048, 10, 2, 1024, 16, torch.bfloat16),
+                                  (4096, 6, 2, 700, 64, torch.float32)):
+        wl = Workload("pair_cap", n, Hq, Hkv, 128, w, G, "bf16", seed=5 * n + Hq)
+        q, k, v = generate(wl, device=DEV)
+
+        def run_plain():
+            return run_gpu_attention(q, k, v, wl, out_dtype=odt)
+
+        assert_same_bits(on_clusters(run_plain, cap), on_clusters(run_plain, 0),
+                         f"plain {wl} on {cap} pairs")
+
+    # ring partials (T = 0 units) and a running merge
+    wl = Workload("pair_cap_ring", 2048, 8, 2, 128, 2048, 0, "bf16", seed=47)
+    q, k, v = generate(wl, device=DEV)
+    c = 512
+
+    def run_ring():
+        outs = []
+        for p_ in (3, 1):
+            o = gfull((wl.n, wl.Hq, 128), 3.0, device=DEV)
+            l_ = gempty((wl.Hq, wl.n), device=DEV)
+            B.attn_fwd_partial(q, k[p_ * c:(p_ + 1) * c], v[p_ * c:(p_ + 1) * c], o, l_, 0, p_ * c,
+                               wl.window, wl.scale)
+            outs += [o, l_]
+        o = gzeros((wl.n, wl.Hq, 128), device=DEV)
+        l_ = gfull((wl.Hq, wl.n), float("-inf"), device=DEV)
+        for p_ in (2, 0, 3, 1):
+            B.attn_fwd_partial_merge(q, k[p_ * c:(p_ + 1) * c], v[p_ * c:(p_ + 1) * c], o, l_, 0,
+                                     p_ * c, 700, wl.scale)
+        return outs + [o, l_]
+
+    assert_same_bits(on_clusters(run_ring, cap), on_clusters(run_ring, 0),
+                     f"ring partials and merge on {cap} pairs")
+
+    # the dQ pair kernel (an even group): 16 query tiles x 2 head pairs x 2 KV heads
+    wl = Workload("pair_cap_bwd", 2048, 8, 2, 128, 600, 16, "bf16", seed=53)
+    q, k, v = generate(wl, device=DEV)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(59)
+    do = torch.randn((wl.n, wl.Hq, 128), generator=gen, device=DEV).to(torch.bfloat16)
+    k_lm = gempty((wl.G, wl.Hkv, 128), dtype=k.dtype, device=DEV)
+    v_lm = gempty_like(k_lm)
+    B.landmark_pool(k, v, k_lm, v_lm)
+    out = gempty((wl.n, wl.Hq, 128), device=DEV)
+    lse = gempty((wl.Hq, wl.n), device=DEV)
+    B.attn_fwd(q, k, v, k_lm, v_lm, out, lse, wl.window, wl.G, wl.scale)
+    ws = gempty((B.attn_bwd_workspace_size(wl.n, wl.Hq, wl.Hkv, 128, wl.G),), dtype=torch.uint8,
+                device=DEV)
+
+    def run_bwd():
+        dq = gempty((wl.n, wl.Hq, 128), device=DEV)
+        dk = gempty((wl.n, wl.Hkv, 128), device=DEV)
+        dv = gempty_like(dk)
+        B.attn_bwd(q, k, v, k_lm, v_lm, out, lse, do, dq, dk, dv, wl.window, wl.G, wl.scale, ws)
+        return dq, dk, dv
+
+    assert_same_bits(on_clusters(run_bwd, cap), on_clusters(run_bwd, 0), f"backward on {cap} pairs")
