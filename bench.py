@@ -687,7 +687,7 @@ def main():
     value = job_throughput(world, flops, ms_per_step) / 1e12
     tokens_per_s = job_throughput(world, wl.n, ms_per_step)
     attn_tflops = flops / (res["attn_ms"] * 1e-3) / 1e12
-    tensor_path = B.uses_tensor_cores(wl.Hq, wl.Hkv, wl.d, wl.torch_dtype())
+    tensor_path = B.uses_tensor_cores(wl.Hq, wl.Hkv, wl.d, wl.torch_dtype)
     pool_bytes = 2 * wl.n * wl.Hkv * wl.d * 2 + 2 * wl.G * wl.Hkv * wl.d * 2
     # Q, K, V and the landmarks read once, O (bf16) and lse written once.
     attn_bytes = (wl.n * wl.Hq * wl.d * 2 + 2 * wl.n * wl.Hkv * wl.d * 2
