@@ -81,6 +81,94 @@ def test_attention_small_grid(dt, d, n, G, w, Hq, Hkv):
     assert B.uses_tensor_cores(Hq, Hkv, d, q.dtype) == (dt == "bf16" and d == 128)
 
 
+def _random_cases(count=32, seed=20261203):
+    """Seeded random shapes for both kernel families: ragged n, groups of one
+    to eight query heads (odd ones leave a CTA of the pair idle in a slot),
+    windows from one key to past n, landmark counts drawn from the divisors
+    of n (or none); the work is capped so that the oracle finishes in
+    seconds.  At the larger sizes a CTA pair takes several units in turn."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for c in range(count):
+        dt, d = ("bf16", 128) if c % 4 else ("f32", 64)
+        n = int(rng.integers(129, 5000))
+        Hkv = int(rng.choice([1, 2, 3]))
+        group = int(rng.choice([1, 2, 3, 4, 5, 8]))
+        Hq = Hkv * group
+        w = int(rng.integers(1, n + 100))
+        w = max(1, min(w, int(4e7 // (n * Hq))))
+        divisors = [g for g in range(1, n + 1) if n % g == 0]
+        G = 0 if rng.random() < 0.2 else int(rng.choice(divisors))
+        cases.append((dt, d, n, G, w, Hq, Hkv))
+    return cases
+
+
+@pytest.mark.parametrize("dt,d,n,G,w,Hq,Hkv", _random_cases())
+def test_attention_random_shapes(dt, d, n, G, w, Hq, Hkv):
+    wl = Workload("random", n, Hq, Hkv, d, w, G, dt, seed=n + 3 * w + G)
+    q, k, v = generate(wl, device=DEV)
+    out, lse = run_gpu_attention(q, k, v, wl)
+    torch.cuda.synchronize()
+    assert binding().device_status() == 0
+    ro, rl = oracle_attention(q, k, v, wl)
+    mx, mean = tol(dt)
+    compare(out.cpu().numpy(), ro, mx, mean, f"O {wl}")
+    compare(lse.cpu().numpy(), rl, mx, mean, f"lse {wl}")
+
+
+def _random_ring_cases(count=8, seed=20261204):
+    """Seeded ring rounds: uneven KV chunks (random cut points), a random
+    order of the running merge, windows shorter or longer than a chunk."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for c in range(count):
+        dt, d = ("bf16", 128) if c % 4 else ("f32", 64)
+        n = int(rng.integers(300, 3000))
+        Hkv = int(rng.choice([1, 2]))
+        Hq = Hkv * int(rng.choice([1, 2, 4, 6]))
+        w = int(rng.integers(1, n + 1))
+        chunks = int(rng.integers(2, 7))
+        cuts = sorted(int(x) for x in rng.choice(np.arange(1, n), size=chunks - 1, replace=False))
+        order = [int(x) for x in rng.permutation(chunks)]
+        cases.append((dt, d, n, Hq, Hkv, w, tuple(cuts), tuple(order)))
+    return cases
+
+
+@pytest.mark.parametrize("dt,d,n,Hq,Hkv,w,cuts,order", _random_ring_cases())
+def test_ring_random_chunks(dt, d, n, Hq, Hkv, w, cuts, order):
+    """Each chunk's partial against the oracle restricted to that chunk
+    (rows without a key: lse -inf, O untouched), and the rounds merged into
+    a running result in a random order against the single pass."""
+    B = binding()
+    wl = Workload("ring_rand", n, Hq, Hkv, d, w, 0, dt, seed=n + w + len(cuts))
+    q, k, v = generate(wl, device=DEV)
+    bounds = [0, *cuts, n]
+    pieces = [(bounds[i], bounds[i + 1]) for i in range(len(bounds) - 1)]
+    qn, kn, vn = to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v)
+    mx, mean = tol(dt)
+    for lo, hi in pieces[:2]:
+        o = gfull((n, Hq, d), 5.0, dtype=torch.float32, device=DEV)
+        l = gempty((Hq, n), dtype=torch.float32, device=DEV)
+        B.attn_fwd_partial(q, k[lo:hi], v[lo:hi], o, l, 0, lo, w, wl.scale)
+        torch.cuda.synchronize()
+        ro, rl = oracle.attn(qn, kn[lo:hi], vn[lo:hi], w, 0, wl.scale, kv_start=lo)
+        compare(l.cpu().numpy(), rl, mx, mean, f"partial lse [{lo},{hi})")
+        has = np.isfinite(rl[0])
+        go = o.cpu().numpy()
+        compare(go[has], ro[has], mx, mean, f"partial O [{lo},{hi})")
+        assert np.all(go[~has] == 5.0), "rows without keys must be left untouched"
+    out = gfull((n, Hq, d), float("nan"), dtype=torch.float32, device=DEV)
+    lse = gfull((Hq, n), -float("inf"), dtype=torch.float32, device=DEV)
+    for i in order:
+        lo, hi = pieces[i]
+        B.attn_fwd_partial_merge(q, k[lo:hi], v[lo:hi], out, lse, 0, lo, w, wl.scale)
+    torch.cuda.synchronize()
+    assert B.device_status() == 0
+    ro, rl = oracle.attn(qn, kn, vn, w, 0, wl.scale)
+    compare(out.cpu().numpy(), ro, mx, mean, "running O")
+    compare(lse.cpu().numpy(), rl, mx, mean, "running lse")
+
+
 # ------------------------------------------------------------------ the five workloads
 def test_pr1_2k_all_rows():
     wl = WORKLOADS["pr1_2k"]
