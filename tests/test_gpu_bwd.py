@@ -115,6 +115,37 @@ def test_backward_parity(n, Hq, Hkv, w, G):
     rel_compare(dv.cpu().numpy(), rv, f"dV {wl}")
 
 
+def _random_bwd_cases(count=10, seed=20261205):
+    """Seeded random backward shapes: ragged n, groups of one to eight query
+    heads (even ones take the dQ pair kernel, odd ones the single-CTA one),
+    windows from one key to past n, landmark counts from the divisors of n
+    (or none); small enough for the fp64 backward oracle."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(count):
+        n = int(rng.integers(129, 1600))
+        Hkv = int(rng.choice([1, 2]))
+        Hq = Hkv * int(rng.choice([1, 2, 3, 4, 8]))
+        w = int(rng.integers(1, n + 50))
+        divisors = [g for g in range(1, n + 1) if n % g == 0]
+        G = 0 if rng.random() < 0.25 else int(rng.choice(divisors))
+        cases.append((n, Hq, Hkv, w, G))
+    return cases
+
+
+@pytest.mark.parametrize("n,Hq,Hkv,w,G", _random_bwd_cases())
+def test_backward_random_shapes(n, Hq, Hkv, w, G):
+    wl = Workload("bwd_rand", n, Hq, Hkv, 128, w, G, "bf16", seed=2 * n + w + G)
+    q, k, v = generate(wl, device=DEV)
+    do = make_dout(wl, seed=n + 11)
+    dq, dk, dv = gpu_backward(q, k, v, do, wl)
+    rq, rk, rv = oracle.attn_bwd(to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v),
+                                 to_numpy_bits(do), w, G, wl.scale)
+    rel_compare(dq.cpu().numpy(), rq, f"dQ {wl}")
+    rel_compare(dk.cpu().numpy(), rk, f"dK {wl}")
+    rel_compare(dv.cpu().numpy(), rv, f"dV {wl}")
+
+
 def test_backward_bf16_gradients():
     wl = Workload("bwd16", 2048, 8, 2, 128, 256, 16, "bf16", seed=77)
     q, k, v = generate(wl, device=DEV)
