@@ -294,6 +294,39 @@ def test_band_small(dt, d, n, bb, hw):
     compare(lse.cpu().numpy(), rl, mx, mean, f"band lse n={n} bb={bb} hw={hw}")
 
 
+def _random_band_cases(count=8, seed=20261206):
+    """Seeded block bands: ragged n, block sizes that do and do not divide n
+    or a 128-key tile, half-widths from zero blocks up, several groups."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for c in range(count):
+        dt, d = ("bf16", 128) if c % 4 else ("f32", 64)
+        n = int(rng.integers(100, 4000))
+        Hkv = int(rng.choice([1, 2]))
+        Hq = Hkv * int(rng.choice([1, 2, 4, 5]))
+        bb = int(rng.choice([1, 37, 64, 128, 200, 256]))
+        hw = int(rng.integers(0, 6))
+        cases.append((dt, d, n, Hq, Hkv, bb, hw))
+    return cases
+
+
+@pytest.mark.parametrize("dt,d,n,Hq,Hkv,bb,hw", _random_band_cases())
+def test_band_random_shapes(dt, d, n, Hq, Hkv, bb, hw):
+    B = binding()
+    wl = Workload("band_rand", n, Hq, Hkv, d, 1, 0, dt, seed=n + bb + 5 * hw)
+    q, k, v = generate(wl, device=DEV)
+    out = gempty((n, Hq, d), dtype=torch.float32, device=DEV)
+    lse = gempty((Hq, n), dtype=torch.float32, device=DEV)
+    B.attn_fwd_band(q, k, v, out, lse, bb, hw, wl.scale)
+    torch.cuda.synchronize()
+    assert B.device_status() == 0
+    ro, rl = oracle.attn_band(to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v), bb, hw,
+                              wl.scale)
+    mx, mean = tol(dt)
+    compare(out.cpu().numpy(), ro, mx, mean, f"band O {wl} bb={bb} hw={hw}")
+    compare(lse.cpu().numpy(), rl, mx, mean, f"band lse {wl} bb={bb} hw={hw}")
+
+
 @pytest.mark.large
 def test_band_128k_sampled_rows():
     import long_context_sparse_landmark_gb300.api as api
