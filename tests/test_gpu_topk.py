@@ -240,6 +240,55 @@ def test_topk_fused_against_oracle(dt, d, n, G, w, top_k, Hq, Hkv):
     compare(l_, rgl, mx, mean, f"fused lse, GPU selection {wl}")
 
 
+def _random_topk_cases(count=8, seed=20261207):
+    """Seeded top-k shapes: key blocks of whole 128-key tiles (tensor-core
+    path) or not (fp32 / d = 64 on the CUDA-core kernel), top_k from one to
+    every block, windows shorter and longer than a block, several groups."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for c in range(count):
+        Hkv = int(rng.choice([1, 2]))
+        Hq = Hkv * int(rng.choice([1, 2, 3, 4]))
+        if c % 4:
+            dt, d = "bf16", 128
+            block = 128 * int(rng.integers(1, 4))
+        else:
+            dt, d = "f32", 64
+            block = int(rng.integers(20, 300))
+        G = int(rng.integers(2, 24))
+        n = G * block
+        w = int(rng.integers(1, 3 * block))
+        top_k = int(rng.integers(1, G + 1))
+        cases.append((dt, d, n, G, w, top_k, Hq, Hkv))
+    return cases
+
+
+@pytest.mark.parametrize("dt,d,n,G,w,top_k,Hq,Hkv", _random_topk_cases())
+def test_topk_random_shapes(dt, d, n, G, w, top_k, Hq, Hkv):
+    """The one-call path equals the three steps bit for bit; its selection
+    is valid against the oracle's scores; its output equals the oracle's
+    attention over that selection, and over the oracle's own selection in
+    the KV groups where the two agree."""
+    wl = Workload("topk_rand", n, Hq, Hkv, d, w, G, dt, seed=n + 7 * w + top_k, top_k=top_k)
+    q, k, v = generate(wl, device=DEV)
+    sel, cnt, out, lse = _fused_vs_steps(q, k, v, wl)
+    qn, kn, vn = to_numpy_bits(q), to_numpy_bits(k), to_numpy_bits(v)
+    scores = oracle.block_scores(qn, kn, G, w)
+    same = check_selection(sel, cnt, scores, score_error_bound(q, k, G), top_k)
+    mx, mean = tol(dt)
+    o = out.cpu().numpy()
+    l_ = lse.cpu().numpy()
+    rg, rgl = oracle.attn_select(qn, kn, vn, w, G, sel, cnt, wl.scale)
+    compare(o, rg, mx, mean, f"top-k O, GPU selection {wl}")
+    compare(l_, rgl, mx, mean, f"top-k lse, GPU selection {wl}")
+    sel_o, cnt_o = oracle.select_top_k(scores, top_k)
+    ro, rl = oracle.attn_select(qn, kn, vn, w, G, sel_o, cnt_o, wl.scale)
+    keep = np.repeat(same, Hq // Hkv, axis=1)[np.arange(n) // QB]      # [n, Hq]
+    if keep.any():
+        compare(o[keep], ro[keep], mx, mean, f"top-k O, oracle selection {wl}")
+        compare(l_[keep.T], rl[keep.T], mx, mean, f"top-k lse, oracle selection {wl}")
+
+
 @pytest.mark.large
 def test_topk_128k_sampled_rows():
     """The 128K top-k workload in the benchmark's launch configuration:
